@@ -1,0 +1,466 @@
+"""Pins the CPU oracle to what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: values the
+pages print (tests/golden/*.json, each with its citation), closed forms,
+torch's float64 scaled_dot_product_attention on CPU as an independent library
+routine, or brute force on tiny inputs.
+"""
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def sdpa64(q, k, v, mask=None, scale=None):
+    """Library attention in float64: q [n,D], k [m,D], v [m,Dv], mask [n,m] bool (True = keep)."""
+    q = torch.as_tensor(q, dtype=torch.float64)[None, None]
+    k = torch.as_tensor(k, dtype=torch.float64)[None, None]
+    v = torch.as_tensor(v, dtype=torch.float64)[None, None]
+    m = None if mask is None else torch.as_tensor(mask)[None, None]
+    out = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=m, scale=scale)
+    return out[0, 0].numpy()
+
+
+# ---------------------------------------------------------------- tiling (a1)
+
+def test_tiling_pins_4x4x4():
+    g = golden("vsa_tiling_4x4x4.json")
+    T, H, W = g["grid_THW"]
+    bT, bH, bW = g["block_THW"]
+    blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
+    assert oracle.num_blocks(T, H, W, bT, bH, bW) == g["num_blocks"] == len(blocks)
+    assert list(blocks[0]) == g["A_members"]
+    packed = np.concatenate(blocks)
+    assert "".join(str(int(t)) for t in packed) == g["packed_sequence_digits"]
+    assert packed[2] == g["packed_position_2_holds_token"]
+    assert all(len(b) == g["block_capacity"] for b in blocks)
+    # A lies at t=0..3, y=0..1, x=0..1: check it with the raster formula directly.
+    for t, y, x in itertools.product(range(4), range(2), range(2)):
+        assert oracle.token_index(t, y, x, H, W) in set(blocks[0].tolist())
+
+
+@pytest.mark.parametrize("grid,block", [((5, 3, 4), (2, 2, 3)), ((30, 48, 80), (4, 4, 8)),
+                                        ((8, 16, 16), (4, 4, 4)), ((3, 5, 7), (4, 2, 2))])
+def test_tiling_is_a_partition_with_ragged_edges(grid, block):
+    T, H, W = grid
+    bT, bH, bW = block
+    blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
+    allm = np.sort(np.concatenate(blocks))
+    assert np.array_equal(allm, np.arange(T * H * W))
+    # each block's length is the product of its clipped extents (closed form)
+    nT, nH, nW = math.ceil(T / bT), math.ceil(H / bH), math.ceil(W / bW)
+    for j, b in enumerate(blocks):
+        jt, jh, jw = j // (nH * nW), (j // nW) % nH, j % nW
+        ext = (min(bT, T - jt * bT), min(bH, H - jh * bH), min(bW, W - jw * bW))
+        assert len(b) == ext[0] * ext[1] * ext[2]
+        # members ascend in raster order (t-major, then y, then x)
+        assert np.all(np.diff(b) > 0)
+
+
+def test_tiling_video_dit_grid_closed_form():
+    blocks = oracle.tile_3d(30, 48, 80, 4, 4, 8)
+    sizes = np.array([len(b) for b in blocks])
+    assert len(blocks) == 8 * 12 * 10 == 960
+    assert (sizes == 64).sum() == 120 and (sizes == 128).sum() == 840
+    assert np.all(sizes[-120:] == 64)
+
+
+def test_index_map_prefix_and_permutation():
+    blocks = oracle.tile_prefix(300, 128) + oracle.tile_permuted(np.array([3, 0, 2, 1, 5, 4]), 4, offset=300)
+    im = oracle.index_map(blocks, 128)
+    assert im.shape == (5, 128)
+    assert list(im[2, :44]) == list(range(256, 300)) and np.all(im[2, 44:] == -1)
+    assert list(im[3, :4]) == [303, 300, 302, 301] and list(im[4, :2]) == [305, 304]
+
+
+def test_budget_pins_and_exact_integer_form():
+    g = golden("vsa_topk.json")["budget_example"]
+    assert oracle.budget(g["J"], g["sparsity"]) == g["R"]
+    assert oracle.budget(960, 0.9) == 96
+    assert oracle.budget(256, 0.9) == 26
+    for J in [1, 2, 3, 7, 32, 100, 256, 960]:
+        for pct in range(0, 101):
+            # integer form: ceil((100 - pct) * J / 100), clamped to [1, J]
+            want = max(1, min(-((-(100 - pct) * J) // 100), J))
+            assert oracle.budget(J, pct / 100) == want
+
+
+# ---------------------------------------------------------------- pool + E (a2, a3)
+
+def test_pool_and_score_d2_example():
+    g = golden("vsa_pool_d2.json")
+    n = g["tokens_per_time_slice"]
+    Qa = np.repeat(np.array(g["A_query_per_time_slice"], float), n, axis=0)
+    Kb = np.repeat(np.array(g["B_key_per_time_slice"], float), n, axis=0)
+    X = np.concatenate([Qa, Kb])
+    blocks = [np.arange(16), np.arange(16, 32)]
+    qbar = oracle.pool_blocks(X, blocks)[0]
+    kbar = oracle.pool_blocks(X, blocks)[1]
+    assert np.allclose(qbar, g["qbar_A"], atol=0) and np.allclose(kbar, g["kbar_B"], atol=0)
+    E = oracle.routing_scores(qbar[None], kbar[None], g["D"])
+    assert E[0, 0] == pytest.approx(g["E_AB_numerator"] / math.sqrt(2), abs=1e-15)
+
+
+def test_pool_score_linearity_brute_force():
+    rng = np.random.default_rng(7)
+    X = rng.normal(size=(60, 5))
+    Y = rng.normal(size=(60, 5))
+    blocks = oracle.tile_3d(3, 4, 5, 2, 3, 2)
+    qbar = oracle.pool_blocks(X, blocks)
+    kbar = oracle.pool_blocks(Y, blocks)
+    E = oracle.routing_scores(qbar, kbar, 5)
+    for i, bi in enumerate(blocks):
+        for j, bj in enumerate(blocks):
+            brute = sum(float(X[a] @ Y[b]) for a in bi for b in bj) / (len(bi) * len(bj))
+            assert E[i, j] == pytest.approx(brute / math.sqrt(5), rel=1e-12, abs=1e-13)
+
+
+def test_pool_dilution_example():
+    g = golden("vsa_topk.json")["dilution_example"]
+    X = np.array(g["queries"] + g["keys"], float)
+    bar = oracle.pool_blocks(X, [np.array([0, 1]), np.array([2, 3])])
+    assert oracle.routing_scores(bar[:1], bar[1:], 1)[0, 0] == g["routing_score"]
+    assert X[0] @ X[2] == g["token_dot"]
+
+
+# ---------------------------------------------------------------- TopK (a3)
+
+def test_topk_page_example():
+    g = golden("vsa_topk.json")
+    idx, num = oracle.route(np.array([g["scores_row_A"]]), g["k"], len(g["scores_row_A"]))
+    assert list(idx[0]) == g["q2k_idx_A"] and num[0] == g["q2k_num_A"]
+    mask = np.zeros(4, int)
+    mask[idx[0][:num[0]]] = 1
+    assert list(mask) == g["block_mask_A"]
+
+
+def test_topk_brute_force_max_sum_subset():
+    rng = np.random.default_rng(3)
+    for _ in range(40):
+        J = int(rng.integers(1, 8))
+        k = int(rng.integers(1, J + 1))
+        row = rng.normal(size=J)
+        best = max(itertools.combinations(range(J), k), key=lambda c: sum(row[list(c)]))
+        assert oracle.topk_row(row, k) == sorted(best)
+
+
+def test_topk_ties_keep_lower_index():
+    row = [1.0, 2.0, 2.0, 0.5, 2.0]
+    assert oracle.topk_row(row, 2) == [1, 2]
+    assert oracle.topk_row(row, 3) == [1, 2, 4]
+    assert oracle.topk_row([0.0] * 6, 3) == [0, 1, 2]
+
+
+def test_near_tie_rows():
+    E = np.array([[3.0, 2.0, 1.0, 0.0], [3.0, 2.0, 2.0 - 1e-7, 0.0]])
+    assert list(oracle.near_tie_rows(E, 2)) == [1]
+    assert list(oracle.near_tie_rows(E, 4)) == []
+
+
+# ---------------------------------------------------------------- attention (a4)
+
+def test_pair_counts_page_table():
+    g = golden("vsa_topk.json")["pair_counts"]
+    got = oracle.pair_counts(g["M"], g["J"], g["R"])
+    assert got == {"dense": g["dense"], "pooled": g["pooled"], "sparse": g["sparse"]}
+
+
+def _random_qkv(N, D, seed):
+    rng = np.random.default_rng(seed)
+    return rng.normal(size=(N, D)), rng.normal(size=(N, D)), rng.normal(size=(N, D))
+
+
+def test_keep_all_equals_dense_library():
+    Q, K, V = _random_qkv(60, 8, 1)
+    blocks = oracle.tile_3d(5, 3, 4, 2, 2, 3)
+    J = len(blocks)
+    idx, num = oracle.route(np.zeros((J, J)), J, J)
+    O, L = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, 8 ** -0.5)
+    assert np.abs(O - sdpa64(Q, K, V)).max() < 1e-13
+    Od, Ld = oracle.dense_attention(Q, K, V, 8 ** -0.5)
+    s = Q @ K.T * 8 ** -0.5
+    assert np.abs(L - np.log(np.exp(s).sum(1))).max() < 1e-12 and np.abs(Od - O).max() < 1e-13
+
+
+@pytest.mark.parametrize("grid,block,k", [((5, 3, 4), (2, 2, 3), 3), ((4, 4, 4), (4, 2, 2), 2),
+                                          ((3, 5, 7), (2, 2, 2), 5)])
+def test_block_sparse_equals_masked_attention_original_order(grid, block, k):
+    T, H, W = grid
+    N, D = T * H * W, 6
+    Q, K, V = _random_qkv(N, D, 11)
+    blocks = oracle.tile_3d(T, H, W, *block)
+    qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+    idx, num = oracle.route(oracle.routing_scores(qbar, kbar, D), k, len(blocks))
+    O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5)
+    # explicit token mask in original order: query a may see key b iff block(b) in sel(block(a))
+    owner = np.empty(N, int)
+    for j, b in enumerate(blocks):
+        owner[b] = j
+    mask = np.zeros((N, N), bool)
+    for a in range(N):
+        sel = set(idx[owner[a]][:num[owner[a]]].tolist())
+        mask[a] = [owner[b] in sel for b in range(N)]
+    assert np.abs(O - sdpa64(Q, K, V, mask)).max() < 1e-13
+
+
+def test_kept_mass_decomposition():
+    Q, K, V = _random_qkv(32, 4, 5)
+    blocks = oracle.tile_prefix(32, 8)
+    idx, num = oracle.route(np.array([[0, 1, 2, 3]] * 4, float), 2, 4)  # keeps blocks 2, 3
+    O_kept, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, 0.5)
+    O_drop, _ = oracle.block_sparse_attention(Q, K, V, blocks, np.array([[0, 1]] * 4), num, 0.5)
+    w = np.exp(Q @ K.T * 0.5)
+    c = w[:, 16:].sum(1) / w.sum(1)
+    assert np.abs(sdpa64(Q, K, V, scale=0.5) - (c[:, None] * O_kept + (1 - c[:, None]) * O_drop)).max() < 1e-13
+
+
+def test_prefix_rows_dense_and_video_rows_keep_prefix():
+    Q, K, V = _random_qkv(40, 4, 9)
+    blocks = oracle.tile_prefix(10, 8) + oracle.tile_permuted(np.arange(30)[::-1], 8, offset=10)
+    idx = np.array([[1, -1], [0, -1], [3, -1], [2, -1]])
+    num = np.array([1, 1, 1, 1])
+    O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, 0.5, prefix_blocks=2)
+    owner = np.empty(40, int)
+    for j, b in enumerate(blocks):
+        owner[b] = j
+    mask = np.zeros((40, 40), bool)
+    for a in range(40):
+        i = owner[a]
+        if i < 2:
+            mask[a] = True
+        else:
+            keep = {0, 1, 2 + int(idx[i - 2][0])}
+            mask[a] = [owner[b] in keep for b in range(40)]
+    assert np.abs(O - sdpa64(Q, K, V, mask, scale=0.5)).max() < 1e-13
+
+
+def test_permutation_invariance_of_dense_attention():
+    Q, K, V = _random_qkv(48, 5, 21)
+    rng = np.random.default_rng(0)
+    pq, pk = rng.permutation(48), rng.permutation(48)
+    blocks_q = oracle.tile_permuted(pq, 48)  # one block holding every token: dense
+    O, _ = oracle.block_sparse_attention(Q, K, V, blocks_q, np.array([[0]]), np.array([1]), 5 ** -0.5)
+    # permute K/V jointly, Q separately, restore Q order: dense output unchanged
+    Op = sdpa64(Q[pq], K[pk], V[pk])
+    restored = np.empty_like(Op)
+    restored[pq] = Op
+    assert np.abs(restored - O).max() < 1e-13
+
+
+def test_empty_row_outputs_zero():
+    O, L = oracle.softmax_attention(np.ones((2, 3)), np.zeros((0, 3)), np.zeros((0, 4)), 1.0)
+    assert np.all(O == 0) and np.all(np.isneginf(L))
+
+
+# ---------------------------------------------------------------- NSA selected attention (a4, token mode)
+
+def _nsa_inputs(T, HQ, H, D, BS, S, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.normal(size=(T, HQ, D))
+    k = rng.normal(size=(T, H, D))
+    v = rng.normal(size=(T, H, D))
+    nb = math.ceil(T / BS)
+    idx = np.full((T, H, S), -1, np.int64)
+    cnt = np.zeros((T, H), np.int64)
+    for t in range(T):
+        own = t // BS
+        for h in range(H):
+            c = int(rng.integers(1, min(S, own + 1) + 1))
+            others = rng.permutation(own)[:c - 1] if own else np.zeros(0, int)
+            sel = np.sort(np.concatenate([others, [own]]))
+            idx[t, h, :c] = sel
+            cnt[t, h] = c
+    return q, k, v, idx, cnt, nb
+
+
+def test_nsa_equals_masked_library_attention():
+    T, HQ, H, D, BS, S = 40, 4, 2, 8, 8, 3
+    q, k, v, idx, cnt, _ = _nsa_inputs(T, HQ, H, D, BS, S, 4)
+    o, _ = oracle.nsa_selected_attention(q, k, v, idx, cnt, BS)
+    G = HQ // H
+    for hq in range(HQ):
+        h = hq // G
+        mask = np.zeros((T, T), bool)
+        for t in range(T):
+            for s in range(cnt[t, h]):
+                b = idx[t, h, s]
+                mask[t, b * BS:(b + 1) * BS] = True
+            mask[t, t + 1:] = False
+        ref = sdpa64(q[:, hq], k[:, h], v[:, h], mask)
+        assert np.abs(o[:, hq] - ref).max() < 1e-13
+
+
+def test_nsa_all_blocks_equals_dense_causal():
+    T, HQ, H, D, BS = 32, 4, 1, 8, 8
+    rng = np.random.default_rng(8)
+    q, k, v = rng.normal(size=(T, HQ, D)), rng.normal(size=(T, H, D)), rng.normal(size=(T, H, D))
+    S = T // BS
+    idx = np.tile(np.arange(S), (T, H, 1))
+    cnt = np.full((T, H), S)
+    o, _ = oracle.nsa_selected_attention(q, k, v, idx, cnt, BS)
+    for hq in range(HQ):
+        qt = torch.as_tensor(q[:, hq])[None, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt, torch.as_tensor(k[:, 0])[None, None], torch.as_tensor(v[:, 0])[None, None], is_causal=True)
+        assert np.abs(o[:, hq] - ref[0, 0].numpy()).max() < 1e-13
+
+
+def test_nsa_counts_win_over_padding_slots():
+    # a count below S must ignore whatever the later slots hold
+    T, HQ, H, D, BS, S = 24, 2, 1, 4, 8, 3
+    q, k, v, idx, cnt, _ = _nsa_inputs(T, HQ, H, D, BS, S, 12)
+    idx2 = idx.copy()
+    for t in range(T):
+        idx2[t, 0, cnt[t, 0]:] = 0
+    a, _ = oracle.nsa_selected_attention(q, k, v, idx, cnt, BS)
+    b, _ = oracle.nsa_selected_attention(q, k, v, idx2, cnt, BS)
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- KV-outer (a5, a6, a7)
+
+def test_reverse_index_page_example():
+    g = golden("msa_reverse_index.json")
+    names = g["blocks"]
+    qs = sorted(g["q2k"])
+    q2k = np.full((1, len(qs), 2), -1)
+    num = np.zeros((1, len(qs)), int)
+    for i, qn in enumerate(qs):
+        sel = sorted(names.index(b) for b in g["q2k"][qn])
+        q2k[0, i, :len(sel)] = sel
+        num[0, i] = len(sel)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, len(names))
+    for b, bn in enumerate(names):
+        got = ["q%d" % i for i in q_idx[row_ptr[b]:row_ptr[b + 1]]]
+        assert got == g["k2q"][bn]
+    assert list(row_ptr) == [0, 4, 5, 7, 8] and list(q_idx) == [0, 1, 2, 3, 3, 0, 2, 1]
+    for b, bn in enumerate(names):
+        assert row_ptr[b + 1] - row_ptr[b] == g["repeat_loads_q_outer"].get(bn, row_ptr[b + 1] - row_ptr[b])
+
+
+def test_reverse_index_brute_force_and_chunks():
+    rng = np.random.default_rng(2)
+    R, N, S, nblk = 3, 50, 4, 9
+    q2k = np.full((R, N, S), -1)
+    num = rng.integers(0, S + 1, size=(R, N))
+    for r in range(R):
+        for i in range(N):
+            q2k[r, i, :num[r, i]] = np.sort(rng.permutation(nblk)[:num[r, i]])
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk)
+    for r in range(R):
+        for b in range(nblk):
+            row = r * nblk + b
+            want = [(i, s) for i in range(N) for s in range(num[r, i]) if q2k[r, i, s] == b]
+            got = list(zip(q_idx[row_ptr[row]:row_ptr[row + 1]], slot[row_ptr[row]:row_ptr[row + 1]]))
+            assert got == want
+    chunks = oracle.schedule_chunks(row_ptr, 7)
+    covered = np.zeros(row_ptr[-1], int)
+    for row, s, n in chunks:
+        assert 0 < n <= 7 and row_ptr[row] <= s and s + n <= row_ptr[row + 1]
+        covered[s:s + n] += 1
+    assert np.all(covered == 1)
+
+
+def test_kvouter_combine_equals_q_outer():
+    T, HQ, H, D, BS, S = 48, 4, 2, 8, 8, 4
+    q, k, v, idx, cnt, nb = _nsa_inputs(T, HQ, H, D, BS, S, 31)
+    ref, ref_lse = oracle.nsa_selected_attention(q, k, v, idx, cnt, BS)
+    q2k = np.transpose(idx, (1, 0, 2))
+    num = np.transpose(cnt, (1, 0))
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nb)
+    obuf, lbuf = oracle.kvouter_partials(q, k, v, row_ptr, q_idx, slot, nb, BS, S, H)
+    nslots = np.repeat(cnt, HQ // H, axis=1)
+    O, L = oracle.combine_partials(obuf, lbuf, nslots)
+    assert np.abs(O - ref).max() < 1e-13 and np.abs(L - ref_lse).max() < 1e-12
+
+
+def test_combine_single_slot_is_identity_and_weights_sum_to_one():
+    rng = np.random.default_rng(4)
+    ob = rng.normal(size=(5, 3, 6))
+    lb = rng.normal(size=(5, 3))
+    O, L = oracle.combine_partials(ob, lb, np.ones(5, int))
+    assert np.array_equal(O, ob[:, 0]) and np.allclose(L, lb[:, 0], atol=0)
+    # equal partials combine to themselves whatever their masses
+    ob2 = np.repeat(ob[:, :1], 3, axis=1)
+    O2, L2 = oracle.combine_partials(ob2, lb, np.full(5, 3))
+    assert np.abs(O2 - ob[:, 0]).max() < 1e-14
+    assert np.abs(L2 - np.log(np.exp(lb).sum(1))).max() < 1e-14
+
+
+# ---------------------------------------------------------------- summary (a8)
+
+def test_summary_two_token_example():
+    g = golden("spark_summary.json")["two_token_block"]
+    K = np.array(g["keys"], float)[:, None]
+    V = np.array(g["values"], float)[:, None]
+    q = np.array([[g["q"]]], float)
+    d = g["d"]
+    o_true, l_true = oracle.softmax_attention(q, K, V, d ** -0.5)
+    assert round(math.exp(l_true[0]), 6) == g["true_mass"]
+    assert round(o_true[0, 0], 6) == g["true_weighted_value"]
+    # the block as the only unselected block of a one-block routed sequence
+    blocks = [np.array([0, 1])]
+    kbar, vbar = oracle.pool_blocks(K, blocks), oracle.pool_blocks(V, blocks)
+    assert vbar[0, 0] == g["mean_value"]
+    o_sum, l_sum = oracle.summary_attention(np.array([[1.0], [1.0]]), K, V, blocks, np.zeros((1, 1), int),
+                                            np.zeros(1, int), kbar, vbar, d ** -0.5)
+    assert math.exp(l_sum[0]) == pytest.approx(g["mean_plus_log_m_mass"], abs=1e-12)
+    assert o_sum[0, 0] == pytest.approx(g["mean_value"], abs=1e-15)
+
+
+def test_summary_numpy_check_mean_tail_error():
+    g = golden("spark_summary.json")["numpy_check"]
+    rng = np.random.default_rng(20261024)
+    k = rng.normal(size=(32, 8))
+    v = rng.normal(size=(32, 5))
+    a = rng.normal(size=8)
+    blocks = oracle.tile_prefix(32, g["block"])
+    exact = sorted(g["exact_blocks"])
+    idx = np.full((len(blocks), len(exact)), -1)
+    idx[:] = exact
+    num = np.full(len(blocks), len(exact))
+    kbar, vbar = oracle.pool_blocks(k, blocks), oracle.pool_blocks(v, blocks)
+    Q = np.tile(a, (32, 1))
+    o, _ = oracle.summary_attention(Q, k, v, blocks, idx, num, kbar, vbar, 8 ** -0.5, query_blocks=[0])
+    dense = sdpa64(a[None], k, v)
+    assert round(float(np.abs(o[0] - dense[0]).max()), 6) == g["mean_tail_max_abs_error_vs_dense"]
+
+
+def test_summary_identical_keys_is_exact_and_all_selected_is_dense():
+    rng = np.random.default_rng(6)
+    N, D = 32, 4
+    Q = rng.normal(size=(N, D))
+    V = rng.normal(size=(N, D))
+    K = np.repeat(rng.normal(size=(4, D)), 8, axis=0)  # each block of 8 holds one repeated key
+    blocks = oracle.tile_prefix(N, 8)
+    kbar, vbar = oracle.pool_blocks(K, blocks), oracle.pool_blocks(V, blocks)
+    idx = np.array([[i] for i in range(4)])
+    num = np.ones(4, int)
+    O, _ = oracle.summary_attention(Q, K, V, blocks, idx, num, kbar, vbar, 0.5)
+    assert np.abs(O - sdpa64(Q, K, V, scale=0.5)).max() < 1e-13
+    K2 = rng.normal(size=(N, D))
+    kbar2 = oracle.pool_blocks(K2, blocks)
+    O2, _ = oracle.summary_attention(Q, K2, V, blocks, np.tile(np.arange(4), (4, 1)), np.full(4, 4),
+                                     kbar2, vbar, 0.5)
+    assert np.abs(O2 - sdpa64(Q, K2, V, scale=0.5)).max() < 1e-13
+
+
+def test_summary_prefix_rows_are_dense():
+    rng = np.random.default_rng(10)
+    N, D = 40, 4
+    Q, K, V = rng.normal(size=(N, D)), rng.normal(size=(N, D)), rng.normal(size=(N, D))
+    blocks = oracle.tile_prefix(8, 8) + oracle.tile_permuted(rng.permutation(32), 8, offset=8)
+    kbar = oracle.pool_blocks(K, blocks[1:])
+    vbar = oracle.pool_blocks(V, blocks[1:])
+    idx = np.array([[0], [1], [2], [3]])
+    O, _ = oracle.summary_attention(Q, K, V, blocks, idx, np.ones(4, int), kbar, vbar, 0.5,
+                                    prefix_blocks=1, query_blocks=[0])
+    assert np.abs(O[:8] - sdpa64(Q[:8], K, V, scale=0.5)).max() < 1e-13
