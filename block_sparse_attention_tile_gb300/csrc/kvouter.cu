@@ -1,0 +1,434 @@
+// a5 reverse index + schedule, a6 KV-outer partial pass (CUDA cores), a7 combine.
+//
+// "MSA 为什么采用 KV-outer Sparse Attention Forward": §5 (count per
+// (KV head, block), prefix sum into row pointers, scatter of query ids),
+// §6.1 (K1: L_s = log sum exp S_j, O_s = sum exp(S_j - L_s) V_j per slot),
+// §6.2 (K2: a = max L_s, L = a + log sum exp(L_s - a), O = sum exp(L_s - L) O_s),
+// §7 (hot rows split into chunks of bounded length, preassigned slots, no
+// atomics on outputs).
+//
+// The reverse index is deterministic: queries are processed in tiles of 256;
+// a first pass counts (tile, block) pairs, one CTA turns the counts into
+// per-tile offsets, row pointers and the chunk list, and a second pass ranks
+// every entry inside its tile with per-warp lane masks, so each CSR row lists
+// its queries in ascending order.
+#include "simt_tile.cuh"
+
+namespace bsa {
+
+constexpr int kQT = 256;       // queries per reverse-index tile
+constexpr int kMaxNblk = 2048;
+
+// Pass 1: counts[g][tile][blk] = number of queries of the tile selecting blk.
+__global__ void __launch_bounds__(kQT) rev_count_kernel(
+    const int32_t* __restrict__ q2k_idx, const int32_t* __restrict__ q2k_num, int N, int H, int S,
+    int nblk, int ntile, int32_t* __restrict__ counts, int* status) {
+    extern __shared__ int cnt[];
+    const int tile = blockIdx.x, g = blockIdx.y;
+    const int b = g / H, h = g % H;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) cnt[j] = 0;
+    __syncthreads();
+    const int i = tile * kQT + threadIdx.x;
+    if (i < N) {
+        const long long sel = ((long long)b * N + i) * H + h;
+        int n = q2k_num[sel];
+        if (n > S || n < 0) { raise_status(status, BSA_ERR_INDEX); n = max(0, min(n, S)); }
+        int prev = -1;
+        for (int s = 0; s < n; ++s) {
+            const int blk = q2k_idx[sel * S + s];
+            // lists must hold distinct ids in ascending order
+            if (blk < 0 || blk >= nblk || blk <= prev) { raise_status(status, BSA_ERR_INDEX); continue; }
+            prev = blk;
+            atomicAdd(&cnt[blk], 1);
+        }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x)
+        counts[((long long)g * ntile + tile) * nblk + j] = cnt[j];
+}
+
+// Pass 2 (one CTA): per-tile offsets inside every row, row pointers, chunks.
+__global__ void __launch_bounds__(1024) rev_scan_kernel(
+    int32_t* __restrict__ counts, int R, int nblk, int ntile, int cap, int32_t* __restrict__ row_ptr,
+    int32_t* __restrict__ chunks, int32_t* __restrict__ n_chunks, int max_chunks, int* status) {
+    __shared__ int carry_rows, carry_chunks;
+    const int rows = R * nblk;
+    if (threadIdx.x == 0) { carry_rows = 0; carry_chunks = 0; }
+    __syncthreads();
+    for (int base = 0; base < rows; base += blockDim.x) {
+        const int row = base + threadIdx.x;
+        int total = 0;
+        if (row < rows) {
+            const int g = row / nblk, blk = row % nblk;
+            for (int t = 0; t < ntile; ++t) {
+                int32_t* c = counts + ((long long)g * ntile + t) * nblk + blk;
+                const int v = *c;
+                *c = total;  // exclusive offset of this tile inside the row
+                total += v;
+            }
+        }
+        const int nch = (total + cap - 1) / cap;
+        // block-wide exclusive scans of total and nch
+        int incl_t = total, incl_c = nch;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, incl_t, o);
+            const int c = __shfl_up_sync(0xffffffffu, incl_c, o);
+            if (lane >= o) { incl_t += a; incl_c += c; }
+        }
+        __shared__ int wt[32], wc[32];
+        if (lane == 31) { wt[warp] = incl_t; wc[warp] = incl_c; }
+        __syncthreads();
+        if (warp == 0) {
+            int x = lane < (int)(blockDim.x >> 5) ? wt[lane] : 0;
+            int y = lane < (int)(blockDim.x >> 5) ? wc[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int a = __shfl_up_sync(0xffffffffu, x, o);
+                const int c = __shfl_up_sync(0xffffffffu, y, o);
+                if (lane >= o) { x += a; y += c; }
+            }
+            wt[lane] = x;
+            wc[lane] = y;
+        }
+        __syncthreads();
+        const int excl_t = carry_rows + (warp ? wt[warp - 1] : 0) + incl_t - total;
+        const int excl_c = carry_chunks + (warp ? wc[warp - 1] : 0) + incl_c - nch;
+        if (row < rows) {
+            row_ptr[row] = excl_t;
+            for (int c = 0; c < nch; ++c) {
+                const int id = excl_c + c;
+                if (id >= max_chunks) { raise_status(status, BSA_ERR_INDEX); break; }
+                chunks[4 * id + 0] = row;
+                chunks[4 * id + 1] = excl_t + c * cap;
+                chunks[4 * id + 2] = min(cap, total - c * cap);
+                chunks[4 * id + 3] = 0;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {
+            carry_rows = excl_t + total;
+            carry_chunks = excl_c + nch;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        row_ptr[rows] = carry_rows;
+        *n_chunks = min(carry_chunks, max_chunks);
+    }
+}
+
+// Pass 3: scatter.  Each warp owns 32 consecutive queries of the tile; ranks
+// inside the tile come from per-warp counts (scanned across warps) plus the
+// position of the lane in the warp's lane mask for that block.
+__global__ void __launch_bounds__(kQT) rev_scatter_kernel(
+    const int32_t* __restrict__ q2k_idx, const int32_t* __restrict__ q2k_num, int N, int H, int S,
+    int nblk, int ntile, const int32_t* __restrict__ counts, const int32_t* __restrict__ row_ptr,
+    int32_t* __restrict__ q_idx, int32_t* __restrict__ slot) {
+    extern __shared__ unsigned int sm[];
+    constexpr int W = kQT / 32;
+    unsigned int* mask = sm;                                   // [W][nblk]
+    int* off = reinterpret_cast<int*>(sm + W * nblk);          // [W][nblk]
+    const int tile = blockIdx.x, g = blockIdx.y;
+    const int b = g / H, h = g % H;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int j = threadIdx.x; j < W * nblk; j += blockDim.x) { mask[j] = 0u; off[j] = 0; }
+    __syncthreads();
+    const int i = tile * kQT + threadIdx.x;
+    int n = 0;
+    long long sel = 0;
+    if (i < N) {
+        sel = ((long long)b * N + i) * H + h;
+        n = max(0, min(q2k_num[sel], S));
+        int prev = -1;
+        for (int s = 0; s < n; ++s) {
+            const int blk = q2k_idx[sel * S + s];
+            if (blk >= 0 && blk < nblk && blk > prev) {
+                atomicOr(&mask[warp * nblk + blk], 1u << lane);
+                prev = blk;
+            }
+        }
+    }
+    __syncthreads();
+    // exclusive scan over warps, per block
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < W; ++w) {
+            off[w * nblk + j] = run;
+            run += __popc(mask[w * nblk + j]);
+        }
+    }
+    __syncthreads();
+    if (i < N) {
+        const unsigned lt = (1u << lane) - 1u;
+        int prev = -1;
+        for (int s = 0; s < n; ++s) {
+            const int blk = q2k_idx[sel * S + s];
+            if (blk < 0 || blk >= nblk || blk <= prev) continue;
+            prev = blk;
+            const int row = g * nblk + blk;
+            const int pos = row_ptr[row] + counts[((long long)g * ntile + tile) * nblk + blk] +
+                            off[warp * nblk + blk] + __popc(mask[warp * nblk + blk] & lt);
+            q_idx[pos] = i;
+            slot[pos] = s;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- K1 on CUDA cores
+template <typename T, typename TO>
+__global__ void __launch_bounds__(256) kvouter_simt_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int HQ, int H,
+    int D, int Dp, const int32_t* __restrict__ q_idx, const int32_t* __restrict__ slot,
+    const int32_t* __restrict__ chunks, const int32_t* __restrict__ n_chunks, int nblk, int BS, int S,
+    int causal, float scale_log2, TO* __restrict__ obuf, float* __restrict__ lsebuf, int* status) {
+    extern __shared__ __align__(16) float ks_smem[];
+    if ((int)blockIdx.x >= *n_chunks) return;
+    const int row = chunks[4 * blockIdx.x + 0];
+    const int start = chunks[4 * blockIdx.x + 1];
+    const int len = chunks[4 * blockIdx.x + 2];
+    const int G = HQ / H;
+    const int grp = row / nblk, blk = row % nblk;
+    const int b = grp / H, h = grp % H;
+    float* Ks = ks_smem;              // [BS][Dp]
+    float* Vs = Ks + BS * Dp;         // [BS][Dp]
+    float* Qs = Vs + BS * Dp;         // [128][Dp]
+    float* bias = Qs + 128 * Dp;      // [BS]
+    float* Pw = bias + BS;            // [8][128]
+    int* kpos = reinterpret_cast<int*>(Pw + 8 * 128);  // [BS]
+    int* qpos = kpos + BS;            // [128]
+    int* orow = qpos + 128;           // [128]
+    const long long kvrow = (long long)b * N * H + h;   // row of token 0 for head h
+    for (int idx = threadIdx.x; idx < BS * Dp; idx += blockDim.x) {
+        const int u = idx / Dp, d = idx % Dp;
+        const int key = blk * BS + u;
+        float kv = 0.f, vv = 0.f;
+        if (key < N && d < D) {
+            kv = to_f32(k[(kvrow + (long long)key * H) * D + d]);
+            vv = to_f32(v[(kvrow + (long long)key * H) * D + d]);
+        }
+        Ks[idx] = kv;
+        Vs[idx] = vv;
+    }
+    for (int u = threadIdx.x; u < BS; u += blockDim.x) {
+        const int key = blk * BS + u;
+        kpos[u] = key;
+        bias[u] = key < N ? 0.f : -CUDART_INF_F;
+    }
+    const int warp = threadIdx.x >> 5;
+    const int per_batch = max(1, 128 / G);  // query positions per batch of 128 rows
+    for (int e0 = 0; e0 < len; e0 += per_batch) {
+        const int npos = min(per_batch, len - e0);
+        const int nrows = npos * G;
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < 128 * Dp; idx += blockDim.x) {
+            const int r = idx / Dp, d = idx % Dp;
+            float x = 0.f;
+            if (r < nrows && d < D) {
+                const int pos = q_idx[start + e0 + r / G];
+                const int hq = h * G + r % G;
+                x = to_f32(q[(((long long)b * N + pos) * HQ + hq) * D + d]) * scale_log2;
+            }
+            Qs[idx] = x;
+        }
+        for (int r = threadIdx.x; r < 128; r += blockDim.x) {
+            if (r < nrows) {
+                const int e = start + e0 + r / G;
+                const int pos = q_idx[e];
+                const int s = slot[e];
+                if (s < 0 || s >= S) { raise_status(status, BSA_ERR_INDEX); orow[r] = -1; continue; }
+                qpos[r] = pos;
+                orow[r] = (int)((((long long)b * N + pos) * HQ + h * G + r % G) * S + s);
+            } else {
+                qpos[r] = 0;
+                orow[r] = -1;
+            }
+        }
+        __syncthreads();
+        RowState st;
+        init_state(st);
+        const int rows_per_warp = 16;
+        const int warp_row0 = warp * rows_per_warp;
+        const int nrw = max(0, min(rows_per_warp, nrows - warp_row0));
+        fold_tile(st, Qs, Ks, Vs, bias, BS, D, Dp, warp_row0, nrw, causal ? qpos : nullptr, kpos,
+                  Pw + warp * 128);
+        write_rows(st, obuf, D, lsebuf, 1, orow, warp_row0, nrw, D);
+    }
+}
+
+// ---------------------------------------------------------------- K2
+template <typename TI, typename TO>
+__global__ void __launch_bounds__(256) combine_kernel(
+    const TI* __restrict__ obuf, const float* __restrict__ lsebuf, const int32_t* __restrict__ nslots,
+    int N, int HQ, int H, int S, int D, long long rows, TO* __restrict__ out, float* __restrict__ lse) {
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int hq = (int)(row % HQ);
+    const long long bt = row / HQ;  // b*N + t
+    const int G = HQ / H;
+    const int n = max(0, min(nslots[bt * H + hq / G], S));
+    const float* L = lsebuf + row * S;
+    float a = -CUDART_INF_F;
+    for (int s = lane; s < n; s += 32) a = fmaxf(a, L[s]);
+    a = warp_max(a);
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+    float total = 0.f;
+    if (a != -CUDART_INF_F) {
+        for (int s = lane; s < n; s += 32) total += __expf(L[s] - a);
+        total = warp_sum(total);
+        const float Lrow = a + __logf(total);
+        for (int s = 0; s < n; ++s) {
+            const float ls = L[s];
+            if (ls == -CUDART_INF_F) continue;
+            const float w = __expf(ls - Lrow);
+            const TI* o = obuf + (row * S + s) * D;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int d = lane + 32 * c;
+                if (d < D) acc[c] = fmaf(w, to_f32(o[d]), acc[c]);
+            }
+        }
+        if (lse && lane == 0) lse[row] = Lrow;
+    } else if (lse && lane == 0) {
+        lse[row] = -CUDART_INF_F;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const int d = lane + 32 * c;
+        if (d < D) out[row * D + d] = from_f32<TO>(acc[c]);
+    }
+}
+
+// tcgen05 version of K1 (attn_tc.cu); sets *handled = false when the shape is not covered.
+bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N, int HQ, int H, int D,
+                      const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot,
+                      const int32_t* chunks, const int32_t* n_chunks, int max_chunks, int nblk,
+                      int BS, int S, int causal, float scale, void* obuf, float* lsebuf,
+                      cudaStream_t st, bool* handled);
+
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" {
+
+size_t bsa_reverse_index_workspace(int B, int N, int H, int nblk) {
+    if (B < 1 || N < 1 || H < 1 || nblk < 1) return 0;
+    const size_t ntile = ((size_t)N + kQT - 1) / kQT;
+    return (size_t)B * H * ntile * nblk * sizeof(int32_t);
+}
+
+int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap) {
+    if (B < 1 || N < 1 || H < 1 || S < 1 || nblk < 1 || chunk_cap < 1) return -1;
+    const long long rows = (long long)B * H * nblk;
+    const long long nnz = (long long)B * H * N * S;
+    const long long m = rows + nnz / chunk_cap + 1;
+    return m > 0x7fffffff ? -1 : (int)m;
+}
+
+bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_num, int B, int N,
+                                   int H, int S, int nblk, int chunk_cap, int32_t* row_ptr,
+                                   int32_t* q_idx, int32_t* slot, int32_t* chunks,
+                                   int32_t* n_chunks, int max_chunks, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    BSA_REQUIRE(q2k_idx && q2k_num && row_ptr && q_idx && slot && chunks && n_chunks && workspace,
+                "reverse_index: null pointer");
+    BSA_REQUIRE(B > 0 && N > 0 && H > 0 && S > 0 && nblk > 0 && nblk <= kMaxNblk && chunk_cap > 0,
+                "reverse_index: sizes out of range");
+    BSA_REQUIRE((long long)B * H * N * S < 0x7fffffffLL, "reverse_index: too many entries");
+    BSA_REQUIRE(B * H <= 65535, "reverse_index: too many row groups");
+    const int need = bsa_max_chunks(B, N, H, S, nblk, chunk_cap);
+    BSA_REQUIRE(max_chunks >= need, "reverse_index: max_chunks %d < %d", max_chunks, need);
+    BSA_REQUIRE(workspace_bytes >= bsa_reverse_index_workspace(B, N, H, nblk),
+                "reverse_index: workspace too small");
+    cudaStream_t st = as_stream(stream);
+    const int R = B * H;
+    const int ntile = (N + kQT - 1) / kQT;
+    int32_t* counts = static_cast<int32_t*>(workspace);
+    rev_count_kernel<<<dim3(ntile, R), kQT, nblk * sizeof(int), st>>>(
+        q2k_idx, q2k_num, N, H, S, nblk, ntile, counts, status_word());
+    bsa_status rc = check_launch("rev_count_kernel");
+    if (rc != BSA_OK) return rc;
+    rev_scan_kernel<<<1, 1024, 0, st>>>(counts, R, nblk, ntile, chunk_cap, row_ptr, chunks, n_chunks,
+                                        max_chunks, status_word());
+    rc = check_launch("rev_scan_kernel");
+    if (rc != BSA_OK) return rc;
+    const size_t smem = (size_t)2 * (kQT / 32) * nblk * sizeof(int);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(rev_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    rev_scatter_kernel<<<dim3(ntile, R), kQT, smem, st>>>(q2k_idx, q2k_num, N, H, S, nblk, ntile,
+                                                          counts, row_ptr, q_idx, slot);
+    return check_launch("rev_scatter_kernel");
+}
+
+bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtype dtype, int B,
+                           int N, int HQ, int H, int D, const int32_t* row_ptr, const int32_t* q_idx,
+                           const int32_t* slot, const int32_t* chunks, const int32_t* n_chunks,
+                           int max_chunks, int nblk, int block_size, int S, int causal, float scale,
+                           void* obuf, bsa_dtype obuf_dtype, float* lsebuf, void* stream) {
+    BSA_REQUIRE(q && k && v && row_ptr && q_idx && slot && chunks && n_chunks && obuf && lsebuf,
+                "kvouter: null pointer");
+    BSA_REQUIRE(B > 0 && N > 0 && H > 0 && HQ % H == 0 && HQ / H <= 128 && D > 0 && D <= 128,
+                "kvouter: sizes out of range");
+    BSA_REQUIRE(block_size > 0 && block_size <= 128 && S > 0 && nblk > 0 && max_chunks > 0,
+                "kvouter: block sizes out of range");
+    BSA_REQUIRE((long long)B * N * HQ * S < 0x7fffffffLL, "kvouter: partial buffer too large");
+    BSA_REQUIRE(dtype == BSA_F32 || dtype == BSA_BF16, "kvouter: dtype");
+    BSA_REQUIRE(obuf_dtype == BSA_F32 || obuf_dtype == BSA_BF16, "kvouter: obuf dtype");
+    cudaStream_t st = as_stream(stream);
+    if (!force_simt() && dtype == BSA_BF16 && obuf_dtype == BSA_BF16) {
+        bool handled = false;
+        bsa_status rc = kvouter_tc(q, k, v, B, N, HQ, H, D, row_ptr, q_idx, slot, chunks, n_chunks,
+                                   max_chunks, nblk, block_size, S, causal, scale, obuf, lsebuf, st,
+                                   &handled);
+        if (handled) return rc;
+    }
+    const int Dp = (D + 3) / 4 * 4;
+    const size_t smem = sizeof(float) * ((size_t)2 * block_size * Dp + 128 * Dp + block_size + 8 * 128) +
+                        sizeof(int) * ((size_t)block_size + 256);
+    BSA_REQUIRE(smem <= 227 * 1024, "kvouter: shared memory too large");
+    const float sl = scale * kLog2e;
+#define BSA_KV_LAUNCH(T, TO)                                                                      \
+    do {                                                                                          \
+        auto kern = kvouter_simt_kernel<T, TO>;                                                   \
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
+        kern<<<max_chunks, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, N, HQ, H, D, Dp, \
+                                            q_idx, slot, chunks, n_chunks, nblk, block_size, S,   \
+                                            causal, sl, (TO*)obuf, lsebuf, status_word());        \
+    } while (0)
+    if (dtype == BSA_F32 && obuf_dtype == BSA_F32) BSA_KV_LAUNCH(float, float);
+    else if (dtype == BSA_F32) BSA_KV_LAUNCH(float, __nv_bfloat16);
+    else if (obuf_dtype == BSA_F32) BSA_KV_LAUNCH(__nv_bfloat16, float);
+    else BSA_KV_LAUNCH(__nv_bfloat16, __nv_bfloat16);
+#undef BSA_KV_LAUNCH
+    (void)row_ptr;
+    return check_launch("kvouter_simt_kernel");
+}
+
+bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lsebuf,
+                       const int32_t* nslots, int B, int N, int HQ, int H, int S, int D, void* out,
+                       bsa_dtype out_dtype, float* lse, void* stream) {
+    BSA_REQUIRE(obuf && lsebuf && nslots && out, "combine: null pointer");
+    BSA_REQUIRE(B > 0 && N > 0 && H > 0 && HQ % H == 0 && S > 0 && D > 0 && D <= 256,
+                "combine: sizes out of range");
+    const long long rows = (long long)B * N * HQ;
+    const int per_cta = 8;
+    const long long grid = (rows + per_cta - 1) / per_cta;
+    BSA_REQUIRE(grid < 0x7fffffffLL, "combine: too many rows");
+    cudaStream_t st = as_stream(stream);
+#define BSA_CB(TI, TO)                                                                         \
+    combine_kernel<TI, TO><<<(unsigned)grid, 32 * per_cta, 0, st>>>(                           \
+        (const TI*)obuf, lsebuf, nslots, N, HQ, H, S, D, rows, (TO*)out, lse)
+    if (obuf_dtype == BSA_F32 && out_dtype == BSA_F32) BSA_CB(float, float);
+    else if (obuf_dtype == BSA_F32) BSA_CB(float, __nv_bfloat16);
+    else if (out_dtype == BSA_F32) BSA_CB(__nv_bfloat16, float);
+    else BSA_CB(__nv_bfloat16, __nv_bfloat16);
+#undef BSA_CB
+    return check_launch("combine_kernel");
+}
+
+}  // extern "C"

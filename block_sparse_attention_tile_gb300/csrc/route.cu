@@ -1,0 +1,132 @@
+// a3 routing: E = Q_bar K_bar^T * scale and the per-row TopK.
+//
+// "VSA 实现详解：三维分块、均值路由与块稀疏 Attention" §2.2 (E of shape [J, J]
+// per (batch, head); each row keeps its own TopK) and §4 (ascending block ids
+// padded with -1, plus the count).  Ties keep the lower block index.
+//
+// E is a float32 FMA contraction, not a tensor-core one: a bf16/tf32 rounding
+// of the pooled means would move the selected set away from the exact
+// definition.  The TopK is an exact radix select on order-preserving 32-bit
+// keys: one warp per row finds the k-th largest key bit by bit (32 counting
+// passes), then writes the selected ids in ascending order with ballots.
+#include "common.cuh"
+
+namespace bsa {
+
+constexpr int kRouteRows = 16;   // query rows per CTA
+constexpr int kRouteCols = 64;   // key columns per staged tile
+constexpr int kRouteThreads = 256;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    f = f + 0.0f;  // -0 -> +0 so that equal values give equal keys
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
+    const float* __restrict__ qbar, const float* __restrict__ kbar, int J, int D, int Dp,
+    long long head_stride, int k, float scale, int kmax, int32_t* __restrict__ q2k_idx,
+    int32_t* __restrict__ q2k_num) {
+    extern __shared__ __align__(16) float smem[];
+    float* qs = smem;                              // [kRouteRows][Dp]
+    float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp]
+    float* E = ks + kRouteCols * Dp;               // [kRouteRows][J]
+    const int bh = blockIdx.y;
+    const int row0 = blockIdx.x * kRouteRows;
+    const int nrows = min(kRouteRows, J - row0);
+    const float* qh = qbar + (long long)bh * head_stride;
+    const float* kh = kbar + (long long)bh * head_stride;
+    const int tid = threadIdx.x;
+
+    for (int idx = tid; idx < kRouteRows * Dp; idx += blockDim.x) {
+        const int r = idx / Dp, d = idx % Dp;
+        qs[idx] = (r < nrows && d < D) ? qh[(long long)(row0 + r) * D + d] : 0.f;
+    }
+    const int r = tid / 16;        // row of this thread
+    const int cg = tid % 16;       // column group: columns cg + 16*c
+    for (int c0 = 0; c0 < J; c0 += kRouteCols) {
+        __syncthreads();
+        for (int idx = tid; idx < kRouteCols * Dp; idx += blockDim.x) {
+            const int c = idx / Dp, d = idx % Dp;
+            ks[idx] = (c0 + c < J && d < D) ? kh[(long long)(c0 + c) * D + d] : 0.f;
+        }
+        __syncthreads();
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const float4* q4 = reinterpret_cast<const float4*>(qs + r * Dp);
+        for (int d4 = 0; d4 < Dp / 4; ++d4) {
+            const float4 a = q4[d4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float4 b = reinterpret_cast<const float4*>(ks + (cg + 16 * c) * Dp)[d4];
+                acc[c] = fmaf(a.x, b.x, acc[c]);
+                acc[c] = fmaf(a.y, b.y, acc[c]);
+                acc[c] = fmaf(a.z, b.z, acc[c]);
+                acc[c] = fmaf(a.w, b.w, acc[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int col = c0 + cg + 16 * c;
+            if (col < J) E[r * J + col] = acc[c] * scale;
+        }
+    }
+    __syncthreads();
+
+    const int warp = tid / 32, lane = tid % 32;
+    for (int rr = warp; rr < nrows; rr += kRouteThreads / 32) {
+        const float* e = E + rr * J;
+        uint32_t prefix = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = prefix | (1u << bit);
+            int cnt = 0;
+            for (int c = lane; c < J; c += 32) cnt += order_key(e[c]) >= cand;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if (cnt >= k) prefix = cand;
+        }
+        // prefix is the k-th largest key; keep everything above it and the
+        // lowest-index entries equal to it.
+        int n_gt = 0;
+        for (int c = lane; c < J; c += 32) n_gt += order_key(e[c]) > prefix;
+        n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+        const int need_eq = k - n_gt;
+        int eq_seen = 0, written = 0;
+        int32_t* out = q2k_idx + ((long long)bh * J + row0 + rr) * kmax;
+        for (int base = 0; base < J; base += 32) {
+            const int c = base + lane;
+            const uint32_t key = c < J ? order_key(e[c]) : 0u;
+            const bool eq = c < J && key == prefix;
+            const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+            const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
+            const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
+            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
+            written += __popc(sel_mask);
+            eq_seen += __popc(eq_mask);
+        }
+        for (int s = k + lane; s < kmax; s += 32) out[s] = -1;
+        if (lane == 0) q2k_num[(long long)bh * J + row0 + rr] = k;
+    }
+}
+
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, int D,
+                                     int64_t head_stride, int k, float scale, int kmax,
+                                     int32_t* q2k_idx, int32_t* q2k_num, void* stream) {
+    BSA_REQUIRE(qbar && kbar && q2k_idx && q2k_num, "route: null pointer");
+    BSA_REQUIRE(BH > 0 && BH <= 65535 && J > 0 && J <= 8192 && D > 0 && D <= 256,
+                "route: sizes out of range (BH=%d J=%d D=%d)", BH, J, D);
+    BSA_REQUIRE(k >= 1 && k <= J && kmax >= k, "route: need 1 <= k <= J and k <= kmax");
+    BSA_REQUIRE(head_stride >= (int64_t)J * D, "route: head_stride smaller than J*D");
+    const int Dp = (D + 3) / 4 * 4;
+    const size_t smem = sizeof(float) * ((size_t)(kRouteRows + kRouteCols) * Dp + (size_t)kRouteRows * J);
+    if (smem > 227 * 1024) return fail(BSA_ERR_UNSUPPORTED, "route: J=%d D=%d needs too much shared memory", J, D);
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    dim3 grid((J + kRouteRows - 1) / kRouteRows, BH);
+    route_topk_kernel<<<grid, kRouteThreads, smem, as_stream(stream)>>>(
+        qbar, kbar, J, D, Dp, (long long)head_stride, k, scale, kmax, q2k_idx, q2k_num);
+    return check_launch("route_topk_kernel");
+}

@@ -1,0 +1,197 @@
+// a1 tile map and a2 mean pooling.
+//
+// Tile map: "VSA 实现详解：三维分块、均值路由与块稀疏 Attention" §1 (raster index,
+// block count, ragged edge blocks), §3 (t-major, y, x member order), §5.2
+// (dense prefix cut into contiguous blocks placed first); "深度解读|Spark-H3"
+// §04 (a permutation of the video tokens defines the blocks).
+// Pool: the same VSA page, §2.1 (mean over the block's n_i valid tokens).
+#include "common.cuh"
+
+namespace bsa {
+
+// One thread per (block, slot).  Writes the token id of the slot (valid
+// members first, in t,y,x order) or -1, and n_j from slot 0.
+__global__ void tile_map_kernel(int T, int H, int W, int bT, int bH, int bW, int n_prefix,
+                                const int32_t* __restrict__ perm, int M, int prefix_blocks,
+                                int J, int32_t* __restrict__ index_map,
+                                int32_t* __restrict__ block_sizes) {
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)J * M) return;
+    const int j = (int)(gid / M);
+    const int m = (int)(gid % M);
+    int token = -1;
+    int n = 0;
+    if (j < prefix_blocks) {
+        const int start = j * M;
+        n = min(M, n_prefix - start);
+        if (m < n) token = start + m;
+    } else {
+        const int jv = j - prefix_blocks;
+        const int n_video = T * H * W;
+        if (perm) {
+            const int start = jv * M;
+            n = min(M, n_video - start);
+            if (m < n) token = n_prefix + perm[start + m];
+        } else {
+            const int nH = (H + bH - 1) / bH, nW = (W + bW - 1) / bW;
+            const int jt = jv / (nH * nW), jh = (jv / nW) % nH, jw = jv % nW;
+            const int et = min(bT, T - jt * bT), eh = min(bH, H - jh * bH), ew = min(bW, W - jw * bW);
+            n = et * eh * ew;
+            if (m < n) {
+                const int dt = m / (eh * ew), dy = (m / ew) % eh, dx = m % ew;
+                token = n_prefix + ((jt * bT + dt) * H + (jh * bH + dy)) * W + (jw * bW + dx);
+            }
+        }
+    }
+    index_map[gid] = token;
+    if (m == 0) block_sizes[j] = n;
+}
+
+// Pool one (block, head, tensor): 256 threads = VL vector lanes x RG row groups.
+// Each thread sums its rows for VEC consecutive channels in float32; the RG
+// partial sums are added in a fixed tree order, then divided by n_j.
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) pool_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D,
+    const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M,
+    float* __restrict__ qbar, float* __restrict__ kbar, float* __restrict__ vbar,
+    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, int* status) {
+    extern __shared__ float red[];  // [RG][D]
+    const int j = blockIdx.x;
+    const int bh = blockIdx.y;
+    const int which = blockIdx.z;  // 0 = q, 1 = k, 2 = v
+    const T* src = which == 0 ? q : (which == 1 ? k : v);
+    float* dst = which == 0 ? qbar : (which == 1 ? kbar : vbar);
+    T* dst_lp = which == 1 ? kbar_lp : (which == 2 ? vbar_lp : nullptr);
+    int VL = 1;  // vector lanes, rounded up to a power of two so RG is one too
+    while (VL * VEC < D) VL <<= 1;
+    const int RG = 256 / VL;
+    const int lane = threadIdx.x % VL;
+    const int rg = threadIdx.x / VL;
+    const int n = block_sizes[j];
+    const int32_t* rows = index_map + (size_t)j * M;
+    const T* base = src + (size_t)bh * N * D;
+
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    if (rg < RG && lane * VEC < D) {
+        for (int r = rg; r < n; r += RG) {
+            const int tok = rows[r];
+            if (tok < 0 || tok >= N) { raise_status(status, BSA_ERR_INDEX); continue; }
+            const T* row = base + (size_t)tok * D + lane * VEC;
+            if (VEC > 1 && lane * VEC + VEC <= D) {
+                if constexpr (sizeof(T) * VEC == 16) {
+                    uint4 raw = *reinterpret_cast<const uint4*>(row);
+                    const T* e8 = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) acc[e] += to_f32(row[e]);
+                }
+            } else {
+                for (int e = 0; e < VEC; ++e)
+                    if (lane * VEC + e < D) acc[e] += to_f32(row[e]);
+            }
+        }
+        for (int e = 0; e < VEC; ++e)
+            if (lane * VEC + e < D) red[rg * D + lane * VEC + e] = acc[e];
+    }
+    __syncthreads();
+    // tree over row groups (RG is a power of two when VL is)
+    for (int stride = 1; stride < RG; stride <<= 1) {
+        for (int idx = threadIdx.x; idx < D * RG; idx += blockDim.x) {
+            const int g = idx / D, d = idx % D;
+            if ((g % (2 * stride)) == 0 && g + stride < RG) red[g * D + d] += red[(g + stride) * D + d];
+        }
+        __syncthreads();
+    }
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        const float mean = n > 0 ? red[d] / (float)n : 0.f;
+        dst[((size_t)bh * J + j) * D + d] = mean;
+        if (dst_lp) dst_lp[((size_t)bh * J + j) * D + d] = from_f32<T>(mean);
+    }
+}
+
+template <typename T>
+static bsa_status launch_pool(const void* q, const void* k, const void* v, int BH, int N, int D,
+                              const int32_t* im, const int32_t* bs, int J, int M, float* qbar,
+                              float* kbar, float* vbar, void* klp, void* vlp, cudaStream_t st) {
+    constexpr int VEC = 16 / sizeof(T);
+    const bool vec_ok = (D % VEC) == 0;
+    const int vec = vec_ok ? VEC : 1;
+    int vl2 = 1;  // same rounding as the kernel
+    while (vl2 * vec < D) vl2 <<= 1;
+    if (vl2 > 256) return fail(BSA_ERR_UNSUPPORTED, "pool: D=%d too large", D);
+    const int RG = 256 / vl2;
+    dim3 grid(J, BH, v ? 3 : 2);
+    const size_t smem = (size_t)RG * D * sizeof(float);
+    if (vec_ok) {
+        pool_kernel<T, VEC><<<grid, 256, smem, st>>>(
+            (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, qbar, kbar, vbar, (T*)klp,
+            (T*)vlp, status_word());
+    } else {
+        pool_kernel<T, 1><<<grid, 256, smem, st>>>(
+            (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, qbar, kbar, vbar, (T*)klp,
+            (T*)vlp, status_word());
+    }
+    return check_launch("pool_kernel");
+}
+
+}  // namespace bsa
+
+using namespace bsa;
+
+extern "C" {
+
+int bsa_tile_count(int T, int H, int W, int bT, int bH, int bW, int n_prefix, int permuted, int M) {
+    if (T < 0 || H < 0 || W < 0 || n_prefix < 0 || M < 1) return -1;
+    const long long prefix = ((long long)n_prefix + M - 1) / M;
+    long long video;
+    if (permuted) {
+        video = ((long long)T * H * W + M - 1) / M;
+    } else {
+        if (bT < 1 || bH < 1 || bW < 1 || (long long)bT * bH * bW > M) return -1;
+        video = (long long)((T + bT - 1) / bT) * ((H + bH - 1) / bH) * ((W + bW - 1) / bW);
+    }
+    const long long total = prefix + video;
+    return total > 0x7fffffff ? -1 : (int)total;
+}
+
+bsa_status bsa_tile_map(int T, int H, int W, int bT, int bH, int bW, int n_prefix,
+                        const int32_t* perm, int M, int32_t* index_map, int32_t* block_sizes,
+                        void* stream) {
+    const int J = bsa_tile_count(T, H, W, bT, bH, bW, n_prefix, perm != nullptr, M);
+    BSA_REQUIRE(J > 0, "tile_map: invalid geometry");
+    BSA_REQUIRE(index_map && block_sizes, "tile_map: null output");
+    BSA_REQUIRE((long long)T * H * W + n_prefix < 0x7fffffffLL, "tile_map: too many tokens");
+    const int prefix_blocks = (n_prefix + M - 1) / M;
+    const long long total = (long long)J * M;
+    const int threads = 256;
+    const long long grid = (total + threads - 1) / threads;
+    tile_map_kernel<<<(unsigned)grid, threads, 0, as_stream(stream)>>>(
+        T, H, W, bT, bH, bW, n_prefix, perm, M, prefix_blocks, J, index_map, block_sizes);
+    return check_launch("tile_map_kernel");
+}
+
+bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
+                           int N, int D, const int32_t* index_map, const int32_t* block_sizes,
+                           int J, int M, float* qbar, float* kbar, float* vbar, void* kbar_lp,
+                           void* vbar_lp, void* stream) {
+    BSA_REQUIRE(q && k && qbar && kbar && index_map && block_sizes, "pool: null pointer");
+    BSA_REQUIRE(!v || vbar, "pool: v given without vbar");
+    BSA_REQUIRE(!vbar_lp || v, "pool: vbar_lp needs v");
+    BSA_REQUIRE(BH > 0 && N > 0 && D > 0 && D <= 256 && J > 0 && M > 0 && M <= 1024,
+                "pool: sizes out of range");
+    BSA_REQUIRE(J <= 65535 && BH <= 65535, "pool: grid too large");
+    if (dtype == BSA_F32)
+        return launch_pool<float>(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar, kbar, vbar,
+                                  kbar_lp, vbar_lp, as_stream(stream));
+    if (dtype == BSA_BF16)
+        return launch_pool<__nv_bfloat16>(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar,
+                                          kbar, vbar, kbar_lp, vbar_lp, as_stream(stream));
+    return fail(BSA_ERR_INVALID_ARG, "pool: unknown dtype");
+}
+
+}  // extern "C"

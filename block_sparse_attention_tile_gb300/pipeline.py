@@ -1,0 +1,177 @@
+"""The hot path end to end, composed from the C-ABI entry points.
+
+Each function allocates the outputs and intermediates with torch (device
+memory is the only thing torch provides here) and calls the library's
+stages in order on the current stream.  No arithmetic of the method happens
+in Python.
+"""
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import bsa
+
+
+@dataclass
+class Geometry:
+    """Token layout of one sequence: an optional dense prefix of ``n_prefix``
+    tokens, then a (T, H, W) video grid cut into (bT, bH, bW) blocks, or, when
+    ``perm`` is given, into runs of M consecutive entries of that permutation
+    of the raster video order.  M is the block capacity."""
+    T: int
+    H: int
+    W: int
+    bT: int = 1
+    bH: int = 1
+    bW: int = 1
+    M: int = 128
+    n_prefix: int = 0
+    perm: Optional[torch.Tensor] = None  # int32 [T*H*W] on the device
+
+    @property
+    def n_tokens(self):
+        return self.n_prefix + self.T * self.H * self.W
+
+    @property
+    def prefix_blocks(self):
+        return -(-self.n_prefix // self.M)
+
+    @property
+    def num_blocks(self):
+        return bsa.bsa_tile_count(self.T, self.H, self.W, self.bT, self.bH, self.bW, self.n_prefix,
+                                  self.perm is not None, self.M)
+
+
+def tile_map(geom, device="cuda"):
+    J = geom.num_blocks
+    index_map = torch.empty((J, geom.M), dtype=torch.int32, device=device)
+    block_sizes = torch.empty((J,), dtype=torch.int32, device=device)
+    bsa.bsa_tile_map(geom.T, geom.H, geom.W, geom.bT, geom.bH, geom.bW, geom.n_prefix, geom.perm, geom.M,
+                     index_map, block_sizes)
+    return index_map, block_sizes
+
+
+@dataclass
+class BlockSparseResult:
+    out: torch.Tensor
+    lse: Optional[torch.Tensor]
+    index_map: torch.Tensor
+    block_sizes: torch.Tensor
+    qbar: torch.Tensor
+    kbar: torch.Tensor
+    q2k_idx: torch.Tensor
+    q2k_num: torch.Tensor
+
+
+def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=False, need_lse=True,
+                           tiles=None):
+    """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
+
+    q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
+    covers the video blocks; prefix blocks are always attended.  Returns the
+    output in raster order plus every intermediate."""
+    BH, N, D = q.shape
+    assert N == geom.n_tokens
+    dev = q.device
+    scale = D ** -0.5 if scale is None else scale
+    index_map, block_sizes = tile_map(geom, dev) if tiles is None else tiles
+    J = index_map.shape[0]
+    P = geom.prefix_blocks
+    Jr = J - P
+    kmax = topk if kmax is None else kmax
+    qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
+    kbar = torch.empty_like(qbar)
+    vbar = torch.empty_like(qbar) if summary else None
+    kbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
+    vbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
+    bsa.bsa_pool_blocks(q, k, v if summary else None, BH, N, D, index_map, block_sizes, J, geom.M, qbar,
+                        kbar, vbar, kbar_lp, vbar_lp)
+    q2k_idx = torch.empty((BH, Jr, kmax), dtype=torch.int32, device=dev)
+    q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
+    bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num)
+    out = torch.empty_like(q)
+    lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
+    if summary:
+        bsa.bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, q2k_idx, q2k_num,
+                            kmax, kbar_lp, vbar_lp, scale, out, lse)
+    else:
+        bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, q2k_idx, q2k_num,
+                           kmax, scale, out, lse)
+    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num)
+
+
+def nsa_qouter(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None, need_lse=True):
+    """Token-granular GQA selected attention, query-outer.  q [B,T,HQ,D],
+    k/v [B,T,H,D], block_indices [B,T,H,S] int32, block_counts [B,T,H] int32."""
+    B, T, HQ, D = q.shape
+    H = k.shape[2]
+    S = block_indices.shape[-1]
+    scale = D ** -0.5 if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty((B, T, HQ), dtype=torch.float32, device=q.device) if need_lse else None
+    bsa.bsa_fwd_qouter_tokens(q, k, v, B, T, HQ, H, D, block_indices, block_counts, S, block_size, causal,
+                              scale, out, lse)
+    return out, lse
+
+
+@dataclass
+class KVOuterPlan:
+    row_ptr: torch.Tensor
+    q_idx: torch.Tensor
+    slot: torch.Tensor
+    chunks: torch.Tensor
+    n_chunks: torch.Tensor
+    max_chunks: int
+    nblk: int
+
+
+def reverse_index(block_indices, block_counts, nblk, chunk_cap, workspace=None):
+    B, N, H, S = block_indices.shape
+    dev = block_indices.device
+    max_chunks = bsa.bsa_max_chunks(B, N, H, S, nblk, chunk_cap)
+    row_ptr = torch.empty((B * H * nblk + 1,), dtype=torch.int32, device=dev)
+    q_idx = torch.empty((B * H * N * S,), dtype=torch.int32, device=dev)
+    slot = torch.empty_like(q_idx)
+    chunks = torch.empty((max_chunks, 4), dtype=torch.int32, device=dev)
+    n_chunks = torch.empty((1,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        ws = bsa.bsa_reverse_index_workspace(B, N, H, nblk)
+        workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
+    bsa.bsa_build_reverse_index(block_indices, block_counts, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx,
+                                slot, chunks, n_chunks, max_chunks, workspace)
+    return KVOuterPlan(row_ptr, q_idx, slot, chunks, n_chunks, max_chunks, nblk)
+
+
+def kvouter_attention(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None,
+                      chunk_cap=None, obuf_dtype=torch.bfloat16, need_lse=True, plan=None):
+    """KV-outer order: reverse index -> partial pass -> combine.  Same inputs
+    and result as nsa_qouter."""
+    B, N, HQ, D = q.shape
+    H = k.shape[2]
+    S = block_indices.shape[-1]
+    scale = D ** -0.5 if scale is None else scale
+    nblk = -(-N // block_size)
+    if chunk_cap is None:
+        chunk_cap = 2 * S * block_size
+    if plan is None:
+        plan = reverse_index(block_indices, block_counts, nblk, chunk_cap)
+    obuf = torch.empty((B, N, HQ, S, D), dtype=obuf_dtype, device=q.device)
+    lsebuf = torch.empty((B, N, HQ, S), dtype=torch.float32, device=q.device)
+    bsa.bsa_fwd_kvouter(q, k, v, B, N, HQ, H, D, plan.row_ptr, plan.q_idx, plan.slot, plan.chunks,
+                        plan.n_chunks, plan.max_chunks, nblk, block_size, S, causal, scale, obuf, lsebuf)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, N, HQ), dtype=torch.float32, device=q.device) if need_lse else None
+    bsa.bsa_combine(obuf, lsebuf, block_counts, B, N, HQ, H, S, D, out, lse)
+    return out, lse, plan, obuf, lsebuf
+
+
+def effective_flops(hq, n, d, k, bk, batch=1):
+    """The metric's FLOP count 4*Hq*N*d*k*B_k ("MSA ... KV-outer" page, eq. 13/15)."""
+    return 4.0 * batch * hq * n * d * k * bk
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+

@@ -1,0 +1,230 @@
+/*
+ * bsa.h -- C ABI of the GB300 (sm_103a) block-sparse attention library.
+ *
+ * Mean-pooled, block-routed, block-sparse attention:
+ *   tile map -> mean pool -> E = Q_bar K_bar^T / sqrt(D) -> per-row TopK ->
+ *   exact online-softmax attention over the selected key blocks,
+ * plus the caller-routed GQA variant (NSA selected branch), the KV-outer
+ * order (reverse index, partial pass, log-sum-exp combine) and the
+ * exact-plus-summary variant.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers marked [device] are CUDA device pointers owned by the caller;
+ *    the library never frees or keeps them past the call.  Pointers marked
+ *    [host] are host memory.  No entry point allocates device memory.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) unless it says otherwise.
+ *  - The return value reports host-side validation and launch errors:
+ *    BSA_ERR_INVALID_ARG (a null pointer, a size out of range),
+ *    BSA_ERR_UNSUPPORTED (a valid request this build does not implement),
+ *    BSA_ERR_CUDA (a CUDA launch error).  bsa_last_error() gives the message.
+ *  - Errors found on the device (an index outside its range, a bounded wait
+ *    that expired) are latched in a device status word; bsa_device_status()
+ *    synchronises the stream, returns that status and clears it.
+ *  - Index lists use -1 as padding; kernels read only the first `num` entries.
+ *  - dtype: BSA_F32 (float) or BSA_BF16 (bfloat16).  Accumulation is float32.
+ *  - LSE outputs are natural-log log-sum-exp of the scaled logits of a row
+ *    (-inf for a row with no visible key).
+ *  - Layout "BHSD" means a contiguous [BH, N, D] array, BH = batch * heads,
+ *    N tokens in raster order (a dense prefix first, then the video tokens
+ *    with x fastest).  Layout "BTHD" means a contiguous [B, T, heads, D].
+ *
+ * Pages cited (by title and section):
+ *  [VSA]   "VSA 实现详解：三维分块、均值路由与块稀疏 Attention" (maple.link)
+ *  [NSA]   "NSA 算子解析（Torch/Tilelang）" (devpress.csdn.net)
+ *  [MSA]   "MSA 为什么采用 KV-outer Sparse Attention Forward" (notes.kuangjux.top)
+ *  [Spark] "深度解读|Spark-H3：从注意力几何到稀疏内核代码" (jefxiong.cn)
+ */
+#ifndef BSA_H
+#define BSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSA_OK = 0,
+    BSA_ERR_INVALID_ARG = 1,
+    BSA_ERR_UNSUPPORTED = 2,
+    BSA_ERR_CUDA = 3,
+    BSA_ERR_INDEX = 4,   /* device: an index outside its range was skipped */
+    BSA_ERR_TIMEOUT = 5  /* device: a bounded wait expired; that tile was abandoned */
+} bsa_status;
+
+typedef enum { BSA_F32 = 0, BSA_BF16 = 1 } bsa_dtype;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int bsa_version(void);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* bsa_last_error(void);
+
+/* Synchronises `stream`, then returns and clears the device status word of
+ * the current device (BSA_OK, BSA_ERR_INDEX or BSA_ERR_TIMEOUT), or
+ * BSA_ERR_CUDA if the synchronisation itself failed. */
+bsa_status bsa_device_status(void* stream);
+
+/* ------------------------------------------------------------------ a1 ----
+ * Tile map.  [VSA] §1: index(t,y,x) = t*H*W + y*W + x; the (bT,bH,bW) grid
+ * of blocks numbered row-major, J = ceil(T/bT)*ceil(H/bH)*ceil(W/bW); edge
+ * blocks keep their true length n_i.  [VSA] §3: members laid out t-major,
+ * then y, then x.  [VSA] §5.2: a dense prefix is cut into contiguous blocks
+ * placed first.  [Spark] §04: with a permutation, block j holds the raster
+ * video tokens perm[j*M .. j*M+M-1] (the reblocked layout).
+ *
+ * Total block count for a geometry (host, no CUDA call): the prefix blocks
+ * ceil(n_prefix/M) plus either the 3-D block count or ceil(T*H*W/M) when
+ * `permuted` is nonzero.  Returns -1 on invalid sizes. */
+int bsa_tile_count(int T, int H, int W, int bT, int bH, int bW, int n_prefix, int permuted, int M);
+
+/* Writes index_map [J, M] int32 [device] (token position of each slot, valid
+ * members first, -1 padding) and block_sizes [J] int32 [device] (n_j).
+ * perm: [device] int32 [T*H*W] permutation of the raster video order, or NULL
+ * for 3-D tiling.  Requires bT*bH*bW <= M when perm is NULL. */
+bsa_status bsa_tile_map(int T, int H, int W, int bT, int bH, int bW, int n_prefix,
+                        const int32_t* perm, int M, int32_t* index_map, int32_t* block_sizes,
+                        void* stream);
+
+/* Keep budget R = max(1, min(ceil((1-s)*J), J)) ([VSA] §2.2), with
+ * (1-s)*J computed in double and 1e-9 subtracted before the ceiling so that a
+ * decimal sparsity such as 0.9 gives ceil(96) and not ceil(96.00000000000001).
+ * Host, no CUDA call; returns -1 for J < 1 or s outside [0, 1]. */
+int bsa_budget(int J, double sparsity);
+
+/* ------------------------------------------------------------------ a2 ----
+ * Mean pooling.  [VSA] §2.1: q_bar_i = (1/n_i) sum_{a in block i} q_a, per
+ * (batch, head), channels not mixed; the divisor is the true length n_i.
+ * q, k: [device] BHSD of `dtype`; v may be NULL.  index_map / block_sizes as
+ * written by bsa_tile_map, J blocks of capacity M (M <= 1024).
+ * qbar, kbar (and vbar when v != NULL): [device] float [BH, J, D].
+ * kbar_lp / vbar_lp: optional [device] copies of kbar / vbar in `dtype`
+ * (the summary keys and values consumed by bsa_fwd_summary), or NULL.
+ * 1 <= D <= 256. */
+bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtype dtype,
+                           int BH, int N, int D, const int32_t* index_map,
+                           const int32_t* block_sizes, int J, int M,
+                           float* qbar, float* kbar, float* vbar,
+                           void* kbar_lp, void* vbar_lp, void* stream);
+
+/* ------------------------------------------------------------------ a3 ----
+ * Routing.  [VSA] §2.2: E = Q_bar K_bar^T * scale per (batch, head), shape
+ * [J, J] (scale = 1/sqrt(D) on the page); every row keeps its own TopK.
+ * [VSA] §4: the result is q2k_idx (ascending block ids, -1 padded to kmax)
+ * and q2k_num.  Ties keep the lower block index.
+ * qbar, kbar: [device] float; row i of head h at ptr + h*head_stride + i*D.
+ * q2k_idx: [device] int32 [BH, J, kmax]; q2k_num: [device] int32 [BH, J].
+ * 1 <= k <= J, k <= kmax, J <= 8192, D <= 256.  E is computed in float32. */
+bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, int D,
+                          int64_t head_stride, int k, float scale, int kmax,
+                          int32_t* q2k_idx, int32_t* q2k_num, void* stream);
+
+/* ------------------------------------------------------------------ a4 ----
+ * Block-sparse attention, query-outer order.  [VSA] §6.3: for query block i,
+ * loop over its selected key blocks j, S = Q_i K_j^T * scale, mask keys at
+ * slots >= n_j, online softmax, O = U / l, outputs written back through the
+ * inverse map ([VSA] §3).  [VSA] §5.3: the first `prefix_blocks` blocks are a
+ * dense prefix: every query keeps all of their keys, and their own query rows
+ * attend to every key.  q2k_idx [BH, J-prefix_blocks, kmax] / q2k_num hold
+ * routed block ids counted among the routed blocks.
+ * q, k, v, out: [device] BHSD of `dtype`; lse: [device] float [BH, N] or NULL.
+ * bf16 with D = 128 and M = 128 runs on the tcgen05 tensor-core kernel;
+ * other shapes (D <= 128, M <= 128) on the CUDA-core kernel. */
+bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype dtype,
+                          int BH, int N, int D, const int32_t* index_map,
+                          const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                          const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
+                          float scale, void* out, float* lse, void* stream);
+
+/* Token-granular GQA variant (the NSA selected branch).  [NSA] naive
+ * definition: query head hq of token t reads KV head hq / G (G = HQ/H) and
+ * the keys idx*BS + u of the first block_counts[b,t,h] slots of
+ * block_indices[b,t,h,:]; keys after t are masked when `causal`; scale is
+ * applied to the logits (K^-1/2 on the page).
+ * q, out: [device] BTHD [B, T, HQ, D]; k, v: [device] BTHD [B, T, H, D];
+ * block_indices: [device] int32 [B, T, H, S]; block_counts: [device] int32
+ * [B, T, H]; lse: [device] float [B, T, HQ] or NULL.  D <= 128, BS <= 128. */
+bsa_status bsa_fwd_qouter_tokens(const void* q, const void* k, const void* v, bsa_dtype dtype,
+                                 int B, int T, int HQ, int H, int D,
+                                 const int32_t* block_indices, const int32_t* block_counts,
+                                 int S, int block_size, int causal, float scale,
+                                 void* out, float* lse, void* stream);
+
+/* ------------------------------------------------------------------ a5 ----
+ * Reverse index and schedule.  [MSA] §5: q2k (query -> blocks) becomes a CSR
+ * k2q (block -> queries): count per (KV head, block), prefix sum, scatter.
+ * [MSA] §7: rows are cut into chunks of at most chunk_cap queries; every
+ * entry carries its slot s in [0, S) (the position of the block in the
+ * query's list), so partials never collide.
+ * q2k_idx: [device] int32 [B, N, H, S] (token-major, as the NSA
+ * block_indices); q2k_num: [device] int32 [B, N, H].  R = B*H CSR row groups,
+ * row id = (b*H + h)*nblk + blk.  Within a row, query ids ascend.
+ * Outputs [device]: row_ptr int32 [R*nblk + 1]; q_idx, slot int32 [R*N*S]
+ * (first row_ptr[R*nblk] entries used); chunks int32 [max_chunks, 4] =
+ * (row, start, length, 0) in row order; n_chunks int32 [1].
+ * workspace: [device] scratch of bsa_reverse_index_workspace() bytes.
+ * max_chunks must be >= bsa_max_chunks(...). */
+size_t bsa_reverse_index_workspace(int B, int N, int H, int nblk);
+int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap);
+bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_num,
+                                   int B, int N, int H, int S, int nblk, int chunk_cap,
+                                   int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
+                                   int32_t* chunks, int32_t* n_chunks, int max_chunks,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------ a6 ----
+ * KV-outer partial pass (K1).  [MSA] §4 and §6.1: one CTA per chunk keeps
+ * the K/V block resident and streams the chunk's queries (all G heads of a
+ * position together); for each (query, head): S_j over the block's visible
+ * keys (causal: key <= query position), L_s = log sum exp S_j,
+ * O_s = sum exp(S_j - L_s) V_j, written to slot s.
+ * q: [device] BTHD [B, N, HQ, D]; k, v: [device] BTHD [B, N, H, D];
+ * CSR / chunks from bsa_build_reverse_index.
+ * obuf: [device] [B, N, HQ, S, D] of obuf_dtype; lsebuf: [device] float
+ * [B, N, HQ, S].  Slots that no chunk writes are left untouched. */
+bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtype dtype,
+                           int B, int N, int HQ, int H, int D,
+                           const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot,
+                           const int32_t* chunks, const int32_t* n_chunks, int max_chunks,
+                           int nblk, int block_size, int S, int causal, float scale,
+                           void* obuf, bsa_dtype obuf_dtype, float* lsebuf, void* stream);
+
+/* ------------------------------------------------------------------ a7 ----
+ * Exact combine (K2).  [MSA] §6.2: a = max_s L_s, L = a + log sum_s
+ * exp(L_s - a), w_s = exp(L_s - L), O = sum_s w_s O_s, over the first
+ * nslots[b, t, h] slots (h = hq / G) whose L_s is finite.
+ * obuf / lsebuf as written by bsa_fwd_kvouter; nslots: [device] int32
+ * [B, N, H]; out: [device] BTHD [B, N, HQ, D] of out_dtype; lse: [device]
+ * float [B, N, HQ] or NULL. */
+bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lsebuf,
+                       const int32_t* nslots, int B, int N, int HQ, int H, int S, int D,
+                       void* out, bsa_dtype out_dtype, float* lse, void* stream);
+
+/* ------------------------------------------------------------------ a8 ----
+ * Exact plus summary.  [Spark] §03: each unselected routed block j becomes
+ * one virtual key kbar_j with value vbar_j and logit q.kbar_j*scale + log(n_j),
+ * merged into the same softmax as the exact keys (the prefix blocks and the
+ * selected routed blocks).  Prefix query rows attend densely to every key
+ * ([VSA] §5.3, Context rows are global).
+ * Arguments as bsa_fwd_qouter, plus kbar_lp / vbar_lp: [device] [BH, J, D]
+ * in `dtype`, the block means as written by bsa_pool_blocks (the rows of
+ * the prefix blocks are not read).  J - prefix_blocks <= 1024. */
+bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype,
+                           int BH, int N, int D, const int32_t* index_map,
+                           const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                           const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
+                           const void* kbar_lp, const void* vbar_lp,
+                           float scale, void* out, float* lse, void* stream);
+
+/* Forces the CUDA-core attention kernels even where a tensor-core kernel
+ * exists (1) or restores the default dispatch (0).  Host, process-wide. */
+void bsa_set_force_simt(int force);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H */

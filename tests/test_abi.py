@@ -1,0 +1,84 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol, and its
+host-only helpers and argument checks behave (no GPU needed)."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import ROOT
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "bsa.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*[A-Za-z_][A-Za-z0-9_\s\*]*?\b(bsa_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def bsa():
+    from block_sparse_attention_tile_gb300.build import build
+    build()
+    from block_sparse_attention_tile_gb300 import bsa as mod
+    return mod
+
+
+def test_every_declared_symbol_is_exported(bsa):
+    declared = _declared_functions()
+    assert len(declared) >= 17
+    for name in declared:
+        assert hasattr(bsa._lib, name), name
+        assert name in bsa.EXPORTED, name
+
+
+def test_only_declared_symbols_are_exported():
+    import subprocess
+    from block_sparse_attention_tile_gb300.build import LIB, build
+    build()
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB], capture_output=True, text=True).stdout
+    ours = sorted({l.split()[-1] for l in out.splitlines() if l.split()[-1].startswith("bsa_")})
+    assert ours == _declared_functions()
+
+
+def test_budget_matches_oracle(bsa):
+    for J in [1, 2, 7, 32, 256, 960, 4096]:
+        for pct in range(0, 101):
+            s = pct / 100
+            assert bsa.bsa_budget(J, s) == oracle.budget(J, s), (J, s)
+    assert bsa.bsa_budget(0, 0.5) == -1 and bsa.bsa_budget(4, 1.5) == -1
+
+
+def test_tile_count_matches_oracle(bsa):
+    for (T, H, W), (bT, bH, bW) in [((4, 4, 4), (4, 2, 2)), ((5, 3, 4), (2, 2, 3)),
+                                    ((30, 48, 80), (4, 4, 8)), ((8, 16, 16), (4, 4, 4))]:
+        M = bT * bH * bW
+        assert bsa.bsa_tile_count(T, H, W, bT, bH, bW, 0, False, M) == oracle.num_blocks(T, H, W, bT, bH, bW)
+        assert bsa.bsa_tile_count(T, H, W, bT, bH, bW, 300, False, M) == \
+            oracle.num_blocks(T, H, W, bT, bH, bW) + len(oracle.tile_prefix(300, M))
+    assert bsa.bsa_tile_count(16, 32, 64, 1, 1, 1, 1024, True, 128) == 8 + 256
+    assert bsa.bsa_tile_count(4, 4, 4, 4, 4, 4, 0, False, 32) == -1  # window larger than M
+
+
+def test_reverse_index_sizes(bsa):
+    assert bsa.bsa_reverse_index_workspace(1, 32768, 4, 256) == 4 * 128 * 256 * 4
+    m = bsa.bsa_max_chunks(1, 32768, 4, 16, 256, 4096)
+    # every chunk list fits: one partial chunk per row plus full chunks
+    assert m >= 4 * 256 + (4 * 32768 * 16) // 4096
+
+
+def test_invalid_arguments_are_rejected_without_cuda(bsa):
+    lib = bsa._lib
+    rc = lib.bsa_route_topk(None, None, 1, 4, 2, 8, 2, 1.0, 4, None, None, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
+    rc = lib.bsa_pool_blocks(1, 1, None, 1, 1, 8, 0, 1, 1, 4, 16, 1, 1, None, None, None, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG
+    rc = lib.bsa_fwd_qouter(1, 1, 1, 1, 1, 64, 128, 1, 1, 1, 256, 0, 1, 1, 8, 1.0, 1, None, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
+    rc = lib.bsa_route_topk(1, 1, 1, 4, 2, 8, 5, 1.0, 5, 1, 1, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG  # k > J
+    rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG  # max_chunks too small
+    assert bsa.bsa_version() >= 100

@@ -1,0 +1,221 @@
+"""CUDA path vs the CPU oracle, element by element, on small seeded inputs
+that still span several tiles and a ragged tail.  Every call goes through the
+C ABI (block_sparse_attention_tile_gb300.bsa)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_tile_gb300 import synthetic
+from parity import assert_close, check_route, f64, oracle_blocks
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean_status(lib):
+    lib.bsa_set_force_simt(False)
+    yield
+    lib.bsa_set_force_simt(False)
+    assert lib.bsa_device_status() == lib.BSA_OK
+
+
+def _pipeline():
+    from block_sparse_attention_tile_gb300 import pipeline
+    return pipeline
+
+
+# ---------------------------------------------------------------- a1 tile map
+
+@pytest.mark.parametrize("grid,block,M,n_prefix,permuted", [
+    ((4, 4, 4), (4, 2, 2), 16, 0, False),
+    ((5, 3, 4), (2, 2, 3), 12, 0, False),
+    ((30, 48, 80), (4, 4, 8), 128, 0, False),
+    ((6, 8, 10), (4, 4, 8), 128, 300, False),
+    ((6, 8, 10), (1, 1, 1), 128, 300, True),
+    ((16, 32, 64), (1, 1, 1), 128, 1024, True),
+])
+def test_tile_map_bit_exact(lib, grid, block, M, n_prefix, permuted):
+    pl = _pipeline()
+    T, H, W = grid
+    perm = synthetic.permutation(T * H * W, 7) if permuted else None
+    geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
+                       perm=torch.as_tensor(perm, device=DEV) if permuted else None)
+    im, bs = pl.tile_map(geom)
+    blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
+    assert np.array_equal(im.cpu().numpy(), oracle.index_map(blocks, M))
+    assert np.array_equal(bs.cpu().numpy(), [len(b) for b in blocks])
+
+
+# ---------------------------------------------------------------- a2-a4, block granularity
+
+def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, force_simt=False,
+                    n_prefix=0, permuted=False, summary=False, cluster=False):
+    pl = _pipeline()
+    T, H, W = grid
+    if cluster:
+        q, kk, v = synthetic.cluster_qkv(B * h, n_prefix, T * H * W, D, seed, dtype)
+    else:
+        q, kk, v = synthetic.video_qkv(B, h, T, H, W, D, seed, dtype, field=field)
+        if n_prefix:
+            extra = synthetic.video_qkv(B, h, 1, 1, n_prefix, D, seed + 50, dtype)
+            q, kk, v = (torch.cat([e, x], dim=1) for e, x in zip(extra, (q, kk, v)))
+    perm = synthetic.permutation(T * H * W, seed + 3) if permuted else None
+    geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
+                       perm=torch.as_tensor(perm, device=DEV) if permuted else None)
+    lib.bsa_set_force_simt(force_simt)
+    res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary)
+    torch.cuda.synchronize()
+    blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
+    P = len(oracle.tile_prefix(n_prefix, M))
+    scale = D ** -0.5
+    flagged = 0
+    for bh in range(B * h):
+        Q, K, V = f64(q[bh]), f64(kk[bh]), f64(v[bh])
+        qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        assert np.abs(res.qbar[bh].cpu().numpy() - qbar).max() <= 1e-5 * max(1.0, np.abs(qbar).max())
+        assert np.abs(res.kbar[bh].cpu().numpy() - kbar).max() <= 1e-5 * max(1.0, np.abs(kbar).max())
+        E = oracle.routing_scores(qbar[P:], kbar[P:], D)
+        gi, gn = res.q2k_idx[bh].cpu().numpy(), res.q2k_num[bh].cpu().numpy()
+        flagged += len(check_route(gi, gn, E, k))
+        if summary:
+            vbar = oracle.pool_blocks(V, blocks)
+            O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kbar[P:], vbar[P:], scale, prefix_blocks=P)
+        else:
+            O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, scale, prefix_blocks=P)
+        assert_close(f64(res.out[bh]), O, dtype, "out[bh=%d]" % bh)
+        assert np.abs(res.lse[bh].cpu().numpy() - L).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
+    return flagged
+
+
+def test_video_tiny_fp32_full_config(lib):
+    # B=1, h=2, D=64, grid (8,16,16), block (4,4,4) -> J=32, k=8, fp32
+    _run_block_case(lib, 1, 2, (8, 16, 16), (4, 4, 4), 64, 64, 8, torch.float32, 101)
+
+
+def test_unit_grid_d2_fp32(lib):
+    _run_block_case(lib, 1, 1, (4, 4, 4), (4, 2, 2), 16, 2, 2, torch.float32, 11)
+
+
+@pytest.mark.parametrize("k", [1, 3, 12])
+def test_ragged_hw_fp32_and_keep_all(lib, k):
+    # (5,3,4) grid in (2,2,3) windows: scattered ragged members; k=12 keeps all
+    _run_block_case(lib, 1, 2, (5, 3, 4), (2, 2, 3), 12, 16, k, torch.float32, 12)
+
+
+@pytest.mark.parametrize("force_simt", [False, True])
+def test_video_dit_shape_small_bf16(lib, force_simt):
+    # (4,4,8) blocks over a (6,16,24) grid: 2*4*3 = 24 blocks, the last t-row holds 2 frames
+    _run_block_case(lib, 1, 2, (6, 16, 24), (4, 4, 8), 128, 128, 6, torch.bfloat16, 202, field=True,
+                    force_simt=force_simt)
+
+
+def test_dense_prefix_and_permutation_bf16(lib):
+    _run_block_case(lib, 1, 2, (4, 8, 16), (1, 1, 1), 128, 128, 2, torch.bfloat16, 31, n_prefix=200,
+                    permuted=True)
+
+
+@pytest.mark.parametrize("force_simt", [False, True])
+def test_summary_small_bf16(lib, force_simt):
+    # 256 text tokens + a (4,16,32) grid under a permutation: 2 prefix + 16 routed blocks, k=3
+    _run_block_case(lib, 1, 2, (4, 16, 32), (1, 1, 1), 128, 128, 3, torch.bfloat16, 505, n_prefix=256,
+                    permuted=True, summary=True, cluster=True, force_simt=force_simt)
+
+
+def test_summary_fp32_ragged(lib):
+    _run_block_case(lib, 1, 1, (5, 3, 4), (2, 2, 3), 12, 8, 2, torch.float32, 14, n_prefix=20,
+                    summary=True)
+
+
+# ---------------------------------------------------------------- token granularity + KV-outer
+
+def _nsa_inputs(B, T, HQ, H, D, BS, S, seed, dtype, zipf=False):
+    q = synthetic.normal((B, T, HQ, D), seed, dtype=dtype)
+    k = synthetic.normal((B, T, H, D), seed + 1, dtype=dtype)
+    v = synthetic.normal((B, T, H, D), seed + 2, dtype=dtype)
+    if zipf:
+        idx, cnt = synthetic.zipf_block_lists(B, T, H, S, BS, seed)
+    else:
+        idx, cnt = synthetic.causal_block_lists(B, T, H, S, BS, seed)
+    return q, k, v, idx, cnt
+
+
+def _oracle_nsa(q, k, v, idx, cnt, BS, b, tokens=None):
+    return oracle.nsa_selected_attention(f64(q[b]), f64(k[b]), f64(v[b]), idx[b], cnt[b], BS,
+                                         tokens=tokens)
+
+
+@pytest.mark.parametrize("dtype,BS,S,zipf", [(torch.bfloat16, 64, 16, False), (torch.float32, 32, 4, False),
+                                             (torch.bfloat16, 128, 16, True)])
+def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf):
+    pl = _pipeline()
+    B, T, HQ, H, D = 2, 448, 32, 2, 128 if dtype == torch.bfloat16 else 64
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 303, dtype, zipf)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    idx_d, cnt_d = torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV)
+    o_q, l_q = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    nblk = -(-T // BS)
+    o_kv, l_kv, plan, obuf, lbuf = pl.kvouter_attention(
+        qd, kd, vd, idx_d, cnt_d, BS, chunk_cap=300,
+        obuf_dtype=torch.float32 if dtype == torch.float32 else torch.bfloat16)
+    torch.cuda.synchronize()
+    # reverse index bit-exact: rows ordered (b, h, blk), ascending queries
+    q2k = np.transpose(idx, (0, 2, 1, 3)).reshape(B * H, T, S)
+    num = np.transpose(cnt, (0, 2, 1)).reshape(B * H, T)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk)
+    assert np.array_equal(plan.row_ptr.cpu().numpy(), row_ptr)
+    nnz = int(row_ptr[-1])
+    assert np.array_equal(plan.q_idx[:nnz].cpu().numpy(), q_idx)
+    assert np.array_equal(plan.slot[:nnz].cpu().numpy(), slot)
+    chunks = oracle.schedule_chunks(row_ptr, 300)
+    nch = int(plan.n_chunks.item())
+    assert nch == len(chunks)
+    assert np.array_equal(plan.chunks[:nch, :3].cpu().numpy(), np.array(chunks))
+    for b in range(B):
+        O, L = _oracle_nsa(q, k, v, idx, cnt, BS, b)
+        assert_close(f64(o_q[b]), O, dtype, "qouter b=%d" % b)
+        assert_close(f64(o_kv[b]), O, dtype, "kvouter b=%d" % b)
+        tol = 1e-5 if dtype == torch.float32 else 2e-3
+        assert np.abs(l_q[b].cpu().numpy() - L).max() <= tol
+        assert np.abs(l_kv[b].cpu().numpy() - L).max() <= tol
+    # partials of batch 0 vs the K1 definition, on every written slot
+    rp, qi, sl = oracle.reverse_index(np.transpose(idx[0], (1, 0, 2)), np.transpose(cnt[0], (1, 0)), nblk)
+    ob, lb = oracle.kvouter_partials(f64(q[0]), f64(k[0]), f64(v[0]), rp, qi, sl, nblk, BS, S, H)
+    G = HQ // H
+    written = np.zeros((T, HQ, S), bool)
+    for t in range(T):
+        for hq in range(HQ):
+            written[t, hq, :cnt[0, t, hq // G]] = True
+    got_o = f64(obuf[0])[written]
+    got_l = lbuf[0].cpu().numpy()[written]
+    assert_close(got_o, ob[written], dtype, "O_buf")
+    assert np.abs(got_l - lb[written]).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
+
+
+# ---------------------------------------------------------------- device-side error reporting
+
+def test_out_of_range_block_index_is_reported_not_faulted(lib):
+    pl = _pipeline()
+    B, T, HQ, H, D, BS, S = 1, 256, 16, 1, 64, 64, 4
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 9, torch.float32)
+    idx = idx.copy()
+    idx[0, 200, 0, 0] = 1000  # block 1000 does not exist
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    pl.nsa_qouter(qd, kd, vd, torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV), BS)
+    assert lib.bsa_device_status() == lib.BSA_ERR_INDEX
+    assert lib.bsa_device_status() == lib.BSA_OK  # cleared by the read
+    # the reverse index flags it too and still builds the valid part
+    pl.reverse_index(torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV), T // BS, 64)
+    assert lib.bsa_device_status() == lib.BSA_ERR_INDEX
+
+
+def test_route_bad_arguments_raise(lib):
+    x = torch.zeros((1, 4, 8), device=DEV)
+    with pytest.raises(lib.BsaError):
+        lib.bsa_route_topk(x, x, 1, 4, 8, 32, 5, 1.0, 5, torch.zeros((1, 4, 5), dtype=torch.int32, device=DEV),
+                           torch.zeros((1, 4), dtype=torch.int32, device=DEV))
