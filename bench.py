@@ -198,7 +198,10 @@ def gpu_arm(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOAD
+    w = dict(WORKLOAD)
+    if args.heads:
+        w["heads"] = args.heads
+        w["name"] = WORKLOAD["name"] + "_%dheads" % args.heads
     T, H, W = w["grid"]
     N = T * H * W
     BH, D, M, k = w["B"] * w["heads"], w["D"], w["M"], w["k"]
@@ -308,6 +311,9 @@ def gpu_arm(args):
         tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         attn_tflops = attn_flops / (stage_ms["attention"] * 1e-3) / 1e12
         pool_gbs = pool_bytes / (stage_ms["pool"] * 1e-3) / 1e9
+        props = torch.cuda.get_device_properties(dev)
+        fp32_peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        route_tflops = 2.0 * BH * J * J * D / (stage_ms["route"] * 1e-3) / 1e12
         line = {
             "metric": "sparse-attn effective TFLOP/s (4*Hq*N*d*k*Bk/s)",
             "value": world * flops / (ms_step * 1e-3) / 1e12,
@@ -332,7 +338,10 @@ def gpu_arm(args):
                          "algorithmic_flops_per_launch": attn_flops},
             "rooflines_secondary": {
                 "pool": {"bound": "hbm", "achieved": pool_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes}},
+                         "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
+                "route": {"bound": "alu", "achieved": route_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                          "frac": route_tflops / fp32_peak, "flops_per_launch": 2.0 * BH * J * J * D,
+                          "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}},
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
                     "ms_per_step": e2e_ms},
@@ -381,6 +390,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="fewer heads than the workload's 24 (a small case for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

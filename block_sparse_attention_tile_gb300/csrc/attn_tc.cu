@@ -323,30 +323,43 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t tS = tS0 + (uint32_t)b * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                ptx::tmem_ld32(tS + c * 32, r);
+            {
+                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
+                ptx::tmem_ld32(tS + 0, xr + 0);
+                ptx::tmem_ld32(tS + 32, xr + 32);
+                ptx::tmem_ld32(tS + 64, xr + 64);
+                ptx::tmem_ld32(tS + 96, xr + 96);
                 ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]);
             }
             const int blk = list[s];
             const int nv = nvalid[s];
-            float mx = -CUDART_INF_F;
-            if (blk >= 0) {
+            float mxp[8];
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = c < nv ? x[c] * prm.scale_log2 : -CUDART_INF_F;
-                    mx = fmaxf(mx, x[c]);
+            for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
+            if (blk >= 0) {
+                if (nv >= kBN) {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] *= prm.scale_log2;
+                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = c < nv ? x[c] * prm.scale_log2 : -CUDART_INF_F;
+                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+                    }
                 }
             } else {
                 const float* bt = bias + (-blk - 1) * kBN;
 #pragma unroll
                 for (int c = 0; c < kBN; ++c) {
                     x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
-                    mx = fmaxf(mx, x[c]);
+                    mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                 }
             }
+            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             const float m_new = fmaxf(m_ref, mx);
             const bool need = m_new > m_ref + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
@@ -369,13 +382,16 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ptx::tmem_wait_st();
                 }
             }
-            float sum = 0.f;
+            float sp[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sp[u] = 0.f;
             const bool live = m_ref != -CUDART_INF_F;
 #pragma unroll
             for (int c = 0; c < kBN; ++c) {
                 x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
-                sum += x[c];
+                sp[c & 7] += x[c];
             }
+            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l += sum;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {

@@ -29,11 +29,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     int32_t* __restrict__ q2k_num) {
     extern __shared__ __align__(16) float smem[];
     float* qs = smem;                              // [kRouteRows][Dp]
-    float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp]
-    float* E = ks + kRouteCols * Dp;               // [kRouteRows][J]
+    float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp + 4]
+    float* E = ks + kRouteCols * (Dp + 4);         // [kRouteRows][J]
     const int bh = blockIdx.y;
     const int row0 = blockIdx.x * kRouteRows;
     const int nrows = min(kRouteRows, J - row0);
+    const int Dk = Dp + 4;  // padded row stride of the staged key tile: conflict-free float4 reads
     const float* qh = qbar + (long long)bh * head_stride;
     const float* kh = kbar + (long long)bh * head_stride;
     const int tid = threadIdx.x;
@@ -48,7 +49,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
         __syncthreads();
         for (int idx = tid; idx < kRouteCols * Dp; idx += blockDim.x) {
             const int c = idx / Dp, d = idx % Dp;
-            ks[idx] = (c0 + c < J && d < D) ? kh[(long long)(c0 + c) * D + d] : 0.f;
+            ks[c * Dk + d] = (c0 + c < J && d < D) ? kh[(long long)(c0 + c) * D + d] : 0.f;
         }
         __syncthreads();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
             const float4 a = q4[d4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const float4 b = reinterpret_cast<const float4*>(ks + (cg + 16 * c) * Dp)[d4];
+                const float4 b = reinterpret_cast<const float4*>(ks + (cg + 16 * c) * Dk)[d4];
                 acc[c] = fmaf(a.x, b.x, acc[c]);
                 acc[c] = fmaf(a.y, b.y, acc[c]);
                 acc[c] = fmaf(a.z, b.z, acc[c]);
@@ -75,33 +76,70 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     const int warp = tid / 32, lane = tid % 32;
     for (int rr = warp; rr < nrows; rr += kRouteThreads / 32) {
         const float* e = E + rr * J;
-        uint32_t prefix = 0;
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = prefix | (1u << bit);
-            int cnt = 0;
-            for (int c = lane; c < J; c += 32) cnt += order_key(e[c]) >= cand;
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
-            if (cnt >= k) prefix = cand;
-        }
-        // prefix is the k-th largest key; keep everything above it and the
-        // lowest-index entries equal to it.
-        int n_gt = 0;
-        for (int c = lane; c < J; c += 32) n_gt += order_key(e[c]) > prefix;
-        n_gt = __reduce_add_sync(0xffffffffu, n_gt);
-        const int need_eq = k - n_gt;
-        int eq_seen = 0, written = 0;
         int32_t* out = q2k_idx + ((long long)bh * J + row0 + rr) * kmax;
-        for (int base = 0; base < J; base += 32) {
-            const int c = base + lane;
-            const uint32_t key = c < J ? order_key(e[c]) : 0u;
-            const bool eq = c < J && key == prefix;
-            const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
-            const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
-            const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
-            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
-            written += __popc(sel_mask);
-            eq_seen += __popc(eq_mask);
+        if (J <= 1024) {
+            // the row's keys stay in registers: lane holds columns lane + 32*i
+            uint32_t key[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = lane + 32 * i;
+                key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
+            }
+            uint32_t prefix = 0;
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t cand = prefix | (1u << bit);
+                int cnt = 0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) cnt += key[i] >= cand;
+                cnt = __reduce_add_sync(0xffffffffu, cnt);
+                if (cnt >= k) prefix = cand;
+            }
+            int n_gt = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) n_gt += key[i] > prefix;
+            n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+            const int need_eq = k - n_gt;
+            int eq_seen = 0, written = 0;
+            const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int c = lane + 32 * i;
+                const bool eq = c < J && key[i] == prefix;
+                const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+                const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
+                const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+                if (sel) out[written + __popc(sel_mask & lt)] = c;
+                written += __popc(sel_mask);
+                eq_seen += __popc(eq_mask);
+            }
+        } else {
+            uint32_t prefix = 0;
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t cand = prefix | (1u << bit);
+                int cnt = 0;
+                for (int c = lane; c < J; c += 32) cnt += order_key(e[c]) >= cand;
+                cnt = __reduce_add_sync(0xffffffffu, cnt);
+                if (cnt >= k) prefix = cand;
+            }
+            // prefix is the k-th largest key; keep everything above it and the
+            // lowest-index entries equal to it.
+            int n_gt = 0;
+            for (int c = lane; c < J; c += 32) n_gt += order_key(e[c]) > prefix;
+            n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+            const int need_eq = k - n_gt;
+            int eq_seen = 0, written = 0;
+            for (int base = 0; base < J; base += 32) {
+                const int c = base + lane;
+                const uint32_t key = c < J ? order_key(e[c]) : 0u;
+                const bool eq = c < J && key == prefix;
+                const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+                const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
+                const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
+                const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+                if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
+                written += __popc(sel_mask);
+                eq_seen += __popc(eq_mask);
+            }
         }
         for (int s = k + lane; s < kmax; s += 32) out[s] = -1;
         if (lane == 0) q2k_num[(long long)bh * J + row0 + rr] = k;
@@ -121,7 +159,7 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     BSA_REQUIRE(k >= 1 && k <= J && kmax >= k, "route: need 1 <= k <= J and k <= kmax");
     BSA_REQUIRE(head_stride >= (int64_t)J * D, "route: head_stride smaller than J*D");
     const int Dp = (D + 3) / 4 * 4;
-    const size_t smem = sizeof(float) * ((size_t)(kRouteRows + kRouteCols) * Dp + (size_t)kRouteRows * J);
+    const size_t smem = sizeof(float) * ((size_t)kRouteRows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)kRouteRows * J);
     if (smem > 227 * 1024) return fail(BSA_ERR_UNSUPPORTED, "route: J=%d D=%d needs too much shared memory", J, D);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

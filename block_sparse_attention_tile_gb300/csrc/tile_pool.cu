@@ -76,21 +76,34 @@ __global__ void __launch_bounds__(256) pool_kernel(
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
     if (rg < RG && lane * VEC < D) {
-        for (int r = rg; r < n; r += RG) {
-            const int tok = rows[r];
-            if (tok < 0 || tok >= N) { raise_status(status, BSA_ERR_INDEX); continue; }
-            const T* row = base + (size_t)tok * D + lane * VEC;
-            if (VEC > 1 && lane * VEC + VEC <= D) {
-                if constexpr (sizeof(T) * VEC == 16) {
-                    uint4 raw = *reinterpret_cast<const uint4*>(row);
-                    const T* e8 = reinterpret_cast<const T*>(&raw);
+        if constexpr (sizeof(T) * VEC == 16) {
+            // batches of 8 rows: the 8 token ids first, then 8 independent 16-byte loads
+            constexpr int U = 8;
+            for (int r0 = rg; r0 < n; r0 += RG * U) {
+                int tok[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int r = r0 + u * RG;
+                    tok[u] = r < n ? rows[r] : -1;
+                    if (r < n && (tok[u] < 0 || tok[u] >= N)) { raise_status(status, BSA_ERR_INDEX); tok[u] = -1; }
+                }
+                uint4 raw[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    raw[u] = tok[u] >= 0 ? __ldg(reinterpret_cast<const uint4*>(base + (size_t)tok[u] * D + lane * VEC))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const T* e8 = reinterpret_cast<const T*>(&raw[u]);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) acc[e] += to_f32(row[e]);
                 }
-            } else {
+            }
+        } else {
+            for (int r = rg; r < n; r += RG) {
+                const int tok = rows[r];
+                if (tok < 0 || tok >= N) { raise_status(status, BSA_ERR_INDEX); continue; }
+                const T* row = base + (size_t)tok * D + lane * VEC;
                 for (int e = 0; e < VEC; ++e)
                     if (lane * VEC + e < D) acc[e] += to_f32(row[e]);
             }
