@@ -10,26 +10,35 @@
 // unselected routed block adds one virtual key (its mean key and value) with
 // logit bias log(n_j), folded into the same online softmax.
 //
-// Design (ours, for sm_103a): one CTA per (head, query block), 8 warps.
-//   warp 0      producer: TMA tile::gather4 loads of Q and of every K/V tile
-//               straight from the token-indexed BHSD tensors (the index map
-//               does the 3-D gather / permutation; no pack pass), into
-//               128-byte-swizzled K-major tiles; 2-stage K and V rings.
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
-//               of two S buffers (double buffered so that QK of tile j+1 runs
-//               while the softmax works on tile j), then O += P_j V_j with P_j
-//               read from TMEM (it overwrites S_j in place as packed bf16) and
-//               V_j as an MN-major operand (no transpose pass).
-//   warps 4-7   softmax: one thread per query row; reads S from TMEM, masks,
-//               updates the running max lazily (O in TMEM is rescaled only
-//               when the max grows by more than 2^8), writes P as bf16 into
-//               TMEM, keeps l in a register; epilogue O / l -> bf16 -> global.
-// TMEM: S0 cols [0,128), S1 [128,256), O [256,384) of a 512-column allocation.
+// Design (ours, for sm_103a).  One CTA per (head, pair of query blocks A, B),
+// 12 warps.  Each query block keeps its own key-tile list; the shorter list
+// is padded with fully masked rounds (the VSA page's dual-Q scheduling, §6.3).
+//   warp 0      producer: TMA tile::gather4 loads straight from the
+//               token-indexed BHSD tensors (the index map performs the 3-D
+//               gather or the permutation; no pack pass) into 128-byte
+//               swizzled K-major tiles; one 4-stage ring whose entries follow
+//               the MMA consumption order K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ...;
+//               the next entry's row ids are fetched while it waits.
+//   warp 1      TMEM owner and single-thread MMA issuer:
+//               S_A0, S_B0, then per round j: PV_A(j), S_A(j+1), PV_B(j),
+//               S_B(j+1).  While softmax A works on S_A(j) the tensor core
+//               runs S_B(j) and PV_B(j-1), and the other way round.
+//   warps 4-7   softmax of A, warps 8-11 softmax of B: one thread per query
+//               row; S from TMEM, mask, lazy running max (O is rescaled in
+//               TMEM only when the max grows by more than 2^8), P written back
+//               over S as packed bf16 = the TMEM A operand of P V; l in a
+//               register; epilogue O / l -> bf16 -> global through the map.
+// TMEM (512 columns): S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
+// Registers: warpgroup 0 gives up registers (setmaxnreg.dec 64) so the two
+// softmax warpgroups can hold a full S row (setmaxnreg.inc 216); the launch
+// holds 384 x 168 = 64512 registers, more than the split needs.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA raises
-// BSA_ERR_TIMEOUT, stops issuing, drains its own copies / MMAs and frees TMEM.
+// BSA_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs, frees TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math_constants.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -37,30 +46,34 @@
 namespace bsa {
 namespace tc {
 
-constexpr int kBM = 128;          // query rows per CTA
+constexpr int kBM = 128;          // query rows per query block
 constexpr int kBN = 128;          // keys per tile
 constexpr int kHD = 128;          // head dim
-constexpr int kThreads = 256;
-constexpr int kMaxList = 1024;    // key tiles per query block, virtual tiles included
+constexpr int kThreads = 384;
+constexpr int kStages = 4;        // K/V ring depth (32 KB each)
+constexpr int kMaxList = 512;     // key tiles per query block, virtual tiles included
 constexpr int kMaxVirtual = 8;    // summary tiles (<= 1024 routed blocks)
+constexpr int kRegsLow = 64, kRegsHigh = 216, kRegsLaunch = 168;
 constexpr uint32_t kTileBytes = kBN * kHD * 2;       // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 16 KB: 128 rows x 64 cols
 constexpr uint64_t kWaitNs = 2000000000ull;          // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
 
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
+
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + kTileBytes;           // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * kTileBytes;       // 2 stages
-constexpr uint32_t OFF_LIST = OFF_V + 2 * kTileBytes;    // int[kMaxList] tile ids (<0: virtual)
-constexpr uint32_t OFF_NVALID = OFF_LIST + 4 * kMaxList; // int[kMaxList]
-constexpr uint32_t OFF_BIAS = OFF_NVALID + 4 * kMaxList; // float[kMaxVirtual][128]
-constexpr uint32_t OFF_SEL = OFF_BIAS + 4 * kMaxVirtual * kBN;  // uint32[32] selected bitmap
-constexpr uint32_t OFF_BAR = OFF_SEL + 4 * 32;           // mbarriers (8 B each)
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9, BAR_PF = 11,
-              BAR_OD = 13, BAR_DRAIN = 14, BAR_OF = 15, NBAR = 16;
-constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;        // tmem base, abort flag, list length
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;    // + alignment slack
+constexpr uint32_t OFF_Q = 0;                                   // Q_A, Q_B
+constexpr uint32_t OFF_RING = OFF_Q + 2 * kTileBytes;
+constexpr uint32_t OFF_LIST = OFF_RING + kStages * kTileBytes;  // int[2][kMaxList]: tile ids (<0: virtual)
+constexpr uint32_t OFF_NVALID = OFF_LIST + 2 * 4 * kMaxList;    // int[2][kMaxList]
+constexpr uint32_t OFF_BIAS = OFF_NVALID + 2 * 4 * kMaxList;    // float[2][kMaxVirtual*128]
+constexpr uint32_t OFF_SEL = OFF_BIAS + 2 * 4 * kMaxVirtual * kBN;  // uint32[2][32]
+constexpr uint32_t OFF_BAR = OFF_SEL + 2 * 4 * 32;
+constexpr int BAR_Q = 0, BAR_FULL = 1, BAR_EMPTY = BAR_FULL + kStages, BAR_SF = BAR_EMPTY + kStages,
+              BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2, BAR_DRAIN = BAR_OF + 2, NBAR = BAR_DRAIN + 1;
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;               // tmem base, abort flag
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;           // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
     const int32_t* index_map;
@@ -89,6 +102,31 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// Entry e of the ring sequence: which query block (X), which round (j), K or V.
+//   one block : K0 | V0 K1 | V1 K2 | ... | V(n-1)                       (2n entries)
+//   two blocks: K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ... | V_A(n-1) V_B(n-1)  (4n entries)
+__device__ __forceinline__ void decode_entry(int e, int n, bool two, int& X, int& j, bool& isV) {
+    if (!two) {
+        X = 0;
+        if (e == 0) { j = 0; isV = false; return; }
+        const int t = e - 1;
+        j = (t >> 1) + (t & 1);
+        isV = !(t & 1);
+        return;
+    }
+    if (e < 2) { X = e; j = 0; isV = false; return; }
+    const int t = e - 2, g = t >> 2, r = t & 3;
+    if (g < n - 1) {
+        X = r >> 1;
+        isV = !(r & 1);
+        j = isV ? g : g + 1;
+    } else {
+        X = r;
+        isV = true;
+        j = n - 1;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -97,37 +135,42 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
-    int* list = reinterpret_cast<int*>(sm + OFF_LIST);
-    int* nvalid = reinterpret_cast<int*>(sm + OFF_NVALID);
-    float* bias = reinterpret_cast<float*>(sm + OFF_BIAS);
+    int* lists = reinterpret_cast<int*>(sm + OFF_LIST);
+    int* nvalids = reinterpret_cast<int*>(sm + OFF_NVALID);
+    float* biases = reinterpret_cast<float*>(sm + OFF_BIAS);
     uint32_t* selbits = reinterpret_cast<uint32_t*>(sm + OFF_SEL);
     uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     const uint32_t bar0 = base + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
-    const int qb = blockIdx.x;      // query block
     const int bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int J = prm.J, P = prm.P, Jr = J - P;
-    const int n_q = prm.block_sizes[qb];
-    const bool dense_row = qb < P;
-    if (n_q <= 0) return;  // an empty block has no query rows
 
-    // ---- prologue: barriers, TMEM, the key-tile list
+    // the two query blocks of this CTA (an empty or missing one is dropped)
+    int qblk[2] = {2 * (int)blockIdx.x, 2 * (int)blockIdx.x + 1};
+    int nq[2];
+    nq[0] = prm.block_sizes[qblk[0]];
+    nq[1] = qblk[1] < J ? prm.block_sizes[qblk[1]] : 0;
+    if (nq[0] <= 0) { qblk[0] = qblk[1]; nq[0] = nq[1]; nq[1] = 0; }
+    if (nq[0] <= 0) return;  // no query rows at all
+    const bool two = nq[1] > 0;
+    const int nX = two ? 2 : 1;
+
+    // ---- prologue: barriers, TMEM, the key-tile lists
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(BAR_Q), 1);
-        for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(bar(BAR_KF + s), 1);
-            ptx::mbar_init(bar(BAR_KE + s), 1);
-            ptx::mbar_init(bar(BAR_VF + s), 1);
-            ptx::mbar_init(bar(BAR_VE + s), 1);
-            ptx::mbar_init(bar(BAR_SF + s), 1);
-            ptx::mbar_init(bar(BAR_PF + s), kBM);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar(BAR_FULL + s), 1);
+            ptx::mbar_init(bar(BAR_EMPTY + s), 1);
         }
-        ptx::mbar_init(bar(BAR_OD), 1);
+        for (int x = 0; x < 2; ++x) {
+            ptx::mbar_init(bar(BAR_SF + x), 1);
+            ptx::mbar_init(bar(BAR_PF + x), kBM);
+            ptx::mbar_init(bar(BAR_OF + x), 1);
+        }
         ptx::mbar_init(bar(BAR_DRAIN), 1);
-        ptx::mbar_init(bar(BAR_OF), 1);
         ptx::fence_mbar_init();
         misc[1] = 0;
     }
@@ -135,194 +178,245 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_alloc(base + OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
-    if (threadIdx.x < 32) selbits[threadIdx.x] = 0u;
-    int n_list;
-    int n_sel = 0;
-    if (dense_row) {
-        n_list = J;
-    } else {
-        n_sel = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
-        n_sel = max(0, min(n_sel, prm.kmax));
-        n_list = P + n_sel;
-    }
-    const int n_virtual = (prm.summary && !dense_row) ? (Jr + kBN - 1) / kBN : 0;
-    n_list += n_virtual;
-    __syncthreads();
-    for (int s = threadIdx.x; s < n_list; s += blockDim.x) {
-        int blk, nv;
-        if (dense_row || s < P) {
-            blk = s;
-            nv = prm.block_sizes[blk];
-        } else if (s < P + n_sel) {
-            const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
-            if (jr < 0 || jr >= Jr) {
-                raise_status(prm.status, BSA_ERR_INDEX);
-                blk = P > 0 ? 0 : qb;
-                nv = 0;  // contributes nothing
-            } else {
-                blk = P + jr;
-                nv = prm.block_sizes[blk];
-                if (prm.summary) atomicOr(&selbits[jr >> 5], 1u << (jr & 31));
-            }
+    if (threadIdx.x < 64) selbits[threadIdx.x] = 0u;
+    int nlist[2] = {0, 0}, nsel[2] = {0, 0};
+    for (int x = 0; x < nX; ++x) {
+        const int qb = qblk[x];
+        if (qb < P) {
+            nlist[x] = J;
         } else {
-            const int t = s - (P + n_sel);
-            blk = -(t + 1);
-            nv = min(kBN, Jr - t * kBN);
+            const int ns = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
+            nsel[x] = max(0, min(ns, prm.kmax));
+            nlist[x] = P + nsel[x] + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
         }
-        list[s] = blk;
-        nvalid[s] = nv;
+    }
+    const int n = max(nlist[0], nlist[1]);
+    __syncthreads();
+    for (int x = 0; x < nX; ++x) {
+        const int qb = qblk[x];
+        const bool dense_row = qb < P;
+        int* list = lists + x * kMaxList;
+        int* nvalid = nvalids + x * kMaxList;
+        for (int s = threadIdx.x; s < n; s += blockDim.x) {
+            int blk, nv;
+            if (s >= nlist[x]) {
+                blk = P > 0 ? 0 : qb;  // padding round: any real tile, fully masked
+                nv = 0;
+            } else if (dense_row || s < P) {
+                blk = s;
+                nv = prm.block_sizes[blk];
+            } else if (s < P + nsel[x]) {
+                const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
+                if (jr < 0 || jr >= Jr) {
+                    raise_status(prm.status, BSA_ERR_INDEX);
+                    blk = P > 0 ? 0 : qb;
+                    nv = 0;  // contributes nothing
+                } else {
+                    blk = P + jr;
+                    nv = prm.block_sizes[blk];
+                    if (prm.summary) atomicOr(&selbits[x * 32 + (jr >> 5)], 1u << (jr & 31));
+                }
+            } else {
+                const int t = s - (P + nsel[x]);
+                blk = -(t + 1);
+                nv = min(kBN, Jr - t * kBN);
+            }
+            list[s] = blk;
+            nvalid[s] = nv;
+        }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < n_virtual * kBN; idx += blockDim.x) {
-        const int jr = idx;  // tile idx / kBN, key idx % kBN
-        float b = -CUDART_INF_F;
-        if (jr < Jr && !((selbits[jr >> 5] >> (jr & 31)) & 1u)) {
-            const int n = prm.block_sizes[P + jr];
-            if (n > 0) b = log2f((float)n);
+    if (prm.summary) {
+        const int nvirt = (Jr + kBN - 1) / kBN;
+        for (int x = 0; x < nX; ++x) {
+            for (int jr = threadIdx.x; jr < nvirt * kBN; jr += blockDim.x) {
+                float b = -CUDART_INF_F;
+                if (jr < Jr && !((selbits[x * 32 + (jr >> 5)] >> (jr & 31)) & 1u)) {
+                    const int nb = prm.block_sizes[P + jr];
+                    if (nb > 0) b = log2f((float)nb);
+                }
+                biases[x * kMaxVirtual * kBN + jr] = b;
+            }
         }
-        bias[idx] = b;
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
+    const int n_entries = two ? 4 * n : 2 * n;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
-        const int32_t* qrows = prm.index_map + (long long)qb * kBM;
         const long long head_row = (long long)bh * prm.N;
-        int rq[4];
-        for (int e = 0; e < 4; ++e) {
-            const int r = 4 * lane + e;
-            int tok = qrows[r < n_q ? r : 0];
-            if (tok < 0 || tok >= prm.N) { raise_status(prm.status, BSA_ERR_INDEX); tok = 0; }
-            rq[e] = (int)(head_row + tok);
-        }
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
+        const int q0tok = prm.index_map[(long long)qblk[0] * kBM];  // a valid row: pads point here
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)nX * kTileBytes);
         __syncwarp();
-        ptx::tma_gather4(base + OFF_Q + 4 * lane * 128, &tm_q, 0, rq[0], rq[1], rq[2], rq[3], bar(BAR_Q));
-        ptx::tma_gather4(base + OFF_Q + kHalfBytes + 4 * lane * 128, &tm_q, 64, rq[0], rq[1], rq[2], rq[3],
-                         bar(BAR_Q));
-        int issued = 0;
-        for (int s = 0; s < n_list; ++s) {
-            const int st = s & 1;
-            const uint32_t ph = (s >> 1) & 1;
-            const int blk = list[s];
-            int rows[4];
-            const CUtensorMap* mk = &tm_k;
-            const CUtensorMap* mv = &tm_v;
-            if (blk >= 0) {
-                const int32_t* krows = prm.index_map + (long long)blk * kBN;
-                const int nv = nvalid[s];
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 4 * lane + e;
-                    int tok = nv > 0 ? krows[r < nv ? r : 0] : qrows[0];
-                    if (tok < 0 || tok >= prm.N) { raise_status(prm.status, BSA_ERR_INDEX); tok = 0; }
-                    rows[e] = (int)(head_row + tok);
+        for (int x = 0; x < nX; ++x) {
+            const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)qblk[x] * kBM + 4 * lane);
+            const int tk[4] = {t4.x, t4.y, t4.z, t4.w};
+            int rq[4];
+            for (int e = 0; e < 4; ++e) {
+                const int r = 4 * lane + e;
+                int tok = tk[e];
+                if (r < nq[x] && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
+                if (tok < 0 || tok >= prm.N) tok = q0tok;
+                rq[e] = (int)(head_row + tok);
+            }
+            const uint32_t qdst = base + OFF_Q + x * kTileBytes + 4 * lane * 128;
+            ptx::tma_gather4(qdst, &tm_q, 0, rq[0], rq[1], rq[2], rq[3], bar(BAR_Q));
+            ptx::tma_gather4(qdst + kHalfBytes, &tm_q, 64, rq[0], rq[1], rq[2], rq[3], bar(BAR_Q));
+        }
+        // row ids of entry e (4 per lane): real tiles through the index map,
+        // virtual (summary) tiles are rows of the block-mean tensors
+        auto fetch_rows = [&](int e, int* rows, bool& virt) -> bool {
+            int X, j;
+            bool isV;
+            decode_entry(e, n, two, X, j, isV);
+            const int blk = lists[X * kMaxList + j];
+            const int nv = nvalids[X * kMaxList + j];
+            virt = blk < 0;
+            if (!virt) {
+                const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)blk * kBN + 4 * lane);
+                rows[0] = t4.x;
+                rows[1] = t4.y;
+                rows[2] = t4.z;
+                rows[3] = t4.w;
+                for (int u = 0; u < 4; ++u) {
+                    const int r = 4 * lane + u;
+                    int tok = rows[u];
+                    if (r < nv && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
+                    if (r >= nv || tok < 0 || tok >= prm.N) tok = q0tok;
+                    rows[u] = (int)(head_row + tok);
                 }
             } else {
                 const int t = -blk - 1;
-                for (int e = 0; e < 4; ++e) {
-                    const int jr = min(t * kBN + 4 * lane + e, Jr - 1);
-                    rows[e] = (int)((long long)bh * J + P + jr);
+                for (int u = 0; u < 4; ++u) {
+                    const int jr = min(t * kBN + 4 * lane + u, Jr - 1);
+                    rows[u] = (int)((long long)bh * J + P + jr);
                 }
-                mk = &tm_kb;
-                mv = &tm_vb;
             }
-            if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_KE + st), ph ^ 1, abort_flag, prm.status))) break;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_KF + st), kTileBytes);
+            return isV;
+        };
+        int cur[4] = {0, 0, 0, 0}, nxt[4] = {0, 0, 0, 0};
+        bool cur_virt = false, nxt_virt = false, cur_v = false, nxt_v = false;
+        int issued = 0;
+        if (n_entries > 0) cur_v = fetch_rows(0, cur, cur_virt);
+        for (int e = 0; e < n_entries; ++e) {
+            if (e + 1 < n_entries) nxt_v = fetch_rows(e + 1, nxt, nxt_virt);
+            const int st = e % kStages;
+            const uint32_t ph = (uint32_t)(e / kStages) & 1u;
+            if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) break;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
             __syncwarp();
-            const uint32_t kdst = base + OFF_K + st * kTileBytes + 4 * lane * 128;
-            ptx::tma_gather4(kdst, mk, 0, rows[0], rows[1], rows[2], rows[3], bar(BAR_KF + st));
-            ptx::tma_gather4(kdst + kHalfBytes, mk, 64, rows[0], rows[1], rows[2], rows[3], bar(BAR_KF + st));
-            if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_VE + st), ph ^ 1, abort_flag, prm.status))) {
-                issued = s * 2 + 1;
-                break;
-            }
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_VF + st), kTileBytes);
-            __syncwarp();
-            const uint32_t vdst = base + OFF_V + st * kTileBytes + 4 * lane * 128;
-            ptx::tma_gather4(vdst, mv, 0, rows[0], rows[1], rows[2], rows[3], bar(BAR_VF + st));
-            ptx::tma_gather4(vdst + kHalfBytes, mv, 64, rows[0], rows[1], rows[2], rows[3], bar(BAR_VF + st));
-            issued = s * 2 + 2;
+            const CUtensorMap* map = cur_virt ? (cur_v ? &tm_vb : &tm_kb) : (cur_v ? &tm_v : &tm_k);
+            const uint32_t dst = base + OFF_RING + st * kTileBytes + 4 * lane * 128;
+            ptx::tma_gather4(dst, map, 0, cur[0], cur[1], cur[2], cur[3], bar(BAR_FULL + st));
+            ptx::tma_gather4(dst + kHalfBytes, map, 64, cur[0], cur[1], cur[2], cur[3], bar(BAR_FULL + st));
+            issued = e + 1;
+            for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+            cur_virt = nxt_virt;
+            cur_v = nxt_v;
         }
         if (*abort_flag) {
-            // drain: wait (bounded) for the last loads of each stage to land
+            // drain: wait (bounded) for this warp's copies still in flight
             const uint64_t t0 = ptx::globaltimer();
-            for (int u = max(0, issued - 4); u < issued; ++u) {
-                const int s = u >> 1;
-                const uint32_t b = (u & 1) ? bar(BAR_VF + (s & 1)) : bar(BAR_KF + (s & 1));
-                while (!ptx::mbar_try_wait(b, (s >> 1) & 1) && ptx::globaltimer() - t0 < kWaitNs) {}
-            }
+            for (int e = max(0, issued - kStages); e < issued; ++e)
+                while (!ptx::mbar_try_wait(bar(BAR_FULL + e % kStages), (uint32_t)(e / kStages) & 1u) &&
+                       ptx::globaltimer() - t0 < kWaitNs) {
+                }
             while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_list > 0) {
+        if (lane == 0 && n > 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kBM, kHD, true);
-            const uint32_t tS0 = tmem, tO = tmem + 256;
+            int ec = 0;  // ring entries consumed
             bool ok = wait_bar(bar(BAR_Q), 0, abort_flag, prm.status);
-            auto issue_s = [&](int s) -> bool {
-                const int st = s & 1;
-                if (!wait_bar(bar(BAR_KF + st), (s >> 1) & 1, abort_flag, prm.status)) return false;
+            auto take = [&](uint32_t& addr) -> bool {
+                const int st = ec % kStages;
+                if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(ec / kStages) & 1u, abort_flag, prm.status))
+                    return false;
                 ptx::tc_fence_after();
-                const uint32_t qa = base + OFF_Q, ka = base + OFF_K + st * kTileBytes;
-                const uint32_t dS = tS0 + (uint32_t)(s & 1) * 128;
+                addr = base + OFF_RING + st * kTileBytes;
+                return true;
+            };
+            auto release = [&]() {
+                ptx::mma_commit(bar(BAR_EMPTY + ec % kStages));
+                ++ec;
+            };
+            auto issue_s = [&](int x) -> bool {
+                uint32_t ka;
+                if (!take(ka)) return false;
+                const uint32_t qa = base + OFF_Q + x * kTileBytes;
+                const uint32_t dS = tmem + (uint32_t)x * 256;
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     ptx::mma_ss(dS, ptx::smem_desc(qa + off, 16, 1024), ptx::smem_desc(ka + off, 16, 1024), idS,
                                 kk > 0);
                 }
-                ptx::mma_commit(bar(BAR_SF + (s & 1)));
-                ptx::mma_commit(bar(BAR_KE + st));
+                ptx::mma_commit(bar(BAR_SF + x));
+                release();
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int s = 0; ok && s < n_list; ++s) {
-                if (s + 1 < n_list && !(ok = issue_s(s + 1))) break;
-                const int b = s & 1;
-                if (!(ok = wait_bar(bar(BAR_PF + b), (s >> 1) & 1, abort_flag, prm.status))) break;
-                if (!(ok = wait_bar(bar(BAR_VF + b), (s >> 1) & 1, abort_flag, prm.status))) break;
-                ptx::tc_fence_after();
-                const uint32_t va = base + OFF_V + b * kTileBytes;
-                const uint32_t aP = tS0 + (uint32_t)b * 128;
+            auto issue_pv = [&](int x, int j) -> bool {
+                if (!wait_bar(bar(BAR_PF + x), (uint32_t)j & 1u, abort_flag, prm.status)) return false;
+                uint32_t va;
+                if (!take(va)) return false;
+                const uint32_t aP = tmem + (uint32_t)x * 256;
+                const uint32_t dO = aP + 128;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
-                    // V advances by two 8-row groups of 1024 B; the second 64-column
-                    // half of V is one leading-dimension step (16 KB) away.
-                    ptx::mma_ts(tO, aP + kk * 8, ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
-                                (s > 0 || kk > 0) ? 1u : 0u);
+                    // V advances by two 8-row groups of 1024 B; the second
+                    // 64-column half of V is one leading-dimension step (16 KB) away.
+                    ptx::mma_ts(dO, aP + kk * 8, ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
+                                (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                ptx::mma_commit(bar(BAR_OD));
-                ptx::mma_commit(bar(BAR_VE + b));
-                if (s + 1 == n_list) ptx::mma_commit(bar(BAR_OF));
+                release();
+                if (j == n - 1) ptx::mma_commit(bar(BAR_OF + x));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && two) ok = issue_s(1);
+            for (int j = 0; ok && j < n; ++j) {
+                for (int x = 0; ok && x < nX; ++x) {
+                    ok = issue_pv(x, j);
+                    if (ok && j + 1 < n) ok = issue_s(x);
+                }
             }
-            // make sure nothing this thread issued is still running before TMEM is freed
+            // nothing this thread issued may still run when TMEM is freed
             ptx::mma_commit(bar(BAR_DRAIN));
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(bar(BAR_DRAIN), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax + epilogue
-        const int row = threadIdx.x - 128;
-        const uint32_t lane_off = (uint32_t)(32 * (warp - 4)) << 16;
-        const uint32_t tS0 = tmem + lane_off, tO = tmem + lane_off + 256;
+      }
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+      if ((warp - 4) / 4 < nX) {
+        // ------------------------------------------------------------ softmax + epilogue of block X
+        const int X = (warp - 4) / 4;
+        const int row = threadIdx.x - 128 - X * 128;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)X * 256;
+        const uint32_t tO = tS + 128;
+        const int* list = lists + X * kMaxList;
+        const int* nvalid = nvalids + X * kMaxList;
+        const float* bias = biases + X * kMaxVirtual * kBN;
         float m_ref = -CUDART_INF_F, l = 0.f;
         bool ok = true;
         uint32_t r[32];
         float x[kBN];
-        for (int s = 0; s < n_list; ++s) {
-            const int b = s & 1;
-            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + b), (s >> 1) & 1, abort_flag, prm.status));
+        for (int s = 0; s < n; ++s) {
+            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + X), (uint32_t)s & 1u, abort_flag, prm.status));
             if (!ok) break;
             ptx::tc_fence_after();
-            const uint32_t tS = tS0 + (uint32_t)b * 128;
             {
                 uint32_t* xr = reinterpret_cast<uint32_t*>(x);
                 ptx::tmem_ld32(tS + 0, xr + 0);
@@ -336,7 +430,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float mxp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
-            if (blk >= 0) {
+            if (blk >= 0 || nv == 0) {
                 if (nv >= kBN) {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) {
@@ -367,10 +461,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (need) m_ref = m_new;
                 l *= alpha;
                 if (s > 0) {
-                    // O holds P_0..P_{s-1} V: wait for PV_{s-1} before rescaling it
-                    ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD), (s - 1) & 1, abort_flag, prm.status));
-                    if (!ok) break;
-                    ptx::tc_fence_after();
+                    // S(s) was issued after PV(s-1), so its completion means O
+                    // already holds P_0..P_{s-1} V: rescale it in place.
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         ptx::tmem_ld32(tO + c * 32, r);
@@ -391,8 +483,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
                 sp[c & 7] += x[c];
             }
-            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            l += sum;
+            l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -401,24 +492,23 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BAR_PF + b));
+            ptx::mbar_arrive(bar(BAR_PF + X));
         }
         // epilogue
-        // the last P V: its own barrier (the OD parity alone could be two phases behind here)
-        if (ok && n_list > 0) ok = wait_bar(bar(BAR_OF), 0, abort_flag, prm.status);
+        if (ok && n > 0) ok = wait_bar(bar(BAR_OF + X), 0, abort_flag, prm.status);
         ok = __all_sync(0xffffffffu, ok);
         ptx::tc_fence_after();
-        const bool write = ok && row < n_q;
-        int tok = 0;
+        const bool write = ok && row < nq[X];
+        int tok = -1;
         if (write) {
-            tok = prm.index_map[(long long)qb * kBM + row];
+            tok = prm.index_map[(long long)qblk[X] * kBM + row];
             if (tok < 0 || tok >= prm.N) tok = -1;
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            if (ok && n_list > 0) {
+            if (ok && n > 0) {
                 ptx::tmem_ld32(tO + c * 32, r);
                 ptx::tmem_wait_ld();
             } else {
@@ -440,6 +530,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (write && tok >= 0 && prm.lse)
             prm.lse[(long long)bh * prm.N + tok] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
+      }
     }
 
     ptx::tc_fence_before();
@@ -479,6 +570,20 @@ static bool make_row_map(CUtensorMap* m, const void* ptr, long long rows) {
     return r == CUDA_SUCCESS;
 }
 
+// The register split assumes the launch reserves kRegsLaunch registers per
+// thread; refuse the tensor-core path otherwise (setmaxnreg.inc would wait).
+static bool register_split_fits() {
+    static int checked = 0;  // 0 unknown, 1 fits, -1 does not
+    if (!checked) {
+        cudaFuncAttributes a;
+        checked = (cudaFuncGetAttributes(&a, bsa_fwd_tc_kernel) == cudaSuccess &&
+                   a.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh)
+                      ? 1
+                      : -1;
+    }
+    return checked == 1;
+}
+
 }  // namespace tc
 
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
@@ -491,8 +596,9 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     const int nvirt = summary ? (Jr + tc::kBN - 1) / tc::kBN : 0;
     const long long longest = P > 0 ? std::max<long long>(J, (long long)P + kmax + nvirt) : (long long)kmax + nvirt;
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
-    if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out) & 15) return BSA_OK;
+    if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
+    if (!tc::register_split_fits()) return BSA_OK;
     CUtensorMap mq, mk, mv, mkb, mvb;
     const long long rows = (long long)BH * N;
     if (!tc::make_row_map(&mq, q, rows) || !tc::make_row_map(&mk, k, rows) || !tc::make_row_map(&mv, v, rows))
@@ -522,7 +628,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     cudaError_t e = cudaFuncSetAttribute(tc::bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));
-    dim3 grid(J, BH);
+    dim3 grid((J + 1) / 2, BH);
     tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mkb, mvb, prm);
     return check_launch("bsa_fwd_tc_kernel");
 }
