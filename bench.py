@@ -211,6 +211,7 @@ def gpu_arm(args):
         q, kk, v = synthetic.video_qkv(w["B"], w["heads"], T, H, W, D, w["seed"] + 1000 * rank,
                                        torch.bfloat16, device=dev, field=True)
     geom = pipeline.Geometry(T, H, W, *w["block"], M=M)
+    geo = geom.geometry
     J = geom.num_blocks
     scale = D ** -0.5
     im = torch.empty((J, M), dtype=torch.int32, device=dev)
@@ -231,7 +232,7 @@ def gpu_arm(args):
         if ev: ev[2].record(stream)
         bsa.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, scale, k, q2k, q2n)
         if ev: ev[3].record(stream)
-        bsa.bsa_fwd_qouter(q, kk, v, BH, N, D, im, bs, J, M, 0, q2k, q2n, k, scale, out, lse)
+        bsa.bsa_fwd_qouter(q, kk, v, BH, N, D, im, bs, J, M, 0, geo, q2k, q2n, k, scale, out, lse)
         if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):
@@ -282,7 +283,7 @@ def gpu_arm(args):
         bsa.bsa_tile_map(T, H, W, *w["block"], 0, None, M, im, bs)
         bsa.bsa_pool_blocks(dq, dk, None, BH, N, D, im, bs, J, M, qbar, kbar)
         bsa.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, scale, k, q2k, q2n)
-        bsa.bsa_fwd_qouter(dq, dk, dv, BH, N, D, im, bs, J, M, 0, q2k, q2n, k, scale, out, lse)
+        bsa.bsa_fwd_qouter(dq, dk, dv, BH, N, D, im, bs, J, M, 0, geo, q2k, q2n, k, scale, out, lse)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):

@@ -47,14 +47,14 @@ _SIGS = {
     "bsa_budget": (I, [I, ctypes.c_double]),
     "bsa_pool_blocks": (I, [P, P, P, I, I, I, I, P, P, I, I, P, P, P, P, P, P]),
     "bsa_route_topk": (I, [P, P, I, I, I, I64, I, F, I, P, P, P]),
-    "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, I, F, P, P, P]),
+    "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, I, F, P, P, P]),
     "bsa_fwd_qouter_tokens": (I, [P, P, P, I, I, I, I, I, I, P, P, I, I, I, F, P, P, P]),
     "bsa_reverse_index_workspace": (SZ, [I, I, I, I]),
     "bsa_max_chunks": (I, [I, I, I, I, I, I]),
     "bsa_build_reverse_index": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P, SZ, P]),
     "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P]),
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
-    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, I, P, P, F, P, P, P]),
+    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, I, P, P, F, P, P, P]),
     "bsa_set_force_simt": (None, [I]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -67,6 +67,16 @@ EXPORTED = tuple(_SIGS)
 
 def _ptr(t):
     return None if t is None else t.data_ptr()
+
+
+def _geometry(geometry):
+    """Host int32[8] {T, H, W, bT, bH, bW, n_prefix, permuted} or None."""
+    if geometry is None:
+        return None
+    vals = [int(x) for x in geometry]
+    if len(vals) != 8:
+        raise ValueError("geometry needs 8 integers")
+    return (ctypes.c_int32 * 8)(*vals)
 
 
 def _dtype(t):
@@ -130,17 +140,17 @@ def bsa_route_topk(qbar, kbar, BH, J, D, head_stride, k, scale, kmax, q2k_idx, q
                                _ptr(q2k_idx), _ptr(q2k_num), _stream(stream)))
 
 
-def bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, q2k_idx, q2k_num,
-                   kmax, scale, out, lse=None, stream=None):
+def bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,
+                   q2k_num, kmax, scale, out, lse=None, stream=None):
     _check(_lib.bsa_fwd_qouter(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
-                               _ptr(block_sizes), J, M, prefix_blocks, _ptr(q2k_idx), _ptr(q2k_num),
-                               kmax, scale, _ptr(out), _ptr(lse), _stream(stream)))
+                               _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(q2k_idx),
+                               _ptr(q2k_num), kmax, scale, _ptr(out), _ptr(lse), _stream(stream)))
 
 
-def bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, q2k_idx, q2k_num,
-                    kmax, kbar_lp, vbar_lp, scale, out, lse=None, stream=None):
+def bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,
+                    q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse=None, stream=None):
     _check(_lib.bsa_fwd_summary(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
-                                _ptr(block_sizes), J, M, prefix_blocks, _ptr(q2k_idx),
+                                _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(q2k_idx),
                                 _ptr(q2k_num), kmax, _ptr(kbar_lp), _ptr(vbar_lp), scale, _ptr(out),
                                 _ptr(lse), _stream(stream)))
 

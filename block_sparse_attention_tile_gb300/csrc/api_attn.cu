@@ -14,10 +14,22 @@ bsa_status simt_token_attention(const void* q, const void* k, const void* v, bsa
                                 int S, int BS, int causal, float scale, void* out, float* lse,
                                 cudaStream_t st);
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
-                              const int32_t* im, const int32_t* bs, int J, int P,
+                              const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
                               const int32_t* idx, const int32_t* num, int kmax, const void* kb,
                               const void* vb, float scale, void* out, float* lse, cudaStream_t st,
                               bool* handled);
+
+// The optional geometry must describe the tiling behind index_map.
+static bsa_status check_geometry(const int32_t* g, int N, int J, int M, int P) {
+    if (!g) return BSA_OK;
+    const int T = g[0], H = g[1], W = g[2], bT = g[3], bH = g[4], bW = g[5], n_prefix = g[6], perm = g[7];
+    BSA_REQUIRE(T > 0 && H > 0 && W > 0 && n_prefix >= 0 && (perm == 0 || perm == 1),
+                "geometry: invalid values");
+    BSA_REQUIRE((long long)T * H * W + n_prefix == N, "geometry: T*H*W + n_prefix != N");
+    BSA_REQUIRE(bsa_tile_count(T, H, W, bT, bH, bW, n_prefix, perm, M) == J, "geometry: block count != J");
+    BSA_REQUIRE((n_prefix + M - 1) / M == P, "geometry: prefix blocks != prefix_blocks");
+    return BSA_OK;
+}
 
 static bsa_status check_block_args(const void* q, const void* k, const void* v, bsa_dtype dtype,
                                    int BH, int N, int D, const int32_t* im, const int32_t* bs, int J,
@@ -41,16 +53,19 @@ extern "C" {
 
 bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                           int N, int D, const int32_t* index_map, const int32_t* block_sizes, int J,
-                          int M, int prefix_blocks, const int32_t* q2k_idx, const int32_t* q2k_num,
-                          int kmax, float scale, void* out, float* lse, void* stream) {
+                          int M, int prefix_blocks, const int32_t* geometry, const int32_t* q2k_idx,
+                          const int32_t* q2k_num, int kmax, float scale, void* out, float* lse,
+                          void* stream) {
     bsa_status rc = check_block_args(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
                                      prefix_blocks, q2k_idx, q2k_num, kmax, out);
+    if (rc != BSA_OK) return rc;
+    rc = check_geometry(geometry, N, J, M, prefix_blocks);
     if (rc != BSA_OK) return rc;
     cudaStream_t st = as_stream(stream);
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
-        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, q2k_idx,
-                                q2k_num, kmax, nullptr, nullptr, scale, out, lse, st, &handled);
+        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry,
+                                q2k_idx, q2k_num, kmax, nullptr, nullptr, scale, out, lse, st, &handled);
         if (handled) return rc;
     }
     return simt_block_attention(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
@@ -60,19 +75,21 @@ bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype
 
 bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                            int N, int D, const int32_t* index_map, const int32_t* block_sizes, int J,
-                           int M, int prefix_blocks, const int32_t* q2k_idx, const int32_t* q2k_num,
-                           int kmax, const void* kbar_lp, const void* vbar_lp, float scale,
-                           void* out, float* lse, void* stream) {
+                           int M, int prefix_blocks, const int32_t* geometry, const int32_t* q2k_idx,
+                           const int32_t* q2k_num, int kmax, const void* kbar_lp, const void* vbar_lp,
+                           float scale, void* out, float* lse, void* stream) {
     bsa_status rc = check_block_args(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
                                      prefix_blocks, q2k_idx, q2k_num, kmax, out);
+    if (rc != BSA_OK) return rc;
+    rc = check_geometry(geometry, N, J, M, prefix_blocks);
     if (rc != BSA_OK) return rc;
     BSA_REQUIRE(kbar_lp && vbar_lp, "summary: kbar_lp / vbar_lp required");
     BSA_REQUIRE(J - prefix_blocks <= 1024, "summary: at most 1024 routed blocks");
     cudaStream_t st = as_stream(stream);
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
-        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, q2k_idx,
-                                q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, st, &handled);
+        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry,
+                                q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, st, &handled);
         if (handled) return rc;
     }
     return simt_block_attention(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,

@@ -13,12 +13,18 @@
 // Design (ours, for sm_103a).  One CTA per (head, pair of query blocks A, B),
 // 12 warps.  Each query block keeps its own key-tile list; the shorter list
 // is padded with fully masked rounds (the VSA page's dual-Q scheduling, §6.3).
-//   warp 0      producer: TMA tile::gather4 loads straight from the
-//               token-indexed BHSD tensors (the index map performs the 3-D
-//               gather or the permutation; no pack pass) into 128-byte
-//               swizzled K-major tiles; one 4-stage ring whose entries follow
-//               the MMA consumption order K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ...;
-//               the next entry's row ids are fetched while it waits.
+//   warp 0      producer: TMA loads straight from the BHSD tensors into
+//               128-byte swizzled K-major tiles, no pack pass: a (bT,bH,bW)
+//               window is ONE box of a 5-D (D, W, H, T, head) tensor map per
+//               64-column half (zero-filled past T, so the valid rows come
+//               first as in the tile map), a dense-prefix block or a summary
+//               tile is one 128-row box, and any other block (a permutation,
+//               a window ragged in H or W) is gathered four rows per
+//               tile::gather4 through the index map.  TMA costs about the same
+//               per operation whatever its size, so the boxes are ~8x faster
+//               than gathering.  One 4-stage ring whose entries follow the MMA
+//               consumption order K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ...; the
+//               next entry's row ids are fetched while it waits.
 //   warp 1      TMEM owner and single-thread MMA issuer:
 //               S_A0, S_B0, then per round j: PV_A(j), S_A(j+1), PV_B(j),
 //               S_B(j+1).  While softmax A works on S_A(j) the tensor core
@@ -86,7 +92,43 @@ struct Params {
     int N, J, P, kmax;
     float scale_log2;
     int summary;
+    // tiling, when known: prefix blocks are contiguous rows; a video window
+    // that is not ragged in H or W is one box of the 5-D (D, W, H, T, head) map
+    int geo, window;  // geometry given; 5-D window boxes usable
+    int T, H, W, bT, bH, bW, nH, nW;
 };
+
+// Where a 128-row tile comes from: gathered rows (mode 0), a box of 128
+// consecutive rows of a 2-D map (mode 1, origin row c1) or one box of the
+// 5-D window map (mode 2, origin (c1, c2, c3, c4) = (x, y, t, head)).
+struct TileSrc {
+    int mode, c1, c2, c3, c4;
+};
+
+__device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int bh) {
+    TileSrc s{0, 0, 0, 0, 0};
+    if (blk < 0) {  // summary tile: rows of the block-mean tensor
+        s.mode = 1;
+        s.c1 = bh * prm.J + prm.P + (-blk - 1) * 128;
+        return s;
+    }
+    if (!prm.geo) return s;
+    if (blk < prm.P) {  // dense prefix: contiguous tokens
+        s.mode = 1;
+        s.c1 = bh * prm.N + blk * 128;
+        return s;
+    }
+    if (!prm.window) return s;
+    const int jv = blk - prm.P;
+    const int jw = jv % prm.nW, jh = (jv / prm.nW) % prm.nH, jt = jv / (prm.nW * prm.nH);
+    if (jh * prm.bH + prm.bH > prm.H || jw * prm.bW + prm.bW > prm.W) return s;  // ragged in H or W
+    s.mode = 2;  // rows land t-major, then y, then x: the tile map's member order
+    s.c1 = jw * prm.bW;
+    s.c2 = jh * prm.bH;
+    s.c3 = jt * prm.bT;
+    s.c4 = bh;
+    return s;
+}
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -129,7 +171,10 @@ __device__ __forceinline__ void decode_entry(int e, int n, bool two, int& X, int
 
 __global__ void __launch_bounds__(kThreads, 1)
 bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qr,
+                  const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr,
+                  const __grid_constant__ CUtensorMap tm_q5, const __grid_constant__ CUtensorMap tm_k5,
+                  const __grid_constant__ CUtensorMap tm_v5, const __grid_constant__ CUtensorMap tm_kb,
                   const __grid_constant__ CUtensorMap tm_vb, const Params prm) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -254,73 +299,79 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::prefetch_tmap(&tm_v);
         const long long head_row = (long long)bh * prm.N;
         const int q0tok = prm.index_map[(long long)qblk[0] * kBM];  // a valid row: pads point here
+        // issue one 32 KB tile (two 64-column halves) from source `src`
+        auto issue_tile = [&](uint32_t dst, const TileSrc& src, const int* rows, const CUtensorMap* mg,
+                              const CUtensorMap* mr, const CUtensorMap* m5, uint32_t b) {
+            if (src.mode == 0) {
+                const uint32_t d = dst + 4 * lane * 128;
+                ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], b);
+                ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], b);
+            } else if (lane == 0) {
+                if (src.mode == 1) {
+                    ptx::tma_load_2d(dst, mr, 0, src.c1, b);
+                    ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.c1, b);
+                } else {
+                    ptx::tma_load_5d(dst, m5, 0, src.c1, src.c2, src.c3, src.c4, b);
+                    ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.c1, src.c2, src.c3, src.c4, b);
+                }
+            }
+        };
+        // gathered rows of a real block (4 per lane); slots past n_j point at a valid row
+        auto gather_rows = [&](int blk, int nv, int* rows) {
+            const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)blk * kBN + 4 * lane);
+            rows[0] = t4.x;
+            rows[1] = t4.y;
+            rows[2] = t4.z;
+            rows[3] = t4.w;
+            for (int u = 0; u < 4; ++u) {
+                const int r = 4 * lane + u;
+                int tok = rows[u];
+                if (r < nv && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
+                if (r >= nv || tok < 0 || tok >= prm.N) tok = q0tok;
+                rows[u] = (int)(head_row + tok);
+            }
+        };
         if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)nX * kTileBytes);
         __syncwarp();
         for (int x = 0; x < nX; ++x) {
-            const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)qblk[x] * kBM + 4 * lane);
-            const int tk[4] = {t4.x, t4.y, t4.z, t4.w};
-            int rq[4];
-            for (int e = 0; e < 4; ++e) {
-                const int r = 4 * lane + e;
-                int tok = tk[e];
-                if (r < nq[x] && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
-                if (tok < 0 || tok >= prm.N) tok = q0tok;
-                rq[e] = (int)(head_row + tok);
-            }
-            const uint32_t qdst = base + OFF_Q + x * kTileBytes + 4 * lane * 128;
-            ptx::tma_gather4(qdst, &tm_q, 0, rq[0], rq[1], rq[2], rq[3], bar(BAR_Q));
-            ptx::tma_gather4(qdst + kHalfBytes, &tm_q, 64, rq[0], rq[1], rq[2], rq[3], bar(BAR_Q));
+            const TileSrc src = tile_source(qblk[x], prm, bh);
+            int rq[4] = {0, 0, 0, 0};
+            if (src.mode == 0) gather_rows(qblk[x], nq[x], rq);
+            issue_tile(base + OFF_Q + x * kTileBytes, src, rq, &tm_q, &tm_qr, &tm_q5, bar(BAR_Q));
         }
-        // row ids of entry e (4 per lane): real tiles through the index map,
-        // virtual (summary) tiles are rows of the block-mean tensors
-        auto fetch_rows = [&](int e, int* rows, bool& virt) -> bool {
-            int X, j;
-            bool isV;
-            decode_entry(e, n, two, X, j, isV);
-            const int blk = lists[X * kMaxList + j];
-            const int nv = nvalids[X * kMaxList + j];
-            virt = blk < 0;
-            if (!virt) {
-                const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)blk * kBN + 4 * lane);
-                rows[0] = t4.x;
-                rows[1] = t4.y;
-                rows[2] = t4.z;
-                rows[3] = t4.w;
-                for (int u = 0; u < 4; ++u) {
-                    const int r = 4 * lane + u;
-                    int tok = rows[u];
-                    if (r < nv && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
-                    if (r >= nv || tok < 0 || tok >= prm.N) tok = q0tok;
-                    rows[u] = (int)(head_row + tok);
-                }
-            } else {
-                const int t = -blk - 1;
-                for (int u = 0; u < 4; ++u) {
-                    const int jr = min(t * kBN + 4 * lane + u, Jr - 1);
-                    rows[u] = (int)((long long)bh * J + P + jr);
-                }
-            }
-            return isV;
+        // the source of ring entry e; gathered row ids are loaded one entry ahead
+        struct Next {
+            TileSrc src;
+            int rows[4];
+            bool isV, virt;
         };
-        int cur[4] = {0, 0, 0, 0}, nxt[4] = {0, 0, 0, 0};
-        bool cur_virt = false, nxt_virt = false, cur_v = false, nxt_v = false;
+        auto fetch = [&](int e, Next& nx) {
+            int X, j;
+            decode_entry(e, n, two, X, j, nx.isV);
+            const int blk = lists[X * kMaxList + j];
+            nx.virt = blk < 0;
+            nx.src = tile_source(blk, prm, bh);
+            if (nx.src.mode == 0) gather_rows(blk, nvalids[X * kMaxList + j], nx.rows);
+        };
+        Next cur{}, nxt{};
         int issued = 0;
-        if (n_entries > 0) cur_v = fetch_rows(0, cur, cur_virt);
+        if (n_entries > 0) fetch(0, cur);
         for (int e = 0; e < n_entries; ++e) {
-            if (e + 1 < n_entries) nxt_v = fetch_rows(e + 1, nxt, nxt_virt);
+            if (e + 1 < n_entries) fetch(e + 1, nxt);
             const int st = e % kStages;
             const uint32_t ph = (uint32_t)(e / kStages) & 1u;
             if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) break;
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
             __syncwarp();
-            const CUtensorMap* map = cur_virt ? (cur_v ? &tm_vb : &tm_kb) : (cur_v ? &tm_v : &tm_k);
-            const uint32_t dst = base + OFF_RING + st * kTileBytes + 4 * lane * 128;
-            ptx::tma_gather4(dst, map, 0, cur[0], cur[1], cur[2], cur[3], bar(BAR_FULL + st));
-            ptx::tma_gather4(dst + kHalfBytes, map, 64, cur[0], cur[1], cur[2], cur[3], bar(BAR_FULL + st));
+            const uint32_t dst = base + OFF_RING + st * kTileBytes;
+            if (cur.virt)
+                issue_tile(dst, cur.src, cur.rows, &tm_k, cur.isV ? &tm_vb : &tm_kb, &tm_k5, bar(BAR_FULL + st));
+            else if (cur.isV)
+                issue_tile(dst, cur.src, cur.rows, &tm_v, &tm_vr, &tm_v5, bar(BAR_FULL + st));
+            else
+                issue_tile(dst, cur.src, cur.rows, &tm_k, &tm_kr, &tm_k5, bar(BAR_FULL + st));
             issued = e + 1;
-            for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
-            cur_virt = nxt_virt;
-            cur_v = nxt_v;
+            cur = nxt;
         }
         if (*abort_flag) {
             // drain: wait (bounded) for this warp's copies still in flight
@@ -331,7 +382,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
@@ -556,15 +607,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2-D map over [rows, 128] bf16 with a {64, 1} box (the gather4 form) and 128-byte swizzle.
-static bool make_row_map(CUtensorMap* m, const void* ptr, long long rows) {
+// 2-D map over [rows, 128] bf16, 128-byte swizzle, box {64, box_rows}:
+// box_rows = 1 is the gather4 form, 128 a whole tile half of consecutive rows.
+static bool make_row_map(CUtensorMap* m, const void* ptr, long long rows, int box_rows = 1) {
     auto fn = encode_fn();
     if (!fn || rows <= 0 || rows > (1LL << 31)) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kHD, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kHD * 2};
-    cuuint32_t box[2] = {64, 1};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 5-D map (D, W, H, T, head) over the video part of a BHSD tensor whose box
+// is one (bT, bH, bW) window: 64 columns x bT*bH*bW rows in t, y, x order.
+static bool make_window_map(CUtensorMap* m, const void* video_base, int T, int H, int W, long long BH, int N,
+                            int bT, int bH, int bW) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t row = (cuuint64_t)kHD * 2;
+    cuuint64_t dims[5] = {(cuuint64_t)kHD, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)BH};
+    cuuint64_t strides[4] = {row, row * W, row * W * H, row * (cuuint64_t)N};
+    cuuint32_t box[5] = {64, (cuuint32_t)bW, (cuuint32_t)bH, (cuuint32_t)bT, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(video_base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -587,9 +656,9 @@ static bool register_split_fits() {
 }  // namespace tc
 
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
-                              const int32_t* im, const int32_t* bs, int J, int P, const int32_t* idx,
-                              const int32_t* num, int kmax, const void* kb, const void* vb, float scale,
-                              void* out, float* lse, cudaStream_t st, bool* handled) {
+                              const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
+                              const int32_t* idx, const int32_t* num, int kmax, const void* kb, const void* vb,
+                              float scale, void* out, float* lse, cudaStream_t st, bool* handled) {
     *handled = false;
     const bool summary = kb != nullptr;
     const int Jr = J - P;
@@ -599,19 +668,49 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
     if (!tc::register_split_fits()) return BSA_OK;
-    CUtensorMap mq, mk, mv, mkb, mvb;
+    tc::Params prm{};
+    CUtensorMap mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5, mkb, mvb;
     const long long rows = (long long)BH * N;
-    if (!tc::make_row_map(&mq, q, rows) || !tc::make_row_map(&mk, k, rows) || !tc::make_row_map(&mv, v, rows))
+    if (!tc::make_row_map(&mq, q, rows) || !tc::make_row_map(&mk, k, rows) || !tc::make_row_map(&mv, v, rows) ||
+        !tc::make_row_map(&mqr, q, rows, 128) || !tc::make_row_map(&mkr, k, rows, 128) ||
+        !tc::make_row_map(&mvr, v, rows, 128))
         return BSA_OK;
+    mq5 = mq;
+    mk5 = mk;
+    mv5 = mv;
+    if (geometry) {
+        const int T = geometry[0], H = geometry[1], W = geometry[2], bT = geometry[3], bH = geometry[4],
+                  bW = geometry[5], n_prefix = geometry[6], perm = geometry[7];
+        prm.geo = 1;
+        prm.T = T;
+        prm.H = H;
+        prm.W = W;
+        prm.bT = bT;
+        prm.bH = bH;
+        prm.bW = bW;
+        prm.nH = (H + bH - 1) / bH;
+        prm.nW = (W + bW - 1) / bW;
+        if (!perm && bT * bH * bW == tc::kBN) {
+            const size_t off = (size_t)n_prefix * tc::kHD * 2;
+            if (tc::make_window_map(&mq5, (const char*)q + off, T, H, W, BH, N, bT, bH, bW) &&
+                tc::make_window_map(&mk5, (const char*)k + off, T, H, W, BH, N, bT, bH, bW) &&
+                tc::make_window_map(&mv5, (const char*)v + off, T, H, W, BH, N, bT, bH, bW))
+                prm.window = 1;
+        }
+        if (!prm.window) {
+            mq5 = mq;
+            mk5 = mk;
+            mv5 = mv;
+        }
+    }
     if (summary) {
-        if (!tc::make_row_map(&mkb, kb, (long long)BH * J) || !tc::make_row_map(&mvb, vb, (long long)BH * J))
+        if (!tc::make_row_map(&mkb, kb, (long long)BH * J, 128) || !tc::make_row_map(&mvb, vb, (long long)BH * J, 128))
             return BSA_OK;
     } else {
-        mkb = mk;
-        mvb = mv;
+        mkb = mkr;
+        mvb = mvr;
     }
     *handled = true;
-    tc::Params prm;
     prm.index_map = im;
     prm.block_sizes = bs;
     prm.q2k_idx = idx;
@@ -629,7 +728,8 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));
     dim3 grid((J + 1) / 2, BH);
-    tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mkb, mvb, prm);
+    tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5,
+                                                                       mkb, mvb, prm);
     return check_launch("bsa_fwd_tc_kernel");
 }
 

@@ -39,6 +39,11 @@ class Geometry:
         return -(-self.n_prefix // self.M)
 
     @property
+    def geometry(self):
+        """The tiling as the 8 host integers the attention entry points take."""
+        return [self.T, self.H, self.W, self.bT, self.bH, self.bW, self.n_prefix, 1 if self.perm is not None else 0]
+
+    @property
     def num_blocks(self):
         return bsa.bsa_tile_count(self.T, self.H, self.W, self.bT, self.bH, self.bW, self.n_prefix,
                                   self.perm is not None, self.M)
@@ -66,7 +71,7 @@ class BlockSparseResult:
 
 
 def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=False, need_lse=True,
-                           tiles=None):
+                           tiles=None, pass_geometry=True):
     """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
 
     q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
@@ -94,11 +99,11 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     out = torch.empty_like(q)
     lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
     if summary:
-        bsa.bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, q2k_idx, q2k_num,
-                            kmax, kbar_lp, vbar_lp, scale, out, lse)
+        bsa.bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
+                            q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse)
     else:
-        bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, q2k_idx, q2k_num,
-                           kmax, scale, out, lse)
+        bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
+                           q2k_idx, q2k_num, kmax, scale, out, lse)
     return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num)
 
 

@@ -130,12 +130,20 @@ bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, i
  * dense prefix: every query keeps all of their keys, and their own query rows
  * attend to every key.  q2k_idx [BH, J-prefix_blocks, kmax] / q2k_num hold
  * routed block ids counted among the routed blocks.
+ * geometry: [host] 8 int32 {T, H, W, bT, bH, bW, n_prefix, permuted} with the
+ * bsa_tile_map arguments that built index_map (permuted = 1 when a
+ * permutation was given), or NULL.  With it the tensor-core kernel loads a
+ * whole (bT,bH,bW) window (not ragged in H or W) or a contiguous prefix
+ * block with one TMA box per half tile; without it, or for other blocks,
+ * tiles are gathered four rows per TMA operation through index_map.  A
+ * geometry that does not describe index_map gives wrong results.
  * q, k, v, out: [device] BHSD of `dtype`; lse: [device] float [BH, N] or NULL.
  * bf16 with D = 128 and M = 128 runs on the tcgen05 tensor-core kernel;
  * other shapes (D <= 128, M <= 128) on the CUDA-core kernel. */
 bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype dtype,
                           int BH, int N, int D, const int32_t* index_map,
                           const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                          const int32_t* geometry,
                           const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
                           float scale, void* out, float* lse, void* stream);
 
@@ -215,6 +223,7 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
 bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype,
                            int BH, int N, int D, const int32_t* index_map,
                            const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                           const int32_t* geometry,
                            const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
                            const void* kbar_lp, const void* vbar_lp,
                            float scale, void* out, float* lse, void* stream);

@@ -55,7 +55,7 @@ def test_tile_map_bit_exact(lib, grid, block, M, n_prefix, permuted):
 # ---------------------------------------------------------------- a2-a4, block granularity
 
 def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, force_simt=False,
-                    n_prefix=0, permuted=False, summary=False, cluster=False):
+                    n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True):
     pl = _pipeline()
     T, H, W = grid
     if cluster:
@@ -69,7 +69,8 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
     geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
                        perm=torch.as_tensor(perm, device=DEV) if permuted else None)
     lib.bsa_set_force_simt(force_simt)
-    res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary)
+    res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary,
+                                    pass_geometry=pass_geometry)
     torch.cuda.synchronize()
     blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
     P = len(oracle.tile_prefix(n_prefix, M))
@@ -113,6 +114,14 @@ def test_video_dit_shape_small_bf16(lib, force_simt):
     # (4,4,8) blocks over a (6,16,24) grid: 2*4*3 = 24 blocks, the last t-row holds 2 frames
     _run_block_case(lib, 1, 2, (6, 16, 24), (4, 4, 8), 128, 128, 6, torch.bfloat16, 202, field=True,
                     force_simt=force_simt)
+
+
+@pytest.mark.parametrize("pass_geometry", [True, False])
+def test_windows_ragged_in_h_and_w_bf16(lib, pass_geometry):
+    # (4,4,8) windows over a (5,6,12) grid: full windows load as one TMA box,
+    # windows ragged in H or W are gathered row by row, the T tail is zero-filled
+    _run_block_case(lib, 1, 2, (5, 6, 12), (4, 4, 8), 128, 128, 3, torch.bfloat16, 77, field=True,
+                    pass_geometry=pass_geometry)
 
 
 def test_dense_prefix_and_permutation_bf16(lib):
