@@ -52,6 +52,7 @@ _SIGS = {
     "bsa_reverse_index_workspace": (SZ, [I, I, I, I]),
     "bsa_max_chunks": (I, [I, I, I, I, I, I]),
     "bsa_build_reverse_index": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P, SZ, P]),
+    "bsa_build_reverse_index_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P]),
     "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P]),
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
     "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, I, P, P, F, P, P, P]),
@@ -178,6 +179,14 @@ def bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_p
                                         _ptr(n_chunks), max_chunks, _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
                                         _stream(stream)))
+
+
+def bsa_build_reverse_index_noalloc(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx, slot,
+                                    chunks, n_chunks, max_chunks, stream=None):
+    """bsa_build_reverse_index with the library's static scratch (no workspace argument)."""
+    _check(_lib.bsa_build_reverse_index_noalloc(_ptr(q2k_idx), _ptr(q2k_num), B, N, H, S, nblk, chunk_cap,
+                                                _ptr(row_ptr), _ptr(q_idx), _ptr(slot), _ptr(chunks),
+                                                _ptr(n_chunks), max_chunks, _stream(stream)))
 
 
 def bsa_fwd_kvouter(q, k, v, B, N, HQ, H, D, row_ptr, q_idx, slot, chunks, n_chunks, max_chunks, nblk,

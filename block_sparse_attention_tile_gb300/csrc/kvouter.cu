@@ -12,6 +12,8 @@
 // per-tile offsets, row pointers and the chunk list, and a second pass ranks
 // every entry inside its tile with per-warp lane masks, so each CSR row lists
 // its queries in ascending order.
+#include <mutex>
+
 #include "simt_tile.cuh"
 
 namespace bsa {
@@ -432,3 +434,65 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- reverse index, no allocation
+//
+// Some callers cannot allocate device memory themselves: their device memory
+// belongs to another allocator or a fixed pool (a framework's caching
+// allocator, a server with a fixed memory budget), or they must not pay the
+// device-wide synchronisation that cudaMalloc / cudaFree can cause.  For
+// them bsa_build_reverse_index_noalloc takes its scratch from the static
+// device array below instead of a caller-provided workspace.  Every GPU that
+// loads this library holds the array until the process exits.
+namespace bsa {
+
+constexpr size_t kNoAllocScratchBytes = BSA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) int32_t g_reverse_index_scratch[kNoAllocScratchBytes / sizeof(int32_t)];
+
+// Device address of the static scratch array on the current device.  In host
+// code the array's name is only a host-side stand-in, so the address is
+// looked up once per device (with that device current) and cached.
+static void* noalloc_scratch(bsa_status* rc) {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *rc = fail(BSA_ERR_CUDA, "reverse_index_noalloc: no current device (%s)", cudaGetErrorString(e));
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_reverse_index_scratch);
+        if (e != cudaSuccess || !p) {
+            *rc = fail(BSA_ERR_CUDA, "reverse_index_noalloc: scratch address lookup failed: %s",
+                       cudaGetErrorString(e));
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace bsa
+
+extern "C" bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, const int32_t* q2k_num, int B,
+                                                      int N, int H, int S, int nblk, int chunk_cap,
+                                                      int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
+                                                      int32_t* chunks, int32_t* n_chunks, int max_chunks,
+                                                      void* stream) {
+    const size_t need = bsa_reverse_index_workspace(B, N, H, nblk);
+    if (need > bsa::kNoAllocScratchBytes)
+        return bsa::fail(BSA_ERR_INVALID_ARG,
+                         "reverse_index_noalloc: needs %zu bytes of scratch but the static buffer holds %zu "
+                         "(B*H*ceil(N/256)*nblk must not exceed %zu)",
+                         need, bsa::kNoAllocScratchBytes, bsa::kNoAllocScratchBytes / sizeof(int32_t));
+    bsa_status rc = BSA_OK;
+    void* ws = bsa::noalloc_scratch(&rc);
+    if (!ws) return rc;
+    // The count pass writes every scratch entry it later reads, so nothing
+    // left over from an earlier call needs clearing.
+    return bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx, slot,
+                                   chunks, n_chunks, max_chunks, ws, bsa::kNoAllocScratchBytes, stream);
+}

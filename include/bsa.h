@@ -183,6 +183,30 @@ bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_nu
                                    int32_t* chunks, int32_t* n_chunks, int max_chunks,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same reverse index for callers that cannot allocate device memory
+ * (their device memory is owned by another allocator or a fixed pool, or they
+ * must avoid the device-wide synchronisation that cudaMalloc / cudaFree can
+ * cause).  The pages have no counterpart; this is a library convenience.
+ * Arguments as bsa_build_reverse_index without the workspace: the scratch is
+ * a static device array of BSA_NOALLOC_SCRATCH_BYTES (1 MiB) inside the
+ * library, held by every GPU that loads it until the process exits.  Sizes
+ * whose scratch (bsa_reverse_index_workspace) exceeds it, i.e.
+ * B*H*ceil(N/256)*nblk > 262144, return BSA_ERR_INVALID_ARG.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current), so make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps the last call's
+ * contents: calls whose kernels may run at the same time on that device (for
+ * example on two streams with no ordering between them) race on it, so the
+ * caller must order them.  Nothing needs clearing between calls (the first
+ * pass overwrites every scratch entry it later reads).  Allocates nothing:
+ * no cudaMalloc, cudaFree or allocating library routine. */
+#define BSA_NOALLOC_SCRATCH_BYTES (1u << 20)
+bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, const int32_t* q2k_num,
+                                           int B, int N, int H, int S, int nblk, int chunk_cap,
+                                           int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
+                                           int32_t* chunks, int32_t* n_chunks, int max_chunks,
+                                           void* stream);
+
 /* ------------------------------------------------------------------ a6 ----
  * KV-outer partial pass (K1).  [MSA] §4 and §6.1: one CTA per chunk keeps
  * the K/V block resident and streams the chunk's queries (all G heads of a
