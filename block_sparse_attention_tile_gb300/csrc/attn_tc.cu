@@ -10,9 +10,8 @@
 // unselected routed block adds one virtual key (its mean key and value) with
 // logit bias log(n_j), folded into the same online softmax.
 //
-// Design (ours, for sm_103a).  One CTA per (head, pair of query blocks A, B),
-// 12 warps.  Each query block keeps its own key-tile list; the shorter list
-// is padded with fully masked rounds (the VSA page's dual-Q scheduling, §6.3).
+// Design (ours, for sm_103a).  One CTA per (head, query block), 12 warps,
+// one CTA per SM (TMEM: S0 [0,128), S1 [128,256), O [256,384) of 512 columns).
 //   warp 0      producer: TMA loads straight from the BHSD tensors into
 //               128-byte swizzled K-major tiles, no pack pass: a (bT,bH,bW)
 //               window is ONE box of a 5-D (D, W, H, T, head) tensor map per
@@ -21,23 +20,22 @@
 //               tile is one 128-row box, and any other block (a permutation,
 //               a window ragged in H or W) is gathered four rows per
 //               tile::gather4 through the index map.  TMA costs about the same
-//               per operation whatever its size, so the boxes are ~8x faster
-//               than gathering.  One 4-stage ring whose entries follow the MMA
-//               consumption order K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ...; the
-//               next entry's row ids are fetched while it waits.
-//   warp 1      TMEM owner and single-thread MMA issuer:
-//               S_A0, S_B0, then per round j: PV_A(j), S_A(j+1), PV_B(j),
-//               S_B(j+1).  While softmax A works on S_A(j) the tensor core
-//               runs S_B(j) and PV_B(j-1), and the other way round.
-//   warps 4-7   softmax of A, warps 8-11 softmax of B: one thread per query
-//               row; S from TMEM, mask, lazy running max (O is rescaled in
-//               TMEM only when the max grows by more than 2^8), P written back
-//               over S as packed bf16 = the TMEM A operand of P V; l in a
-//               register; epilogue O / l -> bf16 -> global through the map.
-// TMEM (512 columns): S_A [0,128), O_A [128,256), S_B [256,384), O_B [384,512).
-// Registers: warpgroup 0 gives up registers (setmaxnreg.dec 64) so the two
-// softmax warpgroups can hold a full S row (setmaxnreg.inc 216); the launch
-// holds 384 x 168 = 64512 registers, more than the split needs.
+//               per operation whatever its size, so boxes are ~8x faster than
+//               gathering.  A 5-stage ring in MMA consumption order
+//               K0 K1 | V0 K2 | V1 K3 | ... gives each load about two tiles of
+//               lead time; the next entry's row ids are fetched while it waits.
+//   warp 1      TMEM owner and single-thread MMA issuer: S0, S1, then
+//               PV_j, S_{j+2} for every j.  S is double buffered, so QK of tile
+//               j+1 (and j+2) runs while the softmax works on tile j.
+//               P_j is read from TMEM, where the softmax wrote it over S_j as
+//               packed bf16 (the A operand of P V); V is an MN-major operand.
+//   warps 4-7   softmax of key columns 0..63, warps 8-11 of columns 64..127,
+//               one query row per thread in each half: the two halves swap
+//               their row maxima through shared memory once per tile, then
+//               each exponentiates and writes its half of P; the running max
+//               is updated lazily (O in TMEM is rescaled only when the max
+//               grows by more than 2^8), l is kept per half and added at the
+//               end; epilogue O / l -> bf16 -> global through the index map.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA raises
 // BSA_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs, frees TMEM.
 #include <cuda.h>
@@ -56,27 +54,29 @@ constexpr int kBM = 128;          // query rows per query block
 constexpr int kBN = 128;          // keys per tile
 constexpr int kHD = 128;          // head dim
 constexpr int kThreads = 384;
-constexpr int kStages = 4;        // K/V ring depth (32 KB each)
+constexpr int kStages = 5;        // K/V ring depth (32 KB each)
 constexpr int kMaxList = 512;     // key tiles per query block, virtual tiles included
 constexpr int kMaxVirtual = 8;    // summary tiles (<= 1024 routed blocks)
-constexpr int kRegsLow = 64, kRegsHigh = 216, kRegsLaunch = 168;
 constexpr uint32_t kTileBytes = kBN * kHD * 2;       // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 16 KB: 128 rows x 64 cols
 constexpr uint64_t kWaitNs = 2000000000ull;          // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
-
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
+constexpr int kSoftmaxBarrier = 1;                   // named barrier of the 256 softmax threads
 
 // shared memory map (offsets from a 1024-byte aligned base)
-constexpr uint32_t OFF_Q = 0;                                   // Q_A, Q_B
-constexpr uint32_t OFF_RING = OFF_Q + 2 * kTileBytes;
-constexpr uint32_t OFF_LIST = OFF_RING + kStages * kTileBytes;  // int[2][kMaxList]: tile ids (<0: virtual)
-constexpr uint32_t OFF_NVALID = OFF_LIST + 2 * 4 * kMaxList;    // int[2][kMaxList]
-constexpr uint32_t OFF_BIAS = OFF_NVALID + 2 * 4 * kMaxList;    // float[2][kMaxVirtual*128]
-constexpr uint32_t OFF_SEL = OFF_BIAS + 2 * 4 * kMaxVirtual * kBN;  // uint32[2][32]
-constexpr uint32_t OFF_BAR = OFF_SEL + 2 * 4 * 32;
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_RING = OFF_Q + kTileBytes;
+constexpr uint32_t OFF_LIST = OFF_RING + kStages * kTileBytes;  // int[kMaxList]: tile ids (<0: virtual)
+constexpr uint32_t OFF_NVALID = OFF_LIST + 4 * kMaxList;        // int[kMaxList]
+constexpr uint32_t OFF_BIAS = OFF_NVALID + 4 * kMaxList;        // float[kMaxVirtual*128]
+constexpr uint32_t OFF_SEL = OFF_BIAS + 4 * kMaxVirtual * kBN;  // uint32[32]
+constexpr uint32_t OFF_XCH = OFF_SEL + 4 * 32;                  // float[3][2 halves][128]: maxima of
+                                                                // tiles of each parity, then l
+constexpr uint32_t OFF_SRC = OFF_XCH + 4 * 3 * 2 * kBM;        // int4[kMaxList]: packed tile sources
+constexpr uint32_t OFF_BAR = OFF_SRC + 16 * kMaxList;
 constexpr int BAR_Q = 0, BAR_FULL = 1, BAR_EMPTY = BAR_FULL + kStages, BAR_SF = BAR_EMPTY + kStages,
-              BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2, BAR_DRAIN = BAR_OF + 2, NBAR = BAR_DRAIN + 1;
+              BAR_PF = BAR_SF + 2, BAR_OD = BAR_PF + 2, BAR_OF = BAR_OD + 1, BAR_DRAIN = BAR_OF + 1,
+              NBAR = BAR_DRAIN + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;               // tmem base, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;           // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -130,6 +130,12 @@ __device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int b
     return s;
 }
 
+// A tile source packed in 16 bytes for the producer's table:
+// x = mode | (virtual << 2), y = c1, z = c2 | (c3 << 16), w = c4.
+__device__ __forceinline__ int4 pack_src(const TileSrc& s, bool virt) {
+    return make_int4(s.mode | (virt ? 4 : 0), s.c1, (s.c2 & 0xffff) | (s.c3 << 16), s.c4);
+}
+
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
@@ -144,29 +150,23 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// Entry e of the ring sequence: which query block (X), which round (j), K or V.
-//   one block : K0 | V0 K1 | V1 K2 | ... | V(n-1)                       (2n entries)
-//   two blocks: K_A0 K_B0 | V_A0 K_A1 V_B0 K_B1 | ... | V_A(n-1) V_B(n-1)  (4n entries)
-__device__ __forceinline__ void decode_entry(int e, int n, bool two, int& X, int& j, bool& isV) {
-    if (!two) {
-        X = 0;
-        if (e == 0) { j = 0; isV = false; return; }
-        const int t = e - 1;
-        j = (t >> 1) + (t & 1);
+// Ring entry e in MMA consumption order S0 S1 | PV0 S2 | PV1 S3 | ... | PV(n-1):
+// K0 K1 | V0 K2 | V1 K3 | ... | V(n-2) | V(n-1)  (2n entries).
+__device__ __forceinline__ void decode_entry(int e, int n, int& j, bool& isV) {
+    if (n == 1) { j = 0; isV = e == 1; return; }
+    if (e < 2) { j = e; isV = false; return; }
+    const int t = e - 2;
+    if (t < 2 * (n - 2)) {
+        j = (t >> 1) + ((t & 1) ? 2 : 0);
         isV = !(t & 1);
-        return;
-    }
-    if (e < 2) { X = e; j = 0; isV = false; return; }
-    const int t = e - 2, g = t >> 2, r = t & 3;
-    if (g < n - 1) {
-        X = r >> 1;
-        isV = !(r & 1);
-        j = isV ? g : g + 1;
     } else {
-        X = r;
+        j = (n - 2) + (t - 2 * (n - 2));
         isV = true;
-        j = n - 1;
     }
+}
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -180,41 +180,37 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
-    int* lists = reinterpret_cast<int*>(sm + OFF_LIST);
-    int* nvalids = reinterpret_cast<int*>(sm + OFF_NVALID);
-    float* biases = reinterpret_cast<float*>(sm + OFF_BIAS);
+    int* list = reinterpret_cast<int*>(sm + OFF_LIST);
+    int* nvalid = reinterpret_cast<int*>(sm + OFF_NVALID);
+    float* bias = reinterpret_cast<float*>(sm + OFF_BIAS);
     uint32_t* selbits = reinterpret_cast<uint32_t*>(sm + OFF_SEL);
+    float* xch = reinterpret_cast<float*>(sm + OFF_XCH);
     uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     const uint32_t bar0 = base + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
 
+    const int qb = blockIdx.x;
     const int bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int J = prm.J, P = prm.P, Jr = J - P;
+    const int nq = prm.block_sizes[qb];
+    if (nq <= 0) return;  // an empty block has no query rows
+    const bool dense_row = qb < P;
 
-    // the two query blocks of this CTA (an empty or missing one is dropped)
-    int qblk[2] = {2 * (int)blockIdx.x, 2 * (int)blockIdx.x + 1};
-    int nq[2];
-    nq[0] = prm.block_sizes[qblk[0]];
-    nq[1] = qblk[1] < J ? prm.block_sizes[qblk[1]] : 0;
-    if (nq[0] <= 0) { qblk[0] = qblk[1]; nq[0] = nq[1]; nq[1] = 0; }
-    if (nq[0] <= 0) return;  // no query rows at all
-    const bool two = nq[1] > 0;
-    const int nX = two ? 2 : 1;
-
-    // ---- prologue: barriers, TMEM, the key-tile lists
+    // ---- prologue: barriers, TMEM, the key-tile list
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(BAR_Q), 1);
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(BAR_FULL + s), 1);
             ptx::mbar_init(bar(BAR_EMPTY + s), 1);
         }
-        for (int x = 0; x < 2; ++x) {
-            ptx::mbar_init(bar(BAR_SF + x), 1);
-            ptx::mbar_init(bar(BAR_PF + x), kBM);
-            ptx::mbar_init(bar(BAR_OF + x), 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(BAR_SF + b), 1);
+            ptx::mbar_init(bar(BAR_PF + b), 2 * kBM);
         }
+        ptx::mbar_init(bar(BAR_OD), 1);
+        ptx::mbar_init(bar(BAR_OF), 1);
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         ptx::fence_mbar_init();
         misc[1] = 0;
@@ -223,82 +219,77 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_alloc(base + OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
-    if (threadIdx.x < 64) selbits[threadIdx.x] = 0u;
-    int nlist[2] = {0, 0}, nsel[2] = {0, 0};
-    for (int x = 0; x < nX; ++x) {
-        const int qb = qblk[x];
-        if (qb < P) {
-            nlist[x] = J;
-        } else {
-            const int ns = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
-            nsel[x] = max(0, min(ns, prm.kmax));
-            nlist[x] = P + nsel[x] + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
-        }
+    if (threadIdx.x < 32) selbits[threadIdx.x] = 0u;
+    int n, nsel = 0;
+    if (dense_row) {
+        n = J;
+    } else {
+        const int ns = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
+        nsel = max(0, min(ns, prm.kmax));
+        n = P + nsel + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
     }
-    const int n = max(nlist[0], nlist[1]);
     __syncthreads();
-    for (int x = 0; x < nX; ++x) {
-        const int qb = qblk[x];
-        const bool dense_row = qb < P;
-        int* list = lists + x * kMaxList;
-        int* nvalid = nvalids + x * kMaxList;
-        for (int s = threadIdx.x; s < n; s += blockDim.x) {
-            int blk, nv;
-            if (s >= nlist[x]) {
-                blk = P > 0 ? 0 : qb;  // padding round: any real tile, fully masked
-                nv = 0;
-            } else if (dense_row || s < P) {
-                blk = s;
-                nv = prm.block_sizes[blk];
-            } else if (s < P + nsel[x]) {
-                const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
-                if (jr < 0 || jr >= Jr) {
-                    raise_status(prm.status, BSA_ERR_INDEX);
-                    blk = P > 0 ? 0 : qb;
-                    nv = 0;  // contributes nothing
-                } else {
-                    blk = P + jr;
-                    nv = prm.block_sizes[blk];
-                    if (prm.summary) atomicOr(&selbits[x * 32 + (jr >> 5)], 1u << (jr & 31));
-                }
+    for (int s = threadIdx.x; s < n; s += blockDim.x) {
+        int blk, nv;
+        if (dense_row || s < P) {
+            blk = s;
+            nv = prm.block_sizes[blk];
+        } else if (s < P + nsel) {
+            const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
+            if (jr < 0 || jr >= Jr) {
+                raise_status(prm.status, BSA_ERR_INDEX);
+                blk = P > 0 ? 0 : qb;
+                nv = 0;  // contributes nothing
             } else {
-                const int t = s - (P + nsel[x]);
-                blk = -(t + 1);
-                nv = min(kBN, Jr - t * kBN);
+                blk = P + jr;
+                nv = prm.block_sizes[blk];
+                if (prm.summary) atomicOr(&selbits[jr >> 5], 1u << (jr & 31));
             }
-            list[s] = blk;
-            nvalid[s] = nv;
+        } else {
+            const int t = s - (P + nsel);
+            blk = -(t + 1);
+            nv = min(kBN, Jr - t * kBN);
         }
+        list[s] = blk;
+        nvalid[s] = nv;
     }
     __syncthreads();
-    if (prm.summary) {
+    {
+        int4* srcs = reinterpret_cast<int4*>(sm + OFF_SRC);
+        for (int s = threadIdx.x; s < n; s += blockDim.x) {
+            const int blk = list[s];
+            srcs[s] = pack_src(tile_source(blk, prm, bh), blk < 0);
+        }
+    }
+    if (prm.summary && !dense_row) {
         const int nvirt = (Jr + kBN - 1) / kBN;
-        for (int x = 0; x < nX; ++x) {
-            for (int jr = threadIdx.x; jr < nvirt * kBN; jr += blockDim.x) {
-                float b = -CUDART_INF_F;
-                if (jr < Jr && !((selbits[x * 32 + (jr >> 5)] >> (jr & 31)) & 1u)) {
-                    const int nb = prm.block_sizes[P + jr];
-                    if (nb > 0) b = log2f((float)nb);
-                }
-                biases[x * kMaxVirtual * kBN + jr] = b;
+        for (int jr = threadIdx.x; jr < nvirt * kBN; jr += blockDim.x) {
+            float b = -CUDART_INF_F;
+            if (jr < Jr && !((selbits[jr >> 5] >> (jr & 31)) & 1u)) {
+                const int nb = prm.block_sizes[P + jr];
+                if (nb > 0) b = log2f((float)nb);
             }
+            bias[jr] = b;
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int n_entries = two ? 4 * n : 2 * n;
+    const int n_entries = 2 * n;
 
-    if (warp < 4) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-      if (warp == 0) {
+    if (warp == 0) {
         // ------------------------------------------------------------ producer
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_q5);
+        ptx::prefetch_tmap(&tm_k5);
+        ptx::prefetch_tmap(&tm_v5);
+        ptx::prefetch_tmap(&tm_kr);
+        ptx::prefetch_tmap(&tm_vr);
         const long long head_row = (long long)bh * prm.N;
-        const int q0tok = prm.index_map[(long long)qblk[0] * kBM];  // a valid row: pads point here
+        const int q0tok = prm.index_map[(long long)qb * kBM];  // a valid row: pads point here
         // issue one 32 KB tile (two 64-column halves) from source `src`
         auto issue_tile = [&](uint32_t dst, const TileSrc& src, const int* rows, const CUtensorMap* mg,
                               const CUtensorMap* mr, const CUtensorMap* m5, uint32_t b) {
@@ -331,47 +322,60 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 rows[u] = (int)(head_row + tok);
             }
         };
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), (uint32_t)nX * kTileBytes);
+        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
         __syncwarp();
-        for (int x = 0; x < nX; ++x) {
-            const TileSrc src = tile_source(qblk[x], prm, bh);
+        {
+            const TileSrc src = tile_source(qb, prm, bh);
             int rq[4] = {0, 0, 0, 0};
-            if (src.mode == 0) gather_rows(qblk[x], nq[x], rq);
-            issue_tile(base + OFF_Q + x * kTileBytes, src, rq, &tm_q, &tm_qr, &tm_q5, bar(BAR_Q));
+            if (src.mode == 0) gather_rows(qb, nq, rq);
+            issue_tile(base + OFF_Q, src, rq, &tm_q, &tm_qr, &tm_q5, bar(BAR_Q));
         }
-        // the source of ring entry e; gathered row ids are loaded one entry ahead
-        struct Next {
-            TileSrc src;
-            int rows[4];
-            bool isV, virt;
-        };
-        auto fetch = [&](int e, Next& nx) {
-            int X, j;
-            decode_entry(e, n, two, X, j, nx.isV);
-            const int blk = lists[X * kMaxList + j];
-            nx.virt = blk < 0;
-            nx.src = tile_source(blk, prm, bh);
-            if (nx.src.mode == 0) gather_rows(blk, nvalids[X * kMaxList + j], nx.rows);
-        };
-        Next cur{}, nxt{};
+        // Ring entry e: its tile's source comes from the table built in the
+        // prologue; gathered row ids (mode 0 only) are loaded one entry ahead.
+        const int4* srcs = reinterpret_cast<const int4*>(sm + OFF_SRC);
         int issued = 0;
-        if (n_entries > 0) fetch(0, cur);
+        int rows_next[4] = {0, 0, 0, 0};
+        int j_next = 0;
+        bool v_next = false;
+        int4 src_next = make_int4(0, 0, 0, 0);
+        auto prepare = [&](int e) {
+            decode_entry(e, n, j_next, v_next);
+            src_next = srcs[j_next];
+            if ((src_next.x & 3) == 0) gather_rows(list[j_next], nvalid[j_next], rows_next);
+        };
+        if (n_entries > 0) prepare(0);
         for (int e = 0; e < n_entries; ++e) {
-            if (e + 1 < n_entries) fetch(e + 1, nxt);
+            const int4 src = src_next;
+            const bool isV = v_next;
+            const int rows[4] = {rows_next[0], rows_next[1], rows_next[2], rows_next[3]};
+            if (e + 1 < n_entries) prepare(e + 1);
             const int st = e % kStages;
             const uint32_t ph = (uint32_t)(e / kStages) & 1u;
             if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) break;
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
             __syncwarp();
             const uint32_t dst = base + OFF_RING + st * kTileBytes;
-            if (cur.virt)
-                issue_tile(dst, cur.src, cur.rows, &tm_k, cur.isV ? &tm_vb : &tm_kb, &tm_k5, bar(BAR_FULL + st));
-            else if (cur.isV)
-                issue_tile(dst, cur.src, cur.rows, &tm_v, &tm_vr, &tm_v5, bar(BAR_FULL + st));
-            else
-                issue_tile(dst, cur.src, cur.rows, &tm_k, &tm_kr, &tm_k5, bar(BAR_FULL + st));
+            const int mode = src.x & 3;
+            const bool virt = (src.x & 4) != 0;
+            const uint32_t fb = bar(BAR_FULL + st);
+            if (mode == 0) {
+                const CUtensorMap* mg = isV ? &tm_v : &tm_k;
+                const uint32_t d = dst + 4 * lane * 128;
+                ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], fb);
+                ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], fb);
+            } else if (lane == 0) {
+                if (mode == 1) {
+                    const CUtensorMap* mr = virt ? (isV ? &tm_vb : &tm_kb) : (isV ? &tm_vr : &tm_kr);
+                    ptx::tma_load_2d(dst, mr, 0, src.y, fb);
+                    ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.y, fb);
+                } else {
+                    const CUtensorMap* m5 = isV ? &tm_v5 : &tm_k5;
+                    const int c2 = src.z & 0xffff, c3 = src.z >> 16;
+                    ptx::tma_load_5d(dst, m5, 0, src.y, c2, c3, src.w, fb);
+                    ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.y, c2, c3, src.w, fb);
+                }
+            }
             issued = e + 1;
-            cur = nxt;
         }
         if (*abort_flag) {
             // drain: wait (bounded) for this warp's copies still in flight
@@ -382,11 +386,12 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-      } else if (warp == 1) {
+    } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kBM, kHD, true);
+            const uint32_t tO = tmem + 256;
             int ec = 0;  // ring entries consumed
             bool ok = wait_bar(bar(BAR_Q), 0, abort_flag, prm.status);
             auto take = [&](uint32_t& addr) -> bool {
@@ -401,121 +406,126 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ptx::mma_commit(bar(BAR_EMPTY + ec % kStages));
                 ++ec;
             };
-            auto issue_s = [&](int x) -> bool {
+            auto issue_s = [&](int j) -> bool {
                 uint32_t ka;
                 if (!take(ka)) return false;
-                const uint32_t qa = base + OFF_Q + x * kTileBytes;
-                const uint32_t dS = tmem + (uint32_t)x * 256;
+                const uint32_t qa = base + OFF_Q;
+                const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < kHD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
                     ptx::mma_ss(dS, ptx::smem_desc(qa + off, 16, 1024), ptx::smem_desc(ka + off, 16, 1024), idS,
                                 kk > 0);
                 }
-                ptx::mma_commit(bar(BAR_SF + x));
+                ptx::mma_commit(bar(BAR_SF + (j & 1)));
                 release();
                 return true;
             };
-            auto issue_pv = [&](int x, int j) -> bool {
-                if (!wait_bar(bar(BAR_PF + x), (uint32_t)j & 1u, abort_flag, prm.status)) return false;
+            auto issue_pv = [&](int j) -> bool {
+                if (!wait_bar(bar(BAR_PF + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, prm.status)) return false;
                 uint32_t va;
                 if (!take(va)) return false;
-                const uint32_t aP = tmem + (uint32_t)x * 256;
-                const uint32_t dO = aP + 128;
+                const uint32_t aP = tmem + (uint32_t)(j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
                     // V advances by two 8-row groups of 1024 B; the second
                     // 64-column half of V is one leading-dimension step (16 KB) away.
-                    ptx::mma_ts(dO, aP + kk * 8, ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
+                    ptx::mma_ts(tO, aP + kk * 8, ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
                                 (j > 0 || kk > 0) ? 1u : 0u);
                 }
+                ptx::mma_commit(bar(BAR_OD));
                 release();
-                if (j == n - 1) ptx::mma_commit(bar(BAR_OF + x));
+                if (j == n - 1) ptx::mma_commit(bar(BAR_OF));
                 return true;
             };
             if (ok) ok = issue_s(0);
-            if (ok && two) ok = issue_s(1);
+            if (ok && n > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n; ++j) {
-                for (int x = 0; ok && x < nX; ++x) {
-                    ok = issue_pv(x, j);
-                    if (ok && j + 1 < n) ok = issue_s(x);
-                }
+                ok = issue_pv(j);
+                if (ok && j + 2 < n) ok = issue_s(j + 2);
             }
             // nothing this thread issued may still run when TMEM is freed
             ptx::mma_commit(bar(BAR_DRAIN));
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(bar(BAR_DRAIN), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-      }
-    } else {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-      if ((warp - 4) / 4 < nX) {
-        // ------------------------------------------------------------ softmax + epilogue of block X
-        const int X = (warp - 4) / 4;
-        const int row = threadIdx.x - 128 - X * 128;
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int half = (warp - 4) >> 2;          // key / output columns [64*half, 64*half + 64)
+        const int row = threadIdx.x & 127;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tS = tmem + lane_off + (uint32_t)X * 256;
-        const uint32_t tO = tS + 128;
-        const int* list = lists + X * kMaxList;
-        const int* nvalid = nvalids + X * kMaxList;
-        const float* bias = biases + X * kMaxVirtual * kBN;
+        const uint32_t tO = tmem + lane_off + 256 + 64 * half;
         float m_ref = -CUDART_INF_F, l = 0.f;
         bool ok = true;
         uint32_t r[32];
-        float x[kBN];
+        float x[64];
+        // After an abort a thread keeps looping without touching TMEM, so that
+        // both halves still meet at every named barrier.
         for (int s = 0; s < n; ++s) {
-            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + X), (uint32_t)s & 1u, abort_flag, prm.status));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            {
+            const int b = s & 1;
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                wait_bar(bar(BAR_SF + b), (uint32_t)(s >> 1) & 1u, abort_flag, prm.status));
+            const uint32_t tS = tmem + lane_off + (uint32_t)b * 128;
+            if (ok) {
+                ptx::tc_fence_after();
                 uint32_t* xr = reinterpret_cast<uint32_t*>(x);
-                ptx::tmem_ld32(tS + 0, xr + 0);
-                ptx::tmem_ld32(tS + 32, xr + 32);
-                ptx::tmem_ld32(tS + 64, xr + 64);
-                ptx::tmem_ld32(tS + 96, xr + 96);
+                ptx::tmem_ld32(tS + 64 * half, xr);
+                ptx::tmem_ld32(tS + 64 * half + 32, xr + 32);
                 ptx::tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) x[c] = 0.f;
             }
             const int blk = list[s];
             const int nv = nvalid[s];
+            const int c0 = 64 * half;
             float mxp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
             if (blk >= 0 || nv == 0) {
                 if (nv >= kBN) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        x[c] *= prm.scale_log2;
-                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
-                    }
+                    for (int c = 0; c < 64; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        x[c] = c < nv ? x[c] * prm.scale_log2 : -CUDART_INF_F;
+                    for (int c = 0; c < 64; ++c) {
+                        x[c] = c0 + c < nv ? x[c] : -CUDART_INF_F;
                         mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                     }
                 }
-            } else {
-                const float* bt = bias + (-blk - 1) * kBN;
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
+                for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
+            } else {
+                const float* bt = bias + (-blk - 1) * kBN + c0;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
                     x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
                     mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                 }
             }
-            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            // swap the partial row maxima of the two column halves
+            float* xb = xch + (b * 2) * kBM;
+            xb[half * kBM + row] = mx;
+            named_sync(kSoftmaxBarrier, 2 * kBM);
+            mx = fmaxf(mx, xb[(1 - half) * kBM + row]);
             const float m_new = fmaxf(m_ref, mx);
             const bool need = m_new > m_ref + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;  // m_ref = -inf -> 0
                 if (need) m_ref = m_new;
                 l *= alpha;
-                if (s > 0) {
-                    // S(s) was issued after PV(s-1), so its completion means O
-                    // already holds P_0..P_{s-1} V: rescale it in place.
+                if (s > 0 && ok) {
+                    // O must hold P_0..P_{s-1} V before it is rescaled
+                    ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD), (uint32_t)(s - 1) & 1u, abort_flag, prm.status));
+                }
+                if (s > 0 && ok) {
+                    ptx::tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         ptx::tmem_ld32(tO + c * 32, r);
                         ptx::tmem_wait_ld();
 #pragma unroll
@@ -529,36 +539,49 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int u = 0; u < 8; ++u) sp[u] = 0.f;
             const bool live = m_ref != -CUDART_INF_F;
+            if (blk >= 0 || nv == 0) {
+                // x holds raw Q.K: one FMA folds the scale and subtracts the reference
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) {
-                x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
-                sp[c & 7] += x[c];
+                for (int c = 0; c < 64; ++c) {
+                    x[c] = live ? ptx::ex2(fmaf(x[c], prm.scale_log2, -m_ref)) : 0.f;
+                    sp[c & 7] += x[c];
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
+                    sp[c & 7] += x[c];
+                }
             }
             l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            // this half's 64 keys -> packed bf16 columns [32*half, 32*half + 32) over S
+            if (ok) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = ptx::pack_bf16x2(x[h * 64 + 2 * e], x[h * 64 + 2 * e + 1]);
-                ptx::tmem_st32(tS + h * 32, r);
+                for (int e = 0; e < 32; ++e) r[e] = ptx::pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                ptx::tmem_st32(tS + 32 * half, r);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(BAR_PF + b));
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BAR_PF + X));
         }
-        // epilogue
-        if (ok && n > 0) ok = wait_bar(bar(BAR_OF + X), 0, abort_flag, prm.status);
+        // epilogue: l of the row is the sum of both halves
+        if (ok && n > 0) ok = wait_bar(bar(BAR_OF), 0, abort_flag, prm.status);
         ok = __all_sync(0xffffffffu, ok);
         ptx::tc_fence_after();
-        const bool write = ok && row < nq[X];
+        float* xl = xch + 4 * kBM;
+        xl[half * kBM + row] = l;
+        named_sync(kSoftmaxBarrier, 2 * kBM);
+        const float l_row = l + xl[(1 - half) * kBM + row];
+        const bool write = ok && row < nq;
         int tok = -1;
         if (write) {
-            tok = prm.index_map[(long long)qblk[X] * kBM + row];
+            tok = prm.index_map[(long long)qb * kBM + row];
             if (tok < 0 || tok >= prm.N) tok = -1;
         }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD;
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD + 64 * half;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
             if (ok && n > 0) {
                 ptx::tmem_ld32(tO + c * 32, r);
                 ptx::tmem_wait_ld();
@@ -579,9 +602,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
         }
-        if (write && tok >= 0 && prm.lse)
-            prm.lse[(long long)bh * prm.N + tok] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -CUDART_INF_F;
-      }
+        if (half == 0 && write && tok >= 0 && prm.lse)
+            prm.lse[(long long)bh * prm.N + tok] = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -CUDART_INF_F;
     }
 
     ptx::tc_fence_before();
@@ -639,20 +661,6 @@ static bool make_window_map(CUtensorMap* m, const void* video_base, int T, int H
     return r == CUDA_SUCCESS;
 }
 
-// The register split assumes the launch reserves kRegsLaunch registers per
-// thread; refuse the tensor-core path otherwise (setmaxnreg.inc would wait).
-static bool register_split_fits() {
-    static int checked = 0;  // 0 unknown, 1 fits, -1 does not
-    if (!checked) {
-        cudaFuncAttributes a;
-        checked = (cudaFuncGetAttributes(&a, bsa_fwd_tc_kernel) == cudaSuccess &&
-                   a.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh)
-                      ? 1
-                      : -1;
-    }
-    return checked == 1;
-}
-
 }  // namespace tc
 
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
@@ -667,7 +675,6 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
-    if (!tc::register_split_fits()) return BSA_OK;
     tc::Params prm{};
     CUtensorMap mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5, mkb, mvb;
     const long long rows = (long long)BH * N;
@@ -727,7 +734,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     cudaError_t e = cudaFuncSetAttribute(tc::bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));
-    dim3 grid((J + 1) / 2, BH);
+    dim3 grid(J, BH);
     tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5,
                                                                        mkb, mvb, prm);
     return check_launch("bsa_fwd_tc_kernel");

@@ -45,13 +45,44 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     }
     const int r = tid / 16;        // row of this thread
     const int cg = tid % 16;       // column group: columns cg + 16*c
+    // The key tile is staged through registers one tile ahead, so its L2
+    // latency overlaps the dot products of the previous tile.
+    constexpr int kMaxV4 = kRouteCols * 256 / 4 / kRouteThreads;  // float4 per thread for D <= 256
+    const bool vec = (D % 4) == 0;
+    const int nv4 = kRouteCols * (Dp / 4);                          // float4 per tile
+    float4 pre[kMaxV4];
+    auto prefetch = [&](int c0) {
+#pragma unroll
+        for (int u = 0; u < kMaxV4; ++u) {
+            const int idx = tid + u * kRouteThreads;
+            float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (vec && idx < nv4) {
+                const int c = idx / (Dp / 4), d4 = idx % (Dp / 4);
+                if (c0 + c < J) val = *reinterpret_cast<const float4*>(kh + (long long)(c0 + c) * D + 4 * d4);
+            }
+            pre[u] = val;
+        }
+    };
+    if (vec) prefetch(0);
     for (int c0 = 0; c0 < J; c0 += kRouteCols) {
         __syncthreads();
-        for (int idx = tid; idx < kRouteCols * Dp; idx += blockDim.x) {
-            const int c = idx / Dp, d = idx % Dp;
-            ks[c * Dk + d] = (c0 + c < J && d < D) ? kh[(long long)(c0 + c) * D + d] : 0.f;
+        if (vec) {
+#pragma unroll
+            for (int u = 0; u < kMaxV4; ++u) {
+                const int idx = tid + u * kRouteThreads;
+                if (idx < nv4) {
+                    const int c = idx / (Dp / 4), d4 = idx % (Dp / 4);
+                    *reinterpret_cast<float4*>(ks + c * Dk + 4 * d4) = pre[u];
+                }
+            }
+        } else {
+            for (int idx = tid; idx < kRouteCols * Dp; idx += blockDim.x) {
+                const int c = idx / Dp, d = idx % Dp;
+                ks[c * Dk + d] = (c0 + c < J && d < D) ? kh[(long long)(c0 + c) * D + d] : 0.f;
+            }
         }
         __syncthreads();
+        if (vec && c0 + kRouteCols < J) prefetch(c0 + kRouteCols);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         const float4* q4 = reinterpret_cast<const float4*>(qs + r * Dp);
         for (int d4 = 0; d4 < Dp / 4; ++d4) {

@@ -127,11 +127,99 @@ __global__ void __launch_bounds__(256) pool_kernel(
     }
 }
 
+
+// Pool for rows of exactly 256 bytes (bf16 D=128, fp32 D=64): one warp per
+// (tensor, head, block).  Lane l reads 16-byte chunk (l % 16) of every other
+// row (l / 16 selects the parity), 16 rows in flight per lane; the two
+// halves are added with one shuffle.  The block's token ids are staged in
+// shared memory first, so no row load waits on an index load.
+template <typename T>
+__global__ void __launch_bounds__(256) pool_rows256_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D,
+    const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M, int BH,
+    long long items, float* __restrict__ qbar, float* __restrict__ kbar, float* __restrict__ vbar,
+    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, int* status) {
+    extern __shared__ int toks_all[];  // [8][M]
+    constexpr int VEC = 16 / sizeof(T);
+    constexpr int U = 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long item = (long long)blockIdx.x * 8 + warp;
+    if (item >= items) return;
+    const int j = (int)(item % J);
+    const int bh = (int)((item / J) % BH);
+    const int which = (int)(item / ((long long)J * BH));
+    const T* src = which == 0 ? q : (which == 1 ? k : v);
+    float* dst = which == 0 ? qbar : (which == 1 ? kbar : vbar);
+    T* dst_lp = which == 1 ? kbar_lp : (which == 2 ? vbar_lp : nullptr);
+    const int n = block_sizes[j];
+    int* tk = toks_all + warp * M;
+    for (int r = lane; r < n; r += 32) {
+        int tok = index_map[(long long)j * M + r];
+        if (tok < 0 || tok >= N) {
+            raise_status(status, BSA_ERR_INDEX);
+            tok = -1;
+        }
+        tk[r] = tok;
+    }
+    __syncwarp();
+    const int chunk = lane & 15, half = lane >> 4;
+    const T* base = src + (size_t)bh * N * D + chunk * VEC;
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    for (int r0 = half; r0 < n; r0 += 2 * U) {
+        uint4 raw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int r = r0 + 2 * u;
+            const int tok = r < n ? tk[r] : -1;
+            raw[u] = tok >= 0 ? __ldg(reinterpret_cast<const uint4*>(base + (size_t)tok * D))
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const T* e8 = reinterpret_cast<const T*>(&raw[u]);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+    if (lane < 16) {
+        float mean[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) mean[e] = n > 0 ? acc[e] / (float)n : 0.f;
+        float* out = dst + ((size_t)bh * J + j) * D + chunk * VEC;
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4)
+            *reinterpret_cast<float4*>(out + e) = make_float4(mean[e], mean[e + 1], mean[e + 2], mean[e + 3]);
+        if (dst_lp) {
+            T lp[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) lp[e] = from_f32<T>(mean[e]);
+            *reinterpret_cast<uint4*>(dst_lp + ((size_t)bh * J + j) * D + chunk * VEC) =
+                *reinterpret_cast<const uint4*>(lp);
+        }
+    }
+}
+
 template <typename T>
 static bsa_status launch_pool(const void* q, const void* k, const void* v, int BH, int N, int D,
                               const int32_t* im, const int32_t* bs, int J, int M, float* qbar,
                               float* kbar, float* vbar, void* klp, void* vlp, cudaStream_t st) {
     constexpr int VEC = 16 / sizeof(T);
+    if ((size_t)D * sizeof(T) == 256 && ((uintptr_t)q % 16 == 0) && ((uintptr_t)k % 16 == 0) &&
+        (!v || (uintptr_t)v % 16 == 0)) {
+        const long long items = (long long)(v ? 3 : 2) * BH * J;
+        const long long grid = (items + 7) / 8;
+        const size_t smem = (size_t)8 * M * sizeof(int);
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(pool_rows256_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        pool_rows256_kernel<T><<<(unsigned)grid, 256, smem, st>>>(
+            (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, BH, items, qbar, kbar, vbar, (T*)klp,
+            (T*)vlp, status_word());
+        return check_launch("pool_rows256_kernel");
+    }
     const bool vec_ok = (D % VEC) == 0;
     const int vec = vec_ok ? VEC : 1;
     int vl2 = 1;  // same rounding as the kernel
