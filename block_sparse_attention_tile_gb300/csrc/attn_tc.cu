@@ -62,6 +62,8 @@ constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 16 KB: 128 rows x 64 col
 constexpr uint64_t kWaitNs = 2000000000ull;          // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
 constexpr int kSoftmaxBarrier = 1;                   // named barrier of the 256 softmax threads
+constexpr int kRegsLow = 64, kRegsHigh = 216, kRegsLaunch = 168;  // setmaxnreg split (x 128 / x 256 threads)
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0;
@@ -75,7 +77,7 @@ constexpr uint32_t OFF_XCH = OFF_SEL + 4 * 32;                  // float[3][2 ha
 constexpr uint32_t OFF_SRC = OFF_XCH + 4 * 3 * 2 * kBM;        // int4[kMaxList]: packed tile sources
 constexpr uint32_t OFF_BAR = OFF_SRC + 16 * kMaxList;
 constexpr int BAR_Q = 0, BAR_FULL = 1, BAR_EMPTY = BAR_FULL + kStages, BAR_SF = BAR_EMPTY + kStages,
-              BAR_PF = BAR_SF + 2, BAR_OD = BAR_PF + 2, BAR_OF = BAR_OD + 1, BAR_DRAIN = BAR_OF + 1,
+              BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2, BAR_DRAIN = BAR_OF + 2,
               NBAR = BAR_DRAIN + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;               // tmem base, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;           // + alignment slack
@@ -207,10 +209,10 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(BAR_SF + b), 1);
-            ptx::mbar_init(bar(BAR_PF + b), 2 * kBM);
+            ptx::mbar_init(bar(BAR_PF + b), kBM);
         }
-        ptx::mbar_init(bar(BAR_OD), 1);
         ptx::mbar_init(bar(BAR_OF), 1);
+        ptx::mbar_init(bar(BAR_OF + 1), 1);
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         ptx::fence_mbar_init();
         misc[1] = 0;
@@ -278,7 +280,9 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
     const int n_entries = 2 * n;
 
-    if (warp == 0) {
+    if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
@@ -386,12 +390,11 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-    } else if (warp == 1) {
+      } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kBM, kHD, true);
-            const uint32_t tO = tmem + 256;
             int ec = 0;  // ring entries consumed
             bool ok = wait_bar(bar(BAR_Q), 0, abort_flag, prm.status);
             auto take = [&](uint32_t& addr) -> bool {
@@ -431,12 +434,11 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
                     // V advances by two 8-row groups of 1024 B; the second
                     // 64-column half of V is one leading-dimension step (16 KB) away.
-                    ptx::mma_ts(tO, aP + kk * 8, ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts(tmem + 256 + (uint32_t)(j & 1) * 128, aP + kk * 8,
+                                ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO, (j >= 2 || kk > 0) ? 1u : 0u);
                 }
-                ptx::mma_commit(bar(BAR_OD));
                 release();
-                if (j == n - 1) ptx::mma_commit(bar(BAR_OF));
+                if (j + 2 >= n) ptx::mma_commit(bar(BAR_OF + (j & 1)));  // last product into O_{j&1}
                 return true;
             };
             if (ok) ok = issue_s(0);
@@ -450,87 +452,80 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint64_t t0 = ptx::globaltimer();
             while (!ptx::mbar_try_wait(bar(BAR_DRAIN), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
-    } else if (warp >= 4) {
+      }
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+      {
         // ------------------------------------------------------------ softmax + epilogue
-        const int half = (warp - 4) >> 2;          // key / output columns [64*half, 64*half + 64)
+        // Warpgroup w takes the key tiles s = w, w+2, w+4, ... with its own
+        // running max m, sum l and accumulator O_w; the two partial results
+        // are merged exactly at the end (weights 2^(m_w - max(m_0, m_1))).
+        const int w = (warp - 4) >> 2;
         const int row = threadIdx.x & 127;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        const uint32_t tO = tmem + lane_off + 256 + 64 * half;
+        const uint32_t tOw = tmem + lane_off + 256 + 128 * w;
         float m_ref = -CUDART_INF_F, l = 0.f;
         bool ok = true;
         uint32_t r[32];
-        float x[64];
-        // After an abort a thread keeps looping without touching TMEM, so that
-        // both halves still meet at every named barrier.
-        for (int s = 0; s < n; ++s) {
-            const int b = s & 1;
-            if (ok)
-                ok = __all_sync(0xffffffffu,
-                                wait_bar(bar(BAR_SF + b), (uint32_t)(s >> 1) & 1u, abort_flag, prm.status));
-            const uint32_t tS = tmem + lane_off + (uint32_t)b * 128;
-            if (ok) {
-                ptx::tc_fence_after();
+        float x[kBN];
+        for (int s = w; s < n; s += 2) {
+            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + w), (uint32_t)(s >> 1) & 1u, abort_flag, prm.status));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
+            {
                 uint32_t* xr = reinterpret_cast<uint32_t*>(x);
-                ptx::tmem_ld32(tS + 64 * half, xr);
-                ptx::tmem_ld32(tS + 64 * half + 32, xr + 32);
+                ptx::tmem_ld32(tS + 0, xr + 0);
+                ptx::tmem_ld32(tS + 32, xr + 32);
+                ptx::tmem_ld32(tS + 64, xr + 64);
+                ptx::tmem_ld32(tS + 96, xr + 96);
                 ptx::tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) x[c] = 0.f;
             }
             const int blk = list[s];
             const int nv = nvalid[s];
-            const int c0 = 64 * half;
             float mxp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
-            if (blk >= 0 || nv == 0) {
+            const bool real = blk >= 0 || nv == 0;
+            if (real) {
                 if (nv >= kBN) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+                    for (int c = 0; c < kBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        x[c] = c0 + c < nv ? x[c] : -CUDART_INF_F;
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = c < nv ? x[c] : -CUDART_INF_F;
                         mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
             } else {
-                const float* bt = bias + (-blk - 1) * kBN + c0;
+                const float* bt = bias + (-blk - 1) * kBN;
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
                     mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                 }
             }
-            float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-            // swap the partial row maxima of the two column halves
-            float* xb = xch + (b * 2) * kBM;
-            xb[half * kBM + row] = mx;
-            named_sync(kSoftmaxBarrier, 2 * kBM);
-            mx = fmaxf(mx, xb[(1 - half) * kBM + row]);
+            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             const float m_new = fmaxf(m_ref, mx);
             const bool need = m_new > m_ref + kRescaleThreshold;
             if (__any_sync(0xffffffffu, need)) {
                 const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;  // m_ref = -inf -> 0
                 if (need) m_ref = m_new;
                 l *= alpha;
-                if (s > 0 && ok) {
-                    // O must hold P_0..P_{s-1} V before it is rescaled
-                    ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_OD), (uint32_t)(s - 1) & 1u, abort_flag, prm.status));
-                }
-                if (s > 0 && ok) {
-                    ptx::tc_fence_after();
+                if (s >= 2) {
+                    // S_s was issued after PV_{s-2}, the last product added to O_w,
+                    // so O_w is complete here and can be rescaled in place.
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        ptx::tmem_ld32(tO + c * 32, r);
+                    for (int c = 0; c < 4; ++c) {
+                        ptx::tmem_ld32(tOw + c * 32, r);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        ptx::tmem_st32(tO + c * 32, r);
+                        ptx::tmem_st32(tOw + c * 32, r);
                     }
                     ptx::tmem_wait_st();
                 }
@@ -539,71 +534,93 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int u = 0; u < 8; ++u) sp[u] = 0.f;
             const bool live = m_ref != -CUDART_INF_F;
-            if (blk >= 0 || nv == 0) {
+            if (real) {
                 // x holds raw Q.K: one FMA folds the scale and subtracts the reference
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     x[c] = live ? ptx::ex2(fmaf(x[c], prm.scale_log2, -m_ref)) : 0.f;
                     sp[c & 7] += x[c];
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < kBN; ++c) {
                     x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
                     sp[c & 7] += x[c];
                 }
             }
             l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-            // this half's 64 keys -> packed bf16 columns [32*half, 32*half + 32) over S
-            if (ok) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = ptx::pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                ptx::tmem_st32(tS + 32 * half, r);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(BAR_PF + b));
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r[e] = ptx::pack_bf16x2(x[h * 64 + 2 * e], x[h * 64 + 2 * e + 1]);
+                ptx::tmem_st32(tS + h * 32, r);
             }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(BAR_PF + w));
         }
-        // epilogue: l of the row is the sum of both halves
-        if (ok && n > 0) ok = wait_bar(bar(BAR_OF), 0, abort_flag, prm.status);
+        // epilogue: both partial results are complete, merge them
+        const bool has_tiles = w < n;
+        if (ok && has_tiles) ok = wait_bar(bar(BAR_OF + w), 0, abort_flag, prm.status);
         ok = __all_sync(0xffffffffu, ok);
         ptx::tc_fence_after();
-        float* xl = xch + 4 * kBM;
-        xl[half * kBM + row] = l;
+        float* xm = xch;             // [2][128] running maxima
+        float* xl = xch + 2 * kBM;   // [2][128] sums
+        xm[w * kBM + row] = m_ref;
+        xl[w * kBM + row] = l;
+        // the two warpgroups also meet here after an abort, so the count matches
         named_sync(kSoftmaxBarrier, 2 * kBM);
-        const float l_row = l + xl[(1 - half) * kBM + row];
+        const float m0 = xm[row], m1 = xm[kBM + row];
+        const float M = fmaxf(m0, m1);
+        const float a0 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m0 - M);
+        const float a1 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m1 - M);
+        const float L = xl[row] * a0 + xl[kBM + row] * a1;
+        const bool n1 = n > 1;  // O_1 holds something only with two or more tiles
         const bool write = ok && row < nq;
         int tok = -1;
         if (write) {
             tok = prm.index_map[(long long)qb * kBM + row];
             if (tok < 0 || tok >= prm.N) tok = -1;
         }
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD + 64 * half;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        // warpgroup w writes output columns [64w, 64w + 64)
+        const uint32_t tO0 = tmem + lane_off + 256 + 64 * w, tO1 = tO0 + 128;
+        __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD + 64 * w;
+        uint32_t r1[32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
             if (ok && n > 0) {
-                ptx::tmem_ld32(tO + c * 32, r);
+                ptx::tmem_ld32(tO0 + c * 32, r);
+                if (n1) ptx::tmem_ld32(tO1 + c * 32, r1);
                 ptx::tmem_wait_ld();
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) r[e] = 0u;
             }
+            if (!(ok && n1)) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) r1[e] = 0u;
+            }
             if (write && tok >= 0) {
+                float o[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    o[e] = (__uint_as_float(r[e]) * a0 + __uint_as_float(r1[e]) * a1) * inv;
                 uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16x2(__uint_as_float(r[8 * v4 + 0]) * inv, __uint_as_float(r[8 * v4 + 1]) * inv);
-                    w.y = ptx::pack_bf16x2(__uint_as_float(r[8 * v4 + 2]) * inv, __uint_as_float(r[8 * v4 + 3]) * inv);
-                    w.z = ptx::pack_bf16x2(__uint_as_float(r[8 * v4 + 4]) * inv, __uint_as_float(r[8 * v4 + 5]) * inv);
-                    w.w = ptx::pack_bf16x2(__uint_as_float(r[8 * v4 + 6]) * inv, __uint_as_float(r[8 * v4 + 7]) * inv);
-                    dst[v4] = w;
+                    uint4 q4;
+                    q4.x = ptx::pack_bf16x2(o[8 * v4 + 0], o[8 * v4 + 1]);
+                    q4.y = ptx::pack_bf16x2(o[8 * v4 + 2], o[8 * v4 + 3]);
+                    q4.z = ptx::pack_bf16x2(o[8 * v4 + 4], o[8 * v4 + 5]);
+                    q4.w = ptx::pack_bf16x2(o[8 * v4 + 6], o[8 * v4 + 7]);
+                    dst[v4] = q4;
                 }
             }
         }
-        if (half == 0 && write && tok >= 0 && prm.lse)
-            prm.lse[(long long)bh * prm.N + tok] = l_row > 0.f ? (m_ref + log2f(l_row)) * kLn2 : -CUDART_INF_F;
+        if (w == 0 && write && tok >= 0 && prm.lse)
+            prm.lse[(long long)bh * prm.N + tok] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+      }
     }
 
     ptx::tc_fence_before();
@@ -661,6 +678,20 @@ static bool make_window_map(CUtensorMap* m, const void* video_base, int T, int H
     return r == CUDA_SUCCESS;
 }
 
+// The register split assumes the launch reserves kRegsLaunch registers per
+// thread; refuse the tensor-core path otherwise (setmaxnreg.inc would wait).
+static bool register_split_fits() {
+    static int checked = 0;  // 0 unknown, 1 fits, -1 does not
+    if (!checked) {
+        cudaFuncAttributes a;
+        checked = (cudaFuncGetAttributes(&a, bsa_fwd_tc_kernel) == cudaSuccess &&
+                   a.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh)
+                      ? 1
+                      : -1;
+    }
+    return checked == 1;
+}
+
 }  // namespace tc
 
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
@@ -675,6 +706,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
+    if (!tc::register_split_fits()) return BSA_OK;
     tc::Params prm{};
     CUtensorMap mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5, mkb, mvb;
     const long long rows = (long long)BH * N;
