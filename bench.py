@@ -160,29 +160,28 @@ def run_oracle_sample(budget_s=15.0):
 
 # ---------------------------------------------------------------- GPU arm
 
-def kernel_source_hash():
+def kernel_source_hash(files):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_sparse_attention_tile_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def read_traffic(kernel):
-    """Per-launch DRAM bytes of `kernel` from a committed ncu summary, only if
-    it was taken on the current kernel sources."""
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, only if
+    it was taken on the kernel's current source files."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-    except (OSError, ValueError):
+        e = t[kernel]
+        if e.get("source_hash") != kernel_source_hash(e["source_files"]):
+            return None
+        return e.get("bytes_per_launch")
+    except (OSError, ValueError, KeyError):
         return None
-    e = t.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
-        return None
-    return e.get("bytes_per_launch")
 
 
 def gpu_arm(args):
