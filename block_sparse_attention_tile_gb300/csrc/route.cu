@@ -23,10 +23,13 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// DPC: the padded head dimension when it is known at compile time (0 = any).
+template <int DPC>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
-    const float* __restrict__ qbar, const float* __restrict__ kbar, int J, int D, int Dp,
+    const float* __restrict__ qbar, const float* __restrict__ kbar, int J, int D, int Dp_rt,
     long long head_stride, int k, float scale, int kmax, int32_t* __restrict__ q2k_idx,
     int32_t* __restrict__ q2k_num) {
+    const int Dp = DPC ? DPC : Dp_rt;
     extern __shared__ __align__(16) float smem[];
     float* qs = smem;                              // [kRouteRows][Dp]
     float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp + 4]
@@ -192,10 +195,10 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     const int Dp = (D + 3) / 4 * 4;
     const size_t smem = sizeof(float) * ((size_t)kRouteRows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)kRouteRows * J);
     if (smem > 227 * 1024) return fail(BSA_ERR_UNSUPPORTED, "route: J=%d D=%d needs too much shared memory", J, D);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = Dp == 128 ? route_topk_kernel<128> : (Dp == 64 ? route_topk_kernel<64> : route_topk_kernel<0>);
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid((J + kRouteRows - 1) / kRouteRows, BH);
-    route_topk_kernel<<<grid, kRouteThreads, smem, as_stream(stream)>>>(
-        qbar, kbar, J, D, Dp, (long long)head_stride, k, scale, kmax, q2k_idx, q2k_num);
+    kern<<<grid, kRouteThreads, smem, as_stream(stream)>>>(qbar, kbar, J, D, Dp, (long long)head_stride, k, scale,
+                                                          kmax, q2k_idx, q2k_num);
     return check_launch("route_topk_kernel");
 }
