@@ -1,15 +1,28 @@
 """Benchmark of the block-sparse attention hot path on GB300.
 
-One step = one pass of the whole path over one batch of the video-DiT
-workload: tile map -> mean pool -> route (E + TopK) -> block-sparse
-attention.  B=1, h=24, D=128, token grid (T,H,W)=(30,48,80) (N=115200),
-(4,4,8) blocks of 128 tokens (J=960, the last temporal block row holds 2
-frames), k=96 kept blocks per query block, bf16 inputs, fp32 accumulation.
+One step = one pass of the whole path over one batch of a workload.  The
+default workload (the one the headline line reports) is the video-DiT one:
+tile map -> mean pool -> route (E + TopK) -> block-sparse attention, B=1,
+h=24, D=128, token grid (T,H,W)=(30,48,80) (N=115200), (4,4,8) blocks of 128
+tokens (J=960, the last temporal block row holds 2 frames), k=96 kept blocks
+per query block, bf16 inputs, fp32 accumulation.
+
+Other workloads (--workload):
+  video_tiny     fp32, h=2, D=64, grid (8,16,16), (4,4,4) blocks, k=8
+  nsa_prefill    bf16 GQA selected prefill, B=2, T=8192, HQ=64, H=4, BS=64,
+                 S=16: reverse index -> KV-outer partials -> combine
+                 (the query-outer order is timed beside it)
+  msa_prefill    bf16, B=1, N=32768, Hq=64, Hkv=4, Bk=128, k=16 with
+                 Zipf(1.1) hot blocks: the same KV-outer pipeline
+  spark_summary  bf16, h=24, 1024 text tokens + (16,32,64) video under a
+                 permutation, 128-token blocks, k=26, summaries of the
+                 unselected blocks
 
 Metric: effective sparse-attention TFLOP/s = 4*Hq*N*d*k*B_k / step time
 (the FLOP count of the "MSA ... KV-outer" page, eq. 13/15).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
 
 Prints one JSON line on rank 0.  With --impl reference the CPU oracle is
 timed on the host cores on a bounded sample of the same workload.
@@ -28,14 +41,26 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = dict(name="video_dit_bsa", B=1, heads=24, D=128, grid=(30, 48, 80), block=(4, 4, 8), M=128,
-                k=96, seed=202)
+METRIC = "sparse-attn effective TFLOP/s (4*Hq*N*d*k*Bk/s)"
+
+WORKLOADS = {
+    "video_dit_bsa": dict(kind="block", B=1, heads=24, D=128, grid=(30, 48, 80), block=(4, 4, 8), M=128, k=96,
+                          seed=202, dtype="bf16"),
+    "video_tiny": dict(kind="block", B=1, heads=2, D=64, grid=(8, 16, 16), block=(4, 4, 4), M=64, k=8, seed=101,
+                       dtype="f32"),
+    "spark_summary": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
+                          seed=505, dtype="bf16", n_text=1024, summary=True),
+    "nsa_prefill": dict(kind="token", B=2, T=8192, HQ=64, H=4, D=128, BS=64, S=16, seed=303, zipf=False),
+    "msa_prefill": dict(kind="token", B=1, T=32768, HQ=64, H=4, D=128, BS=128, S=16, seed=404, zipf=True),
+}
+DEFAULT = "video_dit_bsa"
 
 
 def metric_flops(w):
+    if w["kind"] == "token":
+        return 4.0 * w["B"] * w["HQ"] * w["T"] * w["D"] * w["S"] * w["BS"]
     T, H, W = w["grid"]
-    N = T * H * W
-    return 4.0 * w["B"] * w["heads"] * N * w["D"] * w["k"] * w["M"]
+    return 4.0 * w["B"] * w["heads"] * T * H * W * w["D"] * w["k"] * w["M"]
 
 
 def read_peaks():
@@ -104,9 +129,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ---------------------------------------------------------------- CPU oracle sample
+# ---------------------------------------------------------------- CPU oracle samples
 
-ORACLE_SAMPLE = r"""
+ORACLE_BLOCK = r"""
 import json, os, sys, time
 sys.path.insert(0, {root!r})
 import numpy as np, torch
@@ -114,51 +139,105 @@ import oracle
 from block_sparse_attention_tile_gb300 import synthetic
 w = json.loads({w!r})
 budget_s = {budget}
-T, H, W = w["grid"]; bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]
+T, H, W = w["grid"]; bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
+n_text = w.get("n_text", 0); summary = w.get("summary", False)
+dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
 t0 = time.perf_counter()
-q, kk, v = synthetic.video_qkv(1, 1, T, H, W, D, w["seed"], torch.bfloat16, field=True)
+if summary:
+    q, kk, v = synthetic.cluster_qkv(1, n_text, T * H * W, D, w["seed"], dt)
+    perm = synthetic.permutation(T * H * W, w["seed"] + 1)
+    blocks = oracle.tile_prefix(n_text, M) + oracle.tile_permuted(perm, M, offset=n_text)
+else:
+    q, kk, v = synthetic.video_qkv(1, 1, T, H, W, D, w["seed"], dt, field=(w["dtype"] == "bf16"))
+    blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
 Q, K, V = (x[0].float().numpy().astype(np.float64) for x in (q, kk, v))
 gen_s = time.perf_counter() - t0
+P = len(oracle.tile_prefix(n_text, M)) if n_text else 0
 t0 = time.perf_counter()
-blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
 qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
-E = oracle.routing_scores(qbar, kbar, D)
+vbar = oracle.pool_blocks(V, blocks) if summary else None
+E = oracle.routing_scores(qbar[P:], kbar[P:], D)
 idx, num = oracle.route(E, k, k)
 route_s = time.perf_counter() - t0
 rng = np.random.default_rng(0)
 order = rng.permutation(len(blocks))
 t0 = time.perf_counter(); done = 0
 while done < len(order) and (done < 2 or time.perf_counter() - t0 < budget_s):
-    oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=[int(order[done])])
+    qb = [int(order[done])]
+    if summary:
+        oracle.summary_attention(Q, K, V, blocks, idx, num, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
+                                 query_blocks=qb)
+    else:
+        oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb)
     done += 1
 attn_s = time.perf_counter() - t0
 J = len(blocks)
 step_s = w["B"] * w["heads"] * (route_s + J * attn_s / done)
-print(json.dumps(dict(step_s=step_s, blocks=done, J=J, route_s=route_s, attn_s=attn_s, gen_s=gen_s)))
+print(json.dumps(dict(step_s=step_s, units=done, total_units=J, route_s=route_s, attn_s=attn_s, gen_s=gen_s)))
+"""
+
+ORACLE_TOKEN = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np, torch
+import oracle
+from block_sparse_attention_tile_gb300 import synthetic
+w = json.loads({w!r})
+budget_s = {budget}
+B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+t0 = time.perf_counter()
+q = synthetic.normal((1, T, HQ, D), w["seed"], dtype=torch.bfloat16)
+k = synthetic.normal((1, T, H, D), w["seed"] + 1, dtype=torch.bfloat16)
+v = synthetic.normal((1, T, H, D), w["seed"] + 2, dtype=torch.bfloat16)
+gen = synthetic.zipf_block_lists if w["zipf"] else synthetic.causal_block_lists
+idx, cnt = gen(1, T, H, S, BS, w["seed"])
+Qf, Kf, Vf = (x[0].float().numpy().astype(np.float64) for x in (q, k, v))
+gen_s = time.perf_counter() - t0
+nblk = -(-T // BS)
+t0 = time.perf_counter()
+oracle.reverse_index(np.transpose(idx, (0, 2, 1, 3)).reshape(H, T, S), np.transpose(cnt, (0, 2, 1)).reshape(H, T), nblk)
+index_s = time.perf_counter() - t0
+rng = np.random.default_rng(0)
+order = rng.permutation(T)
+t0 = time.perf_counter(); done = 0
+while done < T and (done < 2 or time.perf_counter() - t0 < budget_s):
+    chunk = [int(t) for t in order[done:done + 8]]
+    oracle.nsa_selected_attention(Qf, Kf, Vf, idx[0], cnt[0], BS, tokens=chunk)
+    done += len(chunk)
+attn_s = time.perf_counter() - t0
+step_s = B * (index_s + T * attn_s / done)
+print(json.dumps(dict(step_s=step_s, units=done, total_units=T, route_s=index_s, attn_s=attn_s, gen_s=gen_s)))
 """
 
 
-def run_oracle_sample(budget_s=15.0):
-    """Times the CPU oracle in a fresh interpreter (spawned, never forked)."""
+def run_oracle_sample(wname, budget_s=15.0):
+    """Times the CPU oracle on a bounded sample in a fresh interpreter (spawned, never forked)."""
+    w = WORKLOADS[wname]
     cores = os.cpu_count() or 1
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
-    code = ORACLE_SAMPLE.format(root=ROOT, w=json.dumps(WORKLOAD), budget=budget_s)
+    tmpl = ORACLE_TOKEN if w["kind"] == "token" else ORACLE_BLOCK
+    code = tmpl.format(root=ROOT, w=json.dumps(w), budget=budget_s)
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if out.returncode != 0:
         raise RuntimeError("oracle sample failed:\n" + out.stderr[-2000:])
     r = json.loads(out.stdout.strip().splitlines()[-1])
-    value = metric_flops(WORKLOAD) / r["step_s"] / 1e12
-    sample = ("1 of %d heads: tile map, pool and route of all %d blocks (%.1f s) plus %d of %d query blocks "
-              "attended (%.1f s); step time scaled by heads and blocks"
-              % (WORKLOAD["heads"], r["J"], r["route_s"], r["blocks"], r["J"], r["attn_s"]))
+    value = metric_flops(w) / r["step_s"] / 1e12
+    if w["kind"] == "token":
+        sample = ("batch element 0 of %d: reverse index of all %d tokens (%.1f s) plus %d of %d query tokens "
+                  "attended, all %d heads (%.1f s); step time scaled by tokens and batch"
+                  % (w["B"], w["T"], r["route_s"], r["units"], r["total_units"], w["HQ"], r["attn_s"]))
+    else:
+        sample = ("1 of %d heads: tile map, pool and route of all %d blocks (%.1f s) plus %d of %d query blocks "
+                  "attended (%.1f s); step time scaled by heads and blocks"
+                  % (w["heads"], r["total_units"], r["route_s"], r["units"], r["total_units"], r["attn_s"]))
     return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
             "step_s_extrapolated": r["step_s"]}
 
 
-# ---------------------------------------------------------------- GPU arm
+# ---------------------------------------------------------------- traffic records
 
 def kernel_source_hash(files):
     h = hashlib.sha256()
@@ -184,11 +263,300 @@ def read_traffic(kernel):
         return None
 
 
+# ---------------------------------------------------------------- workloads
+
+class BlockWorkload:
+    """Tile map -> pool -> route -> block attention (exact, or exact + summary)."""
+
+    stage_names = ["tile_map", "pool", "route", "attention"]
+
+    def __init__(self, name, w, dev, rank):
+        import torch
+        from block_sparse_attention_tile_gb300 import pipeline, synthetic
+        self.name, self.w, self.dev = name, w, dev
+        self.torch = torch
+        T, H, W = w["grid"]
+        self.summary = w.get("summary", False)
+        n_text = w.get("n_text", 0)
+        D, M, k = w["D"], w["M"], w["k"]
+        self.BH = w["B"] * w["heads"]
+        self.dtype = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+        seed = w["seed"] + 1000 * rank
+        with torch.no_grad():
+            if self.summary:
+                self.q, self.k, self.v = synthetic.cluster_qkv(self.BH, n_text, T * H * W, D, seed, self.dtype,
+                                                               device=dev)
+                self.perm = torch.as_tensor(synthetic.permutation(T * H * W, seed + 1), device=dev)
+            else:
+                self.q, self.k, self.v = synthetic.video_qkv(w["B"], w["heads"], T, H, W, D, seed, self.dtype,
+                                                             device=dev, field=(w["dtype"] == "bf16"))
+                self.perm = None
+        self.geom = pipeline.Geometry(T, H, W, *w["block"], M=M, n_prefix=n_text, perm=self.perm)
+        self.N = self.geom.n_tokens
+        self.J = self.geom.num_blocks
+        self.P = self.geom.prefix_blocks
+        self.Jr = self.J - self.P
+        self.scale = D ** -0.5
+        BH, J = self.BH, self.J
+        self.im = torch.empty((J, M), dtype=torch.int32, device=dev)
+        self.bs = torch.empty((J,), dtype=torch.int32, device=dev)
+        self.qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
+        self.kbar = torch.empty_like(self.qbar)
+        self.vbar = torch.empty_like(self.qbar) if self.summary else None
+        self.kbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
+        self.vbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
+        self.q2k = torch.empty((BH, self.Jr, k), dtype=torch.int32, device=dev)
+        self.q2n = torch.empty((BH, self.Jr), dtype=torch.int32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((BH, self.N), dtype=torch.float32, device=dev)
+        self.launches_per_step = 4
+
+    def step(self, ev=None, q=None, k=None, v=None):
+        from block_sparse_attention_tile_gb300 import bsa
+        w, g = self.w, self.geom
+        q = self.q if q is None else q
+        k = self.k if k is None else k
+        v = self.v if v is None else v
+        D, M, kk = w["D"], w["M"], w["k"]
+        st = self.torch.cuda.current_stream()
+        if ev: ev[0].record(st)
+        bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, M, self.im, self.bs)
+        if ev: ev[1].record(st)
+        bsa.bsa_pool_blocks(q, k, v if self.summary else None, self.BH, self.N, D, self.im, self.bs, self.J, M,
+                            self.qbar, self.kbar, self.vbar, self.kbar_lp, self.vbar_lp)
+        if ev: ev[2].record(st)
+        bsa.bsa_route_topk(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.Jr, D, self.J * D, kk,
+                           self.scale, kk, self.q2k, self.q2n)
+        if ev: ev[3].record(st)
+        if self.summary:
+            bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
+                                self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.out, self.lse)
+        else:
+            bsa.bsa_fwd_qouter(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
+                               self.q2k, self.q2n, kk, self.scale, self.out, self.lse)
+        if ev: ev[4].record(st)
+
+    def host_inputs(self):
+        return [self.q, self.k, self.v], [self.out]
+
+    def run_with(self, dev_inputs):
+        self.step(None, *dev_inputs)
+
+    def algorithmic(self):
+        """Valid (query, key) pairs the attention scores, x 4*D FLOPs."""
+        torch = self.torch
+        sizes = self.bs.long()
+        routed = sizes[self.P:]
+        sel = routed[self.q2k.long().clamp(min=0)] * (self.q2k >= 0)       # [BH, Jr, k]
+        keys = sel.sum(-1)                                                   # [BH, Jr]
+        prefix_keys = sizes[:self.P].sum()
+        if self.summary:
+            keys = keys + prefix_keys + (self.Jr - self.q2n.long())          # one virtual key per unselected block
+        else:
+            keys = keys + prefix_keys
+        pairs = (routed[None, :] * keys).sum() + self.BH * sizes[:self.P].sum() * self.N
+        flops = 4.0 * self.w["D"] * float(pairs.item())
+        pool_bytes = ((3 if self.summary else 2) * self.BH * self.N * self.w["D"] * self.q.element_size()
+                      + (3 if self.summary else 2) * self.BH * self.J * self.w["D"] * 4
+                      + (2 * self.BH * self.J * self.w["D"] * self.q.element_size() if self.summary else 0)
+                      + self.J * self.w["M"] * 4 + self.J * 4)
+        return flops, pool_bytes
+
+    def report(self, stage_ms, peaks, peak_kind, props):
+        flops, pool_bytes = self.algorithmic()
+        D, J = self.w["D"], self.J
+        attn_s = stage_ms["attention"] * 1e-3
+        if self.w["dtype"] == "bf16":
+            peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+            roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "peak_kind": peak_kind + " bf16 sustained"}
+        else:
+            peak = fp32_peak(peaks, props)
+            roof = {"bound": "alu", "achieved": flops / attn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                    "peak_kind": "FP32 lanes: SMs x 128 x 2 x max SM clock"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = read_traffic("attention") if self.name == DEFAULT else None
+        roof["kernel"] = "bsa_fwd_summary attention" if self.summary else "bsa_fwd_qouter attention"
+        roof["algorithmic_flops_per_launch"] = flops
+        pool_gbs = pool_bytes / (stage_ms["pool"] * 1e-3) / 1e9
+        rflops = 2.0 * self.BH * self.Jr * self.Jr * D
+        route_tf = rflops / (stage_ms["route"] * 1e-3) / 1e12
+        fp32 = fp32_peak(peaks, props)
+        secondary = {
+            "pool": {"bound": "hbm", "achieved": pool_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
+            "route": {"bound": "alu", "achieved": route_tf, "peak": fp32, "unit": "TFLOP/s", "frac": route_tf / fp32,
+                      "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}}
+        T, H, W = self.w["grid"]
+        config = {"workload": self.name, "B": self.w["B"], "heads": self.w["heads"], "D": D, "seq_len": self.N,
+                  "grid": [T, H, W], "block": list(self.w["block"]), "M": self.w["M"], "J": J, "k": self.w["k"]}
+        if self.summary:
+            config.update({"n_text": self.w["n_text"], "permuted": True, "summary": True})
+        nbytes = 3 * self.q.numel() * self.q.element_size()
+        config["l2"] = ("inputs larger than L2: Q,K,V = %.2f GB per step" % (nbytes / 1e9) if nbytes > 129e6 else
+                        "inputs smaller than L2 (%.1f MB): L2 not flushed, launch-bound tiny case" % (nbytes / 1e6))
+        data = ("synthetic (seeded N(0,1) + per-head low-rank clusters; no dataset or weights)" if self.summary else
+                "synthetic (seeded N(0,1)%s; no dataset or weights)"
+                % (" + smooth space-time field on Q/K" if self.w["dtype"] == "bf16" else ""))
+        return roof, secondary, config, data, self.w["dtype"]
+
+
+class TokenWorkload:
+    """GQA selected attention with supplied block lists: reverse index ->
+    KV-outer partials -> combine (the query-outer order timed beside it)."""
+
+    stage_names = ["reverse_index", "partials", "combine"]
+
+    def __init__(self, name, w, dev, rank):
+        import numpy as np
+        import torch
+        from block_sparse_attention_tile_gb300 import bsa, synthetic
+        self.name, self.w, self.dev, self.torch, self.np = name, w, dev, torch, np
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        seed = w["seed"] + 1000 * rank
+        self.q = synthetic.normal((B, T, HQ, D), seed, device=dev, dtype=torch.bfloat16)
+        self.k = synthetic.normal((B, T, H, D), seed + 1, device=dev, dtype=torch.bfloat16)
+        self.v = synthetic.normal((B, T, H, D), seed + 2, device=dev, dtype=torch.bfloat16)
+        gen = synthetic.zipf_block_lists if w["zipf"] else synthetic.causal_block_lists
+        self.idx_h, self.cnt_h = gen(B, T, H, S, BS, seed)
+        self.idx = torch.as_tensor(self.idx_h, device=dev)
+        self.cnt = torch.as_tensor(self.cnt_h, device=dev)
+        self.nblk = -(-T // BS)
+        self.cap = 2 * S * BS
+        self.max_chunks = bsa.bsa_max_chunks(B, T, H, S, self.nblk, self.cap)
+        self.row_ptr = torch.empty((B * H * self.nblk + 1,), dtype=torch.int32, device=dev)
+        self.q_idx = torch.empty((B * H * T * S,), dtype=torch.int32, device=dev)
+        self.slot = torch.empty_like(self.q_idx)
+        self.chunks = torch.empty((self.max_chunks, 4), dtype=torch.int32, device=dev)
+        self.n_chunks = torch.empty((1,), dtype=torch.int32, device=dev)
+        self.ws = torch.empty((max(16, bsa.bsa_reverse_index_workspace(B, T, H, self.nblk)),), dtype=torch.uint8,
+                              device=dev)
+        self.obuf = torch.empty((B, T, HQ, S, D), dtype=torch.bfloat16, device=dev)
+        self.lsebuf = torch.empty((B, T, HQ, S), dtype=torch.float32, device=dev)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((B, T, HQ), dtype=torch.float32, device=dev)
+        self.out_q = torch.empty_like(self.q)
+        self.lse_q = torch.empty_like(self.lse)
+        self.scale = D ** -0.5
+        self.launches_per_step = 5
+
+    def step(self, ev=None, q=None, k=None, v=None, idx=None, cnt=None):
+        from block_sparse_attention_tile_gb300 import bsa
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        q = self.q if q is None else q
+        k = self.k if k is None else k
+        v = self.v if v is None else v
+        idx = self.idx if idx is None else idx
+        cnt = self.cnt if cnt is None else cnt
+        st = self.torch.cuda.current_stream()
+        if ev: ev[0].record(st)
+        bsa.bsa_build_reverse_index(idx, cnt, B, T, H, S, self.nblk, self.cap, self.row_ptr, self.q_idx, self.slot,
+                                    self.chunks, self.n_chunks, self.max_chunks, self.ws)
+        if ev: ev[1].record(st)
+        bsa.bsa_fwd_kvouter(q, k, v, B, T, HQ, H, D, self.row_ptr, self.q_idx, self.slot, self.chunks,
+                            self.n_chunks, self.max_chunks, self.nblk, BS, S, True, self.scale, self.obuf,
+                            self.lsebuf)
+        if ev: ev[2].record(st)
+        bsa.bsa_combine(self.obuf, self.lsebuf, cnt, B, T, HQ, H, S, D, self.out, self.lse)
+        if ev: ev[3].record(st)
+
+    def qouter(self):
+        from block_sparse_attention_tile_gb300 import bsa
+        w = self.w
+        bsa.bsa_fwd_qouter_tokens(self.q, self.k, self.v, w["B"], w["T"], w["HQ"], w["H"], w["D"], self.idx,
+                                  self.cnt, w["S"], w["BS"], True, self.scale, self.out_q, self.lse_q)
+
+    def host_inputs(self):
+        return [self.q, self.k, self.v, self.idx, self.cnt], [self.out]
+
+    def run_with(self, dev_inputs):
+        self.step(None, *dev_inputs)
+
+    def algorithmic(self):
+        """Visible (query head, key) pairs (causal) x 4*D FLOPs; nnz entries; bytes of the
+        KV-outer partial pass under the page's I/O model (eq. 16): per entry the G query
+        rows in, the G partial rows and LSEs out; per chunk one K/V block."""
+        np = self.np
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        G = HQ // H
+        t = np.arange(T)[None, :, None, None]
+        slot_ok = np.arange(S)[None, None, None, :] < self.cnt_h[..., None]
+        first = self.idx_h.astype(np.int64) * BS
+        vis = np.clip(np.minimum(t - first + 1, T - first), 0, BS) * slot_ok * (self.idx_h >= 0)
+        pairs = float(vis.sum()) * G
+        nnz = int(self.cnt_h.sum())
+        nch = int(self.n_chunks.item())
+        k1_bytes = nnz * G * (2 * D * 2 + 4) + nch * 2 * BS * D * 2
+        return 4.0 * D * pairs, nnz, k1_bytes
+
+    def report(self, stage_ms, peaks, peak_kind, props):
+        torch = self.torch
+        flops, nnz, k1_bytes = self.algorithmic()
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        k1_s = stage_ms["partials"] * 1e-3
+        tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        t_flop = flops / (tensor_peak * 1e12)
+        t_byte = k1_bytes / (peaks["hbm_gbs"] * 1e9)
+        if t_byte >= t_flop:
+            ach = k1_bytes / k1_s / 1e9
+            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "peak_kind": peak_kind + " HBM copy", "algorithmic_bytes_per_launch": k1_bytes}
+        else:
+            ach = flops / k1_s / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                    "peak_kind": peak_kind + " bf16 sustained"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = None
+        roof["kernel"] = "bsa_fwd_kvouter partials (K1)"
+        roof["algorithmic_flops_per_launch"] = flops
+        # combine: reads every written partial (bf16) + LSE, writes O (bf16) + LSE
+        cb_bytes = nnz * (HQ // H) * (D * 2 + 4) + B * T * HQ * (D * 2 + 4) + B * T * H * 4
+        cb_gbs = cb_bytes / (stage_ms["combine"] * 1e-3) / 1e9
+        # the query-outer order on the same inputs
+        for _ in range(2):
+            self.qouter()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(3):
+            self.qouter()
+        e1.record()
+        torch.cuda.synchronize()
+        q_ms = e0.elapsed_time(e1) / 3
+        compulsory = (self.q.numel() + self.k.numel() + self.v.numel() + self.out.numel()) * 2 + \
+            self.idx.numel() * 4 + self.cnt.numel() * 4
+        step_ms = sum(stage_ms.values())
+        ideal = max(flops / (tensor_peak * 1e12), compulsory / (peaks["hbm_gbs"] * 1e9))
+        secondary = {
+            "combine": {"bound": "hbm", "achieved": cb_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": cb_gbs / peaks["hbm_gbs"], "bytes_per_launch": cb_bytes},
+            "strict_step": {"ideal_ms": ideal * 1e3, "step_ms": step_ms, "frac": ideal * 1e3 / step_ms,
+                            "note": "ideal = max(algorithmic FLOP / bf16 peak, compulsory Q,K,V,O,index bytes / "
+                                    "HBM peak)"},
+            "qouter_order": {"ms": q_ms, "effective_tflops": metric_flops(w) / (q_ms * 1e-3) / 1e12,
+                             "kernel": "bsa_fwd_qouter_tokens"}}
+        config = {"workload": self.name, "B": B, "T": T, "HQ": HQ, "H": H, "D": D, "block_size": BS, "S": S,
+                  "selection": "zipf(1.1) sink+own" if w["zipf"] else "causal uniform, counts U{1..S}",
+                  "chunk_cap": self.cap, "nnz": nnz, "n_chunks": int(self.n_chunks.item()), "order": "kv-outer",
+                  "l2": "inputs larger than L2: Q,K,V = %.2f GB per step"
+                        % ((self.q.numel() + self.k.numel() + self.v.numel()) * 2 / 1e9)}
+        return roof, secondary, config, "synthetic (seeded N(0,1); no dataset or weights)", "bf16"
+
+
+def fp32_peak(peaks, props):
+    return props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
+# ---------------------------------------------------------------- GPU arm
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
 
-    from block_sparse_attention_tile_gb300 import bsa, pipeline, synthetic
+    from block_sparse_attention_tile_gb300 import bsa
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -197,57 +565,24 @@ def gpu_arm(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = dict(WORKLOAD)
+    w = dict(WORKLOADS[args.workload])
+    name = args.workload
     if args.heads:
+        if w["kind"] != "block":
+            raise SystemExit("--heads applies to the block workloads")
         w["heads"] = args.heads
-        w["name"] = WORKLOAD["name"] + "_%dheads" % args.heads
-    T, H, W = w["grid"]
-    N = T * H * W
-    BH, D, M, k = w["B"] * w["heads"], w["D"], w["M"], w["k"]
-
-    # inputs resident in HBM (seeded generator on the device; per-rank seed)
-    with torch.no_grad():
-        q, kk, v = synthetic.video_qkv(w["B"], w["heads"], T, H, W, D, w["seed"] + 1000 * rank,
-                                       torch.bfloat16, device=dev, field=True)
-    geom = pipeline.Geometry(T, H, W, *w["block"], M=M)
-    geo = geom.geometry
-    J = geom.num_blocks
-    scale = D ** -0.5
-    im = torch.empty((J, M), dtype=torch.int32, device=dev)
-    bs = torch.empty((J,), dtype=torch.int32, device=dev)
-    qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
-    kbar = torch.empty_like(qbar)
-    q2k = torch.empty((BH, J, k), dtype=torch.int32, device=dev)
-    q2n = torch.empty((BH, J), dtype=torch.int32, device=dev)
-    out = torch.empty_like(q)
-    lse = torch.empty((BH, N), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(ev=None):
-        if ev: ev[0].record(stream)
-        bsa.bsa_tile_map(T, H, W, *w["block"], 0, None, M, im, bs)
-        if ev: ev[1].record(stream)
-        bsa.bsa_pool_blocks(q, kk, None, BH, N, D, im, bs, J, M, qbar, kbar)
-        if ev: ev[2].record(stream)
-        bsa.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, scale, k, q2k, q2n)
-        if ev: ev[3].record(stream)
-        bsa.bsa_fwd_qouter(q, kk, v, BH, N, D, im, bs, J, M, 0, geo, q2k, q2n, k, scale, out, lse)
-        if ev: ev[4].record(stream)
+        name = name + "_%dheads" % args.heads
+    wl = (TokenWorkload if w["kind"] == "token" else BlockWorkload)(name, w, dev, rank)
+    nst = len(wl.stage_names)
 
     for _ in range(args.warmup):
-        step()
+        wl.step()
     torch.cuda.synchronize()
     if bsa.bsa_device_status() != bsa.BSA_OK:
         raise RuntimeError("device status after warm-up: " + bsa.bsa_last_error())
 
-    # algorithmic work of one attention launch: 4*D per valid (query, key) pair
-    sizes = bs.long()
-    sel_sizes = sizes[q2k.long()].sum(-1)                        # [BH, J] keys visited
-    pairs = (sizes[None, :] * sel_sizes).sum().item()
-    attn_flops = 4.0 * D * pairs
-    pool_bytes = 2 * BH * N * D * 2 + 2 * BH * J * D * 4 + J * M * 4 + J * 4
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -258,32 +593,32 @@ def gpu_arm(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(ev[i])
+        wl.step(ev[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    stage_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
-                for j, name in enumerate(["tile_map", "pool", "route", "attention"])}
+    stage_ms = {sn: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, sn in enumerate(wl.stage_names)}
     if bsa.bsa_device_status() != bsa.BSA_OK:
         raise RuntimeError("device status after timing: " + bsa.bsa_last_error())
 
-    # end to end through the public API with host buffers
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, kk, v))
-    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(kk), torch.empty_like(v)
+    # end to end through the public API with host buffers: pinned inputs in,
+    # the result out, every step
+    ins, outs = wl.host_inputs()
+    h_in = [x.cpu().pin_memory() for x in ins]
+    d_in = [torch.empty_like(x) for x in ins]
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in ins)
+    d2h = sum(x.numel() * x.element_size() for x in outs)
 
     def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        bsa.bsa_tile_map(T, H, W, *w["block"], 0, None, M, im, bs)
-        bsa.bsa_pool_blocks(dq, dk, None, BH, N, D, im, bs, J, M, qbar, kbar)
-        bsa.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, scale, k, q2k, q2n)
-        bsa.bsa_fwd_qouter(dq, dk, dv, BH, N, D, im, bs, J, M, 0, geo, q2k, q2n, k, scale, out, lse)
-        hout.copy_(out, non_blocking=True)
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        wl.run_with(d_in)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -307,15 +642,13 @@ def gpu_arm(args):
 
     if rank == 0:
         peaks, peak_kind = read_peaks()
-        flops = metric_flops(w)
-        tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        attn_tflops = attn_flops / (stage_ms["attention"] * 1e-3) / 1e12
-        pool_gbs = pool_bytes / (stage_ms["pool"] * 1e-3) / 1e9
         props = torch.cuda.get_device_properties(dev)
-        fp32_peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        route_tflops = 2.0 * BH * J * J * D / (stage_ms["route"] * 1e-3) / 1e12
+        roof, secondary, config, data, dtype = wl.report(stage_ms, peaks, peak_kind, props)
+        flops = metric_flops(w)
+        config.update({"global_batch": w["B"] * world,
+                       "parallelism": "replicas%d" % world if world > 1 else "single"})
         line = {
-            "metric": "sparse-attn effective TFLOP/s (4*Hq*N*d*k*Bk/s)",
+            "metric": METRIC,
             "value": world * flops / (ms_step * 1e-3) / 1e12,
             "unit": "TFLOP/s",
             "n_gpus": world,
@@ -325,32 +658,20 @@ def gpu_arm(args):
             "higher_is_better": True,
             "scaling": "weak" if world > 1 else "none",
             "vs_baseline": None,
-            "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) + smooth space-time field on Q/K; no dataset or weights)",
-            "config": {"workload": w["name"], "B": w["B"], "heads": w["heads"], "D": w["D"], "seq_len": N,
-                       "grid": list(w["grid"]), "block": list(w["block"]), "J": J, "k": k,
-                       "global_batch": w["B"] * world, "parallelism": "replicas%d" % world if world > 1 else "single",
-                       "l2": "inputs larger than L2: Q,K,V = %.2f GB per step" % (3 * q.numel() * 2 / 1e9)},
-            "stages_us": {kname: round(v * 1e3, 1) for kname, v in stage_ms.items()},
-            "roofline": {"bound": "tensor", "achieved": attn_tflops, "peak": tensor_peak, "unit": "TFLOP/s",
-                         "frac": attn_tflops / tensor_peak, "traffic": read_traffic("attention"),
-                         "kernel": "bsa_fwd_qouter attention", "peak_kind": peak_kind + " bf16 sustained",
-                         "algorithmic_flops_per_launch": attn_flops},
-            "rooflines_secondary": {
-                "pool": {"bound": "hbm", "achieved": pool_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
-                "route": {"bound": "alu", "achieved": route_tflops, "peak": fp32_peak, "unit": "TFLOP/s",
-                          "frac": route_tflops / fp32_peak, "flops_per_launch": 2.0 * BH * J * J * D,
-                          "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}},
+            "dtype": dtype,
+            "data": data,
+            "config": config,
+            "stages_us": {sn: round(v * 1e3, 1) for sn, v in stage_ms.items()},
+            "roofline": roof,
+            "rooflines_secondary": secondary,
             "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
-                    "ms_per_step": e2e_ms},
-            "gpu_launches": 4 * args.steps,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": wl.launches_per_step * args.steps,
             "clocks": clk,
         }
         if not args.no_cpu_baseline and world == 1:
             try:
-                line["cpu_baseline"] = run_oracle_sample(args.cpu_budget)
+                line["cpu_baseline"] = run_oracle_sample(args.workload, args.cpu_budget)
             except Exception as exc:  # noqa: BLE001
                 line["cpu_baseline"] = {"value": None, "error": str(exc)[:300]}
         print(json.dumps(line), flush=True)
@@ -362,20 +683,27 @@ def reference_arm(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    w = WORKLOADS[args.workload]
     steps = []
     cb = None
     for i in range(args.warmup + args.steps):
-        cb = run_oracle_sample(max(2.0, args.cpu_budget / 3))
+        cb = run_oracle_sample(args.workload, max(2.0, args.cpu_budget / 3))
         if i >= args.warmup:
             steps.append(cb["step_s_extrapolated"])
     step_s = statistics.mean(steps)
-    value = metric_flops(WORKLOAD) / step_s / 1e12
-    line = {"impl": "reference", "metric": "sparse-attn effective TFLOP/s (4*Hq*N*d*k*Bk/s)",
+    value = metric_flops(w) / step_s / 1e12
+    if w["kind"] == "token":
+        cfg = {"workload": args.workload, "B": w["B"], "T": w["T"], "HQ": w["HQ"], "H": w["H"], "D": w["D"],
+               "block_size": w["BS"], "S": w["S"]}
+    else:
+        T, H, W = w["grid"]
+        cfg = {"workload": args.workload, "seq_len": T * H * W + w.get("n_text", 0), "heads": w["heads"],
+               "D": w["D"], "k": w["k"]}
+    line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "none", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD["name"], "seq_len": 115200,
-                                            "heads": 24, "D": 128, "k": 96},
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -388,10 +716,11 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
-                    help="fewer heads than the workload's 24 (a small case for profiler captures)")
+                    help="fewer heads than the workload's (a small case for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

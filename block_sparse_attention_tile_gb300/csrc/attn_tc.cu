@@ -772,11 +772,4 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     return check_launch("bsa_fwd_tc_kernel");
 }
 
-bsa_status kvouter_tc(const void*, const void*, const void*, int, int, int, int, int, const int32_t*,
-                      const int32_t*, const int32_t*, const int32_t*, const int32_t*, int, int, int, int,
-                      int, float, void*, float*, cudaStream_t, bool* handled) {
-    *handled = false;
-    return BSA_OK;
-}
-
 }  // namespace bsa

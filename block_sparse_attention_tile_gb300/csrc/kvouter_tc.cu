@@ -1,0 +1,562 @@
+// a6 on the tensor cores: the KV-outer partial pass (K1), bf16 inputs, D = 128,
+// key blocks of 64 or 128 tokens, G = HQ / H query heads per KV head with G a
+// power of two in [8, 128]; partial outputs in bf16.
+//
+// Semantics: "MSA 为什么采用 KV-outer Sparse Attention Forward" §4 (a KV block
+// is loaded once and every query that selected it is scored against it in
+// one larger product; the G heads of a query position share the KV head, so
+// 128 / G positions fill the 128 rows of one MMA), §6.1 (per slot:
+// L_s = log-sum-exp of the block's visible logits, O_s = the softmax-weighted
+// sum of its values), §7 (hot rows cut into chunks; slots are preassigned,
+// so partial outputs never collide and nothing is accumulated atomically).
+//
+// Design (ours, for sm_103a).  A persistent grid of one CTA per SM.  The
+// chunk list covers the CSR entry space [0, nnz) in order (an entry is one
+// (row, query position) pair); CTA i takes the i-th equal share of it, so
+// every CTA does the same number of (position, block) products and loads a
+// K/V block again only where its share crosses into the next chunk.
+//   warp 0     producer: per chunk segment, K and V of the block (one 3-D TMA
+//              box of BS rows per 64-column half); per sub-tile of up to
+//              128 / G positions, one box of the G heads per position and
+//              half, into a Q ring (128-byte swizzled K-major rows, so the
+//              boxes of consecutive positions form one 128-row MMA operand).
+//   warp 1     TMEM owner and single-thread MMA issuer: S_j = Q_j K^T into
+//              S[j&1]; once the softmax wrote P_j over S_j (packed bf16),
+//              O[j&1] = P_j V with V as an MN-major operand.
+//   warps 4-7 / 8-11   sub-tiles of even / odd index: softmax over the
+//              block's visible keys (a prefix of the tile: key < N and, when
+//              causal, key <= the query position), then the epilogue:
+//              O / l in bf16 and L = ln-sum-exp written straight to the
+//              (position, head, slot) rows of the partial buffers.
+// A sub-tile meets exactly one key tile, so the softmax needs no running
+// rescale.  Every mbarrier wait is bounded (2 s); on expiry the CTA raises
+// BSA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace bsa {
+namespace kvtc {
+
+constexpr int kRows = 128;  // MMA rows per sub-tile
+constexpr int kHD = 128;    // head dim
+constexpr int kThreads = 384;
+constexpr uint64_t kWaitNs = 2000000000ull;
+// No register split: every role fits the 168 registers a thread gets at
+// 384 threads per SM (the softmax holds one 128-key row of S at a time).
+
+template <int BS>
+struct Cfg {
+    static constexpr int kQStages = BS == 64 ? 5 : 4;
+    static constexpr uint32_t kQBytes = kRows * kHD * 2;  // 32 KB
+    static constexpr uint32_t kQHalf = kQBytes / 2;       // 128 rows x 64 columns
+    static constexpr uint32_t kKVHalf = BS * 128;         // BS rows x 64 columns
+    static constexpr uint32_t kKVBytes = 2 * kKVHalf;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + kQStages * kQBytes;
+    static constexpr uint32_t OFF_V = OFF_K + kKVBytes;
+    static constexpr uint32_t OFF_BAR = OFF_V + kKVBytes;
+    static constexpr int BAR_KVF = 0, BAR_KVE = 1, BAR_QF = 2, BAR_QE = BAR_QF + kQStages,
+                         BAR_SF = BAR_QE + kQStages, BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2,
+                         BAR_OE = BAR_OF + 2, BAR_DRAIN = BAR_OE + 2, NBAR = BAR_DRAIN + 1;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;  // tmem base, abort flag
+    static constexpr uint32_t SMEM = OFF_MISC + 32 + 1024;    // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+struct Params {
+    const int32_t* q_idx;
+    const int32_t* slot;
+    const int32_t* chunks;
+    const int32_t* n_chunks;
+    __nv_bfloat16* obuf;
+    float* lsebuf;
+    int* status;
+    int N, HQ, H, G, S, nblk, causal, rows_total, max_chunks;
+    long long max_entries;  // capacity of q_idx / slot: B*H*N*S
+    float scale_log2;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > kWaitNs) {
+            *abort_flag = 1;
+            raise_status(status, BSA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// This CTA's share [lo, hi) of the entry space and the chunk holding lo.
+struct Share {
+    int lo, hi, c0, nch;
+};
+
+__device__ __forceinline__ Share cta_share(const Params& p) {
+    Share s{0, 0, 0, 0};
+    const int nch = min(*p.n_chunks, p.max_chunks);
+    if (nch <= 0) return s;
+    const long long nnz = (long long)p.chunks[4 * (nch - 1) + 1] + p.chunks[4 * (nch - 1) + 2];
+    if (nnz <= 0) return s;
+    if (nnz > p.max_entries) {  // more entries than q_idx / slot can hold
+        raise_status(p.status, BSA_ERR_INDEX);
+        return s;
+    }
+    s.nch = nch;
+    s.lo = (int)(nnz * blockIdx.x / gridDim.x);
+    s.hi = (int)(nnz * (blockIdx.x + 1) / gridDim.x);
+    int a = 0, b = nch - 1;  // last chunk whose start is <= lo
+    while (a < b) {
+        const int m = (a + b + 1) >> 1;
+        if (p.chunks[4 * m + 1] <= s.lo) a = m;
+        else b = m - 1;
+    }
+    s.c0 = a;
+    return s;
+}
+
+// Walks this CTA's share one sub-tile (up to PT consecutive entries of one
+// chunk) at a time.  Every role runs its own cursor over the same list, so
+// all of them see the same sub-tiles and stop at the same place.
+struct Cursor {
+    int c, nch, lo, hi;  // next chunk to open, chunk count, share [lo, hi)
+    int e, end;          // next entry of the open segment and its end
+    int row;
+    long long prev_end;
+};
+
+__device__ __forceinline__ Cursor cursor_begin(const Share& sh) {
+    Cursor cu;
+    cu.c = sh.c0;
+    cu.nch = sh.nch;
+    cu.lo = sh.lo;
+    cu.hi = sh.hi;
+    cu.e = 0;
+    cu.end = 0;
+    cu.row = 0;
+    cu.prev_end = -1;
+    return cu;
+}
+
+// 1: the next sub-tile is (row, e0, np); new_seg says it opens a chunk
+// segment (a new K/V block).  0: the share is done.  -1: the chunk list does
+// not tile the entry space in order (BSA_ERR_INDEX raised).
+__device__ __forceinline__ int cursor_next(const Params& p, Cursor& cu, int PT, int& row, int& e0, int& np,
+                                           bool& new_seg) {
+    new_seg = false;
+    while (cu.e >= cu.end) {
+        if (cu.c >= cu.nch) return 0;
+        const int r = p.chunks[4 * cu.c], start = p.chunks[4 * cu.c + 1], len = p.chunks[4 * cu.c + 2];
+        if (start >= cu.hi) return 0;
+        if ((cu.prev_end >= 0 && start != cu.prev_end) || len < 0 || r < 0 || r >= p.rows_total) {
+            raise_status(p.status, BSA_ERR_INDEX);
+            return -1;
+        }
+        cu.prev_end = (long long)start + len;
+        cu.e = max(cu.lo, start);
+        cu.end = (int)min((long long)cu.hi, cu.prev_end);
+        cu.row = r;
+        ++cu.c;
+        new_seg = true;
+    }
+    row = cu.row;
+    e0 = cu.e;
+    np = min(PT, cu.end - cu.e);
+    cu.e += np;
+    return 1;
+}
+
+template <int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const Params prm) {
+    using C = Cfg<BS>;
+    constexpr int QS = C::kQStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    const uint32_t bar0 = base + C::OFF_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = prm.G, PT = kRows / G;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(C::BAR_KVF), 1);
+        ptx::mbar_init(bar(C::BAR_KVE), 1);
+        for (int s = 0; s < QS; ++s) {
+            ptx::mbar_init(bar(C::BAR_QF + s), 1);
+            ptx::mbar_init(bar(C::BAR_QE + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(C::BAR_SF + b), 1);
+            ptx::mbar_init(bar(C::BAR_PF + b), kRows);
+            ptx::mbar_init(bar(C::BAR_OF + b), 1);
+            ptx::mbar_init(bar(C::BAR_OE + b), kRows);
+        }
+        ptx::mbar_init(bar(C::BAR_DRAIN), 1);
+        ptx::fence_mbar_init();
+        misc[1] = 0;
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(base + C::OFF_MISC, 512);
+        ptx::tmem_relinquish();
+    }
+    const Share sh = cta_share(prm);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < 4) {
+      if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+        Cursor cu = cursor_begin(sh);
+        int b = 0, h = 0, issued = 0, segs = 0;
+        for (int j = 0;; ++j) {
+            int row, e0, np;
+            bool new_seg;
+            if (cursor_next(prm, cu, PT, row, e0, np, new_seg) <= 0) break;
+            int pos = 0;
+            if (lane < np) {
+                pos = prm.q_idx[e0 + lane];
+                if (pos < 0 || pos >= prm.N) {
+                    raise_status(prm.status, BSA_ERR_INDEX);
+                    pos = 0;  // load a valid row so the byte count holds; the epilogue skips it
+                }
+            }
+            if (new_seg) {
+                // the previous segment's last P V must be done before K/V are replaced
+                if (segs > 0 && !__all_sync(0xffffffffu, wait_bar(bar(C::BAR_KVE), (uint32_t)(segs - 1) & 1u,
+                                                                   abort_flag, prm.status)))
+                    break;
+                const int g = row / prm.nblk, blk = row % prm.nblk;
+                b = g / prm.H;
+                h = g % prm.H;
+                if (lane == 0) {
+                    const int tok = b * prm.N + blk * BS;
+                    const uint32_t fb = bar(C::BAR_KVF);
+                    ptx::mbar_arrive_expect_tx(fb, 2 * C::kKVBytes);
+                    ptx::tma_load_3d(base + C::OFF_K, &tm_k, 0, h, tok, fb);
+                    ptx::tma_load_3d(base + C::OFF_K + C::kKVHalf, &tm_k, 64, h, tok, fb);
+                    ptx::tma_load_3d(base + C::OFF_V, &tm_v, 0, h, tok, fb);
+                    ptx::tma_load_3d(base + C::OFF_V + C::kKVHalf, &tm_v, 64, h, tok, fb);
+                }
+                __syncwarp();
+                ++segs;
+            }
+            const int st = j % QS;
+            if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_QE + st), ((uint32_t)(j / QS) & 1u) ^ 1u, abort_flag,
+                                                  prm.status)))
+                break;
+            const uint32_t fb = bar(C::BAR_QF + st);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * G * 256u);
+            __syncwarp();
+            if (lane < np) {
+                const uint32_t dst = base + C::OFF_Q + st * C::kQBytes + lane * G * 128;
+                ptx::tma_load_3d(dst, &tm_q, 0, h * G, b * prm.N + pos, fb);
+                ptx::tma_load_3d(dst + C::kQHalf, &tm_q, 64, h * G, b * prm.N + pos, fb);
+            }
+            issued = j + 1;
+        }
+        if (*abort_flag) {
+            // drain: wait (bounded) for this warp's copies still in flight
+            const uint64_t t0 = ptx::globaltimer();
+            for (int j = max(0, issued - QS); j < issued; ++j)
+                while (!ptx::mbar_try_wait(bar(C::BAR_QF + j % QS), (uint32_t)(j / QS) & 1u) &&
+                       ptx::globaltimer() - t0 < kWaitNs) {
+                }
+            if (segs > 0)
+                while (!ptx::mbar_try_wait(bar(C::BAR_KVF), (uint32_t)(segs - 1) & 1u) &&
+                       ptx::globaltimer() - t0 < kWaitNs) {
+                }
+        }
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = ptx::idesc_bf16(kRows, BS, false);
+            constexpr uint32_t idO = ptx::idesc_bf16(kRows, kHD, true);
+            const uint32_t ka = base + C::OFF_K, va = base + C::OFF_V;
+            Cursor cu = cursor_begin(sh);
+            int pending = -1;  // sub-tile whose P V is still to be issued
+            int segs = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                int row, e0, np;
+                bool new_seg;
+                const int more = cursor_next(prm, cu, PT, row, e0, np, new_seg);
+                if (more <= 0 || new_seg) {
+                    // close the previous segment: its last P V, then K/V may be replaced
+                    if (pending >= 0) {
+                        const int pj = pending, w = pj & 1;
+                        ok = wait_bar(bar(C::BAR_PF + w), (uint32_t)(pj >> 1) & 1u, abort_flag, prm.status) &&
+                             (pj < 2 || wait_bar(bar(C::BAR_OE + w), (uint32_t)((pj >> 1) - 1) & 1u, abort_flag,
+                                                 prm.status));
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < BS / 16; ++kk)
+                            ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, tmem + (uint32_t)w * 128 + kk * 8,
+                                        ptx::smem_desc(va + kk * 2048, C::kKVHalf, 1024), idO, kk > 0 ? 1u : 0u);
+                        ptx::mma_commit(bar(C::BAR_OF + w));
+                        pending = -1;
+                    }
+                    if (segs > 0) ptx::mma_commit(bar(C::BAR_KVE));
+                }
+                if (more <= 0) break;
+                if (new_seg) {
+                    if (!wait_bar(bar(C::BAR_KVF), (uint32_t)segs & 1u, abort_flag, prm.status)) break;
+                    ptx::tc_fence_after();
+                    ++segs;
+                }
+                const int st = j % QS;
+                if (!wait_bar(bar(C::BAR_QF + st), (uint32_t)(j / QS) & 1u, abort_flag, prm.status)) break;
+                ptx::tc_fence_after();
+                // S[j&1] is free: P_{j-2} was consumed by P V_{j-2}, issued before this
+                const uint32_t qa = base + C::OFF_Q + st * C::kQBytes;
+                const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
+#pragma unroll
+                for (int kk = 0; kk < kHD / 16; ++kk) {
+                    const uint32_t qo = (kk >> 2) * C::kQHalf + (kk & 3) * 32;
+                    const uint32_t ko = (kk >> 2) * C::kKVHalf + (kk & 3) * 32;
+                    ptx::mma_ss(dS, ptx::smem_desc(qa + qo, 16, 1024), ptx::smem_desc(ka + ko, 16, 1024), idS,
+                                kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(bar(C::BAR_SF + (j & 1)));
+                ptx::mma_commit(bar(C::BAR_QE + st));
+                if (pending >= 0) {
+                    const int pj = pending, w = pj & 1;
+                    // O[w] must have been read by the epilogue of sub-tile pj - 2
+                    ok = wait_bar(bar(C::BAR_PF + w), (uint32_t)(pj >> 1) & 1u, abort_flag, prm.status) &&
+                         (pj < 2 ||
+                          wait_bar(bar(C::BAR_OE + w), (uint32_t)((pj >> 1) - 1) & 1u, abort_flag, prm.status));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BS / 16; ++kk)
+                        ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, tmem + (uint32_t)w * 128 + kk * 8,
+                                    ptx::smem_desc(va + kk * 2048, C::kKVHalf, 1024), idO, kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar(C::BAR_OF + w));
+                }
+                pending = j;
+            }
+            // nothing this thread issued may still run when TMEM is freed
+            ptx::mma_commit(bar(C::BAR_DRAIN));
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar(C::BAR_DRAIN), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
+        }
+      }
+    } else {
+      {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int w = (warp - 4) >> 2;
+        const int trow = threadIdx.x & 127;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
+        const uint32_t tO = tmem + lane_off + 256 + (uint32_t)w * 128;
+        const int p_in = trow / G, gq = trow % G;
+        Cursor cu = cursor_begin(sh);
+        int b = 0, h = 0, key0 = 0;
+        for (int j = 0;; ++j) {
+            int row, e0, np;
+            bool new_seg;
+            if (cursor_next(prm, cu, PT, row, e0, np, new_seg) <= 0) break;
+            if (new_seg) {
+                const int g = row / prm.nblk;
+                b = g / prm.H;
+                h = g % prm.H;
+                key0 = (row % prm.nblk) * BS;
+            }
+            if ((j & 1) != w) continue;
+            int pos = -1, s = -1;
+            if (p_in < np) {
+                pos = prm.q_idx[e0 + p_in];
+                s = prm.slot[e0 + p_in];
+            }
+            const bool valid = p_in < np && pos >= 0 && pos < prm.N && s >= 0 && s < prm.S;
+            if (p_in < np && (s < 0 || s >= prm.S) && gq == 0) raise_status(prm.status, BSA_ERR_INDEX);
+            int lim = valid ? min(BS, prm.N - key0) : 0;
+            if (valid && prm.causal) lim = min(lim, pos - key0 + 1);
+            lim = max(lim, 0);
+            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_SF + w), ph, abort_flag, prm.status))) break;
+            ptx::tc_fence_after();
+            float x[BS];
+            {
+                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
+#pragma unroll
+                for (int c = 0; c < BS / 32; ++c) ptx::tmem_ld32(tS + c * 32, xr + c * 32);
+                ptx::tmem_wait_ld();
+            }
+            float mxp[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
+            if (__all_sync(0xffffffffu, lim == BS)) {
+#pragma unroll
+                for (int c = 0; c < BS; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < BS; ++c) {
+                    x[c] = c < lim ? x[c] : -CUDART_INF_F;
+                    mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+                }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            const bool live = lim > 0;
+            const float m = live ? mx * prm.scale_log2 : 0.f;  // scale > 0 keeps the order
+            // P = exp2(S * scale_log2 - m), packed to bf16 pairs over S half by half
+            // (masked keys hold -inf: exp2(-inf) = 0); l sums the fp32 values
+            float sp[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sp[u] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < BS / 64; ++hh) {
+                uint32_t r[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = live ? ptx::ex2(fmaf(x[hh * 64 + 2 * e], prm.scale_log2, -m)) : 0.f;
+                    const float p1 = live ? ptx::ex2(fmaf(x[hh * 64 + 2 * e + 1], prm.scale_log2, -m)) : 0.f;
+                    sp[(2 * e) & 7] += p0;
+                    sp[(2 * e + 1) & 7] += p1;
+                    r[e] = ptx::pack_bf16x2(p0, p1);
+                }
+                ptx::tmem_st32(tS + hh * 32, r);
+            }
+            const float l = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::BAR_PF + w));
+            // epilogue: O / l -> bf16 -> the (position, head, slot) row; L in natural log
+            if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_OF + w), ph, abort_flag, prm.status))) break;
+            ptx::tc_fence_after();
+            uint32_t o[kHD];
+#pragma unroll
+            for (int c = 0; c < kHD / 32; ++c) ptx::tmem_ld32(tO + c * 32, o + c * 32);
+            ptx::tmem_wait_ld();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(C::BAR_OE + w));
+            if (valid) {
+                const long long orow = (((long long)b * prm.N + pos) * prm.HQ + h * G + gq) * prm.S + s;
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(prm.obuf + orow * kHD);
+#pragma unroll
+                for (int v4 = 0; v4 < kHD / 8; ++v4) {
+                    uint4 q4;
+                    q4.x = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
+                    q4.y = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
+                    q4.z = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
+                    q4.w = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
+                    dst[v4] = q4;
+                }
+                prm.lsebuf[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+            }
+        }
+      }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D map (D, heads, tokens) over a BTHD bf16 tensor with `heads` heads of
+// 128 channels; box (64, box_heads, box_tokens), 128-byte swizzle.
+static bool make_bthd_map(CUtensorMap* m, const void* ptr, int heads, long long tokens, int box_heads,
+                          int box_tokens) {
+    auto fn = encode_fn();
+    if (!fn || tokens <= 0 || tokens > (1LL << 31)) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)kHD * 2, (cuuint64_t)kHD * 2 * heads};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int BS>
+static bsa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm,
+                         int grid, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kvouter_tc_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Cfg<BS>::SMEM);
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "kvouter tc attribute: %s", cudaGetErrorString(e));
+    kvouter_tc_kernel<BS><<<grid, kThreads, Cfg<BS>::SMEM, st>>>(mq, mk, mv, prm);
+    return check_launch("kvouter_tc_kernel");
+}
+
+}  // namespace kvtc
+
+bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N, int HQ, int H, int D,
+                      const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot, const int32_t* chunks,
+                      const int32_t* n_chunks, int max_chunks, int nblk, int BS, int S, int causal, float scale,
+                      void* obuf, float* lsebuf, cudaStream_t st, bool* handled) {
+    *handled = false;
+    (void)row_ptr;
+    const int G = HQ / H;
+    if (D != kvtc::kHD || (BS != 64 && BS != 128) || G < 8 || G > 128 || (G & (G - 1)) != 0) return BSA_OK;
+    if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)obuf) & 15) return BSA_OK;
+    const long long tokens = (long long)B * N;
+    CUtensorMap mq, mk, mv;
+    if (!kvtc::make_bthd_map(&mq, q, HQ, tokens, G, 1) || !kvtc::make_bthd_map(&mk, k, H, tokens, 1, BS) ||
+        !kvtc::make_bthd_map(&mv, v, H, tokens, 1, BS))
+        return BSA_OK;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        return BSA_OK;
+    *handled = true;
+    kvtc::Params prm{};
+    prm.q_idx = q_idx;
+    prm.slot = slot;
+    prm.chunks = chunks;
+    prm.n_chunks = n_chunks;
+    prm.obuf = static_cast<__nv_bfloat16*>(obuf);
+    prm.lsebuf = lsebuf;
+    prm.status = status_word();
+    prm.N = N;
+    prm.HQ = HQ;
+    prm.H = H;
+    prm.G = G;
+    prm.S = S;
+    prm.nblk = nblk;
+    prm.causal = causal ? 1 : 0;
+    prm.rows_total = B * H * nblk;
+    prm.max_chunks = max_chunks;
+    prm.max_entries = (long long)B * H * N * S;
+    prm.scale_log2 = scale * kLog2e;
+    return BS == 64 ? kvtc::launch<64>(mq, mk, mv, prm, sms, st) : kvtc::launch<128>(mq, mk, mv, prm, sms, st);
+}
+
+}  // namespace bsa

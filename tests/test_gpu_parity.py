@@ -206,6 +206,23 @@ def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf):
     assert np.abs(got_l - lb[written]).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
 
 
+@pytest.mark.parametrize("HQ,H,BS", [(16, 2, 64), (64, 1, 128), (128, 1, 64)])
+def test_kvouter_group_sizes(lib, HQ, H, BS):
+    """The tensor-core partial pass at G = 8, 64, 128 query heads per KV head
+    (16, 2 and 1 query positions per 128-row tile), a ragged last key block
+    (T = 300) and the default chunk cap; output and LSE against the oracle."""
+    pl = _pipeline()
+    B, T, D, S = 1, 300, 128, 4
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 311, torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    idx_d, cnt_d = torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV)
+    o_kv, l_kv, _, _, _ = pl.kvouter_attention(qd, kd, vd, idx_d, cnt_d, BS)
+    torch.cuda.synchronize()
+    O, L = _oracle_nsa(q, k, v, idx, cnt, BS, 0)
+    assert_close(f64(o_kv[0]), O, torch.bfloat16, "kvouter G=%d" % (HQ // H))
+    assert np.abs(l_kv[0].cpu().numpy() - L).max() <= 2e-3
+
+
 # ---------------------------------------------------------------- device-side error reporting
 
 def test_out_of_range_block_index_is_reported_not_faulted(lib):
