@@ -305,6 +305,11 @@ class BlockWorkload:
         self.vbar = torch.empty_like(self.qbar) if self.summary else None
         self.kbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
         self.vbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
+        # permuted blocks: the pool pass also writes Q/K/V in block order for the attention
+        self.packed = (torch.empty((3, BH, J, M, D), dtype=self.dtype, device=dev)
+                       if self.perm is not None else None)
+        if self.packed is not None and self.vbar is None:
+            self.vbar = torch.empty_like(self.qbar)
         self.q2k = torch.empty((BH, self.Jr, k), dtype=torch.int32, device=dev)
         self.q2n = torch.empty((BH, self.Jr), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
@@ -322,18 +327,20 @@ class BlockWorkload:
         if ev: ev[0].record(st)
         bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, M, self.im, self.bs)
         if ev: ev[1].record(st)
-        bsa.bsa_pool_blocks(q, k, v if self.summary else None, self.BH, self.N, D, self.im, self.bs, self.J, M,
-                            self.qbar, self.kbar, self.vbar, self.kbar_lp, self.vbar_lp)
+        bsa.bsa_pool_blocks(q, k, v if self.vbar is not None else None, self.BH, self.N, D, self.im, self.bs,
+                            self.J, M, self.qbar, self.kbar, self.vbar, self.kbar_lp, self.vbar_lp,
+                            packed=self.packed)
         if ev: ev[2].record(st)
         bsa.bsa_route_topk(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.Jr, D, self.J * D, kk,
                            self.scale, kk, self.q2k, self.q2n)
         if ev: ev[3].record(st)
         if self.summary:
             bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
-                                self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.out, self.lse)
+                                self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.out, self.lse,
+                                packed=self.packed)
         else:
             bsa.bsa_fwd_qouter(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
-                               self.q2k, self.q2n, kk, self.scale, self.out, self.lse)
+                               self.q2k, self.q2n, kk, self.scale, self.out, self.lse, packed=self.packed)
         if ev: ev[4].record(st)
 
     def host_inputs(self):
@@ -356,9 +363,11 @@ class BlockWorkload:
             keys = keys + prefix_keys
         pairs = (routed[None, :] * keys).sum() + self.BH * sizes[:self.P].sum() * self.N
         flops = 4.0 * self.w["D"] * float(pairs.item())
-        pool_bytes = ((3 if self.summary else 2) * self.BH * self.N * self.w["D"] * self.q.element_size()
-                      + (3 if self.summary else 2) * self.BH * self.J * self.w["D"] * 4
+        ntens = 3 if self.vbar is not None else 2
+        pool_bytes = (ntens * self.BH * self.N * self.w["D"] * self.q.element_size()
+                      + ntens * self.BH * self.J * self.w["D"] * 4
                       + (2 * self.BH * self.J * self.w["D"] * self.q.element_size() if self.summary else 0)
+                      + (self.packed.numel() * self.packed.element_size() if self.packed is not None else 0)
                       + self.J * self.w["M"] * 4 + self.J * 4)
         return flops, pool_bytes
 
@@ -568,9 +577,11 @@ def gpu_arm(args):
     w = dict(WORKLOADS[args.workload])
     name = args.workload
     if args.heads:
-        if w["kind"] != "block":
-            raise SystemExit("--heads applies to the block workloads")
-        w["heads"] = args.heads
+        if w["kind"] == "block":
+            w["heads"] = args.heads
+        else:  # KV heads, each with its G query heads
+            w["HQ"] = w["HQ"] // w["H"] * args.heads
+            w["H"] = args.heads
         name = name + "_%dheads" % args.heads
     wl = (TokenWorkload if w["kind"] == "token" else BlockWorkload)(name, w, dev, rank)
     nst = len(wl.stage_names)
@@ -720,7 +731,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
-                    help="fewer heads than the workload's (a small case for profiler captures)")
+                    help="fewer heads (KV heads for the token workloads) than the workload's: a small case "
+                         "for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

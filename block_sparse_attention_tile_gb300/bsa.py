@@ -45,9 +45,9 @@ _SIGS = {
     "bsa_tile_count": (I, [I, I, I, I, I, I, I, I, I]),
     "bsa_tile_map": (I, [I, I, I, I, I, I, I, P, I, P, P, P]),
     "bsa_budget": (I, [I, ctypes.c_double]),
-    "bsa_pool_blocks": (I, [P, P, P, I, I, I, I, P, P, I, I, P, P, P, P, P, P]),
+    "bsa_pool_blocks": (I, [P, P, P, I, I, I, I, P, P, I, I, P, P, P, P, P, P, P]),
     "bsa_route_topk": (I, [P, P, I, I, I, I64, I, F, I, P, P, P]),
-    "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, I, F, P, P, P]),
+    "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, F, P, P, P]),
     "bsa_fwd_qouter_tokens": (I, [P, P, P, I, I, I, I, I, I, P, P, I, I, I, F, P, P, P]),
     "bsa_reverse_index_workspace": (SZ, [I, I, I, I]),
     "bsa_max_chunks": (I, [I, I, I, I, I, I]),
@@ -55,7 +55,7 @@ _SIGS = {
     "bsa_build_reverse_index_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P]),
     "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P]),
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
-    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, I, P, P, F, P, P, P]),
+    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, F, P, P, P]),
     "bsa_set_force_simt": (None, [I]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -130,10 +130,10 @@ def bsa_tile_map(T, H, W, bT, bH, bW, n_prefix, perm, M, index_map, block_sizes,
 
 
 def bsa_pool_blocks(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar, kbar, vbar=None,
-                    kbar_lp=None, vbar_lp=None, stream=None):
+                    kbar_lp=None, vbar_lp=None, packed=None, stream=None):
     _check(_lib.bsa_pool_blocks(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
                                 _ptr(block_sizes), J, M, _ptr(qbar), _ptr(kbar), _ptr(vbar),
-                                _ptr(kbar_lp), _ptr(vbar_lp), _stream(stream)))
+                                _ptr(kbar_lp), _ptr(vbar_lp), _ptr(packed), _stream(stream)))
 
 
 def bsa_route_topk(qbar, kbar, BH, J, D, head_stride, k, scale, kmax, q2k_idx, q2k_num, stream=None):
@@ -142,18 +142,19 @@ def bsa_route_topk(qbar, kbar, BH, J, D, head_stride, k, scale, kmax, q2k_idx, q
 
 
 def bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,
-                   q2k_num, kmax, scale, out, lse=None, stream=None):
+                   q2k_num, kmax, scale, out, lse=None, packed=None, stream=None):
     _check(_lib.bsa_fwd_qouter(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
-                               _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(q2k_idx),
-                               _ptr(q2k_num), kmax, scale, _ptr(out), _ptr(lse), _stream(stream)))
+                               _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(packed),
+                               _ptr(q2k_idx), _ptr(q2k_num), kmax, scale, _ptr(out), _ptr(lse),
+                               _stream(stream)))
 
 
 def bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,
-                    q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse=None, stream=None):
+                    q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse=None, packed=None, stream=None):
     _check(_lib.bsa_fwd_summary(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
-                                _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(q2k_idx),
-                                _ptr(q2k_num), kmax, _ptr(kbar_lp), _ptr(vbar_lp), scale, _ptr(out),
-                                _ptr(lse), _stream(stream)))
+                                _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(packed),
+                                _ptr(q2k_idx), _ptr(q2k_num), kmax, _ptr(kbar_lp), _ptr(vbar_lp), scale,
+                                _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def bsa_fwd_qouter_tokens(q, k, v, B, T, HQ, H, D, block_indices, block_counts, S, block_size, causal,

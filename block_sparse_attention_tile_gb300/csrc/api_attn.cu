@@ -15,8 +15,8 @@ bsa_status simt_token_attention(const void* q, const void* k, const void* v, bsa
                                 cudaStream_t st);
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
                               const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
-                              const int32_t* idx, const int32_t* num, int kmax, const void* kb,
-                              const void* vb, float scale, void* out, float* lse, cudaStream_t st,
+                              const void* packed, const int32_t* idx, const int32_t* num, int kmax,
+                              const void* kb, const void* vb, float scale, void* out, float* lse, cudaStream_t st,
                               bool* handled);
 
 // The optional geometry must describe the tiling behind index_map.
@@ -53,9 +53,9 @@ extern "C" {
 
 bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                           int N, int D, const int32_t* index_map, const int32_t* block_sizes, int J,
-                          int M, int prefix_blocks, const int32_t* geometry, const int32_t* q2k_idx,
-                          const int32_t* q2k_num, int kmax, float scale, void* out, float* lse,
-                          void* stream) {
+                          int M, int prefix_blocks, const int32_t* geometry, const void* packed,
+                          const int32_t* q2k_idx, const int32_t* q2k_num, int kmax, float scale, void* out,
+                          float* lse, void* stream) {
     bsa_status rc = check_block_args(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
                                      prefix_blocks, q2k_idx, q2k_num, kmax, out);
     if (rc != BSA_OK) return rc;
@@ -64,7 +64,7 @@ bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype
     cudaStream_t st = as_stream(stream);
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
-        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry,
+        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry, packed,
                                 q2k_idx, q2k_num, kmax, nullptr, nullptr, scale, out, lse, st, &handled);
         if (handled) return rc;
     }
@@ -75,9 +75,9 @@ bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype
 
 bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                            int N, int D, const int32_t* index_map, const int32_t* block_sizes, int J,
-                           int M, int prefix_blocks, const int32_t* geometry, const int32_t* q2k_idx,
-                           const int32_t* q2k_num, int kmax, const void* kbar_lp, const void* vbar_lp,
-                           float scale, void* out, float* lse, void* stream) {
+                           int M, int prefix_blocks, const int32_t* geometry, const void* packed,
+                           const int32_t* q2k_idx, const int32_t* q2k_num, int kmax, const void* kbar_lp,
+                           const void* vbar_lp, float scale, void* out, float* lse, void* stream) {
     bsa_status rc = check_block_args(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
                                      prefix_blocks, q2k_idx, q2k_num, kmax, out);
     if (rc != BSA_OK) return rc;
@@ -88,7 +88,7 @@ bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtyp
     cudaStream_t st = as_stream(stream);
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
-        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry,
+        rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry, packed,
                                 q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, st, &handled);
         if (handled) return rc;
     }

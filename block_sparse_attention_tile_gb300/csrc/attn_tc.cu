@@ -98,6 +98,7 @@ struct Params {
     // that is not ragged in H or W is one box of the 5-D (D, W, H, T, head) map
     int geo, window;  // geometry given; 5-D window boxes usable
     int T, H, W, bT, bH, bW, nH, nW;
+    int packed;       // Q/K/V also given in block order: every tile is one box
 };
 
 // Where a 128-row tile comes from: gathered rows (mode 0), a box of 128
@@ -112,6 +113,11 @@ __device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int b
     if (blk < 0) {  // summary tile: rows of the block-mean tensor
         s.mode = 1;
         s.c1 = bh * prm.J + prm.P + (-blk - 1) * 128;
+        return s;
+    }
+    if (prm.packed) {  // block-ordered copy: block blk of head bh is 128 consecutive rows
+        s.mode = 1;
+        s.c1 = (bh * prm.J + blk) * 128;
         return s;
     }
     if (!prm.geo) return s;
@@ -696,8 +702,9 @@ static bool register_split_fits() {
 
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
                               const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
-                              const int32_t* idx, const int32_t* num, int kmax, const void* kb, const void* vb,
-                              float scale, void* out, float* lse, cudaStream_t st, bool* handled) {
+                              const void* packed, const int32_t* idx, const int32_t* num, int kmax,
+                              const void* kb, const void* vb, float scale, void* out, float* lse, cudaStream_t st,
+                              bool* handled) {
     *handled = false;
     const bool summary = kb != nullptr;
     const int Jr = J - P;
@@ -706,14 +713,26 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
+    if ((uintptr_t)packed & 15) return BSA_OK;
     if (!tc::register_split_fits()) return BSA_OK;
     tc::Params prm{};
     CUtensorMap mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5, mkb, mvb;
     const long long rows = (long long)BH * N;
-    if (!tc::make_row_map(&mq, q, rows) || !tc::make_row_map(&mk, k, rows) || !tc::make_row_map(&mv, v, rows) ||
-        !tc::make_row_map(&mqr, q, rows, 128) || !tc::make_row_map(&mkr, k, rows, 128) ||
-        !tc::make_row_map(&mvr, v, rows, 128))
+    if (!tc::make_row_map(&mq, q, rows) || !tc::make_row_map(&mk, k, rows) || !tc::make_row_map(&mv, v, rows))
         return BSA_OK;
+    if (packed) {
+        // [3, BH, J, 128, 128]: Q, K, V blocks of 128 rows in block order
+        const long long prow = (long long)BH * J * tc::kBN;
+        const char* pb = static_cast<const char*>(packed);
+        const size_t part = (size_t)prow * tc::kHD * 2;
+        if (!tc::make_row_map(&mqr, pb, prow, 128) || !tc::make_row_map(&mkr, pb + part, prow, 128) ||
+            !tc::make_row_map(&mvr, pb + 2 * part, prow, 128))
+            return BSA_OK;
+        prm.packed = 1;
+    } else if (!tc::make_row_map(&mqr, q, rows, 128) || !tc::make_row_map(&mkr, k, rows, 128) ||
+               !tc::make_row_map(&mvr, v, rows, 128)) {
+        return BSA_OK;
+    }
     mq5 = mq;
     mk5 = mk;
     mv5 = mv;

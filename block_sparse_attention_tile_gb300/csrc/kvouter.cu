@@ -260,6 +260,8 @@ __global__ void __launch_bounds__(256) kvouter_simt_kernel(
 }
 
 // ---------------------------------------------------------------- K2
+// Generic combine: one warp per (token, query head) row, lane d + 32c holds
+// channel d + 32c.
 template <typename TI, typename TO>
 __global__ void __launch_bounds__(256) combine_kernel(
     const TI* __restrict__ obuf, const float* __restrict__ lsebuf, const int32_t* __restrict__ nslots,
@@ -303,6 +305,79 @@ __global__ void __launch_bounds__(256) combine_kernel(
         const int d = lane + 32 * c;
         if (d < D) out[row * D + d] = from_f32<TO>(acc[c]);
     }
+}
+
+// bf16 partials with D = 128 (256-byte rows): one warp per row; half-warp
+// hf takes the slots s = hf, hf+2, ... and lane l of it the 16-byte chunk l
+// (channels 8l .. 8l+7), four slots in flight per lane; the halves are
+// added with one shuffle.  Same arithmetic as the generic kernel: weights
+// exp(L_s - L) with L = a + log sum exp(L_s - a), fp32 accumulation.
+template <typename TO>
+__global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
+    const __nv_bfloat16* __restrict__ obuf, const float* __restrict__ lsebuf, const int32_t* __restrict__ nslots,
+    int HQ, int H, int S, long long rows, TO* __restrict__ out, float* __restrict__ lse) {
+    constexpr int D = 128, U = 4;
+    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int hq = (int)(row % HQ);
+    const long long bt = row / HQ;
+    const int G = HQ / H;
+    const int n = max(0, min(__ldg(nslots + bt * H + hq / G), S));
+    const float* L = lsebuf + row * S;
+    const float l_own = lane < n ? __ldg(L + lane) : -CUDART_INF_F;  // S <= 32 on this path
+    const float a = warp_max(l_own);
+    const int hf = lane >> 4, ch = lane & 15;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    float Lrow = -CUDART_INF_F;
+    if (a != -CUDART_INF_F) {
+        const float total = warp_sum(l_own == -CUDART_INF_F ? 0.f : __expf(l_own - a));
+        Lrow = a + __logf(total);
+        const uint4* base = reinterpret_cast<const uint4*>(obuf + row * S * D) + ch;
+        for (int s0 = 0; s0 < n; s0 += 2 * U) {  // warp-uniform bound: the shuffles need every lane
+            uint4 raw[U];
+            float w[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int s = s0 + hf + 2 * u;
+                const float ls = __shfl_sync(0xffffffffu, l_own, s & 31);
+                const bool use = s < n && ls != -CUDART_INF_F;
+                w[u] = use ? __expf(ls - Lrow) : 0.f;
+                raw[u] = use ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(p2[e]);
+                    acc[2 * e] = fmaf(w[u], f.x, acc[2 * e]);
+                    acc[2 * e + 1] = fmaf(w[u], f.y, acc[2 * e + 1]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
+    if (lane < 16) {
+        TO* o = out + row * D + 8 * ch;
+        if constexpr (sizeof(TO) == 2) {
+            uint4 q4;
+            uint32_t* w32 = reinterpret_cast<uint32_t*>(&q4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+                w32[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(o) = q4;
+        } else {
+            *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+    if (lse && lane == 0) lse[row] = Lrow;
 }
 
 // tcgen05 version of K1 (attn_tc.cu); sets *handled = false when the shape is not covered.
@@ -422,6 +497,15 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
     const long long grid = (rows + per_cta - 1) / per_cta;
     BSA_REQUIRE(grid < 0x7fffffffLL, "combine: too many rows");
     cudaStream_t st = as_stream(stream);
+    if (obuf_dtype == BSA_BF16 && D == 128 && S <= 32 && ((uintptr_t)obuf & 15) == 0 && ((uintptr_t)out & 15) == 0) {
+        if (out_dtype == BSA_BF16)
+            combine_bf16_d128_kernel<__nv_bfloat16><<<(unsigned)grid, 32 * per_cta, 0, st>>>(
+                (const __nv_bfloat16*)obuf, lsebuf, nslots, HQ, H, S, rows, (__nv_bfloat16*)out, lse);
+        else
+            combine_bf16_d128_kernel<float><<<(unsigned)grid, 32 * per_cta, 0, st>>>(
+                (const __nv_bfloat16*)obuf, lsebuf, nslots, HQ, H, S, rows, (float*)out, lse);
+        return check_launch("combine_bf16_d128_kernel");
+    }
 #define BSA_CB(TI, TO)                                                                         \
     combine_kernel<TI, TO><<<(unsigned)grid, 32 * per_cta, 0, st>>>(                           \
         (const TI*)obuf, lsebuf, nslots, N, HQ, H, S, D, rows, (TO*)out, lse)

@@ -26,8 +26,12 @@
 //   warps 4-7 / 8-11   sub-tiles of even / odd index: softmax over the
 //              block's visible keys (a prefix of the tile: key < N and, when
 //              causal, key <= the query position), then the epilogue:
-//              O / l in bf16 and L = ln-sum-exp written straight to the
-//              (position, head, slot) rows of the partial buffers.
+//              O / l in bf16 to the (position, head, slot) rows of the
+//              partial buffer, staged per warp through shared memory so that
+//              each store instruction writes whole 128-byte lines, and
+//              L = ln-sum-exp.  Query positions and slots are read one owned
+//              sub-tile ahead (the producer reads its positions one sub-tile
+//              ahead too), so no index load sits on the critical path.
 // A sub-tile meets exactly one key tile, so the softmax needs no running
 // rescale.  Every mbarrier wait is bounded (2 s); on expiry the CTA raises
 // BSA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM.
@@ -45,8 +49,11 @@ constexpr int kRows = 128;  // MMA rows per sub-tile
 constexpr int kHD = 128;    // head dim
 constexpr int kThreads = 384;
 constexpr uint64_t kWaitNs = 2000000000ull;
-// No register split: every role fits the 168 registers a thread gets at
-// 384 threads per SM (the softmax holds one 128-key row of S at a time).
+// setmaxnreg split: the producer / MMA warpgroup gives registers to the two
+// softmax warpgroups, which hold a whole 128-key row of S (one TMEM load
+// round trip per sub-tile instead of one per 32 columns).
+constexpr int kRegsLow = 96, kRegsHigh = 200, kRegsLaunch = 168;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 template <int BS>
 struct Cfg {
@@ -58,7 +65,8 @@ struct Cfg {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + kQStages * kQBytes;
     static constexpr uint32_t OFF_V = OFF_K + kKVBytes;
-    static constexpr uint32_t OFF_BAR = OFF_V + kKVBytes;
+    static constexpr uint32_t OFF_STG = OFF_V + kKVBytes;     // 8 warps x 32 rows x 128 B epilogue staging
+    static constexpr uint32_t OFF_BAR = OFF_STG + 8 * 4096;
     static constexpr int BAR_KVF = 0, BAR_KVE = 1, BAR_QF = 2, BAR_QE = BAR_QF + kQStages,
                          BAR_SF = BAR_QE + kQStages, BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2,
                          BAR_OE = BAR_OF + 2, BAR_DRAIN = BAR_OE + 2, NBAR = BAR_DRAIN + 1;
@@ -173,6 +181,37 @@ __device__ __forceinline__ int cursor_next(const Params& p, Cursor& cu, int PT, 
     return 1;
 }
 
+// The next sub-tile of parity w (the ones a softmax warpgroup owns), with the
+// segment it belongs to; jj counts every sub-tile the cursor has passed.
+struct OwnTile {
+    int j, e0, np, b, h, blk;
+};
+
+__device__ __forceinline__ bool next_own(const Params& p, Cursor& cu, int PT, int w, int& jj, int& sb, int& shd,
+                                         int& sblk, OwnTile& t) {
+    while (true) {
+        int row, e0, np;
+        bool ns;
+        if (cursor_next(p, cu, PT, row, e0, np, ns) <= 0) return false;
+        ++jj;
+        if (ns) {
+            const int g = row / p.nblk;
+            sb = g / p.H;
+            shd = g % p.H;
+            sblk = row % p.nblk;
+        }
+        if ((jj & 1) == w) {
+            t.j = jj;
+            t.e0 = e0;
+            t.np = np;
+            t.b = sb;
+            t.h = shd;
+            t.blk = sblk;
+            return true;
+        }
+    }
+}
+
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
 kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -218,6 +257,7 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t tmem = misc[0];
 
     if (warp < 4) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         ptx::prefetch_tmap(&tm_q);
@@ -225,17 +265,20 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::prefetch_tmap(&tm_v);
         Cursor cu = cursor_begin(sh);
         int b = 0, h = 0, issued = 0, segs = 0;
-        for (int j = 0;; ++j) {
-            int row, e0, np;
-            bool new_seg;
-            if (cursor_next(prm, cu, PT, row, e0, np, new_seg) <= 0) break;
-            int pos = 0;
-            if (lane < np) {
-                pos = prm.q_idx[e0 + lane];
-                if (pos < 0 || pos >= prm.N) {
-                    raise_status(prm.status, BSA_ERR_INDEX);
-                    pos = 0;  // load a valid row so the byte count holds; the epilogue skips it
-                }
+        // one sub-tile of lookahead: its query positions load while this one is issued
+        int n_row = 0, n_e0 = 0, n_np = 0;
+        bool n_seg = false;
+        int n_more = cursor_next(prm, cu, PT, n_row, n_e0, n_np, n_seg);
+        int n_pos = (n_more > 0 && lane < n_np) ? prm.q_idx[n_e0 + lane] : 0;
+        for (int j = 0; n_more > 0; ++j) {
+            const int row = n_row, np = n_np;
+            const bool new_seg = n_seg;
+            int pos = n_pos;
+            n_more = cursor_next(prm, cu, PT, n_row, n_e0, n_np, n_seg);
+            n_pos = (n_more > 0 && lane < n_np) ? prm.q_idx[n_e0 + lane] : 0;
+            if (lane < np && (pos < 0 || pos >= prm.N)) {
+                raise_status(prm.status, BSA_ERR_INDEX);
+                pos = 0;  // load a valid row so the byte count holds; the epilogue skips it
             }
             if (new_seg) {
                 // the previous segment's last P V must be done before K/V are replaced
@@ -359,6 +402,7 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       }
     } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
       {
         // ------------------------------------------------------------ softmax + epilogue
         const int w = (warp - 4) >> 2;
@@ -367,58 +411,61 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
         const uint32_t tO = tmem + lane_off + 256 + (uint32_t)w * 128;
         const int p_in = trow / G, gq = trow % G;
+        uint8_t* stg = sm + C::OFF_STG + (warp - 4) * 4096;  // this warp's 32 rows x 128 B
         Cursor cu = cursor_begin(sh);
-        int b = 0, h = 0, key0 = 0;
-        for (int j = 0;; ++j) {
-            int row, e0, np;
-            bool new_seg;
-            if (cursor_next(prm, cu, PT, row, e0, np, new_seg) <= 0) break;
-            if (new_seg) {
-                const int g = row / prm.nblk;
-                b = g / prm.H;
-                h = g % prm.H;
-                key0 = (row % prm.nblk) * BS;
+        int jj = -1, sb = 0, shd = 0, sblk = 0;
+        OwnTile cur, nxt;
+        bool have = next_own(prm, cu, PT, w, jj, sb, shd, sblk, cur);
+        // the row's query position and slot, loaded one owned sub-tile ahead
+        int pos = -1, s = -1;
+        if (have && p_in < cur.np) {
+            pos = prm.q_idx[cur.e0 + p_in];
+            s = prm.slot[cur.e0 + p_in];
+        }
+        while (have) {
+            const OwnTile t = cur;
+            const int tpos = pos, ts = s;
+            const bool have_n = next_own(prm, cu, PT, w, jj, sb, shd, sblk, nxt);
+            pos = -1;
+            s = -1;
+            if (have_n && p_in < nxt.np) {
+                pos = prm.q_idx[nxt.e0 + p_in];
+                s = prm.slot[nxt.e0 + p_in];
             }
-            if ((j & 1) != w) continue;
-            int pos = -1, s = -1;
-            if (p_in < np) {
-                pos = prm.q_idx[e0 + p_in];
-                s = prm.slot[e0 + p_in];
-            }
-            const bool valid = p_in < np && pos >= 0 && pos < prm.N && s >= 0 && s < prm.S;
-            if (p_in < np && (s < 0 || s >= prm.S) && gq == 0) raise_status(prm.status, BSA_ERR_INDEX);
+            cur = nxt;
+            have = have_n;
+
+            const int key0 = t.blk * BS;
+            const bool valid = p_in < t.np && tpos >= 0 && tpos < prm.N && ts >= 0 && ts < prm.S;
+            if (p_in < t.np && (ts < 0 || ts >= prm.S) && gq == 0) raise_status(prm.status, BSA_ERR_INDEX);
             int lim = valid ? min(BS, prm.N - key0) : 0;
-            if (valid && prm.causal) lim = min(lim, pos - key0 + 1);
+            if (valid && prm.causal) lim = min(lim, tpos - key0 + 1);
             lim = max(lim, 0);
-            const uint32_t ph = (uint32_t)(j >> 1) & 1u;
+            const uint32_t ph = (uint32_t)(t.j >> 1) & 1u;
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_SF + w), ph, abort_flag, prm.status))) break;
             ptx::tc_fence_after();
+            // two passes over S in TMEM (32 / 64 columns at a time keep registers low):
+            // the row maximum of the visible keys, then P = exp2(S * scale_log2 - m)
+            // packed to bf16 pairs over the consumed columns of S; l sums the fp32 values
+            const bool full = __all_sync(0xffffffffu, lim == BS);
             float x[BS];
-            {
-                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
 #pragma unroll
-                for (int c = 0; c < BS / 32; ++c) ptx::tmem_ld32(tS + c * 32, xr + c * 32);
-                ptx::tmem_wait_ld();
-            }
+            for (int cc = 0; cc < BS / 32; ++cc) ptx::tmem_ld32(tS + cc * 32, reinterpret_cast<uint32_t*>(x) + cc * 32);
+            ptx::tmem_wait_ld();
             float mxp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
-            if (__all_sync(0xffffffffu, lim == BS)) {
+            if (full) {
 #pragma unroll
                 for (int c = 0; c < BS; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
             } else {
 #pragma unroll
-                for (int c = 0; c < BS; ++c) {
-                    x[c] = c < lim ? x[c] : -CUDART_INF_F;
-                    mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
-                }
+                for (int c = 0; c < BS; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], c < lim ? x[c] : -CUDART_INF_F);
             }
             const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                    fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             const bool live = lim > 0;
-            const float m = live ? mx * prm.scale_log2 : 0.f;  // scale > 0 keeps the order
-            // P = exp2(S * scale_log2 - m), packed to bf16 pairs over S half by half
-            // (masked keys hold -inf: exp2(-inf) = 0); l sums the fp32 values
+            const float m = live ? mx * prm.scale_log2 : 0.f;
             float sp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) sp[u] = 0.f;
@@ -427,8 +474,10 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 uint32_t r[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = live ? ptx::ex2(fmaf(x[hh * 64 + 2 * e], prm.scale_log2, -m)) : 0.f;
-                    const float p1 = live ? ptx::ex2(fmaf(x[hh * 64 + 2 * e + 1], prm.scale_log2, -m)) : 0.f;
+                    const int c0 = hh * 64 + 2 * e;
+                    const bool v0 = live && (full || c0 < lim), v1 = live && (full || c0 + 1 < lim);
+                    const float p0 = v0 ? ptx::ex2(fmaf(x[c0], prm.scale_log2, -m)) : 0.f;
+                    const float p1 = v1 ? ptx::ex2(fmaf(x[c0 + 1], prm.scale_log2, -m)) : 0.f;
                     sp[(2 * e) & 7] += p0;
                     sp[(2 * e + 1) & 7] += p1;
                     r[e] = ptx::pack_bf16x2(p0, p1);
@@ -439,30 +488,54 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::BAR_PF + w));
-            // epilogue: O / l -> bf16 -> the (position, head, slot) row; L in natural log
+            // epilogue: O / l -> bf16 -> the (position, head, slot) row; L in natural log.
+            // Rows go out through the warp's staging buffer so that every store
+            // instruction writes whole 128-byte lines (4 rows x one 64-column half).
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_OF + w), ph, abort_flag, prm.status))) break;
             ptx::tc_fence_after();
-            uint32_t o[kHD];
+            // partial-buffer row; B*N*HQ*S < 2^31 is checked by the entry point
+            const int orow = valid ? (int)((((long long)t.b * prm.N + tpos) * prm.HQ + t.h * G + gq) * prm.S + ts) : -1;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            // The O row comes out of TMEM in OPARTS round trips (one where the
+            // register budget allows: the 64-key variant keeps two); O[w] is
+            // released after the last one.
+            constexpr int OPARTS = BS == 128 ? 1 : 2, OCOLS = kHD / OPARTS;
 #pragma unroll
-            for (int c = 0; c < kHD / 32; ++c) ptx::tmem_ld32(tO + c * 32, o + c * 32);
-            ptx::tmem_wait_ld();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(C::BAR_OE + w));
-            if (valid) {
-                const long long orow = (((long long)b * prm.N + pos) * prm.HQ + h * G + gq) * prm.S + s;
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(prm.obuf + orow * kHD);
+            for (int part = 0; part < OPARTS; ++part) {
+                uint32_t o[OCOLS];
 #pragma unroll
-                for (int v4 = 0; v4 < kHD / 8; ++v4) {
-                    uint4 q4;
-                    q4.x = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 0]) * inv, __uint_as_float(o[8 * v4 + 1]) * inv);
-                    q4.y = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 2]) * inv, __uint_as_float(o[8 * v4 + 3]) * inv);
-                    q4.z = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 4]) * inv, __uint_as_float(o[8 * v4 + 5]) * inv);
-                    q4.w = ptx::pack_bf16x2(__uint_as_float(o[8 * v4 + 6]) * inv, __uint_as_float(o[8 * v4 + 7]) * inv);
-                    dst[v4] = q4;
+                for (int c = 0; c < OCOLS / 32; ++c) ptx::tmem_ld32(tO + part * OCOLS + c * 32, o + c * 32);
+                ptx::tmem_wait_ld();
+                if (part == OPARTS - 1) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(C::BAR_OE + w));
                 }
-                prm.lsebuf[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
+#pragma unroll
+                for (int hl = 0; hl < OCOLS / 64; ++hl) {
+                    const int hh = part * (OCOLS / 64) + hl;  // 64-column half of the row
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint32_t* oc = o + hl * 64 + 8 * c;
+                        uint4 q4;
+                        q4.x = ptx::pack_bf16x2(__uint_as_float(oc[0]) * inv, __uint_as_float(oc[1]) * inv);
+                        q4.y = ptx::pack_bf16x2(__uint_as_float(oc[2]) * inv, __uint_as_float(oc[3]) * inv);
+                        q4.z = ptx::pack_bf16x2(__uint_as_float(oc[4]) * inv, __uint_as_float(oc[5]) * inv);
+                        q4.w = ptx::pack_bf16x2(__uint_as_float(oc[6]) * inv, __uint_as_float(oc[7]) * inv);
+                        // 16-byte chunk c of row `lane`, XOR-swizzled across the bank groups
+                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = q4;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) {
+                        const int r = 4 * i2 + (lane >> 3), c = lane & 7;
+                        const int dst = __shfl_sync(0xffffffffu, orow, r);
+                        const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
+                        if (dst >= 0) *reinterpret_cast<uint4*>(prm.obuf + (long long)dst * kHD + hh * 64 + c * 8) = v;
+                    }
+                    __syncwarp();
+                }
             }
+            if (valid) prm.lsebuf[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
         }
       }
     }
@@ -506,6 +579,21 @@ static bool make_bthd_map(CUtensorMap* m, const void* ptr, int heads, long long 
     return r == CUDA_SUCCESS;
 }
 
+// The split needs the launch to reserve kRegsLaunch registers per thread;
+// refuse the tensor-core path otherwise (setmaxnreg.inc would wait).
+template <int BS>
+static bool register_split_fits() {
+    static int checked = 0;  // 0 unknown, 1 fits, -1 does not
+    if (!checked) {
+        cudaFuncAttributes a;
+        checked = (cudaFuncGetAttributes(&a, kvouter_tc_kernel<BS>) == cudaSuccess &&
+                   a.numRegs * kThreads >= 128 * kRegsLow + 256 * kRegsHigh)
+                      ? 1
+                      : -1;
+    }
+    return checked == 1;
+}
+
 template <int BS>
 static bsa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm,
                          int grid, cudaStream_t st) {
@@ -527,6 +615,7 @@ bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N,
     const int G = HQ / H;
     if (D != kvtc::kHD || (BS != 64 && BS != 128) || G < 8 || G > 128 || (G & (G - 1)) != 0) return BSA_OK;
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)obuf) & 15) return BSA_OK;
+    if (BS == 64 ? !kvtc::register_split_fits<64>() : !kvtc::register_split_fits<128>()) return BSA_OK;
     const long long tokens = (long long)B * N;
     CUtensorMap mq, mk, mv;
     if (!kvtc::make_bthd_map(&mq, q, HQ, tokens, G, 1) || !kvtc::make_bthd_map(&mk, k, H, tokens, 1, BS) ||

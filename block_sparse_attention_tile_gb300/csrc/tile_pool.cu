@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) pool_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D,
     const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M,
     float* __restrict__ qbar, float* __restrict__ kbar, float* __restrict__ vbar,
-    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, int* status) {
+    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, T* __restrict__ packed, int BH, int* status) {
     extern __shared__ float red[];  // [RG][D]
     const int j = blockIdx.x;
     const int bh = blockIdx.y;
@@ -71,10 +71,17 @@ __global__ void __launch_bounds__(256) pool_kernel(
     const int n = block_sizes[j];
     const int32_t* rows = index_map + (size_t)j * M;
     const T* base = src + (size_t)bh * N * D;
+    // block-ordered copy of this (tensor, head, block): M rows, zeros past n
+    T* pk = packed ? packed + (((size_t)which * BH + bh) * J + j) * (size_t)M * D : nullptr;
 
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+    if (pk && rg < RG && lane * VEC < D) {
+        for (int r = n + rg; r < M; r += RG)
+            for (int e = 0; e < VEC; ++e)
+                if (lane * VEC + e < D) pk[(size_t)r * D + lane * VEC + e] = from_f32<T>(0.f);
+    }
     if (rg < RG && lane * VEC < D) {
         if constexpr (sizeof(T) * VEC == 16) {
             // batches of 8 rows: the 8 token ids first, then 8 independent 16-byte loads
@@ -97,15 +104,22 @@ __global__ void __launch_bounds__(256) pool_kernel(
                     const T* e8 = reinterpret_cast<const T*>(&raw[u]);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+                    const int r = r0 + u * RG;
+                    if (pk && r < n) *reinterpret_cast<uint4*>(pk + (size_t)r * D + lane * VEC) = raw[u];
                 }
             }
         } else {
             for (int r = rg; r < n; r += RG) {
                 const int tok = rows[r];
-                if (tok < 0 || tok >= N) { raise_status(status, BSA_ERR_INDEX); continue; }
-                const T* row = base + (size_t)tok * D + lane * VEC;
-                for (int e = 0; e < VEC; ++e)
-                    if (lane * VEC + e < D) acc[e] += to_f32(row[e]);
+                const bool ok = tok >= 0 && tok < N;
+                if (!ok) raise_status(status, BSA_ERR_INDEX);
+                const T* row = base + (size_t)(ok ? tok : 0) * D + lane * VEC;
+                for (int e = 0; e < VEC; ++e) {
+                    if (lane * VEC + e >= D) continue;
+                    const T x = ok ? row[e] : from_f32<T>(0.f);
+                    acc[e] += to_f32(x);
+                    if (pk) pk[(size_t)r * D + lane * VEC + e] = x;
+                }
             }
         }
         for (int e = 0; e < VEC; ++e)
@@ -138,7 +152,7 @@ __global__ void __launch_bounds__(256) pool_rows256_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D,
     const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M, int BH,
     long long items, float* __restrict__ qbar, float* __restrict__ kbar, float* __restrict__ vbar,
-    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, int* status) {
+    T* __restrict__ kbar_lp, T* __restrict__ vbar_lp, T* __restrict__ packed, int* status) {
     extern __shared__ int toks_all[];  // [8][M]
     constexpr int VEC = 16 / sizeof(T);
     constexpr int U = 16;
@@ -164,6 +178,10 @@ __global__ void __launch_bounds__(256) pool_rows256_kernel(
     __syncwarp();
     const int chunk = lane & 15, half = lane >> 4;
     const T* base = src + (size_t)bh * N * D + chunk * VEC;
+    // block-ordered copy of this (tensor, head, block): M rows, zeros past n
+    T* pk = packed ? packed + (((size_t)which * BH + bh) * J + j) * (size_t)M * D + chunk * VEC : nullptr;
+    if (pk)
+        for (int r = n + half; r < M; r += 2) *reinterpret_cast<uint4*>(pk + (size_t)r * D) = make_uint4(0u, 0u, 0u, 0u);
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
@@ -181,6 +199,13 @@ __global__ void __launch_bounds__(256) pool_rows256_kernel(
             const T* e8 = reinterpret_cast<const T*>(&raw[u]);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+        }
+        if (pk) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int r = r0 + 2 * u;
+                if (r < n) *reinterpret_cast<uint4*>(pk + (size_t)r * D) = raw[u];
+            }
         }
     }
 #pragma unroll
@@ -206,10 +231,10 @@ __global__ void __launch_bounds__(256) pool_rows256_kernel(
 template <typename T>
 static bsa_status launch_pool(const void* q, const void* k, const void* v, int BH, int N, int D,
                               const int32_t* im, const int32_t* bs, int J, int M, float* qbar,
-                              float* kbar, float* vbar, void* klp, void* vlp, cudaStream_t st) {
+                              float* kbar, float* vbar, void* klp, void* vlp, void* packed, cudaStream_t st) {
     constexpr int VEC = 16 / sizeof(T);
     if ((size_t)D * sizeof(T) == 256 && ((uintptr_t)q % 16 == 0) && ((uintptr_t)k % 16 == 0) &&
-        (!v || (uintptr_t)v % 16 == 0)) {
+        (!v || (uintptr_t)v % 16 == 0) && (uintptr_t)packed % 16 == 0) {
         const long long items = (long long)(v ? 3 : 2) * BH * J;
         const long long grid = (items + 7) / 8;
         const size_t smem = (size_t)8 * M * sizeof(int);
@@ -217,10 +242,11 @@ static bsa_status launch_pool(const void* q, const void* k, const void* v, int B
             cudaFuncSetAttribute(pool_rows256_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         pool_rows256_kernel<T><<<(unsigned)grid, 256, smem, st>>>(
             (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, BH, items, qbar, kbar, vbar, (T*)klp,
-            (T*)vlp, status_word());
+            (T*)vlp, (T*)packed, status_word());
         return check_launch("pool_rows256_kernel");
     }
-    const bool vec_ok = (D % VEC) == 0;
+    // the 16-byte path also stores 16-byte rows into the packed copy
+    const bool vec_ok = (D % VEC) == 0 && (uintptr_t)packed % 16 == 0;
     const int vec = vec_ok ? VEC : 1;
     int vl2 = 1;  // same rounding as the kernel
     while (vl2 * vec < D) vl2 <<= 1;
@@ -231,11 +257,11 @@ static bsa_status launch_pool(const void* q, const void* k, const void* v, int B
     if (vec_ok) {
         pool_kernel<T, VEC><<<grid, 256, smem, st>>>(
             (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, qbar, kbar, vbar, (T*)klp,
-            (T*)vlp, status_word());
+            (T*)vlp, (T*)packed, BH, status_word());
     } else {
         pool_kernel<T, 1><<<grid, 256, smem, st>>>(
             (const T*)q, (const T*)k, (const T*)v, N, D, im, bs, J, M, qbar, kbar, vbar, (T*)klp,
-            (T*)vlp, status_word());
+            (T*)vlp, (T*)packed, BH, status_word());
     }
     return check_launch("pool_kernel");
 }
@@ -279,19 +305,20 @@ bsa_status bsa_tile_map(int T, int H, int W, int bT, int bH, int bW, int n_prefi
 bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                            int N, int D, const int32_t* index_map, const int32_t* block_sizes,
                            int J, int M, float* qbar, float* kbar, float* vbar, void* kbar_lp,
-                           void* vbar_lp, void* stream) {
+                           void* vbar_lp, void* packed, void* stream) {
     BSA_REQUIRE(q && k && qbar && kbar && index_map && block_sizes, "pool: null pointer");
     BSA_REQUIRE(!v || vbar, "pool: v given without vbar");
+    BSA_REQUIRE(!packed || v, "pool: the packed copy needs v");
     BSA_REQUIRE(!vbar_lp || v, "pool: vbar_lp needs v");
     BSA_REQUIRE(BH > 0 && N > 0 && D > 0 && D <= 256 && J > 0 && M > 0 && M <= 1024,
                 "pool: sizes out of range");
     BSA_REQUIRE(J <= 65535 && BH <= 65535, "pool: grid too large");
     if (dtype == BSA_F32)
         return launch_pool<float>(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar, kbar, vbar,
-                                  kbar_lp, vbar_lp, as_stream(stream));
+                                  kbar_lp, vbar_lp, packed, as_stream(stream));
     if (dtype == BSA_BF16)
         return launch_pool<__nv_bfloat16>(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar,
-                                          kbar, vbar, kbar_lp, vbar_lp, as_stream(stream));
+                                          kbar, vbar, kbar_lp, vbar_lp, packed, as_stream(stream));
     return fail(BSA_ERR_INVALID_ARG, "pool: unknown dtype");
 }
 

@@ -68,14 +68,18 @@ class BlockSparseResult:
     kbar: torch.Tensor
     q2k_idx: torch.Tensor
     q2k_num: torch.Tensor
+    packed: Optional[torch.Tensor] = None
 
 
 def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=False, need_lse=True,
-                           tiles=None, pass_geometry=True):
+                           tiles=None, pass_geometry=True, packed=None):
     """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
 
     q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
-    covers the video blocks; prefix blocks are always attended.  Returns the
+    covers the video blocks; prefix blocks are always attended.  ``packed``:
+    let the pool pass also write Q/K/V in block order for the attention to
+    read (default: when the blocks come from a permutation, whose rows the
+    tensor-core kernel would otherwise gather four at a time).  Returns the
     output in raster order plus every intermediate."""
     BH, N, D = q.shape
     assert N == geom.n_tokens
@@ -86,13 +90,16 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     P = geom.prefix_blocks
     Jr = J - P
     kmax = topk if kmax is None else kmax
+    if packed is None:
+        packed = geom.perm is not None and q.dtype == torch.bfloat16 and D == 128 and geom.M == 128
+    pk = torch.empty((3, BH, J, geom.M, D), dtype=q.dtype, device=dev) if packed else None
     qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
     kbar = torch.empty_like(qbar)
-    vbar = torch.empty_like(qbar) if summary else None
+    vbar = torch.empty_like(qbar) if (summary or packed) else None
     kbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
     vbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
-    bsa.bsa_pool_blocks(q, k, v if summary else None, BH, N, D, index_map, block_sizes, J, geom.M, qbar,
-                        kbar, vbar, kbar_lp, vbar_lp)
+    bsa.bsa_pool_blocks(q, k, v if (summary or packed) else None, BH, N, D, index_map, block_sizes, J, geom.M,
+                        qbar, kbar, vbar, kbar_lp, vbar_lp, packed=pk)
     q2k_idx = torch.empty((BH, Jr, kmax), dtype=torch.int32, device=dev)
     q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
     bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num)
@@ -100,11 +107,11 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
     if summary:
         bsa.bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
-                            q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse)
+                            q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, packed=pk)
     else:
         bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
-                           q2k_idx, q2k_num, kmax, scale, out, lse)
-    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num)
+                           q2k_idx, q2k_num, kmax, scale, out, lse, packed=pk)
+    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk)
 
 
 def nsa_qouter(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None, need_lse=True):

@@ -103,12 +103,17 @@ int bsa_budget(int J, double sparsity);
  * qbar, kbar (and vbar when v != NULL): [device] float [BH, J, D].
  * kbar_lp / vbar_lp: optional [device] copies of kbar / vbar in `dtype`
  * (the summary keys and values consumed by bsa_fwd_summary), or NULL.
+ * packed: optional [device] [3, BH, J, M, D] of `dtype` (needs v): the rows
+ * of Q, K and V gathered into block order while they are read for the means,
+ * row (j, m) = token index_map[j*M + m], zero rows for slots >= n_j (the
+ * packing step of [VSA] §3 made explicit), or NULL.  bsa_fwd_qouter /
+ * bsa_fwd_summary then load every tile as one TMA box.
  * 1 <= D <= 256. */
 bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtype dtype,
                            int BH, int N, int D, const int32_t* index_map,
                            const int32_t* block_sizes, int J, int M,
                            float* qbar, float* kbar, float* vbar,
-                           void* kbar_lp, void* vbar_lp, void* stream);
+                           void* kbar_lp, void* vbar_lp, void* packed, void* stream);
 
 /* ------------------------------------------------------------------ a3 ----
  * Routing.  [VSA] §2.2: E = Q_bar K_bar^T * scale per (batch, head), shape
@@ -137,13 +142,18 @@ bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, i
  * block with one TMA box per half tile; without it, or for other blocks,
  * tiles are gathered four rows per TMA operation through index_map.  A
  * geometry that does not describe index_map gives wrong results.
+ * packed: [device] the block-ordered copy written by bsa_pool_blocks from
+ * the same q, k, v and index_map, or NULL.  With it the tensor-core kernel
+ * loads every tile (permuted blocks, windows ragged in H or W included) as
+ * one box per half tile; outputs still go to raster positions through
+ * index_map.  The CUDA-core kernel ignores it.
  * q, k, v, out: [device] BHSD of `dtype`; lse: [device] float [BH, N] or NULL.
  * bf16 with D = 128 and M = 128 runs on the tcgen05 tensor-core kernel;
  * other shapes (D <= 128, M <= 128) on the CUDA-core kernel. */
 bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype dtype,
                           int BH, int N, int D, const int32_t* index_map,
                           const int32_t* block_sizes, int J, int M, int prefix_blocks,
-                          const int32_t* geometry,
+                          const int32_t* geometry, const void* packed,
                           const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
                           float scale, void* out, float* lse, void* stream);
 
@@ -247,7 +257,7 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
 bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype,
                            int BH, int N, int D, const int32_t* index_map,
                            const int32_t* block_sizes, int J, int M, int prefix_blocks,
-                           const int32_t* geometry,
+                           const int32_t* geometry, const void* packed,
                            const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
                            const void* kbar_lp, const void* vbar_lp,
                            float scale, void* out, float* lse, void* stream);

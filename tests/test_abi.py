@@ -73,9 +73,11 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     lib = bsa._lib
     rc = lib.bsa_route_topk(None, None, 1, 4, 2, 8, 2, 1.0, 4, None, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
-    rc = lib.bsa_pool_blocks(1, 1, None, 1, 1, 8, 0, 1, 1, 4, 16, 1, 1, None, None, None, None)
+    rc = lib.bsa_pool_blocks(1, 1, None, 1, 1, 8, 0, 1, 1, 4, 16, 1, 1, None, None, None, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG
-    rc = lib.bsa_fwd_qouter(1, 1, 1, 1, 1, 64, 128, 1, 1, 1, 256, 0, None, 1, 1, 8, 1.0, 1, None, None)
+    rc = lib.bsa_pool_blocks(1, 1, None, 1, 1, 8, 16, 1, 1, 4, 16, 1, 1, None, None, None, 1, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "packed" in bsa.bsa_last_error()  # packed copy needs v
+    rc = lib.bsa_fwd_qouter(1, 1, 1, 1, 1, 64, 128, 1, 1, 1, 256, 0, None, None, 1, 1, 8, 1.0, 1, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
     rc = lib.bsa_route_topk(1, 1, 1, 4, 2, 8, 5, 1.0, 5, 1, 1, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # k > J

@@ -55,7 +55,7 @@ def test_tile_map_bit_exact(lib, grid, block, M, n_prefix, permuted):
 # ---------------------------------------------------------------- a2-a4, block granularity
 
 def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, force_simt=False,
-                    n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True):
+                    n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True, packed=None):
     pl = _pipeline()
     T, H, W = grid
     if cluster:
@@ -70,9 +70,15 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
                        perm=torch.as_tensor(perm, device=DEV) if permuted else None)
     lib.bsa_set_force_simt(force_simt)
     res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary,
-                                    pass_geometry=pass_geometry)
+                                    pass_geometry=pass_geometry, packed=packed)
     torch.cuda.synchronize()
     blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
+    if res.packed is not None:
+        # the block-ordered copy is a pure gather: bit-exact, zero rows past n_j
+        imap = oracle.index_map(blocks, M)
+        for w, x in enumerate((q, kk, v)):
+            want = x.float().numpy()[:, np.maximum(imap, 0)] * (imap >= 0)[None, :, :, None]
+            assert np.array_equal(res.packed[w].float().cpu().numpy(), want), "packed[%d]" % w
     P = len(oracle.tile_prefix(n_prefix, M))
     scale = D ** -0.5
     flagged = 0
@@ -116,24 +122,26 @@ def test_video_dit_shape_small_bf16(lib, force_simt):
                     force_simt=force_simt)
 
 
-@pytest.mark.parametrize("pass_geometry", [True, False])
-def test_windows_ragged_in_h_and_w_bf16(lib, pass_geometry):
+@pytest.mark.parametrize("pass_geometry,packed", [(True, False), (False, False), (True, True)])
+def test_windows_ragged_in_h_and_w_bf16(lib, pass_geometry, packed):
     # (4,4,8) windows over a (5,6,12) grid: full windows load as one TMA box,
-    # windows ragged in H or W are gathered row by row, the T tail is zero-filled
+    # windows ragged in H or W are gathered row by row, the T tail is zero-filled;
+    # with the packed copy every tile is one box
     _run_block_case(lib, 1, 2, (5, 6, 12), (4, 4, 8), 128, 128, 3, torch.bfloat16, 77, field=True,
-                    pass_geometry=pass_geometry)
+                    pass_geometry=pass_geometry, packed=packed)
 
 
-def test_dense_prefix_and_permutation_bf16(lib):
+@pytest.mark.parametrize("packed", [True, False])
+def test_dense_prefix_and_permutation_bf16(lib, packed):
     _run_block_case(lib, 1, 2, (4, 8, 16), (1, 1, 1), 128, 128, 2, torch.bfloat16, 31, n_prefix=200,
-                    permuted=True)
+                    permuted=True, packed=packed)
 
 
-@pytest.mark.parametrize("force_simt", [False, True])
-def test_summary_small_bf16(lib, force_simt):
+@pytest.mark.parametrize("force_simt,packed", [(False, True), (False, False), (True, True)])
+def test_summary_small_bf16(lib, force_simt, packed):
     # 256 text tokens + a (4,16,32) grid under a permutation: 2 prefix + 16 routed blocks, k=3
     _run_block_case(lib, 1, 2, (4, 16, 32), (1, 1, 1), 128, 128, 3, torch.bfloat16, 505, n_prefix=256,
-                    permuted=True, summary=True, cluster=True, force_simt=force_simt)
+                    permuted=True, summary=True, cluster=True, force_simt=force_simt, packed=packed)
 
 
 def test_summary_fp32_ragged(lib):
