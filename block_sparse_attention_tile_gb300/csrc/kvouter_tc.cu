@@ -52,7 +52,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 // setmaxnreg split: the producer / MMA warpgroup gives registers to the two
 // softmax warpgroups, which hold a whole 128-key row of S (one TMEM load
 // round trip per sub-tile instead of one per 32 columns).
-constexpr int kRegsLow = 96, kRegsHigh = 200, kRegsLaunch = 168;
+constexpr int kRegsLow = 88, kRegsHigh = 200, kRegsLaunch = 168;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
 template <int BS>
@@ -472,15 +472,30 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int hh = 0; hh < BS / 64; ++hh) {
                 uint32_t r[32];
+                if (full) {  // every key visible (full implies live): no selects
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c0 = hh * 64 + 2 * e;
-                    const bool v0 = live && (full || c0 < lim), v1 = live && (full || c0 + 1 < lim);
-                    const float p0 = v0 ? ptx::ex2(fmaf(x[c0], prm.scale_log2, -m)) : 0.f;
-                    const float p1 = v1 ? ptx::ex2(fmaf(x[c0 + 1], prm.scale_log2, -m)) : 0.f;
-                    sp[(2 * e) & 7] += p0;
-                    sp[(2 * e + 1) & 7] += p1;
-                    r[e] = ptx::pack_bf16x2(p0, p1);
+                    for (int e = 0; e < 32; ++e) {
+                        const int c0 = hh * 64 + 2 * e;
+                        const float p0 = ptx::ex2(fmaf(x[c0], prm.scale_log2, -m));
+                        const float p1 = ptx::ex2(fmaf(x[c0 + 1], prm.scale_log2, -m));
+                        sp[(2 * e) & 7] += p0;
+                        sp[(2 * e + 1) & 7] += p1;
+                        r[e] = ptx::pack_bf16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int c0 = hh * 64 + 2 * e;
+                        const bool v0 = live && c0 < lim, v1 = live && c0 + 1 < lim;
+                        // the mask selects the argument (exp2(-inf) = 0): the exp itself is
+                        // unconditional (inline asm is not speculated, so a masked exp
+                        // would become a branch per column)
+                        const float p0 = ptx::ex2(v0 ? fmaf(x[c0], prm.scale_log2, -m) : -CUDART_INF_F);
+                        const float p1 = ptx::ex2(v1 ? fmaf(x[c0 + 1], prm.scale_log2, -m) : -CUDART_INF_F);
+                        sp[(2 * e) & 7] += p0;
+                        sp[(2 * e + 1) & 7] += p1;
+                        r[e] = ptx::pack_bf16x2(p0, p1);
+                    }
                 }
                 ptx::tmem_st32(tS + hh * 32, r);
             }
