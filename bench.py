@@ -248,19 +248,42 @@ def kernel_source_hash(files):
     return h.hexdigest()[:16]
 
 
-def read_traffic(kernel):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, only if
-    it was taken on the kernel's current source files."""
+def read_traffic(workload):
+    """Per-launch DRAM bytes of the workload's dominant kernel from the committed
+    ncu summary, only if it was taken on the kernel's current source files."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
-        e = t[kernel]
+        e = t[workload]
         if e.get("source_hash") != kernel_source_hash(e["source_files"]):
             return None
         return e.get("bytes_per_launch")
     except (OSError, ValueError, KeyError):
         return None
+
+
+# ---------------------------------------------------------------- ranks
+
+def rank_seed(base, rank):
+    """Each replica draws its own inputs: the workload seed offset by the rank."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(values, world, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (the slowest rank
+    sets the job's time); a plain copy when world == 1."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(unit_flops, world, ms):
+    """Whole-job throughput: every rank processes one workload (weak scaling)."""
+    return world * unit_flops / (ms * 1e-3) / 1e12
 
 
 # ---------------------------------------------------------------- workloads
@@ -281,7 +304,7 @@ class BlockWorkload:
         D, M, k = w["D"], w["M"], w["k"]
         self.BH = w["B"] * w["heads"]
         self.dtype = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
-        seed = w["seed"] + 1000 * rank
+        seed = rank_seed(w["seed"], rank)
         with torch.no_grad():
             if self.summary:
                 self.q, self.k, self.v = synthetic.cluster_qkv(self.BH, n_text, T * H * W, D, seed, self.dtype,
@@ -384,7 +407,7 @@ class BlockWorkload:
             roof = {"bound": "alu", "achieved": flops / attn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
                     "peak_kind": "FP32 lanes: SMs x 128 x 2 x max SM clock"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = read_traffic("attention") if self.name == DEFAULT else None
+        roof["traffic"] = read_traffic(self.name)
         roof["kernel"] = "bsa_fwd_summary attention" if self.summary else "bsa_fwd_qouter attention"
         roof["algorithmic_flops_per_launch"] = flops
         pool_gbs = pool_bytes / (stage_ms["pool"] * 1e-3) / 1e9
@@ -422,7 +445,7 @@ class TokenWorkload:
         from block_sparse_attention_tile_gb300 import bsa, synthetic
         self.name, self.w, self.dev, self.torch, self.np = name, w, dev, torch, np
         B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
-        seed = w["seed"] + 1000 * rank
+        seed = rank_seed(w["seed"], rank)
         self.q = synthetic.normal((B, T, HQ, D), seed, device=dev, dtype=torch.bfloat16)
         self.k = synthetic.normal((B, T, H, D), seed + 1, device=dev, dtype=torch.bfloat16)
         self.v = synthetic.normal((B, T, H, D), seed + 2, device=dev, dtype=torch.bfloat16)
@@ -518,7 +541,7 @@ class TokenWorkload:
             roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
                     "peak_kind": peak_kind + " bf16 sustained"}
         roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = None
+        roof["traffic"] = read_traffic(self.name)
         roof["kernel"] = "bsa_fwd_kvouter partials (K1)"
         roof["algorithmic_flops_per_launch"] = flops
         # combine: reads every written partial (bf16) + LSE, writes O (bf16) + LSE
@@ -645,10 +668,7 @@ def gpu_arm(args):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
 
     # max over ranks
-    t = torch.tensor([ms_total, e2e_ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_total, e2e_ms = t.tolist()
+    ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], world, dev)
     ms_step = ms_total / args.steps
 
     if rank == 0:
@@ -660,7 +680,7 @@ def gpu_arm(args):
                        "parallelism": "replicas%d" % world if world > 1 else "single"})
         line = {
             "metric": METRIC,
-            "value": world * flops / (ms_step * 1e-3) / 1e12,
+            "value": job_tflops(flops, world, ms_step),
             "unit": "TFLOP/s",
             "n_gpus": world,
             "steps": args.steps,
@@ -675,7 +695,7 @@ def gpu_arm(args):
             "stages_us": {sn: round(v * 1e3, 1) for sn, v in stage_ms.items()},
             "roofline": roof,
             "rooflines_secondary": secondary,
-            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": wl.launches_per_step * args.steps,
             "clocks": clk,
