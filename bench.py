@@ -372,6 +372,78 @@ class BlockWorkload:
     def run_with(self, dev_inputs):
         self.step(None, *dev_inputs)
 
+    def run_heads(self, q, k, v, h0, h1, packed_chunk):
+        """Pool, route and attention for heads [h0, h1) only (the heads are
+        independent): every entry point takes the head count and pointers
+        offset to the first head; the tile map is shared."""
+        from block_sparse_attention_tile_gb300 import bsa
+        w, g = self.w, self.geom
+        D, M, kk = w["D"], w["M"], w["k"]
+        sl = slice(h0, h1)
+        nh = h1 - h0
+        bsa.bsa_pool_blocks(q[sl], k[sl], v[sl] if self.vbar is not None else None, nh, self.N, D, self.im,
+                            self.bs, self.J, M, self.qbar[sl], self.kbar[sl],
+                            self.vbar[sl] if self.vbar is not None else None,
+                            self.kbar_lp[sl] if self.summary else None, self.vbar_lp[sl] if self.summary else None,
+                            packed=packed_chunk)
+        bsa.bsa_route_topk(self.qbar[sl, self.P:], self.kbar[sl, self.P:], nh, self.Jr, D, self.J * D, kk,
+                           self.scale, kk, self.q2k[sl], self.q2n[sl])
+        if self.summary:
+            bsa.bsa_fwd_summary(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
+                                self.q2k[sl], self.q2n[sl], kk, self.kbar_lp[sl], self.vbar_lp[sl], self.scale,
+                                self.out[sl], self.lse[sl], packed=packed_chunk)
+        else:
+            bsa.bsa_fwd_qouter(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
+                               self.q2k[sl], self.q2n[sl], kk, self.scale, self.out[sl], self.lse[sl],
+                               packed=packed_chunk)
+
+    def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=4):
+        """End-to-end step with host buffers, pipelined by heads: chunk c's
+        inputs are copied in on a copy stream while chunk c-1 computes, and each
+        chunk's output is copied out as soon as it is done."""
+        torch = self.torch
+        g = self.geom
+        comp = torch.cuda.current_stream()
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        chunks = [(h0, min(self.BH, h0 + heads_per_chunk)) for h0 in range(0, self.BH, heads_per_chunk)]
+        per_head = self.J * self.w["M"] * self.w["D"]
+        pk = (torch.empty((3 * heads_per_chunk * per_head,), dtype=self.dtype, device=self.dev)
+              if self.packed is not None else None)
+        dq, dk, dv = d_in
+        hq, hk, hv = h_in
+        (hout,) = h_out
+
+        def step():
+            from block_sparse_attention_tile_gb300 import bsa
+            start = torch.cuda.Event()
+            start.record(comp)
+            h2d_s.wait_event(start)
+            ready = []
+            for h0, h1 in chunks:
+                with torch.cuda.stream(h2d_s):
+                    for d, h in ((dq, hq), (dk, hk), (dv, hv)):
+                        d[h0:h1].copy_(h[h0:h1], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(h2d_s)
+                ready.append(e)
+            bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, self.w["M"], self.im, self.bs)
+            for (h0, h1), e in zip(chunks, ready):
+                comp.wait_event(e)
+                # a contiguous [3, h1 - h0, J, M, D] view for this chunk's packed copy
+                pkc = None if pk is None else pk[:3 * (h1 - h0) * per_head].view(3, h1 - h0, self.J, self.w["M"],
+                                                                                   self.w["D"])
+                self.run_heads(dq, dk, dv, h0, h1, pkc)
+                done = torch.cuda.Event()
+                done.record(comp)
+                d2h_s.wait_event(done)
+                with torch.cuda.stream(d2h_s):
+                    hout[h0:h1].copy_(self.out[h0:h1], non_blocking=True)
+            fin = torch.cuda.Event()
+            fin.record(d2h_s)
+            comp.wait_event(fin)
+
+        return step, 1 + 3 * len(chunks)
+
     def algorithmic(self):
         """Valid (query, key) pairs the attention scores, x 4*D FLOPs."""
         torch = self.torch
@@ -647,12 +719,18 @@ def gpu_arm(args):
     h2d = sum(x.numel() * x.element_size() for x in ins)
     d2h = sum(x.numel() * x.element_size() for x in outs)
 
-    def e2e_step():
+    def e2e_plain():
         for d, h in zip(d_in, h_in):
             d.copy_(h, non_blocking=True)
         wl.run_with(d_in)
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
+
+    if hasattr(wl, "make_e2e"):
+        e2e_step, e2e_launches = wl.make_e2e(h_in, d_in, h_out)
+    else:
+        e2e_step, e2e_launches = e2e_plain, wl.launches_per_step
+    ref_out = [x.clone() for x in outs]  # the device-only run's result, for the check below
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -666,6 +744,11 @@ def gpu_arm(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    # the pipelined end-to-end path must return exactly what the device-only run computed
+    e2e_match = all(torch.equal(h.to(dev), r) for h, r in zip(h_out, ref_out))
+    del ref_out
+    if not e2e_match:
+        raise RuntimeError("end-to-end output differs from the device-only run")
 
     # max over ranks
     ms_total, e2e_ms = max_over_ranks([ms_total, e2e_ms], world, dev)
@@ -696,7 +779,10 @@ def gpu_arm(args):
             "roofline": roof,
             "rooflines_secondary": secondary,
             "e2e": {"value": job_tflops(flops, world, e2e_ms), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "pipelining": ("head chunks: copies in and out overlap the compute of other heads"
+                                   if hasattr(wl, "make_e2e") else "none: copy in, compute, copy out"),
+                    "gpu_launches_per_step": e2e_launches, "matches_device_run": e2e_match},
             "gpu_launches": wl.launches_per_step * args.steps,
             "clocks": clk,
         }

@@ -13,9 +13,14 @@
 
 namespace bsa {
 
-constexpr int kRouteRows = 16;   // query rows per CTA
-constexpr int kRouteCols = 64;   // key columns per staged tile
+constexpr int kRouteCols = 128;  // key columns per staged tile
 constexpr int kRouteThreads = 256;
+// Register tile of the contraction: thread (rg, cg) = (tid / 32, tid % 32)
+// owns rows TR*rg .. TR*rg + TR-1 and columns cg + 32c (c < kTC) of the
+// staged tile, so a CTA covers 8*TR query rows.  TR = 4 (32 rows) when the
+// rows' E fits in shared memory, else 2 or 1.
+constexpr int kTC = 4;
+static_assert(32 * kTC == kRouteCols, "route register tiling");
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     f = f + 0.0f;  // -0 -> +0 so that equal values give equal keys
@@ -24,12 +29,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // DPC: the padded head dimension when it is known at compile time (0 = any).
-template <int DPC>
+template <int DPC, int TR>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     const float* __restrict__ qbar, const float* __restrict__ kbar, int J, int D, int Dp_rt,
     long long head_stride, int k, float scale, int kmax, int32_t* __restrict__ q2k_idx,
     int32_t* __restrict__ q2k_num) {
     const int Dp = DPC ? DPC : Dp_rt;
+    constexpr int kRouteRows = 8 * TR;  // query rows per CTA
+    constexpr int kTR = TR;
     extern __shared__ __align__(16) float smem[];
     float* qs = smem;                              // [kRouteRows][Dp]
     float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp + 4]
@@ -46,11 +53,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
         const int r = idx / Dp, d = idx % Dp;
         qs[idx] = (r < nrows && d < D) ? qh[(long long)(row0 + r) * D + d] : 0.f;
     }
-    const int r = tid / 16;        // row of this thread
-    const int cg = tid % 16;       // column group: columns cg + 16*c
+    const int rg = tid / 32;       // rows kTR*rg .. kTR*rg + kTR - 1
+    const int cg = tid % 32;       // columns cg + 32*c of the tile
     // The key tile is staged through registers one tile ahead, so its L2
     // latency overlaps the dot products of the previous tile.
-    constexpr int kMaxV4 = kRouteCols * 256 / 4 / kRouteThreads;  // float4 per thread for D <= 256
+    constexpr int kMaxV4 = kRouteCols * (DPC ? DPC : 256) / 4 / kRouteThreads;  // float4 per thread
     const bool vec = (D % 4) == 0;
     const int nv4 = kRouteCols * (Dp / 4);                          // float4 per tile
     float4 pre[kMaxV4];
@@ -86,24 +93,35 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
         }
         __syncthreads();
         if (vec && c0 + kRouteCols < J) prefetch(c0 + kRouteCols);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const float4* q4 = reinterpret_cast<const float4*>(qs + r * Dp);
+        // each output accumulates its dot product over d in ascending order
+        float acc[kTR][kTC];
+#pragma unroll
+        for (int i = 0; i < kTR; ++i)
+#pragma unroll
+            for (int c = 0; c < kTC; ++c) acc[i][c] = 0.f;
         for (int d4 = 0; d4 < Dp / 4; ++d4) {
-            const float4 a = q4[d4];
+            float4 a[kTR], b[kTC];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float4 b = reinterpret_cast<const float4*>(ks + (cg + 16 * c) * Dk)[d4];
-                acc[c] = fmaf(a.x, b.x, acc[c]);
-                acc[c] = fmaf(a.y, b.y, acc[c]);
-                acc[c] = fmaf(a.z, b.z, acc[c]);
-                acc[c] = fmaf(a.w, b.w, acc[c]);
+            for (int i = 0; i < kTR; ++i) a[i] = reinterpret_cast<const float4*>(qs + (kTR * rg + i) * Dp)[d4];
+#pragma unroll
+            for (int c = 0; c < kTC; ++c) b[c] = reinterpret_cast<const float4*>(ks + (cg + 32 * c) * Dk)[d4];
+#pragma unroll
+            for (int i = 0; i < kTR; ++i)
+#pragma unroll
+                for (int c = 0; c < kTC; ++c) {
+                    acc[i][c] = fmaf(a[i].x, b[c].x, acc[i][c]);
+                    acc[i][c] = fmaf(a[i].y, b[c].y, acc[i][c]);
+                    acc[i][c] = fmaf(a[i].z, b[c].z, acc[i][c]);
+                    acc[i][c] = fmaf(a[i].w, b[c].w, acc[i][c]);
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < kTR; ++i)
+#pragma unroll
+            for (int c = 0; c < kTC; ++c) {
+                const int col = c0 + cg + 32 * c;
+                if (col < J) E[(kTR * rg + i) * J + col] = acc[i][c] * scale;
             }
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int col = c0 + cg + 16 * c;
-            if (col < J) E[r * J + col] = acc[c] * scale;
-        }
     }
     __syncthreads();
 
@@ -193,11 +211,21 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     BSA_REQUIRE(k >= 1 && k <= J && kmax >= k, "route: need 1 <= k <= J and k <= kmax");
     BSA_REQUIRE(head_stride >= (int64_t)J * D, "route: head_stride smaller than J*D");
     const int Dp = (D + 3) / 4 * 4;
-    const size_t smem = sizeof(float) * ((size_t)kRouteRows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)kRouteRows * J);
+    // the most rows per CTA whose E rows, query rows and key tile fit in shared memory
+    auto smem_for = [&](int rows) {
+        return sizeof(float) * ((size_t)rows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)rows * J);
+    };
+    int TR = 4;
+    while (TR > 1 && smem_for(8 * TR) > 227 * 1024) TR >>= 1;
+    const size_t smem = smem_for(8 * TR);
     if (smem > 227 * 1024) return fail(BSA_ERR_UNSUPPORTED, "route: J=%d D=%d needs too much shared memory", J, D);
-    auto kern = Dp == 128 ? route_topk_kernel<128> : (Dp == 64 ? route_topk_kernel<64> : route_topk_kernel<0>);
+    using Kern = void (*)(const float*, const float*, int, int, int, long long, int, float, int, int32_t*, int32_t*);
+    Kern kern;
+    if (TR == 4) kern = Dp == 128 ? route_topk_kernel<128, 4> : (Dp == 64 ? route_topk_kernel<64, 4> : route_topk_kernel<0, 4>);
+    else if (TR == 2) kern = Dp == 128 ? route_topk_kernel<128, 2> : (Dp == 64 ? route_topk_kernel<64, 2> : route_topk_kernel<0, 2>);
+    else kern = Dp == 128 ? route_topk_kernel<128, 1> : (Dp == 64 ? route_topk_kernel<64, 1> : route_topk_kernel<0, 1>);
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid((J + kRouteRows - 1) / kRouteRows, BH);
+    dim3 grid((J + 8 * TR - 1) / (8 * TR), BH);
     kern<<<grid, kRouteThreads, smem, as_stream(stream)>>>(qbar, kbar, J, D, Dp, (long long)head_stride, k, scale,
                                                           kmax, q2k_idx, q2k_num);
     return check_launch("route_topk_kernel");

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(256) pool_kernel(
 // halves are added with one shuffle.  The block's token ids are staged in
 // shared memory first, so no row load waits on an index load.
 template <typename T>
-__global__ void __launch_bounds__(256) pool_rows256_kernel(
+__global__ void __launch_bounds__(256, 2) pool_rows256_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D,
     const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M, int BH,
     long long items, float* __restrict__ qbar, float* __restrict__ kbar, float* __restrict__ vbar,
@@ -196,9 +196,16 @@ __global__ void __launch_bounds__(256) pool_rows256_kernel(
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const T* e8 = reinterpret_cast<const T*>(&raw[u]);
+            if constexpr (sizeof(T) == 4) {  // four floats: read the words directly
+                acc[0] += __uint_as_float(raw[u].x);
+                acc[1] += __uint_as_float(raw[u].y);
+                acc[2] += __uint_as_float(raw[u].z);
+                acc[3 % VEC] += __uint_as_float(raw[u].w);
+            } else {
+                const T* e8 = reinterpret_cast<const T*>(&raw[u]);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+                for (int e = 0; e < VEC; ++e) acc[e] += to_f32(e8[e]);
+            }
         }
         if (pk) {
 #pragma unroll

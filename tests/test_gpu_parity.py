@@ -231,6 +231,23 @@ def test_kvouter_group_sizes(lib, HQ, H, BS):
     assert np.abs(l_kv[0].cpu().numpy() - L).max() <= 2e-3
 
 
+@pytest.mark.parametrize("J,D", [(1500, 128), (3000, 128), (700, 72)])
+def test_route_rows_per_cta_variants(lib, J, D):
+    """Route alone at block counts that need 16 or 8 query rows per CTA (the
+    E rows of a CTA live in shared memory) and at a head dim without the
+    compile-time specialisation; lists bit-exact except reported near ties."""
+    BH, k = 2, J // 10
+    qbar = synthetic.normal((BH, J, D), 901 + J, device=DEV)
+    kbar = synthetic.normal((BH, J, D), 902 + J, device=DEV)
+    idx = torch.empty((BH, J, k + 3), dtype=torch.int32, device=DEV)
+    num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
+    lib.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, D ** -0.5, k + 3, idx, num)
+    torch.cuda.synchronize()
+    for bh in range(BH):
+        E = oracle.routing_scores(f64(qbar[bh]), f64(kbar[bh]), D)
+        check_route(idx[bh].cpu().numpy(), num[bh].cpu().numpy(), E, k)
+
+
 # ---------------------------------------------------------------- device-side error reporting
 
 def test_out_of_range_block_index_is_reported_not_faulted(lib):
