@@ -12,18 +12,20 @@
 //
 // Design (ours, for sm_103a).  One CTA per (head, query block), 12 warps,
 // one CTA per SM (TMEM: S0 [0,128), S1 [128,256), O [256,384) of 512 columns).
-//   warp 0      producer: TMA loads straight from the BHSD tensors into
+//   warps 0, 2  producers: TMA loads straight from the BHSD tensors into
 //               128-byte swizzled K-major tiles, no pack pass: a (bT,bH,bW)
 //               window is ONE box of a 5-D (D, W, H, T, head) tensor map per
 //               64-column half (zero-filled past T, so the valid rows come
-//               first as in the tile map), a dense-prefix block or a summary
-//               tile is one 128-row box, and any other block (a permutation,
-//               a window ragged in H or W) is gathered four rows per
-//               tile::gather4 through the index map.  TMA costs about the same
-//               per operation whatever its size, so boxes are ~8x faster than
-//               gathering.  A 5-stage ring in MMA consumption order
-//               K0 K1 | V0 K2 | V1 K3 | ... gives each load about two tiles of
-//               lead time; the next entry's row ids are fetched while it waits.
+//               first as in the tile map), a dense-prefix block, a summary tile
+//               or a block of the packed copy is one 128-row box, and any other
+//               block (a permutation, a window ragged in H or W) is gathered
+//               four rows per tile::gather4 through the index map.  TMA costs
+//               about the same per operation whatever its size, so boxes are
+//               ~8x faster than gathering.  Warp 0 loads Q and then the K tiles
+//               into a 3-stage K ring, warp 2 the V tiles into a 2-stage V ring:
+//               a K tile is free as soon as S_j is done, so K runs about three
+//               tiles ahead (one shared ring let it start only one tile ahead,
+//               and the MMA issuer waited ~0.45 us per tile for K).
 //   warp 1      TMEM owner and single-thread MMA issuer: S0, S1, then
 //               PV_j, S_{j+2} for every j.  S is double buffered, so QK of tile
 //               j+1 (and j+2) runs while the softmax works on tile j.
@@ -54,7 +56,8 @@ constexpr int kBM = 128;          // query rows per query block
 constexpr int kBN = 128;          // keys per tile
 constexpr int kHD = 128;          // head dim
 constexpr int kThreads = 384;
-constexpr int kStages = 5;        // K/V ring depth (32 KB each)
+constexpr int kKStages = 3, kVStages = 2;      // K ring and V ring (32 KB stages)
+constexpr int kStages = kKStages + kVStages;
 constexpr int kMaxList = 512;     // key tiles per query block, virtual tiles included
 constexpr int kMaxVirtual = 8;    // summary tiles (<= 1024 routed blocks)
 constexpr uint32_t kTileBytes = kBN * kHD * 2;       // 32 KB
@@ -155,21 +158,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
             raise_status(status, BSA_ERR_TIMEOUT);
             return false;
         }
-    }
-}
-
-// Ring entry e in MMA consumption order S0 S1 | PV0 S2 | PV1 S3 | ... | PV(n-1):
-// K0 K1 | V0 K2 | V1 K3 | ... | V(n-2) | V(n-1)  (2n entries).
-__device__ __forceinline__ void decode_entry(int e, int n, int& j, bool& isV) {
-    if (n == 1) { j = 0; isV = e == 1; return; }
-    if (e < 2) { j = e; isV = false; return; }
-    const int t = e - 2;
-    if (t < 2 * (n - 2)) {
-        j = (t >> 1) + ((t & 1) ? 2 : 0);
-        isV = !(t & 1);
-    } else {
-        j = (n - 2) + (t - 2 * (n - 2));
-        isV = true;
     }
 }
 
@@ -284,12 +272,15 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
-    const int n_entries = 2 * n;
 
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-      if (warp == 0) {
-        // ------------------------------------------------------------ producer
+      if (warp == 0 || warp == 2) {
+        // ------------------------------------------------------------ producers
+        // warp 0: Q, then the K ring; warp 2: the V ring.  Separate rings let each
+        // load start as soon as its own stage is free: a K tile is dead once
+        // S_j is done, so K runs about three tiles ahead, V two.
+        const bool vprod = warp == 2;
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
@@ -332,35 +323,33 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 rows[u] = (int)(head_row + tok);
             }
         };
-        if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
-        __syncwarp();
-        {
+        if (!vprod) {
+            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
+            __syncwarp();
             const TileSrc src = tile_source(qb, prm, bh);
             int rq[4] = {0, 0, 0, 0};
             if (src.mode == 0) gather_rows(qb, nq, rq);
             issue_tile(base + OFF_Q, src, rq, &tm_q, &tm_qr, &tm_q5, bar(BAR_Q));
         }
-        // Ring entry e: its tile's source comes from the table built in the
-        // prologue; gathered row ids (mode 0 only) are loaded one entry ahead.
+        // Tile j's source comes from the table built in the prologue; gathered
+        // row ids (mode 0 only) are loaded one tile ahead.
         const int4* srcs = reinterpret_cast<const int4*>(sm + OFF_SRC);
+        const int RS = vprod ? kVStages : kKStages;
+        const int sbase = vprod ? kKStages : 0;
         int issued = 0;
         int rows_next[4] = {0, 0, 0, 0};
-        int j_next = 0;
-        bool v_next = false;
         int4 src_next = make_int4(0, 0, 0, 0);
-        auto prepare = [&](int e) {
-            decode_entry(e, n, j_next, v_next);
-            src_next = srcs[j_next];
-            if ((src_next.x & 3) == 0) gather_rows(list[j_next], nvalid[j_next], rows_next);
+        auto prepare = [&](int jt) {
+            src_next = srcs[jt];
+            if ((src_next.x & 3) == 0) gather_rows(list[jt], nvalid[jt], rows_next);
         };
-        if (n_entries > 0) prepare(0);
-        for (int e = 0; e < n_entries; ++e) {
+        if (n > 0) prepare(0);
+        for (int jt = 0; jt < n; ++jt) {
             const int4 src = src_next;
-            const bool isV = v_next;
             const int rows[4] = {rows_next[0], rows_next[1], rows_next[2], rows_next[3]};
-            if (e + 1 < n_entries) prepare(e + 1);
-            const int st = e % kStages;
-            const uint32_t ph = (uint32_t)(e / kStages) & 1u;
+            if (jt + 1 < n) prepare(jt + 1);
+            const int st = sbase + jt % RS;
+            const uint32_t ph = (uint32_t)(jt / RS) & 1u;
             if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) break;
             if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
             __syncwarp();
@@ -369,55 +358,55 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const bool virt = (src.x & 4) != 0;
             const uint32_t fb = bar(BAR_FULL + st);
             if (mode == 0) {
-                const CUtensorMap* mg = isV ? &tm_v : &tm_k;
+                const CUtensorMap* mg = vprod ? &tm_v : &tm_k;
                 const uint32_t d = dst + 4 * lane * 128;
                 ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], fb);
                 ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], fb);
             } else if (lane == 0) {
                 if (mode == 1) {
-                    const CUtensorMap* mr = virt ? (isV ? &tm_vb : &tm_kb) : (isV ? &tm_vr : &tm_kr);
+                    const CUtensorMap* mr = virt ? (vprod ? &tm_vb : &tm_kb) : (vprod ? &tm_vr : &tm_kr);
                     ptx::tma_load_2d(dst, mr, 0, src.y, fb);
                     ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.y, fb);
                 } else {
-                    const CUtensorMap* m5 = isV ? &tm_v5 : &tm_k5;
+                    const CUtensorMap* m5 = vprod ? &tm_v5 : &tm_k5;
                     const int c2 = src.z & 0xffff, c3 = src.z >> 16;
                     ptx::tma_load_5d(dst, m5, 0, src.y, c2, c3, src.w, fb);
                     ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.y, c2, c3, src.w, fb);
                 }
             }
-            issued = e + 1;
+            issued = jt + 1;
         }
         if (*abort_flag) {
             // drain: wait (bounded) for this warp's copies still in flight
             const uint64_t t0 = ptx::globaltimer();
-            for (int e = max(0, issued - kStages); e < issued; ++e)
-                while (!ptx::mbar_try_wait(bar(BAR_FULL + e % kStages), (uint32_t)(e / kStages) & 1u) &&
+            for (int jt = max(0, issued - RS); jt < issued; ++jt)
+                while (!ptx::mbar_try_wait(bar(BAR_FULL + sbase + jt % RS), (uint32_t)(jt / RS) & 1u) &&
                        ptx::globaltimer() - t0 < kWaitNs) {
                 }
-            while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
+            if (!vprod)
+                while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && n > 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kBM, kHD, true);
-            int ec = 0;  // ring entries consumed
             bool ok = wait_bar(bar(BAR_Q), 0, abort_flag, prm.status);
-            auto take = [&](uint32_t& addr) -> bool {
-                const int st = ec % kStages;
-                if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(ec / kStages) & 1u, abort_flag, prm.status))
-                    return false;
+            // K_j sits in K stage j % kKStages, V_j in V stage j % kVStages
+            auto take = [&](int j, bool isV, uint32_t& addr) -> bool {
+                const int RS = isV ? kVStages : kKStages;
+                const int st = (isV ? kKStages : 0) + j % RS;
+                if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(j / RS) & 1u, abort_flag, prm.status)) return false;
                 ptx::tc_fence_after();
                 addr = base + OFF_RING + st * kTileBytes;
                 return true;
             };
-            auto release = [&]() {
-                ptx::mma_commit(bar(BAR_EMPTY + ec % kStages));
-                ++ec;
+            auto release = [&](int j, bool isV) {
+                ptx::mma_commit(bar(BAR_EMPTY + (isV ? kKStages + j % kVStages : j % kKStages)));
             };
             auto issue_s = [&](int j) -> bool {
                 uint32_t ka;
-                if (!take(ka)) return false;
+                if (!take(j, false, ka)) return false;
                 const uint32_t qa = base + OFF_Q;
                 const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
 #pragma unroll
@@ -427,13 +416,13 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 kk > 0);
                 }
                 ptx::mma_commit(bar(BAR_SF + (j & 1)));
-                release();
+                release(j, false);
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
                 if (!wait_bar(bar(BAR_PF + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, prm.status)) return false;
                 uint32_t va;
-                if (!take(va)) return false;
+                if (!take(j, true, va)) return false;
                 const uint32_t aP = tmem + (uint32_t)(j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -443,7 +432,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ptx::mma_ts(tmem + 256 + (uint32_t)(j & 1) * 128, aP + kk * 8,
                                 ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO, (j >= 2 || kk > 0) ? 1u : 0u);
                 }
-                release();
+                release(j, true);
                 if (j + 2 >= n) ptx::mma_commit(bar(BAR_OF + (j & 1)));  // last product into O_{j&1}
                 return true;
             };

@@ -309,14 +309,16 @@ __global__ void __launch_bounds__(256) combine_kernel(
 
 // bf16 partials with D = 128 (256-byte rows): one warp per row; half-warp
 // hf takes the slots s = hf, hf+2, ... and lane l of it the 16-byte chunk l
-// (channels 8l .. 8l+7), four slots in flight per lane; the halves are
-// added with one shuffle.  Same arithmetic as the generic kernel: weights
-// exp(L_s - L) with L = a + log sum exp(L_s - a), fp32 accumulation.
+// (channels 8l .. 8l+7).  The partial rows depend only on the slot count, so
+// they are requested together with the LSEs (up to 16 slots per warp in
+// flight) before the log-sum-exp reductions; the halves are added with one
+// shuffle.  Same arithmetic as the generic kernel: weights exp(L_s - L) with
+// L = a + log sum exp(L_s - a), fp32 accumulation.
 template <typename TO>
 __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
     const __nv_bfloat16* __restrict__ obuf, const float* __restrict__ lsebuf, const int32_t* __restrict__ nslots,
     int HQ, int H, int S, long long rows, TO* __restrict__ out, float* __restrict__ lse) {
-    constexpr int D = 128, U = 4;
+    constexpr int D = 128, U = 8;
     const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -325,9 +327,16 @@ __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
     const int G = HQ / H;
     const int n = max(0, min(__ldg(nslots + bt * H + hq / G), S));
     const float* L = lsebuf + row * S;
-    const float l_own = lane < n ? __ldg(L + lane) : -CUDART_INF_F;  // S <= 32 on this path
-    const float a = warp_max(l_own);
     const int hf = lane >> 4, ch = lane & 15;
+    const uint4* base = reinterpret_cast<const uint4*>(obuf + row * S * D) + ch;
+    const float l_own = lane < n ? __ldg(L + lane) : -CUDART_INF_F;  // S <= 32 on this path
+    uint4 raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int s = hf + 2 * u;
+        raw[u] = s < n ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float a = warp_max(l_own);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -335,26 +344,29 @@ __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
     if (a != -CUDART_INF_F) {
         const float total = warp_sum(l_own == -CUDART_INF_F ? 0.f : __expf(l_own - a));
         Lrow = a + __logf(total);
-        const uint4* base = reinterpret_cast<const uint4*>(obuf + row * S * D) + ch;
-        for (int s0 = 0; s0 < n; s0 += 2 * U) {  // warp-uniform bound: the shuffles need every lane
-            uint4 raw[U];
-            float w[U];
+    }
+    for (int s0 = 0; s0 < n; s0 += 2 * U) {  // warp-uniform bound: the shuffles need every lane
+        if (s0 > 0) {
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int s = s0 + hf + 2 * u;
-                const float ls = __shfl_sync(0xffffffffu, l_own, s & 31);
-                const bool use = s < n && ls != -CUDART_INF_F;
-                w[u] = use ? __expf(ls - Lrow) : 0.f;
-                raw[u] = use ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
+                raw[u] = s < n ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
             }
+        }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + hf + 2 * u;
+            const float ls = __shfl_sync(0xffffffffu, l_own, s & 31);
+            // slots past n or with L_s = -inf take no part (their rows are not used,
+            // whatever they hold)
+            if (s < n && ls != -CUDART_INF_F) {
+                const float w = __expf(ls - Lrow);
                 const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 f = __bfloat1622float2(p2[e]);
-                    acc[2 * e] = fmaf(w[u], f.x, acc[2 * e]);
-                    acc[2 * e + 1] = fmaf(w[u], f.y, acc[2 * e + 1]);
+                    acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
+                    acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
                 }
             }
         }

@@ -215,8 +215,17 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     auto smem_for = [&](int rows) {
         return sizeof(float) * ((size_t)rows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)rows * J);
     };
+    // and, where possible, at least two CTAs per SM (few blocks: fewer rows per CTA)
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                      cudaSuccess)
+            sms = 1;
+    }
+    auto ctas = [&](int rows) { return (long long)((J + rows - 1) / rows) * BH; };
     int TR = 4;
-    while (TR > 1 && smem_for(8 * TR) > 227 * 1024) TR >>= 1;
+    while (TR > 1 && (smem_for(8 * TR) > 227 * 1024 || ctas(8 * TR) < 2LL * sms)) TR >>= 1;
     const size_t smem = smem_for(8 * TR);
     if (smem > 227 * 1024) return fail(BSA_ERR_UNSUPPORTED, "route: J=%d D=%d needs too much shared memory", J, D);
     using Kern = void (*)(const float*, const float*, int, int, int, long long, int, float, int, int32_t*, int32_t*);
