@@ -483,16 +483,15 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
             const bool real = blk >= 0 || nv == 0;
             if (real) {
-                if (nv >= kBN) {
+                if (nv < kBN) {
 #pragma unroll
-                    for (int c = 0; c < kBN; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) {
-                        x[c] = c < nv ? x[c] : -CUDART_INF_F;
-                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
-                    }
+                    for (int c = 0; c < kBN; ++c) x[c] = c < nv ? x[c] : -CUDART_INF_F;
                 }
+                // three-input max: two columns per instruction into 8 partial maxima
+#pragma unroll
+                for (int c = 0; c < kBN; c += 16)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
             } else {
@@ -530,11 +529,25 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int u = 0; u < 8; ++u) sp[u] = 0.f;
             const bool live = m_ref != -CUDART_INF_F;
             if (real) {
-                // x holds raw Q.K: one FMA folds the scale and subtracts the reference
+                // x holds raw Q.K: one FMA folds the scale and subtracts the reference;
+                // pairs of columns share one f32x2 FMA and one f32x2 add (sp[c & 7]
+                // accumulates exactly as with scalar adds)
+                const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+                const float2 nm2 = make_float2(-m_ref, -m_ref);
+                float2 acc2[4];
 #pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = live ? ptx::ex2(fmaf(x[c], prm.scale_log2, -m_ref)) : 0.f;
-                    sp[c & 7] += x[c];
+                for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < kBN; c += 2) {
+                    const float2 a = ptx::ffma2(make_float2(x[c], x[c + 1]), sc2, nm2);
+                    x[c] = live ? ptx::ex2(a.x) : 0.f;
+                    x[c + 1] = live ? ptx::ex2(a.y) : 0.f;
+                    acc2[(c >> 1) & 3] = ptx::fadd2(acc2[(c >> 1) & 3], make_float2(x[c], x[c + 1]));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sp[2 * u] = acc2[u].x;
+                    sp[2 * u + 1] = acc2[u].y;
                 }
             } else {
 #pragma unroll
