@@ -307,56 +307,64 @@ __global__ void __launch_bounds__(256) combine_kernel(
     }
 }
 
-// bf16 partials with D = 128 (256-byte rows): one warp per row; half-warp
-// hf takes the slots s = hf, hf+2, ... and lane l of it the 16-byte chunk l
-// (channels 8l .. 8l+7).  The partial rows depend only on the slot count, so
-// they are requested together with the LSEs (up to 16 slots per warp in
-// flight) before the log-sum-exp reductions; the halves are added with one
-// shuffle.  Same arithmetic as the generic kernel: weights exp(L_s - L) with
+// bf16 partials with D = 128 (256-byte rows): one half-warp per (token,
+// query head) row, two rows per warp.  Lane l of a half-warp holds the
+// 16-byte chunk l (channels 8l .. 8l+7) of every slot row, so one load
+// instruction of the half-warp reads a whole 256-byte partial row.  The
+// partial rows depend only on the slot count, so up to 8 of them are requested
+// together with the LSEs, before the log-sum-exp reductions (over the 16
+// lanes).  Same arithmetic as the generic kernel: weights exp(L_s - L) with
 // L = a + log sum exp(L_s - a), fp32 accumulation.
 template <typename TO>
 __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
     const __nv_bfloat16* __restrict__ obuf, const float* __restrict__ lsebuf, const int32_t* __restrict__ nslots,
     int HQ, int H, int S, long long rows, TO* __restrict__ out, float* __restrict__ lse) {
     constexpr int D = 128, U = 8;
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const int hq = (int)(row % HQ);
-    const long long bt = row / HQ;
-    const int G = HQ / H;
-    const int n = max(0, min(__ldg(nslots + bt * H + hq / G), S));
-    const float* L = lsebuf + row * S;
-    const int hf = lane >> 4, ch = lane & 15;
-    const uint4* base = reinterpret_cast<const uint4*>(obuf + row * S * D) + ch;
-    const float l_own = lane < n ? __ldg(L + lane) : -CUDART_INF_F;  // S <= 32 on this path
+    const int lane = threadIdx.x & 31, ch = lane & 15;
+    const long long row = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 2 + (lane >> 4);
+    const bool has_row = row < rows;
+    int n = 0;
+    if (has_row) {
+        const int hq = (int)(row % HQ);
+        const long long bt = row / HQ;
+        const int G = HQ / H;
+        n = max(0, min(__ldg(nslots + bt * H + hq / G), S));
+    }
+    const long long rr = has_row ? row : 0;
+    const float* L = lsebuf + rr * S;
+    const uint4* base = reinterpret_cast<const uint4*>(obuf + rr * S * D) + ch;
+    float l0 = ch < n ? __ldg(L + ch) : -CUDART_INF_F;               // slots ch and ch + 16 (S <= 32)
+    float l1 = ch + 16 < n ? __ldg(L + ch + 16) : -CUDART_INF_F;
     uint4 raw[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int s = hf + 2 * u;
-        raw[u] = s < n ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    const float a = warp_max(l_own);
+    for (int u = 0; u < U; ++u)
+        raw[u] = u < n ? __ldg(base + (long long)u * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
+    // reductions over each half-warp (width 16), executed by the whole warp
+    float a = fmaxf(l0, l1);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o, 16));
+    float t = (l0 == -CUDART_INF_F ? 0.f : __expf(l0 - a)) + (l1 == -CUDART_INF_F ? 0.f : __expf(l1 - a));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o, 16);
+    const float Lrow = a == -CUDART_INF_F ? -CUDART_INF_F : a + __logf(t);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    float Lrow = -CUDART_INF_F;
-    if (a != -CUDART_INF_F) {
-        const float total = warp_sum(l_own == -CUDART_INF_F ? 0.f : __expf(l_own - a));
-        Lrow = a + __logf(total);
-    }
-    for (int s0 = 0; s0 < n; s0 += 2 * U) {  // warp-uniform bound: the shuffles need every lane
+    // both half-warps run the same number of passes (the shuffles need both)
+    const int n_other = __shfl_xor_sync(0xffffffffu, n, 16);
+    const int n_pass = max(n, n_other);
+    for (int s0 = 0; s0 < n_pass; s0 += U) {
         if (s0 > 0) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int s = s0 + hf + 2 * u;
-                raw[u] = s < n ? __ldg(base + (long long)s * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int u = 0; u < U; ++u)
+                raw[u] = s0 + u < n ? __ldg(base + (long long)(s0 + u) * (D / 8)) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int s = s0 + hf + 2 * u;
-            const float ls = __shfl_sync(0xffffffffu, l_own, s & 31);
+            const int s = s0 + u;
+            const float ls0 = __shfl_sync(0xffffffffu, l0, (lane & 16) | (s & 15));
+            const float ls1 = __shfl_sync(0xffffffffu, l1, (lane & 16) | (s & 15));
+            const float ls = s < 16 ? ls0 : ls1;
             // slots past n or with L_s = -inf take no part (their rows are not used,
             // whatever they hold)
             if (s < n && ls != -CUDART_INF_F) {
@@ -371,9 +379,7 @@ __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
             }
         }
     }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
-    if (lane < 16) {
+    if (has_row) {
         TO* o = out + row * D + 8 * ch;
         if constexpr (sizeof(TO) == 2) {
             uint4 q4;
@@ -388,8 +394,8 @@ __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
             *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
             *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
+        if (lse && ch == 0) lse[row] = Lrow;
     }
-    if (lse && lane == 0) lse[row] = Lrow;
 }
 
 // tcgen05 version of K1 (attn_tc.cu); sets *handled = false when the shape is not covered.
@@ -510,11 +516,12 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
     BSA_REQUIRE(grid < 0x7fffffffLL, "combine: too many rows");
     cudaStream_t st = as_stream(stream);
     if (obuf_dtype == BSA_BF16 && D == 128 && S <= 32 && ((uintptr_t)obuf & 15) == 0 && ((uintptr_t)out & 15) == 0) {
+        const long long grid2 = (rows + 2 * per_cta - 1) / (2 * per_cta);  // two rows per warp
         if (out_dtype == BSA_BF16)
-            combine_bf16_d128_kernel<__nv_bfloat16><<<(unsigned)grid, 32 * per_cta, 0, st>>>(
+            combine_bf16_d128_kernel<__nv_bfloat16><<<(unsigned)grid2, 32 * per_cta, 0, st>>>(
                 (const __nv_bfloat16*)obuf, lsebuf, nslots, HQ, H, S, rows, (__nv_bfloat16*)out, lse);
         else
-            combine_bf16_d128_kernel<float><<<(unsigned)grid, 32 * per_cta, 0, st>>>(
+            combine_bf16_d128_kernel<float><<<(unsigned)grid2, 32 * per_cta, 0, st>>>(
                 (const __nv_bfloat16*)obuf, lsebuf, nslots, HQ, H, S, rows, (float*)out, lse);
         return check_launch("combine_bf16_d128_kernel");
     }

@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
         for (int i = 0; i < kTR; ++i)
 #pragma unroll
             for (int c = 0; c < kTC; ++c) acc[i][c] = 0.f;
+        // unrolled so that the next steps' shared loads are in flight during the FMAs
+#pragma unroll 8
         for (int d4 = 0; d4 < Dp / 4; ++d4) {
             float4 a[kTR], b[kTC];
 #pragma unroll
