@@ -333,6 +333,8 @@ class BlockWorkload:
                        if self.perm is not None else None)
         if self.packed is not None and self.vbar is None:
             self.vbar = torch.empty_like(self.qbar)
+        from block_sparse_attention_tile_gb300 import bsa as _bsa
+        self.route_ws = torch.empty((_bsa.bsa_route_workspace(BH, self.Jr) // 4,), dtype=torch.float32, device=dev)
         self.q2k = torch.empty((BH, self.Jr, k), dtype=torch.int32, device=dev)
         self.q2n = torch.empty((BH, self.Jr), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
@@ -355,7 +357,7 @@ class BlockWorkload:
                             packed=self.packed)
         if ev: ev[2].record(st)
         bsa.bsa_route_topk(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.Jr, D, self.J * D, kk,
-                           self.scale, kk, self.q2k, self.q2n)
+                           self.scale, kk, self.q2k, self.q2n, self.route_ws)
         if ev: ev[3].record(st)
         if self.summary:
             bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
@@ -387,7 +389,7 @@ class BlockWorkload:
                             self.kbar_lp[sl] if self.summary else None, self.vbar_lp[sl] if self.summary else None,
                             packed=packed_chunk)
         bsa.bsa_route_topk(self.qbar[sl, self.P:], self.kbar[sl, self.P:], nh, self.Jr, D, self.J * D, kk,
-                           self.scale, kk, self.q2k[sl], self.q2n[sl])
+                           self.scale, kk, self.q2k[sl], self.q2n[sl], self.route_ws)
         if self.summary:
             bsa.bsa_fwd_summary(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                 self.q2k[sl], self.q2n[sl], kk, self.kbar_lp[sl], self.vbar_lp[sl], self.scale,

@@ -46,7 +46,8 @@ _SIGS = {
     "bsa_tile_map": (I, [I, I, I, I, I, I, I, P, I, P, P, P]),
     "bsa_budget": (I, [I, ctypes.c_double]),
     "bsa_pool_blocks": (I, [P, P, P, I, I, I, I, P, P, I, I, P, P, P, P, P, P, P]),
-    "bsa_route_topk": (I, [P, P, I, I, I, I64, I, F, I, P, P, P]),
+    "bsa_route_topk": (I, [P, P, I, I, I, I64, I, F, I, P, P, P, SZ, P]),
+    "bsa_route_workspace": (SZ, [I, I]),
     "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, F, P, P, P]),
     "bsa_fwd_qouter_tokens": (I, [P, P, P, I, I, I, I, I, I, P, P, I, I, I, F, P, P, P]),
     "bsa_reverse_index_workspace": (SZ, [I, I, I, I]),
@@ -136,9 +137,15 @@ def bsa_pool_blocks(q, k, v, BH, N, D, index_map, block_sizes, J, M, qbar, kbar,
                                 _ptr(kbar_lp), _ptr(vbar_lp), _ptr(packed), _stream(stream)))
 
 
-def bsa_route_topk(qbar, kbar, BH, J, D, head_stride, k, scale, kmax, q2k_idx, q2k_num, stream=None):
+def bsa_route_workspace(BH, J):
+    return _lib.bsa_route_workspace(BH, J)
+
+
+def bsa_route_topk(qbar, kbar, BH, J, D, head_stride, k, scale, kmax, q2k_idx, q2k_num, workspace=None,
+                   stream=None):
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.bsa_route_topk(_ptr(qbar), _ptr(kbar), BH, J, D, head_stride, k, scale, kmax,
-                               _ptr(q2k_idx), _ptr(q2k_num), _stream(stream)))
+                               _ptr(q2k_idx), _ptr(q2k_num), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,

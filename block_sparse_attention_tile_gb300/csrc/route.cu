@@ -28,6 +28,79 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// TopK of one row of E (J scores, in shared or global memory) by one warp:
+// exact radix select on order-preserving keys, ties to the lower index, the
+// selected ids written ascending and -1 padded to kmax, and the count.
+__device__ __forceinline__ void select_row(const float* __restrict__ e, int J, int k, int kmax, int lane,
+                                           int32_t* __restrict__ out, int32_t* __restrict__ num_out) {
+    if (J <= 1024) {
+        // the row's keys stay in registers: lane holds columns lane + 32*i
+        uint32_t key[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int c = lane + 32 * i;
+            key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
+        }
+        uint32_t prefix = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = prefix | (1u << bit);
+            int cnt = 0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cnt += key[i] >= cand;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if (cnt >= k) prefix = cand;
+        }
+        int n_gt = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) n_gt += key[i] > prefix;
+        n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+        const int need_eq = k - n_gt;
+        int eq_seen = 0, written = 0;
+        const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int c = lane + 32 * i;
+            const bool eq = c < J && key[i] == prefix;
+            const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+            const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
+            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[written + __popc(sel_mask & lt)] = c;
+            written += __popc(sel_mask);
+            eq_seen += __popc(eq_mask);
+        }
+    } else {
+        uint32_t prefix = 0;
+        for (int bit = 31; bit >= 0; --bit) {
+            const uint32_t cand = prefix | (1u << bit);
+            int cnt = 0;
+            for (int c = lane; c < J; c += 32) cnt += order_key(e[c]) >= cand;
+            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            if (cnt >= k) prefix = cand;
+        }
+        // prefix is the k-th largest key; keep everything above it and the
+        // lowest-index entries equal to it.
+        int n_gt = 0;
+        for (int c = lane; c < J; c += 32) n_gt += order_key(e[c]) > prefix;
+        n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+        const int need_eq = k - n_gt;
+        int eq_seen = 0, written = 0;
+        for (int base = 0; base < J; base += 32) {
+            const int c = base + lane;
+            const uint32_t key = c < J ? order_key(e[c]) : 0u;
+            const bool eq = c < J && key == prefix;
+            const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+            const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
+            const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
+            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
+            written += __popc(sel_mask);
+            eq_seen += __popc(eq_mask);
+        }
+    }
+    for (int s = k + lane; s < kmax; s += 32) out[s] = -1;
+    if (lane == 0) *num_out = k;
+}
+
 // DPC: the padded head dimension when it is known at compile time (0 = any).
 template <int DPC, int TR>
 __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
@@ -128,90 +201,161 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     __syncthreads();
 
     const int warp = tid / 32, lane = tid % 32;
-    for (int rr = warp; rr < nrows; rr += kRouteThreads / 32) {
-        const float* e = E + rr * J;
-        int32_t* out = q2k_idx + ((long long)bh * J + row0 + rr) * kmax;
-        if (J <= 1024) {
-            // the row's keys stay in registers: lane holds columns lane + 32*i
-            uint32_t key[32];
+    for (int rr = warp; rr < nrows; rr += kRouteThreads / 32)
+        select_row(E + rr * J, J, k, kmax, lane, q2k_idx + ((long long)bh * J + row0 + rr) * kmax,
+                   q2k_num + (long long)bh * J + row0 + rr);
+}
+
+// ---------------------------------------------------------------- two-kernel path
+// With a workspace, E goes to global memory (L2-resident at these sizes) and
+// the two halves run as separate kernels: a register-tiled FP32 contraction
+// (128 x 128 block tiles, 8 x 8 outputs per thread, the d axis in stages of
+// 8 double-buffered in shared memory, two CTAs per SM) and the select, one
+// warp per row.  Every E entry accumulates its dot product over d in
+// ascending order with fmaf and is scaled last, as in the fused kernel, so
+// both paths give the same E and the same lists.
+constexpr int kGB = 128, kGK = 8;
+
+__global__ void __launch_bounds__(256, 2) route_gemm_kernel(const float* __restrict__ qbar,
+                                                            const float* __restrict__ kbar, int J, int D,
+                                                            long long head_stride, float scale, float* __restrict__ E) {
+    __shared__ __align__(16) float As[2][kGK][kGB];  // [d][row]
+    __shared__ __align__(16) float Bs[2][kGK][kGB];  // [d][col]
+    const int bh = blockIdx.z;
+    const int r0 = blockIdx.y * kGB, c0 = blockIdx.x * kGB;
+    const float* qh = qbar + (long long)bh * head_stride;
+    const float* kh = kbar + (long long)bh * head_stride;
+    const int tid = threadIdx.x;
+    const int ty = tid >> 4, tx = tid & 15;        // outputs: rows 4ty(+64), columns 4tx(+64)
+    const int lr = tid >> 1, ld0 = (tid & 1) * 4;  // staging: row lr of the tile, d = ld0 .. ld0+3
+    const bool vec = (D & 3) == 0;
+    float4 qa, kb;
+    auto load_stage = [&](int d0) {
+        float qv[4], kv[4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = lane + 32 * i;
-                key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
+        for (int e = 0; e < 4; ++e) { qv[e] = 0.f; kv[e] = 0.f; }
+        const int r = r0 + lr, c = c0 + lr;
+        if (vec && d0 + ld0 + 3 < D) {
+            if (r < J) {
+                const float4 t = *reinterpret_cast<const float4*>(qh + (long long)r * D + d0 + ld0);
+                qv[0] = t.x; qv[1] = t.y; qv[2] = t.z; qv[3] = t.w;
             }
-            uint32_t prefix = 0;
-            for (int bit = 31; bit >= 0; --bit) {
-                const uint32_t cand = prefix | (1u << bit);
-                int cnt = 0;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) cnt += key[i] >= cand;
-                cnt = __reduce_add_sync(0xffffffffu, cnt);
-                if (cnt >= k) prefix = cand;
-            }
-            int n_gt = 0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) n_gt += key[i] > prefix;
-            n_gt = __reduce_add_sync(0xffffffffu, n_gt);
-            const int need_eq = k - n_gt;
-            int eq_seen = 0, written = 0;
-            const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = lane + 32 * i;
-                const bool eq = c < J && key[i] == prefix;
-                const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
-                const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
-                const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-                if (sel) out[written + __popc(sel_mask & lt)] = c;
-                written += __popc(sel_mask);
-                eq_seen += __popc(eq_mask);
+            if (c < J) {
+                const float4 t = *reinterpret_cast<const float4*>(kh + (long long)c * D + d0 + ld0);
+                kv[0] = t.x; kv[1] = t.y; kv[2] = t.z; kv[3] = t.w;
             }
         } else {
-            uint32_t prefix = 0;
-            for (int bit = 31; bit >= 0; --bit) {
-                const uint32_t cand = prefix | (1u << bit);
-                int cnt = 0;
-                for (int c = lane; c < J; c += 32) cnt += order_key(e[c]) >= cand;
-                cnt = __reduce_add_sync(0xffffffffu, cnt);
-                if (cnt >= k) prefix = cand;
-            }
-            // prefix is the k-th largest key; keep everything above it and the
-            // lowest-index entries equal to it.
-            int n_gt = 0;
-            for (int c = lane; c < J; c += 32) n_gt += order_key(e[c]) > prefix;
-            n_gt = __reduce_add_sync(0xffffffffu, n_gt);
-            const int need_eq = k - n_gt;
-            int eq_seen = 0, written = 0;
-            for (int base = 0; base < J; base += 32) {
-                const int c = base + lane;
-                const uint32_t key = c < J ? order_key(e[c]) : 0u;
-                const bool eq = c < J && key == prefix;
-                const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
-                const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
-                const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
-                const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-                if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
-                written += __popc(sel_mask);
-                eq_seen += __popc(eq_mask);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int d = d0 + ld0 + e;
+                if (d < D) {
+                    if (r < J) qv[e] = qh[(long long)r * D + d];
+                    if (c < J) kv[e] = kh[(long long)c * D + d];
+                }
             }
         }
-        for (int s = k + lane; s < kmax; s += 32) out[s] = -1;
-        if (lane == 0) q2k_num[(long long)bh * J + row0 + rr] = k;
+        qa = make_float4(qv[0], qv[1], qv[2], qv[3]);
+        kb = make_float4(kv[0], kv[1], kv[2], kv[3]);
+    };
+    auto store_stage = [&](int buf) {
+        As[buf][ld0 + 0][lr] = qa.x; As[buf][ld0 + 1][lr] = qa.y; As[buf][ld0 + 2][lr] = qa.z; As[buf][ld0 + 3][lr] = qa.w;
+        Bs[buf][ld0 + 0][lr] = kb.x; Bs[buf][ld0 + 1][lr] = kb.y; Bs[buf][ld0 + 2][lr] = kb.z; Bs[buf][ld0 + 3][lr] = kb.w;
+    };
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    const int nst = (D + kGK - 1) / kGK;
+    load_stage(0);
+    store_stage(0);
+    __syncthreads();
+    for (int st = 0; st < nst; ++st) {
+        const int buf = st & 1;
+        if (st + 1 < nst) load_stage((st + 1) * kGK);  // next stage in flight during the FMAs
+#pragma unroll
+        for (int dd = 0; dd < kGK; ++dd) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][dd][4 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][dd][4 * ty + 64]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][dd][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][dd][4 * tx + 64]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        }
+        if (st + 1 < nst) {
+            store_stage(buf ^ 1);  // the other buffer was last read in step st - 1
+            __syncthreads();
+        }
     }
+    float* eh = E + (long long)bh * J * J;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = r0 + 4 * ty + (i & 3) + (i >> 2) * 64;
+        if (r >= J) continue;
+#pragma unroll
+        for (int jh = 0; jh < 2; ++jh) {
+            const int c = c0 + 4 * tx + jh * 64;
+            float* dst = eh + (long long)r * J + c;
+            const float v0 = acc[i][4 * jh] * scale, v1 = acc[i][4 * jh + 1] * scale;
+            const float v2 = acc[i][4 * jh + 2] * scale, v3 = acc[i][4 * jh + 3] * scale;
+            if ((J & 3) == 0 && c + 3 < J) {
+                *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+            } else {
+                if (c < J) dst[0] = v0;
+                if (c + 1 < J) dst[1] = v1;
+                if (c + 2 < J) dst[2] = v2;
+                if (c + 3 < J) dst[3] = v3;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) route_select_kernel(const float* __restrict__ E, int J, int k, int kmax,
+                                                           int32_t* __restrict__ q2k_idx,
+                                                           int32_t* __restrict__ q2k_num) {
+    const int bh = blockIdx.y;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= J) return;
+    select_row(E + ((long long)bh * J + row) * J, J, k, kmax, threadIdx.x & 31,
+               q2k_idx + ((long long)bh * J + row) * kmax, q2k_num + (long long)bh * J + row);
 }
 
 }  // namespace bsa
 
 using namespace bsa;
 
+extern "C" size_t bsa_route_workspace(int BH, int J) {
+    if (BH < 1 || J < 1) return 0;
+    return (size_t)BH * J * J * sizeof(float);
+}
+
 extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, int D,
                                      int64_t head_stride, int k, float scale, int kmax,
-                                     int32_t* q2k_idx, int32_t* q2k_num, void* stream) {
+                                     int32_t* q2k_idx, int32_t* q2k_num, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
     BSA_REQUIRE(qbar && kbar && q2k_idx && q2k_num, "route: null pointer");
     BSA_REQUIRE(BH > 0 && BH <= 65535 && J > 0 && J <= 8192 && D > 0 && D <= 256,
                 "route: sizes out of range (BH=%d J=%d D=%d)", BH, J, D);
     BSA_REQUIRE(k >= 1 && k <= J && kmax >= k, "route: need 1 <= k <= J and k <= kmax");
     BSA_REQUIRE(head_stride >= (int64_t)J * D, "route: head_stride smaller than J*D");
+    if (workspace) {
+        BSA_REQUIRE(workspace_bytes >= bsa_route_workspace(BH, J), "route: workspace smaller than %zu bytes",
+                    bsa_route_workspace(BH, J));
+        BSA_REQUIRE(((uintptr_t)workspace & 15) == 0, "route: workspace not 16-byte aligned");
+        BSA_REQUIRE(J <= 8192, "route: J > 8192");
+        cudaStream_t st = as_stream(stream);
+        float* E = static_cast<float*>(workspace);
+        const dim3 g1((J + kGB - 1) / kGB, (J + kGB - 1) / kGB, BH);
+        route_gemm_kernel<<<g1, 256, 0, st>>>(qbar, kbar, J, D, (long long)head_stride, scale, E);
+        bsa_status rc = check_launch("route_gemm_kernel");
+        if (rc != BSA_OK) return rc;
+        route_select_kernel<<<dim3((J + 7) / 8, BH), 256, 0, st>>>(E, J, k, kmax, q2k_idx, q2k_num);
+        return check_launch("route_select_kernel");
+    }
     const int Dp = (D + 3) / 4 * 4;
     // the most rows per CTA whose E rows, query rows and key tile fit in shared memory
     auto smem_for = [&](int rows) {

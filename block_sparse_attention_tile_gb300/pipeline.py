@@ -102,7 +102,8 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
                         qbar, kbar, vbar, kbar_lp, vbar_lp, packed=pk)
     q2k_idx = torch.empty((BH, Jr, kmax), dtype=torch.int32, device=dev)
     q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
-    bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num)
+    ws = torch.empty((bsa.bsa_route_workspace(BH, Jr) // 4,), dtype=torch.float32, device=dev)
+    bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num, ws)
     out = torch.empty_like(q)
     lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
     if summary:

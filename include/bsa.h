@@ -122,14 +122,20 @@ bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtyp
  * and q2k_num.  Ties keep the lower block index.
  * qbar, kbar: [device] float; row i of head h at ptr + h*head_stride + i*D.
  * q2k_idx: [device] int32 [BH, J, kmax]; q2k_num: [device] int32 [BH, J].
- * 1 <= k <= J, k <= kmax, J <= 8192, D <= 256.  E is computed in float32.
- * A CTA keeps the E rows of 8 to 32 query rows in shared memory for the
- * select; even at 8 rows (8*J + 128*(Dp+4) + 8*Dp) * 4 bytes must fit in
- * 227 KB (Dp = D rounded up to 4; J <= 5024 at D = 128), else
- * BSA_ERR_UNSUPPORTED. */
+ * 1 <= k <= J, k <= kmax, J <= 8192, D <= 256.  E is computed in float32,
+ * each entry as a dot product accumulated over d in ascending order and then
+ * scaled, so both paths below give the same lists.
+ * workspace: [device] bsa_route_workspace(BH, J) bytes (16-byte aligned) for
+ * E, or NULL.  With it, E is written by a register-tiled contraction and
+ * read back by the select (two launches); without it, one fused kernel
+ * keeps the E rows of 8 to 32 query rows in shared memory, so even at 8 rows
+ * (8*J + 128*(Dp+4) + 8*Dp) * 4 bytes must fit in 227 KB (Dp = D rounded up
+ * to 4; J <= 5024 at D = 128), else BSA_ERR_UNSUPPORTED. */
+size_t bsa_route_workspace(int BH, int J);
 bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, int D,
                           int64_t head_stride, int k, float scale, int kmax,
-                          int32_t* q2k_idx, int32_t* q2k_num, void* stream);
+                          int32_t* q2k_idx, int32_t* q2k_num, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------ a4 ----
  * Block-sparse attention, query-outer order.  [VSA] §6.3: for query block i,

@@ -71,7 +71,7 @@ def test_reverse_index_sizes(bsa):
 
 def test_invalid_arguments_are_rejected_without_cuda(bsa):
     lib = bsa._lib
-    rc = lib.bsa_route_topk(None, None, 1, 4, 2, 8, 2, 1.0, 4, None, None, None)
+    rc = lib.bsa_route_topk(None, None, 1, 4, 2, 8, 2, 1.0, 4, None, None, None, 0, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
     rc = lib.bsa_pool_blocks(1, 1, None, 1, 1, 8, 0, 1, 1, 4, 16, 1, 1, None, None, None, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG
@@ -79,8 +79,11 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     assert rc == bsa.BSA_ERR_INVALID_ARG and "packed" in bsa.bsa_last_error()  # packed copy needs v
     rc = lib.bsa_fwd_qouter(1, 1, 1, 1, 1, 64, 128, 1, 1, 1, 256, 0, None, None, 1, 1, 8, 1.0, 1, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
-    rc = lib.bsa_route_topk(1, 1, 1, 4, 2, 8, 5, 1.0, 5, 1, 1, None)
+    rc = lib.bsa_route_topk(1, 1, 1, 4, 2, 8, 5, 1.0, 5, 1, 1, None, 0, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # k > J
+    rc = lib.bsa_route_topk(1, 1, 2, 4, 2, 8, 2, 1.0, 4, 1, 1, 16, 64, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "workspace" in bsa.bsa_last_error()  # 2*4*4*4 = 128 bytes needed
+    assert bsa.bsa_route_workspace(24, 960) == 24 * 960 * 960 * 4
     rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # max_chunks too small
     assert bsa.bsa_version() >= 100

@@ -231,7 +231,7 @@ def test_kvouter_group_sizes(lib, HQ, H, BS):
     assert np.abs(l_kv[0].cpu().numpy() - L).max() <= 2e-3
 
 
-@pytest.mark.parametrize("J,D", [(1500, 128), (3000, 128), (700, 72)])
+@pytest.mark.parametrize("J,D", [(1500, 128), (3000, 128), (700, 72), (130, 62)])
 def test_route_rows_per_cta_variants(lib, J, D):
     """Route alone at block counts that need 16 or 8 query rows per CTA (the
     E rows of a CTA live in shared memory) and at a head dim without the
@@ -242,7 +242,12 @@ def test_route_rows_per_cta_variants(lib, J, D):
     idx = torch.empty((BH, J, k + 3), dtype=torch.int32, device=DEV)
     num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
     lib.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, D ** -0.5, k + 3, idx, num)
+    # the two-kernel path (E in a workspace) computes the same E, so the same lists
+    ws = torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV)
+    idx_ws, num_ws = torch.empty_like(idx), torch.empty_like(num)
+    lib.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, D ** -0.5, k + 3, idx_ws, num_ws, ws)
     torch.cuda.synchronize()
+    assert torch.equal(idx, idx_ws) and torch.equal(num, num_ws)
     for bh in range(BH):
         E = oracle.routing_scores(f64(qbar[bh]), f64(kbar[bh]), D)
         check_route(idx[bh].cpu().numpy(), num[bh].cpu().numpy(), E, k)
