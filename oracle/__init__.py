@@ -10,7 +10,9 @@ float64 restatement of the definitions given on four pages:
 * "MSA 为什么采用 KV-outer Sparse Attention Forward" (notes.kuangjux.top) -- the
   reverse index, the K1 partial pass and the K2 log-sum-exp combine.
 * "深度解读|Spark-H3：从注意力几何到稀疏内核代码" (jefxiong.cn) -- the
-  exact-plus-summary mixture with the +log(m) mass term.
+  exact-plus-summary mixture with the +log(m) mass term, and the Reweight
+  summaries (weighted key and value with a log-mass bias at a representative
+  query).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
@@ -38,3 +40,4 @@ from .attention import (  # noqa: F401
 from .kvouter import (  # noqa: F401
     reverse_index, schedule_chunks, kvouter_partials, combine_partials,
 )
+from .spark import bf16_round, reweight_anchor, reweight_summary, reweight_summaries  # noqa: F401

@@ -98,14 +98,17 @@ def block_sparse_attention(Q, K, V, blocks, q2k_idx, q2k_num, scale,
 
 
 def summary_attention(Q, K, V, blocks, q2k_idx, q2k_num, kbar, vbar, scale,
-                      prefix_blocks=0, query_blocks=None):
-    """Exact keys plus one mean token per unselected routed block.
+                      prefix_blocks=0, query_blocks=None, block_bias=None):
+    """Exact keys plus one summary token per unselected routed block.
 
     Routed query block i: exact logits over every prefix key and every key of
     the selected routed blocks; each unselected routed block j contributes a
-    virtual key kbar[j] with value vbar[j] and logit q.kbar[j]*scale + log(n_j);
+    virtual key kbar[j] with value vbar[j] and logit q.kbar[j]*scale + bias_j;
     all in one softmax.  Prefix query blocks attend densely to every key.
-    kbar / vbar: [J_routed, D] means of the routed blocks.
+    kbar / vbar: [J_routed, D] summary keys and values of the routed blocks
+    (the block means, or the Spark-Reweight k~ / v~).  block_bias: [J_routed]
+    natural-log biases (the Spark-Reweight b); None gives log(n_j), the mass
+    of n_j copies of the mean key ("深度解读|Spark-H3", §03).
     """
     N = np.asarray(Q).shape[0]
     O = np.zeros((N, np.asarray(V).shape[1]))
@@ -131,8 +134,11 @@ def summary_attention(Q, K, V, blocks, q2k_idx, q2k_num, kbar, vbar, scale,
                                 np.asarray(kbar, dtype=np.float64)[others]])
         V_all = np.concatenate([np.asarray(V, dtype=np.float64)[keys],
                                 np.asarray(vbar, dtype=np.float64)[others]])
-        bias = np.concatenate([np.zeros(len(keys)),
-                               np.log([float(len(blocks[prefix_blocks + j])) for j in others])])
+        if block_bias is None:
+            vb = np.log([float(len(blocks[prefix_blocks + j])) for j in others])
+        else:
+            vb = np.asarray(block_bias, dtype=np.float64)[others]
+        bias = np.concatenate([np.zeros(len(keys)), vb])
         o, l = softmax_attention(np.asarray(Q)[rows], K_all, V_all, scale, bias=bias)
         O[rows], L[rows] = o, l
     return O, L

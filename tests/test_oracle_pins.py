@@ -464,3 +464,78 @@ def test_summary_prefix_rows_are_dense():
     O, _ = oracle.summary_attention(Q, K, V, blocks, idx, np.ones(4, int), kbar, vbar, 0.5,
                                     prefix_blocks=1, query_blocks=[0])
     assert np.abs(O[:8] - sdpa64(Q[:8], K, V, scale=0.5)).max() < 1e-13
+
+
+# ---------------------------------------------------------------- Spark-Reweight summaries
+
+def test_reweight_two_token_example():
+    g = golden("spark_reweight.json")["two_token_block"]
+    K = np.array([[-2.0], [2.0]])
+    V = np.array([[0.0], [1.0]])
+    a = np.array([float(g["anchor"])])
+    kt, vt, b = oracle.reweight_summary(a, K, V, 1.0)  # d = 1: scale 1/sqrt(1)
+    assert round(float(kt[0]), 6) == g["weighted_key"]
+    assert round(float(vt[0]), 6) == g["weighted_value"]
+    assert round(float(b), 6) == g["bias"]
+    z = float(a @ kt) + b
+    assert round(z, 6) == g["virtual_logit_at_anchor"]
+    assert round(math.exp(z), 6) == g["exp_virtual_logit"]
+
+
+def test_reweight_tail_is_exact_at_the_anchor():
+    # the page's seeded check: the reweighted tail with anchor = query equals dense
+    g = golden("spark_reweight.json")["numpy_check"]
+    rng = np.random.default_rng(20261024)
+    k = rng.normal(size=(32, 8))
+    v = rng.normal(size=(32, 5))
+    a = rng.normal(size=8)
+    blocks = oracle.tile_prefix(32, g["block"])
+    exact = sorted(g["exact_blocks"])
+    idx = np.full((len(blocks), len(exact)), -1)
+    idx[:] = exact
+    num = np.full(len(blocks), len(exact))
+    kt, vt, bias, _ = oracle.reweight_summaries(np.tile(a, (32, 1)), k, v, blocks, 8 ** -0.5, anchor=a)
+    o, _ = oracle.summary_attention(np.tile(a, (32, 1)), k, v, blocks, idx, num, kt, vt, 8 ** -0.5,
+                                    query_blocks=[0], block_bias=bias)
+    dense = sdpa64(a[None], k, v)
+    assert float(np.abs(o[0] - dense[0]).max()) <= g["reweight_tail_max_abs_error_vs_dense_at_most"]
+
+
+def test_reweight_bias_is_the_entropy_and_the_tangent_stays_below():
+    # unrounded: b = H(p) in [0, log m]; the virtual logit is the tangent of the
+    # convex block log-mass at a, so it never exceeds log Z_B(q)
+    rng = np.random.default_rng(31)
+    for m in (1, 2, 7, 64):
+        K = rng.normal(size=(m, 16)) * 1.5
+        V = rng.normal(size=(m, 16))
+        a = rng.normal(size=16)
+        scale = 16 ** -0.5
+        kt, vt, b = oracle.reweight_summary(a, K, V, scale)
+        s = K @ a * scale
+        p = np.exp(s - s.max())
+        p /= p.sum()
+        H = float(-(p * np.log(np.where(p > 0, p, 1.0))).sum())
+        assert abs(b - H) < 1e-10 and -1e-12 <= b <= math.log(m) + 1e-12
+        for _ in range(20):
+            q = a + rng.normal(size=16)
+            sq = K @ q * scale
+            logZ = sq.max() + math.log(np.exp(sq - sq.max()).sum())
+            assert float(q @ kt) * scale + b <= logZ + 1e-10
+        # at q = a the virtual token carries the block's whole mass and numerator
+        sa = K @ a * scale
+        Z = np.exp(sa).sum()
+        U = np.exp(sa) @ V
+        zh = float(a @ kt) * scale + b
+        assert abs(math.exp(zh) - Z) < 1e-9 * Z and np.abs(math.exp(zh) * vt - U).max() < 1e-9 * max(1.0, Z)
+
+
+def test_reweight_anchor_and_bf16_round():
+    rng = np.random.default_rng(32)
+    Q = rng.normal(size=(40, 6))
+    blocks = [np.arange(0, 4), np.arange(4, 8)] + [np.arange(8 + 8 * i, 16 + 8 * i) for i in range(4)]
+    a = oracle.reweight_anchor(Q, blocks, prefix_blocks=2)
+    assert np.allclose(a, Q[8:].mean(axis=0), atol=1e-15)  # prefix rows do not count
+    x = np.concatenate([rng.normal(size=4000) * 10.0 ** rng.integers(-6, 6, size=4000),
+                        np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.5, 0.0])])  # two exact ties
+    want = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(oracle.bf16_round(x), want)
