@@ -17,6 +17,8 @@ Other workloads (--workload):
   spark_summary  bf16, h=24, 1024 text tokens + (16,32,64) video under a
                  permutation, 128-token blocks, k=26, summaries of the
                  unselected blocks
+  spark_reweight the same with Spark-Reweight summaries (weighted key and
+                 value at the head's mean video query, log-mass bias)
 
 Metric: effective sparse-attention TFLOP/s = 4*Hq*N*d*k*B_k / step time
 (the FLOP count of the "MSA ... KV-outer" page, eq. 13/15).
@@ -50,6 +52,8 @@ WORKLOADS = {
                        dtype="f32"),
     "spark_summary": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
                           seed=505, dtype="bf16", n_text=1024, summary=True),
+    "spark_reweight": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
+                           seed=505, dtype="bf16", n_text=1024, summary=True, reweight=True),
     "nsa_prefill": dict(kind="token", B=2, T=8192, HQ=64, H=4, D=128, BS=64, S=16, seed=303, zipf=False),
     "msa_prefill": dict(kind="token", B=1, T=32768, HQ=64, H=4, D=128, BS=128, S=16, seed=404, zipf=True),
 }
@@ -140,7 +144,7 @@ from block_sparse_attention_tile_gb300 import synthetic
 w = json.loads({w!r})
 budget_s = {budget}
 T, H, W = w["grid"]; bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
-n_text = w.get("n_text", 0); summary = w.get("summary", False)
+n_text = w.get("n_text", 0); summary = w.get("summary", False); reweight = w.get("reweight", False)
 dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
 t0 = time.perf_counter()
 if summary:
@@ -158,6 +162,11 @@ qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
 vbar = oracle.pool_blocks(V, blocks) if summary else None
 E = oracle.routing_scores(qbar[P:], kbar[P:], D)
 idx, num = oracle.route(E, k, k)
+sbias = None
+if reweight:
+    kbar, vbar, sbias, _ = oracle.reweight_summaries(Q, K, V, blocks, D ** -0.5, prefix_blocks=P,
+                                                     round_key=oracle.bf16_round if w["dtype"] == "bf16" else None)
+    kbar = np.concatenate([np.zeros((P, D)), kbar]); vbar = np.concatenate([np.zeros((P, D)), vbar])
 route_s = time.perf_counter() - t0
 rng = np.random.default_rng(0)
 order = rng.permutation(len(blocks))
@@ -166,7 +175,7 @@ while done < len(order) and (done < 2 or time.perf_counter() - t0 < budget_s):
     qb = [int(order[done])]
     if summary:
         oracle.summary_attention(Q, K, V, blocks, idx, num, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
-                                 query_blocks=qb)
+                                 query_blocks=qb, block_bias=sbias)
     else:
         oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb)
     done += 1
@@ -230,9 +239,10 @@ def run_oracle_sample(wname, budget_s=15.0):
                   "attended, all %d heads (%.1f s); step time scaled by tokens and batch"
                   % (w["B"], w["T"], r["route_s"], r["units"], r["total_units"], w["HQ"], r["attn_s"]))
     else:
-        sample = ("1 of %d heads: tile map, pool and route of all %d blocks (%.1f s) plus %d of %d query blocks "
+        pre = "tile map, pool, route" + (" and Spark-Reweight summaries" if w.get("reweight") else "")
+        sample = ("1 of %d heads: %s of all %d blocks (%.1f s) plus %d of %d query blocks "
                   "attended (%.1f s); step time scaled by heads and blocks"
-                  % (w["heads"], r["total_units"], r["route_s"], r["units"], r["total_units"], r["attn_s"]))
+                  % (w["heads"], pre, r["total_units"], r["route_s"], r["units"], r["total_units"], r["attn_s"]))
     return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
             "step_s_extrapolated": r["step_s"]}
 
@@ -300,6 +310,9 @@ class BlockWorkload:
         self.torch = torch
         T, H, W = w["grid"]
         self.summary = w.get("summary", False)
+        self.reweight = self.summary and w.get("reweight", False)
+        if self.reweight:
+            self.stage_names = ["tile_map", "pool", "route", "reweight", "attention"]
         n_text = w.get("n_text", 0)
         D, M, k = w["D"], w["M"], w["k"]
         self.BH = w["B"] * w["heads"]
@@ -339,7 +352,11 @@ class BlockWorkload:
         self.q2n = torch.empty((BH, self.Jr), dtype=torch.int32, device=dev)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((BH, self.N), dtype=torch.float32, device=dev)
-        self.launches_per_step = 4
+        self.sbias = torch.empty((BH, J), dtype=torch.float32, device=dev) if self.reweight else None
+        self.rw_ws = (torch.empty((_bsa.bsa_reweight_workspace(BH, D) // 4,), dtype=torch.float32, device=dev)
+                      if self.reweight else None)
+        # tile map, pool, route (contraction + select), [reweight: mean partials, mean, summaries], attention
+        self.launches_per_step = 5 + (3 if self.reweight else 0)
 
     def step(self, ev=None, q=None, k=None, v=None):
         from block_sparse_attention_tile_gb300 import bsa
@@ -359,14 +376,18 @@ class BlockWorkload:
         bsa.bsa_route_topk(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.Jr, D, self.J * D, kk,
                            self.scale, kk, self.q2k, self.q2n, self.route_ws)
         if ev: ev[3].record(st)
+        if self.reweight:
+            bsa.bsa_reweight_summaries(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, self.scale,
+                                       self.kbar_lp, self.vbar_lp, self.sbias, self.rw_ws, qbar=self.qbar)
+            if ev: ev[4].record(st)
         if self.summary:
             bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                 self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.out, self.lse,
-                                packed=self.packed)
+                                packed=self.packed, summary_bias=self.sbias)
         else:
             bsa.bsa_fwd_qouter(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                self.q2k, self.q2n, kk, self.scale, self.out, self.lse, packed=self.packed)
-        if ev: ev[4].record(st)
+        if ev: ev[len(self.stage_names)].record(st)
 
     def host_inputs(self):
         return [self.q, self.k, self.v], [self.out]
@@ -390,10 +411,16 @@ class BlockWorkload:
                             packed=packed_chunk)
         bsa.bsa_route_topk(self.qbar[sl, self.P:], self.kbar[sl, self.P:], nh, self.Jr, D, self.J * D, kk,
                            self.scale, kk, self.q2k[sl], self.q2n[sl], self.route_ws)
+        sb = None
+        if self.reweight:
+            sb = self.sbias[sl]
+            bsa.bsa_reweight_summaries(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P,
+                                       self.scale, self.kbar_lp[sl], self.vbar_lp[sl], sb, self.rw_ws,
+                                       qbar=self.qbar[sl])
         if self.summary:
             bsa.bsa_fwd_summary(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                 self.q2k[sl], self.q2n[sl], kk, self.kbar_lp[sl], self.vbar_lp[sl], self.scale,
-                                self.out[sl], self.lse[sl], packed=packed_chunk)
+                                self.out[sl], self.lse[sl], packed=packed_chunk, summary_bias=sb)
         else:
             bsa.bsa_fwd_qouter(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                self.q2k[sl], self.q2n[sl], kk, self.scale, self.out[sl], self.lse[sl],
@@ -444,7 +471,7 @@ class BlockWorkload:
             fin.record(d2h_s)
             comp.wait_event(fin)
 
-        return step, 1 + 3 * len(chunks)
+        return step, 1 + (self.launches_per_step - 1) * len(chunks)
 
     def algorithmic(self):
         """Valid (query, key) pairs the attention scores, x 4*D FLOPs."""
@@ -467,6 +494,14 @@ class BlockWorkload:
                       + (self.packed.numel() * self.packed.element_size() if self.packed is not None else 0)
                       + self.J * self.w["M"] * 4 + self.J * 4)
         return flops, pool_bytes
+
+    def reweight_bytes(self):
+        """Routed member rows of K and V read once, the float32 block means
+        of Q read for the mean, k~ and v~ rows and the bias written."""
+        D, el = self.w["D"], self.q.element_size()
+        rows = float(self.bs[self.P:].long().sum().item())
+        return (2 * self.BH * rows * D * el + self.BH * self.Jr * D * 4 + self.BH * self.Jr * (2 * D * el + 4)
+                + self.J * self.w["M"] * 4)
 
     def report(self, stage_ms, peaks, peak_kind, props):
         flops, pool_bytes = self.algorithmic()
@@ -493,11 +528,18 @@ class BlockWorkload:
                      "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
             "route": {"bound": "alu", "achieved": route_tf, "peak": fp32, "unit": "TFLOP/s", "frac": route_tf / fp32,
                       "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}}
+        if self.reweight:
+            rb = self.reweight_bytes()
+            rgbs = rb / (stage_ms["reweight"] * 1e-3) / 1e9
+            secondary["reweight"] = {"bound": "hbm", "achieved": rgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                     "frac": rgbs / peaks["hbm_gbs"], "bytes_per_launch": rb}
         T, H, W = self.w["grid"]
         config = {"workload": self.name, "B": self.w["B"], "heads": self.w["heads"], "D": D, "seq_len": self.N,
                   "grid": [T, H, W], "block": list(self.w["block"]), "M": self.w["M"], "J": J, "k": self.w["k"]}
         if self.summary:
             config.update({"n_text": self.w["n_text"], "permuted": True, "summary": True})
+            if self.reweight:
+                config["summaries"] = "spark-reweight"
         nbytes = 3 * self.q.numel() * self.q.element_size()
         config["l2"] = ("inputs larger than L2: Q,K,V = %.2f GB per step" % (nbytes / 1e9) if nbytes > 129e6 else
                         "inputs smaller than L2 (%.1f MB): L2 not flushed, launch-bound tiny case" % (nbytes / 1e6))

@@ -56,7 +56,9 @@ _SIGS = {
     "bsa_build_reverse_index_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P]),
     "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P]),
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
-    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, F, P, P, P]),
+    "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, P, F, P, P, P]),
+    "bsa_reweight_workspace": (SZ, [I, I]),
+    "bsa_reweight_summaries": (I, [P, P, P, P, I, I, I, I, P, P, I, I, I, F, P, P, P, P, P, SZ, P]),
     "bsa_set_force_simt": (None, [I]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -157,11 +159,24 @@ def bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_block
 
 
 def bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, geometry, q2k_idx,
-                    q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse=None, packed=None, stream=None):
+                    q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse=None, packed=None, summary_bias=None,
+                    stream=None):
     _check(_lib.bsa_fwd_summary(_ptr(q), _ptr(k), _ptr(v), _dtype(q), BH, N, D, _ptr(index_map),
                                 _ptr(block_sizes), J, M, prefix_blocks, _geometry(geometry), _ptr(packed),
-                                _ptr(q2k_idx), _ptr(q2k_num), kmax, _ptr(kbar_lp), _ptr(vbar_lp), scale,
-                                _ptr(out), _ptr(lse), _stream(stream)))
+                                _ptr(q2k_idx), _ptr(q2k_num), kmax, _ptr(kbar_lp), _ptr(vbar_lp),
+                                _ptr(summary_bias), scale, _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def bsa_reweight_workspace(BH, D):
+    return _lib.bsa_reweight_workspace(BH, D)
+
+
+def bsa_reweight_summaries(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, scale, kt_lp, vt_lp,
+                           bias, workspace, anchor=None, qbar=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.bsa_reweight_summaries(_ptr(q), _ptr(qbar), _ptr(k), _ptr(v), _dtype(k), BH, N, D, _ptr(index_map),
+                                       _ptr(block_sizes), J, M, prefix_blocks, scale, _ptr(kt_lp), _ptr(vt_lp),
+                                       _ptr(bias), _ptr(anchor), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def bsa_fwd_qouter_tokens(q, k, v, B, T, HQ, H, D, block_indices, block_counts, S, block_size, causal,

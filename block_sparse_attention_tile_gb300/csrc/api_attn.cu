@@ -7,8 +7,8 @@ namespace bsa {
 bsa_status simt_block_attention(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                                 int N, int D, const int32_t* im, const int32_t* bs, int J, int M,
                                 int P, const int32_t* idx, const int32_t* num, int kmax,
-                                const void* kb, const void* vb, float scale, void* out, float* lse,
-                                cudaStream_t st);
+                                const void* kb, const void* vb, const float* sbias, float scale, void* out,
+                                float* lse, cudaStream_t st);
 bsa_status simt_token_attention(const void* q, const void* k, const void* v, bsa_dtype dtype, int B,
                                 int Tn, int HQ, int H, int D, const int32_t* bi, const int32_t* bc,
                                 int S, int BS, int causal, float scale, void* out, float* lse,
@@ -16,8 +16,8 @@ bsa_status simt_token_attention(const void* q, const void* k, const void* v, bsa
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
                               const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
                               const void* packed, const int32_t* idx, const int32_t* num, int kmax,
-                              const void* kb, const void* vb, float scale, void* out, float* lse, cudaStream_t st,
-                              bool* handled);
+                              const void* kb, const void* vb, const float* sbias, float scale, void* out, float* lse,
+                              cudaStream_t st, bool* handled);
 
 // The optional geometry must describe the tiling behind index_map.
 static bsa_status check_geometry(const int32_t* g, int N, int J, int M, int P) {
@@ -65,11 +65,11 @@ bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
         rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry, packed,
-                                q2k_idx, q2k_num, kmax, nullptr, nullptr, scale, out, lse, st, &handled);
+                                q2k_idx, q2k_num, kmax, nullptr, nullptr, nullptr, scale, out, lse, st, &handled);
         if (handled) return rc;
     }
     return simt_block_attention(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
-                                prefix_blocks, q2k_idx, q2k_num, kmax, nullptr, nullptr, scale, out,
+                                prefix_blocks, q2k_idx, q2k_num, kmax, nullptr, nullptr, nullptr, scale, out,
                                 lse, st);
 }
 
@@ -77,7 +77,8 @@ bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtyp
                            int N, int D, const int32_t* index_map, const int32_t* block_sizes, int J,
                            int M, int prefix_blocks, const int32_t* geometry, const void* packed,
                            const int32_t* q2k_idx, const int32_t* q2k_num, int kmax, const void* kbar_lp,
-                           const void* vbar_lp, float scale, void* out, float* lse, void* stream) {
+                           const void* vbar_lp, const float* summary_bias, float scale, void* out, float* lse,
+                           void* stream) {
     bsa_status rc = check_block_args(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
                                      prefix_blocks, q2k_idx, q2k_num, kmax, out);
     if (rc != BSA_OK) return rc;
@@ -89,11 +90,11 @@ bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtyp
     if (!force_simt() && dtype == BSA_BF16 && D == 128 && M == 128) {
         bool handled = false;
         rc = tc_block_attention(q, k, v, BH, N, index_map, block_sizes, J, prefix_blocks, geometry, packed,
-                                q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, st, &handled);
+                                q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, summary_bias, scale, out, lse, st, &handled);
         if (handled) return rc;
     }
     return simt_block_attention(q, k, v, dtype, BH, N, D, index_map, block_sizes, J, M,
-                                prefix_blocks, q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out,
+                                prefix_blocks, q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, summary_bias, scale, out,
                                 lse, st);
 }
 

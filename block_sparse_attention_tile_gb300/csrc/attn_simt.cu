@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256) block_attn_simt_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int D, int Dp,
     const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M,
     int P, const int32_t* __restrict__ q2k_idx, const int32_t* __restrict__ q2k_num, int kmax,
-    const T* __restrict__ kbar_lp, const T* __restrict__ vbar_lp, float scale_log2,
+    const T* __restrict__ kbar_lp, const T* __restrict__ vbar_lp, const float* __restrict__ sbias, float scale_log2,
     T* __restrict__ out, float* __restrict__ lse, int* status) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const int Jr = J - P;
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(256) block_attn_simt_kernel(
                 float b = -CUDART_INF_F;
                 if (t < nk && !L.sel[jr]) {
                     const int n_j = block_sizes[P + jr];
-                    if (n_j > 0) b = log2f((float)n_j);
+                    // log-mass of the summary token: log n_j, or the caller's bias
+                    if (n_j > 0) b = sbias ? sbias[(long long)bh * J + P + jr] * kLog2e : log2f((float)n_j);
                 }
                 L.bias[t] = b;
             }
@@ -227,7 +228,8 @@ template <typename T, bool kSummary>
 static bsa_status launch_block(const void* q, const void* k, const void* v, int BH, int N, int D,
                                const int32_t* im, const int32_t* bs, int J, int M, int P,
                                const int32_t* idx, const int32_t* num, int kmax, const void* kb,
-                               const void* vb, float scale, void* out, float* lse, cudaStream_t st) {
+                               const void* vb, const float* sbias, float scale, void* out, float* lse,
+                               cudaStream_t st) {
     const int Dp = (D + 3) / 4 * 4;
     const size_t smem = smem_bytes(padded_rows(M, 8), Dp, kSummary ? J - P : 0);
     auto kern = block_attn_simt_kernel<T, kSummary>;
@@ -235,7 +237,7 @@ static bsa_status launch_block(const void* q, const void* k, const void* v, int 
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     dim3 grid(J, BH);
     kern<<<grid, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, N, D, Dp, im, bs, J, M, P,
-                                  idx, num, kmax, (const T*)kb, (const T*)vb, scale * kLog2e,
+                                  idx, num, kmax, (const T*)kb, (const T*)vb, sbias, scale * kLog2e,
                                   (T*)out, lse, status_word());
     return check_launch("block_attn_simt_kernel");
 }
@@ -243,14 +245,14 @@ static bsa_status launch_block(const void* q, const void* k, const void* v, int 
 bsa_status simt_block_attention(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,
                                 int N, int D, const int32_t* im, const int32_t* bs, int J, int M,
                                 int P, const int32_t* idx, const int32_t* num, int kmax,
-                                const void* kb, const void* vb, float scale, void* out, float* lse,
-                                cudaStream_t st) {
+                                const void* kb, const void* vb, const float* sbias, float scale, void* out,
+                                float* lse, cudaStream_t st) {
     const bool summary = kb != nullptr;
     if (dtype == BSA_F32)
-        return summary ? launch_block<float, true>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, scale, out, lse, st)
-                       : launch_block<float, false>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, scale, out, lse, st);
-    return summary ? launch_block<__nv_bfloat16, true>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, scale, out, lse, st)
-                   : launch_block<__nv_bfloat16, false>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, scale, out, lse, st);
+        return summary ? launch_block<float, true>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, sbias, scale, out, lse, st)
+                       : launch_block<float, false>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, sbias, scale, out, lse, st);
+    return summary ? launch_block<__nv_bfloat16, true>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, sbias, scale, out, lse, st)
+                   : launch_block<__nv_bfloat16, false>(q, k, v, BH, N, D, im, bs, J, M, P, idx, num, kmax, kb, vb, sbias, scale, out, lse, st);
 }
 
 template <typename T>

@@ -102,6 +102,7 @@ struct Params {
     int geo, window;  // geometry given; 5-D window boxes usable
     int T, H, W, bT, bH, bW, nH, nW;
     int packed;       // Q/K/V also given in block order: every tile is one box
+    const float* sbias;  // summary biases [BH, J] (natural log), or null for log n_j
 };
 
 // Where a 128-row tile comes from: gathered rows (mode 0), a box of 128
@@ -263,7 +264,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float b = -CUDART_INF_F;
             if (jr < Jr && !((selbits[jr >> 5] >> (jr & 31)) & 1u)) {
                 const int nb = prm.block_sizes[P + jr];
-                if (nb > 0) b = log2f((float)nb);
+                // log-mass of the summary token: log n_j, or the caller's bias
+                if (nb > 0) b = prm.sbias ? prm.sbias[(long long)bh * J + P + jr] * kLog2e : log2f((float)nb);
             }
             bias[jr] = b;
         }
@@ -705,8 +707,8 @@ static bool register_split_fits() {
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
                               const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
                               const void* packed, const int32_t* idx, const int32_t* num, int kmax,
-                              const void* kb, const void* vb, float scale, void* out, float* lse, cudaStream_t st,
-                              bool* handled) {
+                              const void* kb, const void* vb, const float* sbias, float scale, void* out, float* lse,
+                              cudaStream_t st, bool* handled) {
     *handled = false;
     const bool summary = kb != nullptr;
     const int Jr = J - P;
@@ -784,6 +786,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     prm.kmax = kmax;
     prm.scale_log2 = scale * kLog2e;
     prm.summary = summary ? 1 : 0;
+    prm.sbias = sbias;
     cudaError_t e = cudaFuncSetAttribute(tc::bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));

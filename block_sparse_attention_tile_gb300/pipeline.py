@@ -69,10 +69,11 @@ class BlockSparseResult:
     q2k_idx: torch.Tensor
     q2k_num: torch.Tensor
     packed: Optional[torch.Tensor] = None
+    summary_bias: Optional[torch.Tensor] = None
 
 
 def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=False, need_lse=True,
-                           tiles=None, pass_geometry=True, packed=None):
+                           tiles=None, pass_geometry=True, packed=None, reweight=False):
     """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
 
     q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
@@ -80,7 +81,10 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     let the pool pass also write Q/K/V in block order for the attention to
     read (default: when the blocks come from a permutation, whose rows the
     tensor-core kernel would otherwise gather four at a time).  Returns the
-    output in raster order plus every intermediate."""
+    output in raster order plus every intermediate.  ``reweight`` (with
+    ``summary``): the unselected blocks are summarised by Spark-Reweight
+    (weighted key and value at the head's mean video query, log-mass bias)
+    instead of by their means and log(n_j)."""
     BH, N, D = q.shape
     assert N == geom.n_tokens
     dev = q.device
@@ -104,15 +108,21 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
     ws = torch.empty((bsa.bsa_route_workspace(BH, Jr) // 4,), dtype=torch.float32, device=dev)
     bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num, ws)
+    sbias = None
+    if summary and reweight:
+        sbias = torch.empty((BH, J), dtype=torch.float32, device=dev)
+        rws = torch.empty((bsa.bsa_reweight_workspace(BH, D) // 4,), dtype=torch.float32, device=dev)
+        bsa.bsa_reweight_summaries(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, scale, kbar_lp, vbar_lp,
+                                   sbias, rws, qbar=qbar)
     out = torch.empty_like(q)
     lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
     if summary:
         bsa.bsa_fwd_summary(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
-                            q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, packed=pk)
+                            q2k_idx, q2k_num, kmax, kbar_lp, vbar_lp, scale, out, lse, packed=pk, summary_bias=sbias)
     else:
         bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
                            q2k_idx, q2k_num, kmax, scale, out, lse, packed=pk)
-    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk)
+    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk, sbias)
 
 
 def nsa_qouter(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None, need_lse=True):

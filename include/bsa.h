@@ -263,14 +263,47 @@ bsa_status bsa_combine(const void* obuf, bsa_dtype obuf_dtype, const float* lseb
  * ([VSA] §5.3, Context rows are global).
  * Arguments as bsa_fwd_qouter, plus kbar_lp / vbar_lp: [device] [BH, J, D]
  * in `dtype`, the block means as written by bsa_pool_blocks (the rows of
- * the prefix blocks are not read).  J - prefix_blocks <= 1024. */
+ * the prefix blocks are not read), or the weighted summaries written by
+ * bsa_reweight_summaries.  summary_bias: [device] float [BH, J] natural-log
+ * biases replacing log(n_j) in the virtual logit ([Spark] §08, the log-mass
+ * term b_j of Spark-Reweight), or NULL for log(n_j).  J - prefix_blocks <= 1024. */
 bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtype dtype,
                            int BH, int N, int D, const int32_t* index_map,
                            const int32_t* block_sizes, int J, int M, int prefix_blocks,
                            const int32_t* geometry, const void* packed,
                            const int32_t* q2k_idx, const int32_t* q2k_num, int kmax,
                            const void* kbar_lp, const void* vbar_lp,
+                           const float* summary_bias,
                            float scale, void* out, float* lse, void* stream);
+
+/* ------------------------------------------------------------------ a9 ----
+ * Spark-Reweight summaries.  [Spark] §07: one representative query per
+ * (batch, head), a = the mean of the query rows of every routed block
+ * (blocks prefix_blocks .. J-1), taken from q, or, when qbar is given, as
+ * sum_j n_j qbar_j / sum_j n_j (the same mean, from the block means).  [Spark] §08: for each routed block j with
+ * members m (token index_map[j*M + m], m < n_j) and logits
+ * s_m = a.k_m * scale: p_m = exp(s_m - max) / Z', the weighted key
+ * kt_j = sum_m p_m k_m and value vt_j = sum_m p_m v_m, and the bias
+ * b_j = log Z(a) - a.kt_j' * scale, where log Z(a) = max + log Z' and kt_j'
+ * is kt_j as stored in `dtype` (so b_j offsets exactly the logit the summary
+ * attention recomputes at q = a).  Blocks with n_j = 0 get b_j = -inf.
+ * q, k, v: [device] [BH, N, D] of `dtype` (F32 or BF16); q may be NULL
+ * when qbar is given.  qbar: [device] float [BH, J, D] block means as
+ * written by bsa_pool_blocks, or NULL.  index_map, block_sizes as
+ * bsa_pool_blocks.  Outputs (rows of the prefix blocks are
+ * not written): kt_lp, vt_lp [device] [BH, J, D] of `dtype`; bias [device]
+ * float [BH, J]; anchor [device] float [BH, D] or NULL.  workspace: [device]
+ * bsa_reweight_workspace(BH, D) bytes, 16-byte aligned, caller-owned.
+ * Deterministic: every sum runs in a fixed order.  1 <= D <= 256; a member
+ * index outside [0, N) raises BSA_ERR_INDEX and the row is skipped. */
+size_t bsa_reweight_workspace(int BH, int D);
+bsa_status bsa_reweight_summaries(const void* q, const float* qbar, const void* k, const void* v,
+                                  bsa_dtype dtype,
+                                  int BH, int N, int D, const int32_t* index_map,
+                                  const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                                  float scale, void* kt_lp, void* vt_lp, float* bias,
+                                  float* anchor, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 /* Forces the CUDA-core attention kernels even where a tensor-core kernel
  * exists (1) or restores the default dispatch (0).  Host, process-wide. */

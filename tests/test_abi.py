@@ -86,4 +86,15 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     assert bsa.bsa_route_workspace(24, 960) == 24 * 960 * 960 * 4
     rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # max_chunks too small
+    # reweight: null q, then a workspace one int short of 2 heads x (32 splits x (8 floats + 1 int) + 8 floats)
+    rc = lib.bsa_reweight_summaries(None, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
+    assert bsa.bsa_reweight_workspace(2, 8) == 2 * 32 * (8 * 4 + 4) + 2 * 8 * 4
+    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16,
+                                    bsa.bsa_reweight_workspace(2, 8) - 4, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "workspace" in bsa.bsa_last_error()
+    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 4, 0.5, 1, 1, 1, None, 16, 1 << 20, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "block counts" in bsa.bsa_last_error()  # no routed block
+    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 300, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1 << 20, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()  # D > 256
     assert bsa.bsa_version() >= 100

@@ -55,7 +55,8 @@ def test_tile_map_bit_exact(lib, grid, block, M, n_prefix, permuted):
 # ---------------------------------------------------------------- a2-a4, block granularity
 
 def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, force_simt=False,
-                    n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True, packed=None):
+                    n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True, packed=None,
+                    reweight=False):
     pl = _pipeline()
     T, H, W = grid
     if cluster:
@@ -70,7 +71,7 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
                        perm=torch.as_tensor(perm, device=DEV) if permuted else None)
     lib.bsa_set_force_simt(force_simt)
     res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary,
-                                    pass_geometry=pass_geometry, packed=packed)
+                                    pass_geometry=pass_geometry, packed=packed, reweight=reweight)
     torch.cuda.synchronize()
     blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
     if res.packed is not None:
@@ -90,7 +91,11 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
         E = oracle.routing_scores(qbar[P:], kbar[P:], D)
         gi, gn = res.q2k_idx[bh].cpu().numpy(), res.q2k_num[bh].cpu().numpy()
         flagged += len(check_route(gi, gn, E, k))
-        if summary:
+        if summary and reweight:
+            rk = oracle.bf16_round if dtype == torch.bfloat16 else None
+            kt, vt, b, _ = oracle.reweight_summaries(Q, K, V, blocks, scale, prefix_blocks=P, round_key=rk)
+            O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kt, vt, scale, prefix_blocks=P, block_bias=b)
+        elif summary:
             vbar = oracle.pool_blocks(V, blocks)
             O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kbar[P:], vbar[P:], scale, prefix_blocks=P)
         else:
@@ -147,6 +152,88 @@ def test_summary_small_bf16(lib, force_simt, packed):
 def test_summary_fp32_ragged(lib):
     _run_block_case(lib, 1, 1, (5, 3, 4), (2, 2, 3), 12, 8, 2, torch.float32, 14, n_prefix=20,
                     summary=True)
+
+
+# ---------------------------------------------------------------- a9 Spark-Reweight summaries
+
+def _reweight_case(lib, h, n_prefix, grid, block, M, D, dtype, seed, permuted, from_means=False):
+    pl = _pipeline()
+    T, H, W = grid
+    q, kk, v = synthetic.cluster_qkv(h, n_prefix, T * H * W, D, seed, dtype)
+    perm = synthetic.permutation(T * H * W, seed + 3) if permuted else None
+    geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
+                       perm=torch.as_tensor(perm, device=DEV) if permuted else None)
+    im, bs = pl.tile_map(geom)
+    J, P, N = im.shape[0], geom.prefix_blocks, geom.n_tokens
+    scale = D ** -0.5
+    kt = torch.full((h, J, D), 7.0, dtype=dtype, device=DEV)   # prefix rows must stay untouched
+    vt = torch.full_like(kt, 7.0)
+    bias = torch.full((h, J), 7.0, dtype=torch.float32, device=DEV)
+    anchor = torch.empty((h, D), dtype=torch.float32, device=DEV)
+    ws = torch.empty((lib.bsa_reweight_workspace(h, D) // 4,), dtype=torch.float32, device=DEV)
+    qbar = None
+    if from_means:
+        qbar = torch.empty((h, J, D), dtype=torch.float32, device=DEV)
+        lib.bsa_pool_blocks(q.to(DEV), kk.to(DEV), None, h, N, D, im, bs, J, M, qbar, torch.empty_like(qbar))
+    lib.bsa_reweight_summaries(None if from_means else q.to(DEV), kk.to(DEV), v.to(DEV), h, N, D, im, bs, J, M, P,
+                               scale, kt, vt, bias, ws, anchor=anchor, qbar=qbar)
+    torch.cuda.synchronize()
+    blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
+    rk = oracle.bf16_round if dtype == torch.bfloat16 else None
+    # stored rows: half an ulp of the storage type plus the float32 sums
+    rel = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -20
+    for bh in range(h):
+        Q, K, V = f64(q[bh]), f64(kk[bh]), f64(v[bh])
+        okt, ovt, ob, oa = oracle.reweight_summaries(Q, K, V, blocks, scale, prefix_blocks=P, round_key=rk)
+        ga = anchor[bh].cpu().double().numpy()
+        assert np.abs(ga - oa).max() <= 1e-5 * max(1.0, np.abs(oa).max())
+        gkt, gvt = f64(kt[bh]), f64(vt[bh])
+        assert np.all(gkt[:P] == 7.0) and np.all(gvt[:P] == 7.0)
+        # float32 sums of up to M weighted rows: a few ulps of the largest row entry
+        kabs, vabs = 1e-5 * max(1.0, np.abs(K).max()), 1e-5 * max(1.0, np.abs(V).max())
+        assert np.all(np.abs(gkt[P:] - okt) <= rel * np.abs(okt) + kabs), "k~ head %d" % bh
+        assert np.all(np.abs(gvt[P:] - ovt) <= rel * np.abs(ovt) + vabs), "v~ head %d" % bh
+        # b uses the stored key: where the float32 sum and the exact one round
+        # to neighbouring storage values, b moves by at most scale*|a_d|*ulp(k~_d)
+        gb = bias[bh].cpu().double().numpy()
+        assert np.all(gb[:P] == 7.0)
+        ulp = (2.0 ** -7 if dtype == torch.bfloat16 else 2.0 ** -22) * np.abs(okt)
+        tol = scale * (ulp @ np.abs(oa)) + 1e-4 * (1.0 + np.abs(ob))
+        assert np.all(np.abs(gb[P:] - ob) <= tol), "b head %d: %g" % (bh, np.abs(gb[P:] - ob).max())
+        # the defining property at q = a: the virtual logit plus b is log Z(a)
+        lz = np.array([np.log(np.exp(K[blk] @ oa * scale).sum()) for blk in blocks[P:]])
+        assert np.all(np.abs((gkt[P:] @ ga) * scale + gb[P:] - lz) <= 1e-3 * (1.0 + np.abs(lz)))
+
+
+@pytest.mark.parametrize("dtype,from_means", [(torch.bfloat16, False), (torch.bfloat16, True),
+                                              (torch.float32, False)])
+def test_reweight_summaries_prefix_permuted(lib, dtype, from_means):
+    # 256 text tokens (2 prefix blocks) + a (4,16,32) grid under a permutation: 16 routed blocks
+    _reweight_case(lib, 2, 256, (4, 16, 32), (1, 1, 1), 128, 128, dtype, 606, True, from_means)
+
+
+@pytest.mark.parametrize("D,from_means", [(16, False), (16, True), (33, False), (200, True), (256, False)])
+def test_reweight_summaries_ragged_windows_fp32(lib, D, from_means):
+    # (5,3,4) in (2,2,3) windows after a 20-token prefix: ragged blocks, M=12; D=16 leaves
+    # half the lanes idle, D=33 takes the scalar loads (odd rows), D=200 eight channels a lane,
+    # D=256 float32 rows too wide to double-buffer in shared memory (register path)
+    _reweight_case(lib, 3, 20, (5, 3, 4), (2, 2, 3), 12, D, torch.float32, 17, False, from_means)
+
+
+def test_reweight_summaries_large_blocks_bf16(lib):
+    # M=512 blocks (a warp walks 128 rows, four index batches) with a ragged last block
+    _reweight_case(lib, 2, 0, (3, 20, 30), (1, 1, 1), 512, 64, torch.bfloat16, 23, True)
+
+
+@pytest.mark.parametrize("force_simt,packed", [(False, True), (True, False)])
+def test_summary_reweight_bf16(lib, force_simt, packed):
+    _run_block_case(lib, 1, 2, (4, 16, 32), (1, 1, 1), 128, 128, 3, torch.bfloat16, 515, n_prefix=256,
+                    permuted=True, summary=True, cluster=True, force_simt=force_simt, packed=packed, reweight=True)
+
+
+def test_summary_reweight_fp32_ragged(lib):
+    _run_block_case(lib, 1, 1, (5, 3, 4), (2, 2, 3), 12, 8, 2, torch.float32, 24, n_prefix=20,
+                    summary=True, reweight=True)
 
 
 # ---------------------------------------------------------------- token granularity + KV-outer
