@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  This package is a plain, slow, obviously-correct
 float64 restatement of the definitions given on four pages:
 
 * "VSA 实现详解：三维分块、均值路由与块稀疏 Attention" (maple.link) -- 3D tiling,
-  mean pooling, the routing matrix E, per-row TopK, block-sparse attention.
+  mean pooling, the routing matrix E, per-row TopK, block-sparse attention,
+  and the gated coarse branch softmax(E) V_bar.
 * "NSA 算子解析（Torch/Tilelang）" (devpress.csdn.net) -- the selected-attention
   branch with caller-supplied block indices/counts and GQA.
 * "MSA 为什么采用 KV-outer Sparse Attention Forward" (notes.kuangjux.top) -- the
@@ -41,3 +42,4 @@ from .kvouter import (  # noqa: F401
     reverse_index, schedule_chunks, kvouter_partials, combine_partials,
 )
 from .spark import bf16_round, reweight_anchor, reweight_summary, reweight_summaries  # noqa: F401
+from .coarse import coarse_attention, coarse_output  # noqa: F401

@@ -539,3 +539,58 @@ def test_reweight_anchor_and_bf16_round():
                         np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -2.5, 0.0])])  # two exact ties
     want = torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
     assert np.array_equal(oracle.bf16_round(x), want)
+
+
+# ---------------------------------------------------------------- coarse branch (VSA §6.7)
+
+def test_coarse_hand_example():
+    # D = 1, scale 1: qbar = [ln 3, 0], kbar = [0, 1] -> E = [[0, ln 3], [0, 0]];
+    # row 0 weights [1/4, 3/4], row 1 [1/2, 1/2]; vbar = [1, 5] -> C = [4, 3]
+    E = oracle.routing_scores(np.array([[math.log(3.0)], [0.0]]), np.array([[0.0], [1.0]]), 1)
+    C = oracle.coarse_attention(E, np.array([[1.0], [5.0]]))
+    assert np.allclose(C[:, 0], [4.0, 3.0], rtol=0, atol=1e-14)
+
+
+def test_coarse_with_one_token_blocks_is_dense_attention():
+    # 1-token blocks: the means are the rows themselves and the coarse branch is
+    # plain softmax attention over all tokens
+    Q, K, V = _random_qkv(48, 8, 21)
+    blocks = oracle.tile_3d(3, 4, 4, 1, 1, 1)
+    qb, kb, vb = (oracle.pool_blocks(X, blocks) for X in (Q, K, V))
+    C = oracle.coarse_attention(oracle.routing_scores(qb, kb, 8), vb)
+    order = np.concatenate(blocks)
+    assert np.abs(C - sdpa64(Q[order], K[order], V[order], scale=8 ** -0.5)).max() < 1e-13
+
+
+def test_coarse_uniform_and_dominant_rows():
+    rng = np.random.default_rng(5)
+    vbar = rng.normal(size=(6, 4))
+    E = np.zeros((6, 6))
+    E[2, 4] = 800.0  # one logit dominates row 2
+    C = oracle.coarse_attention(E, vbar)
+    assert np.abs(C[0] - vbar.mean(0)).max() < 1e-14
+    assert np.abs(C[2] - vbar[4]).max() < 1e-14
+    # shifting a row of E by a constant changes nothing
+    E2 = E.copy()
+    E2[3] += 123.0
+    assert np.abs(oracle.coarse_attention(E2, vbar) - C).max() < 1e-12
+
+
+def test_coarse_output_gate_and_prefix():
+    rng = np.random.default_rng(6)
+    blocks = oracle.tile_prefix(5, 4) + oracle.tile_3d(2, 2, 3, 1, 2, 2, offset=5)
+    P, N, D = 2, 17, 3
+    O = rng.normal(size=(N, D))
+    C = rng.normal(size=(len(blocks) - P, D))
+    # a zero gate (the page's default without weights) leaves the sparse output
+    assert np.array_equal(oracle.coarse_output(O, C, np.zeros(D), blocks, P), O)
+    g = rng.normal(size=(N, D))
+    got = oracle.coarse_output(O, C, g, blocks, P)
+    assert np.array_equal(got[:5], O[:5])  # prefix rows untouched
+    for r, members in enumerate(blocks[P:]):
+        for t in members:
+            assert np.allclose(got[t], O[t] + g[t] * C[r], rtol=0, atol=1e-15)
+    # a per-channel gate is the per-token gate with equal rows
+    gc = rng.normal(size=D)
+    assert np.array_equal(oracle.coarse_output(O, C, gc, blocks, P),
+                          oracle.coarse_output(O, C, np.tile(gc, (N, 1)), blocks, P))
