@@ -19,6 +19,9 @@ Other workloads (--workload):
                  unselected blocks
   spark_reweight the same with Spark-Reweight summaries (weighted key and
                  value at the head's mean video query, log-mass bias)
+  video_dit_coarse  the default workload plus the gated coarse branch
+                 softmax(E) V_bar broadcast to each block's tokens (synthetic
+                 per-head, per-channel gate)
 
 Metric: effective sparse-attention TFLOP/s = 4*Hq*N*d*k*B_k / step time
 (the FLOP count of the "MSA ... KV-outer" page, eq. 13/15).
@@ -52,6 +55,8 @@ WORKLOADS = {
                        dtype="f32"),
     "spark_summary": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
                           seed=505, dtype="bf16", n_text=1024, summary=True),
+    "video_dit_coarse": dict(kind="block", B=1, heads=24, D=128, grid=(30, 48, 80), block=(4, 4, 8), M=128, k=96,
+                             seed=202, dtype="bf16", coarse=True),
     "spark_reweight": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
                            seed=505, dtype="bf16", n_text=1024, summary=True, reweight=True),
     "nsa_prefill": dict(kind="token", B=2, T=8192, HQ=64, H=4, D=128, BS=64, S=16, seed=303, zipf=False),
@@ -145,6 +150,7 @@ w = json.loads({w!r})
 budget_s = {budget}
 T, H, W = w["grid"]; bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
 n_text = w.get("n_text", 0); summary = w.get("summary", False); reweight = w.get("reweight", False)
+coarse = w.get("coarse", False)
 dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
 t0 = time.perf_counter()
 if summary:
@@ -159,7 +165,7 @@ gen_s = time.perf_counter() - t0
 P = len(oracle.tile_prefix(n_text, M)) if n_text else 0
 t0 = time.perf_counter()
 qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
-vbar = oracle.pool_blocks(V, blocks) if summary else None
+vbar = oracle.pool_blocks(V, blocks) if (summary or coarse) else None
 E = oracle.routing_scores(qbar[P:], kbar[P:], D)
 idx, num = oracle.route(E, k, k)
 sbias = None
@@ -167,6 +173,10 @@ if reweight:
     kbar, vbar, sbias, _ = oracle.reweight_summaries(Q, K, V, blocks, D ** -0.5, prefix_blocks=P,
                                                      round_key=oracle.bf16_round if w["dtype"] == "bf16" else None)
     kbar = np.concatenate([np.zeros((P, D)), kbar]); vbar = np.concatenate([np.zeros((P, D)), vbar])
+C = None
+if coarse:
+    C = oracle.coarse_attention(E, vbar[P:])
+    g = synthetic.normal((1, D), w["seed"] + 71)[0].double().numpy()
 route_s = time.perf_counter() - t0
 rng = np.random.default_rng(0)
 order = rng.permutation(len(blocks))
@@ -177,7 +187,9 @@ while done < len(order) and (done < 2 or time.perf_counter() - t0 < budget_s):
         oracle.summary_attention(Q, K, V, blocks, idx, num, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
                                  query_blocks=qb, block_bias=sbias)
     else:
-        oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb)
+        O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb)
+        if C is not None and qb[0] >= P:
+            oracle.coarse_output(O, C[qb[0] - P:qb[0] - P + 1], g, [blocks[qb[0]]], 0)
     done += 1
 attn_s = time.perf_counter() - t0
 J = len(blocks)
@@ -239,7 +251,8 @@ def run_oracle_sample(wname, budget_s=15.0):
                   "attended, all %d heads (%.1f s); step time scaled by tokens and batch"
                   % (w["B"], w["T"], r["route_s"], r["units"], r["total_units"], w["HQ"], r["attn_s"]))
     else:
-        pre = "tile map, pool, route" + (" and Spark-Reweight summaries" if w.get("reweight") else "")
+        pre = ("tile map, pool, route" + (" and Spark-Reweight summaries" if w.get("reweight") else "")
+               + (" and the coarse branch softmax(E) V_bar" if w.get("coarse") else ""))
         sample = ("1 of %d heads: %s of all %d blocks (%.1f s) plus %d of %d query blocks "
                   "attended (%.1f s); step time scaled by heads and blocks"
                   % (w["heads"], pre, r["total_units"], r["route_s"], r["units"], r["total_units"], r["attn_s"]))
@@ -311,8 +324,11 @@ class BlockWorkload:
         T, H, W = w["grid"]
         self.summary = w.get("summary", False)
         self.reweight = self.summary and w.get("reweight", False)
+        self.coarse = w.get("coarse", False)
         if self.reweight:
             self.stage_names = ["tile_map", "pool", "route", "reweight", "attention"]
+        if self.coarse:
+            self.stage_names = ["tile_map", "pool", "route", "attention", "coarse_attention", "coarse_apply"]
         n_text = w.get("n_text", 0)
         D, M, k = w["D"], w["M"], w["k"]
         self.BH = w["B"] * w["heads"]
@@ -338,7 +354,7 @@ class BlockWorkload:
         self.bs = torch.empty((J,), dtype=torch.int32, device=dev)
         self.qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
         self.kbar = torch.empty_like(self.qbar)
-        self.vbar = torch.empty_like(self.qbar) if self.summary else None
+        self.vbar = torch.empty_like(self.qbar) if (self.summary or self.coarse) else None
         self.kbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
         self.vbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
         # permuted blocks: the pool pass also writes Q/K/V in block order for the attention
@@ -355,8 +371,11 @@ class BlockWorkload:
         self.sbias = torch.empty((BH, J), dtype=torch.float32, device=dev) if self.reweight else None
         self.rw_ws = (torch.empty((_bsa.bsa_reweight_workspace(BH, D) // 4,), dtype=torch.float32, device=dev)
                       if self.reweight else None)
-        # tile map, pool, route (contraction + select), [reweight: mean partials, mean, summaries], attention
-        self.launches_per_step = 5 + (3 if self.reweight else 0)
+        self.C = torch.empty((BH, self.Jr, D), dtype=torch.float32, device=dev) if self.coarse else None
+        self.gate = (synthetic.normal((BH, D), seed + 71, dev) if self.coarse else None)
+        # tile map, pool, route (contraction + select), [reweight: mean partials, mean, summaries], attention,
+        # [coarse: attention, apply]
+        self.launches_per_step = 5 + (3 if self.reweight else 0) + (2 if self.coarse else 0)
 
     def step(self, ev=None, q=None, k=None, v=None):
         from block_sparse_attention_tile_gb300 import bsa
@@ -387,6 +406,13 @@ class BlockWorkload:
         else:
             bsa.bsa_fwd_qouter(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                self.q2k, self.q2n, kk, self.scale, self.out, self.lse, packed=self.packed)
+        if self.coarse:
+            if ev: ev[4].record(st)
+            bsa.bsa_coarse_attention(self.route_ws, self.Jr * self.Jr, self.vbar[:, self.P:], self.J * D, self.BH,
+                                     self.Jr, D, self.C)
+            if ev: ev[5].record(st)
+            bsa.bsa_coarse_apply(self.out, self.C, self.gate, False, self.BH, self.N, D, self.im, self.bs, self.J, M,
+                                 self.P)
         if ev: ev[len(self.stage_names)].record(st)
 
     def host_inputs(self):
@@ -425,6 +451,11 @@ class BlockWorkload:
             bsa.bsa_fwd_qouter(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                self.q2k[sl], self.q2n[sl], kk, self.scale, self.out[sl], self.lse[sl],
                                packed=packed_chunk)
+        if self.coarse:
+            bsa.bsa_coarse_attention(self.route_ws, self.Jr * self.Jr, self.vbar[sl, self.P:], self.J * D, nh,
+                                     self.Jr, D, self.C[sl])
+            bsa.bsa_coarse_apply(self.out[sl], self.C[sl], self.gate[sl], False, nh, self.N, D, self.im, self.bs,
+                                 self.J, M, self.P)
 
     def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=4):
         """End-to-end step with host buffers, pipelined by heads: chunk c's
@@ -528,6 +559,17 @@ class BlockWorkload:
                      "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
             "route": {"bound": "alu", "achieved": route_tf, "peak": fp32, "unit": "TFLOP/s", "frac": route_tf / fp32,
                       "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}}
+        if self.coarse:
+            cflops = 2.0 * self.BH * self.Jr * self.Jr * D
+            ctf = cflops / (stage_ms["coarse_attention"] * 1e-3) / 1e12
+            secondary["coarse_attention"] = {"bound": "alu", "achieved": ctf, "peak": fp32, "unit": "TFLOP/s",
+                                             "frac": ctf / fp32, "flops_per_launch": cflops}
+            el = self.q.element_size()
+            rows = float(self.bs[self.P:].long().sum().item())
+            ab = 2 * self.BH * rows * D * el + self.BH * self.Jr * D * 4 + self.BH * D * 4 + self.J * self.w["M"] * 4
+            agbs = ab / (stage_ms["coarse_apply"] * 1e-3) / 1e9
+            secondary["coarse_apply"] = {"bound": "hbm", "achieved": agbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                         "frac": agbs / peaks["hbm_gbs"], "bytes_per_launch": ab}
         if self.reweight:
             rb = self.reweight_bytes()
             rgbs = rb / (stage_ms["reweight"] * 1e-3) / 1e9
@@ -540,6 +582,8 @@ class BlockWorkload:
             config.update({"n_text": self.w["n_text"], "permuted": True, "summary": True})
             if self.reweight:
                 config["summaries"] = "spark-reweight"
+        if self.coarse:
+            config["coarse"] = "softmax(E) V_bar, per-head per-channel gate"
         nbytes = 3 * self.q.numel() * self.q.element_size()
         config["l2"] = ("inputs larger than L2: Q,K,V = %.2f GB per step" % (nbytes / 1e9) if nbytes > 129e6 else
                         "inputs smaller than L2 (%.1f MB): L2 not flushed, launch-bound tiny case" % (nbytes / 1e6))

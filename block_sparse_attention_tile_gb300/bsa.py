@@ -59,6 +59,8 @@ _SIGS = {
     "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, P, F, P, P, P]),
     "bsa_reweight_workspace": (SZ, [I, I]),
     "bsa_reweight_summaries": (I, [P, P, P, P, I, I, I, I, P, P, I, I, I, F, P, P, P, P, P, SZ, P]),
+    "bsa_coarse_attention": (I, [P, I64, P, I64, I, I, I, P, P]),
+    "bsa_coarse_apply": (I, [P, I, P, P, I, I, I, I, P, P, I, I, I, P]),
     "bsa_set_force_simt": (None, [I]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -223,3 +225,14 @@ def bsa_fwd_kvouter(q, k, v, B, N, HQ, H, D, row_ptr, q_idx, slot, chunks, n_chu
 def bsa_combine(obuf, lsebuf, nslots, B, N, HQ, H, S, D, out, lse=None, stream=None):
     _check(_lib.bsa_combine(_ptr(obuf), _dtype(obuf), _ptr(lsebuf), _ptr(nslots), B, N, HQ, H, S, D,
                             _ptr(out), _dtype(out), _ptr(lse), _stream(stream)))
+
+
+def bsa_coarse_attention(E, e_head_stride, vbar, vbar_head_stride, BH, Jr, D, C, stream=None):
+    _check(_lib.bsa_coarse_attention(_ptr(E), e_head_stride, _ptr(vbar), vbar_head_stride, BH, Jr, D, _ptr(C),
+                                     _stream(stream)))
+
+
+def bsa_coarse_apply(out, C, gate, gate_per_token, BH, N, D, index_map, block_sizes, J, M, prefix_blocks,
+                     stream=None):
+    _check(_lib.bsa_coarse_apply(_ptr(out), _dtype(out), _ptr(C), _ptr(gate), 1 if gate_per_token else 0, BH, N, D,
+                                 _ptr(index_map), _ptr(block_sizes), J, M, prefix_blocks, _stream(stream)))

@@ -70,10 +70,11 @@ class BlockSparseResult:
     q2k_num: torch.Tensor
     packed: Optional[torch.Tensor] = None
     summary_bias: Optional[torch.Tensor] = None
+    coarse: Optional[torch.Tensor] = None
 
 
 def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=False, need_lse=True,
-                           tiles=None, pass_geometry=True, packed=None, reweight=False):
+                           tiles=None, pass_geometry=True, packed=None, reweight=False, coarse_gate=None):
     """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
 
     q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
@@ -84,7 +85,9 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     output in raster order plus every intermediate.  ``reweight`` (with
     ``summary``): the unselected blocks are summarised by Spark-Reweight
     (weighted key and value at the head's mean video query, log-mass bias)
-    instead of by their means and log(n_j)."""
+    instead of by their means and log(n_j).  ``coarse_gate`` (float32 [BH, D]
+    per head and channel, or [BH, N, D] per token): add the gated coarse
+    branch softmax(E) V_bar of each routed query block to its tokens."""
     BH, N, D = q.shape
     assert N == geom.n_tokens
     dev = q.device
@@ -99,10 +102,11 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     pk = torch.empty((3, BH, J, geom.M, D), dtype=q.dtype, device=dev) if packed else None
     qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
     kbar = torch.empty_like(qbar)
-    vbar = torch.empty_like(qbar) if (summary or packed) else None
+    coarse = coarse_gate is not None
+    vbar = torch.empty_like(qbar) if (summary or packed or coarse) else None
     kbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
     vbar_lp = torch.empty((BH, J, D), dtype=q.dtype, device=dev) if summary else None
-    bsa.bsa_pool_blocks(q, k, v if (summary or packed) else None, BH, N, D, index_map, block_sizes, J, geom.M,
+    bsa.bsa_pool_blocks(q, k, v if vbar is not None else None, BH, N, D, index_map, block_sizes, J, geom.M,
                         qbar, kbar, vbar, kbar_lp, vbar_lp, packed=pk)
     q2k_idx = torch.empty((BH, Jr, kmax), dtype=torch.int32, device=dev)
     q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
@@ -122,7 +126,14 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     else:
         bsa.bsa_fwd_qouter(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, geom.geometry if pass_geometry else None,
                            q2k_idx, q2k_num, kmax, scale, out, lse, packed=pk)
-    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk, sbias)
+    C = None
+    if coarse:
+        # E is the route's own score matrix, left in its workspace
+        C = torch.empty((BH, Jr, D), dtype=torch.float32, device=dev)
+        bsa.bsa_coarse_attention(ws, Jr * Jr, vbar[:, P:], J * D, BH, Jr, D, C)
+        bsa.bsa_coarse_apply(out, C, coarse_gate, coarse_gate.dim() == 3, BH, N, D, index_map, block_sizes, J,
+                             geom.M, P)
+    return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk, sbias, C)
 
 
 def nsa_qouter(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None, need_lse=True):

@@ -127,7 +127,9 @@ bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtyp
  * scaled, so both paths below give the same lists.
  * workspace: [device] bsa_route_workspace(BH, J) bytes (16-byte aligned) for
  * E, or NULL.  With it, E is written by a register-tiled contraction and
- * read back by the select (two launches); without it, one fused kernel
+ * read back by the select (two launches) and left there: E[h][i][j] at
+ * workspace + ((h*J + i)*J + j) floats, for bsa_coarse_attention; without
+ * it, one fused kernel
  * keeps the E rows of 8 to 32 query rows in shared memory, so even at 8 rows
  * (8*J + 128*(Dp+4) + 8*Dp) * 4 bytes must fit in 227 KB (Dp = D rounded up
  * to 4; J <= 5024 at D = 128), else BSA_ERR_UNSUPPORTED. */
@@ -304,6 +306,33 @@ bsa_status bsa_reweight_summaries(const void* q, const float* qbar, const void* 
                                   float scale, void* kt_lp, void* vt_lp, float* bias,
                                   float* anchor, void* workspace, size_t workspace_bytes,
                                   void* stream);
+
+/* ------------------------------------------------------------------ a10 ---
+ * Coarse branch.  [VSA] §6.7: every routed query block i attends at block
+ * granularity to every routed key block j with the routing scores as
+ * logits, C_i = sum_j softmax_j(E_ij) vbar_j, and the result is broadcast to
+ * the block's tokens through a gate, O_t += g_t * C_block(t).
+ *
+ * bsa_coarse_attention: E [device] float, head h at E + h*e_head_stride, row
+ * i at + i*Jr (the [BH, Jr, Jr] scaled scores that bsa_route_topk leaves in
+ * its workspace when given one); vbar [device] float, row j of head h at
+ * vbar + h*vbar_head_stride + j*D (the routed rows of bsa_pool_blocks' vbar);
+ * C [device] float [BH, Jr, D].  float32 throughout; 1 <= D <= 256.
+ *
+ * bsa_coarse_apply: out [device] [BH, N, D] of `dtype` (F32 or BF16), updated
+ * in place for every member token of the routed blocks (blocks
+ * prefix_blocks .. J-1; prefix rows are left as they are); C as written by
+ * bsa_coarse_attention; gate [device] float, [BH, D] (one gate per head and
+ * channel, gate_per_token = 0) or [BH, N, D] (gate_per_token = 1).  index_map,
+ * block_sizes as bsa_pool_blocks.  An index outside [0, N) raises
+ * BSA_ERR_INDEX and the row is skipped. */
+bsa_status bsa_coarse_attention(const float* E, int64_t e_head_stride, const float* vbar,
+                                int64_t vbar_head_stride, int BH, int Jr, int D, float* C,
+                                void* stream);
+bsa_status bsa_coarse_apply(void* out, bsa_dtype dtype, const float* C, const float* gate,
+                            int gate_per_token, int BH, int N, int D, const int32_t* index_map,
+                            const int32_t* block_sizes, int J, int M, int prefix_blocks,
+                            void* stream);
 
 /* Forces the CUDA-core attention kernels even where a tensor-core kernel
  * exists (1) or restores the default dispatch (0).  Host, process-wide. */

@@ -97,4 +97,10 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     assert rc == bsa.BSA_ERR_INVALID_ARG and "block counts" in bsa.bsa_last_error()  # no routed block
     rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 300, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()  # D > 256
+    rc = lib.bsa_coarse_attention(None, 16, 1, 8, 1, 4, 2, 1, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
+    rc = lib.bsa_coarse_attention(1, 15, 1, 8, 1, 4, 2, 1, None)  # head stride below Jr*Jr = 16
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "stride" in bsa.bsa_last_error()
+    rc = lib.bsa_coarse_apply(1, 1, 1, 1, 0, 1, 64, 300, 1, 1, 4, 16, 1, None)  # D > 256
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
     assert bsa.bsa_version() >= 100

@@ -56,7 +56,7 @@ def test_tile_map_bit_exact(lib, grid, block, M, n_prefix, permuted):
 
 def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, force_simt=False,
                     n_prefix=0, permuted=False, summary=False, cluster=False, pass_geometry=True, packed=None,
-                    reweight=False):
+                    reweight=False, gate=None):
     pl = _pipeline()
     T, H, W = grid
     if cluster:
@@ -70,8 +70,15 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
     geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
                        perm=torch.as_tensor(perm, device=DEV) if permuted else None)
     lib.bsa_set_force_simt(force_simt)
+    N = q.shape[1]
+    g = None
+    if gate == "channel":
+        g = synthetic.normal((B * h, D), seed + 71, "cpu")
+    elif gate == "token":
+        g = synthetic.normal((B * h, N, D), seed + 71, "cpu")
     res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, k, summary=summary,
-                                    pass_geometry=pass_geometry, packed=packed, reweight=reweight)
+                                    pass_geometry=pass_geometry, packed=packed, reweight=reweight,
+                                    coarse_gate=None if g is None else g.to(DEV))
     torch.cuda.synchronize()
     blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
     if res.packed is not None:
@@ -100,6 +107,12 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
             O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kbar[P:], vbar[P:], scale, prefix_blocks=P)
         else:
             O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, scale, prefix_blocks=P)
+        if g is not None:
+            vbar = oracle.pool_blocks(V, blocks)
+            C = oracle.coarse_attention(E, vbar[P:])
+            # C in float32 on the GPU: a few ulps of the largest |vbar| per entry
+            assert np.abs(res.coarse[bh].cpu().numpy() - C).max() <= 1e-5 * max(1.0, np.abs(vbar).max())
+            O = oracle.coarse_output(O, C, g[bh].double().numpy(), blocks, P)
         assert_close(f64(res.out[bh]), O, dtype, "out[bh=%d]" % bh)
         assert np.abs(res.lse[bh].cpu().numpy() - L).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
     return flagged
@@ -152,6 +165,20 @@ def test_summary_small_bf16(lib, force_simt, packed):
 def test_summary_fp32_ragged(lib):
     _run_block_case(lib, 1, 1, (5, 3, 4), (2, 2, 3), 12, 8, 2, torch.float32, 14, n_prefix=20,
                     summary=True)
+
+
+# ---------------------------------------------------------------- a10 coarse branch
+
+@pytest.mark.parametrize("gate", ["channel", "token"])
+def test_coarse_branch_video_bf16(lib, gate):
+    # (6,16,24) grid in (4,4,8) windows: 24 blocks with a 2-frame tail, k=6, D=128
+    _run_block_case(lib, 1, 2, (6, 16, 24), (4, 4, 8), 128, 128, 6, torch.bfloat16, 212, field=True, gate=gate)
+
+
+def test_coarse_branch_prefix_ragged_fp32(lib):
+    # 20 prefix tokens (4 prefix blocks of M=6) + a (5,9,16) grid in (1,2,3) windows, D=16: prefix rows
+    # untouched, ragged H-edge blocks, 150 routed blocks (E in five 32-wide stages, three 64-row CTAs)
+    _run_block_case(lib, 1, 2, (5, 9, 16), (1, 2, 3), 6, 16, 4, torch.float32, 31, n_prefix=20, gate="token")
 
 
 # ---------------------------------------------------------------- a9 Spark-Reweight summaries
