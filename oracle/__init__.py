@@ -30,10 +30,10 @@ float64 ``scaled_dot_product_attention`` on CPU) or brute force on tiny inputs.
 """
 
 from .tiling import (  # noqa: F401
-    num_blocks, token_index, tile_3d, tile_prefix, tile_permuted, index_map, budget,
+    num_blocks, token_index, tile_3d, tile_prefix, tile_permuted, index_map, budget, tile_segments,
 )
 from .pool import pool_blocks  # noqa: F401
-from .route import routing_scores, topk_row, route, near_tie_rows  # noqa: F401
+from .route import routing_scores, topk_row, route, route_grouped, near_tie_rows  # noqa: F401
 from .attention import (  # noqa: F401
     softmax_attention, dense_attention, block_sparse_attention, summary_attention,
     nsa_selected_attention, pair_counts,

@@ -55,3 +55,24 @@ def near_tie_rows(E, k, eps=1e-5):
     s = -np.sort(-E, axis=1)
     gap = s[:, k - 1] - s[:, k]
     return np.nonzero(gap < eps)[0]
+
+
+def route_grouped(E, spans, budgets, kmax):
+    """Region-grouped TopK (VSA page, §5.3, the R2V "exempt" rule): the key
+    blocks are cut into regions (spans [lo, hi) of E's columns, one per video
+    segment); every row keeps its own top budgets[r] blocks of each region,
+    min(budgets[r], hi - lo) of them, so one region's scores cannot take
+    another's quota.  The kept lists are joined in region order (ascending
+    overall) for one softmax over their union.  Returns q2k_idx [Jq, kmax]
+    (-1 padded) and q2k_num [Jq]."""
+    E = np.asarray(E, dtype=np.float64)
+    Jq = E.shape[0]
+    idx = np.full((Jq, kmax), -1, dtype=np.int32)
+    num = np.zeros(Jq, dtype=np.int32)
+    for i in range(Jq):
+        sel = []
+        for (lo, hi), k in zip(spans, budgets):
+            sel += [lo + j for j in topk_row(E[i, lo:hi], min(k, hi - lo))]
+        idx[i, :len(sel)] = sel
+        num[i] = len(sel)
+    return idx, num

@@ -7,7 +7,9 @@ Follows "VSA 实现详解：三维分块、均值路由与块稀疏 Attention":
     keeps its true length n_i.
   * §3 (pack): inside a block, members are laid out t-major, then y, then x.
   * §5.2 (dense prefix): dense segments are cut into contiguous 1-D blocks and
-    placed before the video blocks.
+    placed before the video blocks; with several segments, each dense segment
+    is chunked on its own, the chunks go first in order of appearance, and the
+    video segments follow in order, each with its own span of blocks.
   * §2.2 (the keep budget R_r = max(1, min(ceil((1-s_r) J_r), J_r))).
 and "深度解读|Spark-H3：从注意力几何到稀疏内核代码" §04 (a permutation replaces the
 fixed space-time grouping; Q and K/V share it, output is restored by the inverse).
@@ -86,3 +88,29 @@ def budget(J, sparsity):
     """
     s = Fraction(repr(float(sparsity)))
     return max(1, min(math.ceil((1 - s) * J), J))
+
+
+def tile_segments(segments, bT, bH, bW, M):
+    """Tiled layout of an ordered segment list (VSA page, §5.2, the metadata
+    builder): an int entry is a dense segment of that many tokens, a (T, H, W)
+    tuple a video grid.  Token ids count along the original order.  Returns
+    (blocks, prefix_blocks, spans): every dense segment cut into its own 1-D
+    chunks of M (last chunk short), all of them first in order of appearance;
+    then each video segment's 3-D blocks in order, spans[v] = [lo, hi) its
+    block range."""
+    starts, pos = [], 0
+    for seg in segments:
+        starts.append(pos)
+        pos += seg if isinstance(seg, int) else seg[0] * seg[1] * seg[2]
+    blocks = []
+    for seg, st in zip(segments, starts):
+        if isinstance(seg, int):
+            blocks += [st + b for b in tile_prefix(seg, M)]
+    prefix_blocks = len(blocks)
+    spans = []
+    for seg, st in zip(segments, starts):
+        if not isinstance(seg, int):
+            lo = len(blocks)
+            blocks += tile_3d(seg[0], seg[1], seg[2], bT, bH, bW, offset=st)
+            spans.append((lo, len(blocks)))
+    return blocks, prefix_blocks, spans

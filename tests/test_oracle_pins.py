@@ -594,3 +594,70 @@ def test_coarse_output_gate_and_prefix():
     gc = rng.normal(size=D)
     assert np.array_equal(oracle.coarse_output(O, C, gc, blocks, P),
                           oracle.coarse_output(O, C, np.tile(gc, (N, 1)), blocks, P))
+
+
+# ---------------------------------------------------------------- multi-segment layout and grouped TopK (VSA §5.2, §5.3)
+
+def test_segment_layout_page_example():
+    g = golden("vsa_r2v_layout.json")
+    pg, ours = g["page_layout"], g["our_segments"]
+    segs = [s if isinstance(s, int) else tuple(s) for s in ours["segments"]]
+    blocks, P, spans = oracle.tile_segments(segs, *ours["block"], pg["block_capacity"])
+    assert P == pg["num_prefix_tiles"] and len(blocks) == pg["num_blocks"]
+    assert [list(s) for s in spans] == pg["video_tile_spans"]
+    sizes = [len(b) for b in blocks]
+    assert sizes[:P] == pg["variable_block_sizes_prefix"] and set(sizes[P:]) == {pg["video_block_size"]}
+    assert sum(sizes) == pg["valid_length"] and len(blocks) * pg["block_capacity"] == pg["tiled_length"]
+    # every token once; dense chunks keep their original token ids in order
+    assert np.array_equal(np.sort(np.concatenate(blocks)), np.arange(pg["valid_length"]))
+    assert list(blocks[1]) == [128, 129]                      # the text's short chunk
+    assert list(blocks[2]) == list(range(130 + 512, 130 + 512 + 60))  # the image comes after the ref video
+    assert list(blocks[3]) == list(range(702, 830))           # audio
+    assert blocks[P][0] == 130 and blocks[spans[1][0]][0] == 902  # the videos start where they stand
+
+
+def test_route_grouped_page_counts():
+    g = golden("vsa_r2v_layout.json")
+    fig = g["r2v_figure"]
+    rng = np.random.default_rng(3)
+    sizes = fig["region_blocks"]
+    spans = [(sum(sizes[:r]), sum(sizes[:r + 1])) for r in range(len(sizes))]
+    E = rng.normal(size=(sum(sizes), sum(sizes)))
+    idx, num = oracle.route_grouped(E, spans, fig["budgets"], sum(fig["budgets"]))
+    assert np.all(num + fig["context_blocks"] == fig["kept_per_video_row"])
+    le = g["length_example"]
+    budgets = [oracle.budget(n, le["sparsity"]) for n in le["region_blocks"]]
+    assert le["context_blocks"] + sum(budgets) == le["kept_per_video_row"]
+    assert le["context_blocks"] + sum(le["region_blocks"]) == le["kept_per_context_row"]
+
+
+def test_route_grouped_quotas_are_independent():
+    # the output region scores higher everywhere; the reference regions keep their quota anyway
+    rng = np.random.default_rng(4)
+    spans, budgets = [(0, 3), (3, 6), (6, 10)], [1, 1, 2]
+    E = rng.normal(size=(10, 10))
+    E[:, 6:] += 100.0
+    idx, num = oracle.route_grouped(E, spans, budgets, 4)
+    for i in range(10):
+        sel = idx[i, :num[i]]
+        assert list(sel) == sorted(sel) and num[i] == 4
+        assert sum(0 <= j < 3 for j in sel) == 1 and sum(3 <= j < 6 for j in sel) == 1
+        assert sum(j >= 6 for j in sel) == 2
+    # a plain TopK of 4 would have taken only output blocks
+    plain, _ = oracle.route(E, 4, 4)
+    assert np.all(plain >= 6)
+
+
+def test_route_grouped_brute_force_per_region():
+    rng = np.random.default_rng(8)
+    spans, budgets = [(0, 4), (4, 5), (5, 11)], [2, 3, 3]  # the middle region is smaller than its budget
+    E = rng.normal(size=(6, 11))
+    idx, num = oracle.route_grouped(E, spans, budgets, 8)
+    for i in range(6):
+        sel = list(idx[i, :num[i]])
+        want = []
+        for (lo, hi), k in zip(spans, budgets):
+            kk = min(k, hi - lo)
+            best = max(itertools.combinations(range(lo, hi), kk), key=lambda c: sum(E[i, list(c)]))
+            want += sorted(best)
+        assert sel == want and num[i] == 6 and np.all(idx[i, 6:] == -1)
