@@ -19,6 +19,9 @@ Other workloads (--workload):
                  unselected blocks
   spark_reweight the same with Spark-Reweight summaries (weighted key and
                  value at the head's mean video query, log-mass bias)
+  r2v_bsa        bf16, h=24, R2V layout: 1024 text tokens, two reference
+                 videos (8,48,80) and the target (30,48,80) in (4,4,8) windows;
+                 region-grouped TopK keeping 10% of each video region
   video_dit_coarse  the default workload plus the gated coarse branch
                  softmax(E) V_bar broadcast to each block's tokens (synthetic
                  per-head, per-channel gate)
@@ -55,6 +58,8 @@ WORKLOADS = {
                        dtype="f32"),
     "spark_summary": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
                           seed=505, dtype="bf16", n_text=1024, summary=True),
+    "r2v_bsa": dict(kind="block", B=1, heads=24, D=128, segments=[1024, (8, 48, 80), (8, 48, 80), (30, 48, 80)],
+                    block=(4, 4, 8), M=128, budgets=[24, 24, 96], k=144, seed=707, dtype="bf16"),
     "video_dit_coarse": dict(kind="block", B=1, heads=24, D=128, grid=(30, 48, 80), block=(4, 4, 8), M=128, k=96,
                              seed=202, dtype="bf16", coarse=True),
     "spark_reweight": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
@@ -68,6 +73,9 @@ DEFAULT = "video_dit_bsa"
 def metric_flops(w):
     if w["kind"] == "token":
         return 4.0 * w["B"] * w["HQ"] * w["T"] * w["D"] * w["S"] * w["BS"]
+    if "segments" in w:  # every video query token, the blocks kept per row
+        nv = sum(s[0] * s[1] * s[2] for s in w["segments"] if not isinstance(s, int))
+        return 4.0 * w["B"] * w["heads"] * nv * w["D"] * w["k"] * w["M"]
     T, H, W = w["grid"]
     return 4.0 * w["B"] * w["heads"] * T * H * W * w["D"] * w["k"] * w["M"]
 
@@ -148,12 +156,19 @@ import oracle
 from block_sparse_attention_tile_gb300 import synthetic
 w = json.loads({w!r})
 budget_s = {budget}
-T, H, W = w["grid"]; bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
+bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
+segs = [s if isinstance(s, int) else tuple(s) for s in w["segments"]] if "segments" in w else None
+if segs is None:
+    T, H, W = w["grid"]
 n_text = w.get("n_text", 0); summary = w.get("summary", False); reweight = w.get("reweight", False)
 coarse = w.get("coarse", False)
 dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
 t0 = time.perf_counter()
-if summary:
+spans = None
+if segs is not None:
+    q, kk, v = synthetic.segment_qkv(1, segs, D, w["seed"], dt)
+    blocks, P_seg, spans = oracle.tile_segments(segs, bT, bH, bW, M)
+elif summary:
     q, kk, v = synthetic.cluster_qkv(1, n_text, T * H * W, D, w["seed"], dt)
     perm = synthetic.permutation(T * H * W, w["seed"] + 1)
     blocks = oracle.tile_prefix(n_text, M) + oracle.tile_permuted(perm, M, offset=n_text)
@@ -163,11 +178,16 @@ else:
 Q, K, V = (x[0].float().numpy().astype(np.float64) for x in (q, kk, v))
 gen_s = time.perf_counter() - t0
 P = len(oracle.tile_prefix(n_text, M)) if n_text else 0
+if segs is not None:
+    P = P_seg
 t0 = time.perf_counter()
 qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
 vbar = oracle.pool_blocks(V, blocks) if (summary or coarse) else None
 E = oracle.routing_scores(qbar[P:], kbar[P:], D)
-idx, num = oracle.route(E, k, k)
+if spans is not None:
+    idx, num = oracle.route_grouped(E, [(lo - P, hi - P) for lo, hi in spans], w["budgets"], k)
+else:
+    idx, num = oracle.route(E, k, k)
 sbias = None
 if reweight:
     kbar, vbar, sbias, _ = oracle.reweight_summaries(Q, K, V, blocks, D ** -0.5, prefix_blocks=P,
@@ -187,7 +207,7 @@ while done < len(order) and (done < 2 or time.perf_counter() - t0 < budget_s):
         oracle.summary_attention(Q, K, V, blocks, idx, num, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
                                  query_blocks=qb, block_bias=sbias)
     else:
-        O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb)
+        O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb, prefix_blocks=P)
         if C is not None and qb[0] >= P:
             oracle.coarse_output(O, C[qb[0] - P:qb[0] - P + 1], g, [blocks[qb[0]]], 0)
     done += 1
@@ -321,7 +341,9 @@ class BlockWorkload:
         from block_sparse_attention_tile_gb300 import pipeline, synthetic
         self.name, self.w, self.dev = name, w, dev
         self.torch = torch
-        T, H, W = w["grid"]
+        self.segments = [s if isinstance(s, int) else tuple(s) for s in w["segments"]] if "segments" in w else None
+        if self.segments is None:
+            T, H, W = w["grid"]
         self.summary = w.get("summary", False)
         self.reweight = self.summary and w.get("reweight", False)
         self.coarse = w.get("coarse", False)
@@ -335,7 +357,11 @@ class BlockWorkload:
         self.dtype = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
         seed = rank_seed(w["seed"], rank)
         with torch.no_grad():
-            if self.summary:
+            if self.segments is not None:
+                self.q, self.k, self.v = synthetic.segment_qkv(self.BH, self.segments, D, seed, self.dtype,
+                                                               device=dev)
+                self.perm = None
+            elif self.summary:
                 self.q, self.k, self.v = synthetic.cluster_qkv(self.BH, n_text, T * H * W, D, seed, self.dtype,
                                                                device=dev)
                 self.perm = torch.as_tensor(synthetic.permutation(T * H * W, seed + 1), device=dev)
@@ -343,11 +369,16 @@ class BlockWorkload:
                 self.q, self.k, self.v = synthetic.video_qkv(w["B"], w["heads"], T, H, W, D, seed, self.dtype,
                                                              device=dev, field=(w["dtype"] == "bf16"))
                 self.perm = None
-        self.geom = pipeline.Geometry(T, H, W, *w["block"], M=M, n_prefix=n_text, perm=self.perm)
+        if self.segments is not None:
+            self.geom = pipeline.SegmentGeometry(self.segments, *w["block"], M=M)
+        else:
+            self.geom = pipeline.Geometry(T, H, W, *w["block"], M=M, n_prefix=n_text, perm=self.perm)
         self.N = self.geom.n_tokens
         self.J = self.geom.num_blocks
         self.P = self.geom.prefix_blocks
         self.Jr = self.J - self.P
+        if self.segments is not None:
+            self.region_starts = [lo - self.P for lo, _ in self.geom.spans] + [self.Jr]
         self.scale = D ** -0.5
         BH, J = self.BH, self.J
         self.im = torch.empty((J, M), dtype=torch.int32, device=dev)
@@ -357,9 +388,10 @@ class BlockWorkload:
         self.vbar = torch.empty_like(self.qbar) if (self.summary or self.coarse) else None
         self.kbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
         self.vbar_lp = torch.empty((BH, J, D), dtype=self.dtype, device=dev) if self.summary else None
-        # permuted blocks: the pool pass also writes Q/K/V in block order for the attention
+        # permuted blocks or a multi-segment layout: the pool pass also writes Q/K/V in block order for
+        # the attention
         self.packed = (torch.empty((3, BH, J, M, D), dtype=self.dtype, device=dev)
-                       if self.perm is not None else None)
+                       if (self.perm is not None or self.segments is not None) else None)
         if self.packed is not None and self.vbar is None:
             self.vbar = torch.empty_like(self.qbar)
         from block_sparse_attention_tile_gb300 import bsa as _bsa
@@ -377,6 +409,25 @@ class BlockWorkload:
         # [coarse: attention, apply]
         self.launches_per_step = 5 + (3 if self.reweight else 0) + (2 if self.coarse else 0)
 
+    def tile_map(self):
+        from block_sparse_attention_tile_gb300 import bsa
+        g, M = self.geom, self.w["M"]
+        if self.segments is not None:
+            bsa.bsa_tile_map_segments(self.segments, g.bT, g.bH, g.bW, M, self.im, self.bs)
+        else:
+            bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, M, self.im, self.bs)
+
+    def route(self, qbar, kbar, nh, q2k, q2n):
+        """TopK per row, or the region-grouped TopK of a multi-segment layout."""
+        from block_sparse_attention_tile_gb300 import bsa
+        D, kk = self.w["D"], self.w["k"]
+        if self.segments is not None:
+            bsa.bsa_route_topk_grouped(qbar, kbar, nh, self.Jr, D, self.J * D, self.region_starts,
+                                       self.w["budgets"], self.scale, kk, q2k, q2n, self.route_ws)
+        else:
+            bsa.bsa_route_topk(qbar, kbar, nh, self.Jr, D, self.J * D, kk, self.scale, kk, q2k, q2n,
+                               self.route_ws)
+
     def step(self, ev=None, q=None, k=None, v=None):
         from block_sparse_attention_tile_gb300 import bsa
         w, g = self.w, self.geom
@@ -386,14 +437,13 @@ class BlockWorkload:
         D, M, kk = w["D"], w["M"], w["k"]
         st = self.torch.cuda.current_stream()
         if ev: ev[0].record(st)
-        bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, M, self.im, self.bs)
+        self.tile_map()
         if ev: ev[1].record(st)
         bsa.bsa_pool_blocks(q, k, v if self.vbar is not None else None, self.BH, self.N, D, self.im, self.bs,
                             self.J, M, self.qbar, self.kbar, self.vbar, self.kbar_lp, self.vbar_lp,
                             packed=self.packed)
         if ev: ev[2].record(st)
-        bsa.bsa_route_topk(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.Jr, D, self.J * D, kk,
-                           self.scale, kk, self.q2k, self.q2n, self.route_ws)
+        self.route(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.q2k, self.q2n)
         if ev: ev[3].record(st)
         if self.reweight:
             bsa.bsa_reweight_summaries(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, self.scale,
@@ -435,8 +485,7 @@ class BlockWorkload:
                             self.vbar[sl] if self.vbar is not None else None,
                             self.kbar_lp[sl] if self.summary else None, self.vbar_lp[sl] if self.summary else None,
                             packed=packed_chunk)
-        bsa.bsa_route_topk(self.qbar[sl, self.P:], self.kbar[sl, self.P:], nh, self.Jr, D, self.J * D, kk,
-                           self.scale, kk, self.q2k[sl], self.q2n[sl], self.route_ws)
+        self.route(self.qbar[sl, self.P:], self.kbar[sl, self.P:], nh, self.q2k[sl], self.q2n[sl])
         sb = None
         if self.reweight:
             sb = self.sbias[sl]
@@ -486,7 +535,7 @@ class BlockWorkload:
                     e = torch.cuda.Event()
                     e.record(h2d_s)
                 ready.append(e)
-            bsa.bsa_tile_map(g.T, g.H, g.W, g.bT, g.bH, g.bW, g.n_prefix, self.perm, self.w["M"], self.im, self.bs)
+            self.tile_map()
             for (h0, h1), e in zip(chunks, ready):
                 comp.wait_event(e)
                 # a contiguous [3, h1 - h0, J, M, D] view for this chunk's packed copy
@@ -575,9 +624,14 @@ class BlockWorkload:
             rgbs = rb / (stage_ms["reweight"] * 1e-3) / 1e9
             secondary["reweight"] = {"bound": "hbm", "achieved": rgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                      "frac": rgbs / peaks["hbm_gbs"], "bytes_per_launch": rb}
-        T, H, W = self.w["grid"]
-        config = {"workload": self.name, "B": self.w["B"], "heads": self.w["heads"], "D": D, "seq_len": self.N,
-                  "grid": [T, H, W], "block": list(self.w["block"]), "M": self.w["M"], "J": J, "k": self.w["k"]}
+        config = {"workload": self.name, "B": self.w["B"], "heads": self.w["heads"], "D": D, "seq_len": self.N}
+        if self.segments is not None:
+            config.update({"segments": [s if isinstance(s, int) else list(s) for s in self.segments],
+                           "prefix_blocks": self.P, "video_spans": self.geom.spans, "budgets": self.w["budgets"],
+                           "routing": "region-grouped TopK (exempt prefix)"})
+        else:
+            config["grid"] = list(self.w["grid"])
+        config.update({"block": list(self.w["block"]), "M": self.w["M"], "J": J, "k": self.w["k"]})
         if self.summary:
             config.update({"n_text": self.w["n_text"], "permuted": True, "summary": True})
             if self.reweight:
@@ -588,6 +642,8 @@ class BlockWorkload:
         config["l2"] = ("inputs larger than L2: Q,K,V = %.2f GB per step" % (nbytes / 1e9) if nbytes > 129e6 else
                         "inputs smaller than L2 (%.1f MB): L2 not flushed, launch-bound tiny case" % (nbytes / 1e6))
         data = ("synthetic (seeded N(0,1) + per-head low-rank clusters; no dataset or weights)" if self.summary else
+                "synthetic (seeded N(0,1) + a smooth space-time field per video segment on Q/K; no dataset or "
+                "weights)" if self.segments is not None else
                 "synthetic (seeded N(0,1)%s; no dataset or weights)"
                 % (" + smooth space-time field on Q/K" if self.w["dtype"] == "bf16" else ""))
         return roof, secondary, config, data, self.w["dtype"]

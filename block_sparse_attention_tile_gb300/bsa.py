@@ -59,6 +59,9 @@ _SIGS = {
     "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, P, F, P, P, P]),
     "bsa_reweight_workspace": (SZ, [I, I]),
     "bsa_reweight_summaries": (I, [P, P, P, P, I, I, I, I, P, P, I, I, I, F, P, P, P, P, P, SZ, P]),
+    "bsa_segments_count": (I, [I, P, P, I, I, I, I, P, P]),
+    "bsa_tile_map_segments": (I, [I, P, P, I, I, I, I, P, P, P]),
+    "bsa_route_topk_grouped": (I, [P, P, I, I, I, I64, I, P, P, F, I, P, P, P, SZ, P]),
     "bsa_coarse_attention": (I, [P, I64, P, I64, I, I, I, P, P]),
     "bsa_coarse_apply": (I, [P, I, P, P, I, I, I, I, P, P, I, I, I, P]),
     "bsa_set_force_simt": (None, [I]),
@@ -236,3 +239,46 @@ def bsa_coarse_apply(out, C, gate, gate_per_token, BH, N, D, index_map, block_si
                      stream=None):
     _check(_lib.bsa_coarse_apply(_ptr(out), _dtype(out), _ptr(C), _ptr(gate), 1 if gate_per_token else 0, BH, N, D,
                                  _ptr(index_map), _ptr(block_sizes), J, M, prefix_blocks, _stream(stream)))
+
+
+def _seg_arrays(segments):
+    """kinds / dims host arrays for an ordered segment list: an int is a dense
+    segment of that many tokens, a (T, H, W) tuple a video grid."""
+    n = len(segments)
+    kinds = (ctypes.c_int32 * n)()
+    dims = (ctypes.c_int32 * (3 * n))()
+    for s, seg in enumerate(segments):
+        if isinstance(seg, int):
+            kinds[s], dims[3 * s] = 0, seg
+        else:
+            kinds[s] = 1
+            dims[3 * s], dims[3 * s + 1], dims[3 * s + 2] = seg
+    return n, kinds, dims
+
+
+def bsa_segments_count(segments, bT, bH, bW, M):
+    """(J, prefix_blocks, spans) of the tiled layout of an ordered segment list."""
+    n, kinds, dims = _seg_arrays(segments)
+    nv = sum(1 for seg in segments if not isinstance(seg, int))
+    P = ctypes.c_int32(0)
+    spans = (ctypes.c_int32 * max(1, 2 * nv))()
+    J = _lib.bsa_segments_count(n, kinds, dims, bT, bH, bW, M, ctypes.byref(P), spans)
+    if J < 0:
+        raise BsaError(BSA_ERR_INVALID_ARG, "bsa_segments_count: invalid segments")
+    return J, P.value, [(spans[2 * v], spans[2 * v + 1]) for v in range(nv)]
+
+
+def bsa_tile_map_segments(segments, bT, bH, bW, M, index_map, block_sizes, stream=None):
+    n, kinds, dims = _seg_arrays(segments)
+    _check(_lib.bsa_tile_map_segments(n, kinds, dims, bT, bH, bW, M, _ptr(index_map), _ptr(block_sizes),
+                                      _stream(stream)))
+
+
+def bsa_route_topk_grouped(qbar, kbar, BH, J, D, head_stride, region_starts, budgets, scale, kmax, q2k_idx,
+                           q2k_num, workspace, stream=None):
+    nreg = len(budgets)
+    starts = (ctypes.c_int32 * (nreg + 1))(*region_starts)
+    ks = (ctypes.c_int32 * nreg)(*budgets)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.bsa_route_topk_grouped(_ptr(qbar), _ptr(kbar), BH, J, D, head_stride, nreg, starts, ks, scale, kmax,
+                                       _ptr(q2k_idx), _ptr(q2k_num), _ptr(workspace), nbytes, _stream(stream)))

@@ -58,7 +58,7 @@ constexpr int kHD = 128;          // head dim
 constexpr int kThreads = 384;
 constexpr int kKStages = 3, kVStages = 2;      // K ring and V ring (32 KB stages)
 constexpr int kStages = kKStages + kVStages;
-constexpr int kMaxList = 512;     // key tiles per query block, virtual tiles included
+constexpr int kMaxList = 512;     // stored key tiles of a routed query block, virtual tiles included
 constexpr int kMaxVirtual = 8;    // summary tiles (<= 1024 routed blocks)
 constexpr uint32_t kTileBytes = kBN * kHD * 2;       // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 16 KB: 128 rows x 64 cols
@@ -226,9 +226,13 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         n = P + nsel + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
     }
     __syncthreads();
-    for (int s = threadIdx.x; s < n; s += blockDim.x) {
+    // the key-tile table of a routed row (a dense row's tile s is block s: its
+    // entries are computed where they are used, so its length is not bounded
+    // by the table)
+    const int ntab = dense_row ? 0 : n;
+    for (int s = threadIdx.x; s < ntab; s += blockDim.x) {
         int blk, nv;
-        if (dense_row || s < P) {
+        if (s < P) {
             blk = s;
             nv = prm.block_sizes[blk];
         } else if (s < P + nsel) {
@@ -253,7 +257,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncthreads();
     {
         int4* srcs = reinterpret_cast<int4*>(sm + OFF_SRC);
-        for (int s = threadIdx.x; s < n; s += blockDim.x) {
+        for (int s = threadIdx.x; s < ntab; s += blockDim.x) {
             const int blk = list[s];
             srcs[s] = pack_src(tile_source(blk, prm, bh), blk < 0);
         }
@@ -342,8 +346,13 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         int rows_next[4] = {0, 0, 0, 0};
         int4 src_next = make_int4(0, 0, 0, 0);
         auto prepare = [&](int jt) {
-            src_next = srcs[jt];
-            if ((src_next.x & 3) == 0) gather_rows(list[jt], nvalid[jt], rows_next);
+            if (dense_row) {
+                src_next = pack_src(tile_source(jt, prm, bh), false);
+                if ((src_next.x & 3) == 0) gather_rows(jt, prm.block_sizes[jt], rows_next);
+            } else {
+                src_next = srcs[jt];
+                if ((src_next.x & 3) == 0) gather_rows(list[jt], nvalid[jt], rows_next);
+            }
         };
         if (n > 0) prepare(0);
         for (int jt = 0; jt < n; ++jt) {
@@ -478,8 +487,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 ptx::tmem_ld32(tS + 96, xr + 96);
                 ptx::tmem_wait_ld();
             }
-            const int blk = list[s];
-            const int nv = nvalid[s];
+            const int blk = dense_row ? s : list[s];
+            const int nv = dense_row ? prm.block_sizes[s] : nvalid[s];
             float mxp[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
@@ -713,7 +722,8 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     const bool summary = kb != nullptr;
     const int Jr = J - P;
     const int nvirt = summary ? (Jr + tc::kBN - 1) / tc::kBN : 0;
-    const long long longest = P > 0 ? std::max<long long>(J, (long long)P + kmax + nvirt) : (long long)kmax + nvirt;
+    // the stored key-tile list of a routed row (dense prefix rows need none)
+    const long long longest = (long long)P + kmax + nvirt;
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;

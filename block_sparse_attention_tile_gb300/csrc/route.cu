@@ -9,6 +9,8 @@
 // definition.  The TopK is an exact radix select on order-preserving 32-bit
 // keys: one warp per row finds the k-th largest key bit by bit (32 counting
 // passes), then writes the selected ids in ascending order with ballots.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace bsa {
@@ -30,9 +32,11 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 // TopK of one row of E (J scores, in shared or global memory) by one warp:
 // exact radix select on order-preserving keys, ties to the lower index, the
-// selected ids written ascending and -1 padded to kmax, and the count.
+// selected ids (plus `first`, the row segment's offset) written ascending and
+// -1 padded to kmax, and the count (when num_out is not null).
 __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, int k, int kmax, int lane,
-                                           int32_t* __restrict__ out, int32_t* __restrict__ num_out) {
+                                           int32_t* __restrict__ out, int32_t* __restrict__ num_out,
+                                           int first = 0) {
     if (J <= 1024) {
         // the row's keys stay in registers: lane holds columns lane + 32*i
         uint32_t key[32];
@@ -64,7 +68,7 @@ __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, i
             const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
             const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
             const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[written + __popc(sel_mask & lt)] = c;
+            if (sel) out[written + __popc(sel_mask & lt)] = first + c;
             written += __popc(sel_mask);
             eq_seen += __popc(eq_mask);
         }
@@ -92,13 +96,13 @@ __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, i
             const int eq_rank = eq_seen + __popc(eq_mask & ((1u << lane) - 1u));
             const bool sel = c < J && (key > prefix || (eq && eq_rank < need_eq));
             const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = c;
+            if (sel) out[written + __popc(sel_mask & ((1u << lane) - 1u))] = first + c;
             written += __popc(sel_mask);
             eq_seen += __popc(eq_mask);
         }
     }
     for (int s = k + lane; s < kmax; s += 32) out[s] = -1;
-    if (lane == 0) *num_out = k;
+    if (lane == 0 && num_out) *num_out = k;
 }
 
 // DPC: the padded head dimension when it is known at compile time (0 = any).
@@ -324,6 +328,36 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
                q2k_idx + ((long long)bh * J + row) * kmax, q2k_num + (long long)bh * J + row);
 }
 
+// Region-grouped TopK ("VSA 实现详解" §5.3, the R2V exempt rule): the key
+// blocks are cut into regions [lo_r, lo_{r+1}); every row keeps its own top
+// min(k_r, size_r) blocks of each region (one region cannot take another's
+// quota), joined in region order, so the list stays ascending.  Warp per row.
+constexpr int kMaxRegions = 32;
+struct Regions {
+    int n;
+    int lo[kMaxRegions + 1];
+    int k[kMaxRegions];
+};
+
+__global__ void __launch_bounds__(256) route_select_grouped_kernel(const float* __restrict__ E, int J, Regions rg,
+                                                                   int kmax, int32_t* __restrict__ q2k_idx,
+                                                                   int32_t* __restrict__ q2k_num) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), bh = blockIdx.y, lane = threadIdx.x & 31;
+    if (row >= J) return;
+    const float* e = E + ((long long)bh * J + row) * J;
+    int32_t* out = q2k_idx + ((long long)bh * J + row) * kmax;
+    int written = 0;
+    for (int r = 0; r < rg.n; ++r) {
+        const int lo = rg.lo[r], size = rg.lo[r + 1] - lo;
+        const int kk = min(rg.k[r], size);
+        if (kk <= 0) continue;
+        select_row(e + lo, size, kk, kk, lane, out + written, nullptr, lo);
+        written += kk;
+    }
+    for (int s = written + lane; s < kmax; s += 32) out[s] = -1;
+    if (lane == 0) q2k_num[(long long)bh * J + row] = written;
+}
+
 }  // namespace bsa
 
 using namespace bsa;
@@ -384,4 +418,41 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     kern<<<grid, kRouteThreads, smem, as_stream(stream)>>>(qbar, kbar, J, D, Dp, (long long)head_stride, k, scale,
                                                           kmax, q2k_idx, q2k_num);
     return check_launch("route_topk_kernel");
+}
+
+extern "C" bsa_status bsa_route_topk_grouped(const float* qbar, const float* kbar, int BH, int J, int D,
+                                             int64_t head_stride, int nreg, const int32_t* region_starts,
+                                             const int32_t* budgets, float scale, int kmax, int32_t* q2k_idx,
+                                             int32_t* q2k_num, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+    BSA_REQUIRE(qbar && kbar && q2k_idx && q2k_num && region_starts && budgets && workspace,
+                "route_grouped: null pointer");
+    BSA_REQUIRE(BH > 0 && BH <= 65535 && J > 0 && J <= 8192 && D > 0 && D <= 256,
+                "route_grouped: sizes out of range (BH=%d J=%d D=%d)", BH, J, D);
+    BSA_REQUIRE(nreg >= 1 && nreg <= kMaxRegions, "route_grouped: 1 <= nreg <= %d", kMaxRegions);
+    BSA_REQUIRE(region_starts[0] == 0 && region_starts[nreg] == J, "route_grouped: regions must cover [0, J)");
+    Regions rg;
+    rg.n = nreg;
+    long long total = 0;
+    for (int r = 0; r < nreg; ++r) {
+        BSA_REQUIRE(region_starts[r + 1] > region_starts[r], "route_grouped: empty or unordered region %d", r);
+        BSA_REQUIRE(budgets[r] >= 0, "route_grouped: negative budget");
+        rg.lo[r] = region_starts[r];
+        rg.k[r] = budgets[r];
+        total += std::min(budgets[r], region_starts[r + 1] - region_starts[r]);
+    }
+    rg.lo[nreg] = J;
+    BSA_REQUIRE(total >= 1 && kmax >= total, "route_grouped: kmax %d below the %lld kept blocks", kmax, total);
+    BSA_REQUIRE(head_stride >= (int64_t)J * D, "route_grouped: head_stride smaller than J*D");
+    BSA_REQUIRE(workspace_bytes >= bsa_route_workspace(BH, J), "route_grouped: workspace smaller than %zu bytes",
+                bsa_route_workspace(BH, J));
+    BSA_REQUIRE(((uintptr_t)workspace & 15) == 0, "route_grouped: workspace not 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    float* E = static_cast<float*>(workspace);
+    const dim3 g1((J + kGB - 1) / kGB, (J + kGB - 1) / kGB, BH);
+    route_gemm_kernel<<<g1, 256, 0, st>>>(qbar, kbar, J, D, (long long)head_stride, scale, E);
+    bsa_status rc = check_launch("route_gemm_kernel");
+    if (rc != BSA_OK) return rc;
+    route_select_grouped_kernel<<<dim3((J + 7) / 8, BH), 256, 0, st>>>(E, J, rg, kmax, q2k_idx, q2k_num);
+    return check_launch("route_select_grouped_kernel");
 }

@@ -47,6 +47,106 @@ __global__ void tile_map_kernel(int T, int H, int W, int bT, int bH, int bW, int
     if (m == 0) block_sizes[j] = n;
 }
 
+// Tiled layout of an ordered list of segments (VSA page §5.2, the metadata
+// builder): every dense segment is chunked on its own into 1-D blocks of M
+// (the last one short) and all chunks go first, in order of appearance; the
+// video segments follow in order, each tiled in 3-D windows.  The table lists
+// the tile segments in that tiled order.
+constexpr int kMaxSegs = 32;
+struct SegTable {
+    int n;                          // tile segments
+    int block_start[kMaxSegs + 1];  // first block of each, then J
+    int token_start[kMaxSegs];      // first token in the original order
+    int T[kMaxSegs], H[kMaxSegs], W[kMaxSegs];  // dense: T = token count, H = 0
+};
+
+__global__ void tile_map_segments_kernel(SegTable tab, int bT, int bH, int bW, int M, int J,
+                                         int32_t* __restrict__ index_map, int32_t* __restrict__ block_sizes) {
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)J * M) return;
+    const int j = (int)(gid / M);
+    const int m = (int)(gid % M);
+    int s = 0;
+    while (s + 1 < tab.n && tab.block_start[s + 1] <= j) ++s;
+    const int jl = j - tab.block_start[s];
+    int token = -1, n = 0;
+    if (tab.H[s] == 0) {
+        const int start = jl * M;
+        n = min(M, tab.T[s] - start);
+        if (m < n) token = tab.token_start[s] + start + m;
+    } else {
+        const int T = tab.T[s], H = tab.H[s], W = tab.W[s];
+        const int nH = (H + bH - 1) / bH, nW = (W + bW - 1) / bW;
+        const int jt = jl / (nH * nW), jh = (jl / nW) % nH, jw = jl % nW;
+        const int et = min(bT, T - jt * bT), eh = min(bH, H - jh * bH), ew = min(bW, W - jw * bW);
+        n = et * eh * ew;
+        if (m < n) {
+            const int dt = m / (eh * ew), dy = (m / ew) % eh, dx = m % ew;
+            token = tab.token_start[s] + ((jt * bT + dt) * H + (jh * bH + dy)) * W + (jw * bW + dx);
+        }
+    }
+    index_map[gid] = token;
+    if (m == 0) block_sizes[j] = n;
+}
+
+// Builds the table; returns J, or -1 on invalid input.  prefix_blocks and
+// spans ([n_video][2] block ranges) are optional outputs.
+static long long build_seg_table(int nseg, const int32_t* kinds, const int32_t* dims, int bT, int bH, int bW,
+                                 int M, SegTable* tab, int32_t* prefix_blocks, int32_t* spans) {
+    if (nseg < 1 || nseg > kMaxSegs || !kinds || !dims || M < 1) return -1;
+    long long tok = 0, blk = 0;
+    long long starts[kMaxSegs];
+    for (int s = 0; s < nseg; ++s) {
+        starts[s] = tok;
+        if (kinds[s] == 0) {
+            if (dims[3 * s] < 0) return -1;
+            tok += dims[3 * s];
+        } else if (kinds[s] == 1) {
+            if (dims[3 * s] < 1 || dims[3 * s + 1] < 1 || dims[3 * s + 2] < 1) return -1;
+            if (bT < 1 || bH < 1 || bW < 1 || (long long)bT * bH * bW > M) return -1;
+            tok += (long long)dims[3 * s] * dims[3 * s + 1] * dims[3 * s + 2];
+        } else {
+            return -1;
+        }
+    }
+    if (tok >= 0x7fffffffLL) return -1;
+    int t = 0, nv = 0;
+    for (int pass = 0; pass < 2; ++pass)
+        for (int s = 0; s < nseg; ++s) {
+            if ((kinds[s] == 1) != (pass == 1)) continue;
+            long long nb;
+            if (pass == 0) {
+                nb = ((long long)dims[3 * s] + M - 1) / M;
+            } else {
+                nb = (long long)((dims[3 * s] + bT - 1) / bT) * ((dims[3 * s + 1] + bH - 1) / bH) *
+                     ((dims[3 * s + 2] + bW - 1) / bW);
+                if (spans) {
+                    spans[2 * nv] = (int32_t)blk;
+                    spans[2 * nv + 1] = (int32_t)(blk + nb);
+                }
+                ++nv;
+            }
+            if (nb == 0) continue;  // an empty dense segment has no block
+            if (tab) {
+                tab->block_start[t] = (int)blk;
+                tab->token_start[t] = (int)starts[s];
+                tab->T[t] = dims[3 * s];
+                tab->H[t] = pass == 0 ? 0 : dims[3 * s + 1];
+                tab->W[t] = pass == 0 ? 0 : dims[3 * s + 2];
+            }
+            ++t;
+            blk += nb;
+            if (blk > 0x7fffffffLL) return -1;
+            if (pass == 0 && prefix_blocks) *prefix_blocks = (int32_t)blk;
+        }
+    if (tab) {
+        tab->n = t;
+        tab->block_start[t] = (int)blk;
+    }
+    if (prefix_blocks && nv == nseg) *prefix_blocks = 0;
+    return blk;
+}
+
 // Pool one (block, head, tensor): 256 threads = VL vector lanes x RG row groups.
 // Each thread sums its rows for VEC consecutive channels in float32; the RG
 // partial sums are added in a fixed tree order, then divided by n_j.
@@ -307,6 +407,28 @@ bsa_status bsa_tile_map(int T, int H, int W, int bT, int bH, int bW, int n_prefi
     tile_map_kernel<<<(unsigned)grid, threads, 0, as_stream(stream)>>>(
         T, H, W, bT, bH, bW, n_prefix, perm, M, prefix_blocks, J, index_map, block_sizes);
     return check_launch("tile_map_kernel");
+}
+
+int bsa_segments_count(int nseg, const int32_t* kinds, const int32_t* dims, int bT, int bH, int bW, int M,
+                       int32_t* prefix_blocks, int32_t* spans) {
+    if (prefix_blocks) *prefix_blocks = 0;
+    const long long J = build_seg_table(nseg, kinds, dims, bT, bH, bW, M, nullptr, prefix_blocks, spans);
+    return J < 0 ? -1 : (int)J;
+}
+
+bsa_status bsa_tile_map_segments(int nseg, const int32_t* kinds, const int32_t* dims, int bT, int bH, int bW,
+                                 int M, int32_t* index_map, int32_t* block_sizes, void* stream) {
+    BSA_REQUIRE(index_map && block_sizes, "tile_map_segments: null output");
+    SegTable tab;
+    int32_t P = 0;
+    const long long J = build_seg_table(nseg, kinds, dims, bT, bH, bW, M, &tab, &P, nullptr);
+    BSA_REQUIRE(J > 0, "tile_map_segments: invalid segments (nseg=%d, at most %d; dense sizes >= 0, video grids "
+                "and blocks >= 1, bT*bH*bW <= M)", nseg, kMaxSegs);
+    const long long total = J * M;
+    const int threads = 256;
+    tile_map_segments_kernel<<<(unsigned)((total + threads - 1) / threads), threads, 0, as_stream(stream)>>>(
+        tab, bT, bH, bW, M, (int)J, index_map, block_sizes);
+    return check_launch("tile_map_segments_kernel");
 }
 
 bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtype dtype, int BH,

@@ -49,12 +49,52 @@ class Geometry:
                                   self.perm is not None, self.M)
 
 
+@dataclass
+class SegmentGeometry:
+    """An ordered list of segments (an int: a dense segment of that many
+    tokens, e.g. text, image or audio; a (T, H, W) tuple: a video grid, e.g. a
+    reference video or the target video), token ids counting along that
+    order.  Dense segments are chunked first, the videos follow in order, each
+    in (bT, bH, bW) windows with its own block span (the routing regions)."""
+    segments: list
+    bT: int = 1
+    bH: int = 1
+    bW: int = 1
+    M: int = 128
+    perm = None
+    geometry = None  # no single video grid: the attention reads tiles by index
+
+    def __post_init__(self):
+        self.segments = [s if isinstance(s, int) else tuple(s) for s in self.segments]
+        self._J, self._P, self._spans = bsa.bsa_segments_count(self.segments, self.bT, self.bH, self.bW, self.M)
+
+    @property
+    def n_tokens(self):
+        return sum(s if isinstance(s, int) else s[0] * s[1] * s[2] for s in self.segments)
+
+    @property
+    def num_blocks(self):
+        return self._J
+
+    @property
+    def prefix_blocks(self):
+        return self._P
+
+    @property
+    def spans(self):
+        """Block range [lo, hi) of each video segment, in tiled order."""
+        return list(self._spans)
+
+
 def tile_map(geom, device="cuda"):
     J = geom.num_blocks
     index_map = torch.empty((J, geom.M), dtype=torch.int32, device=device)
     block_sizes = torch.empty((J,), dtype=torch.int32, device=device)
-    bsa.bsa_tile_map(geom.T, geom.H, geom.W, geom.bT, geom.bH, geom.bW, geom.n_prefix, geom.perm, geom.M,
-                     index_map, block_sizes)
+    if isinstance(geom, SegmentGeometry):
+        bsa.bsa_tile_map_segments(geom.segments, geom.bT, geom.bH, geom.bW, geom.M, index_map, block_sizes)
+    else:
+        bsa.bsa_tile_map(geom.T, geom.H, geom.W, geom.bT, geom.bH, geom.bW, geom.n_prefix, geom.perm, geom.M,
+                         index_map, block_sizes)
     return index_map, block_sizes
 
 
@@ -78,7 +118,9 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     """Tile map -> pool -> route -> block-sparse (or exact+summary) attention.
 
     q, k, v: [BH, N, D] (BHSD) float32 or bfloat16 on the device.  Routing
-    covers the video blocks; prefix blocks are always attended.  ``packed``:
+    covers the video blocks; prefix blocks are always attended.  With a
+    SegmentGeometry, ``topk`` may be a list with one budget per video segment:
+    the region-grouped TopK keeps that many blocks of each segment per row.  ``packed``:
     let the pool pass also write Q/K/V in block order for the attention to
     read (default: when the blocks come from a permutation, whose rows the
     tensor-core kernel would otherwise gather four at a time).  Returns the
@@ -96,9 +138,18 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     J = index_map.shape[0]
     P = geom.prefix_blocks
     Jr = J - P
-    kmax = topk if kmax is None else kmax
+    grouped = not isinstance(topk, int)
+    if grouped:
+        spans = geom.spans
+        assert len(topk) == len(spans), "one budget per video segment"
+        kept = sum(min(kr, hi - lo) for kr, (lo, hi) in zip(topk, spans))
+        kmax = kept if kmax is None else kmax
+    else:
+        kmax = topk if kmax is None else kmax
     if packed is None:
-        packed = geom.perm is not None and q.dtype == torch.bfloat16 and D == 128 and geom.M == 128
+        # tiles that are not one box of a single video grid: gather them once in the pool pass
+        packed = ((geom.perm is not None or isinstance(geom, SegmentGeometry)) and q.dtype == torch.bfloat16
+                  and D == 128 and geom.M == 128)
     pk = torch.empty((3, BH, J, geom.M, D), dtype=q.dtype, device=dev) if packed else None
     qbar = torch.empty((BH, J, D), dtype=torch.float32, device=dev)
     kbar = torch.empty_like(qbar)
@@ -111,7 +162,12 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     q2k_idx = torch.empty((BH, Jr, kmax), dtype=torch.int32, device=dev)
     q2k_num = torch.empty((BH, Jr), dtype=torch.int32, device=dev)
     ws = torch.empty((bsa.bsa_route_workspace(BH, Jr) // 4,), dtype=torch.float32, device=dev)
-    bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num, ws)
+    if grouped:
+        starts = [lo - P for lo, _ in geom.spans] + [Jr]
+        bsa.bsa_route_topk_grouped(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, starts, list(topk), scale, kmax,
+                                   q2k_idx, q2k_num, ws)
+    else:
+        bsa.bsa_route_topk(qbar[:, P:], kbar[:, P:], BH, Jr, D, J * D, topk, scale, kmax, q2k_idx, q2k_num, ws)
     sbias = None
     if summary and reweight:
         sbias = torch.empty((BH, J), dtype=torch.float32, device=dev)

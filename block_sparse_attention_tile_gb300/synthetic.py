@@ -81,6 +81,29 @@ def video_qkv(B, h, T, H, W, D, seed, dtype, device="cpu", field=False):
     return q.to(dtype), k.to(dtype), v.to(dtype)
 
 
+def segment_qkv(h, segments, D, seed, dtype, device="cpu", field=True):
+    """Q, K, V [h, N, D] for an ordered segment list (an int: a dense segment of
+    that many tokens; a (T, H, W) tuple: a video grid), tokens in that order:
+    N(0,1) everywhere, plus on each video segment's Q and K its own smooth
+    space-time field (seeded per segment) when ``field``."""
+    N = sum(s if isinstance(s, int) else s[0] * s[1] * s[2] for s in segments)
+    q = normal((h, N, D), seed, device)
+    k = normal((h, N, D), seed + 1, device)
+    v = normal((h, N, D), seed + 2, device)
+    pos = 0
+    for i, seg in enumerate(segments):
+        if isinstance(seg, int):
+            pos += seg
+            continue
+        T, H, W = seg
+        n = T * H * W
+        if field:
+            q[:, pos:pos + n] += lowfreq_field(h, D, T, H, W, seed + 10 + 7 * i, device)
+            k[:, pos:pos + n] += lowfreq_field(h, D, T, H, W, seed + 20 + 7 * i, device)
+        pos += n
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
 def causal_block_lists(B, T, H, S, BS, seed):
     """NSA-style selections [B, T, H, S] int32 (ascending, -1 padded) and counts
     [B, T, H]: the query's own block always, the rest uniform without

@@ -89,6 +89,25 @@ bsa_status bsa_tile_map(int T, int H, int W, int bT, int bH, int bW, int n_prefi
                         const int32_t* perm, int M, int32_t* index_map, int32_t* block_sizes,
                         void* stream);
 
+/* Multi-segment layout.  [VSA] §5.2 (the metadata builder): an ordered list
+ * of nseg <= 32 segments, kinds[s] = 0 for a dense segment of dims[3s]
+ * tokens (text, image, audio) or 1 for a video grid (T, H, W) =
+ * dims[3s .. 3s+2]; token ids count along this original order.  Every dense
+ * segment is chunked on its own into 1-D blocks of M (the last one short) and
+ * all chunks come first, in order of appearance (the prefix); the video
+ * segments follow in order, each tiled in (bT, bH, bW) windows as
+ * bsa_tile_map ([VSA] §5.3: every video segment keeps its own block range).
+ * kinds, dims, prefix_blocks, spans: host.  bsa_segments_count returns J
+ * (-1 on invalid input) and, when the pointers are not NULL, the number of
+ * prefix blocks and spans [n_video][2] = each video segment's half-open
+ * block range.  bsa_tile_map_segments writes index_map [J, M] and
+ * block_sizes [J] [device] as bsa_tile_map. */
+int bsa_segments_count(int nseg, const int32_t* kinds, const int32_t* dims, int bT, int bH, int bW,
+                       int M, int32_t* prefix_blocks, int32_t* spans);
+bsa_status bsa_tile_map_segments(int nseg, const int32_t* kinds, const int32_t* dims, int bT, int bH,
+                                 int bW, int M, int32_t* index_map, int32_t* block_sizes,
+                                 void* stream);
+
 /* Keep budget R = max(1, min(ceil((1-s)*J), J)) ([VSA] §2.2), with
  * (1-s)*J computed in double and 1e-9 subtracted before the ceiling so that a
  * decimal sparsity such as 0.9 gives ceil(96) and not ceil(96.00000000000001).
@@ -138,6 +157,23 @@ bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, i
                           int64_t head_stride, int k, float scale, int kmax,
                           int32_t* q2k_idx, int32_t* q2k_num, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* Region-grouped routing.  [VSA] §5.3 (R2V, the "exempt" rule): the key
+ * blocks [0, J) are cut into nreg <= 32 regions [region_starts[r],
+ * region_starts[r+1]) (one per video segment: the spans of
+ * bsa_segments_count minus the prefix blocks); every query row keeps its own
+ * top min(budgets[r], size_r) blocks of each region, so a region cannot take
+ * another's quota, and the lists are joined in region order (ascending).
+ * q2k_num = the sum of those counts; kmax must be at least that.  E is
+ * computed as in bsa_route_topk (same float32 values, same tie rule) into
+ * the workspace, which is required here and keeps E afterwards.
+ * region_starts (nreg + 1, starting at 0 and ending at J) and budgets
+ * (nreg): host. */
+bsa_status bsa_route_topk_grouped(const float* qbar, const float* kbar, int BH, int J, int D,
+                                  int64_t head_stride, int nreg, const int32_t* region_starts,
+                                  const int32_t* budgets, float scale, int kmax, int32_t* q2k_idx,
+                                  int32_t* q2k_num, void* workspace, size_t workspace_bytes,
+                                  void* stream);
 
 /* ------------------------------------------------------------------ a4 ----
  * Block-sparse attention, query-outer order.  [VSA] §6.3: for query block i,

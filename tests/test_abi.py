@@ -104,3 +104,24 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     rc = lib.bsa_coarse_apply(1, 1, 1, 1, 0, 1, 64, 300, 1, 1, 4, 16, 1, None)  # D > 256
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
     assert bsa.bsa_version() >= 100
+
+
+def test_segments_count_matches_oracle_layout(bsa):
+    """The host-side layout of bsa_segments_count (no CUDA call) against the
+    oracle's tile_segments, on the VSA page's metadata example and two others."""
+    import oracle
+    from conftest import golden
+    g = golden("vsa_r2v_layout.json")
+    page = [s if isinstance(s, int) else tuple(s) for s in g["our_segments"]["segments"]]
+    for segs, blk, M in [(page, (4, 4, 8), 128), ([5, (2, 3, 5), 0, 7, (2, 2, 3)], (2, 2, 2), 8),
+                         ([(3, 5, 7)], (2, 2, 2), 8), ([9, 300], (1, 1, 1), 128)]:
+        J, P, spans = bsa.bsa_segments_count(segs, *blk, M)
+        blocks, P_o, spans_o = oracle.tile_segments(segs, *blk, M)
+        assert (J, P, spans) == (len(blocks), P_o, spans_o), segs
+    assert bsa.bsa_segments_count(page, 4, 4, 8, 128)[:2] == (g["page_layout"]["num_blocks"],
+                                                               g["page_layout"]["num_prefix_tiles"])
+    lib = bsa._lib
+    n, kinds, dims = bsa._seg_arrays([(2, 2, 2)])
+    assert lib.bsa_segments_count(n, kinds, dims, 4, 4, 4, 8, None, None) == -1  # window larger than M
+    kinds[0] = 7
+    assert lib.bsa_segments_count(n, kinds, dims, 1, 1, 1, 8, None, None) == -1  # unknown kind

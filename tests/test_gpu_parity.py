@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from block_sparse_attention_tile_gb300 import synthetic
-from parity import assert_close, check_route, f64, oracle_blocks
+from parity import TIE_EPS, assert_close, check_route, f64, oracle_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -165,6 +165,70 @@ def test_summary_small_bf16(lib, force_simt, packed):
 def test_summary_fp32_ragged(lib):
     _run_block_case(lib, 1, 1, (5, 3, 4), (2, 2, 3), 12, 8, 2, torch.float32, 14, n_prefix=20,
                     summary=True)
+
+
+# ---------------------------------------------------------------- multi-segment layout + region-grouped TopK
+
+def _segments_case(lib, h, segments, block, M, D, budgets, dtype, seed, packed=None, force_simt=False):
+    pl = _pipeline()
+    geom = pl.SegmentGeometry(segments, *block, M=M)
+    q, kk, v = synthetic.segment_qkv(h, segments, D, seed, dtype)
+    lib.bsa_set_force_simt(force_simt)
+    res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, budgets, packed=packed)
+    torch.cuda.synchronize()
+    blocks, P, spans = oracle.tile_segments(geom.segments, *block, M)
+    assert P == geom.prefix_blocks and spans == geom.spans
+    assert np.array_equal(res.index_map.cpu().numpy(), oracle.index_map(blocks, M))
+    assert np.array_equal(res.block_sizes.cpu().numpy(), [len(b) for b in blocks])
+    rspans = [(lo - P, hi - P) for lo, hi in spans]
+    kept = sum(min(kr, hi - lo) for kr, (lo, hi) in zip(budgets, rspans))
+    scale = D ** -0.5
+    flagged = 0
+    for bh in range(h):
+        Q, K, V = f64(q[bh]), f64(kk[bh]), f64(v[bh])
+        qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        E = oracle.routing_scores(qbar[P:], kbar[P:], D)
+        want_idx, want_num = oracle.route_grouped(E, rspans, budgets, kept)
+        gi, gn = res.q2k_idx[bh].cpu().numpy(), res.q2k_num[bh].cpu().numpy()
+        assert np.array_equal(gn, want_num)
+        # rows may differ only inside a region whose k-th and (k+1)-th scores nearly tie
+        ties = set()
+        for kr, (lo, hi) in zip(budgets, rspans):
+            ties |= set((oracle.near_tie_rows(E[:, lo:hi], min(kr, hi - lo), TIE_EPS)).tolist())
+        bad = [i for i in range(E.shape[0]) if not np.array_equal(gi[i], want_idx[i])]
+        assert set(bad) <= ties, "rows %s differ without a near tie" % sorted(set(bad) - ties)[:10]
+        flagged += len(bad)
+        for i in bad:
+            pos = 0
+            for kr, (lo, hi) in zip(budgets, rspans):
+                kk_ = min(kr, hi - lo)
+                sel = gi[i][pos:pos + kk_]
+                assert np.all((sel >= lo) & (sel < hi)) and np.all(np.diff(sel) > 0)
+                kth = np.sort(E[i, lo:hi])[::-1][kk_ - 1]
+                assert np.all(E[i][sel] >= kth - TIE_EPS)
+                pos += kk_
+        O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, scale, prefix_blocks=P)
+        assert_close(f64(res.out[bh]), O, dtype, "out[bh=%d]" % bh)
+        assert np.abs(res.lse[bh].cpu().numpy() - L).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
+    return flagged
+
+
+@pytest.mark.parametrize("packed", [None, False])
+def test_segments_page_layout_bf16(lib, packed):
+    # the VSA page's metadata example: text 130, a reference video, image 60, audio 200, the target
+    # video; budgets 25% of each video region (1 of 4, 2 of 8); packed copy (default) or gathered tiles
+    _segments_case(lib, 2, [130, (4, 8, 16), 60, 200, (8, 8, 16)], (4, 4, 8), 128, 128, [1, 2],
+                   torch.bfloat16, 606, packed=packed)
+
+
+def test_segments_three_video_regions_fp32(lib):
+    # the R2V figure's shape: context, two reference videos, the output video; budgets 1, 1, 2
+    _segments_case(lib, 2, [40, (2, 6, 8), (2, 6, 8), (4, 6, 8)], (2, 2, 4), 16, 32, [1, 1, 2], torch.float32, 41)
+
+
+def test_segments_ragged_empty_dense_fp32(lib):
+    # an empty dense segment, ragged windows, a region smaller than its budget (2 blocks, budget 4)
+    _segments_case(lib, 1, [5, (2, 3, 5), 0, 7, (2, 2, 3)], (2, 2, 2), 8, 16, [2, 4], torch.float32, 43)
 
 
 # ---------------------------------------------------------------- a10 coarse branch
@@ -368,6 +432,34 @@ def test_route_rows_per_cta_variants(lib, J, D):
 
 
 # ---------------------------------------------------------------- device-side error reporting
+
+@pytest.mark.parametrize("J,starts,budgets", [(1500, [0, 300, 1500], [7, 40]), (700, [0, 1, 350, 700], [3, 9, 20])])
+def test_route_grouped_matches_oracle(lib, J, starts, budgets):
+    # a region longer than 1024 blocks takes the streaming select; a one-block region keeps its block
+    D, BH = 64, 2
+    qbar = synthetic.normal((BH, J, D), 91, DEV)
+    kbar = synthetic.normal((BH, J, D), 92, DEV)
+    spans = list(zip(starts[:-1], starts[1:]))
+    kept = sum(min(k, hi - lo) for k, (lo, hi) in zip(budgets, spans))
+    idx = torch.empty((BH, J, kept + 3), dtype=torch.int32, device=DEV)
+    num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
+    ws = torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV)
+    lib.bsa_route_topk_grouped(qbar, kbar, BH, J, D, J * D, starts, budgets, D ** -0.5, kept + 3, idx, num, ws)
+    torch.cuda.synchronize()
+    for bh in range(BH):
+        E = oracle.routing_scores(f64(qbar[bh]), f64(kbar[bh]), D)
+        want_idx, want_num = oracle.route_grouped(E, spans, budgets, kept + 3)
+        gi, gn = idx[bh].cpu().numpy(), num[bh].cpu().numpy()
+        assert np.array_equal(gn, want_num)
+        ties = set()
+        for k, (lo, hi) in zip(budgets, spans):
+            ties |= set(oracle.near_tie_rows(E[:, lo:hi], min(k, hi - lo), TIE_EPS).tolist())
+        bad = [i for i in range(J) if not np.array_equal(gi[i], want_idx[i])]
+        assert set(bad) <= ties, "rows %s differ without a near tie" % sorted(set(bad) - ties)[:10]
+        # E is left in the workspace for the coarse branch
+        Ews = ws[bh * J * J:(bh + 1) * J * J].view(J, J).double().cpu().numpy()
+        assert np.abs(Ews - E).max() <= 1e-5 * max(1.0, np.abs(E).max())
+
 
 def test_out_of_range_block_index_is_reported_not_faulted(lib):
     pl = _pipeline()
