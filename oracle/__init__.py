@@ -11,9 +11,10 @@ float64 restatement of the definitions given on four pages:
 * "MSA 为什么采用 KV-outer Sparse Attention Forward" (notes.kuangjux.top) -- the
   reverse index, the K1 partial pass and the K2 log-sum-exp combine.
 * "深度解读|Spark-H3：从注意力几何到稀疏内核代码" (jefxiong.cn) -- the
-  exact-plus-summary mixture with the +log(m) mass term, and the Reweight
+  exact-plus-summary mixture with the +log(m) mass term, the Reweight
   summaries (weighted key and value with a log-mass bias at a representative
-  query).
+  query) and the Reblock layout (second-moment metric, equal-capacity
+  hierarchical partition).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The CUDA
@@ -43,3 +44,6 @@ from .kvouter import (  # noqa: F401
 )
 from .spark import bf16_round, reweight_anchor, reweight_summary, reweight_summaries  # noqa: F401
 from .coarse import coarse_attention, coarse_output  # noqa: F401
+from .reblock import (  # noqa: F401
+    second_moment, metric_factor, unit_features, split_node, partition, reblock_layout, attention_mass_recall,
+)

@@ -661,3 +661,70 @@ def test_route_grouped_brute_force_per_region():
             best = max(itertools.combinations(range(lo, hi), kk), key=lambda c: sum(E[i, list(c)]))
             want += sorted(best)
         assert sel == want and num[i] == 6 and np.all(idx[i, 6:] == -1)
+
+
+# ---------------------------------------------------------------- Spark-Reblock (Spark-H3 §05, §06)
+
+def test_reblock_metric_is_the_score_profile_cosine():
+    # §05: cos(L^T k_i, L^T k_j) with L L^T = Q^T Q / N equals the cosine of the score vectors Q k_i, Q k_j
+    rng = np.random.default_rng(11)
+    Q = rng.normal(size=(300, 6)) @ rng.normal(size=(6, 6))
+    K = rng.normal(size=(40, 6))
+    L = oracle.metric_factor(Q, ridge=0.0)
+    assert np.abs(L @ L.T - Q.T @ Q / 300).max() < 1e-12 and np.allclose(np.triu(L, 1), 0)
+    U = oracle.unit_features(K, L)
+    S = K @ Q.T
+    S /= np.linalg.norm(S, axis=1, keepdims=True)
+    assert np.abs(U @ U.T - S @ S.T).max() < 1e-12
+    # the moment is uncentred: shifting Q changes it (a covariance would not)
+    assert np.abs(oracle.second_moment(Q + 3.0) - oracle.second_moment(Q)).max() > 1.0
+
+
+def test_reblock_partition_capacity_and_bijection():
+    rng = np.random.default_rng(12)
+    U = oracle.unit_features(rng.normal(size=(203, 5)), np.eye(5))
+    leaves = oracle.partition(U, 16)
+    sizes = [len(l) for l in leaves]
+    assert sizes[:-1] == [16] * (len(leaves) - 1) and sizes[-1] == 203 - 16 * 12 and len(leaves) == 13
+    assert np.array_equal(np.sort(np.concatenate(leaves)), np.arange(203))
+    assert all(np.all(np.diff(l) > 0) for l in leaves)
+
+
+def test_reblock_split_separates_two_clusters_and_follows_the_landmarks():
+    # two tight, equal clusters (capacity-aligned): the first split puts each cluster on its own side
+    rng = np.random.default_rng(13)
+    c0, c1 = np.array([1.0, 0.0, 0.0]), np.array([0.0, 1.0, 0.0])
+    X = np.where((np.arange(64) % 2 == 0)[:, None], c0, c1) + 0.01 * rng.normal(size=(64, 3))
+    U = oracle.unit_features(X, np.eye(3))
+    left, right = oracle.split_node(U, np.arange(64), 32)
+    assert set(left) == set(range(1, 64, 2)) or set(left) == set(range(0, 64, 2))
+    # four points on a line by hand: landmarks 3 (farthest from 0) and 0; order by projection on u_0 - u_3
+    U4 = np.array([[1.0, 0], [0.8, 0.6], [0.6, 0.8], [0, 1.0]])
+    l4, r4 = oracle.split_node(U4, np.arange(4), 2)
+    assert list(l4) == [2, 3] and list(r4) == [0, 1]
+
+
+def test_reblock_interleaved_clusters_raise_attention_mass_recall():
+    # the page's teaching experiment: interleaved tokens regrouped by the second-moment features
+    # put the attention mass into fewer blocks; at a fixed budget the kept pairs cover more of it
+    rng = np.random.default_rng(14)
+    N, d, B, k = 256, 8, 16, 4
+    centres = rng.normal(size=(4, d)) * 3.0
+    cid = np.arange(N) % 4  # interleaved: every raster block mixes the four clusters
+    Q = centres[cid] + 0.5 * rng.normal(size=(N, d))
+    K = centres[cid] + 0.5 * rng.normal(size=(N, d))
+    scale = d ** -0.5
+
+    def recall(blocks):
+        qb, kb = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        idx, num = oracle.route(oracle.routing_scores(qb, kb, d), k, k)
+        return oracle.attention_mass_recall(Q, K, blocks, idx, num, scale)
+
+    raster = [np.arange(s, s + B) for s in range(0, N, B)]
+    perm = oracle.reblock_layout(Q, K, B)
+    reblocked = [perm[s:s + B] for s in range(0, N, B)]
+    r0, r1 = recall(raster), recall(reblocked)
+    assert r1 > r0 + 0.3, (r0, r1)
+    # all blocks kept: recall is exactly one
+    idx, num = oracle.route(np.zeros((N // B, N // B)), N // B, N // B)
+    assert abs(oracle.attention_mass_recall(Q, K, raster, idx, num, scale) - 1.0) < 1e-12
