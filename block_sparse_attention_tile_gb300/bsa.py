@@ -62,6 +62,9 @@ _SIGS = {
     "bsa_segments_count": (I, [I, P, P, I, I, I, I, P, P]),
     "bsa_tile_map_segments": (I, [I, P, P, I, I, I, I, P, P, P]),
     "bsa_route_topk_grouped": (I, [P, P, I, I, I, I64, I, P, P, F, I, P, P, P, SZ, P]),
+    "bsa_reblock_workspace": (SZ, [I, I, I, I]),
+    "bsa_reblock_layout": (I, [P, P, I, I, I, I, I, I, F, P, P, P, P, SZ, P]),
+    "bsa_permute_rows": (I, [P, P, I, I, I, I, I, P, I, P]),
     "bsa_coarse_attention": (I, [P, I64, P, I64, I, I, I, P, P]),
     "bsa_coarse_apply": (I, [P, I, P, P, I, I, I, I, P, P, I, I, I, P]),
     "bsa_set_force_simt": (None, [I]),
@@ -282,3 +285,19 @@ def bsa_route_topk_grouped(qbar, kbar, BH, J, D, head_stride, region_starts, bud
     nbytes = workspace.numel() * workspace.element_size()
     _check(_lib.bsa_route_topk_grouped(_ptr(qbar), _ptr(kbar), BH, J, D, head_stride, nreg, starts, ks, scale, kmax,
                                        _ptr(q2k_idx), _ptr(q2k_num), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def bsa_reblock_workspace(BH, N, D, n_prefix):
+    return _lib.bsa_reblock_workspace(BH, N, D, n_prefix)
+
+
+def bsa_reblock_layout(q, k, BH, N, D, n_prefix, block, perm, workspace, ridge=1e-6, moment=None, factor=None,
+                       stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_lib.bsa_reblock_layout(_ptr(q), _ptr(k), _dtype(q), BH, N, D, n_prefix, block, ridge, _ptr(perm),
+                                   _ptr(moment), _ptr(factor), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def bsa_permute_rows(src, dst, BH, N, D, n_prefix, perm, inverse=False, stream=None):
+    _check(_lib.bsa_permute_rows(_ptr(src), _ptr(dst), _dtype(src), BH, N, D, n_prefix, _ptr(perm),
+                                 1 if inverse else 0, _stream(stream)))

@@ -192,6 +192,42 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
     return BlockSparseResult(out, lse, index_map, block_sizes, qbar, kbar, q2k_idx, q2k_num, pk, sbias, C)
 
 
+@dataclass
+class ReblockedResult:
+    out: torch.Tensor
+    lse: Optional[torch.Tensor]
+    perm: torch.Tensor              # [BH, N - n_prefix] the layout of each head
+    inner: BlockSparseResult        # the attention in the layout's order
+
+
+def reblocked_attention(q, k, v, n_prefix, M, topk, scale=None, summary=False, reweight=False, need_lse=True,
+                        ridge=1e-6):
+    """Spark-Reblock layout -> rows gathered into it -> the block-sparse path
+    over consecutive runs of M -> outputs scattered back to the original
+    order.  q, k, v: [BH, N, D] with a dense prefix of n_prefix tokens (always
+    attended, not reblocked) followed by the video tokens."""
+    BH, N, D = q.shape
+    Nv = N - n_prefix
+    dev = q.device
+    perm = torch.empty((BH, Nv), dtype=torch.int32, device=dev)
+    ws = torch.empty((bsa.bsa_reblock_workspace(BH, N, D, n_prefix),), dtype=torch.uint8, device=dev)
+    bsa.bsa_reblock_layout(q, k, BH, N, D, n_prefix, M, perm, ws, ridge=ridge)
+    q2, k2, v2 = (torch.empty_like(x) for x in (q, k, v))
+    for src, dst in ((q, q2), (k, k2), (v, v2)):
+        bsa.bsa_permute_rows(src, dst, BH, N, D, n_prefix, perm)
+    # in the layout's order every block is a run of M consecutive rows: a (1, 1, Nv) grid in (1, 1, M) windows
+    geom = Geometry(1, 1, Nv, 1, 1, M, M=M, n_prefix=n_prefix)
+    inner = block_sparse_attention(q2, k2, v2, geom, topk, scale=scale, summary=summary, reweight=reweight,
+                                   need_lse=need_lse)
+    out = torch.empty_like(q)
+    bsa.bsa_permute_rows(inner.out, out, BH, N, D, n_prefix, perm, inverse=True)
+    lse = None
+    if need_lse:
+        lse = torch.empty_like(inner.lse)
+        bsa.bsa_permute_rows(inner.lse.view(BH, N, 1), lse.view(BH, N, 1), BH, N, 1, n_prefix, perm, inverse=True)
+    return ReblockedResult(out, lse, perm, inner)
+
+
 def nsa_qouter(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None, need_lse=True):
     """Token-granular GQA selected attention, query-outer.  q [B,T,HQ,D],
     k/v [B,T,H,D], block_indices [B,T,H,S] int32, block_counts [B,T,H] int32."""

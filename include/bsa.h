@@ -370,6 +370,37 @@ bsa_status bsa_coarse_apply(void* out, bsa_dtype dtype, const float* C, const fl
                             const int32_t* block_sizes, int J, int M, int prefix_blocks,
                             void* stream);
 
+/* ------------------------------------------------------------------ a11 ---
+ * Spark-Reblock layout.  [Spark] §05: keys are compared through L^T k with
+ * L L^T = M_Q + ridge * tr(M_Q)/d * I, M_Q = Q_v^T Q_v / N_v the uncentred
+ * second moment of the video queries (prefix rows excluded), so that inner
+ * products of the unit features are the cosines of the queries' score
+ * profiles.  [Spark] §06: an equal-capacity hierarchical partition: a node
+ * of nb blocks is split into ceil(nb/2) and the rest along the direction
+ * between two landmarks (a = the member farthest from the node's lowest-id
+ * member, b = the member farthest from a; ties to the lower id), members
+ * ordered by (projection, token id); down to single blocks.  One layout per
+ * (batch, head), built from the keys; the queries reuse it.
+ * q, k: [device] [BH, N, D] (F32 or BF16), D <= 128; the video tokens are
+ * n_prefix .. N-1.  perm: [device] int32 [BH, N - n_prefix]: block j of head h
+ * is video tokens perm[h][j*block .. j*block + block - 1] (ids counted from
+ * the first video token), members ascending.  moment, factor: [device] float
+ * [BH, D, D] or NULL (M_Q and L, for inspection).  workspace: [device]
+ * bsa_reblock_workspace bytes, 256-byte aligned.  1 <= block <= 1024.
+ *
+ * bsa_permute_rows: dst = src with each head's video rows gathered into the
+ * layout's order (dst[h][n_prefix + t] = src[h][n_prefix + perm[h][t]]), or
+ * with inverse != 0 scattered back (dst[h][n_prefix + perm[h][t]] =
+ * src[h][n_prefix + t]); prefix rows copied.  src, dst: [device] [BH, N, D]
+ * of `dtype`, distinct.  A perm entry outside [0, N - n_prefix) raises
+ * BSA_ERR_INDEX and the row is skipped. */
+size_t bsa_reblock_workspace(int BH, int N, int D, int n_prefix);
+bsa_status bsa_reblock_layout(const void* q, const void* k, bsa_dtype dtype, int BH, int N, int D,
+                              int n_prefix, int block, float ridge, int32_t* perm, float* moment,
+                              float* factor, void* workspace, size_t workspace_bytes, void* stream);
+bsa_status bsa_permute_rows(const void* src, void* dst, bsa_dtype dtype, int BH, int N, int D,
+                            int n_prefix, const int32_t* perm, int inverse, void* stream);
+
 /* Forces the CUDA-core attention kernels even where a tensor-core kernel
  * exists (1) or restores the default dispatch (0).  Host, process-wide. */
 void bsa_set_force_simt(int force);

@@ -103,6 +103,11 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     assert rc == bsa.BSA_ERR_INVALID_ARG and "stride" in bsa.bsa_last_error()
     rc = lib.bsa_coarse_apply(1, 1, 1, 1, 0, 1, 64, 300, 1, 1, 4, 16, 1, None)  # D > 256
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
+    rc = lib.bsa_reblock_layout(1, 1, 1, 1, 100, 256, 0, 16, 1e-6, 1, None, None, 256, 1 << 30, None)  # D > 128
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()
+    rc = lib.bsa_permute_rows(1, 1, 1, 2, 10, 4, 2, 1, 0, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "differ" in bsa.bsa_last_error()
+    assert bsa.bsa_reblock_workspace(2, 100, 8, 100) == 0  # no video tokens
     assert bsa.bsa_version() >= 100
 
 

@@ -231,6 +231,99 @@ def test_segments_ragged_empty_dense_fp32(lib):
     _segments_case(lib, 1, [5, (2, 3, 5), 0, 7, (2, 2, 3)], (2, 2, 2), 8, 16, [2, 4], torch.float32, 43)
 
 
+# ---------------------------------------------------------------- a11 Spark-Reblock layout
+
+def _layout_blocks(perm_h, n_prefix, M):
+    """Prefix chunks, then runs of M entries of a head's layout (video ids offset by the prefix)."""
+    perm_h = np.asarray(perm_h, dtype=np.int64)
+    return oracle.tile_prefix(n_prefix, M) + [n_prefix + perm_h[s:s + M] for s in range(0, len(perm_h), M)]
+
+
+@pytest.mark.parametrize("dtype,D,n_prefix,Nv,M", [(torch.float32, 16, 40, 1000, 64),
+                                                   (torch.bfloat16, 64, 0, 2048, 128),
+                                                   (torch.bfloat16, 128, 128, 1536, 128)])
+def test_reblock_layout(lib, dtype, D, n_prefix, Nv, M):
+    BH, N = 2, n_prefix + Nv
+    q, k, v = synthetic.cluster_qkv(BH, n_prefix, Nv, D, 808 + D, dtype)
+    perm = torch.empty((BH, Nv), dtype=torch.int32, device=DEV)
+    mom = torch.empty((BH, D, D), dtype=torch.float32, device=DEV)
+    fac = torch.empty_like(mom)
+    ws = torch.empty((lib.bsa_reblock_workspace(BH, N, D, n_prefix),), dtype=torch.uint8, device=DEV)
+    lib.bsa_reblock_layout(q.to(DEV), k.to(DEV), BH, N, D, n_prefix, M, perm, ws, moment=mom, factor=fac)
+    torch.cuda.synchronize()
+    NB = -(-Nv // M)
+    kk = max(2, NB // 4)  # a quarter of the blocks: with one kept block the recall measure is too coarse
+    scale = D ** -0.5
+    for h in range(BH):
+        Q, K = f64(q[h]), f64(k[h])
+        Mo = oracle.second_moment(Q[n_prefix:])
+        assert np.abs(f64(mom[h]) - Mo).max() <= 1e-5 * np.abs(Mo).max()
+        Lo = oracle.metric_factor(Q[n_prefix:])
+        assert np.abs(f64(fac[h]) - Lo).max() <= 1e-4 * np.abs(Lo).max()
+        ph = perm[h].cpu().numpy()
+        # a bijection of the video ids, blocks of M (the last one short), members ascending
+        assert np.array_equal(np.sort(ph), np.arange(Nv))
+        assert all(np.all(np.diff(ph[s:s + M]) > 0) for s in range(0, Nv, M))
+        # quality: the layout concentrates the attention mass (the partition itself is parity unpinned)
+
+        def recall(blocks):
+            P = len(oracle.tile_prefix(n_prefix, M))
+            qb, kb = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+            idx, num = oracle.route(oracle.routing_scores(qb[P:], kb[P:], D), kk, kk)
+            return oracle.attention_mass_recall(Q, K, blocks, idx, num, scale, prefix_blocks=P)
+
+        r_gpu = recall(_layout_blocks(ph, n_prefix, M))
+        r_raster = recall(_layout_blocks(np.arange(Nv), n_prefix, M))
+        r_oracle = recall(_layout_blocks(oracle.reblock_layout(Q[n_prefix:], K[n_prefix:], M), n_prefix, M))
+        assert r_gpu > r_raster + 0.03, (r_gpu, r_raster)
+        assert r_gpu >= r_oracle - 0.03, (r_gpu, r_oracle)
+
+
+def test_permute_rows_round_trip(lib):
+    BH, N, D, n_prefix = 2, 300, 24, 44
+    x = synthetic.normal((BH, N, D), 5, DEV, torch.bfloat16)
+    perm = torch.stack([torch.randperm(N - n_prefix, generator=torch.Generator().manual_seed(h)) for h in range(BH)])
+    perm = perm.to(torch.int32).to(DEV)
+    y, z = torch.empty_like(x), torch.empty_like(x)
+    lib.bsa_permute_rows(x, y, BH, N, D, n_prefix, perm)
+    lib.bsa_permute_rows(y, z, BH, N, D, n_prefix, perm, inverse=True)
+    torch.cuda.synchronize()
+    assert torch.equal(z, x)
+    for h in range(BH):
+        want = torch.cat([x[h, :n_prefix], x[h, n_prefix:][perm[h].long()]])
+        assert torch.equal(y[h], want)
+
+
+@pytest.mark.parametrize("summary", [False, True])
+def test_reblocked_attention_bf16(lib, summary):
+    pl = _pipeline()
+    BH, n_prefix, Nv, D, M, kk = 2, 256, 4096, 128, 128, 4
+    q, k, v = synthetic.cluster_qkv(BH, n_prefix, Nv, D, 818, torch.bfloat16)
+    res = pl.reblocked_attention(q.to(DEV), k.to(DEV), v.to(DEV), n_prefix, M, kk, summary=summary)
+    torch.cuda.synchronize()
+    scale = D ** -0.5
+    P = len(oracle.tile_prefix(n_prefix, M))
+    for h in range(BH):
+        Q, K, V = f64(q[h]), f64(k[h]), f64(v[h])
+        blocks = _layout_blocks(res.perm[h].cpu().numpy(), n_prefix, M)
+        qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        E = oracle.routing_scores(qbar[P:], kbar[P:], D)
+        gi, gn = res.inner.q2k_idx[h].cpu().numpy(), res.inner.q2k_num[h].cpu().numpy()
+        check_route(gi, gn, E, kk)
+        lse_tol = 2e-3
+        if summary:
+            vbar = oracle.pool_blocks(V, blocks)
+            O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kbar[P:], vbar[P:], scale, prefix_blocks=P)
+            # the summary keys are stored in bf16: a virtual logit moves by at most
+            # scale * |q| * |kbar - bf16(kbar)|, and so does the log-sum-exp
+            kr = np.abs(kbar[P:] - oracle.bf16_round(kbar[P:]))
+            lse_tol += scale * np.linalg.norm(Q, axis=1).max() * np.linalg.norm(kr, axis=1).max()
+        else:
+            O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, scale, prefix_blocks=P)
+        assert_close(f64(res.out[h]), O, torch.bfloat16, "out[h=%d]" % h)
+        assert np.abs(res.lse[h].cpu().numpy() - L).max() <= lse_tol
+
+
 # ---------------------------------------------------------------- a10 coarse branch
 
 @pytest.mark.parametrize("gate", ["channel", "token"])
