@@ -19,6 +19,9 @@ Other workloads (--workload):
                  unselected blocks
   spark_reweight the same with Spark-Reweight summaries (weighted key and
                  value at the head's mean video query, log-mass bias)
+  spark_reblock  the spark_summary inputs in the Spark-Reblock layout (one per
+                 head, built on the GPU each step) instead of a seeded
+                 permutation; rows gathered into it and outputs scattered back
   r2v_bsa        bf16, h=24, R2V layout: 1024 text tokens, two reference
                  videos (8,48,80) and the target (30,48,80) in (4,4,8) windows;
                  region-grouped TopK keeping 10% of each video region
@@ -60,6 +63,8 @@ WORKLOADS = {
                           seed=505, dtype="bf16", n_text=1024, summary=True),
     "r2v_bsa": dict(kind="block", B=1, heads=24, D=128, segments=[1024, (8, 48, 80), (8, 48, 80), (30, 48, 80)],
                     block=(4, 4, 8), M=128, budgets=[24, 24, 96], k=144, seed=707, dtype="bf16"),
+    "spark_reblock": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
+                          seed=505, dtype="bf16", n_text=1024, summary=True, reblock=True),
     "video_dit_coarse": dict(kind="block", B=1, heads=24, D=128, grid=(30, 48, 80), block=(4, 4, 8), M=128, k=96,
                              seed=202, dtype="bf16", coarse=True),
     "spark_reweight": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
@@ -170,7 +175,11 @@ if segs is not None:
     blocks, P_seg, spans = oracle.tile_segments(segs, bT, bH, bW, M)
 elif summary:
     q, kk, v = synthetic.cluster_qkv(1, n_text, T * H * W, D, w["seed"], dt)
-    perm = synthetic.permutation(T * H * W, w["seed"] + 1)
+    if w.get("reblock"):  # the Spark-Reblock layout of this head
+        Qh, Kh = (x[0].float().numpy().astype(np.float64) for x in (q, kk))
+        perm = oracle.reblock_layout(Qh[n_text:], Kh[n_text:], M)
+    else:
+        perm = synthetic.permutation(T * H * W, w["seed"] + 1)
     blocks = oracle.tile_prefix(n_text, M) + oracle.tile_permuted(perm, M, offset=n_text)
 else:
     q, kk, v = synthetic.video_qkv(1, 1, T, H, W, D, w["seed"], dt, field=(w["dtype"] == "bf16"))
@@ -271,7 +280,8 @@ def run_oracle_sample(wname, budget_s=15.0):
                   "attended, all %d heads (%.1f s); step time scaled by tokens and batch"
                   % (w["B"], w["T"], r["route_s"], r["units"], r["total_units"], w["HQ"], r["attn_s"]))
     else:
-        pre = ("tile map, pool, route" + (" and Spark-Reweight summaries" if w.get("reweight") else "")
+        pre = (("Spark-Reblock layout, " if w.get("reblock") else "") + "tile map, pool, route"
+               + (" and Spark-Reweight summaries" if w.get("reweight") else "")
                + (" and the coarse branch softmax(E) V_bar" if w.get("coarse") else ""))
         sample = ("1 of %d heads: %s of all %d blocks (%.1f s) plus %d of %d query blocks "
                   "attended (%.1f s); step time scaled by heads and blocks"
@@ -347,10 +357,16 @@ class BlockWorkload:
         self.summary = w.get("summary", False)
         self.reweight = self.summary and w.get("reweight", False)
         self.coarse = w.get("coarse", False)
+        self.reblock = w.get("reblock", False)
         if self.reweight:
             self.stage_names = ["tile_map", "pool", "route", "reweight", "attention"]
         if self.coarse:
             self.stage_names = ["tile_map", "pool", "route", "attention", "coarse_attention", "coarse_apply"]
+        self.core_stages = len(self.stage_names)
+        self.ev_off = 0
+        if self.reblock:
+            self.stage_names = ["reblock", "permute"] + self.stage_names + ["unpermute"]
+            self.ev_off = 2
         n_text = w.get("n_text", 0)
         D, M, k = w["D"], w["M"], w["k"]
         self.BH = w["B"] * w["heads"]
@@ -364,13 +380,16 @@ class BlockWorkload:
             elif self.summary:
                 self.q, self.k, self.v = synthetic.cluster_qkv(self.BH, n_text, T * H * W, D, seed, self.dtype,
                                                                device=dev)
-                self.perm = torch.as_tensor(synthetic.permutation(T * H * W, seed + 1), device=dev)
+                self.perm = (None if self.reblock else
+                             torch.as_tensor(synthetic.permutation(T * H * W, seed + 1), device=dev))
             else:
                 self.q, self.k, self.v = synthetic.video_qkv(w["B"], w["heads"], T, H, W, D, seed, self.dtype,
                                                              device=dev, field=(w["dtype"] == "bf16"))
                 self.perm = None
         if self.segments is not None:
             self.geom = pipeline.SegmentGeometry(self.segments, *w["block"], M=M)
+        elif self.reblock:  # in the layout's order a block is a run of M rows
+            self.geom = pipeline.Geometry(1, 1, T * H * W, 1, 1, M, M=M, n_prefix=n_text)
         else:
             self.geom = pipeline.Geometry(T, H, W, *w["block"], M=M, n_prefix=n_text, perm=self.perm)
         self.N = self.geom.n_tokens
@@ -408,6 +427,18 @@ class BlockWorkload:
         # tile map, pool, route (contraction + select), [reweight: mean partials, mean, summaries], attention,
         # [coarse: attention, apply]
         self.launches_per_step = 5 + (3 if self.reweight else 0) + (2 if self.coarse else 0)
+        self.core_out, self.core_lse = self.out, self.lse
+        if self.reblock:
+            Nv = self.N - n_text
+            NB = -(-Nv // M)
+            levels = max(0, (NB - 1).bit_length())
+            self.rb_perm = torch.empty((BH, Nv), dtype=torch.int32, device=dev)
+            self.rb_ws = torch.empty((_bsa.bsa_reblock_workspace(BH, self.N, D, n_text),), dtype=torch.uint8,
+                                     device=dev)
+            self.q2, self.k2, self.v2 = (torch.empty_like(x) for x in (self.q, self.k, self.v))
+            self.core_out, self.core_lse = torch.empty_like(self.out), torch.empty_like(self.lse)
+            # moment, reduce, factor, features, iota, one split per level, leaf sort; 3 gathers; 2 scatters
+            self.launches_per_step += 6 + levels + 3 + 2
 
     def tile_map(self):
         from block_sparse_attention_tile_gb300 import bsa
@@ -428,42 +459,75 @@ class BlockWorkload:
             bsa.bsa_route_topk(qbar, kbar, nh, self.Jr, D, self.J * D, kk, self.scale, kk, q2k, q2n,
                                self.route_ws)
 
-    def step(self, ev=None, q=None, k=None, v=None):
+    def reblock_in(self, q, k, v, sl, nh):
+        """The heads' layouts, then their rows gathered into them."""
         from block_sparse_attention_tile_gb300 import bsa
-        w, g = self.w, self.geom
+        n_text, M, D = self.w.get("n_text", 0), self.w["M"], self.w["D"]
+        bsa.bsa_reblock_layout(q[sl], k[sl], nh, self.N, D, n_text, M, self.rb_perm[sl], self.rb_ws)
+
+    def permute_in(self, q, k, v, sl, nh):
+        from block_sparse_attention_tile_gb300 import bsa
+        n_text, D = self.w.get("n_text", 0), self.w["D"]
+        for src, dst in ((q, self.q2), (k, self.k2), (v, self.v2)):
+            bsa.bsa_permute_rows(src[sl], dst[sl], nh, self.N, D, n_text, self.rb_perm[sl])
+
+    def permute_out(self, sl, nh):
+        from block_sparse_attention_tile_gb300 import bsa
+        n_text, D = self.w.get("n_text", 0), self.w["D"]
+        bsa.bsa_permute_rows(self.core_out[sl], self.out[sl], nh, self.N, D, n_text, self.rb_perm[sl], inverse=True)
+        bsa.bsa_permute_rows(self.core_lse[sl].unsqueeze(-1), self.lse[sl].unsqueeze(-1), nh, self.N, 1, n_text,
+                             self.rb_perm[sl], inverse=True)
+
+    def step(self, ev=None, q=None, k=None, v=None):
         q = self.q if q is None else q
         k = self.k if k is None else k
         v = self.v if v is None else v
+        if not self.reblock:
+            return self.core_step(ev, q, k, v)
+        st = self.torch.cuda.current_stream()
+        sl = slice(0, self.BH)
+        if ev: ev[0].record(st)
+        self.reblock_in(q, k, v, sl, self.BH)
+        if ev: ev[1].record(st)
+        self.permute_in(q, k, v, sl, self.BH)
+        self.core_step(ev, self.q2, self.k2, self.v2)
+        self.permute_out(sl, self.BH)
+        if ev: ev[len(self.stage_names)].record(st)
+
+    def core_step(self, ev, q, k, v):
+        from block_sparse_attention_tile_gb300 import bsa
+        w, g = self.w, self.geom
         D, M, kk = w["D"], w["M"], w["k"]
         st = self.torch.cuda.current_stream()
-        if ev: ev[0].record(st)
+        o = self.ev_off
+        if ev: ev[o + 0].record(st)
         self.tile_map()
-        if ev: ev[1].record(st)
+        if ev: ev[o + 1].record(st)
         bsa.bsa_pool_blocks(q, k, v if self.vbar is not None else None, self.BH, self.N, D, self.im, self.bs,
                             self.J, M, self.qbar, self.kbar, self.vbar, self.kbar_lp, self.vbar_lp,
                             packed=self.packed)
-        if ev: ev[2].record(st)
+        if ev: ev[o + 2].record(st)
         self.route(self.qbar[:, self.P:], self.kbar[:, self.P:], self.BH, self.q2k, self.q2n)
-        if ev: ev[3].record(st)
+        if ev: ev[o + 3].record(st)
         if self.reweight:
             bsa.bsa_reweight_summaries(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, self.scale,
                                        self.kbar_lp, self.vbar_lp, self.sbias, self.rw_ws, qbar=self.qbar)
-            if ev: ev[4].record(st)
+            if ev: ev[o + 4].record(st)
         if self.summary:
             bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
-                                self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.out, self.lse,
-                                packed=self.packed, summary_bias=self.sbias)
+                                self.q2k, self.q2n, kk, self.kbar_lp, self.vbar_lp, self.scale, self.core_out,
+                                self.core_lse, packed=self.packed, summary_bias=self.sbias)
         else:
             bsa.bsa_fwd_qouter(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
-                               self.q2k, self.q2n, kk, self.scale, self.out, self.lse, packed=self.packed)
+                               self.q2k, self.q2n, kk, self.scale, self.core_out, self.core_lse, packed=self.packed)
         if self.coarse:
-            if ev: ev[4].record(st)
+            if ev: ev[o + 4].record(st)
             bsa.bsa_coarse_attention(self.route_ws, self.Jr * self.Jr, self.vbar[:, self.P:], self.J * D, self.BH,
                                      self.Jr, D, self.C)
-            if ev: ev[5].record(st)
-            bsa.bsa_coarse_apply(self.out, self.C, self.gate, False, self.BH, self.N, D, self.im, self.bs, self.J, M,
-                                 self.P)
-        if ev: ev[len(self.stage_names)].record(st)
+            if ev: ev[o + 5].record(st)
+            bsa.bsa_coarse_apply(self.core_out, self.C, self.gate, False, self.BH, self.N, D, self.im, self.bs,
+                                 self.J, M, self.P)
+        if ev: ev[o + self.core_stages].record(st)
 
     def host_inputs(self):
         return [self.q, self.k, self.v], [self.out]
@@ -480,6 +544,10 @@ class BlockWorkload:
         D, M, kk = w["D"], w["M"], w["k"]
         sl = slice(h0, h1)
         nh = h1 - h0
+        if self.reblock:
+            self.reblock_in(q, k, v, sl, nh)
+            self.permute_in(q, k, v, sl, nh)
+            q, k, v = self.q2, self.k2, self.v2
         bsa.bsa_pool_blocks(q[sl], k[sl], v[sl] if self.vbar is not None else None, nh, self.N, D, self.im,
                             self.bs, self.J, M, self.qbar[sl], self.kbar[sl],
                             self.vbar[sl] if self.vbar is not None else None,
@@ -495,16 +563,18 @@ class BlockWorkload:
         if self.summary:
             bsa.bsa_fwd_summary(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                 self.q2k[sl], self.q2n[sl], kk, self.kbar_lp[sl], self.vbar_lp[sl], self.scale,
-                                self.out[sl], self.lse[sl], packed=packed_chunk, summary_bias=sb)
+                                self.core_out[sl], self.core_lse[sl], packed=packed_chunk, summary_bias=sb)
         else:
             bsa.bsa_fwd_qouter(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
-                               self.q2k[sl], self.q2n[sl], kk, self.scale, self.out[sl], self.lse[sl],
+                               self.q2k[sl], self.q2n[sl], kk, self.scale, self.core_out[sl], self.core_lse[sl],
                                packed=packed_chunk)
         if self.coarse:
             bsa.bsa_coarse_attention(self.route_ws, self.Jr * self.Jr, self.vbar[sl, self.P:], self.J * D, nh,
                                      self.Jr, D, self.C[sl])
-            bsa.bsa_coarse_apply(self.out[sl], self.C[sl], self.gate[sl], False, nh, self.N, D, self.im, self.bs,
+            bsa.bsa_coarse_apply(self.core_out[sl], self.C[sl], self.gate[sl], False, nh, self.N, D, self.im, self.bs,
                                  self.J, M, self.P)
+        if self.reblock:
+            self.permute_out(sl, nh)
 
     def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=4):
         """End-to-end step with host buffers, pipelined by heads: chunk c's
@@ -608,6 +678,20 @@ class BlockWorkload:
                      "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
             "route": {"bound": "alu", "achieved": route_tf, "peak": fp32, "unit": "TFLOP/s", "frac": route_tf / fp32,
                       "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}}
+        if self.reblock:
+            Nv = self.N - self.w.get("n_text", 0)
+            el = self.q.element_size()
+            rflops = 2 * 2.0 * self.BH * Nv * D * D  # the moment Q^T Q and the features K L
+            secondary["reblock"] = {"bound": "alu", "achieved": rflops / (stage_ms["reblock"] * 1e-3) / 1e12,
+                                    "peak": fp32, "unit": "TFLOP/s",
+                                    "frac": rflops / (stage_ms["reblock"] * 1e-3) / 1e12 / fp32,
+                                    "flops_per_launch": rflops,
+                                    "note": "moment and features; the partition levels are latency-bound"}
+            pb = 3 * 2 * self.q.numel() * el
+            secondary["permute"] = {"bound": "hbm", "achieved": pb / (stage_ms["permute"] * 1e-3) / 1e9,
+                                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": pb / (stage_ms["permute"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                    "bytes_per_launch": pb}
         if self.coarse:
             cflops = 2.0 * self.BH * self.Jr * self.Jr * D
             ctf = cflops / (stage_ms["coarse_attention"] * 1e-3) / 1e12
@@ -636,6 +720,8 @@ class BlockWorkload:
             config.update({"n_text": self.w["n_text"], "permuted": True, "summary": True})
             if self.reweight:
                 config["summaries"] = "spark-reweight"
+            if self.reblock:
+                config["permuted"] = "spark-reblock layout per head, built on the GPU every step"
         if self.coarse:
             config["coarse"] = "softmax(E) V_bar, per-head per-channel gate"
         nbytes = 3 * self.q.numel() * self.q.element_size()

@@ -12,19 +12,30 @@
 //
 //   reblock_moment_kernel      split-K partial sums of q q^T (float32)
 //   reblock_moment_reduce      M = sum of the partials in split order / N
-//   reblock_cholesky_kernel    L = chol(M + ridge * tr(M)/d * I) in float64
-//   reblock_features_kernel    U = rows of K L scaled to unit length
-//   reblock_split_kernel       one tree level: per node the two landmarks, the
-//                              projections, an exact radix select of the cut
-//                              on (projection, token id) and a stable split
+//   reblock_cholesky_kernel    L = chol(M + ridge * tr(M)/d * I) (float32)
+//   reblock_features_kernel    U = rows of K L scaled to unit length, stored
+//                              in bf16 (the partition's only input)
+//   reblock_split_kernel       one tree level: a cluster of up to 8 CTAs per
+//                              node (the top levels have few, large nodes),
+//                              each CTA a share of the members; per node the
+//                              two landmarks, the projections (a thread per
+//                              member, streaming its feature row), an exact
+//                              radix select of the cut on (projection, token
+//                              id) and a stable split, the CTAs' partial
+//                              results combined through distributed shared
+//                              memory at cluster barriers
 //   reblock_leaf_sort_kernel   members of each block in ascending token id
 //   permute_rows_kernel        rows gathered into (or scattered back from) the
 //                              layout's order
 #include <math_constants.h>
 
+#include <cooperative_groups.h>
+
 #include <algorithm>
 
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace bsa {
 
@@ -95,38 +106,38 @@ __global__ void __launch_bounds__(256) reblock_moment_reduce(const float* __rest
 
 // ------------------------------------------------------------------ factor
 // One CTA of kRbMaxD threads per head; column by column, thread i computes
-// row i (float64).  A non-positive pivot (a zero moment) gives a zero column.
+// row i.  A non-positive pivot (a zero moment) gives a zero column.
 __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* __restrict__ M, int D, float ridge,
                                                                    float* __restrict__ L) {
-    extern __shared__ double A[];  // [D][D + 1]
-    __shared__ double s_tr, s_piv;
+    extern __shared__ float A[];  // [D][D + 1]
+    __shared__ float s_tr, s_piv;
     const int bh = blockIdx.x, i = threadIdx.x, ld = D + 1;
     const float* Mh = M + (long long)bh * D * D;
-    for (int e = i; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = (double)Mh[e];
+    for (int e = i; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = Mh[e];
     __syncthreads();
     if (i == 0) {
-        double tr = 0.0;
+        float tr = 0.f;
         for (int d = 0; d < D; ++d) tr += A[d * ld + d];
         s_tr = tr;
     }
     __syncthreads();
-    if (i < D) A[i * ld + i] += (double)ridge * s_tr / D;
+    if (i < D) A[i * ld + i] += ridge * s_tr / D;
     __syncthreads();
     for (int j = 0; j < D; ++j) {
-        double t = 0.0;
+        float t = 0.f;
         if (i >= j && i < D) {
             t = A[i * ld + j];
-            for (int c = 0; c < j; ++c) t -= A[i * ld + c] * A[j * ld + c];
+            for (int c = 0; c < j; ++c) t = fmaf(-A[i * ld + c], A[j * ld + c], t);
         }
-        if (i == j) s_piv = t > 0.0 ? sqrt(t) : 0.0;
+        if (i == j) s_piv = t > 0.f ? sqrtf(t) : 0.f;
         __syncthreads();
-        if (i >= j && i < D) A[i * ld + j] = (i == j) ? s_piv : (s_piv > 0.0 ? t / s_piv : 0.0);
+        if (i >= j && i < D) A[i * ld + j] = (i == j) ? s_piv : (s_piv > 0.f ? t / s_piv : 0.f);
         __syncthreads();
     }
     float* Lh = L + (long long)bh * D * D;
     for (int e = i; e < D * D; e += blockDim.x) {
         const int r = e / D, c = e % D;
-        Lh[e] = c <= r ? (float)A[r * ld + c] : 0.f;
+        Lh[e] = c <= r ? A[r * ld + c] : 0.f;
     }
 }
 
@@ -136,7 +147,8 @@ __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* 
 // the token's 16 threads reduce the squared norm.
 template <typename T>
 __global__ void __launch_bounds__(256) reblock_features_kernel(const T* __restrict__ k, int N, int D, int n_prefix,
-                                                               const float* __restrict__ L, float* __restrict__ U) {
+                                                               const float* __restrict__ L,
+                                                               __nv_bfloat16* __restrict__ U) {
     extern __shared__ __align__(16) float fs[];
     float* Ls = fs;                    // [kRbMaxD][kRbMaxD]
     float* ks = Ls + kRbMaxD * kRbMaxD;  // [64][kRbMaxD]
@@ -180,10 +192,10 @@ __global__ void __launch_bounds__(256) reblock_features_kernel(const T* __restri
         const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
         const int t = t0 + 4 * ty + a;
         if (t < Nv) {
-            float* ur = U + ((long long)bh * Nv + t) * D;
+            __nv_bfloat16* ur = U + ((long long)bh * Nv + t) * D;
 #pragma unroll
             for (int b = 0; b < 8; ++b)
-                if (8 * tx + b < D) ur[8 * tx + b] = acc[a][b] * inv;
+                if (8 * tx + b < D) ur[8 * tx + b] = __float2bfloat16(acc[a][b] * inv);
         }
     }
 }
@@ -230,9 +242,50 @@ __device__ __forceinline__ unsigned long long rb_block_max(unsigned long long v,
     return t;
 }
 
-// CTA (node, head): members are order[r0 .. r1) of the head (token ids).
-__global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const float* __restrict__ U, int Nv, int D,
-                                                                       int block, int NB, int level,
+// The squared distance of a member's feature row to `c`, or its projection on
+// `c` (fp32 arithmetic on the bf16 row; a thread per member).
+template <bool DIST>
+__device__ __forceinline__ float rb_row_op(const __nv_bfloat16* __restrict__ row, const float* c, int D) {
+    float acc = 0.f;
+    if ((D & 7) == 0) {
+        for (int d0 = 0; d0 < D; d0 += 64) {
+            uint4 x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                x[u] = d0 + 8 * u < D ? *reinterpret_cast<const uint4*>(row + d0 + 8 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int d = d0 + 8 * u;
+                if (d >= D) continue;
+                const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+                    if (DIST) {
+                        const float e0 = lo - c[d + 2 * e], e1 = hi - c[d + 2 * e + 1];
+                        acc = fmaf(e0, e0, fmaf(e1, e1, acc));
+                    } else {
+                        acc = fmaf(lo, c[d + 2 * e], fmaf(hi, c[d + 2 * e + 1], acc));
+                    }
+                }
+            }
+        }
+    } else {
+        for (int d = 0; d < D; ++d) {
+            const float x = __bfloat162float(row[d]);
+            if (DIST) acc = fmaf(x - c[d], x - c[d], acc);
+            else acc = fmaf(x, c[d], acc);
+        }
+    }
+    return acc;
+}
+
+// Cluster (node, head), C CTAs: CTA `rank` takes members [c0, c1) of the
+// node's members order[r0 .. r1) (token ids).  Partial results go through
+// shared memory slots that every CTA of the cluster reads after a cluster
+// barrier, so all of them take the same decisions.
+__global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __nv_bfloat16* __restrict__ U, int Nv,
+                                                                       int D, int block, int NB, int level,
                                                                        int32_t* __restrict__ order,
                                                                        int32_t* __restrict__ tmp,
                                                                        unsigned long long* __restrict__ keys) {
@@ -240,98 +293,121 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const fl
     __shared__ unsigned long long red[kRbSplitThreads / 32];
     __shared__ unsigned int hist[256];
     __shared__ int scan[kRbSplitThreads];
-    __shared__ unsigned long long s_prefix;
-    __shared__ int s_need;
-    const int bh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int kWarps = kRbSplitThreads / 32;
+    __shared__ unsigned int hsum[256];
+    __shared__ int s_digit, s_need;
+    __shared__ unsigned long long s_slot;  // this CTA's partial, read by the cluster
+    __shared__ int s_count;                // this CTA's number of left members
+    cg::cluster_group cl = cg::this_cluster();
+    const int C = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+    const int bh = blockIdx.y, tid = threadIdx.x;
     int lo, nb;
-    rb_node(NB, level, blockIdx.x, lo, nb);
-    if (nb <= 1) return;
+    rb_node(NB, level, blockIdx.x / C, lo, nb);
+    if (nb <= 1) return;  // the whole cluster leaves together
     const int r0 = lo * block, r1 = min(Nv, (lo + nb) * block);
     const int n = r1 - r0;
+    const int c0 = r0 + (int)((long long)n * rank / C), c1 = r0 + (int)((long long)n * (rank + 1) / C);
     const int cap_left = ((nb + 1) / 2) * block;
     int32_t* ord = order + (long long)bh * Nv;
     int32_t* tp = tmp + (long long)bh * Nv;
     unsigned long long* ky = keys + (long long)bh * Nv;
-    const float* Uh = U + (long long)bh * Nv * D;
+    const __nv_bfloat16* Uh = U + (long long)bh * Nv * D;
+
+    // the cluster-wide max of one value per CTA
+    auto cluster_max = [&](unsigned long long v) {
+        v = rb_block_max(v, red);
+        if (tid == 0) s_slot = v;
+        cl.sync();
+        unsigned long long t = 0;
+        for (int r = 0; r < C; ++r) {
+            const unsigned long long o = *cl.map_shared_rank(&s_slot, r);
+            t = o > t ? o : t;
+        }
+        cl.sync();  // every CTA has read the slots before they are reused
+        return t;
+    };
+    auto load_row = [&](float* dst, int t) {
+        for (int d = tid; d < D; d += kRbSplitThreads) dst[d] = __bfloat162float(Uh[(long long)t * D + d]);
+    };
 
     // 1. the node's lowest token id
     unsigned long long best = 0;
-    for (int m = tid; m < n; m += kRbSplitThreads)
-        best = max(best, (unsigned long long)(0xffffffffu - (uint32_t)ord[r0 + m]));
-    const int s0 = (int)(0xffffffffu - (uint32_t)rb_block_max(best, red));
-    for (int d = tid; d < D; d += kRbSplitThreads) ua[d] = Uh[(long long)s0 * D + d];
+    for (int m = c0 + tid; m < c1; m += kRbSplitThreads)
+        best = max(best, (unsigned long long)(0xffffffffu - (uint32_t)ord[m]));
+    const int s0 = (int)(0xffffffffu - (uint32_t)cluster_max(best));
+    load_row(ua, s0);
     __syncthreads();
-    // 2-3. the landmarks: farthest from s0, then farthest from that (ties to the lower id)
+    // 2-3. the landmarks: a = farthest from s0, then b = farthest from a (ties to the lower id)
     for (int round = 0; round < 2; ++round) {
         best = 0;
-        for (int m = warp; m < n; m += kWarps) {
-            const int t = ord[r0 + m];
-            float d2 = 0.f;
-            for (int d = lane; d < D; d += 32) {
-                const float x = Uh[(long long)t * D + d] - ua[d];
-                d2 = fmaf(x, x, d2);
-            }
-            for (int o = 16; o > 0; o >>= 1) d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-            const unsigned long long key =
-                ((unsigned long long)rb_order_key(d2) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)t);
-            best = max(best, key);
+        for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+            const int t = ord[m];
+            const float d2 = rb_row_op<true>(Uh + (long long)t * D, ua, D);
+            best = max(best, ((unsigned long long)rb_order_key(d2) << 32) |
+                                 (unsigned long long)(0xffffffffu - (uint32_t)t));
         }
-        const int far = (int)(0xffffffffu - (uint32_t)(rb_block_max(best, red) & 0xffffffffull));
-        float* dst = round == 0 ? ub : ua;  // round 0: u_a into ub (then copied to ua); round 1: u_b into ua
-        for (int d = tid; d < D; d += kRbSplitThreads) dst[d] = Uh[(long long)far * D + d];
-        __syncthreads();
+        const int far = (int)(0xffffffffu - (uint32_t)(cluster_max(best) & 0xffffffffull));
         if (round == 0) {
-            for (int d = tid; d < D; d += kRbSplitThreads) ua[d] = ub[d];  // ua = u_a: the next distances
+            load_row(ub, far);  // u_a
             __syncthreads();
+            for (int d = tid; d < D; d += kRbSplitThreads) ua[d] = ub[d];
+        } else {
+            load_row(ua, far);  // u_b
         }
+        __syncthreads();
     }
-    // now ub = u_a, ua = u_b; the direction u_b - u_a
+    // ub = u_a, ua = u_b: the direction u_b - u_a
     for (int d = tid; d < D; d += kRbSplitThreads) ua[d] -= ub[d];
     __syncthreads();
     // 4. keys (projection, token id), ascending
-    for (int m = warp; m < n; m += kWarps) {
-        const int t = ord[r0 + m];
-        float p = 0.f;
-        for (int d = lane; d < D; d += 32) p = fmaf(Uh[(long long)t * D + d], ua[d], p);
-        for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-        if (lane == 0) ky[r0 + m] = ((unsigned long long)rb_order_key(p) << 32) | (uint32_t)t;
+    for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+        const int t = ord[m];
+        const float p = rb_row_op<false>(Uh + (long long)t * D, ua, D);
+        ky[m] = ((unsigned long long)rb_order_key(p) << 32) | (uint32_t)t;
     }
     __syncthreads();
-    // 5. the cut: the cap_left-th smallest key (exact radix select, 8 bits a pass)
-    if (tid == 0) {
-        s_prefix = 0;
-        s_need = cap_left;  // rank (1-based) of the largest key that goes left
-    }
-    __syncthreads();
+    // 5. the cut: the cap_left-th smallest key of the node (exact radix select,
+    //    8 bits a pass, the CTAs' histograms summed through the cluster)
+    unsigned long long prefix = 0;
+    int need = cap_left;  // rank (1-based) of the largest key that goes left
     for (int shift = 56; shift >= 0; shift -= 8) {
         for (int b = tid; b < 256; b += kRbSplitThreads) hist[b] = 0;
         __syncthreads();
-        const unsigned long long pre = s_prefix;
         const unsigned long long mask_hi = shift == 56 ? 0ull : (~0ull << (shift + 8));
-        for (int m = tid; m < n; m += kRbSplitThreads) {
-            const unsigned long long key = ky[r0 + m];
-            if ((key & mask_hi) == pre) atomicAdd(&hist[(key >> shift) & 255], 1u);
+        for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+            const unsigned long long key = ky[m];
+            if ((key & mask_hi) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1u);
+        }
+        cl.sync();
+        // bin t summed over the cluster's CTAs (same order everywhere), then
+        // one thread walks the sums; every CTA takes the same digit
+        if (tid < 256) {
+            unsigned int h = 0;
+            for (int r = 0; r < C; ++r) h += cl.map_shared_rank(hist, r)[tid];
+            hsum[tid] = h;
         }
         __syncthreads();
         if (tid == 0) {
-            int need = s_need;
-            int b = 0;
+            int b = 0, nd = need;
             for (; b < 255; ++b) {  // (the rank always falls inside: cap_left < n)
-                if (need <= (int)hist[b]) break;
-                need -= hist[b];
+                if (nd <= (int)hsum[b]) break;
+                nd -= (int)hsum[b];
             }
-            s_prefix = pre | ((unsigned long long)b << shift);
-            s_need = need;
+            s_digit = b;
+            s_need = nd;
         }
         __syncthreads();
+        prefix |= (unsigned long long)s_digit << shift;
+        need = s_need;
+        cl.sync();  // the histograms are read before the next pass clears them
     }
-    const unsigned long long cut = s_prefix;  // keys <= cut go left (exactly cap_left: keys are distinct)
-    // 6. stable split: contiguous chunks per thread, counts scanned in thread order
-    const int per = (n + kRbSplitThreads - 1) / kRbSplitThreads;
-    const int m0 = min(n, tid * per), m1 = min(n, m0 + per);
+    const unsigned long long cut = prefix;  // keys <= cut go left (exactly cap_left: keys are distinct)
+    // 6. stable split: contiguous runs per thread, counts scanned in thread,
+    //    then CTA (cluster rank) order
+    const int nc = c1 - c0;
+    const int per = (nc + kRbSplitThreads - 1) / kRbSplitThreads;
+    const int m0 = c0 + min(nc, tid * per), m1 = c0 + min(nc, tid * per + per);
     int nl = 0;
-    for (int m = m0; m < m1; ++m) nl += ky[r0 + m] <= cut;
+    for (int m = m0; m < m1; ++m) nl += ky[m] <= cut;
     scan[tid] = nl;
     __syncthreads();
     if (tid == 0) {
@@ -341,17 +417,26 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const fl
             scan[t] = run;
             run += c;
         }
+        s_count = run;
     }
-    __syncthreads();
-    int wl = scan[tid], wr = cap_left + (m0 - scan[tid]);
+    cl.sync();
+    int left_before = 0, right_before = 0;
+    for (int r = 0; r < rank; ++r) {
+        const int lr = *cl.map_shared_rank(&s_count, r);
+        const int nr = (int)((long long)n * (r + 1) / C) - (int)((long long)n * r / C);
+        left_before += lr;
+        right_before += nr - lr;
+    }
+    int wl = left_before + scan[tid];
+    int wr = cap_left + right_before + (m0 - c0 - scan[tid]);
     for (int m = m0; m < m1; ++m) {
-        const unsigned long long key = ky[r0 + m];
+        const unsigned long long key = ky[m];
         const int t = (int)(key & 0xffffffffull);
         if (key <= cut) tp[r0 + wl++] = t;
         else tp[r0 + wr++] = t;
     }
-    __syncthreads();
-    for (int m = tid; m < n; m += kRbSplitThreads) ord[r0 + m] = tp[r0 + m];
+    cl.sync();  // every CTA's writes to tp are visible to the cluster
+    for (int m = c0 + tid; m < c1; m += kRbSplitThreads) ord[m] = tp[m];
 }
 
 // Members of each block in ascending token id: CTA (block, head), an odd-even
@@ -384,7 +469,8 @@ __global__ void __launch_bounds__(512) reblock_leaf_sort_kernel(int32_t* __restr
 }
 
 // ------------------------------------------------------------------ permute
-// Warp per destination row; 4-byte words (D * sizeof(T) % 4 == 0) or elements.
+// Warp per row; 16-byte vectors, 4-byte words or elements, as the row size
+// and alignment allow.
 template <typename T>
 __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__ src, T* __restrict__ dst, int N,
                                                            int D, int n_prefix, const int32_t* __restrict__ perm,
@@ -409,7 +495,12 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
     }
     const T* sr = src + ((long long)bh * N + s) * D;
     T* dr = dst + ((long long)bh * N + d) * D;
-    if ((D * sizeof(T)) % 4 == 0 && ((uintptr_t)src & 3) == 0 && ((uintptr_t)dst & 3) == 0) {
+    if ((D * sizeof(T)) % 16 == 0 && ((uintptr_t)src & 15) == 0 && ((uintptr_t)dst & 15) == 0) {
+        const int vecs = D * (int)sizeof(T) / 16;
+        const uint4* sv = reinterpret_cast<const uint4*>(sr);
+        uint4* dv = reinterpret_cast<uint4*>(dr);
+        for (int w = lane; w < vecs; w += 32) dv[w] = sv[w];
+    } else if ((D * sizeof(T)) % 4 == 0 && ((uintptr_t)src & 3) == 0 && ((uintptr_t)dst & 3) == 0) {
         const int words = D * (int)sizeof(T) / 4;
         const uint32_t* sw = reinterpret_cast<const uint32_t*>(sr);
         uint32_t* dw = reinterpret_cast<uint32_t*>(dr);
@@ -423,7 +514,7 @@ struct RbWorkspace {
     float* part;
     float* M;
     float* L;
-    float* U;
+    __nv_bfloat16* U;
     unsigned long long* keys;
     int32_t* tmp;
 };
@@ -439,7 +530,7 @@ static RbWorkspace rb_carve(void* ws, int BH, int Nv, int D) {
     w.part = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * kRbSplits * D * D));
     w.M = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * D * D));
     w.L = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * D * D));
-    w.U = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * Nv * D));
+    w.U = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * (size_t)BH * Nv * D));
     w.keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)BH * Nv));
     w.tmp = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)BH * Nv));
     return w;
@@ -461,7 +552,7 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
     if (rc != BSA_OK) return rc;
     reblock_moment_reduce<<<dim3((D * D + 255) / 256, BH), 256, 0, st>>>(w.part, D, Nv, w.M);
     if ((rc = check_launch("reblock_moment_reduce")) != BSA_OK) return rc;
-    const size_t chol_smem = sizeof(double) * (size_t)D * (D + 1);
+    const size_t chol_smem = sizeof(float) * (size_t)D * (D + 1);
     if (chol_smem > 48 * 1024)
         cudaFuncSetAttribute(reblock_cholesky_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem);
     reblock_cholesky_kernel<<<BH, kRbMaxD, chol_smem, st>>>(w.M, D, ridge, w.L);
@@ -477,8 +568,24 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
     int levels = 0;
     while ((1 << levels) < NB) ++levels;  // depth of the binary tree over NB blocks
     for (int l = 0; l < levels; ++l) {
-        reblock_split_kernel<<<dim3(1u << l, BH), kRbSplitThreads, 0, st>>>(w.U, Nv, D, block, NB, l, perm, w.tmp,
-                                                                           w.keys);
+        // CTAs per node: about 4096 members each, a power of two up to 8
+        const long long per_node = (long long)Nv >> l;
+        int C = 1;
+        while (C < 8 && per_node / (2 * C) >= 4096) C *= 2;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((1u << l) * C, BH);
+        cfg.blockDim = dim3(kRbSplitThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, reblock_split_kernel, (const __nv_bfloat16*)w.U, Nv, D, block, NB, l, perm, w.tmp,
+                           w.keys);
         if ((rc = check_launch("reblock_split_kernel")) != BSA_OK) return rc;
     }
     reblock_leaf_sort_kernel<<<dim3(NB, BH), 512, 0, st>>>(perm, Nv, block);
@@ -499,7 +606,7 @@ size_t bsa_reblock_workspace(int BH, int N, int D, int n_prefix) {
     const size_t Nv = (size_t)(N - n_prefix);
     auto r = [](size_t b) { return (b + 255) / 256 * 256; };
     return r(sizeof(float) * (size_t)BH * kRbSplits * D * D) + 2 * r(sizeof(float) * (size_t)BH * D * D) +
-           r(sizeof(float) * (size_t)BH * Nv * D) + r(sizeof(unsigned long long) * (size_t)BH * Nv) +
+           r(sizeof(__nv_bfloat16) * (size_t)BH * Nv * D) + r(sizeof(unsigned long long) * (size_t)BH * Nv) +
            r(sizeof(int32_t) * (size_t)BH * Nv);
 }
 
