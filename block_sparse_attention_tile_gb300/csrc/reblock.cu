@@ -142,16 +142,22 @@ __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* 
 }
 
 // ------------------------------------------------------------------ features
-// CTA (64-token tile, head); thread (ty, tx) computes tokens 4ty.. and
-// channels 8tx.. of K L (L lower-triangular, staged in shared memory), then
-// the token's 16 threads reduce the squared norm.
+// CTA (64-token tile, head); thread (tx, ty) = (tid / 16, tid % 16) computes
+// channels 8tx.. of tokens ty + 16a (a < 4) of K L.  L is lower-triangular, so channel
+// c only needs rows i >= c: with tx shared by a warp's two halves, the loop
+// starts at that warp's first nonzero row.  The K tile rows are padded (one
+// float) so that the 16 rows a warp reads at one column (ty + 16a) fall in 16
+// banks.
+// Then the token's 16 threads reduce the squared norm.
+constexpr int kRbKs = kRbMaxD + 1;
+
 template <typename T>
 __global__ void __launch_bounds__(256) reblock_features_kernel(const T* __restrict__ k, int N, int D, int n_prefix,
                                                                const float* __restrict__ L,
                                                                __nv_bfloat16* __restrict__ U) {
     extern __shared__ __align__(16) float fs[];
-    float* Ls = fs;                    // [kRbMaxD][kRbMaxD]
-    float* ks = Ls + kRbMaxD * kRbMaxD;  // [64][kRbMaxD]
+    float* Ls = fs;                      // [kRbMaxD][kRbMaxD]
+    float* ks = Ls + kRbMaxD * kRbMaxD;  // [64][kRbKs]
     const int bh = blockIdx.y, t0 = blockIdx.x * 64, tid = threadIdx.x;
     const int Nv = N - n_prefix;
     const float* Lh = L + (long long)bh * D * D;
@@ -162,35 +168,47 @@ __global__ void __launch_bounds__(256) reblock_features_kernel(const T* __restri
     const T* kh = k + ((long long)bh * N + n_prefix) * D;
     for (int e = tid; e < 64 * kRbMaxD; e += 256) {
         const int r = e / kRbMaxD, d = e % kRbMaxD;
-        ks[e] = (t0 + r < Nv && d < D) ? to_f32(kh[(long long)(t0 + r) * D + d]) : 0.f;
+        ks[r * kRbKs + d] = (t0 + r < Nv && d < D) ? to_f32(kh[(long long)(t0 + r) * D + d]) : 0.f;
     }
     __syncthreads();
-    const int ty = tid / 16, tx = tid % 16;
+    const int tx = tid / 16, ty = tid % 16;
+    const int i0 = 8 * (tx & ~1);  // the warp's first row with a nonzero entry in its channels
     float acc[4][8];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-    for (int i = 0; i < D; ++i) {
+    for (int i = i0; i < D; ++i) {
         const float4 l0 = *reinterpret_cast<const float4*>(Ls + i * kRbMaxD + 8 * tx);
         const float4 l1 = *reinterpret_cast<const float4*>(Ls + i * kRbMaxD + 8 * tx + 4);
         const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const float x = ks[(4 * ty + a) * kRbMaxD + i];
+            const float x = ks[(ty + 16 * a) * kRbKs + i];
 #pragma unroll
             for (int b = 0; b < 8; ++b) acc[a][b] = fmaf(x, lv[b], acc[a][b]);
         }
     }
+    // the squared norm of each token: its channels are spread over the 16 tx
+    // values, i.e. over lanes 16 apart in two warps' worth of threads -> via
+    // shared memory
+    __syncthreads();
+    float* part = ks;  // reuse: [64][16] partial sums
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
         float ss = 0.f;
 #pragma unroll
         for (int b = 0; b < 8; ++b) ss = fmaf(acc[a][b], acc[a][b], ss);
+        part[(ty + 16 * a) * 16 + tx] = ss;
+    }
+    __syncthreads();
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);  // the row's 16 threads
+    for (int a = 0; a < 4; ++a) {
+        const int r = ty + 16 * a;
+        float ss = 0.f;
+        for (int x = 0; x < 16; ++x) ss += part[r * 16 + x];  // fixed order
         const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
-        const int t = t0 + 4 * ty + a;
+        const int t = t0 + r;
         if (t < Nv) {
             __nv_bfloat16* ur = U + ((long long)bh * Nv + t) * D;
 #pragma unroll
@@ -557,7 +575,7 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
         cudaFuncSetAttribute(reblock_cholesky_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem);
     reblock_cholesky_kernel<<<BH, kRbMaxD, chol_smem, st>>>(w.M, D, ridge, w.L);
     if ((rc = check_launch("reblock_cholesky_kernel")) != BSA_OK) return rc;
-    const size_t feat_smem = sizeof(float) * (size_t)(kRbMaxD * kRbMaxD + 64 * kRbMaxD);
+    const size_t feat_smem = sizeof(float) * (size_t)(kRbMaxD * kRbMaxD + 64 * kRbKs);
     cudaFuncSetAttribute(reblock_features_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)feat_smem);
     reblock_features_kernel<T><<<dim3((Nv + 63) / 64, BH), 256, feat_smem, st>>>((const T*)k, N, D, n_prefix, w.L,
                                                                                   w.U);
