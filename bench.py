@@ -579,12 +579,30 @@ class BlockWorkload:
     def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=4):
         """End-to-end step with host buffers, pipelined by heads: chunk c's
         inputs are copied in on a copy stream while chunk c-1 computes, and each
-        chunk's output is copied out as soon as it is done."""
+        chunk's output is copied out as soon as it is done.  Chunks of 1, 2, then
+        heads_per_chunk heads, and one head last."""
         torch = self.torch
         g = self.geom
         comp = torch.cuda.current_stream()
         h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-        chunks = [(h0, min(self.BH, h0 + heads_per_chunk)) for h0 in range(0, self.BH, heads_per_chunk)]
+        # graded chunks: a one-head first chunk starts the compute early and a
+        # one-head last chunk leaves little output to copy after it
+        sizes = []
+        left = self.BH
+        for first in (1, 2):
+            if left > 1:
+                sizes.append(first)
+                left -= first
+        tail = [1] if left > 2 else []
+        left -= sum(tail)
+        while left > 0:
+            sizes.append(min(heads_per_chunk, left))
+            left -= sizes[-1]
+        sizes += tail
+        chunks, h0 = [], 0
+        for n_h in sizes:
+            chunks.append((h0, h0 + n_h))
+            h0 += n_h
         per_head = self.J * self.w["M"] * self.w["D"]
         pk = (torch.empty((3 * heads_per_chunk * per_head,), dtype=self.dtype, device=self.dev)
               if self.packed is not None else None)
