@@ -160,3 +160,129 @@ def test_msa_prefill_full_size():
     # the sink block is shared by every query of every KV head: it must be split into chunks
     assert row_ptr[1] - row_ptr[0] == T and sum(1 for c in chunks if c[0] == 0) == math.ceil(T / (2 * S * BS))
     _check_token_workload(q, k, v, idx, cnt, BS, {"kvouter": (o_kv, l_kv), "qouter": (o_q, l_q)}, 24, 404)
+
+
+# ---------------------------------------------------------------- the widened rows at their bench sizes
+
+def test_spark_reweight_full_size():
+    """The spark_summary inputs with Spark-Reweight summaries (weighted key and value
+    at the head's mean video query, log-mass bias) for the unselected blocks."""
+    pl = _pl()
+    T, H, W, n_text, D = 16, 32, 64, 1024, 128
+    q, k, v = synthetic.cluster_qkv(24, n_text, T * H * W, D, 505, torch.bfloat16, device=DEV)
+    perm = synthetic.permutation(T * H * W, 506)
+    geom = pl.Geometry(T, H, W, M=128, n_prefix=n_text, perm=torch.as_tensor(perm, device=DEV))
+    res = pl.block_sparse_attention(q, k, v, geom, 26, summary=True, reweight=True)
+    torch.cuda.synchronize()
+    blocks = oracle_blocks(T, H, W, 1, 1, 1, 128, n_text, perm)
+    P, scale = 8, D ** -0.5
+    rng = np.random.default_rng(515)
+    for h in (5, 17):
+        Q, K, V = f64(q[h]), f64(k[h]), f64(v[h])
+        qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        gi, gn = res.q2k_idx[h].cpu().numpy(), res.q2k_num[h].cpu().numpy()
+        check_route(gi, gn, oracle.routing_scores(qbar[P:], kbar[P:], D), 26)
+        kt, vt, b, a = oracle.reweight_summaries(Q, K, V, blocks, scale, prefix_blocks=P,
+                                                 round_key=oracle.bf16_round)
+        gb = res.summary_bias[h].cpu().double().numpy()[P:]
+        # b uses the bf16-stored key: where the float32 and the exact k~ round to neighbouring
+        # bf16 values, b moves by at most scale * |a_d| * ulp(k~_d)
+        tol_b = scale * ((2.0 ** -7 * np.abs(kt)) @ np.abs(a)) + 1e-4 * (1.0 + np.abs(b))
+        assert np.all(np.abs(gb - b) <= tol_b), np.abs(gb - b).max()
+        qbs = [1] + sorted((P + rng.choice(256, 8, replace=False)).tolist())
+        O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kt, vt, scale, prefix_blocks=P,
+                                        query_blocks=qbs, block_bias=b)
+        rows = np.concatenate([blocks[i] for i in qbs])
+        assert_close(f64(res.out[h])[rows], O[rows], torch.bfloat16, "head %d" % h)
+        # the summary keys are stored in bf16: a virtual logit moves by at most scale*|q|*|kt - bf16(kt)|
+        tol = 2e-3 + scale * np.linalg.norm(Q, axis=1).max() * np.linalg.norm(kt - oracle.bf16_round(kt), axis=1).max()
+        assert np.abs(res.lse[h].cpu().numpy()[rows] - L[rows]).max() <= tol
+
+
+def test_r2v_full_size():
+    """1024 text tokens, two reference videos (8,48,80), the target (30,48,80) in (4,4,8)
+    windows; region-grouped TopK keeping 24, 24, 96 blocks (the r2v_bsa bench workload)."""
+    pl = _pl()
+    segs, budgets, D = [1024, (8, 48, 80), (8, 48, 80), (30, 48, 80)], [24, 24, 96], 128
+    q, k, v = synthetic.segment_qkv(24, segs, D, 707, torch.bfloat16, device=DEV)
+    geom = pl.SegmentGeometry(segs, 4, 4, 8, M=128)
+    res = pl.block_sparse_attention(q, k, v, geom, budgets)
+    torch.cuda.synchronize()
+    blocks, P, spans = oracle.tile_segments(geom.segments, 4, 4, 8, 128)
+    assert np.array_equal(res.index_map.cpu().numpy(), oracle.index_map(blocks, 128))
+    rspans = [(lo - P, hi - P) for lo, hi in spans]
+    rng = np.random.default_rng(707)
+    for h in (2, 19):
+        Q, K, V = f64(q[h]), f64(k[h]), f64(v[h])
+        qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+        E = oracle.routing_scores(qbar[P:], kbar[P:], D)
+        want_idx, want_num = oracle.route_grouped(E, rspans, budgets, sum(budgets))
+        gi, gn = res.q2k_idx[h].cpu().numpy(), res.q2k_num[h].cpu().numpy()
+        assert np.array_equal(gn, want_num)
+        ties = set()
+        for kr, (lo, hi) in zip(budgets, rspans):
+            ties |= set(oracle.near_tie_rows(E[:, lo:hi], kr, 1e-5).tolist())
+        bad = [i for i in range(E.shape[0]) if not np.array_equal(gi[i], want_idx[i])]
+        assert set(bad) <= ties, sorted(set(bad) - ties)[:10]
+        # a prefix row (dense over all 177664 keys) and query blocks of each video region
+        qbs = [3] + [int(lo + rng.integers(hi - lo)) for lo, hi in spans for _ in range(3)]
+        O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, D ** -0.5, prefix_blocks=P, query_blocks=qbs)
+        rows = np.concatenate([blocks[i] for i in qbs])
+        assert_close(f64(res.out[h])[rows], O[rows], torch.bfloat16, "head %d" % h)
+        assert np.abs(res.lse[h].cpu().numpy()[rows] - L[rows]).max() <= 2e-3
+
+
+def test_video_dit_coarse_full_size():
+    """The video-DiT workload plus the gated coarse branch softmax(E) V_bar (per head and
+    channel gate, as the video_dit_coarse bench workload)."""
+    pl = _pl()
+    T, H, W, D = 30, 48, 80, 128
+    q, k, v = synthetic.video_qkv(1, 24, T, H, W, D, 202, torch.bfloat16, device=DEV, field=True)
+    gate = synthetic.normal((24, D), 273, DEV)
+    geom = pl.Geometry(T, H, W, 4, 4, 8, M=128)
+    res = pl.block_sparse_attention(q, k, v, geom, 96, coarse_gate=gate)
+    torch.cuda.synchronize()
+    blocks = oracle.tile_3d(T, H, W, 4, 4, 8)
+    rng = np.random.default_rng(273)
+    for h in (7, 22):
+        Q, K, V = f64(q[h]), f64(k[h]), f64(v[h])
+        qbar, kbar, vbar = (oracle.pool_blocks(X, blocks) for X in (Q, K, V))
+        E = oracle.routing_scores(qbar, kbar, D)
+        C = oracle.coarse_attention(E, vbar)
+        assert np.abs(res.coarse[h].cpu().numpy() - C).max() <= 1e-5 * max(1.0, np.abs(vbar).max())
+        gi, gn = res.q2k_idx[h].cpu().numpy(), res.q2k_num[h].cpu().numpy()
+        check_route(gi, gn, E, 96)
+        qbs = [959] + sorted(rng.choice(960, 8, replace=False).tolist())
+        O, L = oracle.block_sparse_attention(Q, K, V, blocks, gi, gn, D ** -0.5, query_blocks=qbs)
+        O = oracle.coarse_output(O, C, gate[h].double().cpu().numpy(), blocks, 0)
+        rows = np.concatenate([blocks[i] for i in qbs])
+        assert_close(f64(res.out[h])[rows], O[rows], torch.bfloat16, "head %d" % h)
+
+
+def test_spark_reblock_full_size():
+    """The spark_summary inputs in the Spark-Reblock layout (built on the GPU per head),
+    exact + summary attention, outputs scattered back to the original order."""
+    pl = _pl()
+    n_text, Nv, D, M = 1024, 32768, 128, 128
+    q, k, v = synthetic.cluster_qkv(24, n_text, Nv, D, 505, torch.bfloat16, device=DEV)
+    res = pl.reblocked_attention(q, k, v, n_text, M, 26, summary=True)
+    torch.cuda.synchronize()
+    P = n_text // M
+    rng = np.random.default_rng(525)
+    for h in (0, 13):
+        ph = res.perm[h].cpu().numpy()
+        assert np.array_equal(np.sort(ph), np.arange(Nv))
+        assert all(np.all(np.diff(ph[s:s + M]) > 0) for s in range(0, Nv, M))
+        blocks = oracle.tile_prefix(n_text, M) + [n_text + ph[s:s + M].astype(np.int64) for s in range(0, Nv, M)]
+        Q, K, V = f64(q[h]), f64(k[h]), f64(v[h])
+        qbar, kbar, vbar = (oracle.pool_blocks(X, blocks) for X in (Q, K, V))
+        gi, gn = res.inner.q2k_idx[h].cpu().numpy(), res.inner.q2k_num[h].cpu().numpy()
+        check_route(gi, gn, oracle.routing_scores(qbar[P:], kbar[P:], D), 26)
+        qbs = [2] + sorted((P + rng.choice(256, 8, replace=False)).tolist())
+        O, L = oracle.summary_attention(Q, K, V, blocks, gi, gn, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
+                                        query_blocks=qbs)
+        rows = np.concatenate([blocks[i] for i in qbs])
+        assert_close(f64(res.out[h])[rows], O[rows], torch.bfloat16, "head %d" % h)
+        kr = np.abs(kbar[P:] - oracle.bf16_round(kbar[P:]))
+        tol = 2e-3 + D ** -0.5 * np.linalg.norm(Q, axis=1).max() * np.linalg.norm(kr, axis=1).max()
+        assert np.abs(res.lse[h].cpu().numpy()[rows] - L[rows]).max() <= tol
