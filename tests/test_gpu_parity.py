@@ -485,6 +485,36 @@ def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf):
     assert np.abs(got_l - lb[written]).max() <= (1e-5 if dtype == torch.float32 else 2e-3)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_nsa_empty_selections(lib, dtype):
+    """Rows whose count is 0 select nothing: output 0 and LSE -inf on both
+    orders (the KV-outer combine sees no slot); the other rows as the oracle."""
+    pl = _pipeline()
+    B, T, HQ, H, D, BS, S = 1, 320, 32, 2, 128 if dtype == torch.bfloat16 else 64, 64, 8
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 331, dtype)
+    rng = np.random.default_rng(331)
+    cnt = cnt.copy()
+    cnt[0, rng.choice(T, 40, replace=False), 0] = 0  # KV head 0 of 40 positions: nothing selected
+    cnt[0, :5, :] = 0                                 # the first positions: nothing on either head
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    idx_d, cnt_d = torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV)
+    o_q, l_q = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    o_kv, l_kv, _, _, _ = pl.kvouter_attention(qd, kd, vd, idx_d, cnt_d, BS,
+                                               obuf_dtype=torch.float32 if dtype == torch.float32 else torch.bfloat16)
+    torch.cuda.synchronize()
+    O, L = _oracle_nsa(q, k, v, idx, cnt, BS, 0)
+    G = HQ // H
+    empty = np.repeat(cnt[0] == 0, G, axis=1)  # [T, HQ]
+    for name, o, l in (("qouter", o_q, l_q), ("kvouter", o_kv, l_kv)):
+        go, gl = f64(o[0]), l[0].cpu().numpy()
+        assert np.all(go[empty] == 0.0), name
+        assert np.all(np.isneginf(gl[empty])), name
+        assert np.all(np.isneginf(L[empty]))
+        assert_close(go[~empty], O[~empty], dtype, name)
+        tol = 1e-5 if dtype == torch.float32 else 2e-3
+        assert np.abs(gl[~empty] - L[~empty]).max() <= tol
+
+
 @pytest.mark.parametrize("HQ,H,BS", [(16, 2, 64), (64, 1, 128), (128, 1, 64)])
 def test_kvouter_group_sizes(lib, HQ, H, BS):
     """The tensor-core partial pass at G = 8, 64, 128 query heads per KV head
