@@ -42,6 +42,8 @@ _SIGS = {
     "bsa_version": (I, []),
     "bsa_last_error": (ctypes.c_char_p, []),
     "bsa_device_status": (I, [P]),
+    "bsa_get_device_status": (I, [P]),
+    "bsa_last_error_string": (ctypes.c_char_p, []),
     "bsa_tile_count": (I, [I, I, I, I, I, I, I, I, I]),
     "bsa_tile_map": (I, [I, I, I, I, I, I, I, P, I, P, P, P]),
     "bsa_budget": (I, [I, ctypes.c_double]),

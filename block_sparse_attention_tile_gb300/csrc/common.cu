@@ -77,6 +77,10 @@ bsa_status bsa_device_status(void* stream) {
     return static_cast<bsa_status>(v);
 }
 
+bsa_status bsa_get_device_status(void* stream) { return bsa_device_status(stream); }
+
+const char* bsa_last_error_string(void) { return bsa_last_error(); }
+
 int bsa_budget(int J, double sparsity) {
     if (J < 1 || !(sparsity >= 0.0 && sparsity <= 1.0)) return -1;
     double r = std::ceil((1.0 - sparsity) * (double)J - 1e-9);

@@ -68,6 +68,11 @@ const char* bsa_last_error(void);
  * BSA_ERR_CUDA if the synchronisation itself failed. */
 bsa_status bsa_device_status(void* stream);
 
+/* The same two calls under the names of the interface the pages imply
+ * (a status query that synchronises, a thread-local message). */
+bsa_status bsa_get_device_status(void* stream);
+const char* bsa_last_error_string(void);
+
 /* ------------------------------------------------------------------ a1 ----
  * Tile map.  [VSA] §1: index(t,y,x) = t*H*W + y*W + x; the (bT,bH,bW) grid
  * of blocks numbered row-major, J = ceil(T/bT)*ceil(H/bH)*ceil(W/bW); edge

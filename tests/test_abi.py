@@ -108,6 +108,9 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     rc = lib.bsa_permute_rows(1, 1, 1, 2, 10, 4, 2, 1, 0, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "differ" in bsa.bsa_last_error()
     assert bsa.bsa_reblock_workspace(2, 100, 8, 100) == 0  # no video tokens
+    # the aliases answer as the primary names
+    lib.bsa_route_topk(None, None, 1, 4, 2, 8, 2, 1.0, 4, None, None, None, 0, None)
+    assert lib.bsa_last_error_string() == lib.bsa_last_error() != b""
     assert bsa.bsa_version() >= 100
 
 
