@@ -187,6 +187,9 @@ __global__ void __launch_bounds__(256) token_attn_simt_kernel(
         L.qpos[r] = t;
         L.orow[r] = r;
     }
+    // the rows' output slots are read by other warps, also when no block is
+    // selected (the key loop below then holds no barrier)
+    __syncthreads();
     const int nwarps = blockDim.x >> 5;
     const int rows_per_warp = (G + nwarps - 1) / nwarps;
     const int warp_row0 = warp * rows_per_warp;

@@ -10,8 +10,15 @@
 // unselected routed block adds one virtual key (its mean key and value) with
 // logit bias log(n_j), folded into the same online softmax.
 //
-// Design (ours, for sm_103a).  One CTA per (head, query block), 12 warps,
-// one CTA per SM (TMEM: S0 [0,128), S1 [128,256), O [256,384) of 512 columns).
+// Design (ours, for sm_103a).  A persistent grid, one CTA per SM, 12 warps;
+// each CTA takes work items (one (head, query block) pair each) until none
+// are left, so one item's table, Q load and first QK products overlap the end
+// of the one before.  TMEM (all 512 columns): S0 [0,128), S1 [128,256),
+// O_0 [256,384), O_1 [384,512).
+//   warp 3      scheduler: takes the next item (a counter in global memory,
+//               or every gridDim.x-th item) and writes its key-tile table
+//               (packed tile sources, valid rows, summary log-masses) into the
+//               spare one of two table buffers.
 //   warps 0, 2  producers: TMA loads straight from the BHSD tensors into
 //               128-byte swizzled K-major tiles, no pack pass: a (bT,bH,bW)
 //               window is ONE box of a 5-D (D, W, H, T, head) tensor map per
@@ -24,20 +31,17 @@
 //               ~8x faster than gathering.  Warp 0 loads Q and then the K tiles
 //               into a 3-stage K ring, warp 2 the V tiles into a 2-stage V ring:
 //               a K tile is free as soon as S_j is done, so K runs about three
-//               tiles ahead (one shared ring let it start only one tile ahead,
-//               and the MMA issuer waited ~0.45 us per tile for K).
-//   warp 1      TMEM owner and single-thread MMA issuer: S0, S1, then
-//               PV_j, S_{j+2} for every j.  S is double buffered, so QK of tile
-//               j+1 (and j+2) runs while the softmax works on tile j.
-//               P_j is read from TMEM, where the softmax wrote it over S_j as
-//               packed bf16 (the A operand of P V); V is an MN-major operand.
-//   warps 4-7   softmax of key columns 0..63, warps 8-11 of columns 64..127,
-//               one query row per thread in each half: the two halves swap
-//               their row maxima through shared memory once per tile, then
-//               each exponentiates and writes its half of P; the running max
-//               is updated lazily (O in TMEM is rescaled only when the max
-//               grows by more than 2^8), l is kept per half and added at the
-//               end; epilogue O / l -> bf16 -> global through the index map.
+//               tiles ahead.
+//   warp 1      TMEM owner and single-thread MMA issuer: per item S_0, S_1,
+//               then PV_j, S_{j+2} for every j.  P_j is read from TMEM, where
+//               the softmax wrote it over S_j as packed bf16 (the A operand of
+//               P V); V is an MN-major operand.
+//   warps 4-7   softmax of the even key tiles into O_0, warps 8-11 of the odd
+//               ones into O_1, one query row per thread: each warpgroup keeps
+//               its own running max (updated lazily: O_w in TMEM is rescaled
+//               only when the max grows by more than 2^8) and sum; at the end
+//               of the item the two are merged exactly and each warpgroup
+//               writes half of the output columns through the index map.
 // Every mbarrier wait is bounded (2 s): on expiry the CTA raises
 // BSA_ERR_TIMEOUT, stops issuing, drains its own copies and MMAs, frees TMEM.
 #include <cuda.h>
@@ -45,6 +49,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -64,26 +69,31 @@ constexpr uint32_t kTileBytes = kBN * kHD * 2;       // 32 KB
 constexpr uint32_t kHalfBytes = kTileBytes / 2;      // 16 KB: 128 rows x 64 cols
 constexpr uint64_t kWaitNs = 2000000000ull;          // bounded waits: 2 s
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
-constexpr int kSoftmaxBarrier = 1;                   // named barrier of the 256 softmax threads
 constexpr int kRegsLow = 64, kRegsHigh = 216, kRegsLaunch = 168;  // setmaxnreg split (x 128 / x 256 threads)
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kRegsLaunch, "register split exceeds the launch");
 
-// shared memory map (offsets from a 1024-byte aligned base)
+// shared memory map (offsets from a 1024-byte aligned base).  The key-tile
+// table of a work item is double buffered: warp 3 fills the table of the next
+// item while the other warps work on the current one.
+constexpr uint32_t TAB_SRC = 0;                                 // int4[kMaxList]: packed tile sources
+constexpr uint32_t TAB_INFO = TAB_SRC + 16 * kMaxList;          // int[kMaxList]: n_j | (summary index + 1) << 8
+constexpr uint32_t TAB_BIAS = TAB_INFO + 4 * kMaxList;          // float[kMaxVirtual*128]: summary log-masses
+constexpr uint32_t TAB_HDR = TAB_BIAS + 4 * kMaxVirtual * kBN;  // int[8]: query block (-1: no more work), head, n, n_q
+constexpr uint32_t kTabBytes = TAB_HDR + 32;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_RING = OFF_Q + kTileBytes;
-constexpr uint32_t OFF_LIST = OFF_RING + kStages * kTileBytes;  // int[kMaxList]: tile ids (<0: virtual)
-constexpr uint32_t OFF_NVALID = OFF_LIST + 4 * kMaxList;        // int[kMaxList]
-constexpr uint32_t OFF_BIAS = OFF_NVALID + 4 * kMaxList;        // float[kMaxVirtual*128]
-constexpr uint32_t OFF_SEL = OFF_BIAS + 4 * kMaxVirtual * kBN;  // uint32[32]
-constexpr uint32_t OFF_XCH = OFF_SEL + 4 * 32;                  // float[3][2 halves][128]: maxima of
-                                                                // tiles of each parity, then l
-constexpr uint32_t OFF_SRC = OFF_XCH + 4 * 3 * 2 * kBM;        // int4[kMaxList]: packed tile sources
-constexpr uint32_t OFF_BAR = OFF_SRC + 16 * kMaxList;
-constexpr int BAR_Q = 0, BAR_FULL = 1, BAR_EMPTY = BAR_FULL + kStages, BAR_SF = BAR_EMPTY + kStages,
-              BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2, BAR_DRAIN = BAR_OF + 2,
-              NBAR = BAR_DRAIN + 1;
+constexpr uint32_t OFF_TAB = OFF_RING + kStages * kTileBytes;
+constexpr uint32_t OFF_SEL = OFF_TAB + 2 * kTabBytes;           // uint32[32]: selected-block bits (warp 3)
+constexpr uint32_t OFF_XCH = OFF_SEL + 4 * 32;                  // float[2 items][m, l][2 warpgroups][128]
+constexpr uint32_t OFF_BAR = OFF_XCH + 4 * 2 * 2 * 2 * kBM;
+constexpr int BAR_QFULL = 0, BAR_QFREE = 1, BAR_FULL = 2, BAR_EMPTY = BAR_FULL + kStages,
+              BAR_SF = BAR_EMPTY + kStages, BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2, BAR_OFREE = BAR_OF + 1,
+              BAR_TFULL = BAR_OFREE + 1, BAR_TFREE = BAR_TFULL + 2, BAR_XCH = BAR_TFREE + 2,
+              BAR_DRAIN = BAR_XCH + 1, NBAR = BAR_DRAIN + 1;
+constexpr int kTabUsers = 3 + 8;  // warps 0, 1, 2 and the eight softmax warps release a table
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;               // tmem base, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;           // + alignment slack
+static_assert(kTabBytes % 16 == 0, "table alignment");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 struct Params {
@@ -103,6 +113,8 @@ struct Params {
     int T, H, W, bT, bH, bW, nH, nW;
     int packed;       // Q/K/V also given in block order: every tile is one box
     const float* sbias;  // summary biases [BH, J] (natural log), or null for log n_j
+    int items;           // work items: (head, query block) pairs, head-major
+    unsigned* sched;     // next item to take (zero at launch), or null: every gridDim.x-th item
 };
 
 // Where a 128-row tile comes from: gathered rows (mode 0), a box of 128
@@ -142,10 +154,12 @@ __device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int b
     return s;
 }
 
-// A tile source packed in 16 bytes for the producer's table:
-// x = mode | (virtual << 2), y = c1, z = c2 | (c3 << 16), w = c4.
-__device__ __forceinline__ int4 pack_src(const TileSrc& s, bool virt) {
-    return make_int4(s.mode | (virt ? 4 : 0), s.c1, (s.c2 & 0xffff) | (s.c3 << 16), s.c4);
+// A tile source packed in 16 bytes for the producers' table: boxes as
+// x = mode | (summary << 2), y = c1, z = c2 | (c3 << 16), w = c4; gathered
+// tiles (mode 0) as x = 0, y = block, z = its valid rows.
+__device__ __forceinline__ int4 pack_src(const TileSrc& s, int blk, int nv) {
+    if (s.mode == 0) return make_int4(0, blk, nv, 0);
+    return make_int4(s.mode | (blk < 0 ? 4 : 0), s.c1, (s.c2 & 0xffff) | (s.c3 << 16), s.c4);
 }
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
@@ -162,9 +176,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-__device__ __forceinline__ void named_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -177,27 +188,21 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
-    int* list = reinterpret_cast<int*>(sm + OFF_LIST);
-    int* nvalid = reinterpret_cast<int*>(sm + OFF_NVALID);
-    float* bias = reinterpret_cast<float*>(sm + OFF_BIAS);
     uint32_t* selbits = reinterpret_cast<uint32_t*>(sm + OFF_SEL);
     float* xch = reinterpret_cast<float*>(sm + OFF_XCH);
     uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     const uint32_t bar0 = base + OFF_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    auto tab = [&](int b) { return sm + OFF_TAB + (uint32_t)b * kTabBytes; };
 
-    const int qb = blockIdx.x;
-    const int bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int J = prm.J, P = prm.P, Jr = J - P;
-    const int nq = prm.block_sizes[qb];
-    if (nq <= 0) return;  // an empty block has no query rows
-    const bool dense_row = qb < P;
 
-    // ---- prologue: barriers, TMEM, the key-tile list
+    // ---- prologue: barriers and TMEM, once per CTA
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(BAR_Q), 1);
+        ptx::mbar_init(bar(BAR_QFULL), 1);
+        ptx::mbar_init(bar(BAR_QFREE), 1);
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(BAR_FULL + s), 1);
             ptx::mbar_init(bar(BAR_EMPTY + s), 1);
@@ -205,9 +210,12 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(BAR_SF + b), 1);
             ptx::mbar_init(bar(BAR_PF + b), kBM);
+            ptx::mbar_init(bar(BAR_TFULL + b), 32);
+            ptx::mbar_init(bar(BAR_TFREE + b), kTabUsers);
         }
         ptx::mbar_init(bar(BAR_OF), 1);
-        ptx::mbar_init(bar(BAR_OF + 1), 1);
+        ptx::mbar_init(bar(BAR_OFREE), 2 * kBM);
+        ptx::mbar_init(bar(BAR_XCH), 2 * kBM);
         ptx::mbar_init(bar(BAR_DRAIN), 1);
         ptx::fence_mbar_init();
         misc[1] = 0;
@@ -216,76 +224,117 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_alloc(base + OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
-    if (threadIdx.x < 32) selbits[threadIdx.x] = 0u;
-    int n, nsel = 0;
-    if (dense_row) {
-        n = J;
-    } else {
-        const int ns = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
-        nsel = max(0, min(ns, prm.kmax));
-        n = P + nsel + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
-    }
-    __syncthreads();
-    // the key-tile table of a routed row (a dense row's tile s is block s: its
-    // entries are computed where they are used, so its length is not bounded
-    // by the table)
-    const int ntab = dense_row ? 0 : n;
-    for (int s = threadIdx.x; s < ntab; s += blockDim.x) {
-        int blk, nv;
-        if (s < P) {
-            blk = s;
-            nv = prm.block_sizes[blk];
-        } else if (s < P + nsel) {
-            const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
-            if (jr < 0 || jr >= Jr) {
-                raise_status(prm.status, BSA_ERR_INDEX);
-                blk = P > 0 ? 0 : qb;
-                nv = 0;  // contributes nothing
-            } else {
-                blk = P + jr;
-                nv = prm.block_sizes[blk];
-                if (prm.summary) atomicOr(&selbits[jr >> 5], 1u << (jr & 31));
-            }
-        } else {
-            const int t = s - (P + nsel);
-            blk = -(t + 1);
-            nv = min(kBN, Jr - t * kBN);
-        }
-        list[s] = blk;
-        nvalid[s] = nv;
-    }
-    __syncthreads();
-    {
-        int4* srcs = reinterpret_cast<int4*>(sm + OFF_SRC);
-        for (int s = threadIdx.x; s < ntab; s += blockDim.x) {
-            const int blk = list[s];
-            srcs[s] = pack_src(tile_source(blk, prm, bh), blk < 0);
-        }
-    }
-    if (prm.summary && !dense_row) {
-        const int nvirt = (Jr + kBN - 1) / kBN;
-        for (int jr = threadIdx.x; jr < nvirt * kBN; jr += blockDim.x) {
-            float b = -CUDART_INF_F;
-            if (jr < Jr && !((selbits[jr >> 5] >> (jr & 31)) & 1u)) {
-                const int nb = prm.block_sizes[P + jr];
-                // log-mass of the summary token: log n_j, or the caller's bias
-                if (nb > 0) b = prm.sbias ? prm.sbias[(long long)bh * J + P + jr] * kLog2e : log2f((float)nb);
-            }
-            bias[jr] = b;
-        }
-    }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = misc[0];
 
+    // Every role walks the same sequence of work items: item it uses table
+    // buffer it & 1, published on TFULL[it & 1] and released on TFREE[it & 1].
     if (warp < 4) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
-      if (warp == 0 || warp == 2) {
+      if (warp == 3) {
+        // ------------------------------------------------------------ scheduler
+        // Takes the next (head, query block) from the launch's work counter
+        // (or, without one, every gridDim.x-th item) and writes its key-tile
+        // table: tile s of a routed row is prefix block s, then the selected
+        // blocks in list order, then the summary tiles.
+        int next = blockIdx.x;
+        for (int it = 0;; ++it) {
+            int qb = -1, bh = 0, nq = 0;
+            while (true) {
+                int t;
+                if (prm.sched) {
+                    unsigned tk = 0;
+                    if (lane == 0) tk = atomicAdd(prm.sched, 1u);
+                    t = (int)__shfl_sync(0xffffffffu, tk, 0);
+                } else {
+                    t = next;
+                    next += gridDim.x;
+                }
+                if (t < 0 || t >= prm.items) break;
+                const int b_ = t % J;
+                const int c = prm.block_sizes[b_];
+                if (c > 0) {  // an empty block has no query rows
+                    qb = b_;
+                    bh = t / J;
+                    nq = c;
+                    break;
+                }
+            }
+            const int b = it & 1;
+            if (it >= 2 && !__all_sync(0xffffffffu, wait_bar(bar(BAR_TFREE + b), (uint32_t)((it - 2) >> 1) & 1u,
+                                                             abort_flag, prm.status)))
+                break;
+            uint8_t* tb = tab(b);
+            int n = 0;
+            if (qb >= 0 && qb < P) {
+                n = J;  // a dense row's tile s is block s: its entries are computed where they are used
+            } else if (qb >= 0) {
+                const int ns = Jr > 0 ? prm.q2k_num[(long long)bh * Jr + (qb - P)] : 0;
+                const int nsel = max(0, min(ns, prm.kmax));
+                n = P + nsel + (prm.summary ? (Jr + kBN - 1) / kBN : 0);
+                selbits[lane] = 0u;
+                __syncwarp();
+                int4* srcs = reinterpret_cast<int4*>(tb + TAB_SRC);
+                int* info = reinterpret_cast<int*>(tb + TAB_INFO);
+                for (int s = lane; s < n; s += 32) {
+                    int blk, nv;
+                    if (s < P) {
+                        blk = s;
+                        nv = prm.block_sizes[blk];
+                    } else if (s < P + nsel) {
+                        const int jr = prm.q2k_idx[((long long)bh * Jr + (qb - P)) * prm.kmax + (s - P)];
+                        if (jr < 0 || jr >= Jr) {
+                            raise_status(prm.status, BSA_ERR_INDEX);
+                            blk = P > 0 ? 0 : qb;
+                            nv = 0;  // contributes nothing
+                        } else {
+                            blk = P + jr;
+                            nv = prm.block_sizes[blk];
+                            if (prm.summary) atomicOr(&selbits[jr >> 5], 1u << (jr & 31));
+                        }
+                    } else {
+                        const int t = s - (P + nsel);
+                        blk = -(t + 1);
+                        nv = min(kBN, Jr - t * kBN);
+                    }
+                    srcs[s] = pack_src(tile_source(blk, prm, bh), blk, nv);
+                    info[s] = nv | ((blk < 0 ? -blk : 0) << 8);
+                }
+                __syncwarp();
+                if (prm.summary) {
+                    float* bias = reinterpret_cast<float*>(tb + TAB_BIAS);
+                    const int nvirt = (Jr + kBN - 1) / kBN;
+                    for (int jr = lane; jr < nvirt * kBN; jr += 32) {
+                        float bv = -CUDART_INF_F;
+                        if (jr < Jr && !((selbits[jr >> 5] >> (jr & 31)) & 1u)) {
+                            const int nb = prm.block_sizes[P + jr];
+                            // log-mass of the summary token: log n_j, or the caller's bias
+                            if (nb > 0)
+                                bv = prm.sbias ? prm.sbias[(long long)bh * J + P + jr] * kLog2e : log2f((float)nb);
+                        }
+                        bias[jr] = bv;
+                    }
+                }
+            }
+            if (lane == 0) {
+                int* hdr = reinterpret_cast<int*>(tb + TAB_HDR);
+                hdr[0] = qb;
+                hdr[1] = bh;
+                hdr[2] = n;
+                hdr[3] = nq;
+            }
+            __syncwarp();
+            ptx::mbar_arrive(bar(BAR_TFULL + b));
+            if (qb < 0) break;
+        }
+      } else if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ producers
         // warp 0: Q, then the K ring; warp 2: the V ring.  Separate rings let each
         // load start as soon as its own stage is free: a K tile is dead once
-        // S_j is done, so K runs about three tiles ahead, V two.
+        // S_j is done, so K runs about three tiles ahead, V two.  The rings
+        // run on across work items (stage = tiles issued so far mod depth).
         const bool vprod = warp == 2;
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
@@ -295,163 +344,201 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::prefetch_tmap(&tm_v5);
         ptx::prefetch_tmap(&tm_kr);
         ptx::prefetch_tmap(&tm_vr);
-        const long long head_row = (long long)bh * prm.N;
-        const int q0tok = prm.index_map[(long long)qb * kBM];  // a valid row: pads point here
-        // issue one 32 KB tile (two 64-column halves) from source `src`
-        auto issue_tile = [&](uint32_t dst, const TileSrc& src, const int* rows, const CUtensorMap* mg,
-                              const CUtensorMap* mr, const CUtensorMap* m5, uint32_t b) {
-            if (src.mode == 0) {
-                const uint32_t d = dst + 4 * lane * 128;
-                ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], b);
-                ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], b);
-            } else if (lane == 0) {
-                if (src.mode == 1) {
-                    ptx::tma_load_2d(dst, mr, 0, src.c1, b);
-                    ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.c1, b);
-                } else {
-                    ptx::tma_load_5d(dst, m5, 0, src.c1, src.c2, src.c3, src.c4, b);
-                    ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.c1, src.c2, src.c3, src.c4, b);
-                }
-            }
-        };
-        // gathered rows of a real block (4 per lane); slots past n_j point at a valid row
-        auto gather_rows = [&](int blk, int nv, int* rows) {
-            const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)blk * kBN + 4 * lane);
-            rows[0] = t4.x;
-            rows[1] = t4.y;
-            rows[2] = t4.z;
-            rows[3] = t4.w;
-            for (int u = 0; u < 4; ++u) {
-                const int r = 4 * lane + u;
-                int tok = rows[u];
-                if (r < nv && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
-                if (r >= nv || tok < 0 || tok >= prm.N) tok = q0tok;
-                rows[u] = (int)(head_row + tok);
-            }
-        };
-        if (!vprod) {
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_Q), kTileBytes);
-            __syncwarp();
-            const TileSrc src = tile_source(qb, prm, bh);
-            int rq[4] = {0, 0, 0, 0};
-            if (src.mode == 0) gather_rows(qb, nq, rq);
-            issue_tile(base + OFF_Q, src, rq, &tm_q, &tm_qr, &tm_q5, bar(BAR_Q));
-        }
-        // Tile j's source comes from the table built in the prologue; gathered
-        // row ids (mode 0 only) are loaded one tile ahead.
-        const int4* srcs = reinterpret_cast<const int4*>(sm + OFF_SRC);
         const int RS = vprod ? kVStages : kKStages;
         const int sbase = vprod ? kKStages : 0;
-        int issued = 0;
-        int rows_next[4] = {0, 0, 0, 0};
-        int4 src_next = make_int4(0, 0, 0, 0);
-        auto prepare = [&](int jt) {
-            if (dense_row) {
-                src_next = pack_src(tile_source(jt, prm, bh), false);
-                if ((src_next.x & 3) == 0) gather_rows(jt, prm.block_sizes[jt], rows_next);
-            } else {
-                src_next = srcs[jt];
-                if ((src_next.x & 3) == 0) gather_rows(list[jt], nvalid[jt], rows_next);
-            }
-        };
-        if (n > 0) prepare(0);
-        for (int jt = 0; jt < n; ++jt) {
-            const int4 src = src_next;
-            const int rows[4] = {rows_next[0], rows_next[1], rows_next[2], rows_next[3]};
-            if (jt + 1 < n) prepare(jt + 1);
-            const int st = sbase + jt % RS;
-            const uint32_t ph = (uint32_t)(jt / RS) & 1u;
-            if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) break;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
-            __syncwarp();
-            const uint32_t dst = base + OFF_RING + st * kTileBytes;
-            const int mode = src.x & 3;
-            const bool virt = (src.x & 4) != 0;
-            const uint32_t fb = bar(BAR_FULL + st);
-            if (mode == 0) {
-                const CUtensorMap* mg = vprod ? &tm_v : &tm_k;
-                const uint32_t d = dst + 4 * lane * 128;
-                ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], fb);
-                ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], fb);
-            } else if (lane == 0) {
-                if (mode == 1) {
-                    const CUtensorMap* mr = virt ? (vprod ? &tm_vb : &tm_kb) : (vprod ? &tm_vr : &tm_kr);
-                    ptx::tma_load_2d(dst, mr, 0, src.y, fb);
-                    ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.y, fb);
-                } else {
-                    const CUtensorMap* m5 = vprod ? &tm_v5 : &tm_k5;
-                    const int c2 = src.z & 0xffff, c3 = src.z >> 16;
-                    ptx::tma_load_5d(dst, m5, 0, src.y, c2, c3, src.w, fb);
-                    ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.y, c2, c3, src.w, fb);
+        int cnt = 0;     // tiles this warp has issued, all items
+        int qloads = 0;  // Q tiles issued
+        for (int it = 0;; ++it) {
+            const int b = it & 1;
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(bar(BAR_TFULL + b), (uint32_t)(it >> 1) & 1u, abort_flag, prm.status)))
+                break;
+            const uint8_t* tb = tab(b);
+            const int* hdr = reinterpret_cast<const int*>(tb + TAB_HDR);
+            const int qb = hdr[0], bh = hdr[1], n = hdr[2], nq = hdr[3];
+            if (qb < 0) break;
+            const bool dense_row = qb < P;
+            const long long head_row = (long long)bh * prm.N;
+            const int q0tok = prm.index_map[(long long)qb * kBM];  // a valid row: pads point here
+            // gathered rows of a real block (4 per lane); slots past n_j point at a valid row
+            auto gather_rows = [&](int blk, int nv, int* rows) {
+                const int4 t4 = *reinterpret_cast<const int4*>(prm.index_map + (long long)blk * kBN + 4 * lane);
+                rows[0] = t4.x;
+                rows[1] = t4.y;
+                rows[2] = t4.z;
+                rows[3] = t4.w;
+                for (int u = 0; u < 4; ++u) {
+                    const int r = 4 * lane + u;
+                    int tok = rows[u];
+                    if (r < nv && (tok < 0 || tok >= prm.N)) raise_status(prm.status, BSA_ERR_INDEX);
+                    if (r >= nv || tok < 0 || tok >= prm.N) tok = q0tok;
+                    rows[u] = (int)(head_row + tok);
                 }
+            };
+            if (!vprod) {
+                // Q of this item, once the last S of the previous item is done with the buffer
+                if (it > 0 && !__all_sync(0xffffffffu, wait_bar(bar(BAR_QFREE), (uint32_t)(it - 1) & 1u,
+                                                                abort_flag, prm.status)))
+                    break;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_QFULL), kTileBytes);
+                __syncwarp();
+                const TileSrc src = tile_source(qb, prm, bh);
+                const uint32_t d = base + OFF_Q, qbar = bar(BAR_QFULL);
+                if (src.mode == 0) {
+                    int rq[4];
+                    gather_rows(qb, nq, rq);
+                    ptx::tma_gather4(d + 4 * lane * 128, &tm_q, 0, rq[0], rq[1], rq[2], rq[3], qbar);
+                    ptx::tma_gather4(d + 4 * lane * 128 + kHalfBytes, &tm_q, 64, rq[0], rq[1], rq[2], rq[3], qbar);
+                } else if (lane == 0) {
+                    if (src.mode == 1) {
+                        ptx::tma_load_2d(d, &tm_qr, 0, src.c1, qbar);
+                        ptx::tma_load_2d(d + kHalfBytes, &tm_qr, 64, src.c1, qbar);
+                    } else {
+                        ptx::tma_load_5d(d, &tm_q5, 0, src.c1, src.c2, src.c3, src.c4, qbar);
+                        ptx::tma_load_5d(d + kHalfBytes, &tm_q5, 64, src.c1, src.c2, src.c3, src.c4, qbar);
+                    }
+                }
+                qloads = it + 1;
             }
-            issued = jt + 1;
+            // Tile jt's source comes from the table (a dense row computes it);
+            // gathered row ids (mode 0 only) are loaded one tile ahead.
+            const int4* srcs = reinterpret_cast<const int4*>(tb + TAB_SRC);
+            int rows_next[4] = {0, 0, 0, 0};
+            int4 src_next = make_int4(0, 0, 0, 0);
+            auto prepare = [&](int jt) {
+                if (dense_row) {
+                    src_next = pack_src(tile_source(jt, prm, bh), jt, prm.block_sizes[jt]);
+                } else {
+                    src_next = srcs[jt];
+                }
+                if ((src_next.x & 3) == 0) gather_rows(src_next.y, src_next.z, rows_next);
+            };
+            if (n > 0) prepare(0);
+            bool ok = true;
+            for (int jt = 0; jt < n; ++jt) {
+                const int4 src = src_next;
+                const int rows[4] = {rows_next[0], rows_next[1], rows_next[2], rows_next[3]};
+                if (jt + 1 < n) prepare(jt + 1);
+                const int st = sbase + cnt % RS;
+                const uint32_t ph = (uint32_t)(cnt / RS) & 1u;
+                if (!__all_sync(0xffffffffu, wait_bar(bar(BAR_EMPTY + st), ph ^ 1u, abort_flag, prm.status))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_FULL + st), kTileBytes);
+                __syncwarp();
+                const uint32_t dst = base + OFF_RING + st * kTileBytes;
+                const int mode = src.x & 3;
+                const bool virt = (src.x & 4) != 0;
+                const uint32_t fb = bar(BAR_FULL + st);
+                if (mode == 0) {
+                    const CUtensorMap* mg = vprod ? &tm_v : &tm_k;
+                    const uint32_t d = dst + 4 * lane * 128;
+                    ptx::tma_gather4(d, mg, 0, rows[0], rows[1], rows[2], rows[3], fb);
+                    ptx::tma_gather4(d + kHalfBytes, mg, 64, rows[0], rows[1], rows[2], rows[3], fb);
+                } else if (lane == 0) {
+                    if (mode == 1) {
+                        const CUtensorMap* mr = virt ? (vprod ? &tm_vb : &tm_kb) : (vprod ? &tm_vr : &tm_kr);
+                        ptx::tma_load_2d(dst, mr, 0, src.y, fb);
+                        ptx::tma_load_2d(dst + kHalfBytes, mr, 64, src.y, fb);
+                    } else {
+                        const CUtensorMap* m5 = vprod ? &tm_v5 : &tm_k5;
+                        const int c2 = src.z & 0xffff, c3 = src.z >> 16;
+                        ptx::tma_load_5d(dst, m5, 0, src.y, c2, c3, src.w, fb);
+                        ptx::tma_load_5d(dst + kHalfBytes, m5, 64, src.y, c2, c3, src.w, fb);
+                    }
+                }
+                ++cnt;
+            }
+            if (!ok) break;
+            if (lane == 0) ptx::mbar_arrive(bar(BAR_TFREE + b));
         }
         if (*abort_flag) {
             // drain: wait (bounded) for this warp's copies still in flight
             const uint64_t t0 = ptx::globaltimer();
-            for (int jt = max(0, issued - RS); jt < issued; ++jt)
-                while (!ptx::mbar_try_wait(bar(BAR_FULL + sbase + jt % RS), (uint32_t)(jt / RS) & 1u) &&
+            for (int c = max(0, cnt - RS); c < cnt; ++c)
+                while (!ptx::mbar_try_wait(bar(BAR_FULL + sbase + c % RS), (uint32_t)(c / RS) & 1u) &&
                        ptx::globaltimer() - t0 < kWaitNs) {
                 }
-            if (!vprod)
-                while (!ptx::mbar_try_wait(bar(BAR_Q), 0) && ptx::globaltimer() - t0 < kWaitNs) {}
+            if (!vprod && qloads > 0)
+                while (!ptx::mbar_try_wait(bar(BAR_QFULL), (uint32_t)(qloads - 1) & 1u) &&
+                       ptx::globaltimer() - t0 < kWaitNs) {
+                }
         }
-      } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n > 0) {
+      } else {
+        // ------------------------------------------------------------ MMA issuer (warp 1)
+        // Per item: S_0, S_1, then PV_j, S_{j+2} for every j.  The next item's
+        // S_0 and S_1 follow this item's last P V, so they run while the
+        // softmax warps write this item's output; its first P V waits until
+        // that epilogue has read O out of TMEM.
+        if (lane == 0) {
             constexpr uint32_t idS = ptx::idesc_bf16(kBM, kBN, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kBM, kHD, true);
-            bool ok = wait_bar(bar(BAR_Q), 0, abort_flag, prm.status);
-            // K_j sits in K stage j % kKStages, V_j in V stage j % kVStages
-            auto take = [&](int j, bool isV, uint32_t& addr) -> bool {
-                const int RS = isV ? kVStages : kKStages;
-                const int st = (isV ? kKStages : 0) + j % RS;
-                if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(j / RS) & 1u, abort_flag, prm.status)) return false;
-                ptx::tc_fence_after();
-                addr = base + OFF_RING + st * kTileBytes;
-                return true;
-            };
-            auto release = [&](int j, bool isV) {
-                ptx::mma_commit(bar(BAR_EMPTY + (isV ? kKStages + j % kVStages : j % kKStages)));
-            };
-            auto issue_s = [&](int j) -> bool {
-                uint32_t ka;
-                if (!take(j, false, ka)) return false;
-                const uint32_t qa = base + OFF_Q;
-                const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
+            int kc = 0, vc = 0;        // K and V tiles consumed, all items
+            int up0 = 0, up1 = 0;      // P tiles consumed from S/P buffer 0 / 1, all items
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                const int b = it & 1;
+                if (!wait_bar(bar(BAR_TFULL + b), (uint32_t)(it >> 1) & 1u, abort_flag, prm.status)) break;
+                const int* hdr = reinterpret_cast<const int*>(tab(b) + TAB_HDR);
+                const int qb = hdr[0], n = hdr[2];
+                if (qb < 0) break;
+                if (!wait_bar(bar(BAR_QFULL), (uint32_t)it & 1u, abort_flag, prm.status)) break;
+                auto issue_s = [&](int j) -> bool {
+                    const int st = kc % kKStages;
+                    if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(kc / kKStages) & 1u, abort_flag, prm.status))
+                        return false;
+                    ptx::tc_fence_after();
+                    const uint32_t ka = base + OFF_RING + st * kTileBytes;
+                    const uint32_t qa = base + OFF_Q;
+                    const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
 #pragma unroll
-                for (int kk = 0; kk < kHD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                    ptx::mma_ss(dS, ptx::smem_desc(qa + off, 16, 1024), ptx::smem_desc(ka + off, 16, 1024), idS,
-                                kk > 0);
-                }
-                ptx::mma_commit(bar(BAR_SF + (j & 1)));
-                release(j, false);
-                return true;
-            };
-            auto issue_pv = [&](int j) -> bool {
-                if (!wait_bar(bar(BAR_PF + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, prm.status)) return false;
-                uint32_t va;
-                if (!take(j, true, va)) return false;
-                const uint32_t aP = tmem + (uint32_t)(j & 1) * 128;
+                    for (int kk = 0; kk < kHD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                        ptx::mma_ss(dS, ptx::smem_desc(qa + off, 16, 1024), ptx::smem_desc(ka + off, 16, 1024), idS,
+                                    kk > 0);
+                    }
+                    ptx::mma_commit(bar(BAR_SF + (j & 1)));
+                    ptx::mma_commit(bar(BAR_EMPTY + st));
+                    ++kc;
+                    if (j == n - 1) ptx::mma_commit(bar(BAR_QFREE));  // the item's last S: Q may be replaced
+                    return true;
+                };
+                auto issue_pv = [&](int j) -> bool {
+                    const int w = j & 1;
+                    const int u = w ? up1++ : up0++;
+                    if (!wait_bar(bar(BAR_PF + w), (uint32_t)u & 1u, abort_flag, prm.status)) return false;
+                    const int st = kKStages + vc % kVStages;
+                    if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(vc / kVStages) & 1u, abort_flag, prm.status))
+                        return false;
+                    ptx::tc_fence_after();
+                    const uint32_t va = base + OFF_RING + st * kTileBytes;
+                    const uint32_t aP = tmem + (uint32_t)w * 128;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
-                    // V advances by two 8-row groups of 1024 B; the second
-                    // 64-column half of V is one leading-dimension step (16 KB) away.
-                    ptx::mma_ts(tmem + 256 + (uint32_t)(j & 1) * 128, aP + kk * 8,
-                                ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO, (j >= 2 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
+                        // V advances by two 8-row groups of 1024 B; the second
+                        // 64-column half of V is one leading-dimension step (16 KB) away.
+                        ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, aP + kk * 8,
+                                    ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
+                                    (j >= 2 || kk > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar(BAR_EMPTY + st));
+                    ++vc;
+                    return true;
+                };
+                if (n == 0) ptx::mma_commit(bar(BAR_QFREE));
+                if (n > 0) ok = issue_s(0);
+                if (ok && n > 1) ok = issue_s(1);
+                // the previous item's epilogue must have read O_0 and O_1
+                if (ok && it > 0) ok = wait_bar(bar(BAR_OFREE), (uint32_t)(it - 1) & 1u, abort_flag, prm.status);
+                for (int j = 0; ok && j < n; ++j) {
+                    ok = issue_pv(j);
+                    if (ok && j + 2 < n) ok = issue_s(j + 2);
                 }
-                release(j, true);
-                if (j + 2 >= n) ptx::mma_commit(bar(BAR_OF + (j & 1)));  // last product into O_{j&1}
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n; ++j) {
-                ok = issue_pv(j);
-                if (ok && j + 2 < n) ok = issue_s(j + 2);
+                if (!ok) break;
+                ptx::mma_commit(bar(BAR_OF));  // every product of this item is in O_0 / O_1
+                ptx::mbar_arrive(bar(BAR_TFREE + b));
             }
             // nothing this thread issued may still run when TMEM is freed
             ptx::mma_commit(bar(BAR_DRAIN));
@@ -463,182 +550,209 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
       {
         // ------------------------------------------------------------ softmax + epilogue
-        // Warpgroup w takes the key tiles s = w, w+2, w+4, ... with its own
-        // running max m, sum l and accumulator O_w; the two partial results
-        // are merged exactly at the end (weights 2^(m_w - max(m_0, m_1))).
+        // Warpgroup w takes the key tiles s = w, w+2, w+4, ... of every item
+        // with its own running max m, sum l and accumulator O_w; the two
+        // partial results are merged exactly at the end of the item (weights
+        // 2^(m_w - max(m_0, m_1))).
         const int w = (warp - 4) >> 2;
         const int row = threadIdx.x & 127;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         const uint32_t tOw = tmem + lane_off + 256 + 128 * w;
-        float m_ref = -CUDART_INF_F, l = 0.f;
-        bool ok = true;
-        uint32_t r[32];
+        const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
+        int su = 0;  // S tiles consumed from buffer w, all items
+        uint32_t r[16];
         float x[kBN];
-        for (int s = w; s < n; s += 2) {
-            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + w), (uint32_t)(s >> 1) & 1u, abort_flag, prm.status));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
-            {
-                uint32_t* xr = reinterpret_cast<uint32_t*>(x);
-                ptx::tmem_ld32(tS + 0, xr + 0);
-                ptx::tmem_ld32(tS + 32, xr + 32);
-                ptx::tmem_ld32(tS + 64, xr + 64);
-                ptx::tmem_ld32(tS + 96, xr + 96);
-                ptx::tmem_wait_ld();
-            }
-            const int blk = dense_row ? s : list[s];
-            const int nv = dense_row ? prm.block_sizes[s] : nvalid[s];
-            float mxp[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
-            const bool real = blk >= 0 || nv == 0;
-            if (real) {
-                if (nv < kBN) {
-#pragma unroll
-                    for (int c = 0; c < kBN; ++c) x[c] = c < nv ? x[c] : -CUDART_INF_F;
+        for (int it = 0;; ++it) {
+            const int b = it & 1;
+            if (!__all_sync(0xffffffffu,
+                            wait_bar(bar(BAR_TFULL + b), (uint32_t)(it >> 1) & 1u, abort_flag, prm.status)))
+                break;
+            const uint8_t* tb = tab(b);
+            const int* hdr = reinterpret_cast<const int*>(tb + TAB_HDR);
+            const int qb = hdr[0], bh = hdr[1], n = hdr[2], nq = hdr[3];
+            if (qb < 0) break;
+            const bool dense_row = qb < P;
+            const int* info = reinterpret_cast<const int*>(tb + TAB_INFO);
+            const float* bias = reinterpret_cast<const float*>(tb + TAB_BIAS);
+            float m_ref = -CUDART_INF_F, l = 0.f;
+            bool ok = true;
+            for (int s = w; s < n; s += 2) {
+                ok = __all_sync(0xffffffffu,
+                                wait_bar(bar(BAR_SF + w), (uint32_t)su & 1u, abort_flag, prm.status));
+                if (!ok) break;
+                ++su;
+                ptx::tc_fence_after();
+                {
+                    uint32_t* xr = reinterpret_cast<uint32_t*>(x);
+                    ptx::tmem_ld32(tS + 0, xr + 0);
+                    ptx::tmem_ld32(tS + 32, xr + 32);
+                    ptx::tmem_ld32(tS + 64, xr + 64);
+                    ptx::tmem_ld32(tS + 96, xr + 96);
+                    ptx::tmem_wait_ld();
                 }
-                // three-input max: two columns per instruction into 8 partial maxima
+                const int inf = dense_row ? prm.block_sizes[s] : info[s];
+                const int nv = inf & 0xff;
+                const int vid = inf >> 8;  // 0: a real block; t + 1: summary tile t
+                float mxp[8];
 #pragma unroll
-                for (int c = 0; c < kBN; c += 16)
+                for (int u = 0; u < 8; ++u) mxp[u] = -CUDART_INF_F;
+                const bool real = vid == 0;
+                if (real) {
+                    if (nv < kBN) {
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
-            } else {
-                const float* bt = bias + (-blk - 1) * kBN;
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
-                    mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
-                }
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
-            const float m_new = fmaxf(m_ref, mx);
-            const bool need = m_new > m_ref + kRescaleThreshold;
-            if (__any_sync(0xffffffffu, need)) {
-                const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;  // m_ref = -inf -> 0
-                if (need) m_ref = m_new;
-                l *= alpha;
-                if (s >= 2) {
-                    // S_s was issued after PV_{s-2}, the last product added to O_w,
-                    // so O_w is complete here and can be rescaled in place.
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        ptx::tmem_ld32(tOw + c * 32, r);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                        ptx::tmem_st32(tOw + c * 32, r);
+                        for (int c = 0; c < kBN; ++c) x[c] = c < nv ? x[c] : -CUDART_INF_F;
                     }
-                    ptx::tmem_wait_st();
+                    // three-input max: two columns per instruction into 8 partial maxima
+#pragma unroll
+                    for (int c = 0; c < kBN; c += 16)
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
+                } else {
+                    const float* bt = bias + (vid - 1) * kBN;
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
+                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
+                    }
+                }
+                const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                       fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                const float m_new = fmaxf(m_ref, mx);
+                const bool need = m_new > m_ref + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ptx::ex2(m_ref - m_new) : 1.f;  // m_ref = -inf -> 0
+                    if (need) m_ref = m_new;
+                    l *= alpha;
+                    if (s >= 2) {
+                        // S_s was issued after PV_{s-2}, the last product added to O_w,
+                        // so O_w is complete here and can be rescaled in place.
+                        // (16 columns at a time: the S row stays in registers meanwhile)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            ptx::tmem_ld16(tOw + c * 16, r);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                            ptx::tmem_st16(tOw + c * 16, r);
+                        }
+                        ptx::tmem_wait_st();
+                    }
+                }
+                float sp[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) sp[u] = 0.f;
+                const bool live = m_ref != -CUDART_INF_F;
+                if (real) {
+                    // x holds raw Q.K: one FMA folds the scale and subtracts the reference;
+                    // pairs of columns share one f32x2 FMA and one f32x2 add (sp[c & 7]
+                    // accumulates exactly as with scalar adds)
+                    const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+                    const float2 nm2 = make_float2(-m_ref, -m_ref);
+                    float2 acc2[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int c = 0; c < kBN; c += 2) {
+                        const float2 a = ptx::ffma2(make_float2(x[c], x[c + 1]), sc2, nm2);
+                        x[c] = live ? ptx::ex2(a.x) : 0.f;
+                        x[c + 1] = live ? ptx::ex2(a.y) : 0.f;
+                        acc2[(c >> 1) & 3] = ptx::fadd2(acc2[(c >> 1) & 3], make_float2(x[c], x[c + 1]));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        sp[2 * u] = acc2[u].x;
+                        sp[2 * u + 1] = acc2[u].y;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
+                        sp[c & 7] += x[c];
+                    }
+                }
+                l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = ptx::pack_bf16x2(x[h * 32 + 2 * e], x[h * 32 + 2 * e + 1]);
+                    ptx::tmem_st16(tS + h * 16, r);
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(BAR_PF + w));
+            }
+            // the table is no longer read
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(BAR_TFREE + b));
+            // epilogue: both partial results of this item are complete, merge them
+            if (ok) ok = wait_bar(bar(BAR_OF), (uint32_t)it & 1u, abort_flag, prm.status);
+            ok = __all_sync(0xffffffffu, ok);
+            ptx::tc_fence_after();
+            float* xm = xch + (it & 1) * 4 * kBM;  // [2][128] running maxima
+            float* xl = xm + 2 * kBM;              // [2][128] sums
+            xm[w * kBM + row] = m_ref;
+            xl[w * kBM + row] = l;
+            ptx::mbar_arrive(bar(BAR_XCH));
+            ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_XCH), (uint32_t)it & 1u, abort_flag, prm.status) && ok);
+            const float m0 = xm[row], m1 = xm[kBM + row];
+            const float M = fmaxf(m0, m1);
+            const float a0 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m0 - M);
+            const float a1 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m1 - M);
+            const float L = xl[row] * a0 + xl[kBM + row] * a1;
+            const bool n1 = n > 1;  // O_1 holds something only with two or more tiles
+            // warpgroup w writes output columns [64w, 64w + 64), 16 at a time; O is
+            // handed back to the MMA issuer once the last columns are read
+            const uint32_t tO0 = tmem + lane_off + 256 + 64 * w, tO1 = tO0 + 128;
+            const bool write = ok && row < nq;
+            int tok = -1;
+            if (write) {
+                tok = prm.index_map[(long long)qb * kBM + row];
+                if (tok < 0 || tok >= prm.N) tok = -1;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD + 64 * w;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r1[16];
+                if (ok && n > 0) {
+                    ptx::tmem_ld16(tO0 + c * 16, r);
+                    if (n1) ptx::tmem_ld16(tO1 + c * 16, r1);
+                    ptx::tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = 0u;
+                }
+                if (!(ok && n1)) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r1[e] = 0u;
+                }
+                if (c == 3) {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar(BAR_OFREE));
+                }
+                if (write && tok >= 0) {
+                    float o[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = (__uint_as_float(r[e]) * a0 + __uint_as_float(r1[e]) * a1) * inv;
+                    uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+#pragma unroll
+                    for (int v4 = 0; v4 < 2; ++v4) {
+                        uint4 q4;
+                        q4.x = ptx::pack_bf16x2(o[8 * v4 + 0], o[8 * v4 + 1]);
+                        q4.y = ptx::pack_bf16x2(o[8 * v4 + 2], o[8 * v4 + 3]);
+                        q4.z = ptx::pack_bf16x2(o[8 * v4 + 4], o[8 * v4 + 5]);
+                        q4.w = ptx::pack_bf16x2(o[8 * v4 + 6], o[8 * v4 + 7]);
+                        dst[v4] = q4;
+                    }
                 }
             }
-            float sp[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) sp[u] = 0.f;
-            const bool live = m_ref != -CUDART_INF_F;
-            if (real) {
-                // x holds raw Q.K: one FMA folds the scale and subtracts the reference;
-                // pairs of columns share one f32x2 FMA and one f32x2 add (sp[c & 7]
-                // accumulates exactly as with scalar adds)
-                const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
-                const float2 nm2 = make_float2(-m_ref, -m_ref);
-                float2 acc2[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < kBN; c += 2) {
-                    const float2 a = ptx::ffma2(make_float2(x[c], x[c + 1]), sc2, nm2);
-                    x[c] = live ? ptx::ex2(a.x) : 0.f;
-                    x[c + 1] = live ? ptx::ex2(a.y) : 0.f;
-                    acc2[(c >> 1) & 3] = ptx::fadd2(acc2[(c >> 1) & 3], make_float2(x[c], x[c + 1]));
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    sp[2 * u] = acc2[u].x;
-                    sp[2 * u + 1] = acc2[u].y;
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kBN; ++c) {
-                    x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
-                    sp[c & 7] += x[c];
-                }
-            }
-            l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = ptx::pack_bf16x2(x[h * 64 + 2 * e], x[h * 64 + 2 * e + 1]);
-                ptx::tmem_st32(tS + h * 32, r);
-            }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(BAR_PF + w));
+            if (w == 0 && write && tok >= 0 && prm.lse)
+                prm.lse[(long long)bh * prm.N + tok] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
+            if (!ok) break;
         }
-        // epilogue: both partial results are complete, merge them
-        const bool has_tiles = w < n;
-        if (ok && has_tiles) ok = wait_bar(bar(BAR_OF + w), 0, abort_flag, prm.status);
-        ok = __all_sync(0xffffffffu, ok);
-        ptx::tc_fence_after();
-        float* xm = xch;             // [2][128] running maxima
-        float* xl = xch + 2 * kBM;   // [2][128] sums
-        xm[w * kBM + row] = m_ref;
-        xl[w * kBM + row] = l;
-        // the two warpgroups also meet here after an abort, so the count matches
-        named_sync(kSoftmaxBarrier, 2 * kBM);
-        const float m0 = xm[row], m1 = xm[kBM + row];
-        const float M = fmaxf(m0, m1);
-        const float a0 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m0 - M);
-        const float a1 = M == -CUDART_INF_F ? 0.f : ptx::ex2(m1 - M);
-        const float L = xl[row] * a0 + xl[kBM + row] * a1;
-        const bool n1 = n > 1;  // O_1 holds something only with two or more tiles
-        const bool write = ok && row < nq;
-        int tok = -1;
-        if (write) {
-            tok = prm.index_map[(long long)qb * kBM + row];
-            if (tok < 0 || tok >= prm.N) tok = -1;
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        // warpgroup w writes output columns [64w, 64w + 64)
-        const uint32_t tO0 = tmem + lane_off + 256 + 64 * w, tO1 = tO0 + 128;
-        __nv_bfloat16* orow = prm.out + ((long long)bh * prm.N + (tok < 0 ? 0 : tok)) * kHD + 64 * w;
-        uint32_t r1[32];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-            if (ok && n > 0) {
-                ptx::tmem_ld32(tO0 + c * 32, r);
-                if (n1) ptx::tmem_ld32(tO1 + c * 32, r1);
-                ptx::tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r[e] = 0u;
-            }
-            if (!(ok && n1)) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) r1[e] = 0u;
-            }
-            if (write && tok >= 0) {
-                float o[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    o[e] = (__uint_as_float(r[e]) * a0 + __uint_as_float(r1[e]) * a1) * inv;
-                uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4) {
-                    uint4 q4;
-                    q4.x = ptx::pack_bf16x2(o[8 * v4 + 0], o[8 * v4 + 1]);
-                    q4.y = ptx::pack_bf16x2(o[8 * v4 + 2], o[8 * v4 + 3]);
-                    q4.z = ptx::pack_bf16x2(o[8 * v4 + 4], o[8 * v4 + 5]);
-                    q4.w = ptx::pack_bf16x2(o[8 * v4 + 6], o[8 * v4 + 7]);
-                    dst[v4] = q4;
-                }
-            }
-        }
-        if (w == 0 && write && tok >= 0 && prm.lse)
-            prm.lse[(long long)bh * prm.N + tok] = L > 0.f ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
       }
     }
 
@@ -725,6 +839,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     // the stored key-tile list of a routed row (dense prefix rows need none)
     const long long longest = (long long)P + kmax + nvirt;
     if (longest > tc::kMaxList || nvirt > tc::kMaxVirtual) return BSA_OK;  // CUDA-core path
+    if ((long long)BH * J > INT_MAX) return BSA_OK;
     if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)out | (uintptr_t)im) & 15) return BSA_OK;
     if (summary && (((uintptr_t)kb | (uintptr_t)vb) & 15)) return BSA_OK;
     if ((uintptr_t)packed & 15) return BSA_OK;
@@ -800,10 +915,32 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     cudaError_t e = cudaFuncSetAttribute(tc::bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));
-    dim3 grid(J, BH);
+    // persistent grid: one CTA per SM takes (head, query block) items from a
+    // counter that lives for this launch only (stream-ordered allocation);
+    // without one, each CTA takes every gridDim.x-th item
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+        return fail(BSA_ERR_CUDA, "tc attention: device query failed");
+    const long long items = (long long)BH * J;
+    prm.items = (int)items;
+    void* counter = nullptr;
+    if (cudaMallocAsync(&counter, sizeof(unsigned), st) == cudaSuccess) {
+        if (cudaMemsetAsync(counter, 0, sizeof(unsigned), st) != cudaSuccess) {
+            cudaFreeAsync(counter, st);
+            counter = nullptr;
+        }
+    } else {
+        cudaGetLastError();  // fall back to the static schedule
+        counter = nullptr;
+    }
+    prm.sched = static_cast<unsigned*>(counter);
+    const int grid = (int)std::min<long long>(items, sms);
     tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5,
                                                                        mkb, mvb, prm);
-    return check_launch("bsa_fwd_tc_kernel");
+    const bsa_status rc = check_launch("bsa_fwd_tc_kernel");
+    if (counter) cudaFreeAsync(counter, st);
+    return rc;
 }
 
 }  // namespace bsa
