@@ -50,6 +50,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -114,7 +115,7 @@ struct Params {
     int packed;       // Q/K/V also given in block order: every tile is one box
     const float* sbias;  // summary biases [BH, J] (natural log), or null for log n_j
     int items;           // work items: (head, query block) pairs, head-major
-    unsigned* sched;     // next item to take (zero at launch), or null: every gridDim.x-th item
+    unsigned* sched;     // [2]: next item, CTAs done (both zero at launch), or null: every gridDim.x-th item
 };
 
 // Where a 128-row tile comes from: gathered rows (mode 0), a box of 128
@@ -153,6 +154,12 @@ __device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int b
     s.c4 = bh;
     return s;
 }
+
+// Work counters of the persistent grid: one pair per (device, stream) slot.
+// Launches on one stream run one after another; the last CTA of a launch
+// puts its pair back to zero for the next one.
+constexpr int kSchedSlots = 64;
+__device__ unsigned g_sched[2 * kSchedSlots];
 
 // A tile source packed in 16 bytes for the producers' table: boxes as
 // x = mode | (summary << 2), y = c1, z = c2 | (c3 << 16), w = c4; gathered
@@ -492,11 +499,13 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     const uint32_t ka = base + OFF_RING + st * kTileBytes;
                     const uint32_t qa = base + OFF_Q;
                     const uint32_t dS = tmem + (uint32_t)(j & 1) * 128;
+                    // the start address is the descriptor's low field (in 16-byte units, no
+                    // carry out below 256 KB): step k by adding the offset to it
+                    const uint64_t dq = ptx::smem_desc(qa, 16, 1024), dk = ptx::smem_desc(ka, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kHD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                        ptx::mma_ss(dS, ptx::smem_desc(qa + off, 16, 1024), ptx::smem_desc(ka + off, 16, 1024), idS,
-                                    kk > 0);
+                        const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                        ptx::mma_ss(dS, dq + off, dk + off, idS, kk > 0);
                     }
                     ptx::mma_commit(bar(BAR_SF + (j & 1)));
                     ptx::mma_commit(bar(BAR_EMPTY + st));
@@ -504,37 +513,49 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (j == n - 1) ptx::mma_commit(bar(BAR_QFREE));  // the item's last S: Q may be replaced
                     return true;
                 };
-                auto issue_pv = [&](int j) -> bool {
-                    const int w = j & 1;
-                    const int u = w ? up1++ : up0++;
-                    if (!wait_bar(bar(BAR_PF + w), (uint32_t)u & 1u, abort_flag, prm.status)) return false;
-                    const int st = kKStages + vc % kVStages;
-                    if (!wait_bar(bar(BAR_FULL + st), (uint32_t)(vc / kVStages) & 1u, abort_flag, prm.status))
-                        return false;
-                    ptx::tc_fence_after();
-                    const uint32_t va = base + OFF_RING + st * kTileBytes;
-                    const uint32_t aP = tmem + (uint32_t)w * 128;
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        // 16 keys per step: P columns advance by 8 (packed bf16 pairs);
-                        // V advances by two 8-row groups of 1024 B; the second
-                        // 64-column half of V is one leading-dimension step (16 KB) away.
-                        ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, aP + kk * 8,
-                                    ptx::smem_desc(va + kk * 2048, kHalfBytes, 1024), idO,
-                                    (j >= 2 || kk > 0) ? 1u : 0u);
-                    }
-                    ptx::mma_commit(bar(BAR_EMPTY + st));
-                    ++vc;
-                    return true;
-                };
                 if (n == 0) ptx::mma_commit(bar(BAR_QFREE));
                 if (n > 0) ok = issue_s(0);
                 if (ok && n > 1) ok = issue_s(1);
                 // the previous item's epilogue must have read O_0 and O_1
                 if (ok && it > 0) ok = wait_bar(bar(BAR_OFREE), (uint32_t)(it - 1) & 1u, abort_flag, prm.status);
+                // steady state: P_j, V_j and K_{j+2} are checked together behind one
+                // fence; PV_j and S_{j+2} then go out back to back and their commits
+                // follow as one group
                 for (int j = 0; ok && j < n; ++j) {
-                    ok = issue_pv(j);
-                    if (ok && j + 2 < n) ok = issue_s(j + 2);
+                    const bool has_s = j + 2 < n;
+                    const int w = j & 1;
+                    const int u = w ? up1++ : up0++;
+                    const int vst = kKStages + vc % kVStages, kst = kc % kKStages;
+                    ok = wait_bar(bar(BAR_PF + w), (uint32_t)u & 1u, abort_flag, prm.status) &&
+                         wait_bar(bar(BAR_FULL + vst), (uint32_t)(vc / kVStages) & 1u, abort_flag, prm.status) &&
+                         (!has_s ||
+                          wait_bar(bar(BAR_FULL + kst), (uint32_t)(kc / kKStages) & 1u, abort_flag, prm.status));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    {
+                        const uint32_t va = base + OFF_RING + vst * kTileBytes;
+                        const uint32_t aP = tmem + (uint32_t)w * 128;
+                        const uint64_t dv = ptx::smem_desc(va, kHalfBytes, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, aP + kk * 8, dv + (uint32_t)(kk * 2048 >> 4),
+                                        idO, (j >= 2 || kk > 0) ? 1u : 0u);
+                    }
+                    if (has_s) {
+                        const uint32_t ka = base + OFF_RING + kst * kTileBytes;
+                        const uint64_t dq = ptx::smem_desc(base + OFF_Q, 16, 1024), dk = ptx::smem_desc(ka, 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kHD / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+                            ptx::mma_ss(tmem + (uint32_t)w * 128, dq + off, dk + off, idS, kk > 0);
+                        }
+                        ptx::mma_commit(bar(BAR_SF + w));
+                        ptx::mma_commit(bar(BAR_EMPTY + kst));
+                        ++kc;
+                        if (j + 2 == n - 1) ptx::mma_commit(bar(BAR_QFREE));  // the item's last S
+                    }
+                    ptx::mma_commit(bar(BAR_EMPTY + vst));
+                    ++vc;
                 }
                 if (!ok) break;
                 ptx::mma_commit(bar(BAR_OF));  // every product of this item is in O_0 / O_1
@@ -607,8 +628,6 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     for (int c = 0; c < kBN; c += 16)
 #pragma unroll
                         for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) mxp[u] *= prm.scale_log2;  // scale > 0 keeps the order
                 } else {
                     const float* bt = bias + (vid - 1) * kBN;
 #pragma unroll
@@ -617,8 +636,10 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                     }
                 }
+                // the real tiles' maxima are of raw Q.K: scale once (scale > 0 keeps the order)
                 const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                                       fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                                       fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]))) *
+                                 (real ? prm.scale_log2 : 1.f);
                 const float m_new = fmaxf(m_ref, mx);
                 const bool need = m_new > m_ref + kRescaleThreshold;
                 if (__any_sync(0xffffffffu, need)) {
@@ -643,21 +664,24 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 float sp[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) sp[u] = 0.f;
+                // A row with no live key yet (m_ref = -inf) has every score at -inf, so
+                // scale 1 and reference 0 give exp2(-inf) = 0 with no per-score select.
                 const bool live = m_ref != -CUDART_INF_F;
+                const float sc = live ? prm.scale_log2 : 1.f, ref = live ? m_ref : 0.f;
                 if (real) {
                     // x holds raw Q.K: one FMA folds the scale and subtracts the reference;
                     // pairs of columns share one f32x2 FMA and one f32x2 add (sp[c & 7]
                     // accumulates exactly as with scalar adds)
-                    const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
-                    const float2 nm2 = make_float2(-m_ref, -m_ref);
+                    const float2 sc2 = make_float2(sc, sc);
+                    const float2 nm2 = make_float2(-ref, -ref);
                     float2 acc2[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int c = 0; c < kBN; c += 2) {
                         const float2 a = ptx::ffma2(make_float2(x[c], x[c + 1]), sc2, nm2);
-                        x[c] = live ? ptx::ex2(a.x) : 0.f;
-                        x[c + 1] = live ? ptx::ex2(a.y) : 0.f;
+                        x[c] = ptx::ex2(a.x);
+                        x[c + 1] = ptx::ex2(a.y);
                         acc2[(c >> 1) & 3] = ptx::fadd2(acc2[(c >> 1) & 3], make_float2(x[c], x[c + 1]));
                     }
 #pragma unroll
@@ -668,7 +692,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 } else {
 #pragma unroll
                     for (int c = 0; c < kBN; ++c) {
-                        x[c] = live ? ptx::ex2(x[c] - m_ref) : 0.f;
+                        x[c] = ptx::ex2(x[c] - ref);
                         sp[c & 7] += x[c];
                     }
                 }
@@ -762,6 +786,15 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
+    if (threadIdx.x == 0 && prm.sched) {
+        // every warp of this CTA is past its last ticket; the last CTA out
+        // leaves both counters at zero for the next launch on this stream
+        __threadfence();
+        if (atomicAdd(prm.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(prm.sched, 0u);
+            atomicExch(prm.sched + 1, 0u);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -809,6 +842,31 @@ static bool make_window_map(CUtensorMap* m, const void* video_base, int T, int H
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The counter pair of (current device, stream); null when every slot is taken
+// (the launch then uses the static schedule).
+static unsigned* sched_slot(cudaStream_t st) {
+    static std::mutex mu;
+    static unsigned* base[64] = {nullptr};
+    static cudaStream_t owner[64][kSchedSlots];
+    static int used[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        base[dev] = static_cast<unsigned*>(p);
+    }
+    for (int i = 0; i < used[dev]; ++i)
+        if (owner[dev][i] == st) return base[dev] + 2 * i;
+    if (used[dev] == kSchedSlots) return nullptr;
+    owner[dev][used[dev]] = st;
+    return base[dev] + 2 * used[dev]++;
 }
 
 // The register split assumes the launch reserves kRegsLaunch registers per
@@ -915,32 +973,19 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
     cudaError_t e = cudaFuncSetAttribute(tc::bsa_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "tc attention attribute: %s", cudaGetErrorString(e));
-    // persistent grid: one CTA per SM takes (head, query block) items from a
-    // counter that lives for this launch only (stream-ordered allocation);
-    // without one, each CTA takes every gridDim.x-th item
+    // persistent grid: one CTA per SM takes (head, query block) items from this
+    // stream's counter pair; without one, each CTA takes every gridDim.x-th item
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess || sms <= 0)
         return fail(BSA_ERR_CUDA, "tc attention: device query failed");
     const long long items = (long long)BH * J;
     prm.items = (int)items;
-    void* counter = nullptr;
-    if (cudaMallocAsync(&counter, sizeof(unsigned), st) == cudaSuccess) {
-        if (cudaMemsetAsync(counter, 0, sizeof(unsigned), st) != cudaSuccess) {
-            cudaFreeAsync(counter, st);
-            counter = nullptr;
-        }
-    } else {
-        cudaGetLastError();  // fall back to the static schedule
-        counter = nullptr;
-    }
-    prm.sched = static_cast<unsigned*>(counter);
+    prm.sched = tc::sched_slot(st);
     const int grid = (int)std::min<long long>(items, sms);
     tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5,
                                                                        mkb, mvb, prm);
-    const bsa_status rc = check_launch("bsa_fwd_tc_kernel");
-    if (counter) cudaFreeAsync(counter, st);
-    return rc;
+    return check_launch("bsa_fwd_tc_kernel");
 }
 
 }  // namespace bsa

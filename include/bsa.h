@@ -22,6 +22,13 @@
  *  - Errors found on the device (an index outside its range, a bounded wait
  *    that expired) are latched in a device status word; bsa_device_status()
  *    synchronises the stream, returns that status and clears it.
+ *  - The tensor-core attention (bsa_fwd_qouter, bsa_fwd_summary with bf16,
+ *    D = 128, M = 128) is a persistent grid that takes its work items from a
+ *    counter pair the library keeps per (device, stream) in static device
+ *    memory (64 streams per device; further streams take a static schedule).
+ *    Launches on one stream run in order and each leaves its pair at zero, so
+ *    the only unsupported use is running two CUDA graphs captured from the
+ *    same stream at the same time.
  *  - Index lists use -1 as padding; kernels read only the first `num` entries.
  *  - dtype: BSA_F32 (float) or BSA_BF16 (bfloat16).  Accumulation is float32.
  *  - LSE outputs are natural-log log-sum-exp of the scaled logits of a row

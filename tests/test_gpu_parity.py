@@ -140,6 +140,38 @@ def test_video_dit_shape_small_bf16(lib, force_simt):
                     force_simt=force_simt)
 
 
+def test_tc_attention_work_counters_across_streams(lib):
+    """The persistent tensor-core attention takes its (head, query block) items
+    from a counter pair per stream that every launch leaves at zero: launches
+    back to back on one stream, and on two streams at once, all give the
+    output and LSE of the first launch bit for bit."""
+    pl = _pipeline()
+    T, H, W, h, topk = 6, 16, 24, 3, 6
+    q, k, v = (x.to(DEV) for x in synthetic.video_qkv(1, h, T, H, W, 128, 909, torch.bfloat16, field=True))
+    geom = pl.Geometry(T=T, H=H, W=W, bT=4, bH=4, bW=8)
+    ref = pl.block_sparse_attention(q, k, v, geom, topk)
+    BH, N, D = q.shape
+    J = ref.index_map.shape[0]
+
+    def launch(stream=None):
+        o = torch.empty_like(q)
+        l = torch.empty((BH, N), dtype=torch.float32, device=DEV)
+        lib.bsa_fwd_qouter(q, k, v, BH, N, D, ref.index_map, ref.block_sizes, J, 128, 0, geom.geometry,
+                           ref.q2k_idx, ref.q2k_num, topk, D ** -0.5, o, l, stream=stream)
+        return o, l
+
+    runs = [launch() for _ in range(3)]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for s in (s1, s2, s1, s2):
+        with torch.cuda.stream(s):
+            runs.append(launch(stream=s))
+    torch.cuda.synchronize()
+    for o, l in runs:
+        assert torch.equal(o, ref.out)
+        assert torch.equal(l, ref.lse)
+
+
 @pytest.mark.parametrize("pass_geometry,packed", [(True, False), (False, False), (True, True)])
 def test_windows_ragged_in_h_and_w_bf16(lib, pass_geometry, packed):
     # (4,4,8) windows over a (5,6,12) grid: full windows load as one TMA box,
