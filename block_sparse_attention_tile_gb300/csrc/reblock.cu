@@ -10,6 +10,8 @@
 // node's lowest-id member, b = the member farthest from a) at the rank that
 // gives the left child ceil(nblocks/2) whole blocks.
 //
+//   (bf16 with D = 128: the moment partials and the features are computed on
+//    the tensor cores instead, reblock_tc.cu)
 //   reblock_moment_kernel      split-K partial sums of q q^T (float32)
 //   reblock_moment_reduce      M = sum of the partials in split order / N
 //   reblock_cholesky_kernel    L = chol(M + ridge * tr(M)/d * I) (float32)
@@ -32,6 +34,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -528,10 +531,18 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
     }
 }
 
+// tensor-core moment partials and features (reblock_tc.cu), bf16 with D = 128;
+// *handled = false when the shape is not covered
+bsa_status reblock_moment_tc(const void* q, int BH, int N, int n_prefix, int splits, float* part, cudaStream_t st,
+                             bool* handled);
+bsa_status reblock_features_tc(const void* k, int BH, int N, int n_prefix, const float* L, void* Lb,
+                               __nv_bfloat16* U, cudaStream_t st, bool* handled);
+
 struct RbWorkspace {
     float* part;
     float* M;
     float* L;
+    __nv_bfloat16* Lb;  // bf16 hi and lo parts of L, [BH][2][D][D] (tensor-core features)
     __nv_bfloat16* U;
     unsigned long long* keys;
     int32_t* tmp;
@@ -548,6 +559,7 @@ static RbWorkspace rb_carve(void* ws, int BH, int Nv, int D) {
     w.part = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * kRbSplits * D * D));
     w.M = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * D * D));
     w.L = reinterpret_cast<float*>(take(sizeof(float) * (size_t)BH * D * D));
+    w.Lb = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * 2 * (size_t)BH * D * D));
     w.U = reinterpret_cast<__nv_bfloat16*>(take(sizeof(__nv_bfloat16) * (size_t)BH * Nv * D));
     w.keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)BH * Nv));
     w.tmp = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)BH * Nv));
@@ -565,9 +577,15 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
                                  float ridge, int32_t* perm, float* moment, float* factor, const RbWorkspace& w,
                                  cudaStream_t st) {
     const int Nv = N - n_prefix;
-    reblock_moment_kernel<T><<<dim3(kRbSplits, BH), 256, 0, st>>>((const T*)q, N, D, n_prefix, w.part);
-    bsa_status rc = check_launch("reblock_moment_kernel");
-    if (rc != BSA_OK) return rc;
+    // bf16 with D = 128: the two contractions on the tensor cores
+    const bool tc = std::is_same<T, __nv_bfloat16>::value && D == 128 && !force_simt();
+    bool handled = false;
+    bsa_status rc = BSA_OK;
+    if (tc && (rc = reblock_moment_tc(q, BH, N, n_prefix, kRbSplits, w.part, st, &handled)) != BSA_OK) return rc;
+    if (!handled) {
+        reblock_moment_kernel<T><<<dim3(kRbSplits, BH), 256, 0, st>>>((const T*)q, N, D, n_prefix, w.part);
+        if ((rc = check_launch("reblock_moment_kernel")) != BSA_OK) return rc;
+    }
     reblock_moment_reduce<<<dim3((D * D + 255) / 256, BH), 256, 0, st>>>(w.part, D, Nv, w.M);
     if ((rc = check_launch("reblock_moment_reduce")) != BSA_OK) return rc;
     const size_t chol_smem = sizeof(float) * (size_t)D * (D + 1);
@@ -575,11 +593,15 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
         cudaFuncSetAttribute(reblock_cholesky_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem);
     reblock_cholesky_kernel<<<BH, kRbMaxD, chol_smem, st>>>(w.M, D, ridge, w.L);
     if ((rc = check_launch("reblock_cholesky_kernel")) != BSA_OK) return rc;
-    const size_t feat_smem = sizeof(float) * (size_t)(kRbMaxD * kRbMaxD + 64 * kRbKs);
-    cudaFuncSetAttribute(reblock_features_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)feat_smem);
-    reblock_features_kernel<T><<<dim3((Nv + 63) / 64, BH), 256, feat_smem, st>>>((const T*)k, N, D, n_prefix, w.L,
-                                                                                  w.U);
-    if ((rc = check_launch("reblock_features_kernel")) != BSA_OK) return rc;
+    handled = false;
+    if (tc && (rc = reblock_features_tc(k, BH, N, n_prefix, w.L, w.Lb, w.U, st, &handled)) != BSA_OK) return rc;
+    if (!handled) {
+        const size_t feat_smem = sizeof(float) * (size_t)(kRbMaxD * kRbMaxD + 64 * kRbKs);
+        cudaFuncSetAttribute(reblock_features_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)feat_smem);
+        reblock_features_kernel<T><<<dim3((Nv + 63) / 64, BH), 256, feat_smem, st>>>((const T*)k, N, D, n_prefix,
+                                                                                      w.L, w.U);
+        if ((rc = check_launch("reblock_features_kernel")) != BSA_OK) return rc;
+    }
     reblock_iota_kernel<<<dim3((Nv + 255) / 256, BH), 256, 0, st>>>(perm, Nv);
     if ((rc = check_launch("reblock_iota_kernel")) != BSA_OK) return rc;
     const int NB = (Nv + block - 1) / block;
@@ -624,7 +646,7 @@ size_t bsa_reblock_workspace(int BH, int N, int D, int n_prefix) {
     const size_t Nv = (size_t)(N - n_prefix);
     auto r = [](size_t b) { return (b + 255) / 256 * 256; };
     return r(sizeof(float) * (size_t)BH * kRbSplits * D * D) + 2 * r(sizeof(float) * (size_t)BH * D * D) +
-           r(sizeof(__nv_bfloat16) * (size_t)BH * Nv * D) + r(sizeof(unsigned long long) * (size_t)BH * Nv) +
+           r(sizeof(__nv_bfloat16) * 2 * (size_t)BH * D * D) + r(sizeof(__nv_bfloat16) * (size_t)BH * Nv * D) + r(sizeof(unsigned long long) * (size_t)BH * Nv) +
            r(sizeof(int32_t) * (size_t)BH * Nv);
 }
 
