@@ -699,12 +699,20 @@ class BlockWorkload:
         if self.reblock:
             Nv = self.N - self.w.get("n_text", 0)
             el = self.q.element_size()
-            rflops = 2 * 2.0 * self.BH * Nv * D * D  # the moment Q^T Q and the features K L
-            secondary["reblock"] = {"bound": "alu", "achieved": rflops / (stage_ms["reblock"] * 1e-3) / 1e12,
-                                    "peak": fp32, "unit": "TFLOP/s",
-                                    "frac": rflops / (stage_ms["reblock"] * 1e-3) / 1e12 / fp32,
-                                    "flops_per_launch": rflops,
-                                    "note": "moment and features; the partition levels are latency-bound"}
+            # the stage is the tree levels' feature passes (three reads of the bf16 unit features a
+            # level) plus one read of Q_v and K_v and one write of the features; the moment and
+            # the features (2 * 2 * BH * Nv * D^2 FLOP) run on the tensor cores
+            NB = -(-Nv // self.w["M"])
+            levels = max(0, (NB - 1).bit_length())
+            fbytes = self.BH * Nv * D * 2
+            rbytes = levels * 3 * fbytes + 2 * self.BH * Nv * D * el + fbytes
+            rgbs = rbytes / (stage_ms["reblock"] * 1e-3) / 1e9
+            secondary["reblock"] = {"bound": "hbm", "achieved": rgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                    "frac": rgbs / peaks["hbm_gbs"], "bytes_per_launch": rbytes,
+                                    "flops_per_launch": 2 * 2.0 * self.BH * Nv * D * D,
+                                    "note": "%d tree levels, each reading the unit features three times; the "
+                                            "levels are latency-bound (radix-select passes and cluster barriers)"
+                                            % levels}
             pb = 3 * 2 * self.q.numel() * el
             secondary["permute"] = {"bound": "hbm", "achieved": pb / (stage_ms["permute"] * 1e-3) / 1e9,
                                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
