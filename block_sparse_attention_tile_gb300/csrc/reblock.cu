@@ -263,6 +263,28 @@ __device__ __forceinline__ unsigned long long rb_block_max(unsigned long long v,
     return t;
 }
 
+// Exclusive prefix sum over the CTA's threads (thread order), and the total.
+// `wsum` holds one int per warp.
+__device__ __forceinline__ int rb_block_exscan(int v, int* wsum, int& total) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = (int)(blockDim.x >> 5);
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    __syncthreads();
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) before += wsum[w];
+        total += wsum[w];
+    }
+    return before + x - v;
+}
+
 // The squared distance of a member's feature row to `c`, or its projection on
 // `c` (fp32 arithmetic on the bf16 row; a thread per member).
 template <bool DIST>
@@ -314,8 +336,9 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     __shared__ unsigned long long red[kRbSplitThreads / 32];
     __shared__ unsigned int hist[256];
     __shared__ int scan[kRbSplitThreads];
+    __shared__ int wsum[kRbSplitThreads / 32];
     __shared__ unsigned int hsum[256];
-    __shared__ int s_digit, s_need;
+    __shared__ int s_digit, s_need, s_bincnt;
     __shared__ unsigned long long s_slot;  // this CTA's partial, read by the cluster
     __shared__ int s_count;                // this CTA's number of left members
     cg::cluster_group cl = cg::this_cluster();
@@ -360,6 +383,7 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     // 2-3. the landmarks: a = farthest from s0, then b = farthest from a (ties to the lower id)
     for (int round = 0; round < 2; ++round) {
         best = 0;
+#pragma unroll 2
         for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
             const int t = ord[m];
             const float d2 = rb_row_op<true>(Uh + (long long)t * D, ua, D);
@@ -380,6 +404,7 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     for (int d = tid; d < D; d += kRbSplitThreads) ua[d] -= ub[d];
     __syncthreads();
     // 4. keys (projection, token id), ascending
+#pragma unroll 2
     for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
         const int t = ord[m];
         const float p = rb_row_op<false>(Uh + (long long)t * D, ua, D);
@@ -406,19 +431,31 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
             for (int r = 0; r < C; ++r) h += cl.map_shared_rank(hist, r)[tid];
             hsum[tid] = h;
         }
-        __syncthreads();
-        if (tid == 0) {
-            int b = 0, nd = need;
-            for (; b < 255; ++b) {  // (the rank always falls inside: cap_left < n)
-                if (nd <= (int)hsum[b]) break;
-                nd -= (int)hsum[b];
-            }
-            s_digit = b;
-            s_need = nd;
+        // the digit: the first bin whose running count reaches `need` (the rank
+        // always falls inside: cap_left < n), found by a scan over the bins
+        int tot;
+        const int h = tid < 256 ? (int)hsum[tid] : 0;
+        const int before = rb_block_exscan(h, wsum, tot);
+        if (tid < 256 && before < need && (need <= before + h || tid == 255)) {
+            s_digit = tid;
+            s_need = need - before;
+            s_bincnt = h;
         }
         __syncthreads();
         prefix |= (unsigned long long)s_digit << shift;
         need = s_need;
+        if (s_bincnt == 1 && shift > 0) {
+            // one key of the node carries these high bits: it is the cut; one pass
+            // finds its low bits (the same decision in every CTA: hsum is shared)
+            const unsigned long long mask = ~0ull << shift;
+            unsigned long long found = 0;
+            for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+                const unsigned long long key = ky[m];
+                if ((key & mask) == prefix) found = key;
+            }
+            prefix = cluster_max(found);
+            break;
+        }
         cl.sync();  // the histograms are read before the next pass clears them
     }
     const unsigned long long cut = prefix;  // keys <= cut go left (exactly cap_left: keys are distinct)
@@ -429,17 +466,9 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     const int m0 = c0 + min(nc, tid * per), m1 = c0 + min(nc, tid * per + per);
     int nl = 0;
     for (int m = m0; m < m1; ++m) nl += ky[m] <= cut;
-    scan[tid] = nl;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int t = 0; t < kRbSplitThreads; ++t) {
-            const int c = scan[t];
-            scan[t] = run;
-            run += c;
-        }
-        s_count = run;
-    }
+    int nl_total;
+    scan[tid] = rb_block_exscan(nl, wsum, nl_total);
+    if (tid == 0) s_count = nl_total;
     cl.sync();
     int left_before = 0, right_before = 0;
     for (int r = 0; r < rank; ++r) {
