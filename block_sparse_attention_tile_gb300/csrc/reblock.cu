@@ -637,10 +637,10 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
     int levels = 0;
     while ((1 << levels) < NB) ++levels;  // depth of the binary tree over NB blocks
     for (int l = 0; l < levels; ++l) {
-        // CTAs per node: about 4096 members each, a power of two up to 8
+        // CTAs per node: about 2048 members each, a power of two up to 8
         const long long per_node = (long long)Nv >> l;
         int C = 1;
-        while (C < 8 && per_node / (2 * C) >= 4096) C *= 2;
+        while (C < 8 && per_node / (2 * C) >= 2048) C *= 2;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((1u << l) * C, BH);
         cfg.blockDim = dim3(kRbSplitThreads);
