@@ -116,12 +116,35 @@ __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* 
     __shared__ float s_tr, s_piv;
     const int bh = blockIdx.x, i = threadIdx.x, ld = D + 1;
     const float* Mh = M + (long long)bh * D * D;
-    for (int e = i; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = Mh[e];
+    if ((D & 3) == 0 && (((uintptr_t)Mh) & 15) == 0) {
+        // 16-byte loads, several in flight per thread
+        const int nq = D * D / 4, qpr = D / 4;
+#pragma unroll 8
+        for (int e = i; e < nq; e += blockDim.x) {
+            const float4 v = *reinterpret_cast<const float4*>(Mh + 4 * e);
+            float* a = A + (e / qpr) * ld + 4 * (e % qpr);
+            a[0] = v.x;
+            a[1] = v.y;
+            a[2] = v.z;
+            a[3] = v.w;
+        }
+    } else {
+#pragma unroll 8
+        for (int e = i; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = Mh[e];
+    }
     __syncthreads();
     if (i == 0) {
-        float tr = 0.f;
-        for (int d = 0; d < D; ++d) tr += A[d * ld + d];
-        s_tr = tr;
+        // the trace in a fixed order, four partial sums
+        float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+        int d = 0;
+        for (; d + 4 <= D; d += 4) {
+            t0 += A[d * ld + d];
+            t1 += A[(d + 1) * ld + d + 1];
+            t2 += A[(d + 2) * ld + d + 2];
+            t3 += A[(d + 3) * ld + d + 3];
+        }
+        for (; d < D; ++d) t0 += A[d * ld + d];
+        s_tr = (t0 + t1) + (t2 + t3);
     }
     __syncthreads();
     if (i < D) A[i * ld + i] += ridge * s_tr / D;
@@ -129,8 +152,18 @@ __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* 
     for (int j = 0; j < D; ++j) {
         float t = 0.f;
         if (i >= j && i < D) {
-            t = A[i * ld + j];
-            for (int c = 0; c < j; ++c) t = fmaf(-A[i * ld + c], A[j * ld + c], t);
+            // four independent partial sums: the loads run ahead of a short FMA chain
+            float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+            int c = 0;
+#pragma unroll 2
+            for (; c + 4 <= j; c += 4) {
+                t0 = fmaf(A[i * ld + c], A[j * ld + c], t0);
+                t1 = fmaf(A[i * ld + c + 1], A[j * ld + c + 1], t1);
+                t2 = fmaf(A[i * ld + c + 2], A[j * ld + c + 2], t2);
+                t3 = fmaf(A[i * ld + c + 3], A[j * ld + c + 3], t3);
+            }
+            for (; c < j; ++c) t0 = fmaf(A[i * ld + c], A[j * ld + c], t0);
+            t = A[i * ld + j] - ((t0 + t1) + (t2 + t3));
         }
         if (i == j) s_piv = t > 0.f ? sqrtf(t) : 0.f;
         __syncthreads();
