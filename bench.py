@@ -604,11 +604,27 @@ class BlockWorkload:
             chunks.append((h0, h0 + n_h))
             h0 += n_h
         per_head = self.J * self.w["M"] * self.w["D"]
-        pk = (torch.empty((3 * heads_per_chunk * per_head,), dtype=self.dtype, device=self.dev)
-              if self.packed is not None else None)
         dq, dk, dv = d_in
         hq, hk, hv = h_in
         (hout,) = h_out
+        # Chunks alternate between two compute streams, each with its own scratch (route
+        # workspace, packed copy, reweight and reblock workspaces), so that one chunk's pool
+        # and route run on the SMs that the other chunk's attention has finished with.
+        comps = [comp, torch.cuda.Stream()]
+        scratch = []
+        for sidx in range(2):
+            scratch.append({
+                "route_ws": self.route_ws if sidx == 0 else torch.empty_like(self.route_ws),
+                "rw_ws": (self.rw_ws if sidx == 0 or self.rw_ws is None else torch.empty_like(self.rw_ws)),
+                "rb_ws": (getattr(self, "rb_ws", None) if sidx == 0 or not self.reblock
+                          else torch.empty_like(self.rb_ws)),
+                "pk": (torch.empty((3 * heads_per_chunk * per_head,), dtype=self.dtype, device=self.dev)
+                       if self.packed is not None else None)})
+
+        def use(sidx):
+            for name in ("route_ws", "rw_ws", "rb_ws"):
+                if scratch[sidx][name] is not None:
+                    setattr(self, name, scratch[sidx][name])
 
         def step():
             from block_sparse_attention_tile_gb300 import bsa
@@ -624,17 +640,25 @@ class BlockWorkload:
                     e.record(h2d_s)
                 ready.append(e)
             self.tile_map()
-            for (h0, h1), e in zip(chunks, ready):
-                comp.wait_event(e)
+            mapped = torch.cuda.Event()
+            mapped.record(comp)
+            comps[1].wait_event(mapped)
+            for c, ((h0, h1), e) in enumerate(zip(chunks, ready)):
+                cs = comps[c % 2]
+                cs.wait_event(e)
+                use(c % 2)
+                pk = scratch[c % 2]["pk"]
                 # a contiguous [3, h1 - h0, J, M, D] view for this chunk's packed copy
                 pkc = None if pk is None else pk[:3 * (h1 - h0) * per_head].view(3, h1 - h0, self.J, self.w["M"],
                                                                                    self.w["D"])
-                self.run_heads(dq, dk, dv, h0, h1, pkc)
-                done = torch.cuda.Event()
-                done.record(comp)
+                with torch.cuda.stream(cs):
+                    self.run_heads(dq, dk, dv, h0, h1, pkc)
+                    done = torch.cuda.Event()
+                    done.record(cs)
                 d2h_s.wait_event(done)
                 with torch.cuda.stream(d2h_s):
                     hout[h0:h1].copy_(self.out[h0:h1], non_blocking=True)
+            use(0)
             fin = torch.cuda.Event()
             fin.record(d2h_s)
             comp.wait_event(fin)
@@ -1045,7 +1069,8 @@ def gpu_arm(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps_timed": e2e_steps, "aggregate": "median of per-step times",
                     "ms_per_step_mean": e2e_mean, "ms_per_step_max": e2e_max,
-                    "pipelining": ("head chunks: copies in and out overlap the compute of other heads"
+                    "pipelining": ("head chunks on two compute streams: copies in and out overlap the compute "
+                                   "of other heads"
                                    if hasattr(wl, "make_e2e") else "none: copy in, compute, copy out"),
                     "gpu_launches_per_step": e2e_launches, "matches_device_run": e2e_match},
             "gpu_launches": wl.launches_per_step * args.steps,

@@ -172,6 +172,33 @@ def test_tc_attention_work_counters_across_streams(lib):
         assert torch.equal(l, ref.lse)
 
 
+def test_tc_attention_static_schedule_past_the_counter_slots(lib):
+    """Past the library's 64 per-device stream counters a stream's launches
+    take every gridDim.x-th item instead: 70 streams (the first of them may
+    already hold slots) all give the first launch's output and LSE bit for bit."""
+    pl = _pipeline()
+    T, H, W, h, topk = 6, 16, 24, 2, 5
+    q, k, v = (x.to(DEV) for x in synthetic.video_qkv(1, h, T, H, W, 128, 919, torch.bfloat16, field=True))
+    geom = pl.Geometry(T=T, H=H, W=W, bT=4, bH=4, bW=8)
+    ref = pl.block_sparse_attention(q, k, v, geom, topk)
+    BH, N, D = q.shape
+    J = ref.index_map.shape[0]
+    streams = [torch.cuda.Stream() for _ in range(70)]
+    torch.cuda.synchronize()
+    runs = []
+    for s in streams:
+        o = torch.empty_like(q)
+        l = torch.empty((BH, N), dtype=torch.float32, device=DEV)
+        with torch.cuda.stream(s):
+            lib.bsa_fwd_qouter(q, k, v, BH, N, D, ref.index_map, ref.block_sizes, J, 128, 0, geom.geometry,
+                               ref.q2k_idx, ref.q2k_num, topk, D ** -0.5, o, l, stream=s)
+        runs.append((o, l))
+    torch.cuda.synchronize()
+    for o, l in runs:
+        assert torch.equal(o, ref.out)
+        assert torch.equal(l, ref.lse)
+
+
 @pytest.mark.parametrize("pass_geometry,packed", [(True, False), (False, False), (True, True)])
 def test_windows_ragged_in_h_and_w_bf16(lib, pass_geometry, packed):
     # (4,4,8) windows over a (5,6,12) grid: full windows load as one TMA box,
