@@ -11,7 +11,10 @@
 // passes), then writes the selected ids in ascending order with ballots.
 #include <algorithm>
 
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace bsa {
 
@@ -265,11 +268,11 @@ __global__ void __launch_bounds__(256, 2) route_gemm_kernel(const float* __restr
         As[buf][ld0 + 0][lr] = qa.x; As[buf][ld0 + 1][lr] = qa.y; As[buf][ld0 + 2][lr] = qa.z; As[buf][ld0 + 3][lr] = qa.w;
         Bs[buf][ld0 + 0][lr] = kb.x; Bs[buf][ld0 + 1][lr] = kb.y; Bs[buf][ld0 + 2][lr] = kb.z; Bs[buf][ld0 + 3][lr] = kb.w;
     };
-    float acc[8][8];
+    float2 acc2[8][4];  // acc2[i][j] = outputs (i, 2j), (i, 2j + 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc2[i][j] = make_float2(0.f, 0.f);
     const int nst = (D + kGK - 1) / kGK;
     load_stage(0);
     store_stage(0);
@@ -284,11 +287,16 @@ __global__ void __launch_bounds__(256, 2) route_gemm_kernel(const float* __restr
             const float4 b0 = *reinterpret_cast<const float4*>(&Bs[buf][dd][4 * tx]);
             const float4 b1 = *reinterpret_cast<const float4*>(&Bs[buf][dd][4 * tx + 64]);
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                                  make_float2(b1.z, b1.w)};
+            // pairs of outputs share one f32x2 FMA: per lane the same rounding as fmaf, so E is
+            // bit for bit that of the fused kernel
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+                const float2 a2 = make_float2(av[i], av[i]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc2[i][j] = ptx::ffma2(a2, bp[j], acc2[i][j]);
+            }
         }
         if (st + 1 < nst) {
             store_stage(buf ^ 1);  // the other buffer was last read in step st - 1
@@ -304,8 +312,8 @@ __global__ void __launch_bounds__(256, 2) route_gemm_kernel(const float* __restr
         for (int jh = 0; jh < 2; ++jh) {
             const int c = c0 + 4 * tx + jh * 64;
             float* dst = eh + (long long)r * J + c;
-            const float v0 = acc[i][4 * jh] * scale, v1 = acc[i][4 * jh + 1] * scale;
-            const float v2 = acc[i][4 * jh + 2] * scale, v3 = acc[i][4 * jh + 3] * scale;
+            const float v0 = acc2[i][2 * jh].x * scale, v1 = acc2[i][2 * jh].y * scale;
+            const float v2 = acc2[i][2 * jh + 1].x * scale, v3 = acc2[i][2 * jh + 1].y * scale;
             if ((J & 3) == 0 && c + 3 < J) {
                 *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
             } else {
