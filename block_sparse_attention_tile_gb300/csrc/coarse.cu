@@ -16,7 +16,10 @@
 //                            tokens of the routed blocks (one pass over O).
 #include <math_constants.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace bsa {
 
@@ -171,10 +174,17 @@ __global__ void __launch_bounds__(kCoThreads, 3) coarse_attention_kernel(const f
                     for (int e = 0; e < 4; ++e) vv[4 * q + e] = c + e < D ? Vs[kk * D + c + e] : 0.f;
                 }
             }
+            // pairs of outputs share one f32x2 FMA (per lane the same rounding as fmaf)
 #pragma unroll
-            for (int a = 0; a < RPT; ++a)
+            for (int a = 0; a < RPT; ++a) {
+                const float2 p2 = make_float2(pw[a], pw[a]);
 #pragma unroll
-                for (int q = 0; q < 4 * NQ; ++q) acc[a][q] = fmaf(pw[a], vv[q], acc[a][q]);
+                for (int q = 0; q < 4 * NQ; q += 2) {
+                    const float2 r = ptx::ffma2(p2, make_float2(vv[q], vv[q + 1]), make_float2(acc[a][q], acc[a][q + 1]));
+                    acc[a][q] = r.x;
+                    acc[a][q + 1] = r.y;
+                }
+            }
         }
         __syncthreads();
     }
