@@ -75,6 +75,10 @@ WORKLOADS = {
 DEFAULT = "video_dit_bsa"
 
 
+# GB300 dense bf16 tensor peak as the metric names it (~2.2 PFLOP/s), reported beside the measured one
+NOMINAL_BF16_TFLOPS = 2200.0
+
+
 def metric_flops(w):
     if w["kind"] == "token":
         return 4.0 * w["B"] * w["HQ"] * w["T"] * w["D"] * w["S"] * w["BS"]
@@ -700,9 +704,13 @@ class BlockWorkload:
         D, J = self.w["D"], self.J
         attn_s = stage_ms["attention"] * 1e-3
         if self.w["dtype"] == "bf16":
-            peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+            # the attention launch is timed on its own (milliseconds, not a seconds-long loop):
+            # graded against the burst bf16 peak, with the nominal dense peak beside it
+            peak = peaks["bf16_tflops"]
             roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
-                    "peak_kind": peak_kind + " bf16 sustained"}
+                    "peak_kind": peak_kind + " bf16 burst",
+                    "frac_nominal": flops / attn_s / 1e12 / NOMINAL_BF16_TFLOPS,
+                    "nominal_peak": NOMINAL_BF16_TFLOPS}
         else:
             peak = fp32_peak(peaks, props)
             roof = {"bound": "alu", "achieved": flops / attn_s / 1e12, "peak": peak, "unit": "TFLOP/s",
@@ -881,7 +889,7 @@ class TokenWorkload:
         w = self.w
         B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
         k1_s = stage_ms["partials"] * 1e-3
-        tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        tensor_peak = peaks["bf16_tflops"]  # launches timed on their own: the burst peak
         t_flop = flops / (tensor_peak * 1e12)
         t_byte = k1_bytes / (peaks["hbm_gbs"] * 1e9)
         if t_byte >= t_flop:
@@ -891,7 +899,8 @@ class TokenWorkload:
         else:
             ach = flops / k1_s / 1e12
             roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
-                    "peak_kind": peak_kind + " bf16 sustained"}
+                    "peak_kind": peak_kind + " bf16 burst", "frac_nominal": ach / NOMINAL_BF16_TFLOPS,
+                    "nominal_peak": NOMINAL_BF16_TFLOPS}
         roof["frac"] = roof["achieved"] / roof["peak"]
         roof["traffic"] = read_traffic(self.name)
         roof["kernel"] = "bsa_fwd_kvouter partials (K1)"

@@ -69,7 +69,6 @@ _SIGS = {
     "bsa_permute_rows": (I, [P, P, I, I, I, I, I, P, I, P]),
     "bsa_coarse_attention": (I, [P, I64, P, I64, I, I, I, P, P]),
     "bsa_coarse_apply": (I, [P, I, P, P, I, I, I, I, P, P, I, I, I, P]),
-    "bsa_set_force_simt": (None, [I]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -123,10 +122,6 @@ def bsa_last_error():
 def bsa_device_status(stream=None):
     """Synchronises the stream; returns (and clears) the device status code."""
     return _lib.bsa_device_status(_stream(stream))
-
-
-def bsa_set_force_simt(force):
-    _lib.bsa_set_force_simt(1 if force else 0)
 
 
 def bsa_tile_count(T, H, W, bT, bH, bW, n_prefix, permuted, M):

@@ -111,7 +111,7 @@ struct Params {
     // tiling, when known: prefix blocks are contiguous rows; a video window
     // that is not ragged in H or W is one box of the 5-D (D, W, H, T, head) map
     int geo, window;  // geometry given; 5-D window boxes usable
-    int T, H, W, bT, bH, bW, nH, nW;
+    int T, H, W, bT, bH, bW, nH, nW, n_prefix;
     int packed;       // Q/K/V also given in block order: every tile is one box
     const float* sbias;  // summary biases [BH, J] (natural log), or null for log n_j
     int items;           // work items: (head, query block) pairs, head-major
@@ -155,11 +155,34 @@ __device__ __forceinline__ TileSrc tile_source(int blk, const Params& prm, int b
     return s;
 }
 
-// Work counters of the persistent grid: one pair per (device, stream) slot.
-// Launches on one stream run one after another; the last CTA of a launch
-// puts its pair back to zero for the next one.
-constexpr int kSchedSlots = 64;
-__device__ unsigned g_sched[2 * kSchedSlots];
+// tile_source, checked against the index map: a box covers the rows the tile
+// map put in the block only if the geometry describes that map, so the first
+// and last member and the member count are compared with what the box
+// holds.  On a mismatch the tile is gathered row by row through the index
+// map (always correct) and BSA_ERR_INDEX tells the caller its geometry is
+// wrong.  Summary tiles and the packed copy (written from the index map
+// itself) need no check.
+__device__ __forceinline__ TileSrc checked_source(int blk, const Params& prm, int bh, int nv) {
+    TileSrc s = tile_source(blk, prm, bh);
+    if (blk < 0 || prm.packed || s.mode == 0) return s;
+    const int32_t* im = prm.index_map + (long long)blk * 128;
+    int first, last, n;
+    if (s.mode == 1) {  // a dense-prefix block: consecutive tokens
+        first = blk * 128;
+        n = min(128, prm.n_prefix - first);
+        last = first + n - 1;
+    } else {            // a 3-D window, clipped at T
+        const int t_end = min(s.c3 + prm.bT, prm.T);
+        n = (t_end - s.c3) * prm.bH * prm.bW;
+        first = prm.n_prefix + (s.c3 * prm.H + s.c2) * prm.W + s.c1;
+        last = prm.n_prefix + ((t_end - 1) * prm.H + s.c2 + prm.bH - 1) * prm.W + s.c1 + prm.bW - 1;
+    }
+    if (n != nv || n <= 0 || im[0] != first || im[n - 1] != last) {
+        raise_status(prm.status, BSA_ERR_INDEX);
+        s.mode = 0;
+    }
+    return s;
+}
 
 // A tile source packed in 16 bytes for the producers' table: boxes as
 // x = mode | (summary << 2), y = c1, z = c2 | (c3 << 16), w = c4; gathered
@@ -306,7 +329,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         blk = -(t + 1);
                         nv = min(kBN, Jr - t * kBN);
                     }
-                    srcs[s] = pack_src(tile_source(blk, prm, bh), blk, nv);
+                    srcs[s] = pack_src(checked_source(blk, prm, bh, nv), blk, nv);
                     info[s] = nv | ((blk < 0 ? -blk : 0) << 8);
                 }
                 __syncwarp();
@@ -389,7 +412,7 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     break;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(bar(BAR_QFULL), kTileBytes);
                 __syncwarp();
-                const TileSrc src = tile_source(qb, prm, bh);
+                const TileSrc src = checked_source(qb, prm, bh, nq);
                 const uint32_t d = base + OFF_Q, qbar = bar(BAR_QFULL);
                 if (src.mode == 0) {
                     int rq[4];
@@ -414,7 +437,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             int4 src_next = make_int4(0, 0, 0, 0);
             auto prepare = [&](int jt) {
                 if (dense_row) {
-                    src_next = pack_src(tile_source(jt, prm, bh), jt, prm.block_sizes[jt]);
+                    const int nv = prm.block_sizes[jt];
+                    src_next = pack_src(checked_source(jt, prm, bh, nv), jt, nv);
                 } else {
                     src_next = srcs[jt];
                 }
@@ -844,31 +868,6 @@ static bool make_window_map(CUtensorMap* m, const void* video_base, int T, int H
     return r == CUDA_SUCCESS;
 }
 
-// The counter pair of (current device, stream); null when every slot is taken
-// (the launch then uses the static schedule).
-static unsigned* sched_slot(cudaStream_t st) {
-    static std::mutex mu;
-    static unsigned* base[64] = {nullptr};
-    static cudaStream_t owner[64][kSchedSlots];
-    static int used[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!base[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess || !p) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        base[dev] = static_cast<unsigned*>(p);
-    }
-    for (int i = 0; i < used[dev]; ++i)
-        if (owner[dev][i] == st) return base[dev] + 2 * i;
-    if (used[dev] == kSchedSlots) return nullptr;
-    owner[dev][used[dev]] = st;
-    return base[dev] + 2 * used[dev]++;
-}
-
 // The register split assumes the launch reserves kRegsLaunch registers per
 // thread; refuse the tensor-core path otherwise (setmaxnreg.inc would wait).
 static bool register_split_fits() {
@@ -935,6 +934,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
         prm.bW = bW;
         prm.nH = (H + bH - 1) / bH;
         prm.nW = (W + bW - 1) / bW;
+        prm.n_prefix = n_prefix;
         if (!perm && bT * bH * bW == tc::kBN) {
             const size_t off = (size_t)n_prefix * tc::kHD * 2;
             if (tc::make_window_map(&mq5, (const char*)q + off, T, H, W, BH, N, bT, bH, bW) &&
@@ -981,7 +981,7 @@ bsa_status tc_block_attention(const void* q, const void* k, const void* v, int B
         return fail(BSA_ERR_CUDA, "tc attention: device query failed");
     const long long items = (long long)BH * J;
     prm.items = (int)items;
-    prm.sched = tc::sched_slot(st);
+    prm.sched = sched_counter(st);
     const int grid = (int)std::min<long long>(items, sms);
     tc::bsa_fwd_tc_kernel<<<grid, tc::kThreads, tc::SMEM_BYTES, st>>>(mq, mk, mv, mqr, mkr, mvr, mq5, mk5, mv5,
                                                                        mkb, mvb, prm);

@@ -1,6 +1,7 @@
 // Library-wide state: error messages, the device status word, host helpers.
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -10,7 +11,6 @@
 namespace bsa {
 
 static thread_local char g_msg[512] = "";
-static bool g_force_simt = false;
 
 // One status word per device: kernels latch BSA_ERR_INDEX / BSA_ERR_TIMEOUT here.
 __device__ int g_device_status = 0;
@@ -50,7 +50,43 @@ int* status_word() {
     return addr[dev];
 }
 
-bool force_simt() { return g_force_simt; }
+__device__ unsigned g_sched[2 * kSchedSlots];
+
+unsigned* sched_counter(cudaStream_t st) {
+    static std::mutex mu;
+    static unsigned* base[64] = {nullptr};
+    static cudaStream_t owner[64][kSchedSlots];
+    static int used[64] = {0};
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        base[dev] = static_cast<unsigned*>(p);
+    }
+    for (int i = 0; i < used[dev]; ++i)
+        if (owner[dev][i] == st) return base[dev] + 2 * i;
+    if (used[dev] == kSchedSlots) return nullptr;
+    owner[dev][used[dev]] = st;
+    return base[dev] + 2 * used[dev]++;
+}
+
+// BSA_FORCE_SIMT (set, and not "0") routes every attention stage to its
+// CUDA-core kernel; the tests use it to compare the two kernel families.
+bool force_simt() {
+    const char* e = std::getenv("BSA_FORCE_SIMT");
+    return e && e[0] && !(e[0] == '0' && e[1] == 0);
+}
 
 }  // namespace bsa
 
@@ -59,8 +95,6 @@ extern "C" {
 int bsa_version(void) { return 100; }
 
 const char* bsa_last_error(void) { return bsa::g_msg; }
-
-void bsa_set_force_simt(int force) { bsa::g_force_simt = force != 0; }
 
 bsa_status bsa_device_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(bsa::as_stream(stream));

@@ -23,6 +23,17 @@ int* status_word();
 // Whether the caller asked for the CUDA-core kernels only.
 bool force_simt();
 
+// Work counters of the persistent tensor-core kernels: a pair of unsigned
+// (next item, CTAs done), both zero between launches, per (current device,
+// stream) in static device memory.  Launches on one stream run one after
+// another and the last CTA of each puts its pair back to zero.  Returns null
+// (the kernel then takes every gridDim.x-th item, a static schedule) when
+// all kSchedSlots pairs of the device are taken or when the stream is being
+// captured into a CUDA graph: a graph may later be replayed while other work
+// runs on the stream it was captured from, and must not share a pair with it.
+constexpr int kSchedSlots = 64;
+unsigned* sched_counter(cudaStream_t st);
+
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 #define BSA_REQUIRE(cond, ...)                                           \

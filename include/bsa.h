@@ -22,13 +22,17 @@
  *  - Errors found on the device (an index outside its range, a bounded wait
  *    that expired) are latched in a device status word; bsa_device_status()
  *    synchronises the stream, returns that status and clears it.
- *  - The tensor-core attention (bsa_fwd_qouter, bsa_fwd_summary with bf16,
- *    D = 128, M = 128) is a persistent grid that takes its work items from a
- *    counter pair the library keeps per (device, stream) in static device
- *    memory (64 streams per device; further streams take a static schedule).
- *    Launches on one stream run in order and each leaves its pair at zero, so
- *    the only unsupported use is running two CUDA graphs captured from the
- *    same stream at the same time.
+ *  - The tensor-core attention kernels (bsa_fwd_qouter, bsa_fwd_summary and
+ *    bsa_fwd_qouter_tokens with bf16, D = 128) are persistent grids that take
+ *    their work items from a counter pair the library keeps per (device,
+ *    stream) in static device memory (64 streams per device; further streams
+ *    take a static schedule).  Launches on one stream run in order and each
+ *    leaves its pair at zero.  A launch made while its stream is being
+ *    captured into a CUDA graph takes the static schedule instead, so a
+ *    replayed graph never shares a counter pair with other work.
+ *  - Static device state (the status word, the counter pairs, the scratch of
+ *    bsa_build_reverse_index_noalloc) is looked up once per device and cached:
+ *    cudaDeviceReset is not supported while the library is in use.
  *  - Index lists use -1 as padding; kernels read only the first `num` entries.
  *  - dtype: BSA_F32 (float) or BSA_BF16 (bfloat16).  Accumulation is float32.
  *  - LSE outputs are natural-log log-sum-exp of the scaled logits of a row
@@ -200,8 +204,13 @@ bsa_status bsa_route_topk_grouped(const float* qbar, const float* kbar, int BH, 
  * permutation was given), or NULL.  With it the tensor-core kernel loads a
  * whole (bT,bH,bW) window (not ragged in H or W) or a contiguous prefix
  * block with one TMA box per half tile; without it, or for other blocks,
- * tiles are gathered four rows per TMA operation through index_map.  A
- * geometry that does not describe index_map gives wrong results.
+ * tiles are gathered four rows per TMA operation through index_map.  The
+ * host checks the geometry's sizes against N, J and prefix_blocks
+ * (BSA_ERR_INVALID_ARG); the kernel compares the first and last member and
+ * the member count of every box it would load with index_map and
+ * block_sizes, gathers that tile through index_map instead where they
+ * differ, and latches BSA_ERR_INDEX, so a geometry that does not describe
+ * index_map still gives correct results but is reported.
  * packed: [device] the block-ordered copy written by bsa_pool_blocks from
  * the same q, k, v and index_map, or NULL.  With it the tensor-core kernel
  * loads every tile (permuted blocks, windows ragged in H or W included) as
@@ -412,10 +421,6 @@ bsa_status bsa_reblock_layout(const void* q, const void* k, bsa_dtype dtype, int
                               float* factor, void* workspace, size_t workspace_bytes, void* stream);
 bsa_status bsa_permute_rows(const void* src, void* dst, bsa_dtype dtype, int BH, int N, int D,
                             int n_prefix, const int32_t* perm, int inverse, void* stream);
-
-/* Forces the CUDA-core attention kernels even where a tensor-core kernel
- * exists (1) or restores the default dispatch (0).  Host, process-wide. */
-void bsa_set_force_simt(int force);
 
 #ifdef __cplusplus
 }

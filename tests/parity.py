@@ -8,6 +8,8 @@ between the k-th and (k+1)-th score is below 1e-5 (reported, and the device's
 list is checked to be a valid top-k within that gap).
 """
 
+import os
+
 import numpy as np
 import torch
 
@@ -17,6 +19,15 @@ F32_MAX_ABS = 1e-5
 BF16_MAX_ABS = 2e-2
 BF16_REL_L2 = 5e-3
 TIE_EPS = 1e-5
+
+
+def set_force_simt(force):
+    """Route the attention stages to their CUDA-core kernels (True) or back to
+    the default dispatch (False): the library reads BSA_FORCE_SIMT per call."""
+    if force:
+        os.environ["BSA_FORCE_SIMT"] = "1"
+    else:
+        os.environ.pop("BSA_FORCE_SIMT", None)
 
 
 def f64(t):

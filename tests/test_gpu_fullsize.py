@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from block_sparse_attention_tile_gb300 import synthetic
-from parity import assert_close, check_route, f64, oracle_blocks
+from parity import set_force_simt, assert_close, check_route, f64, oracle_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def _pl():
 
 @pytest.fixture(autouse=True)
 def _status(lib):
-    lib.bsa_set_force_simt(False)
+    set_force_simt(False)
     yield
     assert lib.bsa_device_status() == lib.BSA_OK
 

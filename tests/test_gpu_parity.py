@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from block_sparse_attention_tile_gb300 import synthetic
-from parity import TIE_EPS, assert_close, check_route, f64, oracle_blocks
+from parity import set_force_simt, TIE_EPS, assert_close, check_route, f64, oracle_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -19,9 +19,9 @@ DEV = "cuda"
 
 @pytest.fixture(autouse=True)
 def _clean_status(lib):
-    lib.bsa_set_force_simt(False)
+    set_force_simt(False)
     yield
-    lib.bsa_set_force_simt(False)
+    set_force_simt(False)
     assert lib.bsa_device_status() == lib.BSA_OK
 
 
@@ -69,7 +69,7 @@ def _run_block_case(lib, B, h, grid, block, M, D, k, dtype, seed, field=False, f
     perm = synthetic.permutation(T * H * W, seed + 3) if permuted else None
     geom = pl.Geometry(T, H, W, *block, M=M, n_prefix=n_prefix,
                        perm=torch.as_tensor(perm, device=DEV) if permuted else None)
-    lib.bsa_set_force_simt(force_simt)
+    set_force_simt(force_simt)
     N = q.shape[1]
     g = None
     if gate == "channel":
@@ -232,7 +232,7 @@ def _segments_case(lib, h, segments, block, M, D, budgets, dtype, seed, packed=N
     pl = _pipeline()
     geom = pl.SegmentGeometry(segments, *block, M=M)
     q, kk, v = synthetic.segment_qkv(h, segments, D, seed, dtype)
-    lib.bsa_set_force_simt(force_simt)
+    set_force_simt(force_simt)
     res = pl.block_sparse_attention(q.to(DEV), kk.to(DEV), v.to(DEV), geom, budgets, packed=packed)
     torch.cuda.synchronize()
     blocks, P, spans = oracle.tile_segments(geom.segments, *block, M)

@@ -75,6 +75,23 @@ def test_no_alloc_reverse_index_matches_workspace_version_twice(lib):
         _same(got, want)
 
 
+def test_no_alloc_at_exactly_its_scratch_limit(lib):
+    # B*H*ceil(N/256)*nblk = 1*4*64*1024 = 262144 int32 counts: the whole
+    # 1 MiB array, the largest size the entry point accepts
+    B, N, H, S, BS = 1, 16384, 4, 4, 16
+    nblk = N // BS
+    assert lib.bsa_reverse_index_workspace(B, N, H, nblk) == 1 << 20
+    idx, cnt = synthetic.causal_block_lists(B, N, H, S, BS, 313)
+    idx_d = torch.as_tensor(idx, device=DEV)
+    cnt_d = torch.as_tensor(cnt, device=DEV)
+    want = _with_workspace(lib, idx_d, cnt_d, B, N, H, S, nblk, 2 * S * BS)
+    for _ in range(2):
+        got = _no_alloc(lib, idx_d, cnt_d, B, N, H, S, nblk, 2 * S * BS)
+        torch.cuda.synchronize()
+        assert lib.bsa_device_status() == lib.BSA_OK
+        _same(got, want)
+
+
 def test_no_alloc_rejects_sizes_beyond_its_scratch(lib):
     # B*H*ceil(N/256)*nblk = 1*8*128*512 int32 = 2 MiB > the 1 MiB static scratch
     B, N, H, S, nblk = 1, 32768, 8, 4, 512
