@@ -13,6 +13,9 @@ bsa_status simt_token_attention(const void* q, const void* k, const void* v, bsa
                                 int Tn, int HQ, int H, int D, const int32_t* bi, const int32_t* bc,
                                 int S, int BS, int causal, float scale, void* out, float* lse,
                                 cudaStream_t st);
+bsa_status tc_token_attention(const void* q, const void* k, const void* v, int B, int T, int HQ, int H, int D,
+                              const int32_t* bidx, const int32_t* bcnt, int S, int BS, int causal, float scale,
+                              void* out, float* lse, cudaStream_t st, int test_stall, bool* handled);
 bsa_status tc_block_attention(const void* q, const void* k, const void* v, int BH, int N,
                               const int32_t* im, const int32_t* bs, int J, int P, const int32_t* geometry,
                               const void* packed, const int32_t* idx, const int32_t* num, int kmax,
@@ -108,8 +111,15 @@ bsa_status bsa_fwd_qouter_tokens(const void* q, const void* k, const void* v, bs
                 "tokens: sizes out of range");
     BSA_REQUIRE(S > 0 && block_size > 0 && block_size <= 1024, "tokens: S / block_size");
     BSA_REQUIRE((long long)B * T * H < 0x7fffffffLL, "tokens: grid too large");
+    cudaStream_t st = as_stream(stream);
+    if (!force_simt() && dtype == BSA_BF16) {
+        bool handled = false;
+        bsa_status rc = tc_token_attention(q, k, v, B, T, HQ, H, D, block_indices, block_counts, S, block_size,
+                                           causal, scale, out, lse, st, test_stall_tile(), &handled);
+        if (handled) return rc;
+    }
     return simt_token_attention(q, k, v, dtype, B, T, HQ, H, D, block_indices, block_counts, S,
-                                block_size, causal, scale, out, lse, as_stream(stream));
+                                block_size, causal, scale, out, lse, st);
 }
 
 }  // extern "C"

@@ -88,6 +88,14 @@ bool force_simt() {
     return e && e[0] && !(e[0] == '0' && e[1] == 0);
 }
 
+int test_stall_tile() {
+    const char* e = std::getenv("BSA_TEST_STALL_TILE");
+    if (!e || !e[0]) return -1;
+    char* end = nullptr;
+    const long v = std::strtol(e, &end, 10);
+    return (end && *end == 0 && v >= 0 && v < 1000000) ? (int)v : -1;
+}
+
 }  // namespace bsa
 
 extern "C" {

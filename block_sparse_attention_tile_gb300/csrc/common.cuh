@@ -23,6 +23,12 @@ int* status_word();
 // Whether the caller asked for the CUDA-core kernels only.
 bool force_simt();
 
+// Tests of the bounded waits only: BSA_TEST_STALL_TILE = n makes the next
+// tensor-core token attention leave the K loads of each CTA's n-th tile
+// unissued and limit every wait to 1 ms, so the waits run out, the kernel
+// latches BSA_ERR_TIMEOUT and returns.  -1 (the default) when unset.
+int test_stall_tile();
+
 // Work counters of the persistent tensor-core kernels: a pair of unsigned
 // (next item, CTAs done), both zero between launches, per (current device,
 // stream) in static device memory.  Launches on one stream run one after

@@ -233,7 +233,17 @@ bsa_status bsa_fwd_qouter(const void* q, const void* k, const void* v, bsa_dtype
  * applied to the logits (K^-1/2 on the page).
  * q, out: [device] BTHD [B, T, HQ, D]; k, v: [device] BTHD [B, T, H, D];
  * block_indices: [device] int32 [B, T, H, S]; block_counts: [device] int32
- * [B, T, H]; lse: [device] float [B, T, HQ] or NULL.  D <= 128, BS <= 128. */
+ * [B, T, H]; lse: [device] float [B, T, HQ] or NULL.  D <= 128.
+ * Slots are read in any order; a block listed twice by one position counts
+ * twice (the definition's gather); an index outside [0, ceil(T/BS)) or a
+ * count above S latches BSA_ERR_INDEX and that slot is skipped (the count
+ * clamped to S).  A row with no visible key outputs 0 and LSE -inf.
+ * bf16 with D = 128, block_size 64 or 128, G = HQ/H a power of two in
+ * [8, 128] and (128/G)*S <= 512 runs on the tcgen05 tensor-core kernel: the
+ * G heads of 128/G consecutive positions form the 128 rows of one product
+ * ([MSA] §4, query concatenation) and run over the union of those positions'
+ * blocks, each row masked to its own selection.  Other shapes run on the
+ * CUDA-core kernel (one CTA per (b, t, h)). */
 bsa_status bsa_fwd_qouter_tokens(const void* q, const void* k, const void* v, bsa_dtype dtype,
                                  int B, int T, int HQ, int H, int D,
                                  const int32_t* block_indices, const int32_t* block_counts,

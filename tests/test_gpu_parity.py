@@ -3,6 +3,7 @@ that still span several tiles and a ragged tail.  Every call goes through the
 C ABI (block_sparse_attention_tile_gb300.bsa)."""
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -572,6 +573,108 @@ def test_nsa_empty_selections(lib, dtype):
         assert_close(go[~empty], O[~empty], dtype, name)
         tol = 1e-5 if dtype == torch.float32 else 2e-3
         assert np.abs(gl[~empty] - L[~empty]).max() <= tol
+
+
+@pytest.mark.parametrize("HQ,H,BS,T,S", [(16, 2, 64, 300, 6), (32, 2, 128, 461, 8), (64, 1, 64, 259, 4),
+                                         (128, 1, 128, 200, 3), (32, 4, 64, 333, 16)])
+def test_nsa_qouter_tensor_core_group_sizes(lib, HQ, H, BS, T, S):
+    """The tensor-core query-outer kernel at G = 8 .. 128 query heads per KV
+    head (16 .. 1 positions per 128-row tile), with a ragged last group of
+    positions and a ragged last key block, against the oracle; the CUDA-core
+    kernel on the same inputs agrees with the oracle too."""
+    pl = _pipeline()
+    B, D = 2, 128
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 317 + HQ, torch.bfloat16)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    idx_d, cnt_d = torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV)
+    o_tc, l_tc = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    set_force_simt(True)
+    o_ct, l_ct = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    set_force_simt(False)
+    torch.cuda.synchronize()
+    for b in range(B):
+        O, L = _oracle_nsa(q, k, v, idx, cnt, BS, b)
+        for name, o, l in (("tensor-core", o_tc, l_tc), ("cuda-core", o_ct, l_ct)):
+            assert_close(f64(o[b]), O, torch.bfloat16, "%s G=%d b=%d" % (name, HQ // H, b))
+            assert np.abs(l[b].cpu().numpy() - L).max() <= 2e-3
+
+
+@pytest.mark.parametrize("BS", [64, 128])
+def test_nsa_qouter_duplicates_and_unsorted_lists(lib, BS):
+    """Lists in any order, and a block listed twice by one position: the
+    definition's gather then counts its keys twice, and so must the kernel
+    (it gives the repeated block a tile of its own)."""
+    pl = _pipeline()
+    B, T, HQ, H, D, S = 1, 390, 32, 2, 128, 8
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 353, torch.bfloat16)
+    rng = np.random.default_rng(353)
+    idx = idx.copy()
+    for t in range(T):
+        for h in range(H):
+            c = int(cnt[0, t, h])
+            idx[0, t, h, :c] = rng.permutation(idx[0, t, h, :c])
+            if c >= 2 and rng.random() < 0.3:
+                idx[0, t, h, rng.integers(c)] = idx[0, t, h, rng.integers(c)]
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, l = pl.nsa_qouter(qd, kd, vd, torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV), BS)
+    torch.cuda.synchronize()
+    O, L = _oracle_nsa(q, k, v, idx, cnt, BS, 0)
+    assert_close(f64(o[0]), O, torch.bfloat16, "duplicates BS=%d" % BS)
+    assert np.abs(l[0].cpu().numpy() - L).max() <= 2e-3
+
+
+def test_nsa_qouter_tensor_core_bad_index_skipped(lib):
+    """An index outside [0, nblk) and a count above S on the tensor-core
+    path: BSA_ERR_INDEX is latched, the bad slot is skipped, the count is
+    clamped to S, and every row equals the oracle on the cleaned lists."""
+    pl = _pipeline()
+    B, T, HQ, H, D, BS, S = 1, 256, 16, 1, 128, 64, 4
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 19, torch.bfloat16)
+    idx, cnt = idx.copy(), cnt.copy()
+    bad_t = [t for t in range(T) if cnt[0, t, 0] >= 2][5]
+    idx[0, bad_t, 0, 0] = 1000
+    # position 7 (block 0) lists one block; a count of S + 3 also reads its -1
+    # padding, which is out of range too and skipped
+    orig7 = int(cnt[0, 7, 0])
+    cnt[0, 7, 0] = S + 3
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, l = pl.nsa_qouter(qd, kd, vd, torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV), BS)
+    assert lib.bsa_device_status() == lib.BSA_ERR_INDEX
+    clean_idx, clean_cnt = idx.copy(), cnt.copy()
+    c = int(clean_cnt[0, bad_t, 0])
+    clean_idx[0, bad_t, 0, :c - 1] = idx[0, bad_t, 0, 1:c]
+    clean_idx[0, bad_t, 0, c - 1] = -1
+    clean_cnt[0, bad_t, 0] = c - 1
+    clean_cnt[0, 7, 0] = orig7
+    O, L = _oracle_nsa(q, k, v, clean_idx, clean_cnt, BS, 0)
+    assert_close(f64(o[0]), O, torch.bfloat16, "bad index")
+
+
+def test_bounded_wait_expiry_is_reported_and_recovers(lib):
+    """The tensor-core kernels' bounded waits.  A test-only switch
+    (BSA_TEST_STALL_TILE) makes the next token attention leave the K loads of
+    each CTA's first tile unissued, so no copy is in flight and nothing ever
+    arrives, and limits every wait to 1 ms.  The waits must run out: the
+    kernel latches BSA_ERR_TIMEOUT, drains its own copies and MMAs, frees its
+    TMEM and returns.  The next launch on the same stream must then give the
+    reference output bit for bit (TMEM was freed, the work counters reset)."""
+    pl = _pipeline()
+    B, T, HQ, H, D, BS, S = 1, 1024, 32, 2, 128, 128, 8
+    q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 29, torch.bfloat16, zipf=True)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    idx_d, cnt_d = torch.as_tensor(idx, device=DEV), torch.as_tensor(cnt, device=DEV)
+    o_ref, l_ref = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    assert lib.bsa_device_status() == lib.BSA_OK
+    os.environ["BSA_TEST_STALL_TILE"] = "0"
+    try:
+        pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+    finally:
+        os.environ.pop("BSA_TEST_STALL_TILE", None)
+    assert lib.bsa_device_status() == lib.BSA_ERR_TIMEOUT
+    for _ in range(2):
+        o, l = pl.nsa_qouter(qd, kd, vd, idx_d, cnt_d, BS)
+        assert lib.bsa_device_status() == lib.BSA_OK
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
 
 
 @pytest.mark.parametrize("HQ,H,BS", [(16, 2, 64), (64, 1, 128), (128, 1, 64)])
