@@ -16,28 +16,47 @@
 Readings taken where the page leaves a detail open: CSR rows are ordered
 (batch, KV head, block); inside a row query ids are ascending; the slot of an
 entry is the position of the block in the query's q2k list; chunks cut each
-row in ascending-query order into runs of at most ``cap`` queries.
+row in ascending-query order into runs of at most ``cap`` queries.  The page
+leaves the order in which the GPU walks the (block, KV head) rows open
+(§7 only bounds a chunk's length); with ``window`` the query positions of a
+batch are first cut into windows of that many positions and each window has
+rows of its own, ordered (batch, window, KV head, block): the same entries,
+regrouped so that a pass can finish one window of queries before the next.
 """
 
 import numpy as np
 
 
-def reverse_index(q2k_idx, q2k_num, nblk):
-    """q2k_idx [R, N, S] (R = batch * KV heads), q2k_num [R, N] ->
-    row_ptr [R*nblk + 1], q_idx [nnz], slot [nnz] (int64)."""
+def reverse_index(q2k_idx, q2k_num, nblk, window=0, heads=1):
+    """q2k_idx [R, N, S] (R = batch * KV heads, r = b * heads + h), q2k_num
+    [R, N] -> row_ptr [rows + 1], q_idx [nnz], slot [nnz] (int64).
+
+    window = 0 (or >= N): rows r * nblk + blk, rows = R * nblk.  Otherwise
+    nwin = ceil(N / window) windows per batch element and rows
+    ((b * nwin + w) * heads + h) * nblk + blk with w = i // window."""
     R, N, S = q2k_idx.shape
-    rows = [[] for _ in range(R * nblk)]
+    nwin = 1 if window <= 0 or window >= N else -(-N // window)
+    assert R % heads == 0
+    nrows = R * nwin * nblk
+
+    def row_of(r, i, blk):
+        if nwin == 1:
+            return r * nblk + blk
+        b, h = divmod(r, heads)
+        return ((b * nwin + i // window) * heads + h) * nblk + blk
+
+    rows = [[] for _ in range(nrows)]
     for r in range(R):
         for i in range(N):
             for s in range(int(q2k_num[r, i])):
                 blk = int(q2k_idx[r, i, s])
-                rows[r * nblk + blk].append((i, s))
-    row_ptr = np.zeros(R * nblk + 1, dtype=np.int64)
-    for row in range(R * nblk):
+                rows[row_of(r, i, blk)].append((i, s))
+    row_ptr = np.zeros(nrows + 1, dtype=np.int64)
+    for row in range(nrows):
         row_ptr[row + 1] = row_ptr[row] + len(rows[row])
     q_idx = np.zeros(row_ptr[-1], dtype=np.int64)
     slot = np.zeros(row_ptr[-1], dtype=np.int64)
-    for row in range(R * nblk):
+    for row in range(nrows):
         for e, (i, s) in enumerate(rows[row]):
             q_idx[row_ptr[row] + e] = i
             slot[row_ptr[row] + e] = s
@@ -59,7 +78,8 @@ def kvouter_partials(q, k, v, row_ptr, q_idx, slot, nblk, block_size, S, H, caus
                      scale=None):
     """K1 over one batch element.
 
-    q [N, HQ, D], k/v [N, H, D]; CSR rows r*nblk + blk for KV head r.
+    q [N, HQ, D], k/v [N, H, D]; CSR rows r*nblk + blk for KV head r (one
+    window, the page's CSR).
     Returns O_buf [N, HQ, S, Dv] and LSE_buf [N, HQ, S] (slots never written
     keep O = 0, L = -inf)."""
     q = np.asarray(q, dtype=np.float64)

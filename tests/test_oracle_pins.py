@@ -369,6 +369,61 @@ def test_reverse_index_brute_force_and_chunks():
     assert np.all(covered == 1)
 
 
+def test_reverse_index_windows_page_example():
+    """The page's q0..q3 example ([MSA] §2) with windows of two positions:
+    window 0 holds q0, q1 and window 1 q2, q3, each with rows A, B, C, D.
+    By hand: A -> q0 q1 | B -> - | C -> q0 | D -> q1 ; A -> q2 q3 | B -> q3 |
+    C -> q2 | D -> -; slots are the block's place in the query's list."""
+    g = golden("msa_reverse_index.json")
+    names = g["blocks"]
+    qs = sorted(g["q2k"])
+    q2k = np.full((1, len(qs), 2), -1)
+    num = np.zeros((1, len(qs)), int)
+    for i, qn in enumerate(qs):
+        sel = sorted(names.index(b) for b in g["q2k"][qn])
+        q2k[0, i, :len(sel)] = sel
+        num[0, i] = len(sel)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, len(names), window=2, heads=1)
+    assert list(row_ptr) == [0, 2, 2, 3, 4, 6, 7, 8, 8]
+    assert list(q_idx) == [0, 1, 0, 1, 2, 3, 3, 2]
+    assert list(slot) == [0, 0, 1, 1, 0, 0, 1, 1]
+    # one window covering every position is the page's CSR
+    plain = oracle.reverse_index(q2k, num, len(names))
+    for w in (0, 4, 100):
+        got = oracle.reverse_index(q2k, num, len(names), window=w, heads=1)
+        assert all(np.array_equal(a, b) for a, b in zip(got, plain))
+
+
+def test_reverse_index_windows_regroup_the_plain_rows():
+    """Brute force, two batch elements x three KV heads: every windowed row
+    holds only positions of its window, and the windows' rows of one
+    (batch, head, block), taken in window order, are exactly the plain row."""
+    rng = np.random.default_rng(5)
+    B, H, N, S, nblk, W = 2, 3, 37, 4, 6, 8
+    R = B * H
+    q2k = np.full((R, N, S), -1)
+    num = rng.integers(0, S + 1, size=(R, N))
+    for r in range(R):
+        for i in range(N):
+            q2k[r, i, :num[r, i]] = np.sort(rng.permutation(nblk)[:num[r, i]])
+    rp, qi, sl = oracle.reverse_index(q2k, num, nblk)
+    wrp, wqi, wsl = oracle.reverse_index(q2k, num, nblk, window=W, heads=H)
+    nwin = -(-N // W)
+    assert len(wrp) == B * nwin * H * nblk + 1 and wrp[-1] == rp[-1]
+    for b in range(B):
+        for h in range(H):
+            for blk in range(nblk):
+                plain_row = (b * H + h) * nblk + blk
+                want = list(zip(qi[rp[plain_row]:rp[plain_row + 1]], sl[rp[plain_row]:rp[plain_row + 1]]))
+                got = []
+                for w in range(nwin):
+                    row = ((b * nwin + w) * H + h) * nblk + blk
+                    ents = list(zip(wqi[wrp[row]:wrp[row + 1]], wsl[wrp[row]:wrp[row + 1]]))
+                    assert all(w * W <= i < (w + 1) * W for i, _ in ents)
+                    got += ents
+                assert got == want
+
+
 def test_kvouter_combine_equals_q_outer():
     T, HQ, H, D, BS, S = 48, 4, 2, 8, 8, 4
     q, k, v, idx, cnt, nb = _nsa_inputs(T, HQ, H, D, BS, S, 31)
