@@ -813,10 +813,13 @@ class TokenWorkload:
         self.idx_h, self.cnt_h = gen(B, T, H, S, BS, seed)
         self.idx = torch.as_tensor(self.idx_h, device=dev)
         self.cnt = torch.as_tensor(self.cnt_h, device=dev)
+        from block_sparse_attention_tile_gb300 import pipeline
         self.nblk = -(-T // BS)
         self.cap = 2 * S * BS
-        self.max_chunks = bsa.bsa_max_chunks(B, T, H, S, self.nblk, self.cap)
-        self.row_ptr = torch.empty((B * H * self.nblk + 1,), dtype=torch.int32, device=dev)
+        self.window = pipeline.default_window(T) if w.get("window") is None else w["window"]
+        nwin = pipeline.windows(T, self.window)
+        self.max_chunks = bsa.bsa_max_chunks(B, T, H, S, self.nblk, self.cap, self.window)
+        self.row_ptr = torch.empty((B * nwin * H * self.nblk + 1,), dtype=torch.int32, device=dev)
         self.q_idx = torch.empty((B * H * T * S,), dtype=torch.int32, device=dev)
         self.slot = torch.empty_like(self.q_idx)
         self.chunks = torch.empty((self.max_chunks, 4), dtype=torch.int32, device=dev)
@@ -844,11 +847,11 @@ class TokenWorkload:
         st = self.torch.cuda.current_stream()
         if ev: ev[0].record(st)
         bsa.bsa_build_reverse_index(idx, cnt, B, T, H, S, self.nblk, self.cap, self.row_ptr, self.q_idx, self.slot,
-                                    self.chunks, self.n_chunks, self.max_chunks, self.ws)
+                                    self.chunks, self.n_chunks, self.max_chunks, self.ws, window=self.window)
         if ev: ev[1].record(st)
         bsa.bsa_fwd_kvouter(q, k, v, B, T, HQ, H, D, self.row_ptr, self.q_idx, self.slot, self.chunks,
                             self.n_chunks, self.max_chunks, self.nblk, BS, S, True, self.scale, self.obuf,
-                            self.lsebuf)
+                            self.lsebuf, window=self.window)
         if ev: ev[2].record(st)
         bsa.bsa_combine(self.obuf, self.lsebuf, cnt, B, T, HQ, H, S, D, self.out, self.lse)
         if ev: ev[3].record(st)
@@ -933,7 +936,8 @@ class TokenWorkload:
                              "kernel": "bsa_fwd_qouter_tokens"}}
         config = {"workload": self.name, "B": B, "T": T, "HQ": HQ, "H": H, "D": D, "block_size": BS, "S": S,
                   "selection": "zipf(1.1) sink+own" if w["zipf"] else "causal uniform, counts U{1..S}",
-                  "chunk_cap": self.cap, "nnz": nnz, "n_chunks": int(self.n_chunks.item()), "order": "kv-outer",
+                  "chunk_cap": self.cap, "window": self.window, "nnz": nnz, "n_chunks": int(self.n_chunks.item()),
+                  "order": "kv-outer",
                   "l2": "inputs larger than L2: Q,K,V = %.2f GB per step"
                         % ((self.q.numel() + self.k.numel() + self.v.numel()) * 2 / 1e9)}
         return roof, secondary, config, "synthetic (seeded N(0,1); no dataset or weights)", "bf16"
@@ -960,6 +964,9 @@ def gpu_arm(args):
     dev = torch.device("cuda", local)
     w = dict(WORKLOADS[args.workload])
     name = args.workload
+    if args.window is not None and w["kind"] == "token":
+        w["window"] = args.window
+        name = name + "_window%d" % args.window
     if args.heads:
         if w["kind"] == "block":
             w["heads"] = args.heads
@@ -1138,6 +1145,9 @@ def main():
     ap.add_argument("--heads", type=int, default=0,
                     help="fewer heads (KV heads for the token workloads) than the workload's: a small case "
                          "for profiler captures")
+    ap.add_argument("--window", type=int, default=None,
+                    help="token workloads: query positions per KV-outer window (0 = one window; default: "
+                         "the library pipeline's choice)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

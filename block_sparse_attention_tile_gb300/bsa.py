@@ -53,10 +53,10 @@ _SIGS = {
     "bsa_fwd_qouter": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, F, P, P, P]),
     "bsa_fwd_qouter_tokens": (I, [P, P, P, I, I, I, I, I, I, P, P, I, I, I, F, P, P, P]),
     "bsa_reverse_index_workspace": (SZ, [I, I, I, I]),
-    "bsa_max_chunks": (I, [I, I, I, I, I, I]),
-    "bsa_build_reverse_index": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P, SZ, P]),
-    "bsa_build_reverse_index_noalloc": (I, [P, P, I, I, I, I, I, I, P, P, P, P, P, I, P]),
-    "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, F, P, I, P, P]),
+    "bsa_max_chunks": (I, [I, I, I, I, I, I, I]),
+    "bsa_build_reverse_index": (I, [P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P, SZ, P]),
+    "bsa_build_reverse_index_noalloc": (I, [P, P, I, I, I, I, I, I, I, P, P, P, P, P, I, P]),
+    "bsa_fwd_kvouter": (I, [P, P, P, I, I, I, I, I, I, P, P, P, P, P, I, I, I, I, I, I, F, P, I, P, P]),
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
     "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, P, F, P, P, P]),
     "bsa_reweight_workspace": (SZ, [I, I]),
@@ -196,13 +196,14 @@ def bsa_reverse_index_workspace(B, N, H, nblk):
     return _lib.bsa_reverse_index_workspace(B, N, H, nblk)
 
 
-def bsa_max_chunks(B, N, H, S, nblk, chunk_cap):
-    return _lib.bsa_max_chunks(B, N, H, S, nblk, chunk_cap)
+def bsa_max_chunks(B, N, H, S, nblk, chunk_cap, window=0):
+    return _lib.bsa_max_chunks(B, N, H, S, nblk, chunk_cap, window)
 
 
 def bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx, slot, chunks,
-                            n_chunks, max_chunks, workspace, stream=None):
-    _check(_lib.bsa_build_reverse_index(_ptr(q2k_idx), _ptr(q2k_num), B, N, H, S, nblk, chunk_cap,
+                            n_chunks, max_chunks, workspace, window=0, stream=None):
+    """`window` (the C argument after chunk_cap) is a keyword here: 0 = one window."""
+    _check(_lib.bsa_build_reverse_index(_ptr(q2k_idx), _ptr(q2k_num), B, N, H, S, nblk, chunk_cap, window,
                                         _ptr(row_ptr), _ptr(q_idx), _ptr(slot), _ptr(chunks),
                                         _ptr(n_chunks), max_chunks, _ptr(workspace),
                                         workspace.numel() * workspace.element_size(),
@@ -210,18 +211,20 @@ def bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_p
 
 
 def bsa_build_reverse_index_noalloc(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx, slot,
-                                    chunks, n_chunks, max_chunks, stream=None):
+                                    chunks, n_chunks, max_chunks, window=0, stream=None):
     """bsa_build_reverse_index with the library's static scratch (no workspace argument)."""
-    _check(_lib.bsa_build_reverse_index_noalloc(_ptr(q2k_idx), _ptr(q2k_num), B, N, H, S, nblk, chunk_cap,
+    _check(_lib.bsa_build_reverse_index_noalloc(_ptr(q2k_idx), _ptr(q2k_num), B, N, H, S, nblk, chunk_cap, window,
                                                 _ptr(row_ptr), _ptr(q_idx), _ptr(slot), _ptr(chunks),
                                                 _ptr(n_chunks), max_chunks, _stream(stream)))
 
 
 def bsa_fwd_kvouter(q, k, v, B, N, HQ, H, D, row_ptr, q_idx, slot, chunks, n_chunks, max_chunks, nblk,
-                    block_size, S, causal, scale, obuf, lsebuf, stream=None):
+                    block_size, S, causal, scale, obuf, lsebuf, window=0, stream=None):
+    """`window` (the C argument after nblk) is a keyword here; it must be the
+    window the reverse index was built with."""
     _check(_lib.bsa_fwd_kvouter(_ptr(q), _ptr(k), _ptr(v), _dtype(q), B, N, HQ, H, D, _ptr(row_ptr),
                                 _ptr(q_idx), _ptr(slot), _ptr(chunks), _ptr(n_chunks), max_chunks,
-                                nblk, block_size, S, 1 if causal else 0, scale, _ptr(obuf),
+                                nblk, window, block_size, S, 1 if causal else 0, scale, _ptr(obuf),
                                 _dtype(obuf), _ptr(lsebuf), _stream(stream)))
 
 

@@ -50,19 +50,23 @@ __global__ void __launch_bounds__(kQT) rev_count_kernel(
 }
 
 // Pass 2 (one CTA): per-tile offsets inside every row, row pointers, chunks.
+// Rows are (batch, window, KV head, block); the row of a window sums the
+// counts of that window's tiles only (wt tiles of 256 queries per window).
 __global__ void __launch_bounds__(1024) rev_scan_kernel(
-    int32_t* __restrict__ counts, int R, int nblk, int ntile, int cap, int32_t* __restrict__ row_ptr,
-    int32_t* __restrict__ chunks, int32_t* __restrict__ n_chunks, int max_chunks, int* status) {
+    int32_t* __restrict__ counts, int B, int H, int nwin, int wt, int nblk, int ntile, int cap,
+    int32_t* __restrict__ row_ptr, int32_t* __restrict__ chunks, int32_t* __restrict__ n_chunks, int max_chunks,
+    int* status) {
     __shared__ int carry_rows, carry_chunks;
-    const int rows = R * nblk;
+    const int rows = B * nwin * H * nblk;
     if (threadIdx.x == 0) { carry_rows = 0; carry_chunks = 0; }
     __syncthreads();
     for (int base = 0; base < rows; base += blockDim.x) {
         const int row = base + threadIdx.x;
         int total = 0;
         if (row < rows) {
-            const int g = row / nblk, blk = row % nblk;
-            for (int t = 0; t < ntile; ++t) {
+            const int blk = row % nblk, h = (row / nblk) % H, bw = row / (nblk * H);
+            const int g = (bw / nwin) * H + h, w = bw % nwin;
+            for (int t = w * wt; t < min(ntile, (w + 1) * wt); ++t) {
                 int32_t* c = counts + ((long long)g * ntile + t) * nblk + blk;
                 const int v = *c;
                 *c = total;  // exclusive offset of this tile inside the row
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(1024) rev_scan_kernel(
 // position of the lane in the warp's lane mask for that block.
 __global__ void __launch_bounds__(kQT) rev_scatter_kernel(
     const int32_t* __restrict__ q2k_idx, const int32_t* __restrict__ q2k_num, int N, int H, int S,
-    int nblk, int ntile, const int32_t* __restrict__ counts, const int32_t* __restrict__ row_ptr,
+    int nblk, int ntile, int nwin, int wt, const int32_t* __restrict__ counts, const int32_t* __restrict__ row_ptr,
     int32_t* __restrict__ q_idx, int32_t* __restrict__ slot) {
     extern __shared__ unsigned int sm[];
     constexpr int W = kQT / 32;
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kQT) rev_scatter_kernel(
             const int blk = q2k_idx[sel * S + s];
             if (blk < 0 || blk >= nblk || blk <= prev) continue;
             prev = blk;
-            const int row = g * nblk + blk;
+            const int row = (((b * nwin + tile / wt) * H) + h) * nblk + blk;
             const int pos = row_ptr[row] + counts[((long long)g * ntile + tile) * nblk + blk] +
                             off[warp * nblk + blk] + __popc(mask[warp * nblk + blk] & lt);
             q_idx[pos] = i;
@@ -184,15 +188,16 @@ __global__ void __launch_bounds__(256) kvouter_simt_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, int N, int HQ, int H,
     int D, int Dp, const int32_t* __restrict__ q_idx, const int32_t* __restrict__ slot,
     const int32_t* __restrict__ chunks, const int32_t* __restrict__ n_chunks, int nblk, int BS, int S,
-    int causal, float scale_log2, TO* __restrict__ obuf, float* __restrict__ lsebuf, int* status) {
+    int causal, int nwin, float scale_log2, TO* __restrict__ obuf, float* __restrict__ lsebuf, int* status) {
     extern __shared__ __align__(16) float ks_smem[];
     if ((int)blockIdx.x >= *n_chunks) return;
     const int row = chunks[4 * blockIdx.x + 0];
     const int start = chunks[4 * blockIdx.x + 1];
     const int len = chunks[4 * blockIdx.x + 2];
     const int G = HQ / H;
+    // row = ((b * nwin + window) * H + h) * nblk + blk
     const int grp = row / nblk, blk = row % nblk;
-    const int b = grp / H, h = grp % H;
+    const int b = grp / (nwin * H), h = grp % H;
     float* Ks = ks_smem;              // [BS][Dp]
     float* Vs = Ks + BS * Dp;         // [BS][Dp]
     float* Qs = Vs + BS * Dp;         // [128][Dp]
@@ -402,8 +407,15 @@ __global__ void __launch_bounds__(256) combine_bf16_d128_kernel(
 bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N, int HQ, int H, int D,
                       const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot,
                       const int32_t* chunks, const int32_t* n_chunks, int max_chunks, int nblk,
-                      int BS, int S, int causal, float scale, void* obuf, float* lsebuf,
+                      int nwin, int BS, int S, int causal, float scale, void* obuf, float* lsebuf,
                       cudaStream_t st, bool* handled);
+
+// Windows of a reverse index: window = 0 (or >= N) is one window of N
+// positions; otherwise a multiple of the 256-query tile.
+static int window_count(int N, int window) {
+    if (window <= 0 || window >= N) return 1;
+    return (N + window - 1) / window;
+}
 
 }  // namespace bsa
 
@@ -417,16 +429,16 @@ size_t bsa_reverse_index_workspace(int B, int N, int H, int nblk) {
     return (size_t)B * H * ntile * nblk * sizeof(int32_t);
 }
 
-int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap) {
-    if (B < 1 || N < 1 || H < 1 || S < 1 || nblk < 1 || chunk_cap < 1) return -1;
-    const long long rows = (long long)B * H * nblk;
+int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap, int window) {
+    if (B < 1 || N < 1 || H < 1 || S < 1 || nblk < 1 || chunk_cap < 1 || window < 0) return -1;
+    const long long rows = (long long)B * window_count(N, window) * H * nblk;
     const long long nnz = (long long)B * H * N * S;
     const long long m = rows + nnz / chunk_cap + 1;
     return m > 0x7fffffff ? -1 : (int)m;
 }
 
 bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_num, int B, int N,
-                                   int H, int S, int nblk, int chunk_cap, int32_t* row_ptr,
+                                   int H, int S, int nblk, int chunk_cap, int window, int32_t* row_ptr,
                                    int32_t* q_idx, int32_t* slot, int32_t* chunks,
                                    int32_t* n_chunks, int max_chunks, void* workspace,
                                    size_t workspace_bytes, void* stream) {
@@ -436,7 +448,11 @@ bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_nu
                 "reverse_index: sizes out of range");
     BSA_REQUIRE((long long)B * H * N * S < 0x7fffffffLL, "reverse_index: too many entries");
     BSA_REQUIRE(B * H <= 65535, "reverse_index: too many row groups");
-    const int need = bsa_max_chunks(B, N, H, S, nblk, chunk_cap);
+    BSA_REQUIRE(window >= 0 && (window == 0 || window >= N || window % kQT == 0),
+                "reverse_index: window must be 0 or a multiple of %d", kQT);
+    const int nwin = window_count(N, window);
+    BSA_REQUIRE((long long)B * nwin * H * nblk < 0x7fffffffLL, "reverse_index: too many rows");
+    const int need = bsa_max_chunks(B, N, H, S, nblk, chunk_cap, window);
     BSA_REQUIRE(max_chunks >= need, "reverse_index: max_chunks %d < %d", max_chunks, need);
     BSA_REQUIRE(workspace_bytes >= bsa_reverse_index_workspace(B, N, H, nblk),
                 "reverse_index: workspace too small");
@@ -448,14 +464,15 @@ bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_nu
         q2k_idx, q2k_num, N, H, S, nblk, ntile, counts, status_word());
     bsa_status rc = check_launch("rev_count_kernel");
     if (rc != BSA_OK) return rc;
-    rev_scan_kernel<<<1, 1024, 0, st>>>(counts, R, nblk, ntile, chunk_cap, row_ptr, chunks, n_chunks,
-                                        max_chunks, status_word());
+    const int wt = nwin == 1 ? ntile : window / kQT;  // query tiles per window
+    rev_scan_kernel<<<1, 1024, 0, st>>>(counts, B, H, nwin, wt, nblk, ntile, chunk_cap, row_ptr, chunks,
+                                        n_chunks, max_chunks, status_word());
     rc = check_launch("rev_scan_kernel");
     if (rc != BSA_OK) return rc;
     const size_t smem = (size_t)2 * (kQT / 32) * nblk * sizeof(int);
     if (smem > 48 * 1024)
         cudaFuncSetAttribute(rev_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    rev_scatter_kernel<<<dim3(ntile, R), kQT, smem, st>>>(q2k_idx, q2k_num, N, H, S, nblk, ntile,
+    rev_scatter_kernel<<<dim3(ntile, R), kQT, smem, st>>>(q2k_idx, q2k_num, N, H, S, nblk, ntile, nwin, wt,
                                                           counts, row_ptr, q_idx, slot);
     return check_launch("rev_scatter_kernel");
 }
@@ -463,7 +480,7 @@ bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_nu
 bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtype dtype, int B,
                            int N, int HQ, int H, int D, const int32_t* row_ptr, const int32_t* q_idx,
                            const int32_t* slot, const int32_t* chunks, const int32_t* n_chunks,
-                           int max_chunks, int nblk, int block_size, int S, int causal, float scale,
+                           int max_chunks, int nblk, int window, int block_size, int S, int causal, float scale,
                            void* obuf, bsa_dtype obuf_dtype, float* lsebuf, void* stream) {
     BSA_REQUIRE(q && k && v && row_ptr && q_idx && slot && chunks && n_chunks && obuf && lsebuf,
                 "kvouter: null pointer");
@@ -474,11 +491,15 @@ bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtyp
     BSA_REQUIRE((long long)B * N * HQ * S < 0x7fffffffLL, "kvouter: partial buffer too large");
     BSA_REQUIRE(dtype == BSA_F32 || dtype == BSA_BF16, "kvouter: dtype");
     BSA_REQUIRE(obuf_dtype == BSA_F32 || obuf_dtype == BSA_BF16, "kvouter: obuf dtype");
+    BSA_REQUIRE(window >= 0 && (window == 0 || window >= N || window % kQT == 0),
+                "kvouter: window must be 0 or a multiple of %d", kQT);
+    const int nwin = window_count(N, window);
+    BSA_REQUIRE((long long)B * nwin * H * nblk < 0x7fffffffLL, "kvouter: too many rows");
     cudaStream_t st = as_stream(stream);
     if (!force_simt() && dtype == BSA_BF16 && obuf_dtype == BSA_BF16) {
         bool handled = false;
         bsa_status rc = kvouter_tc(q, k, v, B, N, HQ, H, D, row_ptr, q_idx, slot, chunks, n_chunks,
-                                   max_chunks, nblk, block_size, S, causal, scale, obuf, lsebuf, st,
+                                   max_chunks, nblk, nwin, block_size, S, causal, scale, obuf, lsebuf, st,
                                    &handled);
         if (handled) return rc;
     }
@@ -493,7 +514,7 @@ bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtyp
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);       \
         kern<<<max_chunks, 256, smem, st>>>((const T*)q, (const T*)k, (const T*)v, N, HQ, H, D, Dp, \
                                             q_idx, slot, chunks, n_chunks, nblk, block_size, S,   \
-                                            causal, sl, (TO*)obuf, lsebuf, status_word());        \
+                                            causal, nwin, sl, (TO*)obuf, lsebuf, status_word());  \
     } while (0)
     if (dtype == BSA_F32 && obuf_dtype == BSA_F32) BSA_KV_LAUNCH(float, float);
     else if (dtype == BSA_F32) BSA_KV_LAUNCH(float, __nv_bfloat16);
@@ -581,7 +602,7 @@ static void* noalloc_scratch(bsa_status* rc) {
 }  // namespace bsa
 
 extern "C" bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, const int32_t* q2k_num, int B,
-                                                      int N, int H, int S, int nblk, int chunk_cap,
+                                                      int N, int H, int S, int nblk, int chunk_cap, int window,
                                                       int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
                                                       int32_t* chunks, int32_t* n_chunks, int max_chunks,
                                                       void* stream) {
@@ -596,6 +617,6 @@ extern "C" bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, co
     if (!ws) return rc;
     // The count pass writes every scratch entry it later reads, so nothing
     // left over from an earlier call needs clearing.
-    return bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx, slot,
+    return bsa_build_reverse_index(q2k_idx, q2k_num, B, N, H, S, nblk, chunk_cap, window, row_ptr, q_idx, slot,
                                    chunks, n_chunks, max_chunks, ws, bsa::kNoAllocScratchBytes, stream);
 }

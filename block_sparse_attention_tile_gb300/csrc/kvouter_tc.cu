@@ -11,10 +11,14 @@
 // so partial outputs never collide and nothing is accumulated atomically).
 //
 // Design (ours, for sm_103a).  A persistent grid of one CTA per SM.  The
-// chunk list covers the CSR entry space [0, nnz) in order (an entry is one
-// (row, query position) pair); CTA i takes the i-th equal share of it, so
-// every CTA does the same number of (position, block) products and loads a
-// K/V block again only where its share crosses into the next chunk.
+// reverse index may order its entries by query window (rows (batch, window,
+// KV head, block)); the chunk list covers the entry space in order.  For every
+// window in turn, CTA i takes the i-th equal share of that window's entries,
+// so the whole grid works on one window at a time and the window's query rows
+// are fetched from HBM once and then served from L2 to every block that
+// selected them.  Every CTA does the same number of (position, block)
+// products per window and loads a K/V block again only where its share
+// crosses into the next chunk.
 //   warp 0     producer: per chunk segment, K and V of the block (one 3-D TMA
 //              box of BS rows per 64-column half); per sub-tile of up to
 //              128 / G positions, one box of the G heads per position and
@@ -65,8 +69,7 @@ struct Cfg {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + kQStages * kQBytes;
     static constexpr uint32_t OFF_V = OFF_K + kKVBytes;
-    static constexpr uint32_t OFF_STG = OFF_V + kKVBytes;     // 8 warps x 32 rows x 128 B epilogue staging
-    static constexpr uint32_t OFF_BAR = OFF_STG + 8 * 4096;
+    static constexpr uint32_t OFF_BAR = OFF_V + kKVBytes;
     static constexpr int BAR_KVF = 0, BAR_KVE = 1, BAR_QF = 2, BAR_QE = BAR_QF + kQStages,
                          BAR_SF = BAR_QE + kQStages, BAR_PF = BAR_SF + 2, BAR_OF = BAR_PF + 2,
                          BAR_OE = BAR_OF + 2, BAR_DRAIN = BAR_OE + 2, NBAR = BAR_DRAIN + 1;
@@ -76,6 +79,7 @@ struct Cfg {
 };
 
 struct Params {
+    const int32_t* row_ptr;  // [B * nwin * H * nblk + 1]
     const int32_t* q_idx;
     const int32_t* slot;
     const int32_t* chunks;
@@ -83,7 +87,7 @@ struct Params {
     __nv_bfloat16* obuf;
     float* lsebuf;
     int* status;
-    int N, HQ, H, G, S, nblk, causal, rows_total, max_chunks;
+    int N, HQ, H, G, S, nblk, nwin, causal, rows_total, max_chunks;
     long long max_entries;  // capacity of q_idx / slot: B*H*N*S
     float scale_log2;
 };
@@ -102,68 +106,81 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
-// This CTA's share [lo, hi) of the entry space and the chunk holding lo.
-struct Share {
-    int lo, hi, c0, nch;
-};
-
-__device__ __forceinline__ Share cta_share(const Params& p) {
-    Share s{0, 0, 0, 0};
-    const int nch = min(*p.n_chunks, p.max_chunks);
-    if (nch <= 0) return s;
-    const long long nnz = (long long)p.chunks[4 * (nch - 1) + 1] + p.chunks[4 * (nch - 1) + 2];
-    if (nnz <= 0) return s;
-    if (nnz > p.max_entries) {  // more entries than q_idx / slot can hold
-        raise_status(p.status, BSA_ERR_INDEX);
-        return s;
-    }
-    s.nch = nch;
-    s.lo = (int)(nnz * blockIdx.x / gridDim.x);
-    s.hi = (int)(nnz * (blockIdx.x + 1) / gridDim.x);
-    int a = 0, b = nch - 1;  // last chunk whose start is <= lo
-    while (a < b) {
-        const int m = (a + b + 1) >> 1;
-        if (p.chunks[4 * m + 1] <= s.lo) a = m;
-        else b = m - 1;
-    }
-    s.c0 = a;
-    return s;
-}
-
-// Walks this CTA's share one sub-tile (up to PT consecutive entries of one
-// chunk) at a time.  Every role runs its own cursor over the same list, so
-// all of them see the same sub-tiles and stop at the same place.
+// Walks this CTA's share of every window in turn, one sub-tile (up to PT
+// consecutive entries of one chunk) at a time.  Every role runs its own
+// cursor over the same list, so all of them see the same sub-tiles and stop
+// at the same place.
 struct Cursor {
-    int c, nch, lo, hi;  // next chunk to open, chunk count, share [lo, hi)
+    int bw, nbw, nch;    // current (batch, window), their count, chunk count
+    int lo, hi;          // this CTA's share [lo, hi) of the window's entries
+    int c;               // next chunk to open
     int e, end;          // next entry of the open segment and its end
     int row;
     long long prev_end;
 };
 
-__device__ __forceinline__ Cursor cursor_begin(const Share& sh) {
+__device__ __forceinline__ Cursor cursor_begin(const Params& p) {
     Cursor cu;
-    cu.c = sh.c0;
-    cu.nch = sh.nch;
-    cu.lo = sh.lo;
-    cu.hi = sh.hi;
-    cu.e = 0;
-    cu.end = 0;
+    cu.bw = -1;
+    cu.nbw = -1;
+    cu.nch = min(*p.n_chunks, p.max_chunks);
+    cu.lo = cu.hi = 0;
+    cu.c = 0;
+    cu.e = cu.end = 0;
     cu.row = 0;
     cu.prev_end = -1;
+    const int rows = p.rows_total;
+    if (cu.nch > 0) {
+        const long long nnz = p.row_ptr[rows];
+        if (nnz > p.max_entries || nnz < 0) {  // more entries than q_idx / slot can hold
+            raise_status(p.status, BSA_ERR_INDEX);
+            cu.nch = 0;
+        } else {
+            cu.nbw = rows / (p.H * p.nblk);
+        }
+    }
     return cu;
+}
+
+// Moves to the next window with a non-empty share; false when none is left.
+__device__ __forceinline__ bool cursor_window(const Params& p, Cursor& cu) {
+    const int rpw = p.H * p.nblk;
+    while (++cu.bw < cu.nbw) {
+        const int e0 = p.row_ptr[cu.bw * rpw], e1 = p.row_ptr[(cu.bw + 1) * rpw];
+        const long long n = (long long)e1 - e0;
+        if (n <= 0) continue;
+        cu.lo = e0 + (int)(n * blockIdx.x / gridDim.x);
+        cu.hi = e0 + (int)(n * (blockIdx.x + 1) / gridDim.x);
+        if (cu.lo >= cu.hi) continue;
+        int a = 0, b = cu.nch - 1;  // last chunk whose start is <= lo
+        while (a < b) {
+            const int m = (a + b + 1) >> 1;
+            if (p.chunks[4 * m + 1] <= cu.lo) a = m;
+            else b = m - 1;
+        }
+        cu.c = a;
+        cu.prev_end = -1;
+        cu.e = cu.end = 0;
+        return true;
+    }
+    return false;
 }
 
 // 1: the next sub-tile is (row, e0, np); new_seg says it opens a chunk
 // segment (a new K/V block).  0: the share is done.  -1: the chunk list does
-// not tile the entry space in order (BSA_ERR_INDEX raised).
+// not tile the window's entries in order (BSA_ERR_INDEX raised).
 __device__ __forceinline__ int cursor_next(const Params& p, Cursor& cu, int PT, int& row, int& e0, int& np,
                                            bool& new_seg) {
     new_seg = false;
     while (cu.e >= cu.end) {
-        if (cu.c >= cu.nch) return 0;
+        if (cu.nbw < 0) return 0;
+        if (cu.bw < 0 || cu.c >= cu.nch || p.chunks[4 * cu.c + 1] >= cu.hi) {
+            if (!cursor_window(p, cu)) return 0;
+            continue;
+        }
         const int r = p.chunks[4 * cu.c], start = p.chunks[4 * cu.c + 1], len = p.chunks[4 * cu.c + 2];
-        if (start >= cu.hi) return 0;
-        if ((cu.prev_end >= 0 && start != cu.prev_end) || len < 0 || r < 0 || r >= p.rows_total) {
+        if ((cu.prev_end >= 0 && start != cu.prev_end) || len < 0 || r < 0 || r >= p.rows_total ||
+            r / (p.H * p.nblk) != cu.bw) {
             raise_status(p.status, BSA_ERR_INDEX);
             return -1;
         }
@@ -181,6 +198,14 @@ __device__ __forceinline__ int cursor_next(const Params& p, Cursor& cu, int PT, 
     return 1;
 }
 
+// (batch, KV head, block) of a row ((batch * nwin + window) * H + head) * nblk + block
+__device__ __forceinline__ void decode_row(const Params& p, int row, int& b, int& h, int& blk) {
+    const int g = row / p.nblk;
+    blk = row - g * p.nblk;
+    h = g % p.H;
+    b = g / (p.H * p.nwin);
+}
+
 // The next sub-tile of parity w (the ones a softmax warpgroup owns), with the
 // segment it belongs to; jj counts every sub-tile the cursor has passed.
 struct OwnTile {
@@ -194,12 +219,7 @@ __device__ __forceinline__ bool next_own(const Params& p, Cursor& cu, int PT, in
         bool ns;
         if (cursor_next(p, cu, PT, row, e0, np, ns) <= 0) return false;
         ++jj;
-        if (ns) {
-            const int g = row / p.nblk;
-            sb = g / p.H;
-            shd = g % p.H;
-            sblk = row % p.nblk;
-        }
+        if (ns) decode_row(p, row, sb, shd, sblk);
         if ((jj & 1) == w) {
             t.j = jj;
             t.e0 = e0;
@@ -214,7 +234,9 @@ __device__ __forceinline__ bool next_own(const Params& p, Cursor& cu, int PT, in
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_q2,
+                  const __grid_constant__ CUtensorMap tm_q4, const __grid_constant__ CUtensorMap tm_q8,
+                  const __grid_constant__ CUtensorMap tm_q16, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params prm) {
     using C = Cfg<BS>;
     constexpr int QS = C::kQStages;
@@ -250,7 +272,6 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_alloc(base + C::OFF_MISC, 512);
         ptx::tmem_relinquish();
     }
-    const Share sh = cta_share(prm);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -263,7 +284,7 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
-        Cursor cu = cursor_begin(sh);
+        Cursor cu = cursor_begin(prm);
         int b = 0, h = 0, issued = 0, segs = 0;
         // one sub-tile of lookahead: its query positions load while this one is issued
         int n_row = 0, n_e0 = 0, n_np = 0;
@@ -285,9 +306,8 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 if (segs > 0 && !__all_sync(0xffffffffu, wait_bar(bar(C::BAR_KVE), (uint32_t)(segs - 1) & 1u,
                                                                    abort_flag, prm.status)))
                     break;
-                const int g = row / prm.nblk, blk = row % prm.nblk;
-                b = g / prm.H;
-                h = g % prm.H;
+                int blk;
+                decode_row(prm, row, b, h, blk);
                 if (lane == 0) {
                     const int tok = b * prm.N + blk * BS;
                     const uint32_t fb = bar(C::BAR_KVF);
@@ -307,10 +327,26 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t fb = bar(C::BAR_QF + st);
             if (lane == 0) ptx::mbar_arrive_expect_tx(fb, (uint32_t)np * G * 256u);
             __syncwarp();
-            if (lane < np) {
-                const uint32_t dst = base + C::OFF_Q + st * C::kQBytes + lane * G * 128;
-                ptx::tma_load_3d(dst, &tm_q, 0, h * G, b * prm.N + pos, fb);
-                ptx::tma_load_3d(dst + C::kQHalf, &tm_q, 64, h * G, b * prm.N + pos, fb);
+            // Positions of a row ascend, and hot blocks are selected by runs of
+            // consecutive positions: a run is loaded with boxes of 2^k positions
+            // (largest first), one TMA operation per box and half instead of one
+            // per position (the TMA unit's operation rate bounds this warp).
+            const int pnext = __shfl_down_sync(0xffffffffu, pos, 1);
+            const int pprev = __shfl_up_sync(0xffffffffu, pos, 1);
+            const bool in = lane < np;
+            const unsigned ends = __ballot_sync(0xffffffffu, in && !(lane + 1 < np && pnext == pos + 1));
+            if (in && (lane == 0 || pprev + 1 != pos)) {
+                int p0 = lane, L = __ffs(ends >> lane), tok = b * prm.N + pos;
+                while (L > 0) {
+                    const int lk = min(31 - __clz(L), 4);
+                    const CUtensorMap* mq = lk == 0 ? &tm_q : lk == 1 ? &tm_q2 : lk == 2 ? &tm_q4 : lk == 3 ? &tm_q8 : &tm_q16;
+                    const uint32_t dst = base + C::OFF_Q + st * C::kQBytes + p0 * G * 128;
+                    ptx::tma_load_3d(dst, mq, 0, h * G, tok, fb);
+                    ptx::tma_load_3d(dst + C::kQHalf, mq, 64, h * G, tok, fb);
+                    p0 += 1 << lk;
+                    tok += 1 << lk;
+                    L -= 1 << lk;
+                }
             }
             issued = j + 1;
         }
@@ -332,7 +368,7 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             constexpr uint32_t idS = ptx::idesc_bf16(kRows, BS, false);
             constexpr uint32_t idO = ptx::idesc_bf16(kRows, kHD, true);
             const uint32_t ka = base + C::OFF_K, va = base + C::OFF_V;
-            Cursor cu = cursor_begin(sh);
+            Cursor cu = cursor_begin(prm);
             int pending = -1;  // sub-tile whose P V is still to be issued
             int segs = 0;
             bool ok = true;
@@ -411,8 +447,7 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t tS = tmem + lane_off + (uint32_t)w * 128;
         const uint32_t tO = tmem + lane_off + 256 + (uint32_t)w * 128;
         const int p_in = trow / G, gq = trow % G;
-        uint8_t* stg = sm + C::OFF_STG + (warp - 4) * 4096;  // this warp's 32 rows x 128 B
-        Cursor cu = cursor_begin(sh);
+        Cursor cu = cursor_begin(prm);
         int jj = -1, sb = 0, shd = 0, sblk = 0;
         OwnTile cur, nxt;
         bool have = next_own(prm, cu, PT, w, jj, sb, shd, sblk, cur);
@@ -503,9 +538,8 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::BAR_PF + w));
-            // epilogue: O / l -> bf16 -> the (position, head, slot) row; L in natural log.
-            // Rows go out through the warp's staging buffer so that every store
-            // instruction writes whole 128-byte lines (4 rows x one 64-column half).
+            // epilogue: O / l -> bf16 -> the (position, head, slot) row, each thread its
+            // own row in 32-byte stores (one sector each); L in natural log.
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_OF + w), ph, abort_flag, prm.status))) break;
             ptx::tc_fence_after();
             // partial-buffer row; B*N*HQ*S < 2^31 is checked by the entry point
@@ -525,29 +559,18 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar(C::BAR_OE + w));
                 }
+                // each thread stores its own row: 32-byte pieces, one sector each
+                if (valid) {
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(prm.obuf + (long long)orow * kHD + part * OCOLS);
 #pragma unroll
-                for (int hl = 0; hl < OCOLS / 64; ++hl) {
-                    const int hh = part * (OCOLS / 64) + hl;  // 64-column half of the row
+                    for (int c = 0; c < OCOLS / 16; ++c) {
+                        uint32_t wv[8];
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t* oc = o + hl * 64 + 8 * c;
-                        uint4 q4;
-                        q4.x = ptx::pack_bf16x2(__uint_as_float(oc[0]) * inv, __uint_as_float(oc[1]) * inv);
-                        q4.y = ptx::pack_bf16x2(__uint_as_float(oc[2]) * inv, __uint_as_float(oc[3]) * inv);
-                        q4.z = ptx::pack_bf16x2(__uint_as_float(oc[4]) * inv, __uint_as_float(oc[5]) * inv);
-                        q4.w = ptx::pack_bf16x2(__uint_as_float(oc[6]) * inv, __uint_as_float(oc[7]) * inv);
-                        // 16-byte chunk c of row `lane`, XOR-swizzled across the bank groups
-                        *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) = q4;
+                        for (int e = 0; e < 8; ++e)
+                            wv[e] = ptx::pack_bf16x2(__uint_as_float(o[16 * c + 2 * e]) * inv,
+                                                     __uint_as_float(o[16 * c + 2 * e + 1]) * inv);
+                        ptx::st_global_v8(dst + 32 * c, wv);
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int i2 = 0; i2 < 8; ++i2) {
-                        const int r = 4 * i2 + (lane >> 3), c = lane & 7;
-                        const int dst = __shfl_sync(0xffffffffu, orow, r);
-                        const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
-                        if (dst >= 0) *reinterpret_cast<uint4*>(prm.obuf + (long long)dst * kHD + hh * 64 + c * 8) = v;
-                    }
-                    __syncwarp();
                 }
             }
             if (valid) prm.lsebuf[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -CUDART_INF_F;
@@ -610,12 +633,12 @@ static bool register_split_fits() {
 }
 
 template <int BS>
-static bsa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm,
+static bsa_status launch(const CUtensorMap* mq, const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm,
                          int grid, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kvouter_tc_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg<BS>::SMEM);
     if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "kvouter tc attribute: %s", cudaGetErrorString(e));
-    kvouter_tc_kernel<BS><<<grid, kThreads, Cfg<BS>::SMEM, st>>>(mq, mk, mv, prm);
+    kvouter_tc_kernel<BS><<<grid, kThreads, Cfg<BS>::SMEM, st>>>(mq[0], mq[1], mq[2], mq[3], mq[4], mk, mv, prm);
     return check_launch("kvouter_tc_kernel");
 }
 
@@ -623,18 +646,21 @@ static bsa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
 
 bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N, int HQ, int H, int D,
                       const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot, const int32_t* chunks,
-                      const int32_t* n_chunks, int max_chunks, int nblk, int BS, int S, int causal, float scale,
-                      void* obuf, float* lsebuf, cudaStream_t st, bool* handled) {
+                      const int32_t* n_chunks, int max_chunks, int nblk, int nwin, int BS, int S, int causal,
+                      float scale, void* obuf, float* lsebuf, cudaStream_t st, bool* handled) {
     *handled = false;
-    (void)row_ptr;
     const int G = HQ / H;
     if (D != kvtc::kHD || (BS != 64 && BS != 128) || G < 8 || G > 128 || (G & (G - 1)) != 0) return BSA_OK;
-    if (((uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)obuf) & 15) return BSA_OK;
+    if ((((uintptr_t)q | (uintptr_t)k | (uintptr_t)v) & 15) || ((uintptr_t)obuf & 31)) return BSA_OK;
     if (BS == 64 ? !kvtc::register_split_fits<64>() : !kvtc::register_split_fits<128>()) return BSA_OK;
     const long long tokens = (long long)B * N;
-    CUtensorMap mq, mk, mv;
-    if (!kvtc::make_bthd_map(&mq, q, HQ, tokens, G, 1) || !kvtc::make_bthd_map(&mk, k, H, tokens, 1, BS) ||
-        !kvtc::make_bthd_map(&mv, v, H, tokens, 1, BS))
+    // Q boxes of 1, 2, 4, 8, 16 consecutive positions (G heads each, at most 128 rows)
+    CUtensorMap mq[5], mk, mv;
+    for (int i = 0; i < 5; ++i) {
+        const int n = (1 << i) * G <= 128 ? 1 << i : 1;
+        if (!kvtc::make_bthd_map(&mq[i], q, HQ, tokens, G, n)) return BSA_OK;
+    }
+    if (!kvtc::make_bthd_map(&mk, k, H, tokens, 1, BS) || !kvtc::make_bthd_map(&mv, v, H, tokens, 1, BS))
         return BSA_OK;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
@@ -642,6 +668,7 @@ bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N,
         return BSA_OK;
     *handled = true;
     kvtc::Params prm{};
+    prm.row_ptr = row_ptr;
     prm.q_idx = q_idx;
     prm.slot = slot;
     prm.chunks = chunks;
@@ -656,7 +683,8 @@ bsa_status kvouter_tc(const void* q, const void* k, const void* v, int B, int N,
     prm.S = S;
     prm.nblk = nblk;
     prm.causal = causal ? 1 : 0;
-    prm.rows_total = B * H * nblk;
+    prm.nwin = nwin;
+    prm.rows_total = B * nwin * H * nblk;
     prm.max_chunks = max_chunks;
     prm.max_entries = (long long)B * H * N * S;
     prm.scale_log2 = scale * kLog2e;

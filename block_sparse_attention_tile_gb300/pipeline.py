@@ -251,13 +251,31 @@ class KVOuterPlan:
     n_chunks: torch.Tensor
     max_chunks: int
     nblk: int
+    window: int = 0
 
 
-def reverse_index(block_indices, block_counts, nblk, chunk_cap, workspace=None):
+# Query positions per window of the KV-outer order (0: one window).  Windows
+# make the grid work through one window of queries at a time, so each query row
+# is read from HBM once (measured: 58% fewer DRAM reads in the partial pass at
+# the MSA shape), but they add K/V segments; the partial pass is bound by its
+# softmax -> P V -> epilogue chain, not by HBM, so the default is one window.
+KV_WINDOW = 0
+
+
+def default_window(N):
+    return KV_WINDOW if 0 < KV_WINDOW < N else 0
+
+
+def windows(N, window):
+    return 1 if window <= 0 or window >= N else -(-N // window)
+
+
+def reverse_index(block_indices, block_counts, nblk, chunk_cap, workspace=None, window=None):
     B, N, H, S = block_indices.shape
     dev = block_indices.device
-    max_chunks = bsa.bsa_max_chunks(B, N, H, S, nblk, chunk_cap)
-    row_ptr = torch.empty((B * H * nblk + 1,), dtype=torch.int32, device=dev)
+    window = default_window(N) if window is None else window
+    max_chunks = bsa.bsa_max_chunks(B, N, H, S, nblk, chunk_cap, window)
+    row_ptr = torch.empty((B * windows(N, window) * H * nblk + 1,), dtype=torch.int32, device=dev)
     q_idx = torch.empty((B * H * N * S,), dtype=torch.int32, device=dev)
     slot = torch.empty_like(q_idx)
     chunks = torch.empty((max_chunks, 4), dtype=torch.int32, device=dev)
@@ -266,12 +284,12 @@ def reverse_index(block_indices, block_counts, nblk, chunk_cap, workspace=None):
         ws = bsa.bsa_reverse_index_workspace(B, N, H, nblk)
         workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
     bsa.bsa_build_reverse_index(block_indices, block_counts, B, N, H, S, nblk, chunk_cap, row_ptr, q_idx,
-                                slot, chunks, n_chunks, max_chunks, workspace)
-    return KVOuterPlan(row_ptr, q_idx, slot, chunks, n_chunks, max_chunks, nblk)
+                                slot, chunks, n_chunks, max_chunks, workspace, window=window)
+    return KVOuterPlan(row_ptr, q_idx, slot, chunks, n_chunks, max_chunks, nblk, window)
 
 
 def kvouter_attention(q, k, v, block_indices, block_counts, block_size, causal=True, scale=None,
-                      chunk_cap=None, obuf_dtype=torch.bfloat16, need_lse=True, plan=None):
+                      chunk_cap=None, obuf_dtype=torch.bfloat16, need_lse=True, plan=None, window=None):
     """KV-outer order: reverse index -> partial pass -> combine.  Same inputs
     and result as nsa_qouter."""
     B, N, HQ, D = q.shape
@@ -282,11 +300,12 @@ def kvouter_attention(q, k, v, block_indices, block_counts, block_size, causal=T
     if chunk_cap is None:
         chunk_cap = 2 * S * block_size
     if plan is None:
-        plan = reverse_index(block_indices, block_counts, nblk, chunk_cap)
+        plan = reverse_index(block_indices, block_counts, nblk, chunk_cap, window=window)
     obuf = torch.empty((B, N, HQ, S, D), dtype=obuf_dtype, device=q.device)
     lsebuf = torch.empty((B, N, HQ, S), dtype=torch.float32, device=q.device)
     bsa.bsa_fwd_kvouter(q, k, v, B, N, HQ, H, D, plan.row_ptr, plan.q_idx, plan.slot, plan.chunks,
-                        plan.n_chunks, plan.max_chunks, nblk, block_size, S, causal, scale, obuf, lsebuf)
+                        plan.n_chunks, plan.max_chunks, nblk, block_size, S, causal, scale, obuf, lsebuf,
+                        window=plan.window)
     out = torch.empty_like(q)
     lse = torch.empty((B, N, HQ), dtype=torch.float32, device=q.device) if need_lse else None
     bsa.bsa_combine(obuf, lsebuf, block_counts, B, N, HQ, H, S, D, out, lse)

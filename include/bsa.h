@@ -257,17 +257,23 @@ bsa_status bsa_fwd_qouter_tokens(const void* q, const void* k, const void* v, bs
  * entry carries its slot s in [0, S) (the position of the block in the
  * query's list), so partials never collide.
  * q2k_idx: [device] int32 [B, N, H, S] (token-major, as the NSA
- * block_indices); q2k_num: [device] int32 [B, N, H].  R = B*H CSR row groups,
- * row id = (b*H + h)*nblk + blk.  Within a row, query ids ascend.
- * Outputs [device]: row_ptr int32 [R*nblk + 1]; q_idx, slot int32 [R*N*S]
- * (first row_ptr[R*nblk] entries used); chunks int32 [max_chunks, 4] =
- * (row, start, length, 0) in row order; n_chunks int32 [1].
+ * block_indices); q2k_num: [device] int32 [B, N, H]; every list ascending
+ * with distinct ids (others latch BSA_ERR_INDEX; the offending slot is left
+ * out).  window: query positions per window, 0 (one window of all N
+ * positions, the page's CSR) or a multiple of 256.  The query positions of a
+ * batch are cut into nwin = ceil(N / window) windows and the rows are
+ * ((b*nwin + w)*H + h)*nblk + blk: the CSR of each window in turn, so the
+ * KV-outer pass can work through one window at a time (its query rows stay
+ * in L2).  Within a row, query ids (absolute positions) ascend.
+ * Outputs [device]: row_ptr int32 [B*nwin*H*nblk + 1]; q_idx, slot int32
+ * [B*H*N*S] (first row_ptr[B*nwin*H*nblk] entries used); chunks int32
+ * [max_chunks, 4] = (row, start, length, 0) in row order; n_chunks int32 [1].
  * workspace: [device] scratch of bsa_reverse_index_workspace() bytes.
- * max_chunks must be >= bsa_max_chunks(...). */
+ * max_chunks must be >= bsa_max_chunks(...) with the same window. */
 size_t bsa_reverse_index_workspace(int B, int N, int H, int nblk);
-int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap);
+int bsa_max_chunks(int B, int N, int H, int S, int nblk, int chunk_cap, int window);
 bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_num,
-                                   int B, int N, int H, int S, int nblk, int chunk_cap,
+                                   int B, int N, int H, int S, int nblk, int chunk_cap, int window,
                                    int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
                                    int32_t* chunks, int32_t* n_chunks, int max_chunks,
                                    void* workspace, size_t workspace_bytes, void* stream);
@@ -291,7 +297,7 @@ bsa_status bsa_build_reverse_index(const int32_t* q2k_idx, const int32_t* q2k_nu
  * no cudaMalloc, cudaFree or allocating library routine. */
 #define BSA_NOALLOC_SCRATCH_BYTES (1u << 20)
 bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, const int32_t* q2k_num,
-                                           int B, int N, int H, int S, int nblk, int chunk_cap,
+                                           int B, int N, int H, int S, int nblk, int chunk_cap, int window,
                                            int32_t* row_ptr, int32_t* q_idx, int32_t* slot,
                                            int32_t* chunks, int32_t* n_chunks, int max_chunks,
                                            void* stream);
@@ -303,14 +309,17 @@ bsa_status bsa_build_reverse_index_noalloc(const int32_t* q2k_idx, const int32_t
  * keys (causal: key <= query position), L_s = log sum exp S_j,
  * O_s = sum exp(S_j - L_s) V_j, written to slot s.
  * q: [device] BTHD [B, N, HQ, D]; k, v: [device] BTHD [B, N, H, D];
- * CSR / chunks from bsa_build_reverse_index.
+ * CSR / chunks from bsa_build_reverse_index, built with the same `window`.
+ * The tensor-core kernel (bf16, D = 128, block_size 64 or 128, G a power of
+ * two in [8, 128]) is a persistent grid: for each window in turn every CTA
+ * takes an equal share of the window's entries.
  * obuf: [device] [B, N, HQ, S, D] of obuf_dtype; lsebuf: [device] float
  * [B, N, HQ, S].  Slots that no chunk writes are left untouched. */
 bsa_status bsa_fwd_kvouter(const void* q, const void* k, const void* v, bsa_dtype dtype,
                            int B, int N, int HQ, int H, int D,
                            const int32_t* row_ptr, const int32_t* q_idx, const int32_t* slot,
                            const int32_t* chunks, const int32_t* n_chunks, int max_chunks,
-                           int nblk, int block_size, int S, int causal, float scale,
+                           int nblk, int window, int block_size, int S, int causal, float scale,
                            void* obuf, bsa_dtype obuf_dtype, float* lsebuf, void* stream);
 
 /* ------------------------------------------------------------------ a7 ----

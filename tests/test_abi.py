@@ -67,6 +67,9 @@ def test_reverse_index_sizes(bsa):
     m = bsa.bsa_max_chunks(1, 32768, 4, 16, 256, 4096)
     # every chunk list fits: one partial chunk per row plus full chunks
     assert m >= 4 * 256 + (4 * 32768 * 16) // 4096
+    # with windows of 1024 positions every window has rows of its own
+    assert bsa.bsa_max_chunks(1, 32768, 4, 16, 256, 4096, 1024) >= 32 * 4 * 256 + (4 * 32768 * 16) // 4096
+    assert bsa.bsa_max_chunks(1, 32768, 4, 16, 256, 4096, 40000) == m  # one window
 
 
 def test_invalid_arguments_are_rejected_without_cuda(bsa):
@@ -84,8 +87,10 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     rc = lib.bsa_route_topk(1, 1, 2, 4, 2, 8, 2, 1.0, 4, 1, 1, 16, 64, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "workspace" in bsa.bsa_last_error()  # 2*4*4*4 = 128 bytes needed
     assert bsa.bsa_route_workspace(24, 960) == 24 * 960 * 960 * 4
-    rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
+    rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 0, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # max_chunks too small
+    rc = lib.bsa_build_reverse_index(1, 1, 1, 4096, 1, 2, 4, 8, 300, 1, 1, 1, 1, 1, 10 ** 6, 1, 1 << 20, None)
+    assert rc == bsa.BSA_ERR_INVALID_ARG and "window" in bsa.bsa_last_error()  # not a multiple of 256
     # reweight: null q, then a workspace one int short of 2 heads x (32 splits x (8 floats + 1 int) + 8 floats)
     rc = lib.bsa_reweight_summaries(None, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()

@@ -127,7 +127,8 @@ def test_nsa_prefill_full_size():
     nblk = T // BS
     q2k = np.transpose(idx, (0, 2, 1, 3)).reshape(B * H, T, S)
     num = np.transpose(cnt, (0, 2, 1)).reshape(B * H, T)
-    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk)
+    assert plan.window == pl.default_window(T)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk, window=plan.window, heads=H)
     assert np.array_equal(plan.row_ptr.cpu().numpy(), row_ptr)
     nnz = int(row_ptr[-1])
     assert np.array_equal(plan.q_idx[:nnz].cpu().numpy(), q_idx)
@@ -148,7 +149,9 @@ def test_msa_prefill_full_size():
     nblk = T // BS
     q2k = np.transpose(idx, (0, 2, 1, 3)).reshape(B * H, T, S)
     num = np.transpose(cnt, (0, 2, 1)).reshape(B * H, T)
-    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk)
+    W = plan.window if plan.window > 0 else T
+    assert plan.window == pl.default_window(T)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk, window=W, heads=H)
     assert np.array_equal(plan.row_ptr.cpu().numpy(), row_ptr)
     nnz = int(row_ptr[-1])
     assert np.array_equal(plan.q_idx[:nnz].cpu().numpy(), q_idx)
@@ -157,8 +160,13 @@ def test_msa_prefill_full_size():
     nch = int(plan.n_chunks.item())
     assert nch == len(chunks)
     assert np.array_equal(plan.chunks[:nch, :3].cpu().numpy(), np.array(chunks))
-    # the sink block is shared by every query of every KV head: it must be split into chunks
-    assert row_ptr[1] - row_ptr[0] == T and sum(1 for c in chunks if c[0] == 0) == math.ceil(T / (2 * S * BS))
+    # the sink block is selected by every query of every KV head: in each window its row
+    # (KV head 0) holds every position of the window, cut into chunks of at most 2*S*BS
+    nwin = T // W
+    for w in range(nwin):
+        row = (w * H + 0) * nblk + 0
+        assert row_ptr[row + 1] - row_ptr[row] == W
+        assert sum(1 for c in chunks if c[0] == row) == math.ceil(W / (2 * S * BS))
     _check_token_workload(q, k, v, idx, cnt, BS, {"kvouter": (o_kv, l_kv), "qouter": (o_q, l_q)}, 24, 404)
 
 

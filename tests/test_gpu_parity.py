@@ -498,9 +498,10 @@ def _oracle_nsa(q, k, v, idx, cnt, BS, b, tokens=None):
                                          tokens=tokens)
 
 
+@pytest.mark.parametrize("window", [0, 256])
 @pytest.mark.parametrize("dtype,BS,S,zipf", [(torch.bfloat16, 64, 16, False), (torch.float32, 32, 4, False),
                                              (torch.bfloat16, 128, 16, True)])
-def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf):
+def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf, window):
     pl = _pipeline()
     B, T, HQ, H, D = 2, 448, 32, 2, 128 if dtype == torch.bfloat16 else 64
     q, k, v, idx, cnt = _nsa_inputs(B, T, HQ, H, D, BS, S, 303, dtype, zipf)
@@ -510,12 +511,12 @@ def test_nsa_qouter_and_kvouter(lib, dtype, BS, S, zipf):
     nblk = -(-T // BS)
     o_kv, l_kv, plan, obuf, lbuf = pl.kvouter_attention(
         qd, kd, vd, idx_d, cnt_d, BS, chunk_cap=300,
-        obuf_dtype=torch.float32 if dtype == torch.float32 else torch.bfloat16)
+        obuf_dtype=torch.float32 if dtype == torch.float32 else torch.bfloat16, window=window)
     torch.cuda.synchronize()
-    # reverse index bit-exact: rows ordered (b, h, blk), ascending queries
+    # reverse index bit-exact: rows ordered (b, window, h, blk), ascending queries
     q2k = np.transpose(idx, (0, 2, 1, 3)).reshape(B * H, T, S)
     num = np.transpose(cnt, (0, 2, 1)).reshape(B * H, T)
-    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk)
+    row_ptr, q_idx, slot = oracle.reverse_index(q2k, num, nblk, window=window, heads=H)
     assert np.array_equal(plan.row_ptr.cpu().numpy(), row_ptr)
     nnz = int(row_ptr[-1])
     assert np.array_equal(plan.q_idx[:nnz].cpu().numpy(), q_idx)
