@@ -339,6 +339,33 @@ def test_reblock_layout(lib, dtype, D, n_prefix, Nv, M):
         assert r_gpu >= r_oracle - 0.03, (r_gpu, r_oracle)
 
 
+@pytest.mark.parametrize("dtype,D,nb", [(torch.bfloat16, 128, 16), (torch.float32, 64, 8)])
+def test_reblock_partition_equals_oracle_leaf_for_leaf(lib, dtype, D, nb):
+    """The GPU Spark-Reblock layout against the oracle's partition, token for
+    token, on inputs whose decisions have margins far above bf16 rounding
+    (tests/reblock_arc.py: one tight cluster per block on an arc, shuffled
+    ids, an identity query moment).  It checks the landmark choice, the
+    projection's orientation, the capacity-aligned cut and the leaf order of
+    the GPU tree, on the bf16 tensor-core path and the fp32 one."""
+    from reblock_arc import arc_inputs
+    block, n_prefix, BH = 16, 5, 2
+    qs, ks, perms = [], [], []
+    for h in range(BH):
+        q, k, _ = arc_inputs(nb, block, D, n_prefix, 500 + 31 * h + D)
+        qs.append(torch.tensor(q, dtype=torch.float32).to(dtype))
+        ks.append(torch.tensor(k, dtype=torch.float32).to(dtype))
+    q, k = torch.stack(qs), torch.stack(ks)
+    N, Nv = n_prefix + nb * block, nb * block
+    perm = torch.empty((BH, Nv), dtype=torch.int32, device=DEV)
+    ws = torch.empty((lib.bsa_reblock_workspace(BH, N, D, n_prefix),), dtype=torch.uint8, device=DEV)
+    lib.bsa_reblock_layout(q.to(DEV), k.to(DEV), BH, N, D, n_prefix, block, perm, ws)
+    torch.cuda.synchronize()
+    for h in range(BH):
+        Q, K = f64(q[h]), f64(k[h])
+        want = oracle.reblock_layout(Q[n_prefix:], K[n_prefix:], block)
+        assert np.array_equal(perm[h].cpu().numpy(), want), h
+
+
 def test_permute_rows_round_trip(lib):
     BH, N, D, n_prefix = 2, 300, 24, 44
     x = synthetic.normal((BH, N, D), 5, DEV, torch.bfloat16)

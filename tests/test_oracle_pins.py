@@ -325,6 +325,50 @@ def test_nsa_counts_win_over_padding_slots():
     assert np.array_equal(a, b)
 
 
+def test_reblock_partition_closed_form_on_an_arc():
+    """[Spark] §06 partition on keys with a known answer (tests/reblock_arc.py):
+    one tight cluster per block on an arc, shuffled token ids, queries with an
+    identity moment.  Every split separates contiguous angle ranges, so the
+    leaves must be the clusters, in angle order (or its reverse), each leaf
+    ascending; rounding the features to bf16 must not move a single token."""
+    from reblock_arc import arc_inputs
+    for nb, block, D in [(8, 16, 64), (16, 16, 128)]:
+        q, k, cluster = arc_inputs(nb, block, D, 5, 77 + nb)
+        Qv, Kv = q[5:], k[5:]
+        L = oracle.metric_factor(Qv)
+        U = oracle.unit_features(Kv, L)
+        leaves = oracle.partition(U, block)
+        assert len(leaves) == nb
+        for leaf in leaves:
+            assert np.all(cluster[leaf] == cluster[leaf[0]]) and np.all(np.diff(leaf) > 0)
+        order = [int(cluster[leaf[0]]) for leaf in leaves]
+
+        def bisection(lo, hi, seq):
+            # the node holds clusters lo .. hi-1; its halves are the lower and upper angle
+            # ranges, and the half with the node's lowest token id goes right (a, the
+            # member farthest from that token, is in the other half and leads the order)
+            assert sorted(seq) == list(range(lo, hi))
+            if hi - lo == 1:
+                return
+            mid = (lo + hi) // 2
+            first_token = min(t for t in range(len(cluster)) if lo <= cluster[t] < hi)
+            right_low = cluster[first_token] < mid
+            left, right = seq[:mid - lo], seq[mid - lo:]
+            if right_low:
+                assert sorted(right) == list(range(lo, mid))
+                bisection(mid, hi, left)
+                bisection(lo, mid, right)
+            else:
+                assert sorted(left) == list(range(lo, mid))
+                bisection(lo, mid, left)
+                bisection(mid, hi, right)
+
+        bisection(0, nb, order)
+        Ub = torch.tensor(U, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+        leaves_b = oracle.partition(Ub, block)
+        assert all(np.array_equal(a, b) for a, b in zip(leaves, leaves_b))
+
+
 # ---------------------------------------------------------------- KV-outer (a5, a6, a7)
 
 def test_reverse_index_page_example():
