@@ -157,141 +157,226 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- CPU oracle samples
 
-ORACLE_BLOCK = r"""
-import json, os, sys, time
-sys.path.insert(0, {root!r})
-import numpy as np, torch
-import oracle
-from block_sparse_attention_tile_gb300 import synthetic
-w = json.loads({w!r})
-budget_s = {budget}
-bT, bH, bW = w["block"]; D = w["D"]; k = w["k"]; M = w["M"]
-segs = [s if isinstance(s, int) else tuple(s) for s in w["segments"]] if "segments" in w else None
-if segs is None:
-    T, H, W = w["grid"]
-n_text = w.get("n_text", 0); summary = w.get("summary", False); reweight = w.get("reweight", False)
-coarse = w.get("coarse", False)
-dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
-t0 = time.perf_counter()
-spans = None
-if segs is not None:
-    q, kk, v = synthetic.segment_qkv(1, segs, D, w["seed"], dt)
-    blocks, P_seg, spans = oracle.tile_segments(segs, bT, bH, bW, M)
-elif summary:
-    q, kk, v = synthetic.cluster_qkv(1, n_text, T * H * W, D, w["seed"], dt)
-    if w.get("reblock"):  # the Spark-Reblock layout of this head
-        Qh, Kh = (x[0].float().numpy().astype(np.float64) for x in (q, kk))
-        perm = oracle.reblock_layout(Qh[n_text:], Kh[n_text:], M)
-    else:
-        perm = synthetic.permutation(T * H * W, w["seed"] + 1)
-    blocks = oracle.tile_prefix(n_text, M) + oracle.tile_permuted(perm, M, offset=n_text)
-else:
-    q, kk, v = synthetic.video_qkv(1, 1, T, H, W, D, w["seed"], dt, field=(w["dtype"] == "bf16"))
-    blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
-Q, K, V = (x[0].float().numpy().astype(np.float64) for x in (q, kk, v))
-gen_s = time.perf_counter() - t0
-P = len(oracle.tile_prefix(n_text, M)) if n_text else 0
-if segs is not None:
-    P = P_seg
-t0 = time.perf_counter()
-qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
-vbar = oracle.pool_blocks(V, blocks) if (summary or coarse) else None
-E = oracle.routing_scores(qbar[P:], kbar[P:], D)
-if spans is not None:
-    idx, num = oracle.route_grouped(E, [(lo - P, hi - P) for lo, hi in spans], w["budgets"], k)
-else:
-    idx, num = oracle.route(E, k, k)
-sbias = None
-if reweight:
-    kbar, vbar, sbias, _ = oracle.reweight_summaries(Q, K, V, blocks, D ** -0.5, prefix_blocks=P,
-                                                     round_key=oracle.bf16_round if w["dtype"] == "bf16" else None)
-    kbar = np.concatenate([np.zeros((P, D)), kbar]); vbar = np.concatenate([np.zeros((P, D)), vbar])
-C = None
-if coarse:
-    C = oracle.coarse_attention(E, vbar[P:])
-    g = synthetic.normal((1, D), w["seed"] + 71)[0].double().numpy()
-route_s = time.perf_counter() - t0
-rng = np.random.default_rng(0)
-order = rng.permutation(len(blocks))
-t0 = time.perf_counter(); done = 0
-while done < len(order) and (done < 2 or time.perf_counter() - t0 < budget_s):
-    qb = [int(order[done])]
-    if summary:
-        oracle.summary_attention(Q, K, V, blocks, idx, num, kbar[P:], vbar[P:], D ** -0.5, prefix_blocks=P,
-                                 query_blocks=qb, block_bias=sbias)
-    else:
-        O, _ = oracle.block_sparse_attention(Q, K, V, blocks, idx, num, D ** -0.5, query_blocks=qb, prefix_blocks=P)
-        if C is not None and qb[0] >= P:
-            oracle.coarse_output(O, C[qb[0] - P:qb[0] - P + 1], g, [blocks[qb[0]]], 0)
-    done += 1
-attn_s = time.perf_counter() - t0
-J = len(blocks)
-step_s = w["B"] * w["heads"] * (route_s + J * attn_s / done)
-print(json.dumps(dict(step_s=step_s, units=done, total_units=J, route_s=route_s, attn_s=attn_s, gen_s=gen_s)))
-"""
+# Everything below runs in a spawned interpreter (bench.py --oracle-sample) with
+# the GPU hidden and one BLAS thread per process: the setup (inputs, pooling,
+# routing, reverse index) and a fixed subset of query blocks (or tokens) on one
+# thread, then the same attention spread over a spawned process pool with one
+# worker per host core.  Workers import this file, so it imports only the
+# standard library at module level.
+_ORACLE_STATE = {}
+ORACLE_CHUNK_TOKENS = 8   # query tokens per unit of the token workloads (all heads)
 
-ORACLE_TOKEN = r"""
-import json, os, sys, time
-sys.path.insert(0, {root!r})
-import numpy as np, torch
-import oracle
-from block_sparse_attention_tile_gb300 import synthetic
-w = json.loads({w!r})
-budget_s = {budget}
-B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
-t0 = time.perf_counter()
-q = synthetic.normal((1, T, HQ, D), w["seed"], dtype=torch.bfloat16)
-k = synthetic.normal((1, T, H, D), w["seed"] + 1, dtype=torch.bfloat16)
-v = synthetic.normal((1, T, H, D), w["seed"] + 2, dtype=torch.bfloat16)
-gen = synthetic.zipf_block_lists if w["zipf"] else synthetic.causal_block_lists
-idx, cnt = gen(1, T, H, S, BS, w["seed"])
-Qf, Kf, Vf = (x[0].float().numpy().astype(np.float64) for x in (q, k, v))
-gen_s = time.perf_counter() - t0
-nblk = -(-T // BS)
-t0 = time.perf_counter()
-oracle.reverse_index(np.transpose(idx, (0, 2, 1, 3)).reshape(H, T, S), np.transpose(cnt, (0, 2, 1)).reshape(H, T), nblk)
-index_s = time.perf_counter() - t0
-rng = np.random.default_rng(0)
-order = rng.permutation(T)
-t0 = time.perf_counter(); done = 0
-while done < T and (done < 2 or time.perf_counter() - t0 < budget_s):
-    chunk = [int(t) for t in order[done:done + 8]]
-    oracle.nsa_selected_attention(Qf, Kf, Vf, idx[0], cnt[0], BS, tokens=chunk)
-    done += len(chunk)
-attn_s = time.perf_counter() - t0
-step_s = B * (index_s + T * attn_s / done)
-print(json.dumps(dict(step_s=step_s, units=done, total_units=T, route_s=index_s, attn_s=attn_s, gen_s=gen_s)))
-"""
+
+def _oracle_setup(w):
+    """The oracle's inputs and routing for one head (block workloads) or one
+    batch element (token workloads); returns (state, setup seconds, units)."""
+    import numpy as np
+    import torch
+    if ROOT not in sys.path:
+        sys.path.insert(0, ROOT)
+    import oracle
+    from block_sparse_attention_tile_gb300 import synthetic
+    st = {"w": w}
+    if w["kind"] == "token":
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        q = synthetic.normal((1, T, HQ, D), w["seed"], dtype=torch.bfloat16)
+        k = synthetic.normal((1, T, H, D), w["seed"] + 1, dtype=torch.bfloat16)
+        v = synthetic.normal((1, T, H, D), w["seed"] + 2, dtype=torch.bfloat16)
+        gen = synthetic.zipf_block_lists if w["zipf"] else synthetic.causal_block_lists
+        idx, cnt = gen(1, T, H, S, BS, w["seed"])
+        st.update(Q=q[0].double().numpy(), K=k[0].double().numpy(), V=v[0].double().numpy(), idx=idx[0],
+                  cnt=cnt[0])
+        t0 = time.perf_counter()
+        nblk = -(-T // BS)
+        oracle.reverse_index(np.transpose(idx, (0, 2, 1, 3)).reshape(H, T, S),
+                             np.transpose(cnt, (0, 2, 1)).reshape(H, T), nblk)
+        setup_s = time.perf_counter() - t0
+        return st, setup_s, -(-T // ORACLE_CHUNK_TOKENS)
+    bT, bH, bW = w["block"]
+    D, k_, M = w["D"], w["k"], w["M"]
+    segs = [x if isinstance(x, int) else tuple(x) for x in w["segments"]] if "segments" in w else None
+    n_text = w.get("n_text", 0)
+    summary, reweight, coarse = w.get("summary", False), w.get("reweight", False), w.get("coarse", False)
+    dt = torch.bfloat16 if w["dtype"] == "bf16" else torch.float32
+    spans = None
+    if segs is not None:
+        q, kk, v = synthetic.segment_qkv(1, segs, D, w["seed"], dt)
+    elif summary:
+        T, H, W = w["grid"]
+        q, kk, v = synthetic.cluster_qkv(1, n_text, T * H * W, D, w["seed"], dt)
+    else:
+        T, H, W = w["grid"]
+        q, kk, v = synthetic.video_qkv(1, 1, T, H, W, D, w["seed"], dt, field=(w["dtype"] == "bf16"))
+    Q, K, V = (x[0].double().numpy() for x in (q, kk, v))
+    t0 = time.perf_counter()
+    if segs is not None:
+        blocks, P, spans = oracle.tile_segments(segs, bT, bH, bW, M)
+    elif summary:
+        T, H, W = w["grid"]
+        if w.get("reblock"):  # the Spark-Reblock layout of this head
+            perm = oracle.reblock_layout(Q[n_text:], K[n_text:], M)
+        else:
+            perm = synthetic.permutation(T * H * W, w["seed"] + 1)
+        blocks = oracle.tile_prefix(n_text, M) + oracle.tile_permuted(perm, M, offset=n_text)
+        P = len(oracle.tile_prefix(n_text, M))
+    else:
+        T, H, W = w["grid"]
+        blocks = oracle.tile_3d(T, H, W, bT, bH, bW)
+        P = 0
+    qbar, kbar = oracle.pool_blocks(Q, blocks), oracle.pool_blocks(K, blocks)
+    vbar = oracle.pool_blocks(V, blocks) if (summary or coarse) else None
+    E = oracle.routing_scores(qbar[P:], kbar[P:], D)
+    if spans is not None:
+        idx, num = oracle.route_grouped(E, [(lo - P, hi - P) for lo, hi in spans], w["budgets"], k_)
+    else:
+        idx, num = oracle.route(E, k_, k_)
+    sbias = None
+    if reweight:
+        kbar, vbar, sbias, _ = oracle.reweight_summaries(
+            Q, K, V, blocks, D ** -0.5, prefix_blocks=P,
+            round_key=oracle.bf16_round if w["dtype"] == "bf16" else None)
+        kbar = np.concatenate([np.zeros((P, D)), kbar])
+        vbar = np.concatenate([np.zeros((P, D)), vbar])
+    C = g = None
+    if coarse:
+        C = oracle.coarse_attention(E, vbar[P:])
+        g = synthetic.normal((1, D), w["seed"] + 71)[0].double().numpy()
+    setup_s = time.perf_counter() - t0
+    st.update(Q=Q, K=K, V=V, blocks=blocks, P=P, idx=idx, num=num, kbar=kbar, vbar=vbar, sbias=sbias, C=C, g=g)
+    return st, setup_s, len(blocks)
+
+
+def _oracle_attend(st, units):
+    """The oracle's attention for some units: query blocks (block workloads)
+    or chunks of ORACLE_CHUNK_TOKENS query tokens with all their heads."""
+    import oracle
+    w = st["w"]
+    if w["kind"] == "token":
+        T = w["T"]
+        toks = [t for u in units for t in range(u * ORACLE_CHUNK_TOKENS, min(T, (u + 1) * ORACLE_CHUNK_TOKENS))]
+        if toks:
+            oracle.nsa_selected_attention(st["Q"], st["K"], st["V"], st["idx"], st["cnt"], w["BS"], tokens=toks)
+        return
+    D, P = w["D"], st["P"]
+    for qb in units:
+        if w.get("summary"):
+            oracle.summary_attention(st["Q"], st["K"], st["V"], st["blocks"], st["idx"], st["num"], st["kbar"][P:],
+                                     st["vbar"][P:], D ** -0.5, prefix_blocks=P, query_blocks=[qb],
+                                     block_bias=st["sbias"])
+        else:
+            O, _ = oracle.block_sparse_attention(st["Q"], st["K"], st["V"], st["blocks"], st["idx"], st["num"],
+                                                 D ** -0.5, query_blocks=[qb], prefix_blocks=P)
+            if st["C"] is not None and qb >= P:
+                oracle.coarse_output(O, st["C"][qb - P:qb - P + 1], st["g"], [st["blocks"][qb]], 0)
+
+
+def _oracle_worker_init(wjson):
+    _ORACLE_STATE["st"] = _oracle_setup(json.loads(wjson))[0]
+
+
+def _oracle_worker_wait(seconds):
+    time.sleep(seconds)
+    return 0
+
+
+def _oracle_worker_task(units):
+    _oracle_attend(_ORACLE_STATE["st"], units)
+    return len(units)
+
+
+def _oracle_sample_main(spec):
+    """The spawned sampler: setup and a fixed subset on one thread, then the
+    process pool, either for a time budget (cpu_baseline) or for `steps` steps
+    of a fixed number of units each (the reference arm)."""
+    import concurrent.futures
+    import multiprocessing
+    import random
+    w = WORKLOADS[spec["workload"]]
+    cores = spec["cores"]
+    st, setup_s, total = _oracle_setup(w)
+    order = list(range(total))
+    random.Random(0).shuffle(order)
+    n1 = min(total, 4 if w["kind"] == "block" else 2)
+    t0 = time.perf_counter()
+    _oracle_attend(st, order[:n1])
+    t1_unit = (time.perf_counter() - t0) / n1
+    out = {"cores": cores, "setup_s": setup_s, "units_total": total, "one_thread_units": n1,
+           "one_thread_s_per_unit": t1_unit}
+    # units per pool task: at least ~50 ms of work, so the pool's per-task
+    # messaging stays small beside it
+    per_task = max(1, min(64, int(0.05 / max(t1_unit, 1e-6)) + 1))
+    out["units_per_task"] = per_task
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(cores, mp_context=ctx, initializer=_oracle_worker_init,
+                                                initargs=(json.dumps(w),)) as ex:
+        # every worker set up (its initializer runs before its first task) before the clock starts
+        list(ex.map(_oracle_worker_wait, [1.0] * (2 * cores)))
+        pos = n1
+        if spec.get("steps"):
+            walls, units = [], []
+            for _ in range(spec["steps"]):
+                n = spec["units_per_step"] * per_task
+                seq = [order[(pos + i) % total] for i in range(n)]
+                pos += n
+                batch = [seq[i:i + per_task] for i in range(0, n, per_task)]
+                t0 = time.perf_counter()
+                done = sum(ex.map(_oracle_worker_task, batch))
+                walls.append(time.perf_counter() - t0)
+                units.append(done)
+            out.update(step_walls_s=walls, step_units=units)
+        else:
+            t0 = time.perf_counter()
+            done = 0
+            while pos < total and (done < cores or time.perf_counter() - t0 < spec["budget_s"]):
+                seq = order[pos:pos + cores * per_task]
+                pos += len(seq)
+                done += sum(ex.map(_oracle_worker_task, [seq[i:i + per_task] for i in range(0, len(seq), per_task)]))
+            out.update(all_core_units=done, all_core_wall_s=time.perf_counter() - t0)
+    print(json.dumps(out), flush=True)
+
+
+def _run_sampler(spec):
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", json.dumps(spec)],
+                         capture_output=True, text=True, env=env, timeout=1800)
+    if out.returncode != 0:
+        raise RuntimeError("oracle sample failed:\n" + out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+def _sample_scale(w):
+    """(independent setups per step, units per setup, unit name)."""
+    if w["kind"] == "token":
+        return w["B"], "chunks of %d query tokens (all %d heads)" % (ORACLE_CHUNK_TOKENS, w["HQ"])
+    return w["B"] * w["heads"], "query blocks of one head"
 
 
 def run_oracle_sample(wname, budget_s=15.0):
-    """Times the CPU oracle on a bounded sample in a fresh interpreter (spawned, never forked)."""
+    """The CPU oracle as it stands, on a bounded sample of the workload: one
+    thread on a fixed subset, and all host cores through a spawned process
+    pool; both extrapolated to a full step."""
     w = WORKLOADS[wname]
     cores = os.cpu_count() or 1
-    env = dict(os.environ)
-    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[var] = str(cores)
-    env["CUDA_VISIBLE_DEVICES"] = ""
-    tmpl = ORACLE_TOKEN if w["kind"] == "token" else ORACLE_BLOCK
-    code = tmpl.format(root=ROOT, w=json.dumps(w), budget=budget_s)
-    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
-    if out.returncode != 0:
-        raise RuntimeError("oracle sample failed:\n" + out.stderr[-2000:])
-    r = json.loads(out.stdout.strip().splitlines()[-1])
-    value = metric_flops(w) / r["step_s"] / 1e12
-    if w["kind"] == "token":
-        sample = ("batch element 0 of %d: reverse index of all %d tokens (%.1f s) plus %d of %d query tokens "
-                  "attended, all %d heads (%.1f s); step time scaled by tokens and batch"
-                  % (w["B"], w["T"], r["route_s"], r["units"], r["total_units"], w["HQ"], r["attn_s"]))
-    else:
-        pre = (("Spark-Reblock layout, " if w.get("reblock") else "") + "tile map, pool, route"
-               + (" and Spark-Reweight summaries" if w.get("reweight") else "")
-               + (" and the coarse branch softmax(E) V_bar" if w.get("coarse") else ""))
-        sample = ("1 of %d heads: %s of all %d blocks (%.1f s) plus %d of %d query blocks "
-                  "attended (%.1f s); step time scaled by heads and blocks"
-                  % (w["heads"], pre, r["total_units"], r["route_s"], r["units"], r["total_units"], r["attn_s"]))
-    return {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
-            "step_s_extrapolated": r["step_s"]}
+    r = _run_sampler({"workload": wname, "cores": cores, "budget_s": budget_s})
+    setups, unit_name = _sample_scale(w)
+    units = setups * r["units_total"]
+    one_s = setups * r["setup_s"] + units * r["one_thread_s_per_unit"]
+    all_s = setups * r["setup_s"] / cores + units * r["all_core_wall_s"] / r["all_core_units"]
+    flops = metric_flops(w)
+    sample = ("setup of one %s on one thread (%.2f s: inputs, %s); attention of %d %s on one thread "
+              "(%.3f s each) and of %d more on %d spawned single-thread workers (%.1f s wall); both "
+              "extrapolated to all %d setups x %d units of a step"
+              % ("batch element" if w["kind"] == "token" else "head", r["setup_s"],
+                 "reverse index" if w["kind"] == "token" else "tile map, pool, route and the other per-head stages",
+                 r["one_thread_units"], unit_name, r["one_thread_s_per_unit"], r["all_core_units"], cores,
+                 r["all_core_wall_s"], setups, r["units_total"]))
+    return {"value": flops / all_s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "extrapolated": True, "step_s_extrapolated": all_s,
+            "one_thread": {"value": flops / one_s / 1e12, "step_s_extrapolated": one_s, "cores": 1},
+            "all_core": {"value": flops / all_s / 1e12, "step_s_extrapolated": all_s, "cores": cores}}
 
 
 # ---------------------------------------------------------------- traffic records
@@ -1103,32 +1188,44 @@ def gpu_arm(args):
 
 
 def reference_arm(args):
+    """The oracle on the host cores (there is no other implementation of the
+    pages to run): every step attends the same number of query units on all
+    cores through the sampler's process pool, so value and ms_per_step are the
+    sampled work over its own wall time; the full-step extrapolation rides
+    along."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
-    steps = []
-    cb = None
-    for i in range(args.warmup + args.steps):
-        cb = run_oracle_sample(args.workload, max(2.0, args.cpu_budget / 3))
-        if i >= args.warmup:
-            steps.append(cb["step_s_extrapolated"])
-    step_s = statistics.mean(steps)
-    value = metric_flops(w) / step_s / 1e12
+    cores = os.cpu_count() or 1
+    per_step = cores  # pool tasks per step, each of the sampler's units_per_task units
+    r = _run_sampler({"workload": args.workload, "cores": cores, "steps": args.warmup + args.steps,
+                      "units_per_step": per_step})
+    setups, unit_name = _sample_scale(w)
+    walls = r["step_walls_s"][args.warmup:]
+    units = r["step_units"][args.warmup:]
+    flops_per_unit = metric_flops(w) / (setups * r["units_total"])
+    step_s = statistics.mean(walls)
+    value = flops_per_unit * statistics.mean(units) / step_s / 1e12
+    full_s = setups * r["setup_s"] / cores + setups * r["units_total"] * step_s / statistics.mean(units)
     if w["kind"] == "token":
         cfg = {"workload": args.workload, "B": w["B"], "T": w["T"], "HQ": w["HQ"], "H": w["H"], "D": w["D"],
                "block_size": w["BS"], "S": w["S"]}
     else:
-        T, H, W = w["grid"]
-        cfg = {"workload": args.workload, "seq_len": T * H * W + w.get("n_text", 0), "heads": w["heads"],
-               "D": w["D"], "k": w["k"]}
+        cfg = {"workload": args.workload, "heads": w["heads"], "D": w["D"], "k": w["k"]}
+        if "grid" in w:
+            T, H, W = w["grid"]
+            cfg["seq_len"] = T * H * W + w.get("n_text", 0)
+    sample = ("each step: %d %s attended on %d spawned single-thread workers (the oracle as it stands); "
+              "a full step (%d setups x %d units) extrapolates to %.1f s"
+              % (per_step * r["units_per_task"], unit_name, cores, setups, r["units_total"], full_s))
     line = {"impl": "reference", "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "none", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfg,
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cb["cores"], "kind": "oracle",
-                             "sample": cb["sample"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             "full_step_s_extrapolated": full_s},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -1148,7 +1245,11 @@ def main():
     ap.add_argument("--window", type=int, default=None,
                     help="token workloads: query positions per KV-outer window (0 = one window; default: "
                          "the library pipeline's choice)")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_sample is not None:  # the spawned CPU sampler (see _oracle_sample_main)
+        _oracle_sample_main(json.loads(args.oracle_sample))
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
