@@ -69,8 +69,12 @@ WORKLOADS = {
                              seed=202, dtype="bf16", coarse=True),
     "spark_reweight": dict(kind="block", B=1, heads=24, D=128, grid=(16, 32, 64), block=(1, 1, 1), M=128, k=26,
                            seed=505, dtype="bf16", n_text=1024, summary=True, reweight=True),
-    "nsa_prefill": dict(kind="token", B=2, T=8192, HQ=64, H=4, D=128, BS=64, S=16, seed=303, zipf=False),
-    "msa_prefill": dict(kind="token", B=1, T=32768, HQ=64, H=4, D=128, BS=128, S=16, seed=404, zipf=True),
+    # each token workload runs in its page's order (the NSA selected branch query-outer, MSA KV-outer);
+    # the other order is timed beside it
+    "nsa_prefill": dict(kind="token", B=2, T=8192, HQ=64, H=4, D=128, BS=64, S=16, seed=303, zipf=False,
+                        order="qouter"),
+    "msa_prefill": dict(kind="token", B=1, T=32768, HQ=64, H=4, D=128, BS=128, S=16, seed=404, zipf=True,
+                        order="kvouter"),
 }
 DEFAULT = "video_dit_bsa"
 
@@ -879,10 +883,9 @@ class BlockWorkload:
 
 
 class TokenWorkload:
-    """GQA selected attention with supplied block lists: reverse index ->
-    KV-outer partials -> combine (the query-outer order timed beside it)."""
-
-    stage_names = ["reverse_index", "partials", "combine"]
+    """GQA selected attention with supplied block lists, in the workload's
+    order: query-outer (one launch) or KV-outer (reverse index -> partials ->
+    combine); the other order is timed beside it."""
 
     def __init__(self, name, w, dev, rank):
         import numpy as np
@@ -918,9 +921,32 @@ class TokenWorkload:
         self.out_q = torch.empty_like(self.q)
         self.lse_q = torch.empty_like(self.lse)
         self.scale = D ** -0.5
-        self.launches_per_step = 5
+        self.order = w.get("order", "kvouter")
+        if self.order == "qouter":
+            self.stage_names = ["attention"]
+            self.launches_per_step = 1
+        else:
+            self.stage_names = ["reverse_index", "partials", "combine"]
+            self.launches_per_step = 5
 
     def step(self, ev=None, q=None, k=None, v=None, idx=None, cnt=None):
+        from block_sparse_attention_tile_gb300 import bsa
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        q = self.q if q is None else q
+        k = self.k if k is None else k
+        v = self.v if v is None else v
+        idx = self.idx if idx is None else idx
+        cnt = self.cnt if cnt is None else cnt
+        st = self.torch.cuda.current_stream()
+        if self.order == "qouter":
+            if ev: ev[0].record(st)
+            bsa.bsa_fwd_qouter_tokens(q, k, v, B, T, HQ, H, D, idx, cnt, S, BS, True, self.scale, self.out, self.lse)
+            if ev: ev[1].record(st)
+            return
+        self.kvouter(ev, q, k, v, idx, cnt)
+
+    def kvouter(self, ev=None, q=None, k=None, v=None, idx=None, cnt=None):
         from block_sparse_attention_tile_gb300 import bsa
         w = self.w
         B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
@@ -971,58 +997,93 @@ class TokenWorkload:
         k1_bytes = nnz * G * (2 * D * 2 + 4) + nch * 2 * BS * D * 2
         return 4.0 * D * pairs, nnz, k1_bytes
 
-    def report(self, stage_ms, peaks, peak_kind, props):
+    def _time(self, fn, reps=3):
         torch = self.torch
-        flops, nnz, k1_bytes = self.algorithmic()
-        w = self.w
-        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
-        k1_s = stage_ms["partials"] * 1e-3
-        tensor_peak = peaks["bf16_tflops"]  # launches timed on their own: the burst peak
-        t_flop = flops / (tensor_peak * 1e12)
-        t_byte = k1_bytes / (peaks["hbm_gbs"] * 1e9)
-        if t_byte >= t_flop:
-            ach = k1_bytes / k1_s / 1e9
-            roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "peak_kind": peak_kind + " HBM copy", "algorithmic_bytes_per_launch": k1_bytes}
-        else:
-            ach = flops / k1_s / 1e12
-            roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
-                    "peak_kind": peak_kind + " bf16 burst", "frac_nominal": ach / NOMINAL_BF16_TFLOPS,
-                    "nominal_peak": NOMINAL_BF16_TFLOPS}
-        roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = read_traffic(self.name)
-        roof["kernel"] = "bsa_fwd_kvouter partials (K1)"
-        roof["algorithmic_flops_per_launch"] = flops
-        # combine: reads every written partial (bf16) + LSE, writes O (bf16) + LSE
-        cb_bytes = nnz * (HQ // H) * (D * 2 + 4) + B * T * HQ * (D * 2 + 4) + B * T * H * 4
-        cb_gbs = cb_bytes / (stage_ms["combine"] * 1e-3) / 1e9
-        # the query-outer order on the same inputs
         for _ in range(2):
-            self.qouter()
+            fn()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record()
-        for _ in range(3):
-            self.qouter()
+        for _ in range(reps):
+            fn()
         e1.record()
         torch.cuda.synchronize()
-        q_ms = e0.elapsed_time(e1) / 3
+        return e0.elapsed_time(e1) / reps
+
+    def report(self, stage_ms, peaks, peak_kind, props):
+        torch = self.torch
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        tensor_peak = peaks["bf16_tflops"]  # launches timed on their own: the burst peak
+        # the other order on the same inputs (the KV-outer one per stage)
+        if self.order == "qouter":
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            for _ in range(2):
+                self.kvouter()
+            torch.cuda.synchronize()
+            kv_stage = {n: 0.0 for n in ("reverse_index", "partials", "combine")}
+            for _ in range(3):
+                self.kvouter(ev)
+                torch.cuda.synchronize()
+                for j, n in enumerate(kv_stage):
+                    kv_stage[n] += ev[j].elapsed_time(ev[j + 1]) / 3
+            kv_ms = sum(kv_stage.values())
+            other = {"kvouter_order": {"ms": kv_ms, "stages_us": {n: v * 1e3 for n, v in kv_stage.items()},
+                                       "effective_tflops": metric_flops(w) / (kv_ms * 1e-3) / 1e12,
+                                       "kernels": "bsa_build_reverse_index, bsa_fwd_kvouter, bsa_combine"}}
+        else:
+            kv_stage = stage_ms
+            q_ms = self._time(self.qouter)
+            other = {"qouter_order": {"ms": q_ms, "effective_tflops": metric_flops(w) / (q_ms * 1e-3) / 1e12,
+                                      "kernel": "bsa_fwd_qouter_tokens"}}
+        flops, nnz, k1_bytes = self.algorithmic()
+        # K1 roofline: bytes of the page's I/O model (eq. 16) or FLOPs, whichever bounds it
+        k1_s = kv_stage["partials"] * 1e-3
+        if k1_bytes / (peaks["hbm_gbs"] * 1e9) >= flops / (tensor_peak * 1e12):
+            ach = k1_bytes / k1_s / 1e9
+            k1_roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "peak_kind": peak_kind + " HBM copy", "algorithmic_bytes_per_launch": k1_bytes}
+        else:
+            ach = flops / k1_s / 1e12
+            k1_roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                       "peak_kind": peak_kind + " bf16 burst", "frac_nominal": ach / NOMINAL_BF16_TFLOPS,
+                       "nominal_peak": NOMINAL_BF16_TFLOPS}
+        k1_roof["frac"] = k1_roof["achieved"] / k1_roof["peak"]
+        k1_roof["kernel"] = "bsa_fwd_kvouter partials (K1)"
+        k1_roof["algorithmic_flops_per_launch"] = flops
+        # combine: reads every written partial (bf16) + LSE, writes O (bf16) + LSE
+        cb_bytes = nnz * (HQ // H) * (D * 2 + 4) + B * T * HQ * (D * 2 + 4) + B * T * H * 4
+        cb_gbs = cb_bytes / (kv_stage["combine"] * 1e-3) / 1e9
+        if self.order == "qouter":
+            a_s = stage_ms["attention"] * 1e-3
+            ach = flops / a_s / 1e12
+            roof = {"bound": "tensor", "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                    "peak_kind": peak_kind + " bf16 burst", "frac": ach / tensor_peak,
+                    "frac_nominal": ach / NOMINAL_BF16_TFLOPS, "nominal_peak": NOMINAL_BF16_TFLOPS,
+                    "kernel": "bsa_fwd_qouter_tokens (tensor-core, query-outer)",
+                    "algorithmic_flops_per_launch": flops,
+                    "note": "FLOPs of the visible (query head, key) pairs; the kernel also multiplies the rows "
+                            "of positions that did not select a tile of the union (masked)"}
+            secondary = {"kvouter_partials": k1_roof}
+        else:
+            roof = k1_roof
+            secondary = {}
+        roof["traffic"] = read_traffic(self.name)
         compulsory = (self.q.numel() + self.k.numel() + self.v.numel() + self.out.numel()) * 2 + \
             self.idx.numel() * 4 + self.cnt.numel() * 4
         step_ms = sum(stage_ms.values())
         ideal = max(flops / (tensor_peak * 1e12), compulsory / (peaks["hbm_gbs"] * 1e9))
-        secondary = {
+        secondary.update({
             "combine": {"bound": "hbm", "achieved": cb_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": cb_gbs / peaks["hbm_gbs"], "bytes_per_launch": cb_bytes},
             "strict_step": {"ideal_ms": ideal * 1e3, "step_ms": step_ms, "frac": ideal * 1e3 / step_ms,
                             "note": "ideal = max(algorithmic FLOP / bf16 peak, compulsory Q,K,V,O,index bytes / "
-                                    "HBM peak)"},
-            "qouter_order": {"ms": q_ms, "effective_tflops": metric_flops(w) / (q_ms * 1e-3) / 1e12,
-                             "kernel": "bsa_fwd_qouter_tokens"}}
+                                    "HBM peak)"}})
+        secondary.update(other)
         config = {"workload": self.name, "B": B, "T": T, "HQ": HQ, "H": H, "D": D, "block_size": BS, "S": S,
                   "selection": "zipf(1.1) sink+own" if w["zipf"] else "causal uniform, counts U{1..S}",
+                  "order": "query-outer" if self.order == "qouter" else "kv-outer",
                   "chunk_cap": self.cap, "window": self.window, "nnz": nnz, "n_chunks": int(self.n_chunks.item()),
-                  "order": "kv-outer",
                   "l2": "inputs larger than L2: Q,K,V = %.2f GB per step"
                         % ((self.q.numel() + self.k.numel() + self.v.numel()) * 2 / 1e9)}
         return roof, secondary, config, "synthetic (seeded N(0,1); no dataset or weights)", "bf16"
