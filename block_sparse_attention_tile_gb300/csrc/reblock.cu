@@ -44,7 +44,6 @@ namespace bsa {
 
 constexpr int kRbSplits = 64;     // partial moments per head
 constexpr int kRbMaxD = 128;      // head dimension limit of the layout builder
-constexpr int kRbSplitThreads = 512;
 
 // ------------------------------------------------------------------ moment
 // CTA (split, head): rows [r0, r1) of the head's video tokens; thread (ty, tx)
@@ -318,58 +317,106 @@ __device__ __forceinline__ int rb_block_exscan(int v, int* wsum, int& total) {
     return before + x - v;
 }
 
-// The squared distance of a member's feature row to `c`, or its projection on
-// `c` (fp32 arithmetic on the bf16 row; a thread per member).
-template <bool DIST>
-__device__ __forceinline__ float rb_row_op(const __nv_bfloat16* __restrict__ row, const float* c, int D) {
-    float acc = 0.f;
-    if ((D & 7) == 0) {
-        for (int d0 = 0; d0 < D; d0 += 64) {
-            uint4 x[8];
+// One pass over the members [c0, c1) of order (token ids), a warp per run of
+// 32 members taken 8 rows at a time: every lane reads 8 bytes (4 features)
+// of each of the 8 rows before using any (8 loads in flight), so one load
+// instruction covers a whole 256-byte row; a reduce-scatter butterfly (9
+// shuffles for the 8 rows) leaves row (lane >> 2) & 7's full sum in the four
+// lanes that share those bits.  The sum is the row's squared distance to c (DIST) or its
+// projection on c; c: the lane's 4 entries (zero past D).  DIST: returns the
+// largest (order key of the distance, ~token id) over the members (ties to
+// the lower id); otherwise writes each member's (order key of the projection,
+// token id) to ky[m] and returns 0.
+template <bool DIST, int NT>
+__device__ __forceinline__ unsigned long long rb_warp_pass(const __nv_bfloat16* __restrict__ Uh,
+                                                           const int32_t* __restrict__ ord, int c0, int c1, int D,
+                                                           const float* c, unsigned long long* __restrict__ ky) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int NW = NT / 32;
+    const bool vec = (D & 3) == 0;
+    unsigned long long best = 0;
+    for (int base = c0 + 32 * warp; base < c1; base += 32 * NW) {
+        const int cnt = min(32, c1 - base);
+        const int tok = lane < cnt ? ord[base + lane] : 0;
+        for (int i = 0; i < cnt; i += 8) {
+            float acc[8];
+            uint2 x[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                x[u] = d0 + 8 * u < D ? *reinterpret_cast<const uint4*>(row + d0 + 8 * u) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < 8; ++j) {
+                const int t = __shfl_sync(0xffffffffu, tok, (i + j) & 31);
+                x[j] = make_uint2(0u, 0u);
+                if (vec && i + j < cnt && 4 * lane < D)
+                    x[j] = *reinterpret_cast<const uint2*>(Uh + (long long)t * D + 4 * lane);
+            }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int d = d0 + 8 * u;
-                if (d >= D) continue;
-                const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+            for (int j = 0; j < 8; ++j) {
+                float f[4] = {__uint_as_float(x[j].x << 16), __uint_as_float(x[j].x & 0xffff0000u),
+                              __uint_as_float(x[j].y << 16), __uint_as_float(x[j].y & 0xffff0000u)};
+                if (!vec) {
+                    const int t = __shfl_sync(0xffffffffu, tok, (i + j) & 31);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        f[e] = (i + j < cnt && 4 * lane + e < D) ? __bfloat162float(Uh[(long long)t * D + 4 * lane + e])
+                                                                 : 0.f;
+                }
+                float a = 0.f;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
                     if (DIST) {
-                        const float e0 = lo - c[d + 2 * e], e1 = hi - c[d + 2 * e + 1];
-                        acc = fmaf(e0, e0, fmaf(e1, e1, acc));
+                        const float df = f[e] - c[e];
+                        a = fmaf(df, df, a);
                     } else {
-                        acc = fmaf(lo, c[d + 2 * e], fmaf(hi, c[d + 2 * e + 1], acc));
+                        a = fmaf(f[e], c[e], a);
                     }
+                }
+                acc[j] = a;
+            }
+            // reduce-scatter: at offset o = 16, 8, 4 a lane keeps the half of its rows
+            // selected by its lane bit and adds the partner's copy of them
+#pragma unroll
+            for (int step = 0; step < 3; ++step) {
+                const int o = 16 >> step, half = 4 >> step;
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int k = 0; k < half; ++k) {
+                    const float send = upper ? acc[k] : acc[k + half];
+                    const float keep = upper ? acc[k + half] : acc[k];
+                    acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            float sum = acc[0] + __shfl_xor_sync(0xffffffffu, acc[0], 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            const int r = i + ((lane >> 2) & 7);  // this lane's row of the batch
+            const int t = __shfl_sync(0xffffffffu, tok, r & 31);
+            if (r < cnt) {
+                if (DIST) {
+                    const unsigned long long key = ((unsigned long long)rb_order_key(sum) << 32) |
+                                                   (unsigned long long)(0xffffffffu - (uint32_t)t);
+                    best = key > best ? key : best;
+                } else if ((lane & 3) == 0) {
+                    ky[base + r] = ((unsigned long long)rb_order_key(sum) << 32) | (uint32_t)t;
                 }
             }
         }
-    } else {
-        for (int d = 0; d < D; ++d) {
-            const float x = __bfloat162float(row[d]);
-            if (DIST) acc = fmaf(x - c[d], x - c[d], acc);
-            else acc = fmaf(x, c[d], acc);
-        }
     }
-    return acc;
+    return best;
 }
 
 // Cluster (node, head), C CTAs: CTA `rank` takes members [c0, c1) of the
 // node's members order[r0 .. r1) (token ids).  Partial results go through
 // shared memory slots that every CTA of the cluster reads after a cluster
 // barrier, so all of them take the same decisions.
-__global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __nv_bfloat16* __restrict__ U, int Nv,
+template <int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) reblock_split_kernel(const __nv_bfloat16* __restrict__ U, int Nv,
                                                                        int D, int block, int NB, int level,
                                                                        int32_t* __restrict__ order,
                                                                        int32_t* __restrict__ tmp,
                                                                        unsigned long long* __restrict__ keys) {
     __shared__ float ua[kRbMaxD], ub[kRbMaxD];
-    __shared__ unsigned long long red[kRbSplitThreads / 32];
+    __shared__ unsigned long long red[NT / 32];
     __shared__ unsigned int hist[256];
-    __shared__ int scan[kRbSplitThreads];
-    __shared__ int wsum[kRbSplitThreads / 32];
+    __shared__ int scan[NT];
+    __shared__ int wsum[NT / 32];
     __shared__ unsigned int hsum[256];
     __shared__ int s_digit, s_need, s_bincnt;
     __shared__ unsigned long long s_slot;  // this CTA's partial, read by the cluster
@@ -403,45 +450,42 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
         return t;
     };
     auto load_row = [&](float* dst, int t) {
-        for (int d = tid; d < D; d += kRbSplitThreads) dst[d] = __bfloat162float(Uh[(long long)t * D + d]);
+        for (int d = tid; d < D; d += NT) dst[d] = __bfloat162float(Uh[(long long)t * D + d]);
     };
 
     // 1. the node's lowest token id
     unsigned long long best = 0;
-    for (int m = c0 + tid; m < c1; m += kRbSplitThreads)
+    for (int m = c0 + tid; m < c1; m += NT)
         best = max(best, (unsigned long long)(0xffffffffu - (uint32_t)ord[m]));
     const int s0 = (int)(0xffffffffu - (uint32_t)cluster_max(best));
     load_row(ua, s0);
     __syncthreads();
     // 2-3. the landmarks: a = farthest from s0, then b = farthest from a (ties to the lower id)
+    const int lane4 = 4 * (tid & 31);
     for (int round = 0; round < 2; ++round) {
-        best = 0;
-#pragma unroll 2
-        for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
-            const int t = ord[m];
-            const float d2 = rb_row_op<true>(Uh + (long long)t * D, ua, D);
-            best = max(best, ((unsigned long long)rb_order_key(d2) << 32) |
-                                 (unsigned long long)(0xffffffffu - (uint32_t)t));
-        }
+        float cv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cv[e] = lane4 + e < D ? ua[lane4 + e] : 0.f;
+        best = rb_warp_pass<true, NT>(Uh, ord, c0, c1, D, cv, ky);
         const int far = (int)(0xffffffffu - (uint32_t)(cluster_max(best) & 0xffffffffull));
         if (round == 0) {
             load_row(ub, far);  // u_a
             __syncthreads();
-            for (int d = tid; d < D; d += kRbSplitThreads) ua[d] = ub[d];
+            for (int d = tid; d < D; d += NT) ua[d] = ub[d];
         } else {
             load_row(ua, far);  // u_b
         }
         __syncthreads();
     }
     // ub = u_a, ua = u_b: the direction u_b - u_a
-    for (int d = tid; d < D; d += kRbSplitThreads) ua[d] -= ub[d];
+    for (int d = tid; d < D; d += NT) ua[d] -= ub[d];
     __syncthreads();
     // 4. keys (projection, token id), ascending
-#pragma unroll 2
-    for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
-        const int t = ord[m];
-        const float p = rb_row_op<false>(Uh + (long long)t * D, ua, D);
-        ky[m] = ((unsigned long long)rb_order_key(p) << 32) | (uint32_t)t;
+    {
+        float cv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cv[e] = lane4 + e < D ? ua[lane4 + e] : 0.f;
+        rb_warp_pass<false, NT>(Uh, ord, c0, c1, D, cv, ky);
     }
     __syncthreads();
     // 5. the cut: the cap_left-th smallest key of the node (exact radix select,
@@ -449,30 +493,43 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     unsigned long long prefix = 0;
     int need = cap_left;  // rank (1-based) of the largest key that goes left
     for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int b = tid; b < 256; b += kRbSplitThreads) hist[b] = 0;
+        for (int b = tid; b < 256; b += NT) hist[b] = 0;
         __syncthreads();
         const unsigned long long mask_hi = shift == 56 ? 0ull : (~0ull << (shift + 8));
-        for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+        for (int m = c0 + tid; m < c1; m += NT) {
             const unsigned long long key = ky[m];
             if ((key & mask_hi) == prefix) atomicAdd(&hist[(key >> shift) & 255], 1u);
         }
         cl.sync();
-        // bin t summed over the cluster's CTAs (same order everywhere), then
-        // one thread walks the sums; every CTA takes the same digit
-        if (tid < 256) {
-            unsigned int h = 0;
-            for (int r = 0; r < C; ++r) h += cl.map_shared_rank(hist, r)[tid];
-            hsum[tid] = h;
+        // each thread owns BPT consecutive bins, each summed over the cluster's
+        // CTAs (same order everywhere); every CTA takes the same digit
+        constexpr int BPT = NT >= 256 ? 1 : 256 / NT;
+        const int b0 = tid * BPT;
+        int hloc = 0;
+        if (b0 < 256) {
+#pragma unroll
+            for (int e = 0; e < BPT; ++e) {
+                unsigned int h = 0;
+                for (int r = 0; r < C; ++r) h += cl.map_shared_rank(hist, r)[b0 + e];
+                hsum[b0 + e] = h;
+                hloc += (int)h;
+            }
         }
         // the digit: the first bin whose running count reaches `need` (the rank
         // always falls inside: cap_left < n), found by a scan over the bins
         int tot;
-        const int h = tid < 256 ? (int)hsum[tid] : 0;
-        const int before = rb_block_exscan(h, wsum, tot);
-        if (tid < 256 && before < need && (need <= before + h || tid == 255)) {
-            s_digit = tid;
-            s_need = need - before;
-            s_bincnt = h;
+        int run = rb_block_exscan(hloc, wsum, tot);
+        if (b0 < 256) {
+#pragma unroll
+            for (int e = 0; e < BPT; ++e) {
+                const int bin = b0 + e, h = (int)hsum[bin];
+                if (run < need && (need <= run + h || bin == 255)) {
+                    s_digit = bin;
+                    s_need = need - run;
+                    s_bincnt = h;
+                }
+                run += h;
+            }
         }
         __syncthreads();
         prefix |= (unsigned long long)s_digit << shift;
@@ -482,7 +539,7 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
             // finds its low bits (the same decision in every CTA: hsum is shared)
             const unsigned long long mask = ~0ull << shift;
             unsigned long long found = 0;
-            for (int m = c0 + tid; m < c1; m += kRbSplitThreads) {
+            for (int m = c0 + tid; m < c1; m += NT) {
                 const unsigned long long key = ky[m];
                 if ((key & mask) == prefix) found = key;
             }
@@ -495,7 +552,7 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
     // 6. stable split: contiguous runs per thread, counts scanned in thread,
     //    then CTA (cluster rank) order
     const int nc = c1 - c0;
-    const int per = (nc + kRbSplitThreads - 1) / kRbSplitThreads;
+    const int per = (nc + NT - 1) / NT;
     const int m0 = c0 + min(nc, tid * per), m1 = c0 + min(nc, tid * per + per);
     int nl = 0;
     for (int m = m0; m < m1; ++m) nl += ky[m] <= cut;
@@ -519,7 +576,7 @@ __global__ void __launch_bounds__(kRbSplitThreads) reblock_split_kernel(const __
         else tp[r0 + wr++] = t;
     }
     cl.sync();  // every CTA's writes to tp are visible to the cluster
-    for (int m = c0 + tid; m < c1; m += kRbSplitThreads) ord[m] = tp[m];
+    for (int m = c0 + tid; m < c1; m += NT) ord[m] = tp[m];
 }
 
 // Members of each block in ascending token id: CTA (block, head), an odd-even
@@ -670,13 +727,18 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
     int levels = 0;
     while ((1 << levels) < NB) ++levels;  // depth of the binary tree over NB blocks
     for (int l = 0; l < levels; ++l) {
-        // CTAs per node: about 2048 members each, a power of two up to 8
+        // CTAs per node: about 2048 members each, a power of two up to 8; threads
+        // per CTA: about four members each (128 to 512), so the deep levels' small
+        // nodes run as many small CTAs that are resident together instead of
+        // waves of mostly idle 512-thread ones
         const long long per_node = (long long)Nv >> l;
         int C = 1;
         while (C < 8 && per_node / (2 * C) >= 2048) C *= 2;
+        const long long per_cta = per_node / C;
+        const int nt = per_cta >= 2048 ? 512 : per_cta >= 1024 ? 256 : 128;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((1u << l) * C, BH);
-        cfg.blockDim = dim3(kRbSplitThreads);
+        cfg.blockDim = dim3(nt);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -686,8 +748,15 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, reblock_split_kernel, (const __nv_bfloat16*)w.U, Nv, D, block, NB, l, perm, w.tmp,
-                           w.keys);
+        if (nt == 512)
+            cudaLaunchKernelEx(&cfg, reblock_split_kernel<512>, (const __nv_bfloat16*)w.U, Nv, D, block, NB, l, perm,
+                               w.tmp, w.keys);
+        else if (nt == 256)
+            cudaLaunchKernelEx(&cfg, reblock_split_kernel<256>, (const __nv_bfloat16*)w.U, Nv, D, block, NB, l, perm,
+                               w.tmp, w.keys);
+        else
+            cudaLaunchKernelEx(&cfg, reblock_split_kernel<128>, (const __nv_bfloat16*)w.U, Nv, D, block, NB, l, perm,
+                               w.tmp, w.keys);
         if ((rc = check_launch("reblock_split_kernel")) != BSA_OK) return rc;
     }
     reblock_leaf_sort_kernel<<<dim3(NB, BH), 512, 0, st>>>(perm, Nv, block);
