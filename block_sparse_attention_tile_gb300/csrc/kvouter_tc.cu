@@ -31,9 +31,8 @@
 //              block's visible keys (a prefix of the tile: key < N and, when
 //              causal, key <= the query position), then the epilogue:
 //              O / l in bf16 to the (position, head, slot) rows of the
-//              partial buffer, staged per warp through shared memory so that
-//              each store instruction writes whole 128-byte lines, and
-//              L = ln-sum-exp.  Query positions and slots are read one owned
+//              partial buffer, each thread storing its own 256-byte row in
+//              32-byte pieces, and L = ln-sum-exp.  Query positions and slots are read one owned
 //              sub-tile ahead (the producer reads its positions one sub-tile
 //              ahead too), so no index load sits on the critical path.
 // A sub-tile meets exactly one key tile, so the softmax needs no running
