@@ -51,16 +51,27 @@ __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, i
         uint32_t prefix = 0;
         for (int bit = 31; bit >= 0; --bit) {
             const uint32_t cand = prefix | (1u << bit);
-            int cnt = 0;
+            // four independent counters: short add chains, and 64 registers a thread
+            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) cnt += key[i] >= cand;
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
+            for (int i = 0; i < 32; i += 4) {
+                c0 += key[i] >= cand;
+                c1 += key[i + 1] >= cand;
+                c2 += key[i + 2] >= cand;
+                c3 += key[i + 3] >= cand;
+            }
+            const int cnt = __reduce_add_sync(0xffffffffu, (c0 + c1) + (c2 + c3));
             if (cnt >= k) prefix = cand;
         }
-        int n_gt = 0;
+        int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) n_gt += key[i] > prefix;
-        n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+        for (int i = 0; i < 32; i += 4) {
+            g0 += key[i] > prefix;
+            g1 += key[i + 1] > prefix;
+            g2 += key[i + 2] > prefix;
+            g3 += key[i + 3] > prefix;
+        }
+        const int n_gt = __reduce_add_sync(0xffffffffu, (g0 + g1) + (g2 + g3));
         const int need_eq = k - n_gt;
         int eq_seen = 0, written = 0;
         const unsigned lt = (1u << lane) - 1u;
