@@ -1095,6 +1095,82 @@ def fp32_peak(peaks, props):
 
 # ---------------------------------------------------------------- GPU arm
 
+def time_device(wl, steps, warmup, local, world):
+    """Warm-up steps, then `steps` steps bracketed by a barrier and a synchronize
+    on both sides, timed with CUDA events on the launching stream (whole region
+    and per stage), with the SM clocks sampled meanwhile."""
+    import torch
+    import torch.distributed as dist
+
+    from block_sparse_attention_tile_gb300 import bsa
+
+    nst = len(wl.stage_names)
+    for _ in range(warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    if bsa.bsa_device_status() != bsa.BSA_OK:
+        raise RuntimeError("device status after warm-up: " + bsa.bsa_last_error())
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(steps):
+        wl.step(ev[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    stage_ms = {sn: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, sn in enumerate(wl.stage_names)}
+    if bsa.bsa_device_status() != bsa.BSA_OK:
+        raise RuntimeError("device status after timing: " + bsa.bsa_last_error())
+    return ms_total, stage_ms, clk
+
+
+def other_workloads(skip, dev, local, steps=5, warmup=3):
+    """Every other workload of the table timed on the device after the headline
+    (inputs resident, no end-to-end or CPU leg): per workload its step time,
+    metric value, stage times, the dominant kernel's roofline and the clocks."""
+    import torch
+
+    peaks, peak_kind = read_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    out = {}
+    for name in sorted(WORKLOADS):
+        if name == skip:
+            continue
+        w = dict(WORKLOADS[name])
+        try:
+            wl = (TokenWorkload if w["kind"] == "token" else BlockWorkload)(name, w, dev, 0)
+            ms_total, stage_ms, clk = time_device(wl, steps, warmup, local, 1)
+            roof, secondary, config, data, dtype = wl.report(stage_ms, peaks, peak_kind, props)
+            ms_step = ms_total / steps
+            entry = {"ms_per_step": round(ms_step, 4), "value": job_tflops(metric_flops(w), 1, ms_step),
+                     "unit": "TFLOP/s", "steps": steps, "warmup": warmup, "dtype": dtype,
+                     "stages_us": {sn: round(v * 1e3, 1) for sn, v in stage_ms.items()},
+                     "roofline": {k: roof.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                           "frac_nominal") if k in roof},
+                     "config": config, "clocks": clk}
+            for key in ("kvouter_order", "qouter_order"):
+                if key in roof:
+                    entry[key] = {k: roof[key].get(k) for k in ("ms", "stages_us") if k in roof[key]}
+            out[name] = entry
+        except Exception as exc:  # noqa: BLE001
+            out[name] = {"error": str(exc)[:300]}
+        wl = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def gpu_arm(args):
     import torch
     import torch.distributed as dist
@@ -1121,36 +1197,8 @@ def gpu_arm(args):
             w["H"] = args.heads
         name = name + "_%dheads" % args.heads
     wl = (TokenWorkload if w["kind"] == "token" else BlockWorkload)(name, w, dev, rank)
-    nst = len(wl.stage_names)
-
-    for _ in range(args.warmup):
-        wl.step()
-    torch.cuda.synchronize()
-    if bsa.bsa_device_status() != bsa.BSA_OK:
-        raise RuntimeError("device status after warm-up: " + bsa.bsa_last_error())
-
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    ms_total, stage_ms, clk = time_device(wl, args.steps, args.warmup, local, world)
     stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        wl.step(ev[i])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    stage_ms = {sn: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev) for j, sn in enumerate(wl.stage_names)}
-    if bsa.bsa_device_status() != bsa.BSA_OK:
-        raise RuntimeError("device status after timing: " + bsa.bsa_last_error())
 
     # end to end through the public API with host buffers: pinned inputs in,
     # the result out, every step
@@ -1243,6 +1291,15 @@ def gpu_arm(args):
                 line["cpu_baseline"] = run_oracle_sample(args.workload, args.cpu_budget)
             except Exception as exc:  # noqa: BLE001
                 line["cpu_baseline"] = {"value": None, "error": str(exc)[:300]}
+        if world == 1 and not args.headline_only and args.workload == DEFAULT and not args.heads:
+            # the other workloads, device-timed in the same run, after the headline's
+            # buffers are released
+            wl = None
+            h_in = d_in = h_out = ins = outs = None
+            e2e_step = None
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            line["other_workloads"] = other_workloads(args.workload, dev, local)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -1300,6 +1357,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="skip the device-timed pass over the other workloads that the default run adds")
     ap.add_argument("--heads", type=int, default=0,
                     help="fewer heads (KV heads for the token workloads) than the workload's: a small case "
                          "for profiler captures")
