@@ -565,6 +565,8 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             ptx::mma_ts(tmem + 256 + (uint32_t)w * 128, aP + kk * 8, dv + (uint32_t)(kk * 2048 >> 4),
                                         idO, (j >= 2 || kk > 0) ? 1u : 0u);
                     }
+                    ptx::mma_commit(bar(BAR_EMPTY + vst));  // V_j's stage is free once P V_j is done
+                    ++vc;
                     if (has_s) {
                         const uint32_t ka = base + OFF_RING + kst * kTileBytes;
                         const uint64_t dq = ptx::smem_desc(base + OFF_Q, 16, 1024), dk = ptx::smem_desc(ka, 16, 1024);
@@ -578,8 +580,6 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         ++kc;
                         if (j + 2 == n - 1) ptx::mma_commit(bar(BAR_QFREE));  // the item's last S
                     }
-                    ptx::mma_commit(bar(BAR_EMPTY + vst));
-                    ++vc;
                 }
                 if (!ok) break;
                 ptx::mma_commit(bar(BAR_OF));  // every product of this item is in O_0 / O_1
