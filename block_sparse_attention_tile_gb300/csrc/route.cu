@@ -4,9 +4,12 @@
 // per (batch, head); each row keeps its own TopK) and §4 (ascending block ids
 // padded with -1, plus the count).  Ties keep the lower block index.
 //
-// E is a float32 FMA contraction, not a tensor-core one: a bf16/tf32 rounding
-// of the pooled means would move the selected set away from the exact
-// definition.  The TopK is an exact radix select on order-preserving 32-bit
+// E must keep float32 accuracy: a bf16 or tf32 rounding of the pooled means
+// would move the selected set away from the exact definition.  With a
+// workspace, E comes from the tensor cores as three tf32 products of split
+// operands (route_tc.cu) where the layout allows, else from the float32 FMA
+// contraction below; the fused path (no workspace) keeps E rows in shared
+// memory and uses FMAs.  The TopK is an exact radix select on order-preserving 32-bit
 // keys: one warp per row finds the k-th largest key bit by bit (32 counting
 // passes), then writes the selected ids in ascending order with ballots.
 #include <algorithm>
@@ -226,12 +229,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
 
 // ---------------------------------------------------------------- two-kernel path
 // With a workspace, E goes to global memory (L2-resident at these sizes) and
-// the two halves run as separate kernels: a register-tiled FP32 contraction
-// (128 x 128 block tiles, 8 x 8 outputs per thread, the d axis in stages of
-// 8 double-buffered in shared memory, two CTAs per SM) and the select, one
-// warp per row.  Every E entry accumulates its dot product over d in
-// ascending order with fmaf and is scaled last, as in the fused kernel, so
-// both paths give the same E and the same lists.
+// the two halves run as separate kernels: the contraction and the select, one
+// warp per row.  The contraction runs on the tensor cores (route_tc.cu) where
+// the operands' layout allows a TMA map; this register-tiled FP32 kernel
+// (128 x 128 block tiles, 8 x 8 outputs per thread, the d axis in stages of 8
+// double-buffered in shared memory, two CTAs per SM) is the other case.  Here
+// every E entry accumulates its dot product over d in ascending order with
+// fmaf and is scaled last, as in the fused kernel.
 constexpr int kGB = 128, kGK = 8;
 
 __global__ void __launch_bounds__(256, 2) route_gemm_kernel(const float* __restrict__ qbar,
@@ -377,6 +381,22 @@ __global__ void __launch_bounds__(256) route_select_grouped_kernel(const float* 
     if (lane == 0) q2k_num[(long long)bh * J + row] = written;
 }
 
+// E on the tensor cores (route_tc.cu); sets *handled = false when the layout is not covered.
+bsa_status route_e_tc(const float* qbar, const float* kbar, int BH, int J, int D, long long head_stride, float scale,
+                      float* E, cudaStream_t st, bool* handled);
+
+// E into the workspace: the tensor-core contraction where it applies, else the
+// CUDA-core one
+static bsa_status route_e(const float* qbar, const float* kbar, int BH, int J, int D, long long head_stride,
+                          float scale, float* E, cudaStream_t st) {
+    bool handled = false;
+    bsa_status rc = route_e_tc(qbar, kbar, BH, J, D, head_stride, scale, E, st, &handled);
+    if (rc != BSA_OK || handled) return rc;
+    const dim3 g1((J + kGB - 1) / kGB, (J + kGB - 1) / kGB, BH);
+    route_gemm_kernel<<<g1, 256, 0, st>>>(qbar, kbar, J, D, head_stride, scale, E);
+    return check_launch("route_gemm_kernel");
+}
+
 }  // namespace bsa
 
 using namespace bsa;
@@ -402,9 +422,7 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
         BSA_REQUIRE(J <= 8192, "route: J > 8192");
         cudaStream_t st = as_stream(stream);
         float* E = static_cast<float*>(workspace);
-        const dim3 g1((J + kGB - 1) / kGB, (J + kGB - 1) / kGB, BH);
-        route_gemm_kernel<<<g1, 256, 0, st>>>(qbar, kbar, J, D, (long long)head_stride, scale, E);
-        bsa_status rc = check_launch("route_gemm_kernel");
+        bsa_status rc = route_e(qbar, kbar, BH, J, D, (long long)head_stride, scale, E, st);
         if (rc != BSA_OK) return rc;
         route_select_kernel<<<dim3((J + 7) / 8, BH), 256, 0, st>>>(E, J, k, kmax, q2k_idx, q2k_num);
         return check_launch("route_select_kernel");
@@ -468,9 +486,7 @@ extern "C" bsa_status bsa_route_topk_grouped(const float* qbar, const float* kba
     BSA_REQUIRE(((uintptr_t)workspace & 15) == 0, "route_grouped: workspace not 16-byte aligned");
     cudaStream_t st = as_stream(stream);
     float* E = static_cast<float*>(workspace);
-    const dim3 g1((J + kGB - 1) / kGB, (J + kGB - 1) / kGB, BH);
-    route_gemm_kernel<<<g1, 256, 0, st>>>(qbar, kbar, J, D, (long long)head_stride, scale, E);
-    bsa_status rc = check_launch("route_gemm_kernel");
+    bsa_status rc = route_e(qbar, kbar, BH, J, D, (long long)head_stride, scale, E, st);
     if (rc != BSA_OK) return rc;
     route_select_grouped_kernel<<<dim3((J + 7) / 8, BH), 256, 0, st>>>(E, J, rg, kmax, q2k_idx, q2k_num);
     return check_launch("route_select_grouped_kernel");

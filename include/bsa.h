@@ -157,14 +157,19 @@ bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtyp
  * and q2k_num.  Ties keep the lower block index.
  * qbar, kbar: [device] float; row i of head h at ptr + h*head_stride + i*D.
  * q2k_idx: [device] int32 [BH, J, kmax]; q2k_num: [device] int32 [BH, J].
- * 1 <= k <= J, k <= kmax, J <= 8192, D <= 256.  E is computed in float32,
- * each entry as a dot product accumulated over d in ascending order and then
- * scaled, so both paths below give the same lists.
+ * 1 <= k <= J, k <= kmax, J <= 8192, D <= 256.  E is computed to float32
+ * accuracy and scaled last; the lists match the exact definition except
+ * where the k-th and (k+1)-th scores of a row differ by less than the
+ * rounding of E (either set is then a valid TopK).
  * workspace: [device] bsa_route_workspace(BH, J) bytes (16-byte aligned) for
- * E, or NULL.  With it, E is written by a register-tiled contraction and
- * read back by the select (two launches) and left there: E[h][i][j] at
- * workspace + ((h*J + i)*J + j) floats, for bsa_coarse_attention; without
- * it, one fused kernel
+ * E, or NULL.  With it, E is written by a contraction and read back by the
+ * select (two launches) and left there: E[h][i][j] at workspace +
+ * ((h*J + i)*J + j) floats, for bsa_coarse_attention.  The contraction runs
+ * on the tensor cores (three tf32 products of operands split into a tf32 high
+ * part and a float32 remainder, accumulated in float32) when qbar and kbar
+ * are 16-byte aligned and D and head_stride are multiples of 4, else as
+ * float32 FMAs over d in ascending order.  Without a workspace, one fused
+ * kernel (float32 FMAs)
  * keeps the E rows of 8 to 32 query rows in shared memory, so even at 8 rows
  * (8*J + 128*(Dp+4) + 8*Dp) * 4 bytes must fit in 227 KB (Dp = D rounded up
  * to 4; J <= 5024 at D = 128), else BSA_ERR_UNSUPPORTED. */

@@ -733,15 +733,20 @@ def test_route_rows_per_cta_variants(lib, J, D):
     idx = torch.empty((BH, J, k + 3), dtype=torch.int32, device=DEV)
     num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
     lib.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, D ** -0.5, k + 3, idx, num)
-    # the two-kernel path (E in a workspace) computes the same E, so the same lists
+    # the two-kernel path: E in a workspace (on the tensor cores, as a three-term
+    # tf32 split, where the layout allows), then the select; each path's lists
+    # must match the oracle's except at reported near ties, and the workspace E
+    # must match the oracle's E
     ws = torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV)
     idx_ws, num_ws = torch.empty_like(idx), torch.empty_like(num)
     lib.bsa_route_topk(qbar, kbar, BH, J, D, J * D, k, D ** -0.5, k + 3, idx_ws, num_ws, ws)
     torch.cuda.synchronize()
-    assert torch.equal(idx, idx_ws) and torch.equal(num, num_ws)
     for bh in range(BH):
         E = oracle.routing_scores(f64(qbar[bh]), f64(kbar[bh]), D)
         check_route(idx[bh].cpu().numpy(), num[bh].cpu().numpy(), E, k)
+        check_route(idx_ws[bh].cpu().numpy(), num_ws[bh].cpu().numpy(), E, k)
+        Ews = ws[bh * J * J:(bh + 1) * J * J].view(J, J).double().cpu().numpy()
+        assert np.abs(Ews - E).max() <= 1e-5 * max(1.0, np.abs(E).max())
 
 
 # ---------------------------------------------------------------- device-side error reporting
