@@ -816,7 +816,10 @@ class BlockWorkload:
             "pool": {"bound": "hbm", "achieved": pool_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": pool_gbs / peaks["hbm_gbs"], "bytes_per_launch": pool_bytes},
             "route": {"bound": "alu", "achieved": route_tf, "peak": fp32, "unit": "TFLOP/s", "frac": route_tf / fp32,
-                      "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock"}}
+                      "flops_per_launch": rflops, "peak_note": "SMs x 128 FP32 lanes x 2 x max SM clock",
+                      "note": "E = Q_bar K_bar^T on the tensor cores (three tf32 products of split float32 "
+                              "operands), then the exact select on the CUDA cores; the FP32 figure is kept as the "
+                              "stage's reference peak"}}
         if self.reblock:
             Nv = self.N - self.w.get("n_text", 0)
             el = self.q.element_size()
