@@ -28,7 +28,8 @@
 //                              memory at cluster barriers
 //   reblock_leaf_sort_kernel   members of each block in ascending token id
 //   permute_rows_kernel        rows gathered into (or scattered back from) the
-//                              layout's order
+//                              layout's order (permute_rows256_kernel for
+//                              256-byte rows)
 #include <math_constants.h>
 
 #include <cooperative_groups.h>
@@ -650,6 +651,49 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const T* __restrict__
     }
 }
 
+// Rows of exactly 256 bytes (bf16 D = 128, float32 D = 64), 16-byte aligned: a
+// warp moves 8 rows, two at a time (a half-warp per row, 16 bytes a lane), with
+// all four pairs' loads issued before their stores.
+__global__ void __launch_bounds__(256) permute_rows256_kernel(const uint8_t* __restrict__ src,
+                                                              uint8_t* __restrict__ dst, int N, int n_prefix,
+                                                              const int32_t* __restrict__ perm, int inverse,
+                                                              int* status) {
+    const int bh = blockIdx.y, lane = threadIdx.x & 31, half = lane >> 4, piece = lane & 15;
+    const long long row0 = (long long)blockIdx.x * 64 + (threadIdx.x >> 5) * 8;
+    const int Nv = N - n_prefix;
+    long long s_row[4], d_row[4];
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long long row = row0 + 2 * i + half;
+        s_row[i] = d_row[i] = -1;
+        if (row < N) {
+            long long s = row, d = row;
+            bool ok = true;
+            if (row >= n_prefix) {
+                const int p = perm[(long long)bh * Nv + (row - n_prefix)];
+                if (p < 0 || p >= Nv) {
+                    if (piece == 0) raise_status(status, BSA_ERR_INDEX);
+                    ok = false;
+                } else if (inverse) {
+                    d = n_prefix + p;
+                } else {
+                    s = n_prefix + p;
+                }
+            }
+            if (ok) {
+                s_row[i] = s;
+                d_row[i] = d;
+            }
+        }
+        if (s_row[i] >= 0)
+            v[i] = reinterpret_cast<const uint4*>(src + ((long long)bh * N + s_row[i]) * 256)[piece];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        if (s_row[i] >= 0) reinterpret_cast<uint4*>(dst + ((long long)bh * N + d_row[i]) * 256)[piece] = v[i];
+}
+
 // tensor-core moment partials and features (reblock_tc.cu), bf16 with D = 128;
 // *handled = false when the shape is not covered
 bsa_status reblock_moment_tc(const void* q, int BH, int N, int n_prefix, int splits, float* part, cudaStream_t st,
@@ -809,6 +853,12 @@ bsa_status bsa_permute_rows(const void* src, void* dst, bsa_dtype dtype, int BH,
     BSA_REQUIRE(BH > 0 && BH <= 65535 && D > 0 && n_prefix >= 0 && N > n_prefix,
                 "permute_rows: sizes out of range (BH=%d N=%d D=%d n_prefix=%d)", BH, N, D, n_prefix);
     cudaStream_t st = as_stream(stream);
+    const size_t row_bytes = (size_t)D * (dtype == BSA_F32 ? 4 : 2);
+    if (row_bytes == 256 && (((uintptr_t)src | (uintptr_t)dst) & 15) == 0) {
+        permute_rows256_kernel<<<dim3((unsigned)((N + 63) / 64), BH), 256, 0, st>>>(
+            (const uint8_t*)src, (uint8_t*)dst, N, n_prefix, perm, inverse, status_word());
+        return check_launch("permute_rows256_kernel");
+    }
     const dim3 grid((unsigned)((N + 7) / 8), BH);
     if (dtype == BSA_F32)
         permute_rows_kernel<float><<<grid, 256, 0, st>>>((const float*)src, (float*)dst, N, D, n_prefix, perm,
