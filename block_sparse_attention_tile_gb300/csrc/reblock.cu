@@ -29,7 +29,8 @@
 //   reblock_leaf_sort_kernel   members of each block in ascending token id
 //   permute_rows_kernel        rows gathered into (or scattered back from) the
 //                              layout's order (permute_rows256_kernel for
-//                              256-byte rows)
+//                              256-byte rows, permute_words_kernel for
+//                              one-element rows such as the LSE)
 #include <math_constants.h>
 
 #include <cooperative_groups.h>
@@ -694,6 +695,28 @@ __global__ void __launch_bounds__(256) permute_rows256_kernel(const uint8_t* __r
         if (s_row[i] >= 0) reinterpret_cast<uint4*>(dst + ((long long)bh * N + d_row[i]) * 256)[piece] = v[i];
 }
 
+// Rows of one 4-byte element (the log-sum-exp of each row): a thread per row.
+__global__ void __launch_bounds__(256) permute_words_kernel(const uint32_t* __restrict__ src,
+                                                            uint32_t* __restrict__ dst, int N, int n_prefix,
+                                                            const int32_t* __restrict__ perm, int inverse,
+                                                            int* status) {
+    const int bh = blockIdx.y;
+    const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= N) return;
+    const int Nv = N - n_prefix;
+    long long s = row, d = row;
+    if (row >= n_prefix) {
+        const int p = perm[(long long)bh * Nv + (row - n_prefix)];
+        if (p < 0 || p >= Nv) {
+            raise_status(status, BSA_ERR_INDEX);
+            return;
+        }
+        if (inverse) d = n_prefix + p;
+        else s = n_prefix + p;
+    }
+    dst[(long long)bh * N + d] = src[(long long)bh * N + s];
+}
+
 // tensor-core moment partials and features (reblock_tc.cu), bf16 with D = 128;
 // *handled = false when the shape is not covered
 bsa_status reblock_moment_tc(const void* q, int BH, int N, int n_prefix, int splits, float* part, cudaStream_t st,
@@ -858,6 +881,11 @@ bsa_status bsa_permute_rows(const void* src, void* dst, bsa_dtype dtype, int BH,
         permute_rows256_kernel<<<dim3((unsigned)((N + 63) / 64), BH), 256, 0, st>>>(
             (const uint8_t*)src, (uint8_t*)dst, N, n_prefix, perm, inverse, status_word());
         return check_launch("permute_rows256_kernel");
+    }
+    if (row_bytes == 4 && (((uintptr_t)src | (uintptr_t)dst) & 3) == 0) {
+        permute_words_kernel<<<dim3((unsigned)((N + 255) / 256), BH), 256, 0, st>>>(
+            (const uint32_t*)src, (uint32_t*)dst, N, n_prefix, perm, inverse, status_word());
+        return check_launch("permute_words_kernel");
     }
     const dim3 grid((unsigned)((N + 7) / 8), BH);
     if (dtype == BSA_F32)

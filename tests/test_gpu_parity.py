@@ -366,9 +366,11 @@ def test_reblock_partition_equals_oracle_leaf_for_leaf(lib, dtype, D, nb):
         assert np.array_equal(perm[h].cpu().numpy(), want), h
 
 
-@pytest.mark.parametrize("D,dtype", [(24, torch.bfloat16), (128, torch.bfloat16), (64, torch.float32)])
+@pytest.mark.parametrize("D,dtype", [(24, torch.bfloat16), (128, torch.bfloat16), (64, torch.float32),
+                                     (1, torch.float32), (2, torch.bfloat16)])
 def test_permute_rows_round_trip(lib, D, dtype):
-    # 256-byte rows (bf16 D = 128, float32 D = 64) take the paired-row kernel; N = 300 leaves a ragged CTA
+    # 256-byte rows (bf16 D = 128, float32 D = 64) take the paired-row kernel and 4-byte rows (float32 D = 1,
+    # bf16 D = 2) the thread-per-row kernel; N = 300 leaves a ragged CTA
     BH, N, n_prefix = 2, 300, 44
     x = synthetic.normal((BH, N, D), 5, DEV, dtype)
     perm = torch.stack([torch.randperm(N - n_prefix, generator=torch.Generator().manual_seed(h)) for h in range(BH)])
