@@ -36,59 +36,64 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// TopK of J <= 32*KPL scores by one warp, the keys in registers (lane holds
+// columns lane + 32*i, i < KPL): exact radix select on order-preserving keys,
+// ties to the lower index, the selected ids (plus `first`) written ascending.
+template <int KPL>
+__device__ __forceinline__ void select_keys(const float* __restrict__ e, int J, int k, int lane,
+                                            int32_t* __restrict__ out, int first) {
+    uint32_t key[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        const int c = lane + 32 * i;
+        key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
+    }
+    uint32_t prefix = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = prefix | (1u << bit);
+        // independent counters: short add chains, and 64 registers a thread at KPL = 32
+        int cn[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) cn[i & 3] += key[i] >= cand;
+        const int cnt = __reduce_add_sync(0xffffffffu, (cn[0] + cn[1]) + (cn[2] + cn[3]));
+        if (cnt >= k) prefix = cand;
+    }
+    int g[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) g[i & 3] += key[i] > prefix;
+    const int n_gt = __reduce_add_sync(0xffffffffu, (g[0] + g[1]) + (g[2] + g[3]));
+    const int need_eq = k - n_gt;
+    int eq_seen = 0, written = 0;
+    const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        const int c = lane + 32 * i;
+        const bool eq = c < J && key[i] == prefix;
+        const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
+        const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
+        const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+        if (sel) out[written + __popc(sel_mask & lt)] = first + c;
+        written += __popc(sel_mask);
+        eq_seen += __popc(eq_mask);
+    }
+}
+
 // TopK of one row of E (J scores, in shared or global memory) by one warp:
 // exact radix select on order-preserving keys, ties to the lower index, the
 // selected ids (plus `first`, the row segment's offset) written ascending and
-// -1 padded to kmax, and the count (when num_out is not null).
+// -1 padded to kmax, and the count (when num_out is not null).  Rows of up to
+// 1024 scores keep their keys in registers, as many a lane as the row needs
+// (a short region of a grouped row does not pay for 32).
 __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, int k, int kmax, int lane,
                                            int32_t* __restrict__ out, int32_t* __restrict__ num_out,
                                            int first = 0) {
     if (J <= 1024) {
-        // the row's keys stay in registers: lane holds columns lane + 32*i
-        uint32_t key[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int c = lane + 32 * i;
-            key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
-        }
-        uint32_t prefix = 0;
-        for (int bit = 31; bit >= 0; --bit) {
-            const uint32_t cand = prefix | (1u << bit);
-            // four independent counters: short add chains, and 64 registers a thread
-            int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                c0 += key[i] >= cand;
-                c1 += key[i + 1] >= cand;
-                c2 += key[i + 2] >= cand;
-                c3 += key[i + 3] >= cand;
-            }
-            const int cnt = __reduce_add_sync(0xffffffffu, (c0 + c1) + (c2 + c3));
-            if (cnt >= k) prefix = cand;
-        }
-        int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-            g0 += key[i] > prefix;
-            g1 += key[i + 1] > prefix;
-            g2 += key[i + 2] > prefix;
-            g3 += key[i + 3] > prefix;
-        }
-        const int n_gt = __reduce_add_sync(0xffffffffu, (g0 + g1) + (g2 + g3));
-        const int need_eq = k - n_gt;
-        int eq_seen = 0, written = 0;
-        const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int c = lane + 32 * i;
-            const bool eq = c < J && key[i] == prefix;
-            const unsigned eq_mask = __ballot_sync(0xffffffffu, eq);
-            const bool sel = c < J && (key[i] > prefix || (eq && eq_seen + __popc(eq_mask & lt) < need_eq));
-            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
-            if (sel) out[written + __popc(sel_mask & lt)] = first + c;
-            written += __popc(sel_mask);
-            eq_seen += __popc(eq_mask);
-        }
+        if (J <= 32) select_keys<1>(e, J, k, lane, out, first);
+        else if (J <= 64) select_keys<2>(e, J, k, lane, out, first);
+        else if (J <= 128) select_keys<4>(e, J, k, lane, out, first);
+        else if (J <= 256) select_keys<8>(e, J, k, lane, out, first);
+        else if (J <= 512) select_keys<16>(e, J, k, lane, out, first);
+        else select_keys<32>(e, J, k, lane, out, first);
     } else {
         uint32_t prefix = 0;
         for (int bit = 31; bit >= 0; --bit) {
