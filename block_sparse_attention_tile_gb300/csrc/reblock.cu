@@ -109,32 +109,36 @@ __global__ void __launch_bounds__(256) reblock_moment_reduce(const float* __rest
 }
 
 // ------------------------------------------------------------------ factor
-// One CTA of kRbMaxD threads per head; column by column, thread i computes
-// row i.  A non-positive pivot (a zero moment) gives a zero column.
-__global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* __restrict__ M, int D, float ridge,
-                                                                   float* __restrict__ L) {
-    extern __shared__ float A[];  // [D][D + 1]
+// One CTA of 4*kRbMaxD threads per head, column by column; row i belongs to
+// threads 4i .. 4i+3.  Thread 4i+q accumulates the dot product's partial sum
+// over the columns c = q (mod 4) below the last multiple of 4 (plus, for q = 0,
+// the remaining columns), in ascending c, and the four are combined as
+// (t0 + t1) + (t2 + t3): the same sums, in the same order, as one thread per
+// row with four interleaved accumulators, a quarter of the dependent chain.
+// Rows are padded to D + 4 floats, so the warp's 8 rows x 4 columns fall in
+// 32 banks.  A non-positive pivot (a zero moment) gives a zero column.
+constexpr int kRbCholThreads = 4 * kRbMaxD;
+
+__global__ void __launch_bounds__(kRbCholThreads) reblock_cholesky_kernel(const float* __restrict__ M, int D,
+                                                                          float ridge, float* __restrict__ L) {
+    extern __shared__ float A[];  // [D][D + 4]
     __shared__ float s_tr, s_piv;
-    const int bh = blockIdx.x, i = threadIdx.x, ld = D + 1;
+    const int bh = blockIdx.x, tid = threadIdx.x, i = tid >> 2, q = tid & 3, ld = D + 4;
     const float* Mh = M + (long long)bh * D * D;
     if ((D & 3) == 0 && (((uintptr_t)Mh) & 15) == 0) {
         // 16-byte loads, several in flight per thread
         const int nq = D * D / 4, qpr = D / 4;
-#pragma unroll 8
-        for (int e = i; e < nq; e += blockDim.x) {
+#pragma unroll 4
+        for (int e = tid; e < nq; e += blockDim.x) {
             const float4 v = *reinterpret_cast<const float4*>(Mh + 4 * e);
-            float* a = A + (e / qpr) * ld + 4 * (e % qpr);
-            a[0] = v.x;
-            a[1] = v.y;
-            a[2] = v.z;
-            a[3] = v.w;
+            *reinterpret_cast<float4*>(A + (e / qpr) * ld + 4 * (e % qpr)) = v;
         }
     } else {
-#pragma unroll 8
-        for (int e = i; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = Mh[e];
+#pragma unroll 4
+        for (int e = tid; e < D * D; e += blockDim.x) A[(e / D) * ld + e % D] = Mh[e];
     }
     __syncthreads();
-    if (i == 0) {
+    if (tid == 0) {
         // the trace in a fixed order, four partial sums
         float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
         int d = 0;
@@ -148,31 +152,31 @@ __global__ void __launch_bounds__(kRbMaxD) reblock_cholesky_kernel(const float* 
         s_tr = (t0 + t1) + (t2 + t3);
     }
     __syncthreads();
-    if (i < D) A[i * ld + i] += ridge * s_tr / D;
+    if (q == 0 && i < D) A[i * ld + i] += ridge * s_tr / D;
     __syncthreads();
     for (int j = 0; j < D; ++j) {
-        float t = 0.f;
-        if (i >= j && i < D) {
-            // four independent partial sums: the loads run ahead of a short FMA chain
-            float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
-            int c = 0;
-#pragma unroll 2
-            for (; c + 4 <= j; c += 4) {
-                t0 = fmaf(A[i * ld + c], A[j * ld + c], t0);
-                t1 = fmaf(A[i * ld + c + 1], A[j * ld + c + 1], t1);
-                t2 = fmaf(A[i * ld + c + 2], A[j * ld + c + 2], t2);
-                t3 = fmaf(A[i * ld + c + 3], A[j * ld + c + 3], t3);
-            }
-            for (; c < j; ++c) t0 = fmaf(A[i * ld + c], A[j * ld + c], t0);
-            t = A[i * ld + j] - ((t0 + t1) + (t2 + t3));
+        const bool row = i >= j && i < D;
+        float p = 0.f;
+        if (row) {
+            const int j4 = j & ~3;
+#pragma unroll 4
+            for (int c = q; c < j4; c += 4) p = fmaf(A[i * ld + c], A[j * ld + c], p);
+            if (q == 0)
+                for (int c = j4; c < j; ++c) p = fmaf(A[i * ld + c], A[j * ld + c], p);
         }
-        if (i == j) s_piv = t > 0.f ? sqrtf(t) : 0.f;
+        // (t0 + t1) + (t2 + t3) across the row's four threads (every lane takes part)
+        const float p1 = __shfl_xor_sync(0xffffffffu, p, 1);
+        const float s01 = (q & 1) ? p1 + p : p + p1;  // both lanes of a pair: t_{2k} + t_{2k+1}
+        const float s23 = __shfl_xor_sync(0xffffffffu, s01, 2);
+        const float tot = (q & 2) ? s23 + s01 : s01 + s23;
+        const float t = row ? A[i * ld + j] - tot : 0.f;
+        if (i == j && q == 0) s_piv = t > 0.f ? sqrtf(t) : 0.f;
         __syncthreads();
-        if (i >= j && i < D) A[i * ld + j] = (i == j) ? s_piv : (s_piv > 0.f ? t / s_piv : 0.f);
+        if (row && q == 0) A[i * ld + j] = (i == j) ? s_piv : (s_piv > 0.f ? t / s_piv : 0.f);
         __syncthreads();
     }
     float* Lh = L + (long long)bh * D * D;
-    for (int e = i; e < D * D; e += blockDim.x) {
+    for (int e = tid; e < D * D; e += blockDim.x) {
         const int r = e / D, c = e % D;
         Lh[e] = c <= r ? A[r * ld + c] : 0.f;
     }
@@ -774,10 +778,10 @@ static bsa_status launch_reblock(const void* q, const void* k, int BH, int N, in
     }
     reblock_moment_reduce<<<dim3((D * D + 255) / 256, BH), 256, 0, st>>>(w.part, D, Nv, w.M);
     if ((rc = check_launch("reblock_moment_reduce")) != BSA_OK) return rc;
-    const size_t chol_smem = sizeof(float) * (size_t)D * (D + 1);
+    const size_t chol_smem = sizeof(float) * (size_t)D * (D + 4);
     if (chol_smem > 48 * 1024)
         cudaFuncSetAttribute(reblock_cholesky_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chol_smem);
-    reblock_cholesky_kernel<<<BH, kRbMaxD, chol_smem, st>>>(w.M, D, ridge, w.L);
+    reblock_cholesky_kernel<<<BH, kRbCholThreads, chol_smem, st>>>(w.M, D, ridge, w.L);
     if ((rc = check_launch("reblock_cholesky_kernel")) != BSA_OK) return rc;
     handled = false;
     if (tc && (rc = reblock_features_tc(k, BH, N, n_prefix, w.L, w.Lb, w.U, st, &handled)) != BSA_OK) return rc;
