@@ -32,9 +32,12 @@
 //              causal, key <= the query position), then the epilogue:
 //              O / l in bf16 to the (position, head, slot) rows of the
 //              partial buffer, each thread storing its own 256-byte row in
-//              32-byte pieces, and L = ln-sum-exp.  Query positions and slots are read one owned
+//              32-byte pieces, and L = ln-sum-exp.  The next owned sub-tile
+//              (its place in the chunk list, its rows' query positions and
+//              slots) is looked up while this one's P V runs, one owned
 //              sub-tile ahead (the producer reads its positions one sub-tile
-//              ahead too), so no index load sits on the critical path.
+//              ahead too), so neither the chunk walk nor an index load sits
+//              on the path from a sub-tile's S to its softmax.
 // A sub-tile meets exactly one key tile, so the softmax needs no running
 // rescale.  Every mbarrier wait is bounded (2 s); on expiry the CTA raises
 // BSA_ERR_TIMEOUT, stops issuing, drains its copies and MMAs, frees TMEM.
@@ -459,15 +462,6 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         while (have) {
             const OwnTile t = cur;
             const int tpos = pos, ts = s;
-            const bool have_n = next_own(prm, cu, PT, w, jj, sb, shd, sblk, nxt);
-            pos = -1;
-            s = -1;
-            if (have_n && p_in < nxt.np) {
-                pos = prm.q_idx[nxt.e0 + p_in];
-                s = prm.slot[nxt.e0 + p_in];
-            }
-            cur = nxt;
-            have = have_n;
 
             const int key0 = t.blk * BS;
             const bool valid = p_in < t.np && tpos >= 0 && tpos < prm.N && ts >= 0 && ts < prm.S;
@@ -537,6 +531,19 @@ kvouter_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(C::BAR_PF + w));
+            // the next owned sub-tile and its rows' positions and slots, while P V runs
+            // (off the path from one sub-tile's S to its softmax)
+            {
+                const bool have_n = next_own(prm, cu, PT, w, jj, sb, shd, sblk, nxt);
+                pos = -1;
+                s = -1;
+                if (have_n && p_in < nxt.np) {
+                    pos = prm.q_idx[nxt.e0 + p_in];
+                    s = prm.slot[nxt.e0 + p_in];
+                }
+                cur = nxt;
+                have = have_n;
+            }
             // epilogue: O / l -> bf16 -> the (position, head, slot) row, each thread its
             // own row in 32-byte stores (one sector each); L in natural log.
             if (!__all_sync(0xffffffffu, wait_bar(bar(C::BAR_OF + w), ph, abort_flag, prm.status))) break;
