@@ -622,6 +622,9 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float m_ref = -CUDART_INF_F, l = 0.f;
             bool ok = true;
             for (int s = w; s < n; s += 2) {
+                // the tile's size and kind do not depend on S: read them before waiting for it
+                // (a dense row's come from global memory)
+                const int inf = dense_row ? prm.block_sizes[s] : info[s];
                 ok = __all_sync(0xffffffffu,
                                 wait_bar(bar(BAR_SF + w), (uint32_t)su & 1u, abort_flag, prm.status));
                 if (!ok) break;
@@ -635,7 +638,6 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     ptx::tmem_ld32(tS + 96, xr + 96);
                     ptx::tmem_wait_ld();
                 }
-                const int inf = dense_row ? prm.block_sizes[s] : info[s];
                 const int nv = inf & 0xff;
                 const int vid = inf >> 8;  // 0: a real block; t + 1: summary tile t
                 float mxp[8];

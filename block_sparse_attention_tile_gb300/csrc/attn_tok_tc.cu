@@ -478,12 +478,8 @@ token_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             float m_ref = -CUDART_INF_F, l = 0.f;
             bool ok = true;
             for (int s = w; s < n; s += 2) {
-                ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + w), (uint32_t)su & 1u, abort_flag, prm.status,
-                                                      wait_ns));
-                if (!ok) break;
-                ++su;
-                ptx::tc_fence_after();
-                // this row's visible keys in each block of the tile (a prefix of the block)
+                // this row's visible keys in each block of the tile (a prefix of the block):
+                // independent of S, so worked out before waiting for it
                 int lim[SB];
                 bool full = true, any = false;
 #pragma unroll
@@ -493,6 +489,11 @@ token_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     full = full && lim[e] == BS;
                     any = any || lim[e] > 0;
                 }
+                ok = __all_sync(0xffffffffu, wait_bar(bar(BAR_SF + w), (uint32_t)su & 1u, abort_flag, prm.status,
+                                                      wait_ns));
+                if (!ok) break;
+                ++su;
+                ptx::tc_fence_after();
                 if (!__any_sync(0xffffffffu, any)) {
                     // no row of this warp selected the tile: P = 0
 #pragma unroll
