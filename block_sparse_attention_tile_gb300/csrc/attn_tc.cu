@@ -655,21 +655,12 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                         for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
                 } else {
-                    // a summary tile: scores scaled and biased by the log-mass of their block
-                    // (paired FMAs: the same results as fmaf on each lane), then the same
-                    // three-input max as a real tile
-                    const float2* bt2 = reinterpret_cast<const float2*>(bias + (vid - 1) * kBN);
-                    const float2 sc2 = make_float2(prm.scale_log2, prm.scale_log2);
+                    const float* bt = bias + (vid - 1) * kBN;
 #pragma unroll
-                    for (int c = 0; c < kBN; c += 2) {
-                        const float2 y = ptx::ffma2(make_float2(x[c], x[c + 1]), sc2, bt2[c >> 1]);
-                        x[c] = y.x;
-                        x[c + 1] = y.y;
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = fmaf(x[c], prm.scale_log2, bt[c]);
+                        mxp[c & 7] = fmaxf(mxp[c & 7], x[c]);
                     }
-#pragma unroll
-                    for (int c = 0; c < kBN; c += 16)
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) mxp[u] = ptx::fmax3(mxp[u], x[c + u], x[c + 8 + u]);
                 }
                 // the real tiles' maxima are of raw Q.K: scale once (scale > 0 keeps the order)
                 const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
@@ -725,23 +716,10 @@ bsa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                         sp[2 * u + 1] = acc2[u].y;
                     }
                 } else {
-                    // x holds the biased, scaled scores: subtract the reference (paired adds,
-                    // the same per-lane results and the same sp[c & 7] order as scalar code)
-                    const float2 nm2 = make_float2(-ref, -ref);
-                    float2 acc2[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) acc2[u] = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int c = 0; c < kBN; c += 2) {
-                        const float2 a = ptx::fadd2(make_float2(x[c], x[c + 1]), nm2);
-                        x[c] = ptx::ex2(a.x);
-                        x[c + 1] = ptx::ex2(a.y);
-                        acc2[(c >> 1) & 3] = ptx::fadd2(acc2[(c >> 1) & 3], make_float2(x[c], x[c + 1]));
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        sp[2 * u] = acc2[u].x;
-                        sp[2 * u + 1] = acc2[u].y;
+                    for (int c = 0; c < kBN; ++c) {
+                        x[c] = ptx::ex2(x[c] - ref);
+                        sp[c & 7] += x[c];
                     }
                 }
                 l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
