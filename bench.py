@@ -669,12 +669,17 @@ class BlockWorkload:
         if self.reblock:
             self.permute_out(sl, nh)
 
-    def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=2):
+    def make_e2e(self, h_in, d_in, h_out, heads_per_chunk=None):
         """End-to-end step with host buffers, pipelined by heads: chunk c's
         inputs are copied in on a copy stream while chunk c-1 computes, and each
         chunk's output is copied out as soon as it is done.  Chunks of 1, 2, then
-        heads_per_chunk heads, and one head last (the host-to-device copies bind
-        the step: at C2, 2-head chunks gave 15.31 ms, 3: 15.41, 4: 15.72, 8: 17.2)."""
+        heads_per_chunk heads, and one head last.  The host-to-device copies bind
+        the plain steps (at C2, 2-head chunks gave 15.31 ms, 3: 15.41, 4: 15.72,
+        8: 17.2); a step that builds the Spark-Reblock layout pays its tree
+        levels once a chunk, whatever the chunk's heads, so it takes 12-head
+        chunks (2: 10.5 ms, 4: 8.0, 8: 6.9, 12: 6.7)."""
+        if heads_per_chunk is None:
+            heads_per_chunk = 12 if self.reblock else 2
         torch = self.torch
         g = self.geom
         comp = torch.cuda.current_stream()
