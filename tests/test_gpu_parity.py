@@ -753,6 +753,29 @@ def test_route_rows_per_cta_variants(lib, J, D):
         assert np.abs(Ews - E).max() <= 1e-5 * max(1.0, np.abs(E).max())
 
 
+@pytest.mark.parametrize("J,D,pad", [(300, 128, 16), (517, 64, 4), (130, 96, 0)])
+def test_route_workspace_padded_heads(lib, J, D, pad):
+    """The workspace route (E on the tensor cores where the layout allows) with heads spaced
+    head_stride = J*D + pad apart and J not a multiple of 4 or of the 128-block tile: E within 1e-5 of
+    the oracle's, lists bit-exact except reported near ties."""
+    BH, k = 3, max(1, J // 7)
+    hs = J * D + pad
+    qflat = synthetic.normal((BH * hs,), 731 + J, device=DEV)
+    kflat = synthetic.normal((BH * hs,), 732 + J, device=DEV)
+    idx = torch.empty((BH, J, k), dtype=torch.int32, device=DEV)
+    num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
+    ws = torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV)
+    lib.bsa_route_topk(qflat, kflat, BH, J, D, hs, k, D ** -0.5, k, idx, num, ws)
+    torch.cuda.synchronize()
+    for bh in range(BH):
+        qb = f64(qflat[bh * hs:bh * hs + J * D].view(J, D))
+        kb = f64(kflat[bh * hs:bh * hs + J * D].view(J, D))
+        E = oracle.routing_scores(qb, kb, D)
+        Ews = ws[bh * J * J:(bh + 1) * J * J].view(J, J).double().cpu().numpy()
+        assert np.abs(Ews - E).max() <= 1e-5 * max(1.0, np.abs(E).max())
+        check_route(idx[bh].cpu().numpy(), num[bh].cpu().numpy(), E, k)
+
+
 # ---------------------------------------------------------------- device-side error reporting
 
 @pytest.mark.parametrize("J,starts,budgets", [(1500, [0, 300, 1500], [7, 40]), (700, [0, 1, 350, 700], [3, 9, 20])])
