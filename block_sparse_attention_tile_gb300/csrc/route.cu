@@ -10,8 +10,9 @@
 // operands (route_tc.cu) where the layout allows, else from the float32 FMA
 // contraction below; the fused path (no workspace) keeps E rows in shared
 // memory and uses FMAs.  The TopK is an exact radix select on order-preserving 32-bit
-// keys: one warp per row finds the k-th largest key bit by bit (32 counting
-// passes), then writes the selected ids in ascending order with ballots.
+// keys: one warp per row finds the k-th largest key bit by bit (counting
+// passes over the row until the k-th key's bucket holds at most 64 keys, then
+// over those alone), then writes the selected ids in ascending order with ballots.
 #include <algorithm>
 
 #include <cuda.h>
@@ -36,35 +37,91 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Capacity of a warp's candidate buffer in select_keys (two keys a lane).
+constexpr int kSelCap = 64;
+
 // TopK of J <= 32*KPL scores by one warp, the keys in registers (lane holds
 // columns lane + 32*i, i < KPL): exact radix select on order-preserving keys,
 // ties to the lower index, the selected ids (plus `first`) written ascending.
+// The bits of the k-th largest key are decided from the top.  After bit b the
+// key lies in the bucket [prefix, prefix + 2^b), n_lo keys are >= prefix (at
+// least k) and n_hi keys are >= prefix + 2^b (fewer than k).  Once the bucket
+// holds at most kSelCap keys (about ten bits into a row of scores), a warp with
+// many keys a lane gathers them into `cbuf` (kSelCap words of shared memory of
+// its own) and decides the remaining bits on those alone; the bucket count
+// n_hi then also gives the keys above the k-th without another pass.
 template <int KPL>
 __device__ __forceinline__ void select_keys(const float* __restrict__ e, int J, int k, int lane,
-                                            int32_t* __restrict__ out, int first) {
+                                            int32_t* __restrict__ out, int first, uint32_t* __restrict__ cbuf) {
+    constexpr bool kGather = KPL >= 8;
     uint32_t key[KPL];
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
         const int c = lane + 32 * i;
         key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
     }
+    const unsigned lt = (1u << lane) - 1u;
     uint32_t prefix = 0;
-    for (int bit = 31; bit >= 0; --bit) {
+    int n_lo = J, n_hi = 0;
+    int bit = 31;
+    for (; bit >= 0; --bit) {
         const uint32_t cand = prefix | (1u << bit);
         // independent counters: short add chains, and 64 registers a thread at KPL = 32
         int cn[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < KPL; ++i) cn[i & 3] += key[i] >= cand;
         const int cnt = __reduce_add_sync(0xffffffffu, (cn[0] + cn[1]) + (cn[2] + cn[3]));
-        if (cnt >= k) prefix = cand;
+        if (cnt >= k) {
+            prefix = cand;
+            n_lo = cnt;
+        } else {
+            n_hi = cnt;
+        }
+        if (kGather && bit > 0 && n_lo - n_hi <= kSelCap) break;
     }
-    int g[4] = {0, 0, 0, 0};
+    if (kGather && bit > 0) {
+        // the bucket's keys, in column order, and the count of keys above it
+        const uint32_t width = 1u << bit;
+        int base = 0;
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) g[i & 3] += key[i] > prefix;
-    const int n_gt = __reduce_add_sync(0xffffffffu, (g[0] + g[1]) + (g[2] + g[3]));
-    const int need_eq = k - n_gt;
-    int eq_seen = 0, written = 0;
-    const unsigned lt = (1u << lane) - 1u;
+        for (int i = 0; i < KPL; ++i) {
+            const bool inb = lane + 32 * i < J && key[i] - prefix < width;
+            const unsigned m = __ballot_sync(0xffffffffu, inb);
+            if (inb) cbuf[base + __popc(m & lt)] = key[i];
+            base += __popc(m);
+        }
+        __syncwarp();
+        const int n_top = n_hi;
+        const uint32_t c0 = lane < base ? cbuf[lane] : 0u;
+        const uint32_t c1 = lane + 32 < base ? cbuf[lane + 32] : 0u;
+        for (int b = bit - 1; b >= 0; --b) {
+            const uint32_t cand = prefix | (1u << b);
+            const int cnt = n_top + __reduce_add_sync(0xffffffffu, (int)(c0 >= cand) + (int)(c1 >= cand));
+            if (cnt >= k) {
+                prefix = cand;
+                n_lo = cnt;
+            } else {
+                n_hi = cnt;
+            }
+        }
+        __syncwarp();  // the buffer is reused by the warp's next row
+    }
+    // prefix is the k-th largest key: n_hi keys lie above it and n_lo - n_hi equal it
+    const int need_eq = k - n_hi;
+    int written = 0;
+    if (need_eq == n_lo - n_hi) {
+        // every key equal to the k-th is kept
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+            const int c = lane + 32 * i;
+            const bool sel = c < J && key[i] >= prefix;
+            const unsigned sel_mask = __ballot_sync(0xffffffffu, sel);
+            if (sel) out[written + __popc(sel_mask & lt)] = first + c;
+            written += __popc(sel_mask);
+        }
+        return;
+    }
+    int eq_seen = 0;
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
         const int c = lane + 32 * i;
@@ -83,17 +140,18 @@ __device__ __forceinline__ void select_keys(const float* __restrict__ e, int J, 
 // selected ids (plus `first`, the row segment's offset) written ascending and
 // -1 padded to kmax, and the count (when num_out is not null).  Rows of up to
 // 1024 scores keep their keys in registers, as many a lane as the row needs
-// (a short region of a grouped row does not pay for 32).
+// (a short region of a grouped row does not pay for 32); cbuf is the warp's
+// kSelCap words of shared memory.
 __device__ __forceinline__ void select_row(const float* __restrict__ e, int J, int k, int kmax, int lane,
                                            int32_t* __restrict__ out, int32_t* __restrict__ num_out,
-                                           int first = 0) {
+                                           uint32_t* __restrict__ cbuf, int first = 0) {
     if (J <= 1024) {
-        if (J <= 32) select_keys<1>(e, J, k, lane, out, first);
-        else if (J <= 64) select_keys<2>(e, J, k, lane, out, first);
-        else if (J <= 128) select_keys<4>(e, J, k, lane, out, first);
-        else if (J <= 256) select_keys<8>(e, J, k, lane, out, first);
-        else if (J <= 512) select_keys<16>(e, J, k, lane, out, first);
-        else select_keys<32>(e, J, k, lane, out, first);
+        if (J <= 32) select_keys<1>(e, J, k, lane, out, first, cbuf);
+        else if (J <= 64) select_keys<2>(e, J, k, lane, out, first, cbuf);
+        else if (J <= 128) select_keys<4>(e, J, k, lane, out, first, cbuf);
+        else if (J <= 256) select_keys<8>(e, J, k, lane, out, first, cbuf);
+        else if (J <= 512) select_keys<16>(e, J, k, lane, out, first, cbuf);
+        else select_keys<32>(e, J, k, lane, out, first, cbuf);
     } else {
         uint32_t prefix = 0;
         for (int bit = 31; bit >= 0; --bit) {
@@ -140,6 +198,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     float* qs = smem;                              // [kRouteRows][Dp]
     float* ks = qs + kRouteRows * Dp;              // [kRouteCols][Dp + 4]
     float* E = ks + kRouteCols * (Dp + 4);         // [kRouteRows][J]
+    uint32_t* cbuf = reinterpret_cast<uint32_t*>(E + kRouteRows * J);  // [8][kSelCap]
     const int bh = blockIdx.y;
     const int row0 = blockIdx.x * kRouteRows;
     const int nrows = min(kRouteRows, J - row0);
@@ -229,7 +288,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_topk_kernel(
     const int warp = tid / 32, lane = tid % 32;
     for (int rr = warp; rr < nrows; rr += kRouteThreads / 32)
         select_row(E + rr * J, J, k, kmax, lane, q2k_idx + ((long long)bh * J + row0 + rr) * kmax,
-                   q2k_num + (long long)bh * J + row0 + rr);
+                   q2k_num + (long long)bh * J + row0 + rr, cbuf + warp * kSelCap);
 }
 
 // ---------------------------------------------------------------- two-kernel path
@@ -351,9 +410,11 @@ __global__ void __launch_bounds__(256) route_select_kernel(const float* __restri
                                                            int32_t* __restrict__ q2k_num) {
     const int bh = blockIdx.y;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    __shared__ uint32_t cbuf[8][kSelCap];
     if (row >= J) return;
     select_row(E + ((long long)bh * J + row) * J, J, k, kmax, threadIdx.x & 31,
-               q2k_idx + ((long long)bh * J + row) * kmax, q2k_num + (long long)bh * J + row);
+               q2k_idx + ((long long)bh * J + row) * kmax, q2k_num + (long long)bh * J + row,
+               cbuf[threadIdx.x >> 5]);
 }
 
 // Region-grouped TopK ("VSA 实现详解" §5.3, the R2V exempt rule): the key
@@ -371,6 +432,7 @@ __global__ void __launch_bounds__(256) route_select_grouped_kernel(const float* 
                                                                    int kmax, int32_t* __restrict__ q2k_idx,
                                                                    int32_t* __restrict__ q2k_num) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), bh = blockIdx.y, lane = threadIdx.x & 31;
+    __shared__ uint32_t cbuf[8][kSelCap];
     if (row >= J) return;
     const float* e = E + ((long long)bh * J + row) * J;
     int32_t* out = q2k_idx + ((long long)bh * J + row) * kmax;
@@ -379,7 +441,7 @@ __global__ void __launch_bounds__(256) route_select_grouped_kernel(const float* 
         const int lo = rg.lo[r], size = rg.lo[r + 1] - lo;
         const int kk = min(rg.k[r], size);
         if (kk <= 0) continue;
-        select_row(e + lo, size, kk, kk, lane, out + written, nullptr, lo);
+        select_row(e + lo, size, kk, kk, lane, out + written, nullptr, cbuf[threadIdx.x >> 5], lo);
         written += kk;
     }
     for (int s = written + lane; s < kmax; s += 32) out[s] = -1;
@@ -435,7 +497,8 @@ extern "C" bsa_status bsa_route_topk(const float* qbar, const float* kbar, int B
     const int Dp = (D + 3) / 4 * 4;
     // the most rows per CTA whose E rows, query rows and key tile fit in shared memory
     auto smem_for = [&](int rows) {
-        return sizeof(float) * ((size_t)rows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)rows * J);
+        return sizeof(float) * ((size_t)rows * Dp + (size_t)kRouteCols * (Dp + 4) + (size_t)rows * J +
+                                (size_t)(kRouteThreads / 32) * kSelCap);
     };
     // and, where possible, at least two CTAs per SM (few blocks: fewer rows per CTA)
     static int sms = 0;
