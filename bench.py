@@ -434,6 +434,34 @@ def job_tflops(unit_flops, world, ms):
 
 # ---------------------------------------------------------------- workloads
 
+_MEMCPY2D = []
+
+
+def cuda_memcpy2d():
+    """cudaMemcpy2DAsync of the CUDA runtime this process has loaded (torch's),
+    through ctypes, or None.  A pitched copy moves one head slice of a
+    [B, T, heads, D] host tensor without staging it: torch's copy of a
+    non-contiguous pinned tensor first makes a contiguous pageable copy."""
+    if _MEMCPY2D:
+        return _MEMCPY2D[0]
+    import ctypes
+    fn = None
+    try:
+        paths = sorted({ln.split()[-1] for ln in open("/proc/self/maps") if "libcudart.so" in ln})
+        for path in paths:
+            lib = ctypes.CDLL(path)
+            if hasattr(lib, "cudaMemcpy2DAsync"):
+                fn = lib.cudaMemcpy2DAsync
+                fn.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_size_t,
+                               ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+                fn.restype = ctypes.c_int
+                break
+    except OSError:
+        fn = None
+    _MEMCPY2D.append(fn)
+    return fn
+
+
 class BlockWorkload:
     """Tile map -> pool -> route -> block attention (exact, or exact + summary)."""
 
@@ -762,6 +790,8 @@ class BlockWorkload:
             fin.record(d2h_s)
             comp.wait_event(fin)
 
+        self.e2e_pipelining = ("head chunks of %s heads on two compute streams: copies in and out overlap the "
+                               "compute of other heads" % "/".join(str(n) for n in sizes))
         return step, 1 + (self.launches_per_step - 1) * len(chunks)
 
     def algorithmic(self):
@@ -987,6 +1017,122 @@ class TokenWorkload:
 
     def run_with(self, dev_inputs):
         self.step(None, *dev_inputs)
+
+    def _kv_scratch(self, T, G, S, D):
+        """KV-outer scratch for one (batch, KV head): reverse index, partials."""
+        from block_sparse_attention_tile_gb300 import bsa, pipeline
+        torch, dev = self.torch, self.dev
+        nwin = pipeline.windows(T, self.window)
+        mc = bsa.bsa_max_chunks(1, T, 1, S, self.nblk, self.cap, self.window)
+        return {"max_chunks": mc,
+                "row_ptr": torch.empty((nwin * self.nblk + 1,), dtype=torch.int32, device=dev),
+                "q_idx": torch.empty((T * S,), dtype=torch.int32, device=dev),
+                "slot": torch.empty((T * S,), dtype=torch.int32, device=dev),
+                "chunks": torch.empty((mc, 4), dtype=torch.int32, device=dev),
+                "n_chunks": torch.empty((1,), dtype=torch.int32, device=dev),
+                "ws": torch.empty((max(16, bsa.bsa_reverse_index_workspace(1, T, 1, self.nblk)),), dtype=torch.uint8,
+                                  device=dev),
+                "obuf": torch.empty((1, T, G, S, D), dtype=torch.bfloat16, device=dev),
+                "lsebuf": torch.empty((1, T, G, S), dtype=torch.float32, device=dev)}
+
+    def make_e2e(self, h_in, d_in, h_out):
+        """End-to-end step with host buffers, pipelined by (batch, KV head): the
+        G query heads of one KV head and their selections are independent of the
+        others' in both orders, so each such chunk runs through the same public
+        calls with B = 1, HQ = G, H = 1.  K, V and the block lists (small) are
+        copied in whole first; each chunk's Q comes in by a pitched copy while
+        the chunk before it computes, and its output goes back by a pitched
+        copy into the host [B, T, HQ, D] tensor as soon as it is done.  Every
+        row's arithmetic is the same as in the whole-problem call (a row's scores,
+        softmax and products do not depend on which rows share its tile), so
+        the result is identical.  Falls back to copy-in / compute / copy-out when
+        the runtime's pitched copy cannot be found."""
+        torch = self.torch
+        memcpy2d = cuda_memcpy2d()
+        w = self.w
+        B, T, HQ, H, D, BS, S = (w[x] for x in ("B", "T", "HQ", "H", "D", "BS", "S"))
+        G = HQ // H
+        hq, hk, hv, hidx, hcnt = h_in
+        _, dk, dv, didx, dcnt = d_in
+        (hout,) = h_out
+        if memcpy2d is None or B * H < 2:
+            def plain():
+                for d, h in zip(d_in, h_in):
+                    d.copy_(h, non_blocking=True)
+                self.run_with(d_in)
+                hout.copy_(self.out, non_blocking=True)
+            return plain, self.launches_per_step
+        dev = self.dev
+        chunks = [(b, h) for b in range(B) for h in range(H)]
+        qc = [torch.empty((1, T, G, D), dtype=torch.bfloat16, device=dev) for _ in chunks]
+        oc = [torch.empty((1, T, G, D), dtype=torch.bfloat16, device=dev) for _ in chunks]
+        lc = [torch.empty((1, T, G), dtype=torch.float32, device=dev) for _ in chunks]
+        kc, vc, ic, cc = ([torch.empty(shape, dtype=dt, device=dev) for _ in range(2)]
+                          for shape, dt in (((1, T, 1, D), torch.bfloat16), ((1, T, 1, D), torch.bfloat16),
+                                            ((1, T, 1, S), torch.int32), ((1, T, 1), torch.int32)))
+        scratch = [self._kv_scratch(T, G, S, D) for _ in range(2)] if self.order != "qouter" else None
+        comp = torch.cuda.current_stream()
+        comps = [comp, torch.cuda.Stream()]
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        row_b = G * D * 2                       # one position's G heads, bf16
+        esz = hq.element_size()
+
+        def check(rc):
+            if rc != 0:
+                raise RuntimeError("cudaMemcpy2DAsync failed (%d)" % rc)
+
+        def step():
+            from block_sparse_attention_tile_gb300 import bsa
+            start = torch.cuda.Event()
+            start.record(comp)
+            h2d_s.wait_event(start)
+            ready = []
+            with torch.cuda.stream(h2d_s):
+                for d, h in ((dk, hk), (dv, hv), (didx, hidx), (dcnt, hcnt)):
+                    d.copy_(h, non_blocking=True)
+                for c, (b, h) in enumerate(chunks):
+                    src = hq.data_ptr() + ((b * T) * HQ + h * G) * D * esz
+                    check(memcpy2d(qc[c].data_ptr(), row_b, src, HQ * D * esz, row_b, T, 1, h2d_s.cuda_stream))
+                    e = torch.cuda.Event()
+                    e.record(h2d_s)
+                    ready.append(e)
+            for c, (b, h) in enumerate(chunks):
+                i = c % 2
+                cs = comps[i]
+                cs.wait_event(ready[c])
+                with torch.cuda.stream(cs):
+                    kc[i].copy_(dk[b:b + 1, :, h:h + 1])
+                    vc[i].copy_(dv[b:b + 1, :, h:h + 1])
+                    ic[i].copy_(didx[b:b + 1, :, h:h + 1])
+                    cc[i].copy_(dcnt[b:b + 1, :, h:h + 1])
+                    if self.order == "qouter":
+                        bsa.bsa_fwd_qouter_tokens(qc[c], kc[i], vc[i], 1, T, G, 1, D, ic[i], cc[i], S, BS, True,
+                                                  self.scale, oc[c], lc[c])
+                    else:
+                        sc = scratch[i]
+                        bsa.bsa_build_reverse_index(ic[i], cc[i], 1, T, 1, S, self.nblk, self.cap, sc["row_ptr"],
+                                                    sc["q_idx"], sc["slot"], sc["chunks"], sc["n_chunks"],
+                                                    sc["max_chunks"], sc["ws"], window=self.window)
+                        bsa.bsa_fwd_kvouter(qc[c], kc[i], vc[i], 1, T, G, 1, D, sc["row_ptr"], sc["q_idx"], sc["slot"],
+                                            sc["chunks"], sc["n_chunks"], sc["max_chunks"], self.nblk, BS, S, True,
+                                            self.scale, sc["obuf"], sc["lsebuf"], window=self.window)
+                        bsa.bsa_combine(sc["obuf"], sc["lsebuf"], cc[i], 1, T, G, 1, S, D, oc[c], lc[c])
+                    done = torch.cuda.Event()
+                    done.record(cs)
+                d2h_s.wait_event(done)
+                dst = hout.data_ptr() + ((b * T) * HQ + h * G) * D * esz
+                check(memcpy2d(dst, HQ * D * esz, oc[c].data_ptr(), row_b, row_b, T, 2, d2h_s.cuda_stream))
+                # the next chunk on this stream reuses the small buffers only after
+                # this chunk's kernels have read them (same stream: ordered)
+            fin = torch.cuda.Event()
+            fin.record(d2h_s)
+            comp.wait_event(fin)
+            comps[1].wait_event(fin)
+
+        self.e2e_pipelining = ("(batch, KV head) chunks on two compute streams: each chunk's Q in and output out "
+                               "by pitched copies that overlap the compute of other chunks; K, V and the block "
+                               "lists copied in whole first")
+        return step, self.launches_per_step * len(chunks)
 
     def algorithmic(self):
         """Visible (query head, key) pairs (causal) x 4*D FLOPs; nnz entries; bytes of the
@@ -1288,9 +1434,7 @@ def gpu_arm(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "steps_timed": e2e_steps, "aggregate": "median of per-step times",
                     "ms_per_step_mean": e2e_mean, "ms_per_step_max": e2e_max,
-                    "pipelining": ("head chunks on two compute streams: copies in and out overlap the compute "
-                                   "of other heads"
-                                   if hasattr(wl, "make_e2e") else "none: copy in, compute, copy out"),
+                    "pipelining": getattr(wl, "e2e_pipelining", "none: copy in, compute, copy out"),
                     "gpu_launches_per_step": e2e_launches, "matches_device_run": e2e_match},
             "gpu_launches": wl.launches_per_step * args.steps,
             "clocks": clk,
