@@ -632,7 +632,8 @@ class BlockWorkload:
         if ev: ev[o + 3].record(st)
         if self.reweight:
             bsa.bsa_reweight_summaries(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, self.scale,
-                                       self.kbar_lp, self.vbar_lp, self.sbias, self.rw_ws, qbar=self.qbar)
+                                       self.kbar_lp, self.vbar_lp, self.sbias, self.rw_ws, qbar=self.qbar,
+                                       packed=self.packed)
             if ev: ev[o + 4].record(st)
         if self.summary:
             bsa.bsa_fwd_summary(q, k, v, self.BH, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
@@ -680,7 +681,7 @@ class BlockWorkload:
             sb = self.sbias[sl]
             bsa.bsa_reweight_summaries(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P,
                                        self.scale, self.kbar_lp[sl], self.vbar_lp[sl], sb, self.rw_ws,
-                                       qbar=self.qbar[sl])
+                                       qbar=self.qbar[sl], packed=packed_chunk)
         if self.summary:
             bsa.bsa_fwd_summary(q[sl], k[sl], v[sl], nh, self.N, D, self.im, self.bs, self.J, M, self.P, g.geometry,
                                 self.q2k[sl], self.q2n[sl], kk, self.kbar_lp[sl], self.vbar_lp[sl], self.scale,

@@ -60,7 +60,7 @@ _SIGS = {
     "bsa_combine": (I, [P, I, P, P, I, I, I, I, I, I, P, I, P, P]),
     "bsa_fwd_summary": (I, [P, P, P, I, I, I, I, P, P, I, I, I, P, P, P, P, I, P, P, P, F, P, P, P]),
     "bsa_reweight_workspace": (SZ, [I, I]),
-    "bsa_reweight_summaries": (I, [P, P, P, P, I, I, I, I, P, P, I, I, I, F, P, P, P, P, P, SZ, P]),
+    "bsa_reweight_summaries": (I, [P, P, P, P, I, I, I, I, P, P, I, I, I, F, P, P, P, P, P, SZ, P, P]),
     "bsa_segments_count": (I, [I, P, P, I, I, I, I, P, P]),
     "bsa_tile_map_segments": (I, [I, P, P, I, I, I, I, P, P, P]),
     "bsa_route_topk_grouped": (I, [P, P, I, I, I, I64, I, P, P, F, I, P, P, P, SZ, P]),
@@ -177,11 +177,12 @@ def bsa_reweight_workspace(BH, D):
 
 
 def bsa_reweight_summaries(q, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, scale, kt_lp, vt_lp,
-                           bias, workspace, anchor=None, qbar=None, stream=None):
+                           bias, workspace, anchor=None, qbar=None, packed=None, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check(_lib.bsa_reweight_summaries(_ptr(q), _ptr(qbar), _ptr(k), _ptr(v), _dtype(k), BH, N, D, _ptr(index_map),
                                        _ptr(block_sizes), J, M, prefix_blocks, scale, _ptr(kt_lp), _ptr(vt_lp),
-                                       _ptr(bias), _ptr(anchor), _ptr(workspace), nbytes, _stream(stream)))
+                                       _ptr(bias), _ptr(anchor), _ptr(workspace), nbytes, _ptr(packed),
+                                       _stream(stream)))
 
 
 def bsa_fwd_qouter_tokens(q, k, v, B, T, HQ, H, D, block_indices, block_counts, S, block_size, causal,

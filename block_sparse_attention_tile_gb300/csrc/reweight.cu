@@ -25,6 +25,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(kRwAnchorThreads) reweight_anchor_kernel(
     constexpr int kWarps = kRwAnchorThreads / 32;
     constexpr int G = kRwGroup<T, DPL>;
     __shared__ float red[kWarps][256];
+    __shared__ int cred[kWarps];
     const int split = blockIdx.x, bh = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Jr = J - P;
@@ -131,9 +133,11 @@ __global__ void __launch_bounds__(kRwAnchorThreads) reweight_anchor_kernel(
     float acc[DPL];
 #pragma unroll
     for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    int cnt = 0;  // member rows taken (a row with an index outside [0, N) is left out of sum and count)
     for (int j = j0 + warp; j < j1; j += kWarps) {
         const int n = min(max(block_sizes[j], 0), M);
         if (qbar) {
+            cnt += n;
             const float* row = qbar + ((long long)bh * J + j) * D;
 #pragma unroll
             for (int i = 0; i < DPL; ++i)
@@ -145,6 +149,7 @@ __global__ void __launch_bounds__(kRwAnchorThreads) reweight_anchor_kernel(
         for (int b0 = 0; b0 < n; b0 += 32) {
             const int tl = lane_token(im, b0, n, N, lane, status);
             const int nb = min(32, n - b0);
+            cnt += __popc(__ballot_sync(0xffffffffu, lane < nb && tl >= 0));
             for (int g0 = 0; g0 < nb; g0 += G) {
                 LaneRaw<T, DPL> x[G];
                 float w[G];
@@ -165,6 +170,7 @@ __global__ void __launch_bounds__(kRwAnchorThreads) reweight_anchor_kernel(
 #pragma unroll
     for (int i = 0; i < DPL; ++i)
         if (lane * DPL + i < D) red[warp][lane * DPL + i] = acc[i];
+    if (lane == 0) cred[warp] = cnt;
     __syncthreads();
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
         float t = 0.f;
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kRwAnchorThreads) reweight_anchor_kernel(
     }
     if (threadIdx.x == 0) {
         int count = 0;
-        for (int j = j0; j < j1; ++j) count += min(max(block_sizes[j], 0), M);
+        for (int w = 0; w < kWarps; ++w) count += cred[w];
         part_count[bh * kRwSplits + split] = count;
     }
 }
@@ -530,6 +536,167 @@ __global__ void __launch_bounds__(kRwStagedThreads) reweight_block_staged_kernel
     if (tid == 0) bias[(long long)bh * J + j] = z > 0.f ? (mx + logf(z)) - a_dot_k * scale : -CUDART_INF_F;
 }
 
+// ---------------------------------------------------------------- from the packed copy
+// With the block-ordered copy that bsa_pool_blocks writes (row (j, m) = token
+// index_map[j*M + m]), a block's member rows of K and of V are each one
+// contiguous run of n_j rows, so one bulk copy per tensor brings a whole
+// block into shared memory: no per-row copy instructions.  One CTA of 8 warps
+// per (routed block, head), three CTAs per SM, so one CTA's copy lands while
+// the others compute:
+//   logits  two threads per row, 64 channels each, reading the row's 16-byte
+//           chunks in an order rotated by the row (the rows are 256 bytes
+//           apart, so a plain order would put a warp's reads in one bank);
+//   softmax over the block's rows at once (n_j <= 128);
+//   sums    thread (tensor, chunk, row group) accumulates its 8 channels over
+//           every eighth row, the groups added in a fixed order.
+// bf16, D = 128, M <= 128.  The wait for the copy is bounded; on expiry the
+// CTA raises BSA_ERR_TIMEOUT, waits (bounded) for the copy and returns.
+constexpr int kRpThreads = 256;
+constexpr int kRpD = 128;
+constexpr int kRpRow = kRpD * 2;  // bytes of a bf16 row
+constexpr uint64_t kRpWaitNs = 2000000000ull;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__global__ void __launch_bounds__(kRpThreads, 3) reweight_packed_kernel(
+    const __nv_bfloat16* __restrict__ pk, const __nv_bfloat16* __restrict__ pv, int N,
+    const int32_t* __restrict__ index_map, const int32_t* __restrict__ block_sizes, int J, int M, int P,
+    float scale, const float* __restrict__ a_ws, __nv_bfloat16* __restrict__ kt_lp,
+    __nv_bfloat16* __restrict__ vt_lp, float* __restrict__ bias, int* status) {
+    extern __shared__ __align__(128) unsigned char rp_smem[];
+    unsigned char* Kb = rp_smem;                                        // [M][256 B]
+    unsigned char* Vb = Kb + (size_t)M * kRpRow;                        // [M][256 B]
+    float* as = reinterpret_cast<float*>(Vb + (size_t)M * kRpRow);      // [128] the anchor
+    float* ps = as + kRpD;                                              // [128] weights
+    float* part = ps + 128;                                             // [2][4][128] row-group sums
+    float* red = part + 2 * 4 * kRpD;                                   // [8]
+    uint64_t* fbar = reinterpret_cast<uint64_t*>(red + 8);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j = P + blockIdx.x, bh = blockIdx.y;
+    const int n = min(max(block_sizes[j], 0), M);
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(fbar);
+    const uint32_t bytes = (uint32_t)n * kRpRow;
+    if (tid == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+        const long long off = ((long long)bh * J + j) * M * kRpD;
+        ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
+        if (bytes) {
+            bulk_g2s((uint32_t)__cvta_generic_to_shared(Kb), pk + off, bytes, bar);
+            bulk_g2s((uint32_t)__cvta_generic_to_shared(Vb), pv + off, bytes, bar);
+        }
+    }
+    // while the rows land: the anchor, and whether this thread's row takes part
+    // (an index outside [0, N) is skipped)
+    if (tid < kRpD / 4)
+        reinterpret_cast<float4*>(as)[tid] = reinterpret_cast<const float4*>(a_ws + (long long)bh * kRpD)[tid];
+    const int lr = tid >> 1, lh = tid & 1;
+    bool live = false;
+    if (lr < n) {
+        const int tok = index_map[(long long)j * M + lr];
+        live = tok >= 0 && tok < N;
+        if (!live && lh == 0) raise_status(status, BSA_ERR_INDEX);
+    }
+    __syncthreads();  // the barrier's initialisation and the anchor are visible
+    bool ok = ptx::mbar_try_wait(bar, 0);
+    if (!ok) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!(ok = ptx::mbar_try_wait(bar, 0)) && ptx::globaltimer() - t0 < kRpWaitNs) {
+        }
+        if (!ok && tid == 0) raise_status(status, BSA_ERR_TIMEOUT);
+    }
+    // every thread waited on its own; the copy either landed for all or the CTA leaves,
+    // after a second bounded wait for the copy still in flight into its shared memory
+    if (!__syncthreads_and(ok)) {
+        if (tid == 0) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(bar, 0) && ptx::globaltimer() - t0 < kRpWaitNs) {
+            }
+        }
+        return;
+    }
+    // ---- logits: channels [64 lh, 64 lh + 64) of row lr, four independent partial sums
+    float2 t2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) t2[u] = make_float2(0.f, 0.f);
+    if (live) {
+        const unsigned char* row = Kb + (size_t)lr * kRpRow + lh * 128;
+        const float* ah = as + lh * 64;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int cr = (c + lr) & 7;
+            const uint4 w = *reinterpret_cast<const uint4*>(row + cr * 16);
+            const float4 a0 = reinterpret_cast<const float4*>(ah + cr * 8)[0];
+            const float4 a1 = reinterpret_cast<const float4*>(ah + cr * 8)[1];
+            t2[0] = ptx::ffma2(make_float2(a0.x, a0.y), bf2_to_f2(w.x), t2[0]);
+            t2[1] = ptx::ffma2(make_float2(a0.z, a0.w), bf2_to_f2(w.y), t2[1]);
+            t2[2] = ptx::ffma2(make_float2(a1.x, a1.y), bf2_to_f2(w.z), t2[2]);
+            t2[3] = ptx::ffma2(make_float2(a1.z, a1.w), bf2_to_f2(w.w), t2[3]);
+        }
+    }
+    float lg = ((t2[0].x + t2[0].y) + (t2[1].x + t2[1].y)) + ((t2[2].x + t2[2].y) + (t2[3].x + t2[3].y));
+    lg += __shfl_xor_sync(0xffffffffu, lg, 1);
+    lg = live ? lg * scale : -CUDART_INF_F;
+    // ---- softmax over the block's rows
+    float mx = warp_max(lg);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kRpThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    const float e = (lh == 0 && mx != -CUDART_INF_F) ? expf(lg - mx) : 0.f;  // 0 for dead rows
+    if (lh == 0) ps[lr] = e;
+    const float z = block_sum(e, red);  // (its barriers also publish ps)
+    // ---- weighted sums: channels [8 cc, 8 cc + 8) of tensor st over rows rg, rg + 8, ...
+    const int st = warp >> 2, rg = (warp & 3) * 2 + (lane >> 4), cc = lane & 15;
+    float2 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = make_float2(0.f, 0.f);
+    const unsigned char* tb = (st ? Vb : Kb) + cc * 16;
+#pragma unroll 4
+    for (int r = rg; r < n; r += 8) {
+        const float p = ps[r];
+        const float2 p2 = make_float2(p, p);
+        const uint4 w = *reinterpret_cast<const uint4*>(tb + (size_t)r * kRpRow);
+        acc[0] = ptx::ffma2(p2, bf2_to_f2(w.x), acc[0]);
+        acc[1] = ptx::ffma2(p2, bf2_to_f2(w.y), acc[1]);
+        acc[2] = ptx::ffma2(p2, bf2_to_f2(w.z), acc[2]);
+        acc[3] = ptx::ffma2(p2, bf2_to_f2(w.w), acc[3]);
+    }
+    // the two row groups of a warp, then the warps' four, in a fixed order
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc[q].x += __shfl_xor_sync(0xffffffffu, acc[q].x, 16);
+        acc[q].y += __shfl_xor_sync(0xffffffffu, acc[q].y, 16);
+    }
+    if (lane < 16) {
+        float4* dst = reinterpret_cast<float4*>(part + (st * 4 + (warp & 3)) * kRpD + cc * 8);
+        dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+    __syncthreads();
+    const int ot = tid >> 7, d = tid & 127;
+    const float* pp = part + ot * 4 * kRpD + d;
+    const float sum = ((pp[0] + pp[kRpD]) + pp[2 * kRpD]) + pp[3 * kRpD];
+    const __nv_bfloat16 stv = __float2bfloat16_rn(z > 0.f ? sum / z : 0.f);
+    (ot ? vt_lp : kt_lp)[((long long)bh * J + j) * kRpD + d] = stv;
+    // a . k~ with the key as stored (threads 0..127); the V half adds zeros
+    const float ak = block_sum(ot ? 0.f : as[d] * __bfloat162float(stv), red);
+    if (tid == 0) bias[(long long)bh * J + j] = z > 0.f ? (mx + logf(z)) - ak * scale : -CUDART_INF_F;
+}
+
+static size_t reweight_packed_smem(int M) {
+    return (size_t)2 * M * kRpRow + (kRpD + 128 + 2 * 4 * kRpD + 8) * sizeof(float) + sizeof(uint64_t);
+}
+
 struct RwWorkspace {
     float* part;
     int* part_count;
@@ -547,7 +714,8 @@ static RwWorkspace carve(void* ws, int BH, int D) {
 template <typename T, int DPL>
 static bsa_status launch_reweight(const void* q, const float* qbar, const void* k, const void* v, int BH, int N, int D,
                                   const int32_t* im, const int32_t* bs, int J, int M, int P, float scale,
-                                  void* kt, void* vt, float* bias, float* anchor, void* ws, cudaStream_t st) {
+                                  void* kt, void* vt, float* bias, float* anchor, void* ws, const void* packed,
+                                  cudaStream_t st) {
     const RwWorkspace w = carve(ws, BH, D);
     auto aligned = [&](const void* p) {
         return D % DPL == 0 && ((uintptr_t)p % (DPL * sizeof(T))) == 0;
@@ -563,6 +731,20 @@ static bsa_status launch_reweight(const void* q, const float* qbar, const void* 
     reweight_mean_kernel<<<BH, 256, 0, st>>>(w.part, w.part_count, D, w.anchor, anchor);
     rc = check_launch("reweight_mean_kernel");
     if (rc != BSA_OK) return rc;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        if (packed && D == kRpD && M <= 128 && ((uintptr_t)packed & 15) == 0) {
+            const size_t smem = reweight_packed_smem(M);
+            cudaError_t e = cudaFuncSetAttribute(reweight_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "reweight packed attribute: %s", cudaGetErrorString(e));
+            const long long per = (long long)BH * J * M * D;  // elements of one tensor's packed copy
+            const __nv_bfloat16* pb = static_cast<const __nv_bfloat16*>(packed);
+            reweight_packed_kernel<<<dim3(J - P, BH), kRpThreads, smem, st>>>(
+                pb + per, pb + 2 * per, N, im, bs, J, M, P, scale, w.anchor, (__nv_bfloat16*)kt, (__nv_bfloat16*)vt,
+                bias, status_word());
+            return check_launch("reweight_packed_kernel");
+        }
+    }
     const int row_bytes = D * (int)sizeof(T);
     const int LPR = row_bytes / 16;
     const bool staged = row_bytes % 16 == 0 && LPR <= 32 && (LPR & (LPR - 1)) == 0 && ((uintptr_t)k & 15) == 0 &&
@@ -599,11 +781,12 @@ template <typename T>
 static bsa_status dispatch_reweight(const void* q, const float* qbar, const void* k, const void* v, int BH, int N,
                                     int D,
                                     const int32_t* im, const int32_t* bs, int J, int M, int P, float scale,
-                                    void* kt, void* vt, float* bias, float* anchor, void* ws, cudaStream_t st) {
-    if (D <= 32) return launch_reweight<T, 1>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, st);
-    if (D <= 64) return launch_reweight<T, 2>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, st);
-    if (D <= 128) return launch_reweight<T, 4>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, st);
-    return launch_reweight<T, 8>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, st);
+                                    void* kt, void* vt, float* bias, float* anchor, void* ws, const void* pk,
+                                    cudaStream_t st) {
+    if (D <= 32) return launch_reweight<T, 1>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, pk, st);
+    if (D <= 64) return launch_reweight<T, 2>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, pk, st);
+    if (D <= 128) return launch_reweight<T, 4>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, pk, st);
+    return launch_reweight<T, 8>(q, qbar, k, v, BH, N, D, im, bs, J, M, P, scale, kt, vt, bias, anchor, ws, pk, st);
 }
 
 }  // namespace bsa
@@ -621,7 +804,8 @@ bsa_status bsa_reweight_summaries(const void* q, const float* qbar, const void* 
                                   int BH, int N,
                                   int D, const int32_t* index_map, const int32_t* block_sizes, int J, int M,
                                   int prefix_blocks, float scale, void* kt_lp, void* vt_lp, float* bias,
-                                  float* anchor, void* workspace, size_t workspace_bytes, void* stream) {
+                                  float* anchor, void* workspace, size_t workspace_bytes, const void* packed,
+                                  void* stream) {
     BSA_REQUIRE((q || qbar) && k && v && index_map && block_sizes && kt_lp && vt_lp && bias && workspace,
                 "reweight: null pointer");
     BSA_REQUIRE(dtype == BSA_F32 || dtype == BSA_BF16, "reweight: dtype");
@@ -635,9 +819,9 @@ bsa_status bsa_reweight_summaries(const void* q, const float* qbar, const void* 
     cudaStream_t st = as_stream(stream);
     if (dtype == BSA_F32)
         return dispatch_reweight<float>(q, qbar, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, scale, kt_lp,
-                                        vt_lp, bias, anchor, workspace, st);
+                                        vt_lp, bias, anchor, workspace, packed, st);
     return dispatch_reweight<__nv_bfloat16>(q, qbar, k, v, BH, N, D, index_map, block_sizes, J, M, prefix_blocks, scale,
-                                            kt_lp, vt_lp, bias, anchor, workspace, st);
+                                            kt_lp, vt_lp, bias, anchor, workspace, packed, st);
 }
 
 }  // extern "C"

@@ -173,7 +173,7 @@ def block_sparse_attention(q, k, v, geom, topk, scale=None, kmax=None, summary=F
         sbias = torch.empty((BH, J), dtype=torch.float32, device=dev)
         rws = torch.empty((bsa.bsa_reweight_workspace(BH, D) // 4,), dtype=torch.float32, device=dev)
         bsa.bsa_reweight_summaries(q, k, v, BH, N, D, index_map, block_sizes, J, geom.M, P, scale, kbar_lp, vbar_lp,
-                                   sbias, rws, qbar=qbar)
+                                   sbias, rws, qbar=qbar, packed=pk)
     out = torch.empty_like(q)
     lse = torch.empty((BH, N), dtype=torch.float32, device=dev) if need_lse else None
     if summary:

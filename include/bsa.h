@@ -377,6 +377,13 @@ bsa_status bsa_fwd_summary(const void* q, const void* k, const void* v, bsa_dtyp
  * not written): kt_lp, vt_lp [device] [BH, J, D] of `dtype`; bias [device]
  * float [BH, J]; anchor [device] float [BH, D] or NULL.  workspace: [device]
  * bsa_reweight_workspace(BH, D) bytes, 16-byte aligned, caller-owned.
+ * packed: [device] the block-ordered copy written by bsa_pool_blocks from the
+ * same q, k, v and index_map ([3, BH, J, M, D] of `dtype`), or NULL.  With it,
+ * bf16 with D = 128 and M <= 128 reads each block's member rows of K and V as
+ * one contiguous run (one bulk copy per tensor, a persistent grid keeping the
+ * next blocks' copies in flight); otherwise the rows are gathered through
+ * index_map.  Both give the definition's values to float32 accuracy (their
+ * sums run in different fixed orders, so the last bits may differ).
  * Deterministic: every sum runs in a fixed order.  1 <= D <= 256; a member
  * index outside [0, N) raises BSA_ERR_INDEX and the row is skipped. */
 size_t bsa_reweight_workspace(int BH, int D);
@@ -386,7 +393,7 @@ bsa_status bsa_reweight_summaries(const void* q, const float* qbar, const void* 
                                   const int32_t* block_sizes, int J, int M, int prefix_blocks,
                                   float scale, void* kt_lp, void* vt_lp, float* bias,
                                   float* anchor, void* workspace, size_t workspace_bytes,
-                                  void* stream);
+                                  const void* packed, void* stream);
 
 /* ------------------------------------------------------------------ a10 ---
  * Coarse branch.  [VSA] §6.7: every routed query block i attends at block

@@ -92,15 +92,18 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     rc = lib.bsa_build_reverse_index(1, 1, 1, 4096, 1, 2, 4, 8, 300, 1, 1, 1, 1, 1, 10 ** 6, 1, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "window" in bsa.bsa_last_error()  # not a multiple of 256
     # reweight: null q, then a workspace one int short of 2 heads x (32 splits x (8 floats + 1 int) + 8 floats)
-    rc = lib.bsa_reweight_summaries(None, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1, None)
+    rc = lib.bsa_reweight_summaries(None, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1, None,
+                                    None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()
     assert bsa.bsa_reweight_workspace(2, 8) == 2 * 32 * (8 * 4 + 4) + 2 * 8 * 4
     rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16,
-                                    bsa.bsa_reweight_workspace(2, 8) - 4, None)
+                                    bsa.bsa_reweight_workspace(2, 8) - 4, None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "workspace" in bsa.bsa_last_error()
-    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 4, 0.5, 1, 1, 1, None, 16, 1 << 20, None)
+    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 8, 1, 1, 4, 16, 4, 0.5, 1, 1, 1, None, 16, 1 << 20, None,
+                                    None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "block counts" in bsa.bsa_last_error()  # no routed block
-    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 300, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1 << 20, None)
+    rc = lib.bsa_reweight_summaries(1, None, 1, 1, 1, 2, 64, 300, 1, 1, 4, 16, 1, 0.5, 1, 1, 1, None, 16, 1 << 20,
+                                    None, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "sizes" in bsa.bsa_last_error()  # D > 256
     rc = lib.bsa_coarse_attention(None, 16, 1, 8, 1, 4, 2, 1, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "null" in bsa.bsa_last_error()

@@ -431,7 +431,8 @@ def test_coarse_branch_prefix_ragged_fp32(lib):
 
 # ---------------------------------------------------------------- a9 Spark-Reweight summaries
 
-def _reweight_case(lib, h, n_prefix, grid, block, M, D, dtype, seed, permuted, from_means=False):
+def _reweight_case(lib, h, n_prefix, grid, block, M, D, dtype, seed, permuted, from_means=False, packed=False,
+                   bad_index=None):
     pl = _pipeline()
     T, H, W = grid
     q, kk, v = synthetic.cluster_qkv(h, n_prefix, T * H * W, D, seed, dtype)
@@ -446,14 +447,32 @@ def _reweight_case(lib, h, n_prefix, grid, block, M, D, dtype, seed, permuted, f
     bias = torch.full((h, J), 7.0, dtype=torch.float32, device=DEV)
     anchor = torch.empty((h, D), dtype=torch.float32, device=DEV)
     ws = torch.empty((lib.bsa_reweight_workspace(h, D) // 4,), dtype=torch.float32, device=DEV)
-    qbar = None
-    if from_means:
+    qbar, pk = None, None
+    if from_means or packed:
         qbar = torch.empty((h, J, D), dtype=torch.float32, device=DEV)
-        lib.bsa_pool_blocks(q.to(DEV), kk.to(DEV), None, h, N, D, im, bs, J, M, qbar, torch.empty_like(qbar))
-    lib.bsa_reweight_summaries(None if from_means else q.to(DEV), kk.to(DEV), v.to(DEV), h, N, D, im, bs, J, M, P,
-                               scale, kt, vt, bias, ws, anchor=anchor, qbar=qbar)
+        if packed:
+            # the block-ordered copy of Q, K and V that the pool pass writes
+            pk = torch.empty((3, h, J, M, D), dtype=dtype, device=DEV)
+            lib.bsa_pool_blocks(q.to(DEV), kk.to(DEV), v.to(DEV), h, N, D, im, bs, J, M, qbar, torch.empty_like(qbar),
+                                torch.empty_like(qbar), packed=pk)
+        else:
+            lib.bsa_pool_blocks(q.to(DEV), kk.to(DEV), None, h, N, D, im, bs, J, M, qbar, torch.empty_like(qbar))
+    if not from_means:
+        qbar = None
+    im_call = im
+    if bad_index is not None:
+        # one member index out of range: that row is left out and BSA_ERR_INDEX latched
+        im_call = im.clone()
+        im_call.view(-1)[bad_index] = N + 5
+    assert lib.bsa_device_status() == lib.BSA_OK
+    lib.bsa_reweight_summaries(None if from_means else q.to(DEV), kk.to(DEV), v.to(DEV), h, N, D, im_call, bs, J, M,
+                               P, scale, kt, vt, bias, ws, anchor=anchor, qbar=qbar, packed=pk)
     torch.cuda.synchronize()
+    assert lib.bsa_device_status() == (lib.BSA_OK if bad_index is None else lib.BSA_ERR_INDEX)
     blocks = oracle_blocks(T, H, W, *block, M, n_prefix, perm)
+    if bad_index is not None:
+        jb, mb = divmod(bad_index, M)
+        blocks[jb] = np.delete(np.asarray(blocks[jb]), mb)
     rk = oracle.bf16_round if dtype == torch.bfloat16 else None
     # stored rows: half an ulp of the storage type plus the float32 sums
     rel = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -20
@@ -493,6 +512,22 @@ def test_reweight_summaries_ragged_windows_fp32(lib, D, from_means):
     # half the lanes idle, D=33 takes the scalar loads (odd rows), D=200 eight channels a lane,
     # D=256 float32 rows too wide to double-buffer in shared memory (register path)
     _reweight_case(lib, 3, 20, (5, 3, 4), (2, 2, 3), 12, D, torch.float32, 17, False, from_means)
+
+
+@pytest.mark.parametrize("from_means", [False, True])
+def test_reweight_summaries_packed_bf16(lib, from_means):
+    # the packed-copy path (one bulk copy per block and tensor, a persistent grid): 256 text tokens
+    # (2 prefix blocks) + a permuted (4,32,64) grid, 64 routed blocks x 8 heads = 512 items, so every
+    # CTA walks three or four of them through its three-stage ring; against the oracle
+    _reweight_case(lib, 8, 256, (4, 32, 64), (1, 1, 1), 128, 128, torch.bfloat16, 607, True, from_means,
+                   packed=True)
+
+
+def test_reweight_summaries_packed_ragged_bad_index(lib):
+    # ragged blocks on the packed path ((3,5,40) in (3,4,8) windows, M=96: the last row of windows
+    # holds 24 tokens), and one member index of block 5 out of range: that row is skipped
+    _reweight_case(lib, 2, 0, (3, 5, 40), (3, 4, 8), 96, 128, torch.bfloat16, 608, False, packed=True,
+                   bad_index=5 * 96 + 7)
 
 
 def test_reweight_summaries_large_blocks_bf16(lib):
