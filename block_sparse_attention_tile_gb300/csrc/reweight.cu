@@ -21,7 +21,10 @@
 //   reweight_block_kernel    per (head, routed block): each warp an online
 //                            softmax over its rows at a (running max, mass,
 //                            weighted key and value sums), the warps merged
-//                            in order, then k~, v~ and b.
+//                            in order, then k~, v~ and b (the staged variant
+//                            copies the member rows to shared memory first;
+//                            reweight_packed_kernel reads them from the
+//                            block-ordered packed copy, one bulk copy each).
 #include <math_constants.h>
 
 #include <algorithm>
@@ -578,22 +581,45 @@ __global__ void __launch_bounds__(kRpThreads, 3) reweight_packed_kernel(
     float* ps = as + kRpD;                                              // [128] weights
     float* part = ps + 128;                                             // [2][4][128] row-group sums
     float* red = part + 2 * 4 * kRpD;                                   // [8]
-    uint64_t* fbar = reinterpret_cast<uint64_t*>(red + 8);
+    uint64_t* fbar = reinterpret_cast<uint64_t*>(red + 8);  // [2]: K rows, V rows
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int j = P + blockIdx.x, bh = blockIdx.y;
     const int n = min(max(block_sizes[j], 0), M);
-    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(fbar);
+    const uint32_t kbar = (uint32_t)__cvta_generic_to_shared(fbar), vbar = kbar + 8;
     const uint32_t bytes = (uint32_t)n * kRpRow;
     if (tid == 0) {
-        ptx::mbar_init(bar, 1);
+        ptx::mbar_init(kbar, 1);
+        ptx::mbar_init(vbar, 1);
         ptx::fence_mbar_init();
         const long long off = ((long long)bh * J + j) * M * kRpD;
-        ptx::mbar_arrive_expect_tx(bar, 2 * bytes);
+        // K and V on barriers of their own: the logits and the softmax need only K
+        ptx::mbar_arrive_expect_tx(kbar, bytes);
+        ptx::mbar_arrive_expect_tx(vbar, bytes);
         if (bytes) {
-            bulk_g2s((uint32_t)__cvta_generic_to_shared(Kb), pk + off, bytes, bar);
-            bulk_g2s((uint32_t)__cvta_generic_to_shared(Vb), pv + off, bytes, bar);
+            bulk_g2s((uint32_t)__cvta_generic_to_shared(Kb), pk + off, bytes, kbar);
+            bulk_g2s((uint32_t)__cvta_generic_to_shared(Vb), pv + off, bytes, vbar);
         }
     }
+    // bounded wait for one tensor's rows; on expiry the CTA leaves after a second
+    // bounded wait for both copies still in flight into its shared memory
+    auto landed = [&](uint32_t b) {
+        bool ok = ptx::mbar_try_wait(b, 0);
+        if (!ok) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (!(ok = ptx::mbar_try_wait(b, 0)) && ptx::globaltimer() - t0 < kRpWaitNs) {
+            }
+            if (!ok) raise_status(status, BSA_ERR_TIMEOUT);
+        }
+        if (__syncthreads_and(ok)) return true;
+        if (tid == 0) {
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(kbar, 0) && ptx::globaltimer() - t0 < kRpWaitNs) {
+            }
+            while (!ptx::mbar_try_wait(vbar, 0) && ptx::globaltimer() - t0 < 2 * kRpWaitNs) {
+            }
+        }
+        return false;
+    };
     // while the rows land: the anchor, and whether this thread's row takes part
     // (an index outside [0, N) is skipped)
     if (tid < kRpD / 4)
@@ -605,24 +631,8 @@ __global__ void __launch_bounds__(kRpThreads, 3) reweight_packed_kernel(
         live = tok >= 0 && tok < N;
         if (!live && lh == 0) raise_status(status, BSA_ERR_INDEX);
     }
-    __syncthreads();  // the barrier's initialisation and the anchor are visible
-    bool ok = ptx::mbar_try_wait(bar, 0);
-    if (!ok) {
-        const uint64_t t0 = ptx::globaltimer();
-        while (!(ok = ptx::mbar_try_wait(bar, 0)) && ptx::globaltimer() - t0 < kRpWaitNs) {
-        }
-        if (!ok && tid == 0) raise_status(status, BSA_ERR_TIMEOUT);
-    }
-    // every thread waited on its own; the copy either landed for all or the CTA leaves,
-    // after a second bounded wait for the copy still in flight into its shared memory
-    if (!__syncthreads_and(ok)) {
-        if (tid == 0) {
-            const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try_wait(bar, 0) && ptx::globaltimer() - t0 < kRpWaitNs) {
-            }
-        }
-        return;
-    }
+    __syncthreads();  // the barriers' initialisation and the anchor are visible
+    if (!landed(kbar)) return;
     // ---- logits: channels [64 lh, 64 lh + 64) of row lr, four independent partial sums
     float2 t2[4];
 #pragma unroll
@@ -655,6 +665,7 @@ __global__ void __launch_bounds__(kRpThreads, 3) reweight_packed_kernel(
     const float e = (lh == 0 && mx != -CUDART_INF_F) ? expf(lg - mx) : 0.f;  // 0 for dead rows
     if (lh == 0) ps[lr] = e;
     const float z = block_sum(e, red);  // (its barriers also publish ps)
+    if (!landed(vbar)) return;
     // ---- weighted sums: channels [8 cc, 8 cc + 8) of tensor st over rows rg, rg + 8, ...
     const int st = warp >> 2, rg = (warp & 3) * 2 + (lane >> 4), cc = lane & 15;
     float2 acc[4];
@@ -694,7 +705,7 @@ __global__ void __launch_bounds__(kRpThreads, 3) reweight_packed_kernel(
 }
 
 static size_t reweight_packed_smem(int M) {
-    return (size_t)2 * M * kRpRow + (kRpD + 128 + 2 * 4 * kRpD + 8) * sizeof(float) + sizeof(uint64_t);
+    return (size_t)2 * M * kRpRow + (kRpD + 128 + 2 * 4 * kRpD + 8) * sizeof(float) + 2 * sizeof(uint64_t);
 }
 
 struct RwWorkspace {
