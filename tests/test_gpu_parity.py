@@ -811,6 +811,64 @@ def test_route_workspace_padded_heads(lib, J, D, pad):
         check_route(idx[bh].cpu().numpy(), num[bh].cpu().numpy(), E, k)
 
 
+def _integer_means(BH, J, D, seed):
+    # entries in {-2, ..., 2}: every dot product is a small integer, exact in float32, in each tf32
+    # part of the split (the low part is zero) and in float64, and a row holds many equal scores
+    rng = np.random.default_rng(seed)
+    return (rng.integers(-2, 3, size=(BH, J, D)).astype(np.float32),
+            rng.integers(-2, 3, size=(BH, J, D)).astype(np.float32))
+
+
+@pytest.mark.parametrize("J,D,k", [(960, 16, 96), (960, 16, 1), (300, 8, 37), (200, 16, 199), (1500, 16, 150),
+                                   (50, 4, 50), (130, 16, 13), (700, 4, 300)])
+def test_route_exact_ties_keep_lower_index(lib, J, D, k):
+    """Exact ties: integer pooled means make E exact on every path, with many equal scores in each
+    row, so the lists must equal the oracle's bit for bit with no near-tie exemption: the k-th key
+    found exactly, every key above it kept, and equal keys taken from the lowest block index up.
+    Covers keys in registers (8 to 32 a lane, the bucket gathered or never small enough to gather),
+    the streaming select (J > 1024), the tensor-core contraction with the select (workspace) and the
+    fused FMA path (none)."""
+    BH, scale = 2, 0.25
+    qb, kb = _integer_means(BH, J, D, J * 31 + k)
+    qd, kd = torch.as_tensor(qb, device=DEV), torch.as_tensor(kb, device=DEV)
+    kmax = k + 3
+    for use_ws in (True, False):
+        idx = torch.empty((BH, J, kmax), dtype=torch.int32, device=DEV)
+        num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
+        ws = (torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV) if use_ws
+              else None)
+        lib.bsa_route_topk(qd, kd, BH, J, D, J * D, k, scale, kmax, idx, num, ws)
+        torch.cuda.synchronize()
+        for bh in range(BH):
+            E = (qb[bh].astype(np.float64) @ kb[bh].astype(np.float64).T) * scale
+            want_idx, want_num = oracle.route(E, k, kmax)
+            assert np.array_equal(num[bh].cpu().numpy(), want_num)
+            gi = idx[bh].cpu().numpy()
+            bad = [i for i in range(J) if not np.array_equal(gi[i], want_idx[i])]
+            assert not bad, "workspace=%s rows %s" % (use_ws, bad[:5])
+
+
+def test_route_grouped_exact_ties_keep_lower_index(lib):
+    # the region-grouped select on integer means: regions of 1, 40, 300 and 900 blocks (keys per
+    # lane from 1 to 32 across the regions), exact ties inside every region
+    J, D, BH, scale = 1241, 16, 2, 0.25
+    starts, budgets = [0, 1, 41, 341, 1241], [1, 7, 30, 90]
+    qb, kb = _integer_means(BH, J, D, 77)
+    spans = list(zip(starts[:-1], starts[1:]))
+    kept = sum(min(k, hi - lo) for k, (lo, hi) in zip(budgets, spans))
+    qd, kd = torch.as_tensor(qb, device=DEV), torch.as_tensor(kb, device=DEV)
+    idx = torch.empty((BH, J, kept), dtype=torch.int32, device=DEV)
+    num = torch.empty((BH, J), dtype=torch.int32, device=DEV)
+    ws = torch.empty((lib.bsa_route_workspace(BH, J) // 4,), dtype=torch.float32, device=DEV)
+    lib.bsa_route_topk_grouped(qd, kd, BH, J, D, J * D, starts, budgets, scale, kept, idx, num, ws)
+    torch.cuda.synchronize()
+    for bh in range(BH):
+        E = (qb[bh].astype(np.float64) @ kb[bh].astype(np.float64).T) * scale
+        want_idx, want_num = oracle.route_grouped(E, spans, budgets, kept)
+        assert np.array_equal(num[bh].cpu().numpy(), want_num)
+        assert np.array_equal(idx[bh].cpu().numpy(), want_idx)
+
+
 # ---------------------------------------------------------------- device-side error reporting
 
 @pytest.mark.parametrize("J,starts,budgets", [(1500, [0, 300, 1500], [7, 40]), (700, [0, 1, 350, 700], [3, 9, 20])])
