@@ -10,9 +10,10 @@
 // operands (route_tc.cu) where the layout allows, else from the float32 FMA
 // contraction below; the fused path (no workspace) keeps E rows in shared
 // memory and uses FMAs.  The TopK is an exact radix select on order-preserving 32-bit
-// keys: one warp per row finds the k-th largest key bit by bit (counting
-// passes over the row until the k-th key's bucket holds at most 64 keys, then
-// over those alone), then writes the selected ids in ascending order with ballots.
+// keys: one warp per row finds the k-th largest key by bisection over key
+// values (counting passes over the row, from a bucket two binades below the row
+// maximum, until the k-th key's bucket holds at most 64 keys, then over those
+// alone), then writes the selected ids in ascending order with ballots.
 #include <algorithm>
 
 #include <cuda.h>
@@ -43,49 +44,70 @@ constexpr int kSelCap = 64;
 // TopK of J <= 32*KPL scores by one warp, the keys in registers (lane holds
 // columns lane + 32*i, i < KPL): exact radix select on order-preserving keys,
 // ties to the lower index, the selected ids (plus `first`) written ascending.
-// The bits of the k-th largest key are decided from the top.  After bit b the
-// key lies in the bucket [prefix, prefix + 2^b), n_lo keys are >= prefix (at
-// least k) and n_hi keys are >= prefix + 2^b (fewer than k).  Once the bucket
-// holds at most kSelCap keys (about ten bits into a row of scores), a warp with
-// many keys a lane gathers them into `cbuf` (kSelCap words of shared memory of
-// its own) and decides the remaining bits on those alone; the bucket count
-// n_hi then also gives the keys above the k-th without another pass.
+// The k-th largest key is found by bisection over key values: the bucket
+// [lo, hi) holds it, n_lo keys are >= lo (at least k) and n_hi keys are >= hi
+// (fewer than k); a counting pass at the bucket's middle halves it.  The first
+// bucket is [max - 2^24, max] when a pass shows at least k keys there (two
+// binades below the row maximum: on rows of scores this skips the passes that
+// would decide the sign and most of the exponent), else [0, max - 2^24).  Once
+// the bucket holds at most kSelCap keys, a warp with many keys a lane gathers
+// them into `cbuf` (kSelCap words of shared memory of its own) and bisects on
+// those alone; the bucket counts also give the keys above the k-th without
+// another pass.
 template <int KPL>
 __device__ __forceinline__ void select_keys(const float* __restrict__ e, int J, int k, int lane,
                                             int32_t* __restrict__ out, int first, uint32_t* __restrict__ cbuf) {
     constexpr bool kGather = KPL >= 8;
     uint32_t key[KPL];
+    uint32_t mx = 0;
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
         const int c = lane + 32 * i;
         key[i] = c < J ? order_key(e[c]) : 0u;  // 0 sorts below every float
+        mx = max(mx, key[i]);
     }
+    mx = __reduce_max_sync(0xffffffffu, mx);
     const unsigned lt = (1u << lane) - 1u;
-    uint32_t prefix = 0;
-    int n_lo = J, n_hi = 0;
-    int bit = 31;
-    for (; bit >= 0; --bit) {
-        const uint32_t cand = prefix | (1u << bit);
+    // keys >= cand, over the row
+    auto count_ge = [&](uint32_t cand) {
         // independent counters: short add chains, and 64 registers a thread at KPL = 32
         int cn[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < KPL; ++i) cn[i & 3] += key[i] >= cand;
-        const int cnt = __reduce_add_sync(0xffffffffu, (cn[0] + cn[1]) + (cn[2] + cn[3]));
+        return __reduce_add_sync(0xffffffffu, (cn[0] + cn[1]) + (cn[2] + cn[3]));
+    };
+    uint64_t lo = 0, hi = (uint64_t)mx + 1;  // nothing is >= max + 1
+    int n_lo = J, n_hi = 0;
+    if (mx > (1u << 24)) {
+        const uint32_t L = mx - (1u << 24);
+        const int cnt = count_ge(L);
         if (cnt >= k) {
-            prefix = cand;
+            lo = L;
             n_lo = cnt;
         } else {
+            hi = L;
             n_hi = cnt;
         }
-        if (kGather && bit > 0 && n_lo - n_hi <= kSelCap) break;
     }
-    if (kGather && bit > 0) {
+    while (hi - lo > 1) {
+        if (kGather && n_lo - n_hi <= kSelCap) break;
+        const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
+        const int cnt = count_ge(mid);
+        if (cnt >= k) {
+            lo = mid;
+            n_lo = cnt;
+        } else {
+            hi = mid;
+            n_hi = cnt;
+        }
+    }
+    if (kGather && hi - lo > 1) {
         // the bucket's keys, in column order, and the count of keys above it
-        const uint32_t width = 1u << bit;
+        const uint32_t lo32 = (uint32_t)lo, span = (uint32_t)(hi - lo - 1);
         int base = 0;
 #pragma unroll
         for (int i = 0; i < KPL; ++i) {
-            const bool inb = lane + 32 * i < J && key[i] - prefix < width;
+            const bool inb = lane + 32 * i < J && key[i] - lo32 <= span;
             const unsigned m = __ballot_sync(0xffffffffu, inb);
             if (inb) cbuf[base + __popc(m & lt)] = key[i];
             base += __popc(m);
@@ -94,18 +116,20 @@ __device__ __forceinline__ void select_keys(const float* __restrict__ e, int J, 
         const int n_top = n_hi;
         const uint32_t c0 = lane < base ? cbuf[lane] : 0u;
         const uint32_t c1 = lane + 32 < base ? cbuf[lane + 32] : 0u;
-        for (int b = bit - 1; b >= 0; --b) {
-            const uint32_t cand = prefix | (1u << b);
-            const int cnt = n_top + __reduce_add_sync(0xffffffffu, (int)(c0 >= cand) + (int)(c1 >= cand));
+        while (hi - lo > 1) {
+            const uint32_t mid = (uint32_t)(lo + ((hi - lo) >> 1));
+            const int cnt = n_top + __reduce_add_sync(0xffffffffu, (int)(c0 >= mid) + (int)(c1 >= mid));
             if (cnt >= k) {
-                prefix = cand;
+                lo = mid;
                 n_lo = cnt;
             } else {
+                hi = mid;
                 n_hi = cnt;
             }
         }
         __syncwarp();  // the buffer is reused by the warp's next row
     }
+    const uint32_t prefix = (uint32_t)lo;
     // prefix is the k-th largest key: n_hi keys lie above it and n_lo - n_hi equal it
     const int need_eq = k - n_hi;
     int written = 0;
@@ -428,7 +452,7 @@ struct Regions {
     int k[kMaxRegions];
 };
 
-__global__ void __launch_bounds__(256) route_select_grouped_kernel(const float* __restrict__ E, int J, Regions rg,
+__global__ void __launch_bounds__(256, 3) route_select_grouped_kernel(const float* __restrict__ E, int J, Regions rg,
                                                                    int kmax, int32_t* __restrict__ q2k_idx,
                                                                    int32_t* __restrict__ q2k_num) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5), bh = blockIdx.y, lane = threadIdx.x & 31;
