@@ -171,8 +171,9 @@ bsa_status bsa_pool_blocks(const void* q, const void* k, const void* v, bsa_dtyp
  * float32 FMAs over d in ascending order.  Without a workspace, one fused
  * kernel (float32 FMAs)
  * keeps the E rows of 8 to 32 query rows in shared memory, so even at 8 rows
- * (8*J + 128*(Dp+4) + 8*Dp) * 4 bytes must fit in 227 KB (Dp = D rounded up
- * to 4; J <= 5024 at D = 128), else BSA_ERR_UNSUPPORTED. */
+ * (8*J + 128*(Dp+4) + 8*Dp + 512) * 4 bytes (the 512 words: the select's
+ * candidate buffers) must fit in 227 KB (Dp = D rounded up to 4; J <= 4960
+ * at D = 128), else BSA_ERR_UNSUPPORTED. */
 size_t bsa_route_workspace(int BH, int J);
 bsa_status bsa_route_topk(const float* qbar, const float* kbar, int BH, int J, int D,
                           int64_t head_stride, int k, float scale, int kmax,

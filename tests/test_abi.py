@@ -87,6 +87,10 @@ def test_invalid_arguments_are_rejected_without_cuda(bsa):
     rc = lib.bsa_route_topk(1, 1, 2, 4, 2, 8, 2, 1.0, 4, 1, 1, 16, 64, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG and "workspace" in bsa.bsa_last_error()  # 2*4*4*4 = 128 bytes needed
     assert bsa.bsa_route_workspace(24, 960) == 24 * 960 * 960 * 4
+    # the fused route (no workspace) keeps 8 rows of E, the key tile and the select's candidate
+    # buffers in shared memory: at D = 128 J = 4961 is one row element past 227 KB (host check)
+    rc = lib.bsa_route_topk(1, 1, 1, 4961, 128, 4961 * 128, 8, 0.5, 8, 1, 1, None, 0, None)
+    assert rc == bsa.BSA_ERR_UNSUPPORTED and "shared memory" in bsa.bsa_last_error()
     rc = lib.bsa_build_reverse_index(1, 1, 1, 16, 1, 2, 4, 8, 0, 1, 1, 1, 1, 1, 1, 1, 1 << 20, None)
     assert rc == bsa.BSA_ERR_INVALID_ARG  # max_chunks too small
     rc = lib.bsa_build_reverse_index(1, 1, 1, 4096, 1, 2, 4, 8, 300, 1, 1, 1, 1, 1, 10 ** 6, 1, 1 << 20, None)
