@@ -545,15 +545,16 @@ __global__ void __launch_bounds__(kRwStagedThreads) reweight_block_staged_kernel
 // contiguous run of n_j rows, so one bulk copy per tensor brings a whole
 // block into shared memory: no per-row copy instructions.  One CTA of 8 warps
 // per (routed block, head), three CTAs per SM, so one CTA's copy lands while
-// the others compute:
+// the others compute; K and V complete on barriers of their own, so the
+// logits and the softmax run while V still arrives:
 //   logits  two threads per row, 64 channels each, reading the row's 16-byte
 //           chunks in an order rotated by the row (the rows are 256 bytes
 //           apart, so a plain order would put a warp's reads in one bank);
 //   softmax over the block's rows at once (n_j <= 128);
 //   sums    thread (tensor, chunk, row group) accumulates its 8 channels over
 //           every eighth row, the groups added in a fixed order.
-// bf16, D = 128, M <= 128.  The wait for the copy is bounded; on expiry the
-// CTA raises BSA_ERR_TIMEOUT, waits (bounded) for the copy and returns.
+// bf16, D = 128, M <= 128.  The waits for the copies are bounded; on expiry
+// the CTA raises BSA_ERR_TIMEOUT, waits (bounded) for both copies and returns.
 constexpr int kRpThreads = 256;
 constexpr int kRpD = 128;
 constexpr int kRpRow = kRpD * 2;  // bytes of a bf16 row
